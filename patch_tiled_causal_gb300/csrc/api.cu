@@ -1,0 +1,1135 @@
+// C ABI of libvaedec: argument checks, host plans, the decoder handle and its layer schedule.
+//
+// The decoder runs the layer sequence of the causal video-VAE decoders described in DistVAE PR #14
+// "Add tiled VAE parallelism & extended model support" (Wan, LTX-2 adapter commits) and TensorRT-LLM
+// PR #16066 "ParallelVAE_TrtllmWan for native Wan VAE", split into spatial patches: the band rule of
+// the Patchify commit fixes the patch edges at the latent grid, every layer keeps those bands scaled
+// by its up-sampling factor, and every kernel of a layer covers all patches at once (a halo read
+// needs the neighbour's previous layer, so layers are synchronous).  Chunked temporal decode keeps
+// per-conv 2-frame caches in the handle; tiled decode follows TensorRT-LLM PR #15753 "LTX-2
+// tile-parallel VAE decode".  Everything is stream-ordered; nothing here synchronises the host
+// except create/destroy/reserve (allocation) and vae_last_error.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+
+namespace vae {
+
+__device__ uint32_t g_fault[4];
+
+uint32_t* fault_word() {
+  static uint32_t* ptrs[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fault) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<uint32_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+uint64_t wait_limit_ns() { return 2000000000ull; }
+
+}  // namespace vae
+
+using namespace vae;
+
+// ================================================================================ errors
+struct vae_decoder;
+namespace {
+
+vae_error_info_t g_last{};  // op-level calls
+std::mutex g_last_mu;
+
+vae_status_t set_err(vae_error_info_t* e, vae_status_t code, int rows, int factor, const char* fmt, ...) {
+  vae_error_info_t tmp{};
+  tmp.code = code;
+  tmp.rows = rows;
+  tmp.factor = factor;
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(tmp.message, sizeof(tmp.message), fmt, ap);
+  va_end(ap);
+  if (e) {
+    *e = tmp;
+  } else {
+    std::lock_guard<std::mutex> lk(g_last_mu);
+    g_last = tmp;
+  }
+  return code;
+}
+
+#define CK(call)                                                                               \
+  do {                                                                                         \
+    cudaError_t _e = (call);                                                                   \
+    if (_e != cudaSuccess)                                                                     \
+      return set_err(ERRP, _e == cudaErrorMemoryAllocation ? VAE_ERR_OOM : VAE_ERR_CUDA, 0, 0, \
+                     "%s failed: %s", #call, cudaGetErrorString(_e));                          \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+vae_status_t band_edges(int length, int n, int scale, int reach, int* edges, vae_error_info_t* e) {
+  if (length <= 0 || n <= 0 || scale <= 0 || n > VAE_MAX_PATCHES)
+    return set_err(e, VAE_ERR_INVALID_ARG, 0, 0, "bad band request: length %d, n %d, scale %d", length, n, scale);
+  const int q = length / n, r = length % n;
+  edges[0] = 0;
+  for (int i = 0; i < n; ++i) {
+    const int sz = (i < r ? q + 1 : q) * scale;
+    if (sz < reach)
+      return set_err(e, VAE_ERR_PATCH_TOO_NARROW, sz, reach,
+                     "patch %d has %d rows, narrower than the kernel reach %d", i, sz, reach);
+    edges[i + 1] = edges[i] + sz;
+  }
+  return VAE_OK;
+}
+
+}  // namespace
+
+// ================================================================================ decoder
+namespace {
+
+// bf16 mode keeps the residual stream and the first conv's output (the two group-norm inputs
+// that are not conv operands) in fp32; conv operands are bf16.
+constexpr bool kResidF32 = true;
+constexpr bool kC1F32 = true;
+
+struct ConvL {
+  int C_in = 0, C_out = 0, C_in_pad = 0, N_pad = 0, st = 1, sh = 1, sw = 1;
+  bool tc = false;
+  void* w = nullptr;       // packed weights
+  float* bias = nullptr;   // fp32 [C_out]
+  void* cache = nullptr;   // [B, 2, H, W, C_in_pad] (chunked decode)
+  size_t cache_bytes = 0;
+};
+struct NormL {
+  float* gamma = nullptr;
+  float* beta = nullptr;
+  int C = 0;
+};
+struct ResL {
+  NormL n1, n2;
+  ConvL c1, c2;
+};
+struct AttnL {
+  NormL n;
+  void* w[4] = {nullptr, nullptr, nullptr, nullptr};  // q, k, v, o: bf16 (or fp32) [C, C]
+  float* b[4] = {nullptr, nullptr, nullptr, nullptr};
+};
+
+struct Level {  // one spatial/temporal scale of the decode
+  int T, H, W, C;
+  int ph[VAE_MAX_PATCHES + 1], pw[VAE_MAX_PATCHES + 1];
+};
+
+}  // namespace
+
+struct vae_decoder {
+  vae_config_t cfg{};
+  bool f32 = false;  // fp32 storage mode
+  ConvL conv_in;
+  std::vector<ResL> mid;
+  bool has_attn = false;
+  AttnL attn;
+  std::vector<std::vector<ResL>> stages;
+  std::vector<ConvL> ups;
+  NormL head_norm;
+  ConvL head;
+  std::vector<void*> owned;  // every cudaMalloc of the handle
+  // workspace
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  int64_t ws_shape[5] = {0, 0, 0, 0, 0};
+  int ws_nph = 0, ws_npw = 0;
+  bool caches_ready = false;
+  int64_t cache_shape[5] = {0, 0, 0, 0, 0};
+  int cache_nph = 0, cache_npw = 0;
+  // tiled decode tile storage
+  void* tiles = nullptr;
+  size_t tiles_bytes = 0;
+  vae_error_info_t err{};
+};
+
+namespace {
+
+#define ERRP (&d->err)
+
+template <typename T>
+vae_status_t dalloc(vae_decoder* d, T** p, size_t bytes) {
+  void* q = nullptr;
+  cudaError_t e = cudaMalloc(&q, std::max<size_t>(bytes, 256));
+  if (e != cudaSuccess) return set_err(&d->err, VAE_ERR_OOM, 0, 0, "cudaMalloc(%zu) failed: %s", bytes, cudaGetErrorString(e));
+  d->owned.push_back(q);
+  *p = static_cast<T*>(q);
+  return VAE_OK;
+}
+
+int act_bytes(const vae_decoder* d) { return d->f32 ? 4 : 2; }
+int res_bytes(const vae_decoder* d) { return (d->f32 || kResidF32) ? 4 : 2; }
+int c1_bytes(const vae_decoder* d) { return (d->f32 || kC1F32) ? 4 : 2; }
+
+vae_status_t make_conv(vae_decoder* d, ConvL& c, const float* w, const float* b, int C_in, int C_out, int st, int sh,
+                       int sw, bool pad_input = false) {
+  c.C_in = C_in;
+  c.C_out = C_out;
+  c.st = st; c.sh = sh; c.sw = sw;
+  const int S = st * sh * sw;
+  if (C_out % S) return set_err(&d->err, VAE_ERR_INVALID_ARG, 0, 0, "conv out channels %d not divisible by %d", C_out, S);
+  // tensor cores take 64-channel K blocks; the latent is zero-padded up to them when it is converted
+  c.tc = !d->f32 && (C_in % 64 == 0 || pad_input);
+  c.C_in_pad = c.tc ? round_up(C_in, 64) : C_in;
+  if (c.tc) {
+    c.N_pad = C_out <= 256 ? round_up(C_out, 16) : round_up(C_out, 16);
+    const size_t bytes = static_cast<size_t>(c.N_pad) * 27 * c.C_in_pad * 2;
+    vae_status_t s = dalloc(d, &c.w, bytes);
+    if (s) return s;
+    CK(launch_pack_weights_bf16(w, C_out, C_in, c.C_in_pad, c.N_pad, S, c.w, nullptr));
+  } else {
+    const size_t bytes = 27ull * C_in * C_out * 4;
+    vae_status_t s = dalloc(d, &c.w, bytes);
+    if (s) return s;
+    CK(launch_pack_weights_f32(w, C_out, C_in, c.w, nullptr));
+  }
+  vae_status_t s = dalloc(d, &c.bias, C_out * 4ull);
+  if (s) return s;
+  CK(cudaMemcpy(c.bias, b, C_out * 4ull, cudaMemcpyDeviceToDevice));
+  return VAE_OK;
+}
+
+vae_status_t make_norm(vae_decoder* d, NormL& n, const float* g, const float* b, int C) {
+  n.C = C;
+  vae_status_t s = dalloc(d, &n.gamma, C * 4ull);
+  if (s) return s;
+  s = dalloc(d, &n.beta, C * 4ull);
+  if (s) return s;
+  CK(cudaMemcpy(n.gamma, g, C * 4ull, cudaMemcpyDeviceToDevice));
+  CK(cudaMemcpy(n.beta, b, C * 4ull, cudaMemcpyDeviceToDevice));
+  return VAE_OK;
+}
+
+int count_weights(const vae_config_t& c) {
+  int n = 2;
+  n += 8 * c.mid_res;
+  if (c.mid_attn) n += 2 + 8;
+  for (int i = 0; i < c.n_stages; ++i) {
+    n += 8 * c.n_res[i];
+    if (i + 1 < c.n_stages) n += 2;
+  }
+  n += 4;
+  return n;
+}
+
+vae_status_t check_config(const vae_config_t* c, vae_error_info_t* e) {
+  if (!c) return set_err(e, VAE_ERR_INVALID_ARG, 0, 0, "null config");
+  if (c->n_stages < 1 || c->n_stages > VAE_MAX_STAGES || c->latent_c <= 0 || c->gn_groups <= 0 || c->out_c <= 0 ||
+      c->mid_res < 0 || c->out_d2s_t < 1 || c->out_d2s_h < 1 || c->out_d2s_w < 1 ||
+      (c->dtype != VAE_BF16 && c->dtype != VAE_FP32))
+    return set_err(e, VAE_ERR_INVALID_ARG, 0, 0, "invalid decoder config");
+  if (c->out_d2s_t != 1) return set_err(e, VAE_ERR_UNSUPPORTED, 0, 0, "temporal depth-to-space in conv_out is not supported");
+  for (int i = 0; i < c->n_stages; ++i) {
+    const int C = c->stage_c[i];
+    if (C <= 0 || C % c->gn_groups || c->n_res[i] < 0) return set_err(e, VAE_ERR_INVALID_ARG, 0, 0, "stage %d channels", i);
+    const int cpg = C / c->gn_groups;
+    if (C % 8 || C > 8192 || !(cpg % 8 == 0 || 8 % cpg == 0))
+      return set_err(e, VAE_ERR_UNSUPPORTED, 0, 0, "stage %d: %d channels / %d groups not supported", i, C, c->gn_groups);
+    if (i + 1 < c->n_stages && (c->up_t[i] < 1 || c->up_t[i] > 2 || c->up_h[i] < 1 || c->up_w[i] < 1 || c->up_h[i] != c->up_w[i]))
+      return set_err(e, VAE_ERR_UNSUPPORTED, 0, 0, "up-sampler %d factors", i);
+  }
+  if (c->out_d2s_h != c->out_d2s_w) return set_err(e, VAE_ERR_UNSUPPORTED, 0, 0, "non-square final depth-to-space");
+  return VAE_OK;
+}
+
+#undef ERRP
+
+}  // namespace
+
+extern "C" vae_status_t vae_decoder_n_weights(const vae_config_t* cfg, int* n_weights) {
+  vae_status_t s = check_config(cfg, nullptr);
+  if (s) return s;
+  if (!n_weights) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null n_weights");
+  *n_weights = count_weights(*cfg);
+  return VAE_OK;
+}
+
+extern "C" void vae_decoder_destroy(vae_decoder_t* d) {
+  if (!d) return;
+  cudaDeviceSynchronize();
+  for (void* p : d->owned) cudaFree(p);
+  if (d->ws) cudaFree(d->ws);
+  if (d->tiles) cudaFree(d->tiles);
+  delete d;
+}
+
+extern "C" vae_status_t vae_decoder_create(const vae_config_t* cfg, const void* const* weights, int n_weights,
+                                           vae_decoder_t** out) {
+  if (!out) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null out");
+  *out = nullptr;
+  vae_status_t s = check_config(cfg, nullptr);
+  if (s) return s;
+  if (!weights || n_weights != count_weights(*cfg))
+    return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "expected %d weight tensors, got %d", count_weights(*cfg), n_weights);
+  for (int i = 0; i < n_weights; ++i)
+    if (!weights[i] || !aligned16(weights[i]))
+      return set_err(nullptr, weights[i] ? VAE_ERR_ALIGNMENT : VAE_ERR_INVALID_ARG, 0, 0, "weight %d pointer", i);
+  vae_decoder* d = new vae_decoder();
+  d->cfg = *cfg;
+  d->f32 = cfg->dtype == VAE_FP32;
+  int k = 0;
+  auto W = [&](void) { return static_cast<const float*>(weights[k++]); };
+  auto res_block = [&](ResL& r, int C) -> vae_status_t {
+    const float *g1 = W(), *b1 = W(), *w1 = W(), *bb1 = W(), *g2 = W(), *b2 = W(), *w2 = W(), *bb2 = W();
+    vae_status_t st = make_norm(d, r.n1, g1, b1, C);
+    if (!st) st = make_conv(d, r.c1, w1, bb1, C, C, 1, 1, 1);
+    if (!st) st = make_norm(d, r.n2, g2, b2, C);
+    if (!st) st = make_conv(d, r.c2, w2, bb2, C, C, 1, 1, 1);
+    return st;
+  };
+  const int C0 = cfg->stage_c[0];
+  {
+    const float* w = W();
+    const float* b = W();
+    s = make_conv(d, d->conv_in, w, b, cfg->latent_c, C0, 1, 1, 1, true);
+  }
+  d->mid.resize(cfg->mid_res);
+  for (int r = 0; r < cfg->mid_res && !s; ++r) s = res_block(d->mid[r], C0);
+  d->has_attn = cfg->mid_attn != 0;
+  if (d->has_attn && !s) {
+    const float* g = W();
+    const float* b = W();
+    s = make_norm(d, d->attn.n, g, b, C0);
+    for (int q = 0; q < 4 && !s; ++q) {
+      const float* w = W();
+      const float* bb = W();
+      s = dalloc(d, &d->attn.w[q], static_cast<size_t>(C0) * C0 * (d->f32 ? 4 : 2));
+      if (!s) s = dalloc(d, &d->attn.b[q], C0 * 4ull);
+      if (!s) {
+        cudaError_t e = d->f32 ? cudaMemcpy(d->attn.w[q], w, static_cast<size_t>(C0) * C0 * 4, cudaMemcpyDeviceToDevice)
+                               : launch_pack_matrix_bf16(w, C0, C0, d->attn.w[q], nullptr);
+        if (e == cudaSuccess) e = cudaMemcpy(d->attn.b[q], bb, C0 * 4ull, cudaMemcpyDeviceToDevice);
+        if (e != cudaSuccess) s = set_err(&d->err, VAE_ERR_CUDA, 0, 0, "attention weights: %s", cudaGetErrorString(e));
+      }
+    }
+    if (!s && (C0 % 64 || C0 % 16)) s = set_err(&d->err, VAE_ERR_UNSUPPORTED, 0, 0, "attention channels %d", C0);
+  }
+  d->stages.resize(cfg->n_stages);
+  d->ups.resize(std::max(0, cfg->n_stages - 1));
+  for (int i = 0; i < cfg->n_stages && !s; ++i) {
+    d->stages[i].resize(cfg->n_res[i]);
+    for (int r = 0; r < cfg->n_res[i] && !s; ++r) s = res_block(d->stages[i][r], cfg->stage_c[i]);
+    if (i + 1 < cfg->n_stages && !s) {
+      const float* w = W();
+      const float* b = W();
+      const int S = cfg->up_t[i] * cfg->up_h[i] * cfg->up_w[i];
+      s = make_conv(d, d->ups[i], w, b, cfg->stage_c[i], S * cfg->stage_c[i + 1], cfg->up_t[i], cfg->up_h[i], cfg->up_w[i]);
+    }
+  }
+  if (!s) {
+    const int CL = cfg->stage_c[cfg->n_stages - 1];
+    const float* g = W();
+    const float* b = W();
+    s = make_norm(d, d->head_norm, g, b, CL);
+    const float* w = W();
+    const float* bb = W();
+    const int S = cfg->out_d2s_t * cfg->out_d2s_h * cfg->out_d2s_w;
+    if (!s) s = make_conv(d, d->head, w, bb, CL, cfg->out_c * S, cfg->out_d2s_t, cfg->out_d2s_h, cfg->out_d2s_w);
+  }
+  if (!s) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) s = set_err(&d->err, VAE_ERR_CUDA, 0, 0, "weight packing: %s", cudaGetErrorString(e));
+  }
+  if (s) {
+    {
+      std::lock_guard<std::mutex> lk(g_last_mu);
+      g_last = d->err;
+    }
+    vae_decoder_destroy(d);
+    return s;
+  }
+  *out = d;
+  return VAE_OK;
+}
+
+// ------------------------------------------------------------------------------ workspace plan
+namespace {
+
+struct Plan {
+  std::vector<Level> lv;  // level i = stage i; lv[n_stages] = pixel level of conv_out's output
+  int Tlat, h, w, B, nph, npw;
+  bool first;
+  // buffer sizes in bytes
+  size_t x_bytes, hin_bytes, c1_bytes, gn_bytes, lat_bytes;
+  size_t attn_tok, attn_tokp;  // tokens per frame and padded
+  size_t q_bytes, s_bytes, p_bytes, vt_bytes;
+};
+
+vae_status_t make_plan(vae_decoder* d, int B, int Tlat, int h, int w, int nph, int npw, bool first, Plan& p) {
+  const vae_config_t& c = d->cfg;
+  p.B = B; p.Tlat = Tlat; p.h = h; p.w = w; p.nph = nph; p.npw = npw; p.first = first;
+  p.lv.clear();
+  int T = Tlat, sh = 1, sw = 1;
+  for (int i = 0; i < c.n_stages; ++i) {
+    Level L{};
+    L.T = T; L.H = h * sh; L.W = w * sw; L.C = c.stage_c[i];
+    vae_status_t s = band_edges(h, nph, sh, 1, L.ph, &d->err);
+    if (s) return s;
+    s = band_edges(w, npw, sw, 1, L.pw, &d->err);
+    if (s) return s;
+    p.lv.push_back(L);
+    if (i + 1 < c.n_stages) {
+      T = c.up_t[i] * T - (first ? c.up_t[i] - 1 : 0);
+      sh *= c.up_h[i];
+      sw *= c.up_w[i];
+    }
+  }
+  {
+    Level L{};
+    L.T = T; L.H = h * sh * c.out_d2s_h; L.W = w * sw * c.out_d2s_w; L.C = c.out_c;
+    vae_status_t s = band_edges(h, nph, sh * c.out_d2s_h, 1, L.ph, &d->err);
+    if (!s) s = band_edges(w, npw, sw * c.out_d2s_w, 1, L.pw, &d->err);
+    if (s) return s;
+    p.lv.push_back(L);
+  }
+  const int ab = act_bytes(d), rb = res_bytes(d), cb = c1_bytes(d);
+  p.x_bytes = p.hin_bytes = p.c1_bytes = p.gn_bytes = 0;
+  for (int i = 0; i < c.n_stages; ++i) {
+    const Level& L = p.lv[i];
+    const size_t px = static_cast<size_t>(B) * L.H * L.W;
+    p.x_bytes = std::max(p.x_bytes, px * L.T * L.C * rb);
+    p.hin_bytes = std::max(p.hin_bytes, px * (L.T + 2) * L.C * ab);
+    p.c1_bytes = std::max(p.c1_bytes, px * L.T * L.C * cb);
+    p.gn_bytes = std::max(p.gn_bytes, gn_partials_bytes(nph, npw, B, L.T, c.gn_groups));
+  }
+  const int Clat = d->conv_in.C_in_pad;
+  p.lat_bytes = static_cast<size_t>(B) * (Tlat + 2) * h * w * Clat * ab;
+  p.hin_bytes = std::max(p.hin_bytes, p.lat_bytes);
+  p.attn_tok = static_cast<size_t>(h) * w;
+  p.attn_tokp = round_up(static_cast<int>(p.attn_tok), 64);
+  if (d->has_attn) {
+    const size_t F = static_cast<size_t>(B) * Tlat, C0 = c.stage_c[0];
+    p.q_bytes = F * p.attn_tok * C0 * ab;
+    p.vt_bytes = F * C0 * p.attn_tokp * ab;
+    p.s_bytes = F * p.attn_tok * p.attn_tok * 4;
+    p.p_bytes = F * p.attn_tok * p.attn_tokp * ab;
+  } else {
+    p.q_bytes = p.vt_bytes = p.s_bytes = p.p_bytes = 0;
+  }
+  return VAE_OK;
+}
+
+size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Bufs {
+  char *x, *hin, *c1, *gn, *q, *k, *v, *vt, *s, *p, *o;
+};
+
+size_t ws_total(const Plan& p) {
+  return align_up(p.x_bytes) + align_up(p.hin_bytes) + align_up(p.c1_bytes) + align_up(p.gn_bytes) +
+         4 * align_up(p.q_bytes) + align_up(p.vt_bytes) + align_up(p.s_bytes) + align_up(p.p_bytes) + 256;
+}
+
+Bufs carve(void* base, const Plan& p) {
+  Bufs b{};
+  char* c = static_cast<char*>(base);
+  b.x = c; c += align_up(p.x_bytes);
+  b.hin = c; c += align_up(p.hin_bytes);
+  b.c1 = c; c += align_up(p.c1_bytes);
+  b.gn = c; c += align_up(p.gn_bytes);
+  b.q = c; c += align_up(p.q_bytes);
+  b.k = c; c += align_up(p.q_bytes);
+  b.v = c; c += align_up(p.q_bytes);
+  b.o = c; c += align_up(p.q_bytes);
+  b.vt = c; c += align_up(p.vt_bytes);
+  b.s = c; c += align_up(p.s_bytes);
+  b.p = c;
+  return b;
+}
+
+#define ERRP (&d->err)
+
+vae_status_t ensure_ws(vae_decoder* d, const Plan& p) {
+  const size_t need = ws_total(p);
+  if (need <= d->ws_bytes) return VAE_OK;
+  if (d->ws) {
+    CK(cudaDeviceSynchronize());
+    cudaFree(d->ws);
+    d->ws = nullptr;
+    d->ws_bytes = 0;
+  }
+  CK(cudaMalloc(&d->ws, need));
+  d->ws_bytes = need;
+  return VAE_OK;
+}
+
+// all convs of the decoder in schedule order (for cache allocation)
+template <typename F>
+void for_each_conv(vae_decoder* d, F f) {
+  f(d->conv_in, 0);
+  for (auto& r : d->mid) { f(r.c1, 0); f(r.c2, 0); }
+  for (size_t i = 0; i < d->stages.size(); ++i) {
+    for (auto& r : d->stages[i]) { f(r.c1, static_cast<int>(i)); f(r.c2, static_cast<int>(i)); }
+    if (i + 1 < d->stages.size()) f(d->ups[i], static_cast<int>(i));
+  }
+  f(d->head, static_cast<int>(d->stages.size()) - 1);
+}
+
+vae_status_t ensure_caches(vae_decoder* d, const Plan& p) {
+  bool ok = d->caches_ready;
+  vae_status_t st = VAE_OK;
+  for_each_conv(d, [&](ConvL& c, int lvl) {
+    const Level& L = p.lv[lvl];
+    const size_t need = static_cast<size_t>(p.B) * 2 * L.H * L.W * c.C_in_pad * act_bytes(d);
+    if (c.cache_bytes < need) ok = false;
+  });
+  if (ok) return VAE_OK;
+  CK(cudaDeviceSynchronize());
+  for_each_conv(d, [&](ConvL& c, int lvl) {
+    if (st) return;
+    const Level& L = p.lv[lvl];
+    const size_t need = static_cast<size_t>(p.B) * 2 * L.H * L.W * c.C_in_pad * act_bytes(d);
+    if (c.cache_bytes >= need) return;
+    void* q = nullptr;
+    if (cudaMalloc(&q, need) != cudaSuccess) {
+      st = set_err(&d->err, VAE_ERR_OOM, 0, 0, "cache allocation of %zu bytes failed", need);
+      return;
+    }
+    d->owned.push_back(q);
+    c.cache = q;
+    c.cache_bytes = need;
+  });
+  if (!st) d->caches_ready = true;
+  return st;
+}
+
+// ------------------------------------------------------------------------------ layer runners
+struct Ctx {
+  vae_decoder* d;
+  const Plan* p;
+  Bufs b;
+  cudaStream_t s;
+  bool chunked;  // keep per-conv caches
+};
+
+// Run conv `c` at level L. x = the conv-input buffer hin (bf16 / fp32 act, B x (2+T) frames, frame 0..1 cache).
+vae_status_t run_conv(Ctx& x, ConvL& c, const Level& L, void* y, int y_f32, int y_T_alloc, int out_ncthw,
+                      const void* residual, int res_f32, int drop_first) {
+  vae_decoder* d = x.d;
+  const int B = x.p->B, T = L.T, Ta = T + 2;
+  const int64_t frame_bytes = static_cast<int64_t>(L.H) * L.W * c.C_in_pad * act_bytes(d);
+  const bool use_cache = x.chunked && !x.p->first;
+  if (use_cache) CK(launch_copy_frames(c.cache, 2, 0, x.b.hin, Ta, 0, 2, B, frame_bytes, x.s));
+  const char* xin = x.b.hin + (use_cache ? 0 : 2 * frame_bytes);
+  const int cache_frames = use_cache ? 2 : 0;
+  if (c.tc) {
+    ConvTcArgs a{};
+    a.mode = 0;
+    a.B = B; a.T = T; a.H = L.H; a.W = L.W;
+    a.C_in_pad = c.C_in_pad; a.T_in = T + cache_frames; a.x_T_alloc = Ta; a.cache_frames = cache_frames;
+    a.nph = x.p->nph; a.npw = x.p->npw; a.ph_edges = L.ph; a.pw_edges = L.pw;
+    a.x = xin; a.w = c.w; a.N_real = c.C_out; a.N_pad = c.N_pad; a.bias = c.bias;
+    a.residual = residual; a.res_f32 = res_f32; a.res_T_alloc = T;
+    a.y = y; a.out_f32 = y_f32; a.out_ncthw = out_ncthw; a.y_T_alloc = y_T_alloc;
+    a.d2s_t = c.st; a.d2s_h = c.sh; a.d2s_w = c.sw; a.drop_first = drop_first;
+    CK(launch_conv_tc(a, x.s));
+  } else {
+    ConvSimtArgs a{};
+    a.B = B; a.T = T; a.H = L.H; a.W = L.W; a.C_in = c.C_in; a.C_out = c.C_out;
+    a.T_in = T + cache_frames; a.x_T_alloc = Ta; a.cache_frames = cache_frames;
+    a.x = xin; a.x_f32 = d->f32; a.w = static_cast<const float*>(c.w); a.bias = c.bias;
+    a.residual = residual; a.res_f32 = res_f32; a.res_T_alloc = T;
+    a.y = y; a.out_f32 = y_f32; a.out_ncthw = out_ncthw; a.y_T_alloc = y_T_alloc;
+    a.d2s_t = c.st; a.d2s_h = c.sh; a.d2s_w = c.sw; a.drop_first = drop_first;
+    a.nph = x.p->nph; a.npw = x.p->npw; a.ph_edges = L.ph; a.pw_edges = L.pw;
+    CK(launch_conv_simt(a, x.s));
+  }
+  if (x.chunked) {
+    // keep the last 2 frames of this conv's (padded) input sequence for the next chunk
+    if (use_cache || T >= 2) {
+      const int last = 2 + T;  // frames [last-2, last) of hin are the newest two
+      CK(launch_copy_frames(x.b.hin, Ta, last - 2, c.cache, 2, 0, 2, B, frame_bytes, x.s));
+    } else {  // first chunk of one frame: the padded sequence ends x0, x0
+      CK(launch_copy_frames(x.b.hin, Ta, 2, c.cache, 2, 0, 1, B, frame_bytes, x.s));
+      CK(launch_copy_frames(x.b.hin, Ta, 2, c.cache, 2, 1, 1, B, frame_bytes, x.s));
+    }
+  }
+  return VAE_OK;
+}
+
+// GN (+SiLU) of src (B x T frames, dtype src_f32) into hin frames [2, 2+T)
+vae_status_t run_gn(Ctx& x, const NormL& n, const Level& L, const void* src, int src_f32, int silu) {
+  vae_decoder* d = x.d;
+  GnArgs g{};
+  g.B = x.p->B; g.T = L.T; g.H = L.H; g.W = L.W; g.C = L.C; g.groups = d->cfg.gn_groups;
+  g.eps = d->cfg.gn_eps; g.silu = silu;
+  g.nph = x.p->nph; g.npw = x.p->npw; g.ph_edges = L.ph; g.pw_edges = L.pw;
+  g.x = src; g.x_f32 = src_f32; g.x_T_alloc = L.T;
+  const int64_t frame_bytes = static_cast<int64_t>(L.H) * L.W * L.C * act_bytes(d);
+  g.y = x.b.hin + 2 * frame_bytes; g.y_f32 = d->f32; g.y_T_alloc = L.T + 2;
+  g.gamma = n.gamma; g.beta = n.beta;
+  g.partials = x.b.gn;
+  CK(launch_gn_stats(g, x.s));
+  CK(launch_gn_apply(g, x.s));
+  return VAE_OK;
+}
+
+vae_status_t run_resblock(Ctx& x, ResL& r, const Level& L) {
+  vae_decoder* d = x.d;
+  const int rf = res_bytes(d) == 4, cf = c1_bytes(d) == 4;
+  vae_status_t s = run_gn(x, r.n1, L, x.b.x, rf, 1);
+  if (!s) s = run_conv(x, r.c1, L, x.b.c1, cf, L.T, 0, nullptr, 0, 0);
+  if (!s) s = run_gn(x, r.n2, L, x.b.c1, cf, 1);
+  if (!s) s = run_conv(x, r.c2, L, x.b.x, rf, L.T, 0, x.b.x, rf, 0);  // in-place residual add
+  return s;
+}
+
+vae_status_t run_attention(Ctx& x, const Level& L) {
+  vae_decoder* d = x.d;
+  const int C = L.C, F = x.p->B * L.T;
+  const int tok = L.H * L.W, tokp = static_cast<int>(x.p->attn_tokp);
+  const int rf = res_bytes(d) == 4;
+  // GN without SiLU into hn (= buffer q's neighbour o, reused before O is produced)
+  {
+    GnArgs g{};
+    g.B = x.p->B; g.T = L.T; g.H = L.H; g.W = L.W; g.C = C; g.groups = d->cfg.gn_groups;
+    g.eps = d->cfg.gn_eps; g.silu = 0;
+    g.nph = x.p->nph; g.npw = x.p->npw; g.ph_edges = L.ph; g.pw_edges = L.pw;
+    g.x = x.b.x; g.x_f32 = rf; g.x_T_alloc = L.T;
+    g.y = x.b.o; g.y_f32 = d->f32; g.y_T_alloc = L.T;
+    g.gamma = d->attn.n.gamma; g.beta = d->attn.n.beta;
+    g.partials = x.b.gn;
+    CK(launch_gn_stats(g, x.s));
+    CK(launch_gn_apply(g, x.s));
+  }
+  const float scale = 1.0f / std::sqrt(static_cast<float>(C));
+  const int64_t M = static_cast<int64_t>(F) * tok;
+  if (d->f32) {
+    const float* hn = reinterpret_cast<const float*>(x.b.o);
+    float* qkv[3] = {reinterpret_cast<float*>(x.b.q), reinterpret_cast<float*>(x.b.k), reinterpret_cast<float*>(x.b.v)};
+    for (int i = 0; i < 3; ++i)
+      CK(launch_gemm_simt(hn, static_cast<const float*>(d->attn.w[i]), qkv[i], d->attn.b[i], nullptr, static_cast<int>(M), C,
+                          C, 1, 0, 0, 0, C, 1, 1.0f, x.s));
+    float* S = reinterpret_cast<float*>(x.b.s);
+    CK(launch_gemm_simt(qkv[0], qkv[1], S, nullptr, nullptr, tok, tok, C, F, static_cast<int64_t>(tok) * C,
+                        static_cast<int64_t>(tok) * C, static_cast<int64_t>(tok) * tok, C, 1, scale, x.s));
+    float* P = reinterpret_cast<float*>(x.b.p);
+    CK(launch_softmax_rows(S, P, 1, F * tok, tok, tok, x.s));
+    // O = P V: B element (n = c, k = token) = V[token * C + c]
+    float* O = reinterpret_cast<float*>(x.b.o);
+    CK(launch_gemm_simt(P, qkv[2], O, nullptr, nullptr, tok, C, tok, F, static_cast<int64_t>(tok) * tok,
+                        static_cast<int64_t>(tok) * C, static_cast<int64_t>(tok) * C, 1, C, 1.0f, x.s));
+    float* X = reinterpret_cast<float*>(x.b.x);
+    CK(launch_gemm_simt(O, static_cast<const float*>(d->attn.w[3]), X, d->attn.b[3], X, static_cast<int>(M), C, C, 1, 0,
+                        0, 0, C, 1, 1.0f, x.s));
+    return VAE_OK;
+  }
+  auto gemm = [&](const void* A, const void* Bm, void* D, const float* bias, int Mm, int N, int K, int batch,
+                  int64_t sa, int64_t sb, int64_t sd, int64_t ldd, float alpha, int out_f32, const void* res,
+                  int r_f32) -> vae_status_t {
+    ConvTcArgs a{};
+    a.mode = 1;
+    a.M = Mm; a.K = K; a.batch = batch; a.stride_a = sa; a.stride_b = sb; a.stride_d = sd; a.alpha = alpha;
+    a.x = A; a.w = Bm; a.N_real = N; a.N_pad = round_up(N, 16); a.bias = bias;
+    a.residual = res; a.res_f32 = r_f32; a.y = D; a.out_f32 = out_f32; a.ldd = ldd;
+    a.d2s_t = a.d2s_h = a.d2s_w = 1;
+    CK(launch_conv_tc(a, x.s));
+    return VAE_OK;
+  };
+  vae_status_t s = VAE_OK;
+  char* qkv[3] = {x.b.q, x.b.k, x.b.v};
+  for (int i = 0; i < 3 && !s; ++i)
+    s = gemm(x.b.o, d->attn.w[i], qkv[i], d->attn.b[i], static_cast<int>(M), C, C, 1, 0, 0, 0, 0, 1.0f, 0, nullptr, 0);
+  if (s) return s;
+  CK(launch_transpose_bf16(x.b.v, x.b.vt, F, tok, C, x.s));  // V^T [F, C, tokp], zero padded
+  s = gemm(x.b.q, x.b.k, x.b.s, nullptr, tok, tok, C, F, static_cast<int64_t>(tok) * C, static_cast<int64_t>(tok) * C,
+           static_cast<int64_t>(tok) * tok, 0, scale, 1, nullptr, 0);
+  if (s) return s;
+  CK(launch_softmax_rows(reinterpret_cast<const float*>(x.b.s), x.b.p, 0, F * tok, tok, tokp, x.s));
+  s = gemm(x.b.p, x.b.vt, x.b.o, nullptr, tok, C, tokp, F, static_cast<int64_t>(tok) * tokp,
+           static_cast<int64_t>(C) * tokp, static_cast<int64_t>(tok) * C, 0, 1.0f, 0, nullptr, 0);
+  if (s) return s;
+  return gemm(x.b.o, d->attn.w[3], x.b.x, d->attn.b[3], static_cast<int>(M), C, C, 1, 0, 0, 0, 0, 1.0f, rf, x.b.x, rf);
+}
+
+// Decode one chunk (or the whole latent) into out (NCTHW, out_T_alloc frames per (b, c)).
+// lat_full = (T, H, W) of the latent tensor, lat_box = (t0, h0, w0) of the decoded box.
+vae_status_t run_decode(vae_decoder* d, const Plan& p, const float* latent, const int lat_full[3], const int lat_box[3],
+                        void* out, int out_T_alloc, bool chunked, cudaStream_t s) {
+  Ctx x{d, &p, carve(d->ws, p), s, chunked};
+  const vae_config_t& c = d->cfg;
+  const int rf = res_bytes(d) == 4;
+  vae_status_t st = VAE_OK;
+  // latent box NCTHW fp32 -> channels-last conv input (frames 2.. of hin), channels zero-padded
+  {
+    const Level& L0 = p.lv[0];
+    const int Cp = d->conv_in.C_in_pad;
+    const int64_t fb = static_cast<int64_t>(p.h) * p.w * Cp * act_bytes(d);
+    CK(launch_latent_to_cl(latent, p.B, c.latent_c, lat_full[0], lat_full[1], lat_full[2], lat_box[0], p.Tlat,
+                           lat_box[1], p.h, lat_box[2], p.w, Cp, x.b.hin + 2 * fb, d->f32, p.Tlat + 2, s));
+    st = run_conv(x, d->conv_in, L0, x.b.x, rf, L0.T, 0, nullptr, 0, 0);
+    if (st) return st;
+  }
+  for (auto& r : d->mid) {
+    st = run_resblock(x, r, p.lv[0]);
+    if (st) return st;
+  }
+  if (d->has_attn) {
+    st = run_attention(x, p.lv[0]);
+    if (st) return st;
+  }
+  for (int i = 0; i < c.n_stages; ++i) {
+    const Level& L = p.lv[i];
+    for (auto& r : d->stages[i]) {
+      st = run_resblock(x, r, L);
+      if (st) return st;
+    }
+    if (i + 1 < c.n_stages) {
+      // conv input = the residual stream in the conv dtype, behind 2 cache frames
+      const int64_t fe = static_cast<int64_t>(L.H) * L.W * L.C;
+      CK(launch_cast_frames(x.b.x, rf, L.T, x.b.hin + 2 * fe * act_bytes(d), d->f32, L.T + 2, p.B, L.T, fe, s));
+      st = run_conv(x, d->ups[i], L, x.b.x, rf, p.lv[i + 1].T, 0, nullptr, 0, p.first ? 1 : 0);
+      if (st) return st;
+    }
+  }
+  const Level& LL = p.lv[c.n_stages - 1];
+  st = run_gn(x, d->head_norm, LL, x.b.x, rf, 1);
+  if (st) return st;
+  return run_conv(x, d->head, LL, out, d->f32, out_T_alloc, 1, nullptr, 0, p.first ? 1 : 0);
+}
+
+vae_status_t check_shape(vae_decoder* d, const int64_t* shp, int nph, int npw) {
+  if (!shp) return set_err(&d->err, VAE_ERR_INVALID_ARG, 0, 0, "null shape");
+  if (shp[0] <= 0 || shp[1] != d->cfg.latent_c || shp[2] <= 0 || shp[3] <= 0 || shp[4] <= 0)
+    return set_err(&d->err, VAE_ERR_INVALID_ARG, 0, 0, "latent shape mismatch");
+  if (shp[0] > 64 || shp[2] > 4096 || shp[3] > 8192 || shp[4] > 8192)
+    return set_err(&d->err, VAE_ERR_UNSUPPORTED, 0, 0, "latent too large");
+  if (nph < 1 || npw < 1 || nph > VAE_MAX_PATCHES || npw > VAE_MAX_PATCHES)
+    return set_err(&d->err, VAE_ERR_INVALID_ARG, 0, 0, "patch counts %d x %d", nph, npw);
+  return VAE_OK;
+}
+
+vae_status_t check_gn_range(vae_decoder* d, const Plan& p) {
+  // exact integer group sums need fewer than 2^23 elements per (frame, group)
+  for (int i = 0; i < d->cfg.n_stages; ++i) {
+    const Level& L = p.lv[i];
+    const double n = static_cast<double>(L.C / d->cfg.gn_groups) * L.H * L.W;
+    if (n >= 8388608.0)
+      return set_err(&d->err, VAE_ERR_UNSUPPORTED, 0, 0, "group of %.0f elements exceeds the exact-sum range", n);
+  }
+  return VAE_OK;
+}
+
+}  // namespace
+
+extern "C" vae_status_t vae_decoder_reserve(vae_decoder_t* d, const int64_t shp[5], int nph, int npw) {
+  if (!d) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null decoder");
+  vae_status_t s = check_shape(d, shp, nph, npw);
+  if (s) return s;
+  Plan p;
+  s = make_plan(d, static_cast<int>(shp[0]), static_cast<int>(shp[2]), static_cast<int>(shp[3]),
+                static_cast<int>(shp[4]), nph, npw, false, p);
+  if (s) return s;
+  return ensure_ws(d, p);
+}
+
+extern "C" vae_status_t vae_decode(vae_decoder_t* d, const void* latent, const int64_t shp[5], void* out, int nph,
+                                   int npw, void* stream) {
+  if (!d) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null decoder");
+  if (!latent || !out) return set_err(&d->err, VAE_ERR_INVALID_ARG, 0, 0, "null latent or out");
+  if (!aligned16(latent) || !aligned16(out)) return set_err(&d->err, VAE_ERR_ALIGNMENT, 0, 0, "latent/out not 16-byte aligned");
+  vae_status_t s = check_shape(d, shp, nph, npw);
+  if (s) return s;
+  Plan p;
+  s = make_plan(d, static_cast<int>(shp[0]), static_cast<int>(shp[2]), static_cast<int>(shp[3]),
+                static_cast<int>(shp[4]), nph, npw, true, p);
+  if (s) return s;
+  s = check_gn_range(d, p);
+  if (s) return s;
+  s = ensure_ws(d, p);
+  if (s) return s;
+  const int full[3] = {static_cast<int>(shp[2]), static_cast<int>(shp[3]), static_cast<int>(shp[4])};
+  const int box[3] = {0, 0, 0};
+  return run_decode(d, p, static_cast<const float*>(latent), full, box, out, p.lv.back().T, false,
+                    static_cast<cudaStream_t>(stream));
+}
+
+extern "C" vae_status_t vae_decode_chunk(vae_decoder_t* d, const void* latent, const int64_t shp[5], int first_chunk,
+                                         void* out, int nph, int npw, void* stream) {
+  if (!d) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null decoder");
+  if (!latent || !out) return set_err(&d->err, VAE_ERR_INVALID_ARG, 0, 0, "null latent or out");
+  if (!aligned16(latent) || !aligned16(out)) return set_err(&d->err, VAE_ERR_ALIGNMENT, 0, 0, "latent/out not 16-byte aligned");
+  vae_status_t s = check_shape(d, shp, nph, npw);
+  if (s) return s;
+  if (!first_chunk && !d->caches_ready)
+    return set_err(&d->err, VAE_ERR_INVALID_ARG, 0, 0, "a later chunk came before the first chunk");
+  if (!first_chunk && (shp[0] != d->cache_shape[0] || shp[3] != d->cache_shape[3] || shp[4] != d->cache_shape[4] ||
+                       nph != d->cache_nph || npw != d->cache_npw))
+    return set_err(&d->err, VAE_ERR_INVALID_ARG, 0, 0, "chunk shape or patch grid differs from the first chunk");
+  Plan p;
+  s = make_plan(d, static_cast<int>(shp[0]), static_cast<int>(shp[2]), static_cast<int>(shp[3]),
+                static_cast<int>(shp[4]), nph, npw, first_chunk != 0, p);
+  if (s) return s;
+  s = check_gn_range(d, p);
+  if (s) return s;
+  Plan pmax;  // caches and workspace sized for a non-first chunk of this size
+  s = make_plan(d, static_cast<int>(shp[0]), static_cast<int>(shp[2]), static_cast<int>(shp[3]),
+                static_cast<int>(shp[4]), nph, npw, false, pmax);
+  if (s) return s;
+  s = ensure_ws(d, pmax);
+  if (s) return s;
+  if (first_chunk) d->caches_ready = false;
+  s = ensure_caches(d, p);
+  if (s) return s;
+  for (int i = 0; i < 5; ++i) d->cache_shape[i] = shp[i];
+  d->cache_nph = nph;
+  d->cache_npw = npw;
+  const int full[3] = {static_cast<int>(shp[2]), static_cast<int>(shp[3]), static_cast<int>(shp[4])};
+  const int box[3] = {0, 0, 0};
+  return run_decode(d, p, static_cast<const float*>(latent), full, box, out, p.lv.back().T, true,
+                    static_cast<cudaStream_t>(stream));
+}
+
+#undef ERRP
+
+// ================================================================================ tile plan
+extern "C" vae_status_t vae_tile_plan(const int lat[3], const int tile[3], const int ovl[3], int scale_t, int scale_s,
+                                      int causal_t, vae_tile_t* tiles, int* n_tiles) {
+  if (!lat || !tile || !ovl || !n_tiles || scale_t < 1 || scale_s < 1)
+    return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "tile plan arguments");
+  int starts[3][4096], ext[3][4096], cnt[3];
+  int px0[3][4096], pxn[3][4096];
+  for (int a = 0; a < 3; ++a) {
+    if (lat[a] <= 0 || tile[a] <= 0 || ovl[a] < 0 || ovl[a] >= tile[a])
+      return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "axis %d: length %d tile %d overlap %d", a, lat[a], tile[a], ovl[a]);
+    const int stride = tile[a] - ovl[a];
+    int n = 0, s = 0;
+    while (true) {
+      if (n >= 4096) return set_err(nullptr, VAE_ERR_UNSUPPORTED, 0, 0, "too many tiles on axis %d", a);
+      starts[a][n] = s;
+      ext[a][n] = std::min(tile[a], lat[a] - s);
+      ++n;
+      if (s + tile[a] >= lat[a]) break;
+      s += stride;
+    }
+    cnt[a] = n;
+    const int sc = a == 0 ? scale_t : scale_s;
+    for (int i = 0; i < n; ++i) {
+      px0[a][i] = sc * starts[a][i];
+      pxn[a][i] = (a == 0 && causal_t) ? sc * (ext[a][i] - 1) + 1 : sc * ext[a][i];
+    }
+  }
+  const long total = static_cast<long>(cnt[0]) * cnt[1] * cnt[2];
+  if (!tiles) {
+    *n_tiles = static_cast<int>(std::min<long>(total, 0x7fffffff));
+    return VAE_OK;
+  }
+  if (total > *n_tiles) {
+    *n_tiles = static_cast<int>(std::min<long>(total, 0x7fffffff));
+    return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "tile array holds %d, plan needs %ld", *n_tiles, total);
+  }
+  int k = 0;
+  for (int it = 0; it < cnt[0]; ++it)
+    for (int ih = 0; ih < cnt[1]; ++ih)
+      for (int iw = 0; iw < cnt[2]; ++iw) {
+        vae_tile_t& t = tiles[k++];
+        const int idx[3] = {it, ih, iw};
+        for (int a = 0; a < 3; ++a) {
+          const int i = idx[a];
+          t.lat[2 * a] = starts[a][i];
+          t.lat[2 * a + 1] = ext[a][i];
+          t.pix[2 * a] = px0[a][i];
+          t.pix[2 * a + 1] = pxn[a][i];
+          t.ovl[2 * a] = i > 0 ? px0[a][i - 1] + pxn[a][i - 1] - px0[a][i] : 0;
+          t.ovl[2 * a + 1] = i + 1 < cnt[a] ? px0[a][i] + pxn[a][i] - px0[a][i + 1] : 0;
+        }
+      }
+  *n_tiles = k;
+  return VAE_OK;
+}
+
+extern "C" vae_status_t vae_patch_edges(int length, int n, int scale, int reach, int* edges) {
+  if (!edges) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null edges");
+  return band_edges(length, n, scale, reach, edges, nullptr);
+}
+
+#define ERRP (&d->err)
+extern "C" vae_status_t vae_decode_tiled(vae_decoder_t* d, const void* latent, const int64_t shp[5], void* out,
+                                         const int tile_thw[3], const int ovl_thw[3], void* stream) {
+  if (!d) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null decoder");
+  if (!latent || !out || !tile_thw || !ovl_thw) return set_err(&d->err, VAE_ERR_INVALID_ARG, 0, 0, "null argument");
+  if (!aligned16(latent) || !aligned16(out)) return set_err(&d->err, VAE_ERR_ALIGNMENT, 0, 0, "latent/out not 16-byte aligned");
+  vae_status_t s = check_shape(d, shp, 1, 1);
+  if (s) return s;
+  const vae_config_t& c = d->cfg;
+  int st = c.out_d2s_t, ss = c.out_d2s_h;
+  for (int i = 0; i + 1 < c.n_stages; ++i) {
+    st *= c.up_t[i];
+    ss *= c.up_h[i];
+  }
+  const int lat[3] = {static_cast<int>(shp[2]), static_cast<int>(shp[3]), static_cast<int>(shp[4])};
+  std::vector<vae_tile_t> tl(VAE_MAX_TILES);
+  int n = VAE_MAX_TILES;
+  s = vae_tile_plan(lat, tile_thw, ovl_thw, st, ss, 1, tl.data(), &n);
+  if (s) return set_err(&d->err, s, 0, 0, "tile plan failed (%d tiles max)", VAE_MAX_TILES);
+  const int B = static_cast<int>(shp[0]), Cl = c.latent_c;
+  const int ob = d->f32 ? 4 : 2;
+  // storage for every decoded tile (the blend gathers them)
+  size_t total = 0;
+  std::vector<size_t> off(n);
+  for (int i = 0; i < n; ++i) {
+    off[i] = total;
+    total += align_up(static_cast<size_t>(B) * c.out_c * tl[i].pix[1] * tl[i].pix[3] * tl[i].pix[5] * ob);
+  }
+  (void)Cl;
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  {
+    // workspace for the largest tile first, so the loop below allocates nothing
+    Plan pm;
+    s = make_plan(d, B, tl[0].lat[1], tl[0].lat[3], tl[0].lat[5], 1, 1, true, pm);
+    if (s) return s;
+    s = ensure_ws(d, pm);
+    if (s) return s;
+  }
+  if (d->tiles_bytes < total) {
+    CK(cudaDeviceSynchronize());
+    if (d->tiles) cudaFree(d->tiles);
+    d->tiles = nullptr;
+    d->tiles_bytes = 0;
+    CK(cudaMalloc(&d->tiles, total));
+    d->tiles_bytes = total;
+  }
+  char* base = static_cast<char*>(d->tiles);
+  std::vector<const void*> ptrs(n);
+  const int full[3] = {lat[0], lat[1], lat[2]};
+  for (int i = 0; i < n; ++i) {
+    const vae_tile_t& t = tl[i];
+    Plan p;
+    s = make_plan(d, B, t.lat[1], t.lat[3], t.lat[5], 1, 1, true, p);
+    if (s) return s;
+    s = check_gn_range(d, p);
+    if (s) return s;
+    s = ensure_ws(d, p);
+    if (s) return s;
+    const int box[3] = {t.lat[0], t.lat[2], t.lat[4]};
+    s = run_decode(d, p, static_cast<const float*>(latent), full, box, base + off[i], p.lv.back().T, false, strm);
+    if (s) return s;
+    ptrs[i] = base + off[i];
+  }
+  vae_blend_desc_t bd{};
+  bd.B = B; bd.C = c.out_c;
+  bd.T = st * (lat[0] - 1) + 1; bd.H = ss * lat[1]; bd.W = ss * lat[2];
+  bd.tile_dtype = bd.out_dtype = d->f32 ? VAE_FP32 : VAE_BF16;
+  CK(launch_blend(ptrs.data(), tl.data(), n, out, bd, strm));
+  return VAE_OK;
+}
+#undef ERRP
+
+// ================================================================================ op level
+#define ERRP nullptr
+namespace {
+vae_status_t check_edges(int n, const int* e, int extent, const char* what) {
+  if (n < 1 || n > VAE_MAX_PATCHES) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "%s: %d patches", what, n);
+  if (e[0] != 0 || e[n] != extent) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "%s edges must span 0..%d", what, extent);
+  for (int i = 0; i < n; ++i)
+    if (e[i + 1] - e[i] < 1)
+      return set_err(nullptr, VAE_ERR_PATCH_TOO_NARROW, e[i + 1] - e[i], 1, "%s patch %d has %d rows", what, i, e[i + 1] - e[i]);
+  return VAE_OK;
+}
+bool conv_tc_ok(const vae_conv_desc_t* d) { return d->in_dtype == VAE_BF16 && d->C_in % 64 == 0; }
+int conv_npad(const vae_conv_desc_t* d) { return (d->C_out + 15) / 16 * 16; }
+}  // namespace
+
+extern "C" size_t vae_conv3d_packed_bytes(const vae_conv_desc_t* d) {
+  if (!d || d->C_in <= 0 || d->C_out <= 0) return 0;
+  if (conv_tc_ok(d)) return static_cast<size_t>(conv_npad(d)) * 27 * d->C_in * 2;
+  return 27ull * d->C_in * d->C_out * 4;
+}
+
+extern "C" vae_status_t vae_conv3d_pack_weights(const float* w, const vae_conv_desc_t* d, void* w_packed, void* stream) {
+  if (!w || !d || !w_packed) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null argument");
+  const int S = d->d2s_t * d->d2s_h * d->d2s_w;
+  if (S < 1 || d->C_out % S) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "C_out %% depth-to-space");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (conv_tc_ok(d)) CK(launch_pack_weights_bf16(w, d->C_out, d->C_in, d->C_in, conv_npad(d), S, w_packed, s));
+  else CK(launch_pack_weights_f32(w, d->C_out, d->C_in, w_packed, s));
+  return VAE_OK;
+}
+
+extern "C" vae_status_t vae_conv3d_causal(const void* x, const void* w_packed, const float* bias, const void* residual,
+                                          void* y, const vae_conv_desc_t* d, void* stream) {
+  if (!x || !w_packed || !y || !d) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null argument");
+  if (!aligned16(x) || !aligned16(y) || !aligned16(w_packed) || (residual && !aligned16(residual)))
+    return set_err(nullptr, VAE_ERR_ALIGNMENT, 0, 0, "pointers must be 16-byte aligned");
+  if (d->B <= 0 || d->T <= 0 || d->H <= 0 || d->W <= 0 || d->C_in <= 0 || d->C_out <= 0 ||
+      (d->cache_frames != 0 && d->cache_frames != 2) || d->d2s_t < 1 || d->d2s_h < 1 || d->d2s_w < 1)
+    return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "bad conv descriptor");
+  const int S = d->d2s_t * d->d2s_h * d->d2s_w;
+  if (d->C_out % S) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "C_out not divisible by the depth-to-space factor");
+  if (residual && S != 1) return set_err(nullptr, VAE_ERR_UNSUPPORTED, 0, 0, "residual with depth-to-space");
+  if (d->in_dtype == VAE_FP32 && d->out_dtype == VAE_BF16 && false) return VAE_ERR_UNSUPPORTED;
+  vae_status_t st = check_edges(d->n_patch_h, d->patch_h_edges, d->H, "height");
+  if (!st) st = check_edges(d->n_patch_w, d->patch_w_edges, d->W, "width");
+  if (st) return st;
+  if ((x == y) || (residual && residual == y && S != 1)) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "y aliases x");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (conv_tc_ok(d)) {
+    ConvTcArgs a{};
+    a.mode = 0;
+    a.B = d->B; a.T = d->T; a.H = d->H; a.W = d->W; a.C_in_pad = d->C_in;
+    a.T_in = d->T + d->cache_frames; a.x_T_alloc = a.T_in; a.cache_frames = d->cache_frames;
+    a.nph = d->n_patch_h; a.npw = d->n_patch_w; a.ph_edges = d->patch_h_edges; a.pw_edges = d->patch_w_edges;
+    a.x = x; a.w = w_packed; a.N_real = d->C_out; a.N_pad = conv_npad(d); a.bias = bias;
+    a.residual = residual; a.res_f32 = d->res_dtype == VAE_FP32;
+    a.y = y; a.out_f32 = d->out_dtype == VAE_FP32; a.out_ncthw = d->out_ncthw;
+    a.d2s_t = d->d2s_t; a.d2s_h = d->d2s_h; a.d2s_w = d->d2s_w; a.drop_first = d->drop_first;
+    CK(launch_conv_tc(a, s));
+  } else {
+    ConvSimtArgs a{};
+    a.B = d->B; a.T = d->T; a.H = d->H; a.W = d->W; a.C_in = d->C_in; a.C_out = d->C_out;
+    a.T_in = d->T + d->cache_frames; a.x_T_alloc = a.T_in; a.cache_frames = d->cache_frames;
+    a.x = x; a.x_f32 = d->in_dtype == VAE_FP32; a.w = static_cast<const float*>(w_packed); a.bias = bias;
+    a.residual = residual; a.res_f32 = d->res_dtype == VAE_FP32;
+    a.y = y; a.out_f32 = d->out_dtype == VAE_FP32; a.out_ncthw = d->out_ncthw;
+    a.d2s_t = d->d2s_t; a.d2s_h = d->d2s_h; a.d2s_w = d->d2s_w; a.drop_first = d->drop_first;
+    a.nph = d->n_patch_h; a.npw = d->n_patch_w; a.ph_edges = d->patch_h_edges; a.pw_edges = d->patch_w_edges;
+    CK(launch_conv_simt(a, s));
+  }
+  return VAE_OK;
+}
+
+extern "C" size_t vae_patch_groupnorm_workspace_bytes(const vae_gn_desc_t* d) {
+  if (!d || d->B <= 0 || d->T <= 0 || d->groups <= 0 || d->n_patch_h <= 0 || d->n_patch_w <= 0) return 0;
+  return gn_partials_bytes(d->n_patch_h, d->n_patch_w, d->B, d->T, d->groups);
+}
+
+namespace {
+vae_status_t check_gn_desc(const vae_gn_desc_t* d) {
+  if (d->B <= 0 || d->T <= 0 || d->H <= 0 || d->W <= 0 || d->C <= 0 || d->groups <= 0 || d->C % d->groups)
+    return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "bad group-norm descriptor");
+  const int cpg = d->C / d->groups;
+  if (d->C % 8 || d->C > 8192 || d->groups > 1024 || !(cpg % 8 == 0 || 8 % cpg == 0))
+    return set_err(nullptr, VAE_ERR_UNSUPPORTED, 0, 0, "%d channels in %d groups not supported", d->C, d->groups);
+  if (static_cast<double>(cpg) * d->H * d->W >= 8388608.0)
+    return set_err(nullptr, VAE_ERR_UNSUPPORTED, 0, 0, "group larger than the exact-sum range (2^23 elements)");
+  vae_status_t st = check_edges(d->n_patch_h, d->patch_h_edges, d->H, "height");
+  if (!st) st = check_edges(d->n_patch_w, d->patch_w_edges, d->W, "width");
+  return st;
+}
+}  // namespace
+
+extern "C" vae_status_t vae_patch_groupnorm_silu(const void* x, const float* gamma, const float* beta, void* y,
+                                                 void* workspace, const vae_gn_desc_t* d, void* stream) {
+  if (!x || !gamma || !beta || !y || !workspace || !d) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null argument");
+  if (!aligned16(x) || !aligned16(y) || !aligned16(workspace))
+    return set_err(nullptr, VAE_ERR_ALIGNMENT, 0, 0, "pointers must be 16-byte aligned");
+  vae_status_t st = check_gn_desc(d);
+  if (st) return st;
+  GnArgs g{};
+  g.B = d->B; g.T = d->T; g.H = d->H; g.W = d->W; g.C = d->C; g.groups = d->groups; g.eps = d->eps; g.silu = d->silu;
+  g.nph = d->n_patch_h; g.npw = d->n_patch_w; g.ph_edges = d->patch_h_edges; g.pw_edges = d->patch_w_edges;
+  g.x = x; g.x_f32 = d->in_dtype == VAE_FP32; g.y = y; g.y_f32 = d->out_dtype == VAE_FP32;
+  g.gamma = gamma; g.beta = beta; g.partials = workspace;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CK(launch_gn_stats(g, s));
+  CK(launch_gn_apply(g, s));
+  return VAE_OK;
+}
+
+extern "C" vae_status_t vae_upsample_d2s(const void* x, void* y, const vae_d2s_desc_t* d, void* stream) {
+  if (!x || !y || !d) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null argument");
+  if (d->B <= 0 || d->T <= 0 || d->H <= 0 || d->W <= 0 || d->C <= 0 || d->s_t < 1 || d->s_h < 1 || d->s_w < 1)
+    return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "bad depth-to-space descriptor");
+  if (x == y) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "y aliases x");
+  CK(launch_d2s(x, y, d->B, d->T, d->H, d->W, d->C, d->s_t, d->s_h, d->s_w, d->drop_first, d->dtype == VAE_FP32,
+                static_cast<cudaStream_t>(stream)));
+  return VAE_OK;
+}
+
+extern "C" vae_status_t vae_tile_blend(const void* const* tiles, const vae_tile_t* meta, int n_tiles, void* out,
+                                       const vae_blend_desc_t* d, void* stream) {
+  if (!tiles || !meta || !out || !d || n_tiles <= 0) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null argument");
+  if (n_tiles > VAE_MAX_TILES) return set_err(nullptr, VAE_ERR_UNSUPPORTED, 0, 0, "more than %d tiles", VAE_MAX_TILES);
+  if (d->B <= 0 || d->C <= 0 || d->T <= 0 || d->H <= 0 || d->W <= 0)
+    return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "bad blend descriptor");
+  for (int i = 0; i < n_tiles; ++i) {
+    const int* p = meta[i].pix;
+    if (!tiles[i] || p[1] <= 0 || p[3] <= 0 || p[5] <= 0 || p[0] < 0 || p[2] < 0 || p[4] < 0 || p[0] + p[1] > d->T ||
+        p[2] + p[3] > d->H || p[4] + p[5] > d->W)
+      return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "tile %d box outside the output", i);
+    for (int k = 0; k < 6; ++k)
+      if (meta[i].ovl[k] < 0 || meta[i].ovl[k] > 65535) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "tile %d overlap", i);
+  }
+  CK(launch_blend(tiles, meta, n_tiles, out, *d, static_cast<cudaStream_t>(stream)));
+  return VAE_OK;
+}
+
+extern "C" vae_status_t vae_gemm_bf16(const void* A, const void* Bm, void* D, const float* bias, int M, int N, int K,
+                                      int batch, int64_t sa, int64_t sb, int64_t sd, float alpha, vae_dtype_t out_dtype,
+                                      void* stream) {
+  if (!A || !Bm || !D) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null argument");
+  if (M <= 0 || N <= 0 || K <= 0 || batch <= 0 || K % 64 || N % 16 || (batch > 1 && (sa % 8 || sb % 8)))
+    return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "gemm sizes (K %% 64, N %% 16)");
+  if (!aligned16(A) || !aligned16(Bm) || !aligned16(D)) return set_err(nullptr, VAE_ERR_ALIGNMENT, 0, 0, "alignment");
+  ConvTcArgs a{};
+  a.mode = 1;
+  a.M = M; a.K = K; a.batch = batch; a.stride_a = batch > 1 ? sa : static_cast<int64_t>(M) * K;
+  a.stride_b = batch > 1 ? sb : static_cast<int64_t>(N) * K; a.stride_d = sd; a.alpha = alpha;
+  a.x = A; a.w = Bm; a.N_real = N; a.N_pad = N; a.bias = bias;
+  a.y = D; a.out_f32 = out_dtype == VAE_FP32;
+  a.d2s_t = a.d2s_h = a.d2s_w = 1;
+  CK(launch_conv_tc(a, static_cast<cudaStream_t>(stream)));
+  return VAE_OK;
+}
+
+extern "C" vae_status_t vae_watchdog_selftest(int timeout_us, void* stream) {
+  if (timeout_us <= 0 || timeout_us > 10000000) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "timeout_us");
+  CK(launch_watchdog_test(static_cast<uint64_t>(timeout_us) * 1000ull, static_cast<cudaStream_t>(stream)));
+  CK(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  vae_error_info_t info{};
+  return vae_last_error(nullptr, &info);
+}
+#undef ERRP
+
+extern "C" vae_status_t vae_last_error(vae_decoder_t* d, vae_error_info_t* info) {
+  vae_error_info_t out{};
+  if (d) out = d->err;
+  else {
+    std::lock_guard<std::mutex> lk(g_last_mu);
+    out = g_last;
+  }
+  int dev_count = 0;
+  if (cudaGetDeviceCount(&dev_count) == cudaSuccess && dev_count > 0) {
+    cudaError_t e = cudaDeviceSynchronize();
+    uint32_t* fw = fault_word();
+    uint32_t host[4] = {0, 0, 0, 0};
+    if (e == cudaSuccess && fw) e = cudaMemcpy(host, fw, sizeof(host), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) {
+      out.code = VAE_ERR_CUDA;
+      snprintf(out.message, sizeof(out.message), "CUDA error: %s", cudaGetErrorString(e));
+    } else if (host[0] != 0) {
+      out.code = static_cast<int>(host[0]);
+      out.rows = 0;
+      out.factor = 0;
+      snprintf(out.message, sizeof(out.message), "device fault %u at site %u (block %u)", host[0], host[1], host[2]);
+      const uint32_t zero[4] = {0, 0, 0, 0};
+      cudaMemcpy(fw, zero, sizeof(zero), cudaMemcpyHostToDevice);
+    }
+  }
+  if (info) *info = out;
+  if (d) d->err = vae_error_info_t{};
+  else {
+    std::lock_guard<std::mutex> lk(g_last_mu);
+    g_last = vae_error_info_t{};
+  }
+  return static_cast<vae_status_t>(out.code);
+}

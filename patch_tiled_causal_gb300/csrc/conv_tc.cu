@@ -1,0 +1,544 @@
+// Causal Conv3d as an implicit GEMM on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// Computes, for every output voxel of every patch,
+//   y[b,t,h,w,co] = bias[co] + sum_{kt,kh,kw,ci} W[co,ci,kt,kh,kw] * x[b, max(t-2+kt,0), h-1+kh, w-1+kw, ci]
+// (+ residual, then depth-to-space), the causal convolution of the video-VAE decoders in DistVAE
+// PR #14 "Add tiled VAE parallelism & extended model support" (PatchConv3d padding commit: zero
+// padding at image edges, halo rows from the neighbour patch at interior edges; the temporal pad is
+// one-sided, frames repeated).
+//
+// GEMM view: M = output pixels of one frame tile (128 = rows_t x cols_t pixels of one patch),
+// N = output channels (tile BN <= 256), K = 27 taps x C_in, walked tap-major in 64-channel blocks.
+// Per K block one TMA box load brings the tap-shifted 128 x 64 input tile (5-D tensor map over the
+// channels-last activation; out-of-image rows and columns arrive as zeros, the causal time index is
+// clamped at frame 0 or points into the 2 cached frames) and one brings the BN x 64 weight tile.
+// Halo taps of a tile at an interior patch edge land in the neighbouring patch's rows of the same
+// activation, so halo rows are read in place.  The M tile never crosses a patch edge, so every block
+// writes to exactly one patch.  There is no split-K and the K order is fixed, so each output's sum
+// runs in the same order whatever the patch grid: outputs are bit-identical across patch counts.
+//
+// Warp roles (192 threads): warp 0 issues TMA loads into a STAGES-deep shared-memory ring, warp 1
+// owns the tensor memory and issues tcgen05.mma (128 x BN x 16, bf16 -> fp32 accumulators in TMEM),
+// warps 2-5 drain TMEM with tcgen05.ld and run the epilogue (bias, residual, depth-to-space scatter,
+// bf16/fp32 store, optional fused group-norm partial sums).  Every mbarrier wait is bounded.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace vae {
+
+struct TcParams {
+  int mode;  // 0 conv, 1 gemm
+  int B, T, H, W, T_in, cache_frames, C_in_pad;
+  int res_T_alloc, y_T_alloc;
+  int64_t ldd;
+  int rows_t, cols_t, n_trows, n_tcols;
+  int nph, npw;
+  int trow_prefix[kMaxP + 1], tcol_prefix[kMaxP + 1];
+  int ph_edges[kMaxP + 1], pw_edges[kMaxP + 1];
+  int M, K, batch, m_tiles_per_batch;
+  int64_t stride_d;
+  float alpha;
+  int num_kb, cchunks;
+  int N_real, BN, n_ntiles, tmem_cols, stages;
+  const float* bias;
+  const void* residual;
+  int res_f32;
+  void* y;
+  int out_f32, out_ncthw;
+  int d2s_t, d2s_h, d2s_w, drop, C_d2s, S;
+  int T_out, H_out, W_out;
+  void* gn_partials;
+  int gn_groups, gn_cpg;
+  uint32_t* fault;
+  uint64_t limit_ns;
+};
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBlockM = 128;
+constexpr int kBlockK = 64;
+constexpr uint32_t kABytes = kBlockM * kBlockK * 2;  // 16 KB
+
+VAE_DEV int find_band(const int* prefix, int n, int idx) {
+  int i = 0;
+  while (i + 1 < n && prefix[i + 1] <= idx) ++i;
+  return i;
+}
+
+// Group-norm partial sums of one (patch, b, t, group): exact integer sums of q = round(x * 2^18)
+// and q^2 (128-bit), see norm.cu.  Layout must match GnPartial there.
+struct GnPart {
+  unsigned long long s1;      // two's complement int64 sum of q
+  unsigned long long s2_lo;   // 128-bit sum of q^2
+  unsigned long long s2_hi;
+  unsigned long long pad;
+};
+
+VAE_DEV void gn_accumulate(GnPart* dst, long long s1, unsigned long long lo, unsigned long long hi) {
+  atomicAdd(&dst->s1, static_cast<unsigned long long>(s1));
+  unsigned long long old = atomicAdd(&dst->s2_lo, lo);
+  unsigned long long carry = (old + lo < old) ? 1ull : 0ull;
+  if (hi + carry) atomicAdd(&dst->s2_hi, hi + carry);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    conv_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ TcParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t b_bytes = static_cast<uint32_t>(p.BN) * kBlockK * 2;
+  const uint32_t stage_bytes = kABytes + b_bytes;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + p.stages * stage_bytes);
+  uint64_t* empty_bar = full_bar + p.stages;
+  uint64_t* accum_bar = empty_bar + p.stages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum_bar + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- tile coordinates
+  const int ntile = blockIdx.x % p.n_ntiles;
+  const int mt = blockIdx.x / p.n_ntiles;
+  int b = 0, t = 0, h0 = 0, w0 = 0, h_end = 0, w_end = 0, patch = 0, m0 = 0, bat = 0;
+  if (p.mode == 0) {
+    const int per_frame = p.n_trows * p.n_tcols;
+    const int frame = mt / per_frame;
+    const int r = mt % per_frame;
+    const int tr = r / p.n_tcols, tc = r % p.n_tcols;
+    const int pi = find_band(p.trow_prefix, p.nph, tr);
+    const int pj = find_band(p.tcol_prefix, p.npw, tc);
+    b = frame / p.T;
+    t = frame % p.T;
+    h0 = p.ph_edges[pi] + (tr - p.trow_prefix[pi]) * p.rows_t;
+    w0 = p.pw_edges[pj] + (tc - p.tcol_prefix[pj]) * p.cols_t;
+    h_end = p.ph_edges[pi + 1];
+    w_end = p.pw_edges[pj + 1];
+    patch = pi * p.npw + pj;
+  } else {
+    bat = mt / p.m_tiles_per_batch;
+    m0 = (mt % p.m_tiles_per_batch) * kBlockM;
+  }
+  const int n0 = ntile * p.BN;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(accum_bar, 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, static_cast<uint32_t>(p.tmem_cols));
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued_kb = 0;
+      bool ok = true;
+      for (int kb = 0; kb < p.num_kb && ok; ++kb) {
+        const int s = kb % p.stages;
+        const int use = kb / p.stages;
+        if (use > 0) ok = mbar_wait(&empty_bar[s], (use - 1) & 1, p.fault, p.limit_ns, 1);
+        if (!ok) break;
+        uint8_t* a_dst = smem + s * stage_bytes;
+        uint8_t* b_dst = a_dst + kABytes;
+        mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
+        if (p.mode == 0) {
+          const int tap = kb / p.cchunks;
+          const int cc = kb - tap * p.cchunks;
+          const int kt = tap / 9, kh = (tap / 3) % 3, kw = tap % 3;
+          const int ti = max(t + kt - 2 + p.cache_frames, 0);
+          tma_load_5d(a_dst, &tmA, &full_bar[s], cc * kBlockK, w0 + kw - 1, h0 + kh - 1, ti, b);
+          tma_load_2d(b_dst, &tmB, &full_bar[s], tap * p.C_in_pad + cc * kBlockK, n0);
+        } else {
+          tma_load_3d(a_dst, &tmA, &full_bar[s], kb * kBlockK, m0, bat);
+          tma_load_3d(b_dst, &tmB, &full_bar[s], kb * kBlockK, n0, bat);
+        }
+        issued_kb = kb + 1;
+      }
+      // drain: every issued load has landed before the block may exit
+      for (int kb = max(0, issued_kb - p.stages); kb < issued_kb; ++kb)
+        mbar_wait(&full_bar[kb % p.stages], (kb / p.stages) & 1, p.fault, p.limit_ns, 2);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kBlockM, static_cast<uint32_t>(p.BN));
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        const int s = kb % p.stages;
+        if (!mbar_wait(&full_bar[s], (kb / p.stages) & 1, p.fault, p.limit_ns, 3)) break;
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(smem + s * stage_bytes);
+        const uint64_t adesc = sdesc_kmajor_sw128(a_addr);
+        const uint64_t bdesc = sdesc_kmajor_sw128(a_addr + kABytes);
+#pragma unroll
+        for (int k = 0; k < kBlockK / 16; ++k) {
+          // advance 16 bf16 (32 B) along K inside the 128-byte swizzle atom
+          tc_mma_bf16(tmem_base, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), idesc,
+                      (kb > 0 || k > 0) ? 1u : 0u);
+        }
+        tc_commit(&empty_bar[s]);
+      }
+      tc_commit(accum_bar);
+      mbar_wait(accum_bar, 0, p.fault, p.limit_ns, 4);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int m = q * 32 + lane;
+    mbar_wait(accum_bar, 0, p.fault, p.limit_ns, 5);
+    tc_fence_after();
+
+    bool valid;
+    int h = 0, w = 0, row = 0;
+    if (p.mode == 0) {
+      h = h0 + m / p.cols_t;
+      w = w0 + m % p.cols_t;
+      valid = (h < h_end) && (w < w_end);
+    } else {
+      row = m0 + m;
+      valid = row < p.M;
+    }
+    const bool vec = (p.mode == 1) ? (p.N_real % 32 == 0)
+                                   : (!p.out_ncthw && (p.C_d2s % 32 == 0));
+    const int sh = p.d2s_h, sw = p.d2s_w;
+    const bool gn = (p.gn_partials != nullptr) && p.mode == 0;
+
+    for (int j = 0; j < (p.BN + 31) / 32; ++j) {
+      uint32_t raw[32];
+      tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(j * 32), raw);
+      tmem_ld_wait();
+      const int nb = n0 + j * 32;
+      if (nb >= p.N_real) continue;
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(raw[i]);
+
+      if (p.mode == 1) {
+        // ---- GEMM epilogue: D[bat, row, n] = alpha * acc + bias[n]
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = v[i] * p.alpha + (p.bias ? p.bias[min(nb + i, p.N_real - 1)] : 0.f);
+        if (!valid) continue;
+        const int64_t base = static_cast<int64_t>(bat) * p.stride_d + static_cast<int64_t>(row) * p.ldd;
+        if (p.residual) {
+          for (int i = 0; i < 32 && nb + i < p.N_real; ++i)
+            v[i] += p.res_f32 ? static_cast<const float*>(p.residual)[base + nb + i]
+                              : bf2f(static_cast<const __nv_bfloat16*>(p.residual)[base + nb + i]);
+        }
+        if (vec) {
+          if (p.out_f32) {
+            float* o = static_cast<float*>(p.y) + base + nb;
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) store8(o + i, v + i);
+          } else {
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.y) + base + nb;
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) store8(o + i, v + i);
+          }
+        } else {
+          for (int i = 0; i < 32 && nb + i < p.N_real; ++i) {
+            if (p.out_f32) static_cast<float*>(p.y)[base + nb + i] = v[i];
+            else static_cast<__nv_bfloat16*>(p.y)[base + nb + i] = f2bf(v[i]);
+          }
+        }
+        continue;
+      }
+
+      // ---- conv epilogue
+      if (vec) {
+        const int sub = nb / p.C_d2s;
+        const int c = nb - sub * p.C_d2s;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] += p.bias ? p.bias[(c + i) * p.S + sub] : 0.f;
+        const int dt = sub / (sh * sw);
+        const int rem = sub - dt * sh * sw;
+        const int dy = rem / sw, dx = rem - (rem / sw) * sw;
+        const int to = p.d2s_t * t + dt - p.drop;
+        if (valid && p.residual) {
+          const int64_t ridx = (((static_cast<int64_t>(b) * p.res_T_alloc + t) * p.H + h) * p.W + w) * p.N_real + nb;
+          float r8[8];
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            if (p.res_f32) load8(static_cast<const float*>(p.residual) + ridx + i, r8);
+            else load8(static_cast<const __nv_bfloat16*>(p.residual) + ridx + i, r8);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[i + k] += r8[k];
+          }
+        }
+        const bool st_ok = valid && to >= 0;
+        if (st_ok) {
+          const int64_t oidx =
+              (((static_cast<int64_t>(b) * p.y_T_alloc + to) * p.H_out + (h * sh + dy)) * p.W_out + (w * sw + dx)) *
+                  p.C_d2s + c;
+          if (p.out_f32) {
+            float* o = static_cast<float*>(p.y) + oidx;
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) store8(o + i, v + i);
+          } else {
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.y) + oidx;
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) store8(o + i, v + i);
+            // statistics see the stored (rounded) values
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = bf2f(f2bf(v[i]));
+          }
+        }
+        if (gn) {
+          // exact per-patch group sums of the stored values; groups never straddle 8 channels here
+          // (cpg is a multiple of 8 or divides 32), the output frame is `to`.
+          const int cpg = p.gn_cpg;
+          for (int i0 = 0; i0 < 32; i0 += min(cpg, 32)) {
+            long long s1 = 0;
+            unsigned long long lo = 0, hi = 0;
+            if (st_ok) {
+              for (int i = i0; i < i0 + min(cpg, 32); ++i) {
+                const float xv = v[i];
+                if (fabsf(xv) >= 8192.f) raise_fault(p.fault, FAULT_RANGE, 20);
+                const int qv = __float2int_rn(fminf(fmaxf(xv, -8191.f), 8191.f) * 262144.f);
+                s1 += qv;
+                const unsigned long long sq = static_cast<unsigned long long>(static_cast<long long>(qv) * qv);
+                lo += sq;
+                if (lo < sq) ++hi;
+              }
+            }
+            // warp reduction (all lanes of the warp share sub, hence frame `to`, and the group)
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+              const long long o1 = __shfl_xor_sync(0xffffffffu, s1, off);
+              const unsigned long long olo = __shfl_xor_sync(0xffffffffu, lo, off);
+              const unsigned long long ohi = __shfl_xor_sync(0xffffffffu, hi, off);
+              s1 += o1;
+              const unsigned long long nlo = lo + olo;
+              hi += ohi + (nlo < lo ? 1ull : 0ull);
+              lo = nlo;
+            }
+            if (lane == 0 && to >= 0) {
+              const int g = (c + i0) / cpg;
+              GnPart* parts = static_cast<GnPart*>(p.gn_partials);
+              const int64_t slot =
+                  ((static_cast<int64_t>(patch) * p.B + b) * p.T_out + to) * p.gn_groups + g;
+              if (s1 != 0 || lo != 0 || hi != 0) gn_accumulate(parts + slot, s1, lo, hi);
+            }
+          }
+        }
+      } else {
+        // generic scalar path (NCTHW pixels, or channel counts not a multiple of 32)
+        for (int i = 0; i < 32; ++i) {
+          const int n = nb + i;
+          if (n >= p.N_real) break;
+          const int sub = n / p.C_d2s;
+          const int c = n - sub * p.C_d2s;
+          float val = v[i] + (p.bias ? p.bias[c * p.S + sub] : 0.f);
+          const int dt = sub / (sh * sw);
+          const int rem = sub - dt * sh * sw;
+          const int dy = rem / sw, dx = rem - (rem / sw) * sw;
+          const int to = p.d2s_t * t + dt - p.drop;
+          if (!valid || to < 0) continue;
+          if (p.residual) {
+            const int64_t ridx = (((static_cast<int64_t>(b) * p.res_T_alloc + t) * p.H + h) * p.W + w) * p.N_real + n;
+            val += p.res_f32 ? static_cast<const float*>(p.residual)[ridx]
+                             : bf2f(static_cast<const __nv_bfloat16*>(p.residual)[ridx]);
+          }
+          const int ho = h * sh + dy, wo = w * sw + dx;
+          int64_t oidx;
+          if (p.out_ncthw)
+            oidx = (((static_cast<int64_t>(b) * p.C_d2s + c) * p.y_T_alloc + to) * p.H_out + ho) * p.W_out + wo;
+          else
+            oidx = (((static_cast<int64_t>(b) * p.y_T_alloc + to) * p.H_out + ho) * p.W_out + wo) * p.C_d2s + c;
+          if (p.out_f32) static_cast<float*>(p.y)[oidx] = val;
+          else static_cast<__nv_bfloat16*>(p.y)[oidx] = f2bf(val);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
+  }
+}
+
+// ================================================================================ host side
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+              const uint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[5], s[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) s[i] = strides_bytes[i];
+  }
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, s, bx, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int pick_cols(const int* pw, int npw) {
+  // tile width (pixels) that wastes the fewest M rows over the patch widths; ties -> 16
+  static const int cand[4] = {16, 8, 32, 64};
+  int best = 16;
+  long best_tiles = -1;
+  for (int ci = 0; ci < 4; ++ci) {
+    const int cw = cand[ci];
+    long tiles = 0;
+    for (int j = 0; j < npw; ++j) tiles += (pw[j + 1] - pw[j] + cw - 1) / cw;
+    const long area = tiles * cw;  // pixels computed per tile-row band
+    if (best_tiles < 0 || area < best_tiles) {
+      best_tiles = area;
+      best = cw;
+    }
+  }
+  return best;
+}
+
+}  // namespace
+
+cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
+  static TcParams p;  // large: built on the host then copied into the launch
+  p = TcParams{};
+  p.mode = a.mode;
+  p.N_real = a.N_real;
+  if (a.N_pad <= 256) {
+    p.BN = a.N_pad;
+  } else {
+    p.BN = 256;
+  }
+  if (p.BN % 16 != 0 || p.BN < 16) return cudaErrorInvalidValue;
+  p.n_ntiles = (a.N_pad + p.BN - 1) / p.BN;
+  p.tmem_cols = 32;
+  while (p.tmem_cols < p.BN) p.tmem_cols <<= 1;
+  const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(p.BN) * kBlockK * 2;
+  p.stages = std::min(8, static_cast<int>((200u * 1024u) / stage_bytes));
+  p.bias = a.bias;
+  p.residual = a.residual;
+  p.res_f32 = a.res_f32;
+  p.y = a.y;
+  p.out_f32 = a.out_f32;
+  p.out_ncthw = a.out_ncthw;
+  p.fault = fault_word();
+  p.limit_ns = wait_limit_ns();
+
+  CUtensorMap tmA, tmB;
+  long long n_blocks;
+  if (a.mode == 0) {
+    p.B = a.B; p.T = a.T; p.H = a.H; p.W = a.W; p.T_in = a.T_in; p.cache_frames = a.cache_frames;
+    p.C_in_pad = a.C_in_pad;
+    if (a.C_in_pad % 64 != 0 || a.nph > kMaxP || a.npw > kMaxP) return cudaErrorInvalidValue;
+    p.nph = a.nph; p.npw = a.npw;
+    for (int i = 0; i <= a.nph; ++i) p.ph_edges[i] = a.ph_edges[i];
+    for (int j = 0; j <= a.npw; ++j) p.pw_edges[j] = a.pw_edges[j];
+    p.cols_t = pick_cols(a.pw_edges, a.npw);
+    p.rows_t = kBlockM / p.cols_t;
+    p.trow_prefix[0] = 0;
+    for (int i = 0; i < a.nph; ++i)
+      p.trow_prefix[i + 1] = p.trow_prefix[i] + (a.ph_edges[i + 1] - a.ph_edges[i] + p.rows_t - 1) / p.rows_t;
+    p.tcol_prefix[0] = 0;
+    for (int j = 0; j < a.npw; ++j)
+      p.tcol_prefix[j + 1] = p.tcol_prefix[j] + (a.pw_edges[j + 1] - a.pw_edges[j] + p.cols_t - 1) / p.cols_t;
+    p.n_trows = p.trow_prefix[a.nph];
+    p.n_tcols = p.tcol_prefix[a.npw];
+    p.cchunks = a.C_in_pad / kBlockK;
+    p.num_kb = 27 * p.cchunks;
+    p.d2s_t = a.d2s_t; p.d2s_h = a.d2s_h; p.d2s_w = a.d2s_w;
+    p.S = a.d2s_t * a.d2s_h * a.d2s_w;
+    p.C_d2s = a.N_real / p.S;
+    p.drop = a.drop_first ? a.d2s_t - 1 : 0;
+    p.T_out = a.d2s_t * a.T - p.drop;
+    p.H_out = a.H * a.d2s_h;
+    p.W_out = a.W * a.d2s_w;
+    p.res_T_alloc = a.res_T_alloc ? a.res_T_alloc : a.T;
+    p.y_T_alloc = a.y_T_alloc ? a.y_T_alloc : p.T_out;
+    if (a.residual && p.S != 1) return cudaErrorInvalidValue;
+    p.gn_partials = a.gn_partials;
+    p.gn_groups = a.gn_groups;
+    p.gn_cpg = a.gn_groups ? p.C_d2s / a.gn_groups : 0;
+    if (a.gn_partials && (p.C_d2s % 32 != 0 || a.out_ncthw || (p.gn_cpg < 32 ? 32 % p.gn_cpg : p.gn_cpg % 32) != 0))
+      return cudaErrorInvalidValue;
+    const uint64_t C = a.C_in_pad;
+    const uint64_t xTa = a.x_T_alloc ? a.x_T_alloc : a.T_in;
+    uint64_t dims[5] = {C, (uint64_t)a.W, (uint64_t)a.H, (uint64_t)a.T_in, (uint64_t)a.B};
+    uint64_t strides[4] = {C * 2, C * 2 * a.W, C * 2 * a.W * a.H, C * 2 * a.W * a.H * xTa};
+    uint32_t box[5] = {64u, (uint32_t)p.cols_t, (uint32_t)p.rows_t, 1u, 1u};
+    if (!make_map(&tmA, a.x, 5, dims, strides, box)) return cudaErrorInvalidValue;
+    const uint64_t K = 27ull * C;
+    uint64_t wd[2] = {K, (uint64_t)a.N_pad};
+    uint64_t ws[1] = {K * 2};
+    uint32_t wb[2] = {64u, (uint32_t)p.BN};
+    if (!make_map(&tmB, a.w, 2, wd, ws, wb)) return cudaErrorInvalidValue;
+    n_blocks = static_cast<long long>(a.B) * a.T * p.n_trows * p.n_tcols * p.n_ntiles;
+  } else {
+    p.M = a.M; p.K = a.K; p.batch = a.batch; p.stride_d = a.stride_d; p.alpha = a.alpha;
+    p.ldd = a.ldd ? a.ldd : a.N_real;
+    if (a.K % 64 != 0) return cudaErrorInvalidValue;
+    p.m_tiles_per_batch = (a.M + kBlockM - 1) / kBlockM;
+    p.num_kb = a.K / kBlockK;
+    p.S = 1; p.C_d2s = a.N_real; p.d2s_t = p.d2s_h = p.d2s_w = 1;
+    const int64_t sa = a.batch > 1 ? a.stride_a : static_cast<int64_t>(a.M) * a.K;
+    const int64_t sb = a.batch > 1 ? a.stride_b : static_cast<int64_t>(a.N_real) * a.K;
+    if (sa % 8 || sb % 8 || a.K % 8) return cudaErrorInvalidValue;
+    uint64_t ad[3] = {(uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.batch};
+    uint64_t as[2] = {(uint64_t)a.K * 2, (uint64_t)sa * 2};
+    uint32_t ab[3] = {64u, 128u, 1u};
+    if (!make_map(&tmA, a.x, 3, ad, as, ab)) return cudaErrorInvalidValue;
+    // B rows beyond N_real read as zeros (never the next batch item's rows)
+    uint64_t bd[3] = {(uint64_t)a.K, (uint64_t)a.N_real, (uint64_t)a.batch};
+    uint64_t bs[2] = {(uint64_t)a.K * 2, (uint64_t)sb * 2};
+    uint32_t bb[3] = {64u, (uint32_t)p.BN, 1u};
+    if (!make_map(&tmB, a.w, 3, bd, bs, bb)) return cudaErrorInvalidValue;
+    n_blocks = static_cast<long long>(a.batch) * p.m_tiles_per_batch * p.n_ntiles;
+  }
+  if (n_blocks <= 0) return cudaSuccess;
+  if (n_blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const size_t smem = 1024 + static_cast<size_t>(p.stages) * stage_bytes + (2 * p.stages + 1) * 8 + 16;
+  static int attr_set = 0;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(conv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_set = 1;
+  }
+  conv_tc_kernel<<<static_cast<unsigned>(n_blocks), kThreads, smem, stream>>>(tmA, tmB, p);
+  return cudaGetLastError();
+}
+
+}  // namespace vae

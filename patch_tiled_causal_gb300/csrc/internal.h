@@ -1,0 +1,112 @@
+// Internal launcher interface shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/vaedec.h"
+
+namespace vae {
+
+constexpr int kMaxP = VAE_MAX_PATCHES;
+
+// Device fault word of the current device (4 x u32, see common.cuh).
+uint32_t* fault_word();
+// Default bound of every in-kernel wait, nanoseconds.
+uint64_t wait_limit_ns();
+
+// Tensor-core (tcgen05) convolution / GEMM.  All pointers device.
+struct ConvTcArgs {
+  int mode;  // 0 = causal conv3d (implicit GEMM over 27 taps), 1 = batched GEMM
+  // conv geometry
+  int B, T, H, W;       // output frames / rows / cols before depth-to-space
+  int C_in_pad;         // channels of x (multiple of 64)
+  int T_in;             // frames readable from x (T + cache_frames)
+  int x_T_alloc;        // frames between consecutive batch items of x (>= T_in)
+  int cache_frames;     // 0 or 2
+  int nph, npw;
+  const int* ph_edges;  // host arrays nph+1 / npw+1
+  const int* pw_edges;
+  // gemm geometry
+  int M, K, batch;
+  int64_t stride_a, stride_b, stride_d;
+  float alpha;
+  // operands
+  const void* x;        // conv: x channels-last bf16; gemm: A
+  const void* w;        // conv: packed weights bf16 [N_pad, 27*C_in_pad]; gemm: B [N, K]
+  int N_real, N_pad;
+  const float* bias;    // conv: PyTorch channel order (index c*S + sub); gemm: [N]
+  const void* residual; int res_f32; int res_T_alloc;  // residual [B, res_T_alloc, H, W, N] (0 = T)
+  void* y; int out_f32; int out_ncthw; int y_T_alloc;    // y frames per batch item (0 = T_out)
+  int64_t ldd;                                           // gemm: row stride of D (0 = N_real)
+  int d2s_t, d2s_h, d2s_w, drop_first;
+  // fused group-norm statistics of y (nullptr = none): exact per-patch sums, see norm.cu
+  void* gn_partials; int gn_groups;
+};
+cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t s);
+
+// CUDA-core convolution (any channel count, fp32 or bf16 storage, fp32 accumulation).
+struct ConvSimtArgs {
+  int B, T, H, W, C_in, C_out, T_in, x_T_alloc, cache_frames;
+  const void* x; int x_f32;
+  const float* w;  // [27, C_in, C_out] fp32
+  const float* bias;
+  const void* residual; int res_f32; int res_T_alloc;
+  void* y; int out_f32; int out_ncthw; int y_T_alloc;
+  int d2s_t, d2s_h, d2s_w, drop_first;
+  int nph, npw; const int* ph_edges; const int* pw_edges;
+};
+cudaError_t launch_conv_simt(const ConvSimtArgs& a, cudaStream_t s);
+
+// Weight packing.
+cudaError_t launch_pack_weights_bf16(const float* w, int C_out, int C_in, int C_in_pad, int N_pad, int S,
+                                     void* out, cudaStream_t s);
+cudaError_t launch_pack_weights_f32(const float* w, int C_out, int C_in, void* out, cudaStream_t s);
+cudaError_t launch_pack_matrix_bf16(const float* w, int rows, int cols, void* out, cudaStream_t s);
+
+// Group norm.
+struct GnArgs {
+  int B, T, H, W, C, groups;
+  float eps;
+  int silu;
+  int nph, npw; const int* ph_edges; const int* pw_edges;
+  const void* x; int x_f32; int x_T_alloc;  // frames per batch item in memory (0 = T)
+  void* y; int y_f32; int y_T_alloc;
+  const float* gamma; const float* beta;
+  void* partials;          // [nph*npw, B, T, groups] x GnPartial
+};
+size_t gn_partials_bytes(int nph, int npw, int B, int T, int groups);
+cudaError_t launch_gn_stats(const GnArgs& a, cudaStream_t s);  // clears and fills partials
+cudaError_t launch_gn_apply(const GnArgs& a, cudaStream_t s);
+
+// Layout helpers.
+// Latent box [B, C, t0:t0+nt, h0:h0+nh, w0:w0+nw] of an NCTHW fp32 tensor [B, C, T, H, W] ->
+// channels-last [B, y_T_alloc, nh, nw, C_pad] (frames 0..nt-1 of each batch item), zero channels >= C.
+cudaError_t launch_latent_to_cl(const float* z, int B, int C, int T, int H, int W, int t0, int nt, int h0, int nh, int w0,
+                                int nw, int C_pad, void* y, int y_f32, int y_T_alloc, cudaStream_t s);
+cudaError_t launch_d2s(const void* x, void* y, int B, int T, int H, int W, int C, int st, int sh, int sw,
+                       int drop_first, int f32, cudaStream_t s);
+cudaError_t launch_copy_frames(const void* src, int src_T, int src_t0, void* dst, int dst_T, int dst_t0, int n_frames,
+                               int B, int64_t frame_bytes, cudaStream_t s);
+
+// Tile blend.
+cudaError_t launch_blend(const void* const* tiles, const vae_tile_t* meta, int n_tiles, void* out,
+                         const vae_blend_desc_t& d, cudaStream_t s);
+
+// CUDA-core batched GEMM (fp32 storage): D[b] = alpha * A[b] B[b]^T + bias[n] + residual, with
+// B element (n, k) at B + n*ldb_n + k*ldb_k.  A [M, K] row-major, D/residual [M, N] row-major.
+cudaError_t launch_gemm_simt(const float* A, const float* Bm, float* D, const float* bias, const float* residual,
+                             int M, int N, int K, int batch, int64_t sa, int64_t sb, int64_t sd, int64_t ldb_n,
+                             int64_t ldb_k, float alpha, cudaStream_t s);
+// Cast / copy a channels-last tensor between frame layouts and dtypes.
+cudaError_t launch_cast_frames(const void* x, int x_f32, int x_T_alloc, void* y, int y_f32, int y_T_alloc, int B, int T,
+                               int64_t frame_elems, cudaStream_t s);
+
+// Softmax over rows of an fp32 matrix, written as bf16 (attention probabilities).
+cudaError_t launch_softmax_rows(const float* s_in, void* p_out, int p_f32, int rows, int cols, int ld_out, cudaStream_t s);
+// Channels-last bf16 [N, C] -> transposed copy [C, N] (per batch).
+cudaError_t launch_transpose_bf16(const void* in, void* out, int batch, int rows, int cols, cudaStream_t s);
+
+cudaError_t launch_watchdog_test(uint64_t limit_ns, cudaStream_t s);
+
+}  // namespace vae

@@ -1,0 +1,646 @@
+// HBM-bound kernels: PatchGroupNorm (+ SiLU), tile blend, depth-to-space, layout changes,
+// attention softmax, weight packing, and the watchdog self-test.
+//
+// PatchGroupNorm follows DistVAE PR #14 "Add tiled VAE parallelism & extended model support"
+// (PatchGroupNorm commit: the exact global mean and the population variance, divide by the count;
+// two-collective commit: per-patch counts and sums are merged before anything is normalised).
+// Statistics are per (batch, frame, group).  Every element contributes q = round(x * 2^18) (|x| <
+// 2^13, so q fits in 32 bits) to an int64 sum and q^2 to a 128-bit sum.  Integer addition is
+// associative, so the totals are exact and identical whichever patch, block or warp adds which
+// element: the normalised output does not change by one bit with the patch grid.  Each patch owns
+// its own partial-sum slots; the merge adds them in patch order, then forms mean = S1 / (N 2^18) and
+// var = S2 / (N 2^36) - mean^2 in fp64 (the exact totals carry the cancellation a float
+// E[x^2] - E[x]^2 would suffer, so the two passes of the pages' estimator fold into one read).
+//
+// The tile blend follows TensorRT-LLM PR #15753 "LTX-2 tile-parallel VAE decode" (Approach: a
+// per-tile mask built on the device from 1-D parts, weighted sum over the weight sum); here each
+// output pixel gathers the tiles that cover it, in tile order, so the result is written once.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace vae {
+
+// ============================================================================ group norm
+struct GnPartial {
+  unsigned long long s1;     // int64 sum of q (two's complement)
+  unsigned long long s2_lo;  // 128-bit sum of q^2
+  unsigned long long s2_hi;
+  unsigned long long pad;
+};
+static_assert(sizeof(GnPartial) == 32, "GnPartial layout is shared with the conv epilogue");
+
+size_t gn_partials_bytes(int nph, int npw, int B, int T, int groups) {
+  return static_cast<size_t>(nph) * npw * B * T * groups * sizeof(GnPartial);
+}
+
+struct GnParams {
+  int B, T, H, W, C, groups, cpg;
+  float eps;
+  int silu;
+  int nph, npw;
+  int ph_edges[kMaxP + 1], pw_edges[kMaxP + 1];
+  const void* x;
+  int x_f32, x_T_alloc;
+  void* y;
+  int y_f32, y_T_alloc;
+  const float* gamma;
+  const float* beta;
+  GnPartial* parts;
+  uint32_t* fault;
+  int vec_per_px;   // C / 8
+  int px_per_iter;  // blockDim / vec_per_px
+};
+
+namespace {
+
+VAE_DEV void add128(unsigned long long& lo, unsigned long long& hi, unsigned long long a_lo, unsigned long long a_hi) {
+  const unsigned long long n = lo + a_lo;
+  hi += a_hi + (n < lo ? 1ull : 0ull);
+  lo = n;
+}
+
+VAE_DEV int quantize(float x, uint32_t* fault) {
+  if (!(fabsf(x) < 8192.f)) {  // also catches NaN
+    raise_fault(fault, FAULT_RANGE, 30);
+    x = fminf(fmaxf(x, -8191.f), 8191.f);
+    if (x != x) x = 0.f;
+  }
+  return __float2int_rn(x * 262144.f);  // exact scaling by 2^18
+}
+
+}  // namespace
+
+// One block per (frame, image row, patch column): the row segment lies in exactly one patch.
+// GPV = groups met by one 8-channel vector (1 when channels-per-group is a multiple of 8).
+template <int GPV, typename T>
+__global__ void __launch_bounds__(256) gn_stats_kernel(const __grid_constant__ GnParams p) {
+  __shared__ unsigned long long sh_s1[1024], sh_lo[1024], sh_hi[1024];
+  const int j = blockIdx.x % p.npw;
+  const int row = blockIdx.x / p.npw;  // frame * H + h
+  const int h = row % p.H;
+  const int frame = row / p.H;
+  const int fb = frame / p.T, ft = frame % p.T;
+  for (int g = threadIdx.x; g < p.groups; g += blockDim.x) sh_s1[g] = sh_lo[g] = sh_hi[g] = 0ull;
+  __syncthreads();
+
+  const int vid = threadIdx.x % p.vec_per_px;
+  const int pxo = threadIdx.x / p.vec_per_px;
+  const int c0 = vid * 8;
+  const int w_beg = p.pw_edges[j], w_end = p.pw_edges[j + 1];
+  const T* xr = static_cast<const T*>(p.x) + ((static_cast<int64_t>(fb) * p.x_T_alloc + ft) * p.H + h) * p.W * p.C;
+  long long s1[GPV];
+  unsigned long long lo[GPV], hi[GPV];
+#pragma unroll
+  for (int k = 0; k < GPV; ++k) { s1[k] = 0; lo[k] = hi[k] = 0ull; }
+  if (threadIdx.x < p.vec_per_px * p.px_per_iter) {
+    for (int w = w_beg + pxo; w < w_end; w += p.px_per_iter) {
+      float v[8];
+      load8(xr + static_cast<int64_t>(w) * p.C + c0, v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int k = (GPV == 1) ? 0 : e / (8 / GPV);
+        const int qv = quantize(v[e], p.fault);
+        s1[k] += qv;
+        const unsigned long long sq = static_cast<unsigned long long>(static_cast<long long>(qv) * qv);
+        add128(lo[k], hi[k], sq, 0ull);
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < GPV; ++k) {
+    const int g = (GPV == 1) ? c0 / p.cpg : (c0 / p.cpg + k);
+    if (s1[k] != 0 || lo[k] != 0 || hi[k] != 0) {
+      atomicAdd(&sh_s1[g], static_cast<unsigned long long>(s1[k]));
+      const unsigned long long old = atomicAdd(&sh_lo[g], lo[k]);
+      const unsigned long long carry = (old + lo[k] < old) ? 1ull : 0ull;
+      if (hi[k] + carry) atomicAdd(&sh_hi[g], hi[k] + carry);
+    }
+  }
+  __syncthreads();
+  // this block's segment belongs to patch (band of h, j)
+  int i = 0;
+  while (i + 1 < p.nph && p.ph_edges[i + 1] <= h) ++i;
+  const int patch = i * p.npw + j;
+  const int b = frame / p.T, t = frame % p.T;
+  for (int g = threadIdx.x; g < p.groups; g += blockDim.x) {
+    GnPartial* d = p.parts + ((static_cast<int64_t>(patch) * p.B + b) * p.T + t) * p.groups + g;
+    const unsigned long long a1 = sh_s1[g], alo = sh_lo[g], ahi = sh_hi[g];
+    if (a1 == 0 && alo == 0 && ahi == 0) continue;
+    atomicAdd(&d->s1, a1);
+    const unsigned long long old = atomicAdd(&d->s2_lo, alo);
+    const unsigned long long carry = (old + alo < old) ? 1ull : 0ull;
+    if (ahi + carry) atomicAdd(&d->s2_hi, ahi + carry);
+  }
+}
+
+// Merge the per-patch sums (patch order) and normalise; one block per (frame, image row).
+template <typename TI, typename TO>
+__global__ void __launch_bounds__(256) gn_apply_kernel(const __grid_constant__ GnParams p) {
+  __shared__ float sh_mean[1024], sh_rstd[1024];
+  const int row = blockIdx.x;  // frame * H + h
+  const int frame = row / p.H, h = row % p.H;
+  const int b = frame / p.T, t = frame % p.T;
+  const double n = static_cast<double>(p.cpg) * p.H * p.W;
+  const int P = p.nph * p.npw;
+  for (int g = threadIdx.x; g < p.groups; g += blockDim.x) {
+    long long s1 = 0;
+    unsigned long long lo = 0, hi = 0;
+    for (int q = 0; q < P; ++q) {
+      const GnPartial& d = p.parts[((static_cast<int64_t>(q) * p.B + b) * p.T + t) * p.groups + g];
+      s1 += static_cast<long long>(d.s1);
+      add128(lo, hi, d.s2_lo, d.s2_hi);
+    }
+    const double mq = static_cast<double>(s1) / n;                                   // mean, units 2^-18
+    const double e2 = (static_cast<double>(hi) * 18446744073709551616.0 + static_cast<double>(lo)) / n;
+    double var = (e2 - mq * mq) * (1.0 / 68719476736.0);                             // / 2^36
+    if (var < 0.0) var = 0.0;
+    sh_mean[g] = static_cast<float>(mq * (1.0 / 262144.0));
+    sh_rstd[g] = static_cast<float>(1.0 / sqrt(var + static_cast<double>(p.eps)));
+  }
+  __syncthreads();
+  const TI* xr = static_cast<const TI*>(p.x) + ((static_cast<int64_t>(b) * p.x_T_alloc + t) * p.H + h) * p.W * p.C;
+  const int64_t yrow = (static_cast<int64_t>(b) * p.y_T_alloc + t) * p.H + h;
+  TO* yr = static_cast<TO*>(p.y) + yrow * p.W * p.C;
+  const int nvec = p.W * p.C / 8;
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+    const int c0 = (v * 8) % p.C;
+    float a[8], o[8];
+    load8(xr + static_cast<int64_t>(v) * 8, a);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int c = c0 + e;
+      const int g = c / p.cpg;
+      float z = (a[e] - sh_mean[g]) * sh_rstd[g] * p.gamma[c] + p.beta[c];
+      o[e] = p.silu ? silu_f(z) : z;
+    }
+    store8(yr + static_cast<int64_t>(v) * 8, o);
+  }
+}
+
+namespace {
+bool fill_gn(GnParams& p, const GnArgs& a) {
+  p = GnParams{};
+  p.B = a.B; p.T = a.T; p.H = a.H; p.W = a.W; p.C = a.C; p.groups = a.groups;
+  if (a.groups <= 0 || a.groups > 1024 || a.C % a.groups) return false;
+  p.cpg = a.C / a.groups;
+  if (a.C % 8 || a.C > 8192 || !(p.cpg % 8 == 0 || 8 % p.cpg == 0)) return false;
+  if (a.nph > kMaxP || a.npw > kMaxP) return false;
+  p.eps = a.eps; p.silu = a.silu;
+  p.nph = a.nph; p.npw = a.npw;
+  for (int i = 0; i <= a.nph; ++i) p.ph_edges[i] = a.ph_edges[i];
+  for (int j = 0; j <= a.npw; ++j) p.pw_edges[j] = a.pw_edges[j];
+  p.x = a.x; p.x_f32 = a.x_f32; p.y = a.y; p.y_f32 = a.y_f32;
+  p.x_T_alloc = a.x_T_alloc ? a.x_T_alloc : a.T;
+  p.y_T_alloc = a.y_T_alloc ? a.y_T_alloc : a.T;
+  p.gamma = a.gamma; p.beta = a.beta;
+  p.parts = static_cast<GnPartial*>(a.partials);
+  p.fault = fault_word();
+  p.vec_per_px = a.C / 8;
+  p.px_per_iter = std::max(1, 256 / p.vec_per_px);
+  return true;
+}
+}  // namespace
+
+cudaError_t launch_gn_stats(const GnArgs& a, cudaStream_t s) {
+  static GnParams p;
+  if (!fill_gn(p, a)) return cudaErrorInvalidValue;
+  cudaError_t e = cudaMemsetAsync(a.partials, 0, gn_partials_bytes(a.nph, a.npw, a.B, a.T, a.groups), s);
+  if (e != cudaSuccess) return e;
+  const long long nb = static_cast<long long>(a.B) * a.T * a.H * a.npw;
+  if (nb == 0) return cudaSuccess;
+  const int threads = std::max(p.vec_per_px * p.px_per_iter, 32);
+  if (threads > 1024) return cudaErrorInvalidValue;
+  const int gpv = p.cpg >= 8 ? 1 : 8 / p.cpg;
+  dim3 grid(static_cast<unsigned>(nb));
+#define VAE_GN_STATS(G)                                                                   \
+  if (a.x_f32) gn_stats_kernel<G, float><<<grid, threads, 0, s>>>(p);                     \
+  else gn_stats_kernel<G, __nv_bfloat16><<<grid, threads, 0, s>>>(p);
+  switch (gpv) {
+    case 1: VAE_GN_STATS(1) break;
+    case 2: VAE_GN_STATS(2) break;
+    case 4: VAE_GN_STATS(4) break;
+    default: VAE_GN_STATS(8) break;
+  }
+#undef VAE_GN_STATS
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gn_apply(const GnArgs& a, cudaStream_t s) {
+  static GnParams p;
+  if (!fill_gn(p, a)) return cudaErrorInvalidValue;
+  const long long nb = static_cast<long long>(a.B) * a.T * a.H;
+  if (nb == 0) return cudaSuccess;
+  dim3 grid(static_cast<unsigned>(nb));
+  if (a.x_f32 && a.y_f32) gn_apply_kernel<float, float><<<grid, 256, 0, s>>>(p);
+  else if (a.x_f32) gn_apply_kernel<float, __nv_bfloat16><<<grid, 256, 0, s>>>(p);
+  else if (a.y_f32) gn_apply_kernel<__nv_bfloat16, float><<<grid, 256, 0, s>>>(p);
+  else gn_apply_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ============================================================================ layouts
+template <typename TO>
+__global__ void latent_to_cl_kernel(const float* z, int B, int C, int T, int H, int W, int t0, int nt, int h0, int nh,
+                                    int w0, int nw, int Cp, TO* y, int yTa) {
+  const int64_t n = static_cast<int64_t>(B) * nt * nh * nw * Cp;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(i % Cp);
+    int64_t r = i / Cp;
+    const int w = static_cast<int>(r % nw); r /= nw;
+    const int h = static_cast<int>(r % nh); r /= nh;
+    const int t = static_cast<int>(r % nt);
+    const int b = static_cast<int>(r / nt);
+    float v = 0.f;
+    if (c < C) v = z[((((static_cast<int64_t>(b) * C + c) * T + t0 + t) * H + h0 + h) * W) + w0 + w];
+    y[(((static_cast<int64_t>(b) * yTa + t) * nh + h) * nw + w) * Cp + c] = from_f<TO>(v);
+  }
+}
+
+cudaError_t launch_latent_to_cl(const float* z, int B, int C, int T, int H, int W, int t0, int nt, int h0, int nh, int w0,
+                                int nw, int C_pad, void* y, int y_f32, int y_T_alloc, cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(B) * nt * nh * nw * C_pad;
+  if (n == 0) return cudaSuccess;
+  const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 152 * 64));
+  if (y_f32)
+    latent_to_cl_kernel<float><<<blocks, 256, 0, s>>>(z, B, C, T, H, W, t0, nt, h0, nh, w0, nw, C_pad,
+                                                       static_cast<float*>(y), y_T_alloc);
+  else
+    latent_to_cl_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(z, B, C, T, H, W, t0, nt, h0, nh, w0, nw, C_pad,
+                                                               static_cast<__nv_bfloat16*>(y), y_T_alloc);
+  return cudaGetLastError();
+}
+
+// depth-to-space, channels-last; one thread per 8 output channels (C % 8 == 0) or per element
+template <typename T>
+__global__ void d2s_kernel(const T* x, T* y, int B, int T_, int H, int W, int C, int st, int sh, int sw, int drop,
+                           int vec) {
+  const int To = st * T_ - drop, Ho = H * sh, Wo = W * sw;
+  const int cw = vec ? 8 : 1;
+  const int64_t n = static_cast<int64_t>(B) * To * Ho * Wo * (C / cw);
+  const int S = st * sh * sw;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int cv = static_cast<int>(i % (C / cw));
+    int64_t r = i / (C / cw);
+    const int wo = static_cast<int>(r % Wo); r /= Wo;
+    const int ho = static_cast<int>(r % Ho); r /= Ho;
+    const int to = static_cast<int>(r % To);
+    const int b = static_cast<int>(r / To);
+    const int tf = to + drop;
+    const int t = tf / st, dt = tf % st, h = ho / sh, dy = ho % sh, w = wo / sw, dx = wo % sw;
+    const int sub = (dt * sh + dy) * sw + dx;
+    const int64_t xpix = ((static_cast<int64_t>(b) * T_ + t) * H + h) * W + w;
+    const int64_t ypix = ((static_cast<int64_t>(b) * To + to) * Ho + ho) * Wo + wo;
+    for (int e = 0; e < cw; ++e) {
+      const int c = cv * cw + e;
+      y[ypix * C + c] = x[xpix * C * S + static_cast<int64_t>(c) * S + sub];
+    }
+  }
+}
+
+cudaError_t launch_d2s(const void* x, void* y, int B, int T, int H, int W, int C, int st, int sh, int sw,
+                       int drop_first, int f32, cudaStream_t s) {
+  const int drop = drop_first ? st - 1 : 0;
+  const int64_t n = static_cast<int64_t>(B) * (st * T - drop) * H * sh * W * sw * C;
+  if (n <= 0) return cudaSuccess;
+  const int blocks = static_cast<int>(std::min<int64_t>((n / 8 + 255) / 256 + 1, 152 * 64));
+  const int vec = (C % 8 == 0);
+  if (f32) d2s_kernel<float><<<blocks, 256, 0, s>>>(static_cast<const float*>(x), static_cast<float*>(y), B, T, H, W, C, st, sh, sw, drop, vec);
+  else d2s_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), B, T, H, W, C, st, sh, sw, drop, vec);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_frames(const void* src, int src_T, int src_t0, void* dst, int dst_T, int dst_t0, int n_frames,
+                               int B, int64_t frame_bytes, cudaStream_t s) {
+  if (n_frames <= 0 || B <= 0) return cudaSuccess;
+  const char* sp = static_cast<const char*>(src) + src_t0 * frame_bytes;
+  char* dp = static_cast<char*>(dst) + dst_t0 * frame_bytes;
+  return cudaMemcpy2DAsync(dp, dst_T * frame_bytes, sp, src_T * frame_bytes, n_frames * frame_bytes, B,
+                           cudaMemcpyDeviceToDevice, s);
+}
+
+// ============================================================================ tile blend
+struct BlendTile {
+  const void* ptr;
+  int t0, nt, h0, nh, w0, nw;
+  unsigned short ovl[6];
+};
+struct BlendParams {
+  int B, C, T, H, W, n;
+  int tile_f32, out_f32;
+  void* out;
+  BlendTile tiles[VAE_MAX_TILES];
+};
+
+VAE_DEV float ramp_w(int y, int n, int lo, int hi) {
+  float w = 1.f;
+  if (y < lo) w *= static_cast<float>(y + 1) / static_cast<float>(lo + 1);
+  if (y >= n - hi) w *= static_cast<float>(n - y) / static_cast<float>(hi + 1);
+  return w;
+}
+
+// one block per output row (b, c, t, y): collect the tiles covering (t, y) in order, then gather
+template <typename TT, typename TO>
+__global__ void __launch_bounds__(128) blend_kernel(const __grid_constant__ BlendParams p) {
+  __shared__ int list[VAE_MAX_TILES];
+  __shared__ float wty[VAE_MAX_TILES];
+  __shared__ unsigned char flag[VAE_MAX_TILES];
+  __shared__ int count;
+  int64_t r = blockIdx.x;
+  const int y = static_cast<int>(r % p.H); r /= p.H;
+  const int t = static_cast<int>(r % p.T); r /= p.T;
+  const int c = static_cast<int>(r % p.C);
+  const int b = static_cast<int>(r / p.C);
+  for (int i = threadIdx.x; i < p.n; i += blockDim.x) {
+    const BlendTile& tl = p.tiles[i];
+    flag[i] = (t >= tl.t0 && t < tl.t0 + tl.nt && y >= tl.h0 && y < tl.h0 + tl.nh) ? 1 : 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int k = 0;
+    for (int i = 0; i < p.n; ++i)
+      if (flag[i]) {
+        const BlendTile& tl = p.tiles[i];
+        list[k] = i;
+        wty[k] = ramp_w(t - tl.t0, tl.nt, tl.ovl[0], tl.ovl[1]) * ramp_w(y - tl.h0, tl.nh, tl.ovl[2], tl.ovl[3]);
+        ++k;
+      }
+    count = k;
+  }
+  __syncthreads();
+  const int nk = count;
+  TO* orow = static_cast<TO*>(p.out) + (((static_cast<int64_t>(b) * p.C + c) * p.T + t) * p.H + y) * p.W;
+  for (int x0 = threadIdx.x * 8; x0 < p.W; x0 += blockDim.x * 8) {
+    float acc[8], ws[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = ws[e] = 0.f;
+    for (int k = 0; k < nk; ++k) {
+      const BlendTile& tl = p.tiles[list[k]];
+      if (x0 + 8 <= tl.w0 || x0 >= tl.w0 + tl.nw) continue;
+      const TT* trow = static_cast<const TT*>(tl.ptr) +
+                       (((static_cast<int64_t>(b) * p.C + c) * tl.nt + (t - tl.t0)) * tl.nh + (y - tl.h0)) * tl.nw;
+      const float wk = wty[k];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int x = x0 + e;
+        if (x < tl.w0 || x >= tl.w0 + tl.nw || x >= p.W) continue;
+        const float wx = wk * ramp_w(x - tl.w0, tl.nw, tl.ovl[4], tl.ovl[5]);
+        acc[e] += wx * to_f<TT>(trow[x - tl.w0]);
+        ws[e] += wx;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (x0 + e < p.W) orow[x0 + e] = from_f<TO>(ws[e] > 0.f ? acc[e] / ws[e] : 0.f);
+  }
+}
+
+cudaError_t launch_blend(const void* const* tiles, const vae_tile_t* meta, int n_tiles, void* out,
+                         const vae_blend_desc_t& d, cudaStream_t s) {
+  static BlendParams p;
+  if (n_tiles > VAE_MAX_TILES) return cudaErrorInvalidValue;
+  p.B = d.B; p.C = d.C; p.T = d.T; p.H = d.H; p.W = d.W; p.n = n_tiles;
+  p.tile_f32 = d.tile_dtype == VAE_FP32;
+  p.out_f32 = d.out_dtype == VAE_FP32;
+  p.out = out;
+  for (int i = 0; i < n_tiles; ++i) {
+    BlendTile& t = p.tiles[i];
+    t.ptr = tiles[i];
+    t.t0 = meta[i].pix[0]; t.nt = meta[i].pix[1];
+    t.h0 = meta[i].pix[2]; t.nh = meta[i].pix[3];
+    t.w0 = meta[i].pix[4]; t.nw = meta[i].pix[5];
+    for (int k = 0; k < 6; ++k) t.ovl[k] = static_cast<unsigned short>(meta[i].ovl[k]);
+  }
+  const long long nb = static_cast<long long>(d.B) * d.C * d.T * d.H;
+  if (nb == 0) return cudaSuccess;
+  dim3 grid(static_cast<unsigned>(nb));
+  if (p.tile_f32 && p.out_f32) blend_kernel<float, float><<<grid, 128, 0, s>>>(p);
+  else if (p.tile_f32) blend_kernel<float, __nv_bfloat16><<<grid, 128, 0, s>>>(p);
+  else if (p.out_f32) blend_kernel<__nv_bfloat16, float><<<grid, 128, 0, s>>>(p);
+  else blend_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 128, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ============================================================================ attention helpers
+// softmax over each row's first `cols` entries; padded columns of P (up to ld_out) are zeroed
+template <typename TO>
+__global__ void __launch_bounds__(256) softmax_rows_kernel(const float* s, TO* p, int cols, int ld_out) {
+  __shared__ float red[32];
+  const float* row = s + static_cast<int64_t>(blockIdx.x) * cols;
+  TO* out = p + static_cast<int64_t>(blockIdx.x) * ld_out;
+  float m = -INFINITY;
+  for (int i = threadIdx.x; i < cols; i += blockDim.x) m = fmaxf(m, row[i]);
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : -INFINITY;
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  m = red[0];
+  __syncthreads();
+  float sum = 0.f;
+  for (int i = threadIdx.x; i < cols; i += blockDim.x) sum += expf(row[i] - m);
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sum;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float inv = 1.f / red[0];
+  for (int i = threadIdx.x; i < ld_out; i += blockDim.x)
+    out[i] = from_f<TO>(i < cols ? expf(row[i] - m) * inv : 0.f);
+}
+
+cudaError_t launch_softmax_rows(const float* s_in, void* p_out, int p_f32, int rows, int cols, int ld_out,
+                                cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (p_f32) softmax_rows_kernel<float><<<rows, 256, 0, s>>>(s_in, static_cast<float*>(p_out), cols, ld_out);
+  else softmax_rows_kernel<__nv_bfloat16><<<rows, 256, 0, s>>>(s_in, static_cast<__nv_bfloat16*>(p_out), cols, ld_out);
+  return cudaGetLastError();
+}
+
+// CUDA-core batched GEMM, 32 x 32 output tile per block, fp32
+__global__ void __launch_bounds__(256) gemm_simt_kernel(const float* A, const float* Bm, float* D, const float* bias,
+                                                        const float* res, int M, int N, int K, int64_t sa, int64_t sb,
+                                                        int64_t sd, int64_t ldb_n, int64_t ldb_k, float alpha) {
+  __shared__ float As[32][33], Bs[32][33];
+  const int bz = blockIdx.z;
+  const float* a = A + bz * sa;
+  const float* bmat = Bm + bz * sb;
+  const int m0 = blockIdx.y * 32, n0 = blockIdx.x * 32;
+  const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;  // 32 x 8
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int k0 = 0; k0 < K; k0 += 32) {
+    for (int r = ty; r < 32; r += 8) {
+      const int m = m0 + r, k = k0 + tx, n = n0 + r;
+      As[r][tx] = (m < M && k < K) ? a[static_cast<int64_t>(m) * K + k] : 0.f;
+      Bs[r][tx] = (n < N && k < K) ? bmat[n * ldb_n + k * ldb_k] : 0.f;
+    }
+    __syncthreads();
+    for (int k = 0; k < 32; ++k) {
+      const float bv = Bs[tx][k];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] = fmaf(As[ty + 8 * i][k], bv, acc[i]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty + 8 * i, n = n0 + tx;
+    if (m < M && n < N) {
+      const int64_t o = bz * sd + static_cast<int64_t>(m) * N + n;
+      float v = acc[i] * alpha + (bias ? bias[n] : 0.f);
+      if (res) v += res[o];
+      D[o] = v;
+    }
+  }
+}
+
+cudaError_t launch_gemm_simt(const float* A, const float* Bm, float* D, const float* bias, const float* residual,
+                             int M, int N, int K, int batch, int64_t sa, int64_t sb, int64_t sd, int64_t ldb_n,
+                             int64_t ldb_k, float alpha, cudaStream_t s) {
+  if (M <= 0 || N <= 0 || batch <= 0) return cudaSuccess;
+  dim3 grid((N + 31) / 32, (M + 31) / 32, batch);
+  gemm_simt_kernel<<<grid, 256, 0, s>>>(A, Bm, D, bias, residual, M, N, K, sa, sb, sd, ldb_n, ldb_k, alpha);
+  return cudaGetLastError();
+}
+
+template <typename TI, typename TO>
+__global__ void cast_frames_kernel(const TI* x, int xTa, TO* y, int yTa, int T, int64_t fe, int64_t n) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = i % fe;
+    const int64_t f = i / fe;
+    const int64_t t = f % T, b = f / T;
+    y[(b * yTa + t) * fe + e] = from_f<TO>(to_f<TI>(x[(b * xTa + t) * fe + e]));
+  }
+}
+
+cudaError_t launch_cast_frames(const void* x, int x_f32, int x_T_alloc, void* y, int y_f32, int y_T_alloc, int B, int T,
+                               int64_t frame_elems, cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(B) * T * frame_elems;
+  if (n <= 0) return cudaSuccess;
+  const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 152 * 64));
+  const float* xf = static_cast<const float*>(x);
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  if (x_f32 && y_f32) cast_frames_kernel<<<blocks, 256, 0, s>>>(xf, x_T_alloc, static_cast<float*>(y), y_T_alloc, T, frame_elems, n);
+  else if (x_f32) cast_frames_kernel<<<blocks, 256, 0, s>>>(xf, x_T_alloc, static_cast<__nv_bfloat16*>(y), y_T_alloc, T, frame_elems, n);
+  else if (y_f32) cast_frames_kernel<<<blocks, 256, 0, s>>>(xb, x_T_alloc, static_cast<float*>(y), y_T_alloc, T, frame_elems, n);
+  else cast_frames_kernel<<<blocks, 256, 0, s>>>(xb, x_T_alloc, static_cast<__nv_bfloat16*>(y), y_T_alloc, T, frame_elems, n);
+  return cudaGetLastError();
+}
+
+// [batch, rows, cols] -> [batch, cols, ld] with ld = rows rounded up to 64 (zero padded)
+__global__ void transpose_kernel(const __nv_bfloat16* in, __nv_bfloat16* out, int rows, int cols, int ld) {
+  __shared__ __nv_bfloat16 tile[32][33];
+  const int bz = blockIdx.z;
+  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  const __nv_bfloat16* ib = in + static_cast<int64_t>(bz) * rows * cols;
+  __nv_bfloat16* ob = out + static_cast<int64_t>(bz) * cols * ld;
+  for (int k = threadIdx.y; k < 32; k += blockDim.y) {
+    const int r = r0 + k, c = c0 + threadIdx.x;
+    tile[k][threadIdx.x] = (r < rows && c < cols) ? ib[static_cast<int64_t>(r) * cols + c] : f2bf(0.f);
+  }
+  __syncthreads();
+  for (int k = threadIdx.y; k < 32; k += blockDim.y) {
+    const int c = c0 + k, r = r0 + threadIdx.x;
+    if (c < cols && r < ld) ob[static_cast<int64_t>(c) * ld + r] = tile[threadIdx.x][k];
+  }
+}
+
+cudaError_t launch_transpose_bf16(const void* in, void* out, int batch, int rows, int cols, cudaStream_t s) {
+  const int ld = (rows + 63) / 64 * 64;
+  dim3 grid((cols + 31) / 32, (ld + 31) / 32, batch);
+  transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(static_cast<const __nv_bfloat16*>(in), static_cast<__nv_bfloat16*>(out),
+                                                rows, cols, ld);
+  return cudaGetLastError();
+}
+
+// ============================================================================ weight packing
+// bf16 K-major [N_pad, 27 * C_in_pad]; row n' = sub * (C_out/S) + c holds PyTorch channel c * S + sub
+__global__ void pack_bf16_kernel(const float* w, int C_out, int C_in, int C_in_pad, int N_pad, int S,
+                                 __nv_bfloat16* out) {
+  const int64_t n = static_cast<int64_t>(N_pad) * 27 * C_in_pad;
+  const int Cd = C_out / S;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int ci = static_cast<int>(i % C_in_pad);
+    const int tap = static_cast<int>((i / C_in_pad) % 27);
+    const int np = static_cast<int>(i / (27LL * C_in_pad));
+    float v = 0.f;
+    if (np < C_out && ci < C_in) {
+      const int sub = np / Cd, c = np % Cd;
+      const int co = c * S + sub;
+      v = w[(static_cast<int64_t>(co) * C_in + ci) * 27 + tap];
+    }
+    out[i] = f2bf(v);
+  }
+}
+
+cudaError_t launch_pack_weights_bf16(const float* w, int C_out, int C_in, int C_in_pad, int N_pad, int S, void* out,
+                                     cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(N_pad) * 27 * C_in_pad;
+  const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 152 * 64));
+  pack_bf16_kernel<<<blocks, 256, 0, s>>>(w, C_out, C_in, C_in_pad, N_pad, S, static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+// fp32 [27, C_in, C_out] (PyTorch channel order)
+__global__ void pack_f32_kernel(const float* w, int C_out, int C_in, float* out) {
+  const int64_t n = 27LL * C_in * C_out;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int co = static_cast<int>(i % C_out);
+    const int ci = static_cast<int>((i / C_out) % C_in);
+    const int tap = static_cast<int>(i / (static_cast<int64_t>(C_out) * C_in));
+    out[i] = w[(static_cast<int64_t>(co) * C_in + ci) * 27 + tap];
+  }
+}
+
+cudaError_t launch_pack_weights_f32(const float* w, int C_out, int C_in, void* out, cudaStream_t s) {
+  const int64_t n = 27LL * C_in * C_out;
+  const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 152 * 64));
+  pack_f32_kernel<<<blocks, 256, 0, s>>>(w, C_out, C_in, static_cast<float*>(out));
+  return cudaGetLastError();
+}
+
+__global__ void to_bf16_kernel(const float* w, int64_t n, __nv_bfloat16* out) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    out[i] = f2bf(w[i]);
+}
+
+cudaError_t launch_pack_matrix_bf16(const float* w, int rows, int cols, void* out, cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(rows) * cols;
+  const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 152 * 64));
+  to_bf16_kernel<<<blocks, 256, 0, s>>>(w, n, static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+// ============================================================================ watchdog self-test
+__global__ void watchdog_kernel(uint32_t* fault, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, fault, limit_ns, 99);  // nothing ever arrives
+  __syncthreads();
+}
+
+cudaError_t launch_watchdog_test(uint64_t limit_ns, cudaStream_t s) {
+  watchdog_kernel<<<1, 32, 0, s>>>(fault_word(), limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace vae

@@ -1,0 +1,395 @@
+#!/usr/bin/env python
+"""Benchmark: bf16 decode of a 720p x 81-frame video latent through libvaedec on GB300.
+
+Metric: decoded Mframe-px/s = B * 81 * 704 * 1280 / decode time / 1e6 (whole job, all ranks).
+Default workload: the Wan-shaped decoder (latent [1, 48, 21, 44, 80] -> pixels [1, 3, 81, 704, 1280],
+stage channels 1024/1024/512/256, mid attention), random-init weights, seeded synthetic latent.
+
+One JSON line on rank 0 with the contract's keys plus:
+  roofline      the dominant kernel (tcgen05 causal conv) inside the timed decodes: algorithmic
+                FLOPs / CUDA-event time over all its launches, against the measured bf16 peak
+  kernels       the same per kernel class (conv, group norm stats/apply, attention GEMMs, ...)
+  ops           the op-level workloads: PatchGroupNorm+SiLU, causal conv 512->512, tile blend
+  cpu_baseline  the CPU oracle on a bounded spatial crop of the same decode, host cores
+N > 1 (torchrun): each rank decodes its own latent (independent videos, weak scaling), no
+collective on the data path; barriers and the max over ranks bracket the timed region.
+--impl reference times the CPU oracle (the reference arm of this build) on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from patch_tiled_causal_gb300 import synth  # noqa: E402
+
+FRAME_PX_720P_81 = 81 * 704 * 1280
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def _src_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "patch_tiled_causal_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(kernel)
+        if e and e.get("src_sha") == _src_sha(e["src_files"]):
+            return e
+    except Exception:
+        return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"vae_clocks_{os.getpid()}.csv")
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------- CPU oracle
+def oracle_sample(cfg, crop_hw, seed=0):
+    """Time the CPU oracle (Tier B, float32) decoding a spatial crop of the workload's latent."""
+    from oracle import decoder as odec
+    b, c, t, h, w = cfg.latent_shape
+    ch, cw = crop_hw
+    sub = dataclasses.replace(cfg, latent_shape=(b, c, t, ch, cw))
+    p = synth.draw_params(sub, seed)
+    z = synth.draw_latent(cfg, seed)[:, :, :, :ch, :cw].copy()
+    t0 = time.perf_counter()
+    y = odec.decode(sub, p, z, tier="B")
+    dt = time.perf_counter() - t0
+    frame_px = y.shape[0] * y.shape[2] * y.shape[3] * y.shape[4]
+    return frame_px, dt
+
+
+def run_reference(args, cfg):
+    crop = (2, 4)
+    for _ in range(args.warmup):
+        oracle_sample(cfg, crop)
+    times, fpx = [], 0
+    for _ in range(args.steps):
+        fpx, dt = oracle_sample(cfg, crop)
+        times.append(dt)
+    total = sum(times)
+    v = fpx * args.steps / total / 1e6
+    cores = os.cpu_count()
+    line = {"impl": "reference", "metric": "decoded Mframe-px/s at 720p x 81f (bf16 target; oracle fp32)",
+            "value": v, "unit": "Mframe-px/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{cfg.name}-shaped decoder, latent {list(cfg.latent_shape)} -> "
+                                   f"{list(cfg.output_shape())}, CPU oracle on a {crop[0]}x{crop[1]} latent crop "
+                                   "(all frames)", "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": v, "unit": "Mframe-px/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{cfg.name} decode, latent crop {crop[0]}x{crop[1]} of "
+                                       f"{cfg.latent_shape[3]}x{cfg.latent_shape[4]}, all {cfg.latent_shape[2]} "
+                                       "frames, Tier B float32"},
+            "e2e": {"value": v, "unit": "Mframe-px/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------- GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="wan", choices=["wan", "ltx"])
+    ap.add_argument("--patches", default="1x4", help="patch grid h x w of the timed decode")
+    ap.add_argument("--no-ops", action="store_true", help="skip the op-level workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    cfg = synth.WAN if args.workload == "wan" else synth.LTX
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, cfg)
+        return
+
+    import torch
+    from patch_tiled_causal_gb300 import build, vaedec
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    build.build()
+    vaedec.load()
+    peaks = _peaks()
+    stream = torch.cuda.current_stream()
+
+    nph, npw = (int(v) for v in args.patches.lower().split("x"))
+    params = synth.draw_params(cfg, 0)
+    latent_np = synth.draw_latent(cfg, seed=rank)
+    dec = vaedec.Decoder(cfg, params, vaedec.VAE_BF16)
+    del params
+    dec.reserve(cfg.latent_shape, nph, npw)
+    latent = torch.from_numpy(latent_np).cuda()
+    out = torch.empty(dec.output_shape(latent.shape), dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")  # > L2 (129 MB)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        dec.decode(latent, out, nph, npw)
+    code, msg = vaedec.last_error(dec.h)
+    if code:
+        raise RuntimeError(f"decode failed: {msg}")
+
+    # ---- timed region: device-resident inputs, L2 flushed between steps, events on the stream
+    sampler = ClockSampler(local)
+    sampler.start()
+    dec.profile(True)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        dec.decode(latent, out, nph, npw)
+        b.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    prof = dec.profile_read()
+    dec.profile(False)
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    t_local = sum(step_ms) / 1000.0
+    t = torch.tensor([t_local], device="cuda")
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    t_max = float(t.item())
+    code, msg = vaedec.last_error(dec.h)
+    if code:
+        raise RuntimeError(f"decode failed in the timed region: {msg}")
+    frame_px = out.shape[0] * out.shape[2] * out.shape[3] * out.shape[4]
+    value = frame_px * args.steps * world / t_max / 1e6
+    launches = sum(v["launches"] for v in prof.values()) // args.steps
+
+    # ---- end to end through the public API: pinned host latent in, pinned host pixels out
+    h_lat = torch.from_numpy(latent_np).pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d_lat = torch.empty_like(latent)
+    for _ in range(2):
+        d_lat.copy_(h_lat, non_blocking=True)
+        dec.decode(d_lat, out, nph, npw)
+        h_out.copy_(out, non_blocking=True)
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    for a, b in eev:
+        flush.zero_()
+        a.record(stream)
+        d_lat.copy_(h_lat, non_blocking=True)
+        dec.decode(d_lat, out, nph, npw)
+        h_out.copy_(out, non_blocking=True)
+        b.record(stream)
+    barrier()
+    e_local = sum(a.elapsed_time(b) for a, b in eev) / 1000.0
+    te = torch.tensor([e_local], device="cuda")
+    if dist is not None:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_value = frame_px * args.steps * world / float(te.item()) / 1e6
+
+    kernels = {}
+    for k, v in sorted(prof.items(), key=lambda kv: -kv[1]["ms"]):
+        e = {"launches_per_step": v["launches"] // args.steps, "ms_per_step": v["ms"] / args.steps,
+             "share": v["ms"] / max(sum(x["ms"] for x in prof.values()), 1e-9)}
+        if v["flops"]:
+            e["tflops"] = v["flops"] / (v["ms"] / 1e3) / 1e12
+            e["frac_of_bf16_sustained"] = e["tflops"] / peaks["bf16_tflops_sustained"]
+        if v["bytes"]:
+            e["gbs"] = v["bytes"] / (v["ms"] / 1e3) / 1e9
+            e["frac_of_hbm"] = e["gbs"] / peaks["hbm_gbs"]
+        kernels[k] = e
+    conv = prof.get("conv_tc", {"flops": 0.0, "ms": 1.0, "launches": 1})
+    conv_tf = conv["flops"] / (conv["ms"] / 1e3) / 1e12
+    tr = _traffic("conv_tc_decode")
+    roofline = {"bound": "tensor", "kernel": "conv_tc (tcgen05 implicit-GEMM causal conv), all launches of the decode",
+                "achieved": conv_tf, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": conv_tf / peaks["bf16_tflops_sustained"],
+                "peak_kind": f"bf16 dense, sustained, {'of measured' if peaks['source'] == 'measured' else 'of fallback'}",
+                "traffic": tr["bytes_per_launch"] if tr else None,
+                "flops_per_launch": conv["flops"] / conv["launches"],
+                "ms_per_launch": conv["ms"] / conv["launches"]}
+    if tr:
+        roofline["traffic_note"] = tr.get("note", "")
+
+    ops = None
+    if not args.no_ops and rank == 0:
+        ops = run_ops(args, torch, vaedec, peaks, flush)
+
+    cpu = None
+    if not args.no_cpu and rank == 0 and world == 1:
+        fpx, dt = oracle_sample(cfg, (4, 6))
+        cpu = {"value": fpx / dt / 1e6, "unit": "Mframe-px/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{cfg.name} decode of a 4x6 latent crop (of {cfg.latent_shape[3]}x{cfg.latent_shape[4]}), "
+                         f"all {cfg.latent_shape[2]} latent frames, Tier B float32 (numpy BLAS), {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": "decoded Mframe-px/s at 720p x 81f bf16", "value": value, "unit": "Mframe-px/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * t_max / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) latent, N(0,1/fan_in) random-init weights)",
+            "config": {"workload": f"{cfg.name}-shaped causal VAE decoder, latent {list(cfg.latent_shape)} -> "
+                                   f"pixels {list(out.shape)}, {nph}x{npw} spatial patches",
+                       "global_batch": out.shape[0] * world, "frames": out.shape[2],
+                       "resolution": f"{out.shape[3]}x{out.shape[4]}", "patches": f"{nph}x{npw}",
+                       "parallelism": f"replicas x{world} (independent videos)", "l2": "flushed between steps"},
+            "e2e": {"value": e2e_value, "unit": "Mframe-px/s", "h2d_bytes_per_step": latent.numel() * 4,
+                    "d2h_bytes_per_step": out.numel() * out.element_size()},
+            "gpu_launches": launches,
+            "roofline": roofline,
+            "kernels": kernels,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "ops": ops,
+            "peaks": peaks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def _time(torch, fn, steps, flush):
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    for a, b in evs:
+        flush.zero_()
+        a.record(s)
+        fn()
+        b.record(s)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / steps
+
+
+def run_ops(args, torch, vd, peaks, flush):
+    res = {}
+    B, C, T, H, W = 1, 512, 21, 88, 160
+    eh, ew = vd.patch_edges(H, 1), vd.patch_edges(W, 4)
+    # (a) PatchGroupNorm + SiLU, 4 width patches
+    x = torch.from_numpy(synth.draw_normal((B, T, H, W, C), 100)).to("cuda", torch.bfloat16)
+    y = torch.empty_like(x)
+    g = torch.ones(C, device="cuda")
+    bt = torch.zeros(C, device="cuda")
+    gd = vd.gn_desc(B, T, H, W, C, 32, eh, ew)
+    ws = vd.gn_workspace(gd, "cuda")
+    ms = _time(torch, lambda: vd.patch_groupnorm_silu(x, g, bt, y, ws, gd), args.steps, flush)
+    nbytes = 3 * x.numel() * 2
+    res["groupnorm_silu"] = {"workload": "[1,512,21,88,160] bf16, 32 groups, 4 width patches", "ms": ms,
+                             "bytes": nbytes, "gbs": nbytes / ms / 1e6, "frac_of_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"],
+                             "bound": "hbm"}
+    # (b) causal conv 3x3x3 512 -> 512, 4 width patches
+    w = torch.from_numpy(synth.conv_weight(C, C, 101)).cuda()
+    cd = vd.conv_desc(B, T, H, W, C, C, eh, ew)
+    wp = vd.conv3d_pack_weights(w, cd)
+    yc = torch.empty_like(x)
+    ms = _time(torch, lambda: vd.conv3d_causal(x, wp, None, None, yc, cd), args.steps, flush)
+    fl = 2.0 * 27 * C * C * T * H * W
+    tr = _traffic("conv_tc_c2b")
+    res["conv3d_causal"] = {"workload": "3x3x3 512->512 on [1,512,21,88,160] bf16, 4 width patches", "ms": ms,
+                            "tflops": fl / ms / 1e9, "frac_of_bf16": fl / ms / 1e9 / peaks["bf16_tflops"],
+                            "bound": "tensor", "traffic": tr["bytes_per_launch"] if tr else None}
+    del x, y, yc, wp
+    # (c) tile blend: 28 tiles of 256^2 with 64 px overlap -> [1, 3, 81, 704, 1280]
+    meta = vd.tile_plan((81, 704, 1280), (81, 256, 256), (0, 64, 64), 1, 1, causal_t=False)
+    tiles = [torch.from_numpy(synth.draw_normal((1, 3, m["pix"][1], m["pix"][3], m["pix"][5]), 200 + i)).to(
+        "cuda", torch.bfloat16) for i, m in enumerate(meta)]
+    outb = torch.empty((1, 3, 81, 704, 1280), dtype=torch.bfloat16, device="cuda")
+    ms = _time(torch, lambda: vd.tile_blend(tiles, meta, outb), args.steps, flush)
+    nbytes = sum(t.numel() for t in tiles) * 2 + outb.numel() * 2
+    res["tile_blend"] = {"workload": f"{len(meta)} tiles of up to [1,3,81,256,256] bf16, 64 px overlap -> "
+                                     "[1,3,81,704,1280]", "ms": ms, "bytes": nbytes, "gbs": nbytes / ms / 1e6,
+                         "frac_of_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"], "bound": "hbm"}
+    return res
+
+
+if __name__ == "__main__":
+    main()

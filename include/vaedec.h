@@ -150,6 +150,26 @@ vae_status_t vae_decode_chunk(vae_decoder_t* dec, const void* latent_chunk, cons
 vae_status_t vae_decode_tiled(vae_decoder_t* dec, const void* latent, const int64_t latent_shape[5],
                               void* out, const int tile_thw[3], const int ovl_thw[3], void* stream);
 
+/* Per-kernel timing of the decoder's launches (profiling aid).  While enabled, every kernel the
+ * handle enqueues is bracketed by CUDA events on its stream and tagged with its kernel class and its
+ * algorithmic work (conv/GEMM FLOPs = 2 * MACs of the real channel counts; norm/blend bytes = the
+ * reads and writes the operation needs).  Enabling creates events per launch: do not enable it
+ * inside a CUDA-graph capture. */
+typedef struct {
+  char name[32];   /* kernel class: conv_tc, conv_simt, gn_stats, gn_apply, gemm_tc, gemm_simt, softmax,
+                      transpose, cast, copy, latent, blend */
+  int launches;    /* launches since the last read */
+  double ms;       /* summed device time of those launches */
+  double flops;    /* summed algorithmic FLOPs */
+  double bytes;    /* summed algorithmic DRAM bytes */
+} vae_prof_t;
+
+vae_status_t vae_decoder_profile(vae_decoder_t* dec, int enable);
+
+/* Synchronises the device, folds the recorded launches into per-class totals (at most *n entries;
+ * *n returns the count) and starts a new recording. */
+vae_status_t vae_decoder_profile_read(vae_decoder_t* dec, vae_prof_t* out, int* n);
+
 /* Last failure of `dec` (or of the op-level calls when dec is NULL).  Synchronises the device and
  * folds in the device fault word (VAE_ERR_TIMEOUT / VAE_ERR_RANGE), then clears it. */
 vae_status_t vae_last_error(vae_decoder_t* dec, vae_error_info_t* info);

@@ -160,9 +160,44 @@ struct vae_decoder {
   void* tiles = nullptr;
   size_t tiles_bytes = 0;
   vae_error_info_t err{};
+  // profiling: events around every launch while enabled
+  bool prof = false;
+  struct Rec {
+    int kind;
+    cudaEvent_t a, b;
+    double flops, bytes;
+  };
+  std::vector<Rec> recs;
 };
 
 namespace {
+
+enum Kind { K_CONV_TC, K_CONV_SIMT, K_GN_STATS, K_GN_APPLY, K_GEMM_TC, K_GEMM_SIMT, K_SOFTMAX, K_TRANSPOSE, K_CAST,
+            K_COPY, K_LATENT, K_BLEND, K_COUNT };
+const char* kKindNames[K_COUNT] = {"conv_tc", "conv_simt", "gn_stats", "gn_apply", "gemm_tc", "gemm_simt",
+                                   "softmax", "transpose", "cast", "copy", "latent", "blend"};
+
+// Brackets one launch with events when the handle is profiling.
+struct Prof {
+  vae_decoder* d;
+  cudaStream_t s;
+  int kind;
+  double fl, by;
+  cudaEvent_t a = nullptr;
+  Prof(vae_decoder* dd, cudaStream_t ss, int k, double flops, double bytes) : d(dd), s(ss), kind(k), fl(flops), by(bytes) {
+    if (d && d->prof && cudaEventCreate(&a) == cudaSuccess) cudaEventRecord(a, s);
+  }
+  ~Prof() {
+    if (!a) return;
+    cudaEvent_t b = nullptr;
+    if (cudaEventCreate(&b) != cudaSuccess) {
+      cudaEventDestroy(a);
+      return;
+    }
+    cudaEventRecord(b, s);
+    d->recs.push_back({kind, a, b, fl, by});
+  }
+};
 
 #define ERRP (&d->err)
 
@@ -528,7 +563,11 @@ vae_status_t run_conv(Ctx& x, ConvL& c, const Level& L, void* y, int y_f32, int 
   const int B = x.p->B, T = L.T, Ta = T + 2;
   const int64_t frame_bytes = static_cast<int64_t>(L.H) * L.W * c.C_in_pad * act_bytes(d);
   const bool use_cache = x.chunked && !x.p->first;
-  if (use_cache) CK(launch_copy_frames(c.cache, 2, 0, x.b.hin, Ta, 0, 2, B, frame_bytes, x.s));
+  if (use_cache) {
+    Prof pr(d, x.s, K_COPY, 0, 4.0 * B * frame_bytes);
+    CK(launch_copy_frames(c.cache, 2, 0, x.b.hin, Ta, 0, 2, B, frame_bytes, x.s));
+  }
+  const double conv_flops = 2.0 * 27 * c.C_in * c.C_out * static_cast<double>(B) * T * L.H * L.W;
   const char* xin = x.b.hin + (use_cache ? 0 : 2 * frame_bytes);
   const int cache_frames = use_cache ? 2 : 0;
   if (c.tc) {
@@ -541,6 +580,7 @@ vae_status_t run_conv(Ctx& x, ConvL& c, const Level& L, void* y, int y_f32, int 
     a.residual = residual; a.res_f32 = res_f32; a.res_T_alloc = T;
     a.y = y; a.out_f32 = y_f32; a.out_ncthw = out_ncthw; a.y_T_alloc = y_T_alloc;
     a.d2s_t = c.st; a.d2s_h = c.sh; a.d2s_w = c.sw; a.drop_first = drop_first;
+    Prof pr(d, x.s, K_CONV_TC, conv_flops, 0);
     CK(launch_conv_tc(a, x.s));
   } else {
     ConvSimtArgs a{};
@@ -551,9 +591,11 @@ vae_status_t run_conv(Ctx& x, ConvL& c, const Level& L, void* y, int y_f32, int 
     a.y = y; a.out_f32 = y_f32; a.out_ncthw = out_ncthw; a.y_T_alloc = y_T_alloc;
     a.d2s_t = c.st; a.d2s_h = c.sh; a.d2s_w = c.sw; a.drop_first = drop_first;
     a.nph = x.p->nph; a.npw = x.p->npw; a.ph_edges = L.ph; a.pw_edges = L.pw;
+    Prof pr(d, x.s, K_CONV_SIMT, conv_flops, 0);
     CK(launch_conv_simt(a, x.s));
   }
   if (x.chunked) {
+    Prof pr(d, x.s, K_COPY, 0, 4.0 * B * frame_bytes);
     // keep the last 2 frames of this conv's (padded) input sequence for the next chunk
     if (use_cache || T >= 2) {
       const int last = 2 + T;  // frames [last-2, last) of hin are the newest two
@@ -578,8 +620,15 @@ vae_status_t run_gn(Ctx& x, const NormL& n, const Level& L, const void* src, int
   g.y = x.b.hin + 2 * frame_bytes; g.y_f32 = d->f32; g.y_T_alloc = L.T + 2;
   g.gamma = n.gamma; g.beta = n.beta;
   g.partials = x.b.gn;
-  CK(launch_gn_stats(g, x.s));
-  CK(launch_gn_apply(g, x.s));
+  const double elems = static_cast<double>(g.B) * L.T * L.H * L.W * L.C;
+  {
+    Prof pr(d, x.s, K_GN_STATS, 0, elems * (src_f32 ? 4 : 2));
+    CK(launch_gn_stats(g, x.s));
+  }
+  {
+    Prof pr(d, x.s, K_GN_APPLY, 0, elems * ((src_f32 ? 4 : 2) + act_bytes(d)));
+    CK(launch_gn_apply(g, x.s));
+  }
   return VAE_OK;
 }
 
@@ -608,8 +657,15 @@ vae_status_t run_attention(Ctx& x, const Level& L) {
     g.y = x.b.o; g.y_f32 = d->f32; g.y_T_alloc = L.T;
     g.gamma = d->attn.n.gamma; g.beta = d->attn.n.beta;
     g.partials = x.b.gn;
-    CK(launch_gn_stats(g, x.s));
-    CK(launch_gn_apply(g, x.s));
+    const double elems = static_cast<double>(g.B) * L.T * L.H * L.W * C;
+    {
+      Prof pr(d, x.s, K_GN_STATS, 0, elems * (rf ? 4 : 2));
+      CK(launch_gn_stats(g, x.s));
+    }
+    {
+      Prof pr(d, x.s, K_GN_APPLY, 0, elems * ((rf ? 4 : 2) + act_bytes(d)));
+      CK(launch_gn_apply(g, x.s));
+    }
   }
   const float scale = 1.0f / std::sqrt(static_cast<float>(C));
   const int64_t M = static_cast<int64_t>(F) * tok;
@@ -642,6 +698,7 @@ vae_status_t run_attention(Ctx& x, const Level& L) {
     a.x = A; a.w = Bm; a.N_real = N; a.N_pad = round_up(N, 16); a.bias = bias;
     a.residual = res; a.res_f32 = r_f32; a.y = D; a.out_f32 = out_f32; a.ldd = ldd;
     a.d2s_t = a.d2s_h = a.d2s_w = 1;
+    Prof pr(d, x.s, K_GEMM_TC, 2.0 * Mm * N * K * batch, 0);
     CK(launch_conv_tc(a, x.s));
     return VAE_OK;
   };
@@ -650,11 +707,17 @@ vae_status_t run_attention(Ctx& x, const Level& L) {
   for (int i = 0; i < 3 && !s; ++i)
     s = gemm(x.b.o, d->attn.w[i], qkv[i], d->attn.b[i], static_cast<int>(M), C, C, 1, 0, 0, 0, 0, 1.0f, 0, nullptr, 0);
   if (s) return s;
-  CK(launch_transpose_bf16(x.b.v, x.b.vt, F, tok, C, x.s));  // V^T [F, C, tokp], zero padded
+  {
+    Prof pr(d, x.s, K_TRANSPOSE, 0, 2.0 * F * tok * C * 2);
+    CK(launch_transpose_bf16(x.b.v, x.b.vt, F, tok, C, x.s));  // V^T [F, C, tokp], zero padded
+  }
   s = gemm(x.b.q, x.b.k, x.b.s, nullptr, tok, tok, C, F, static_cast<int64_t>(tok) * C, static_cast<int64_t>(tok) * C,
            static_cast<int64_t>(tok) * tok, 0, scale, 1, nullptr, 0);
   if (s) return s;
-  CK(launch_softmax_rows(reinterpret_cast<const float*>(x.b.s), x.b.p, 0, F * tok, tok, tokp, x.s));
+  {
+    Prof pr(d, x.s, K_SOFTMAX, 0, static_cast<double>(F) * tok * (tok * 4.0 + tokp * 2.0));
+    CK(launch_softmax_rows(reinterpret_cast<const float*>(x.b.s), x.b.p, 0, F * tok, tok, tokp, x.s));
+  }
   s = gemm(x.b.p, x.b.vt, x.b.o, nullptr, tok, C, tokp, F, static_cast<int64_t>(tok) * tokp,
            static_cast<int64_t>(C) * tokp, static_cast<int64_t>(tok) * C, 0, 1.0f, 0, nullptr, 0);
   if (s) return s;
@@ -674,8 +737,11 @@ vae_status_t run_decode(vae_decoder* d, const Plan& p, const float* latent, cons
     const Level& L0 = p.lv[0];
     const int Cp = d->conv_in.C_in_pad;
     const int64_t fb = static_cast<int64_t>(p.h) * p.w * Cp * act_bytes(d);
-    CK(launch_latent_to_cl(latent, p.B, c.latent_c, lat_full[0], lat_full[1], lat_full[2], lat_box[0], p.Tlat,
-                           lat_box[1], p.h, lat_box[2], p.w, Cp, x.b.hin + 2 * fb, d->f32, p.Tlat + 2, s));
+    {
+      Prof pr(d, s, K_LATENT, 0, static_cast<double>(p.B) * p.Tlat * p.h * p.w * (c.latent_c * 4.0 + Cp * act_bytes(d)));
+      CK(launch_latent_to_cl(latent, p.B, c.latent_c, lat_full[0], lat_full[1], lat_full[2], lat_box[0], p.Tlat,
+                             lat_box[1], p.h, lat_box[2], p.w, Cp, x.b.hin + 2 * fb, d->f32, p.Tlat + 2, s));
+    }
     st = run_conv(x, d->conv_in, L0, x.b.x, rf, L0.T, 0, nullptr, 0, 0);
     if (st) return st;
   }
@@ -696,7 +762,10 @@ vae_status_t run_decode(vae_decoder* d, const Plan& p, const float* latent, cons
     if (i + 1 < c.n_stages) {
       // conv input = the residual stream in the conv dtype, behind 2 cache frames
       const int64_t fe = static_cast<int64_t>(L.H) * L.W * L.C;
-      CK(launch_cast_frames(x.b.x, rf, L.T, x.b.hin + 2 * fe * act_bytes(d), d->f32, L.T + 2, p.B, L.T, fe, s));
+      {
+        Prof pr(d, s, K_CAST, 0, static_cast<double>(p.B) * L.T * fe * (res_bytes(d) + act_bytes(d)));
+        CK(launch_cast_frames(x.b.x, rf, L.T, x.b.hin + 2 * fe * act_bytes(d), d->f32, L.T + 2, p.B, L.T, fe, s));
+      }
       st = run_conv(x, d->ups[i], L, x.b.x, rf, p.lv[i + 1].T, 0, nullptr, 0, p.first ? 1 : 0);
       if (st) return st;
     }
@@ -929,7 +998,46 @@ extern "C" vae_status_t vae_decode_tiled(vae_decoder_t* d, const void* latent, c
   bd.B = B; bd.C = c.out_c;
   bd.T = st * (lat[0] - 1) + 1; bd.H = ss * lat[1]; bd.W = ss * lat[2];
   bd.tile_dtype = bd.out_dtype = d->f32 ? VAE_FP32 : VAE_BF16;
-  CK(launch_blend(ptrs.data(), tl.data(), n, out, bd, strm));
+  {
+    double by = static_cast<double>(B) * c.out_c * bd.T * bd.H * bd.W * ob;
+    for (int i = 0; i < n; ++i) by += static_cast<double>(B) * c.out_c * tl[i].pix[1] * tl[i].pix[3] * tl[i].pix[5] * ob;
+    Prof pr(d, strm, K_BLEND, 0, by);
+    CK(launch_blend(ptrs.data(), tl.data(), n, out, bd, strm));
+  }
+  return VAE_OK;
+}
+
+extern "C" vae_status_t vae_decoder_profile(vae_decoder_t* d, int enable) {
+  if (!d) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null decoder");
+  d->prof = enable != 0;
+  return VAE_OK;
+}
+
+extern "C" vae_status_t vae_decoder_profile_read(vae_decoder_t* d, vae_prof_t* out, int* n) {
+  if (!d || !out || !n) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null argument");
+  CK(cudaDeviceSynchronize());
+  vae_prof_t acc[K_COUNT];
+  memset(acc, 0, sizeof(acc));
+  for (auto& r : d->recs) {
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, r.a, r.b);
+    vae_prof_t& e = acc[r.kind];
+    e.launches += 1;
+    e.ms += ms;
+    e.flops += r.flops;
+    e.bytes += r.bytes;
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  d->recs.clear();
+  int k = 0;
+  for (int i = 0; i < K_COUNT && k < *n; ++i) {
+    if (!acc[i].launches) continue;
+    out[k] = acc[i];
+    snprintf(out[k].name, sizeof(out[k].name), "%s", kKindNames[i]);
+    ++k;
+  }
+  *n = k;
   return VAE_OK;
 }
 #undef ERRP

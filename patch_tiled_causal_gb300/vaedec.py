@@ -70,8 +70,15 @@ class VaeBlendDesc(C.Structure):
                 ("tile_dtype", C.c_int), ("out_dtype", C.c_int)]
 
 
+class VaeProf(C.Structure):
+    _fields_ = [("name", C.c_char * 32), ("launches", C.c_int), ("ms", C.c_double), ("flops", C.c_double),
+                ("bytes", C.c_double)]
+
+
 _P = C.c_void_p
 _SIGS = {
+    "vae_decoder_profile": (C.c_int, [_P, C.c_int]),
+    "vae_decoder_profile_read": (C.c_int, [_P, C.POINTER(VaeProf), C.POINTER(C.c_int)]),
     "vae_decoder_n_weights": (C.c_int, [C.POINTER(VaeConfig), C.POINTER(C.c_int)]),
     "vae_decoder_create": (C.c_int, [C.POINTER(VaeConfig), C.POINTER(_P), C.c_int, C.POINTER(_P)]),
     "vae_decoder_destroy": (None, [_P]),
@@ -358,6 +365,16 @@ class Decoder:
     def reserve(self, latent_shape, n_patch_h=1, n_patch_w=1):
         shp = (C.c_int64 * 5)(*latent_shape)
         _check(load().vae_decoder_reserve(self.h, shp, n_patch_h, n_patch_w), "vae_decoder_reserve", self.h)
+
+    def profile(self, enable: bool):
+        _check(load().vae_decoder_profile(self.h, int(enable)), "vae_decoder_profile", self.h)
+
+    def profile_read(self) -> Dict[str, dict]:
+        arr = (VaeProf * 32)()
+        n = C.c_int(32)
+        _check(load().vae_decoder_profile_read(self.h, arr, C.byref(n)), "vae_decoder_profile_read", self.h)
+        return {arr[i].name.decode(): {"launches": arr[i].launches, "ms": arr[i].ms, "flops": arr[i].flops,
+                                        "bytes": arr[i].bytes} for i in range(n.value)}
 
     def decode(self, latent, out=None, n_patch_h=1, n_patch_w=1, stream=None):
         torch = _torch()

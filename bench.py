@@ -122,14 +122,15 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------- CPU oracle
-def oracle_sample(cfg, crop_hw, seed=0):
-    """Time the CPU oracle (Tier B, float32) decoding a spatial crop of the workload's latent."""
+def oracle_sample(cfg, crop_thw, seed=0):
+    """Time the CPU oracle (Tier B, float32) decoding a crop (first frames, top-left latent pixels)
+    of the workload's latent; returns (decoded frame-px, seconds)."""
     from oracle import decoder as odec
     b, c, t, h, w = cfg.latent_shape
-    ch, cw = crop_hw
-    sub = dataclasses.replace(cfg, latent_shape=(b, c, t, ch, cw))
+    ct, ch, cw = crop_thw
+    sub = dataclasses.replace(cfg, latent_shape=(b, c, ct, ch, cw))
     p = synth.draw_params(sub, seed)
-    z = synth.draw_latent(cfg, seed)[:, :, :, :ch, :cw].copy()
+    z = synth.draw_latent(cfg, seed)[:, :, :ct, :ch, :cw].copy()
     t0 = time.perf_counter()
     y = odec.decode(sub, p, z, tier="B")
     dt = time.perf_counter() - t0
@@ -137,8 +138,17 @@ def oracle_sample(cfg, crop_hw, seed=0):
     return frame_px, dt
 
 
+REF_CROP = (5, 1, 2)   # latent frames, rows, cols of the reference arm's per-step sample
+CPU_CROP = (5, 2, 2)   # the GPU arm's cpu_baseline sample
+
+
+def _crop_text(cfg, crop):
+    return (f"{cfg.name} decode of the first {crop[0]} latent frames x a {crop[1]}x{crop[2]} latent crop "
+            f"(of {cfg.latent_shape[2]} x {cfg.latent_shape[3]}x{cfg.latent_shape[4]}), Tier B float32 (numpy BLAS)")
+
+
 def run_reference(args, cfg):
-    crop = (2, 4)
+    crop = REF_CROP
     for _ in range(args.warmup):
         oracle_sample(cfg, crop)
     times, fpx = [], 0
@@ -153,12 +163,10 @@ def run_reference(args, cfg):
             "ms_per_step": 1000 * total / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": f"{cfg.name}-shaped decoder, latent {list(cfg.latent_shape)} -> "
-                                   f"{list(cfg.output_shape())}, CPU oracle on a {crop[0]}x{crop[1]} latent crop "
-                                   "(all frames)", "l2": "n/a (CPU)"},
+                                   f"{list(cfg.output_shape())}; each step the CPU oracle on a bounded sample",
+                       "l2": "n/a (CPU)"},
             "cpu_baseline": {"value": v, "unit": "Mframe-px/s", "cores": cores, "kind": "oracle",
-                             "sample": f"{cfg.name} decode, latent crop {crop[0]}x{crop[1]} of "
-                                       f"{cfg.latent_shape[3]}x{cfg.latent_shape[4]}, all {cfg.latent_shape[2]} "
-                                       "frames, Tier B float32"},
+                             "sample": _crop_text(cfg, crop)},
             "e2e": {"value": v, "unit": "Mframe-px/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -174,6 +182,8 @@ def main():
     ap.add_argument("--patches", default="1x4", help="patch grid h x w of the timed decode")
     ap.add_argument("--no-ops", action="store_true", help="skip the op-level workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--only", default="all", choices=["all", "decode", "ops"],
+                    help="run only the decode or only the op workloads (profiling runs)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     cfg = synth.WAN if args.workload == "wan" else synth.LTX
@@ -199,6 +209,13 @@ def main():
     vaedec.load()
     peaks = _peaks()
     stream = torch.cuda.current_stream()
+
+    if args.only == "ops":
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        print(json.dumps({"ops": run_ops(args, torch, vaedec, peaks, flush), "peaks": peaks}), flush=True)
+        return
+    if args.only == "decode":
+        args.no_ops = args.no_cpu = True
 
     nph, npw = (int(v) for v in args.patches.lower().split("x"))
     params = synth.draw_params(cfg, 0)
@@ -303,10 +320,9 @@ def main():
 
     cpu = None
     if not args.no_cpu and rank == 0 and world == 1:
-        fpx, dt = oracle_sample(cfg, (4, 6))
+        fpx, dt = oracle_sample(cfg, CPU_CROP)
         cpu = {"value": fpx / dt / 1e6, "unit": "Mframe-px/s", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"{cfg.name} decode of a 4x6 latent crop (of {cfg.latent_shape[3]}x{cfg.latent_shape[4]}), "
-                         f"all {cfg.latent_shape[2]} latent frames, Tier B float32 (numpy BLAS), {dt:.1f} s"}
+               "sample": _crop_text(cfg, CPU_CROP) + f", {fpx} frame-px in {dt:.1f} s"}
 
     if rank == 0:
         line = {

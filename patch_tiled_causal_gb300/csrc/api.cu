@@ -277,7 +277,7 @@ vae_status_t check_config(const vae_config_t* c, vae_error_info_t* e) {
     const int C = c->stage_c[i];
     if (C <= 0 || C % c->gn_groups || c->n_res[i] < 0) return set_err(e, VAE_ERR_INVALID_ARG, 0, 0, "stage %d channels", i);
     const int cpg = C / c->gn_groups;
-    if (C % 8 || C > 8192 || !(cpg % 8 == 0 || 8 % cpg == 0))
+    if (C % 8 || C > 6144 || !(cpg % 8 == 0 || 8 % cpg == 0))
       return set_err(e, VAE_ERR_UNSUPPORTED, 0, 0, "stage %d: %d channels / %d groups not supported", i, C, c->gn_groups);
     if (i + 1 < c->n_stages && (c->up_t[i] < 1 || c->up_t[i] > 2 || c->up_h[i] < 1 || c->up_w[i] < 1 || c->up_h[i] != c->up_w[i]))
       return set_err(e, VAE_ERR_UNSUPPORTED, 0, 0, "up-sampler %d factors", i);
@@ -443,8 +443,8 @@ vae_status_t make_plan(vae_decoder* d, int B, int Tlat, int h, int w, int nph, i
     const size_t px = static_cast<size_t>(B) * L.H * L.W;
     p.x_bytes = std::max(p.x_bytes, px * L.T * L.C * rb);
     p.hin_bytes = std::max(p.hin_bytes, px * (L.T + 2) * L.C * ab);
-    p.c1_bytes = std::max(p.c1_bytes, px * L.T * L.C * cb);
-    p.gn_bytes = std::max(p.gn_bytes, gn_partials_bytes(nph, npw, B, L.T, c.gn_groups));
+    p.c1_bytes = std::max(p.c1_bytes, px * std::max<size_t>(static_cast<size_t>(L.T) * cb, (L.T + 2ull) * ab) * L.C);
+    p.gn_bytes = std::max(p.gn_bytes, gn_workspace_bytes(nph, npw, B, L.T, c.gn_groups, L.C));
   }
   const int Clat = d->conv_in.C_in_pad;
   p.lat_bytes = static_cast<size_t>(B) * (Tlat + 2) * h * w * Clat * ab;
@@ -553,22 +553,39 @@ struct Ctx {
   const Plan* p;
   Bufs b;
   cudaStream_t s;
-  bool chunked;  // keep per-conv caches
+  bool chunked;                      // keep per-conv caches
+  const void* stats_src = nullptr;   // tensor whose group-norm partial sums the last conv produced
 };
 
-// Run conv `c` at level L. x = the conv-input buffer hin (bf16 / fp32 act, B x (2+T) frames, frame 0..1 cache).
-vae_status_t run_conv(Ctx& x, ConvL& c, const Level& L, void* y, int y_f32, int y_T_alloc, int out_ncthw,
-                      const void* residual, int res_f32, int drop_first) {
+// Where a conv writes and what its epilogue fuses.
+struct ConvOut {
+  void* y = nullptr;
+  int y_f32 = 0, y_T_alloc = 0, out_ncthw = 0;
+  const void* residual = nullptr;
+  int res_f32 = 0;
+  int drop_first = 0;
+  const Level* stats_level = nullptr;  // fuse group-norm partial sums of y at this level (nullptr = no)
+  void* y2 = nullptr;                  // bf16 copy of y behind 2 cache frames (next conv's operand)
+};
+
+// Run conv `c` at level L.  `in` is its input buffer (conv operand dtype, B x (2+T) frames, frames 0..1
+// the temporal cache).
+vae_status_t run_conv(Ctx& x, ConvL& c, const Level& L, char* in, const ConvOut& o) {
   vae_decoder* d = x.d;
   const int B = x.p->B, T = L.T, Ta = T + 2;
   const int64_t frame_bytes = static_cast<int64_t>(L.H) * L.W * c.C_in_pad * act_bytes(d);
   const bool use_cache = x.chunked && !x.p->first;
+  x.stats_src = nullptr;
+  void* y = o.y;
+  const int y_f32 = o.y_f32, y_T_alloc = o.y_T_alloc, out_ncthw = o.out_ncthw, res_f32 = o.res_f32;
+  const void* residual = o.residual;
+  const int drop_first = o.drop_first;
   if (use_cache) {
     Prof pr(d, x.s, K_COPY, 0, 4.0 * B * frame_bytes);
-    CK(launch_copy_frames(c.cache, 2, 0, x.b.hin, Ta, 0, 2, B, frame_bytes, x.s));
+    CK(launch_copy_frames(c.cache, 2, 0, in, Ta, 0, 2, B, frame_bytes, x.s));
   }
   const double conv_flops = 2.0 * 27 * c.C_in * c.C_out * static_cast<double>(B) * T * L.H * L.W;
-  const char* xin = x.b.hin + (use_cache ? 0 : 2 * frame_bytes);
+  const char* xin = in + (use_cache ? 0 : 2 * frame_bytes);
   const int cache_frames = use_cache ? 2 : 0;
   if (c.tc) {
     ConvTcArgs a{};
@@ -580,8 +597,26 @@ vae_status_t run_conv(Ctx& x, ConvL& c, const Level& L, void* y, int y_f32, int 
     a.residual = residual; a.res_f32 = res_f32; a.res_T_alloc = T;
     a.y = y; a.out_f32 = y_f32; a.out_ncthw = out_ncthw; a.y_T_alloc = y_T_alloc;
     a.d2s_t = c.st; a.d2s_h = c.sh; a.d2s_w = c.sw; a.drop_first = drop_first;
-    Prof pr(d, x.s, K_CONV_TC, conv_flops, 0);
-    CK(launch_conv_tc(a, x.s));
+    const int Cd = c.C_out / (c.st * c.sh * c.sw);
+    const int G = d->cfg.gn_groups;
+    const int cpg = Cd % G == 0 ? Cd / G : 0;
+    const bool fuse = o.stats_level && !out_ncthw && Cd % 32 == 0 && cpg > 0 &&
+                      (cpg < 32 ? 32 % cpg == 0 : cpg % 32 == 0);
+    if (fuse) {
+      CK(cudaMemsetAsync(x.b.gn, 0, gn_partials_bytes(x.p->nph, x.p->npw, B, o.stats_level->T, G), x.s));
+      a.gn_partials = x.b.gn;
+      a.gn_groups = G;
+    }
+    if (o.y2) {
+      const int64_t f2 = static_cast<int64_t>(L.H) * c.sh * L.W * c.sw * Cd * 2;
+      a.y2 = static_cast<char*>(o.y2) + 2 * f2;
+      a.y2_T_alloc = (o.stats_level ? o.stats_level->T : T) + 2;
+    }
+    {
+      Prof pr(d, x.s, K_CONV_TC, conv_flops, 0);
+      CK(launch_conv_tc(a, x.s));
+    }
+    if (fuse) x.stats_src = y;
   } else {
     ConvSimtArgs a{};
     a.B = B; a.T = T; a.H = L.H; a.W = L.W; a.C_in = c.C_in; a.C_out = c.C_out;
@@ -598,11 +633,11 @@ vae_status_t run_conv(Ctx& x, ConvL& c, const Level& L, void* y, int y_f32, int 
     Prof pr(d, x.s, K_COPY, 0, 4.0 * B * frame_bytes);
     // keep the last 2 frames of this conv's (padded) input sequence for the next chunk
     if (use_cache || T >= 2) {
-      const int last = 2 + T;  // frames [last-2, last) of hin are the newest two
-      CK(launch_copy_frames(x.b.hin, Ta, last - 2, c.cache, 2, 0, 2, B, frame_bytes, x.s));
+      const int last = 2 + T;  // frames [last-2, last) of the input are the newest two
+      CK(launch_copy_frames(in, Ta, last - 2, c.cache, 2, 0, 2, B, frame_bytes, x.s));
     } else {  // first chunk of one frame: the padded sequence ends x0, x0
-      CK(launch_copy_frames(x.b.hin, Ta, 2, c.cache, 2, 0, 1, B, frame_bytes, x.s));
-      CK(launch_copy_frames(x.b.hin, Ta, 2, c.cache, 2, 1, 1, B, frame_bytes, x.s));
+      CK(launch_copy_frames(in, Ta, 2, c.cache, 2, 0, 1, B, frame_bytes, x.s));
+      CK(launch_copy_frames(in, Ta, 2, c.cache, 2, 1, 1, B, frame_bytes, x.s));
     }
   }
   return VAE_OK;
@@ -621,7 +656,7 @@ vae_status_t run_gn(Ctx& x, const NormL& n, const Level& L, const void* src, int
   g.gamma = n.gamma; g.beta = n.beta;
   g.partials = x.b.gn;
   const double elems = static_cast<double>(g.B) * L.T * L.H * L.W * L.C;
-  {
+  if (x.stats_src != src) {  // not already summed by the producing conv's epilogue
     Prof pr(d, x.s, K_GN_STATS, 0, elems * (src_f32 ? 4 : 2));
     CK(launch_gn_stats(g, x.s));
   }
@@ -632,13 +667,22 @@ vae_status_t run_gn(Ctx& x, const NormL& n, const Level& L, const void* src, int
   return VAE_OK;
 }
 
-vae_status_t run_resblock(Ctx& x, ResL& r, const Level& L) {
+// One residual block.  With up_copy, conv2 also stores a bf16 copy of the new residual stream into
+// the conv1 buffer (behind 2 cache frames) for the up-sampling conv that follows; *copied says so.
+vae_status_t run_resblock(Ctx& x, ResL& r, const Level& L, bool up_copy = false, bool* copied = nullptr) {
   vae_decoder* d = x.d;
   const int rf = res_bytes(d) == 4, cf = c1_bytes(d) == 4;
   vae_status_t s = run_gn(x, r.n1, L, x.b.x, rf, 1);
-  if (!s) s = run_conv(x, r.c1, L, x.b.c1, cf, L.T, 0, nullptr, 0, 0);
+  ConvOut o1;
+  o1.y = x.b.c1; o1.y_f32 = cf; o1.y_T_alloc = L.T; o1.stats_level = &L;
+  if (!s) s = run_conv(x, r.c1, L, x.b.hin, o1);
   if (!s) s = run_gn(x, r.n2, L, x.b.c1, cf, 1);
-  if (!s) s = run_conv(x, r.c2, L, x.b.x, rf, L.T, 0, x.b.x, rf, 0);  // in-place residual add
+  ConvOut o2;  // in-place residual add
+  o2.y = x.b.x; o2.y_f32 = rf; o2.y_T_alloc = L.T; o2.residual = x.b.x; o2.res_f32 = rf; o2.stats_level = &L;
+  const bool cp = up_copy && r.c2.tc && !d->f32 && L.C % 32 == 0;
+  if (cp) o2.y2 = x.b.c1;
+  if (!s) s = run_conv(x, r.c2, L, x.b.hin, o2);
+  if (copied) *copied = cp && !s;
   return s;
 }
 
@@ -647,6 +691,7 @@ vae_status_t run_attention(Ctx& x, const Level& L) {
   const int C = L.C, F = x.p->B * L.T;
   const int tok = L.H * L.W, tokp = static_cast<int>(x.p->attn_tokp);
   const int rf = res_bytes(d) == 4;
+  x.stats_src = nullptr;
   // GN without SiLU into hn (= buffer q's neighbour o, reused before O is produced)
   {
     GnArgs g{};
@@ -742,7 +787,9 @@ vae_status_t run_decode(vae_decoder* d, const Plan& p, const float* latent, cons
       CK(launch_latent_to_cl(latent, p.B, c.latent_c, lat_full[0], lat_full[1], lat_full[2], lat_box[0], p.Tlat,
                              lat_box[1], p.h, lat_box[2], p.w, Cp, x.b.hin + 2 * fb, d->f32, p.Tlat + 2, s));
     }
-    st = run_conv(x, d->conv_in, L0, x.b.x, rf, L0.T, 0, nullptr, 0, 0);
+    ConvOut o;
+    o.y = x.b.x; o.y_f32 = rf; o.y_T_alloc = L0.T; o.stats_level = &L0;
+    st = run_conv(x, d->conv_in, L0, x.b.hin, o);
     if (st) return st;
   }
   for (auto& r : d->mid) {
@@ -755,25 +802,35 @@ vae_status_t run_decode(vae_decoder* d, const Plan& p, const float* latent, cons
   }
   for (int i = 0; i < c.n_stages; ++i) {
     const Level& L = p.lv[i];
-    for (auto& r : d->stages[i]) {
-      st = run_resblock(x, r, L);
+    bool copied = false;
+    for (size_t r = 0; r < d->stages[i].size(); ++r) {
+      const bool last = r + 1 == d->stages[i].size() && i + 1 < c.n_stages;
+      st = run_resblock(x, d->stages[i][r], L, last, &copied);
       if (st) return st;
     }
     if (i + 1 < c.n_stages) {
-      // conv input = the residual stream in the conv dtype, behind 2 cache frames
+      // conv input = the residual stream in the conv dtype, behind 2 cache frames: either the copy
+      // the last conv2 stored, or a cast of the residual stream
       const int64_t fe = static_cast<int64_t>(L.H) * L.W * L.C;
-      {
+      char* in = x.b.c1;
+      if (!copied) {
+        in = x.b.hin;
         Prof pr(d, s, K_CAST, 0, static_cast<double>(p.B) * L.T * fe * (res_bytes(d) + act_bytes(d)));
         CK(launch_cast_frames(x.b.x, rf, L.T, x.b.hin + 2 * fe * act_bytes(d), d->f32, L.T + 2, p.B, L.T, fe, s));
       }
-      st = run_conv(x, d->ups[i], L, x.b.x, rf, p.lv[i + 1].T, 0, nullptr, 0, p.first ? 1 : 0);
+      ConvOut o;
+      o.y = x.b.x; o.y_f32 = rf; o.y_T_alloc = p.lv[i + 1].T; o.drop_first = p.first ? 1 : 0;
+      o.stats_level = &p.lv[i + 1];
+      st = run_conv(x, d->ups[i], L, in, o);
       if (st) return st;
     }
   }
   const Level& LL = p.lv[c.n_stages - 1];
   st = run_gn(x, d->head_norm, LL, x.b.x, rf, 1);
   if (st) return st;
-  return run_conv(x, d->head, LL, out, d->f32, out_T_alloc, 1, nullptr, 0, p.first ? 1 : 0);
+  ConvOut o;
+  o.y = out; o.y_f32 = d->f32; o.y_T_alloc = out_T_alloc; o.out_ncthw = 1; o.drop_first = p.first ? 1 : 0;
+  return run_conv(x, d->head, LL, x.b.hin, o);
 }
 
 vae_status_t check_shape(vae_decoder* d, const int64_t* shp, int nph, int npw) {
@@ -1117,7 +1174,7 @@ extern "C" vae_status_t vae_conv3d_causal(const void* x, const void* w_packed, c
 
 extern "C" size_t vae_patch_groupnorm_workspace_bytes(const vae_gn_desc_t* d) {
   if (!d || d->B <= 0 || d->T <= 0 || d->groups <= 0 || d->n_patch_h <= 0 || d->n_patch_w <= 0) return 0;
-  return gn_partials_bytes(d->n_patch_h, d->n_patch_w, d->B, d->T, d->groups);
+  return gn_workspace_bytes(d->n_patch_h, d->n_patch_w, d->B, d->T, d->groups, d->C);
 }
 
 namespace {
@@ -1125,7 +1182,7 @@ vae_status_t check_gn_desc(const vae_gn_desc_t* d) {
   if (d->B <= 0 || d->T <= 0 || d->H <= 0 || d->W <= 0 || d->C <= 0 || d->groups <= 0 || d->C % d->groups)
     return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "bad group-norm descriptor");
   const int cpg = d->C / d->groups;
-  if (d->C % 8 || d->C > 8192 || d->groups > 1024 || !(cpg % 8 == 0 || 8 % cpg == 0))
+  if (d->C % 8 || d->C > 6144 || d->groups > 1024 || !(cpg % 8 == 0 || 8 % cpg == 0))
     return set_err(nullptr, VAE_ERR_UNSUPPORTED, 0, 0, "%d channels in %d groups not supported", d->C, d->groups);
   if (static_cast<double>(cpg) * d->H * d->W >= 8388608.0)
     return set_err(nullptr, VAE_ERR_UNSUPPORTED, 0, 0, "group larger than the exact-sum range (2^23 elements)");

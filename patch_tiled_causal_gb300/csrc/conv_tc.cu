@@ -55,6 +55,9 @@ struct TcParams {
   int T_out, H_out, W_out;
   void* gn_partials;
   int gn_groups, gn_cpg;
+  void* y2;          // optional bf16 copy of y (channels-last), y2_T_alloc frames per batch item
+  int y2_T_alloc;
+  int n_tiles;
   uint32_t* fault;
   uint64_t limit_ns;
 };
@@ -90,6 +93,190 @@ VAE_DEV void gn_accumulate(GnPart* dst, long long s1, unsigned long long lo, uns
 
 }  // namespace
 
+struct TileCoord {
+  int b, t, h0, w0, h_end, w_end, patch, m0, bat, n0;
+};
+
+VAE_DEV TileCoord tile_coord(const TcParams& p, int tile) {
+  TileCoord c{};
+  const int ntile = tile % p.n_ntiles;
+  const int mt = tile / p.n_ntiles;
+  c.n0 = ntile * p.BN;
+  if (p.mode == 0) {
+    const int per_frame = p.n_trows * p.n_tcols;
+    const int frame = mt / per_frame;
+    const int r = mt - frame * per_frame;
+    const int tr = r / p.n_tcols, tc = r - (r / p.n_tcols) * p.n_tcols;
+    const int pi = find_band(p.trow_prefix, p.nph, tr);
+    const int pj = find_band(p.tcol_prefix, p.npw, tc);
+    c.b = frame / p.T;
+    c.t = frame - c.b * p.T;
+    c.h0 = p.ph_edges[pi] + (tr - p.trow_prefix[pi]) * p.rows_t;
+    c.w0 = p.pw_edges[pj] + (tc - p.tcol_prefix[pj]) * p.cols_t;
+    c.h_end = p.ph_edges[pi + 1];
+    c.w_end = p.pw_edges[pj + 1];
+    c.patch = pi * p.npw + pj;
+  } else {
+    c.bat = mt / p.m_tiles_per_batch;
+    c.m0 = (mt - c.bat * p.m_tiles_per_batch) * kBlockM;
+  }
+  return c;
+}
+
+// Epilogue of one 32-column chunk held by this thread (one accumulator row).
+VAE_DEV void epilogue_chunk(const TcParams& p, const TileCoord& tc, int m, int nb, float* v, int lane) {
+  const int sh = p.d2s_h, sw = p.d2s_w;
+  if (p.mode == 1) {
+    // ---- GEMM epilogue: D[bat, row, n] = alpha * acc + bias[n] (+ residual)
+    const int row = tc.m0 + m;
+    const bool valid = row < p.M;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = v[i] * p.alpha + (p.bias ? p.bias[min(nb + i, p.N_real - 1)] : 0.f);
+    if (!valid) return;
+    const int64_t base = static_cast<int64_t>(tc.bat) * p.stride_d + static_cast<int64_t>(row) * p.ldd;
+    if (p.residual) {
+      for (int i = 0; i < 32 && nb + i < p.N_real; ++i)
+        v[i] += p.res_f32 ? static_cast<const float*>(p.residual)[base + nb + i]
+                          : bf2f(static_cast<const __nv_bfloat16*>(p.residual)[base + nb + i]);
+    }
+    if (p.N_real % 32 == 0) {
+      if (p.out_f32) {
+        float* o = static_cast<float*>(p.y) + base + nb;
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) store8(o + i, v + i);
+      } else {
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.y) + base + nb;
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) store8(o + i, v + i);
+      }
+    } else {
+      for (int i = 0; i < 32 && nb + i < p.N_real; ++i) {
+        if (p.out_f32) static_cast<float*>(p.y)[base + nb + i] = v[i];
+        else static_cast<__nv_bfloat16*>(p.y)[base + nb + i] = f2bf(v[i]);
+      }
+    }
+    return;
+  }
+  // ---- conv epilogue
+  const int h = tc.h0 + m / p.cols_t;
+  const int w = tc.w0 + m % p.cols_t;
+  const bool valid = (h < tc.h_end) && (w < tc.w_end);
+  const bool vec = !p.out_ncthw && (p.C_d2s % 32 == 0);
+  if (vec) {
+    const int sub = nb / p.C_d2s;
+    const int c = nb - sub * p.C_d2s;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] += p.bias ? p.bias[(c + i) * p.S + sub] : 0.f;
+    const int dt = sub / (sh * sw);
+    const int rem = sub - dt * sh * sw;
+    const int dy = rem / sw, dx = rem - (rem / sw) * sw;
+    const int to = p.d2s_t * tc.t + dt - p.drop;
+    if (valid && p.residual) {
+      const int64_t ridx =
+          (((static_cast<int64_t>(tc.b) * p.res_T_alloc + tc.t) * p.H + h) * p.W + w) * p.N_real + nb;
+      float r8[8];
+#pragma unroll
+      for (int i = 0; i < 32; i += 8) {
+        if (p.res_f32) load8(static_cast<const float*>(p.residual) + ridx + i, r8);
+        else load8(static_cast<const __nv_bfloat16*>(p.residual) + ridx + i, r8);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[i + k] += r8[k];
+      }
+    }
+    const bool st_ok = valid && to >= 0;
+    if (st_ok) {
+      const int64_t oidx =
+          (((static_cast<int64_t>(tc.b) * p.y_T_alloc + to) * p.H_out + (h * sh + dy)) * p.W_out + (w * sw + dx)) *
+              p.C_d2s + c;
+      if (p.out_f32) {
+        float* o = static_cast<float*>(p.y) + oidx;
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) store8(o + i, v + i);
+      } else {
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.y) + oidx;
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) store8(o + i, v + i);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = bf2f(f2bf(v[i]));  // statistics see the stored values
+      }
+      if (p.y2) {  // bf16 copy for the next conv's operand
+        const int64_t o2 =
+            (((static_cast<int64_t>(tc.b) * p.y2_T_alloc + to) * p.H_out + (h * sh + dy)) * p.W_out + (w * sw + dx)) *
+                p.C_d2s + c;
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.y2) + o2;
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) store8(o + i, v + i);
+      }
+    }
+    if (p.gn_partials) {
+      // exact per-patch group sums of the stored values (all lanes share sub, frame `to` and the group)
+      const int cpg = p.gn_cpg;
+      const int step = min(cpg, 32);
+      for (int i0 = 0; i0 < 32; i0 += step) {
+        long long s1 = 0;
+        unsigned long long lo = 0, hi = 0;
+        if (st_ok) {
+          for (int i = i0; i < i0 + step; ++i) {
+            const float xv = v[i];
+            if (!(fabsf(xv) < 8192.f)) raise_fault(p.fault, FAULT_RANGE, 20);
+            const int qv = __float2int_rn(fminf(fmaxf(xv, -8191.f), 8191.f) * 262144.f);
+            s1 += qv;
+            const unsigned long long sq = static_cast<unsigned long long>(static_cast<long long>(qv) * qv);
+            lo += sq;
+            if (lo < sq) ++hi;
+          }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const long long o1 = __shfl_xor_sync(0xffffffffu, s1, off);
+          const unsigned long long olo = __shfl_xor_sync(0xffffffffu, lo, off);
+          const unsigned long long ohi = __shfl_xor_sync(0xffffffffu, hi, off);
+          s1 += o1;
+          const unsigned long long nlo = lo + olo;
+          hi += ohi + (nlo < lo ? 1ull : 0ull);
+          lo = nlo;
+        }
+        if (lane == 0 && to >= 0) {
+          const int g = (c + i0) / cpg;
+          GnPart* parts = static_cast<GnPart*>(p.gn_partials);
+          const int64_t slot = ((static_cast<int64_t>(tc.patch) * p.B + tc.b) * p.T_out + to) * p.gn_groups + g;
+          if (s1 != 0 || lo != 0 || hi != 0) gn_accumulate(parts + slot, s1, lo, hi);
+        }
+      }
+    }
+  } else {
+    // generic scalar path (NCTHW pixels, or channel counts not a multiple of 32)
+    for (int i = 0; i < 32; ++i) {
+      const int n = nb + i;
+      if (n >= p.N_real) break;
+      const int sub = n / p.C_d2s;
+      const int c = n - sub * p.C_d2s;
+      float val = v[i] + (p.bias ? p.bias[c * p.S + sub] : 0.f);
+      const int dt = sub / (sh * sw);
+      const int rem = sub - dt * sh * sw;
+      const int dy = rem / sw, dx = rem - (rem / sw) * sw;
+      const int to = p.d2s_t * tc.t + dt - p.drop;
+      if (!valid || to < 0) continue;
+      if (p.residual) {
+        const int64_t ridx = (((static_cast<int64_t>(tc.b) * p.res_T_alloc + tc.t) * p.H + h) * p.W + w) * p.N_real + n;
+        val += p.res_f32 ? static_cast<const float*>(p.residual)[ridx]
+                         : bf2f(static_cast<const __nv_bfloat16*>(p.residual)[ridx]);
+      }
+      const int ho = h * sh + dy, wo = w * sw + dx;
+      int64_t oidx;
+      if (p.out_ncthw)
+        oidx = (((static_cast<int64_t>(tc.b) * p.C_d2s + c) * p.y_T_alloc + to) * p.H_out + ho) * p.W_out + wo;
+      else
+        oidx = (((static_cast<int64_t>(tc.b) * p.y_T_alloc + to) * p.H_out + ho) * p.W_out + wo) * p.C_d2s + c;
+      if (p.out_f32) static_cast<float*>(p.y)[oidx] = val;
+      else static_cast<__nv_bfloat16*>(p.y)[oidx] = f2bf(val);
+    }
+  }
+}
+
+// Persistent kernel: each block walks tiles blockIdx.x, blockIdx.x + gridDim.x, ...  The shared-
+// memory ring runs continuously across tiles; two TMEM accumulators let the epilogue of one tile
+// overlap the MMAs of the next.
 __global__ void __launch_bounds__(kThreads, 1)
     conv_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ TcParams p) {
@@ -99,42 +286,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t stage_bytes = kABytes + b_bytes;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + p.stages * stage_bytes);
   uint64_t* empty_bar = full_bar + p.stages;
-  uint64_t* accum_bar = empty_bar + p.stages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum_bar + 1);
+  uint64_t* accf_bar = empty_bar + p.stages;  // [2] accumulator full (MMA -> epilogue)
+  uint64_t* acce_bar = accf_bar + 2;          // [2] accumulator empty (epilogue -> MMA)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---- tile coordinates
-  const int ntile = blockIdx.x % p.n_ntiles;
-  const int mt = blockIdx.x / p.n_ntiles;
-  int b = 0, t = 0, h0 = 0, w0 = 0, h_end = 0, w_end = 0, patch = 0, m0 = 0, bat = 0;
-  if (p.mode == 0) {
-    const int per_frame = p.n_trows * p.n_tcols;
-    const int frame = mt / per_frame;
-    const int r = mt % per_frame;
-    const int tr = r / p.n_tcols, tc = r % p.n_tcols;
-    const int pi = find_band(p.trow_prefix, p.nph, tr);
-    const int pj = find_band(p.tcol_prefix, p.npw, tc);
-    b = frame / p.T;
-    t = frame % p.T;
-    h0 = p.ph_edges[pi] + (tr - p.trow_prefix[pi]) * p.rows_t;
-    w0 = p.pw_edges[pj] + (tc - p.tcol_prefix[pj]) * p.cols_t;
-    h_end = p.ph_edges[pi + 1];
-    w_end = p.pw_edges[pj + 1];
-    patch = pi * p.npw + pj;
-  } else {
-    bat = mt / p.m_tiles_per_batch;
-    m0 = (mt % p.m_tiles_per_batch) * kBlockM;
-  }
-  const int n0 = ntile * p.BN;
+  const int acc_stride = p.tmem_cols / 2;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    mbar_init(accum_bar, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&accf_bar[a], 1);
+      mbar_init(&acce_bar[a], 4 * 32);
+    }
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -148,221 +316,97 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int issued_kb = 0;
+      int kc = 0;  // k blocks issued so far (all tiles)
       bool ok = true;
-      for (int kb = 0; kb < p.num_kb && ok; ++kb) {
-        const int s = kb % p.stages;
-        const int use = kb / p.stages;
-        if (use > 0) ok = mbar_wait(&empty_bar[s], (use - 1) & 1, p.fault, p.limit_ns, 1);
-        if (!ok) break;
-        uint8_t* a_dst = smem + s * stage_bytes;
-        uint8_t* b_dst = a_dst + kABytes;
-        mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
-        if (p.mode == 0) {
-          const int tap = kb / p.cchunks;
-          const int cc = kb - tap * p.cchunks;
-          const int kt = tap / 9, kh = (tap / 3) % 3, kw = tap % 3;
-          const int ti = max(t + kt - 2 + p.cache_frames, 0);
-          tma_load_5d(a_dst, &tmA, &full_bar[s], cc * kBlockK, w0 + kw - 1, h0 + kh - 1, ti, b);
-          tma_load_2d(b_dst, &tmB, &full_bar[s], tap * p.C_in_pad + cc * kBlockK, n0);
-        } else {
-          tma_load_3d(a_dst, &tmA, &full_bar[s], kb * kBlockK, m0, bat);
-          tma_load_3d(b_dst, &tmB, &full_bar[s], kb * kBlockK, n0, bat);
+      for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x) {
+        const TileCoord tc = tile_coord(p, tile);
+        for (int kb = 0; kb < p.num_kb; ++kb, ++kc) {
+          const int s = kc % p.stages;
+          const int use = kc / p.stages;
+          if (use > 0 && !mbar_wait(&empty_bar[s], (use - 1) & 1, p.fault, p.limit_ns, 1)) {
+            ok = false;
+            break;
+          }
+          uint8_t* a_dst = smem + s * stage_bytes;
+          uint8_t* b_dst = a_dst + kABytes;
+          mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
+          if (p.mode == 0) {
+            const int tap = kb / p.cchunks;
+            const int cc = kb - tap * p.cchunks;
+            const int kt = tap / 9, kh = (tap / 3) % 3, kw = tap % 3;
+            const int ti = max(tc.t + kt - 2 + p.cache_frames, 0);
+            tma_load_5d(a_dst, &tmA, &full_bar[s], cc * kBlockK, tc.w0 + kw - 1, tc.h0 + kh - 1, ti, tc.b);
+            tma_load_2d(b_dst, &tmB, &full_bar[s], tap * p.C_in_pad + cc * kBlockK, tc.n0);
+          } else {
+            tma_load_3d(a_dst, &tmA, &full_bar[s], kb * kBlockK, tc.m0, tc.bat);
+            tma_load_3d(b_dst, &tmB, &full_bar[s], kb * kBlockK, tc.n0, tc.bat);
+          }
         }
-        issued_kb = kb + 1;
       }
       // drain: every issued load has landed before the block may exit
-      for (int kb = max(0, issued_kb - p.stages); kb < issued_kb; ++kb)
-        mbar_wait(&full_bar[kb % p.stages], (kb / p.stages) & 1, p.fault, p.limit_ns, 2);
+      for (int k = max(0, kc - p.stages); k < kc; ++k)
+        mbar_wait(&full_bar[k % p.stages], (k / p.stages) & 1, p.fault, p.limit_ns, 2);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kBlockM, static_cast<uint32_t>(p.BN));
-      for (int kb = 0; kb < p.num_kb; ++kb) {
-        const int s = kb % p.stages;
-        if (!mbar_wait(&full_bar[s], (kb / p.stages) & 1, p.fault, p.limit_ns, 3)) break;
+      int kc = 0, it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++it) {
+        const int acc = it & 1, u = it >> 1;
+        if (u > 0 && !mbar_wait(&acce_bar[acc], (u - 1) & 1, p.fault, p.limit_ns, 6)) break;
         tc_fence_after();
-        const uint32_t a_addr = smem_u32(smem + s * stage_bytes);
-        const uint64_t adesc = sdesc_kmajor_sw128(a_addr);
-        const uint64_t bdesc = sdesc_kmajor_sw128(a_addr + kABytes);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * acc_stride);
+        for (int kb = 0; kb < p.num_kb; ++kb, ++kc) {
+          const int s = kc % p.stages;
+          if (!mbar_wait(&full_bar[s], (kc / p.stages) & 1, p.fault, p.limit_ns, 3)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + s * stage_bytes);
+          const uint64_t adesc = sdesc_kmajor_sw128(a_addr);
+          const uint64_t bdesc = sdesc_kmajor_sw128(a_addr + kABytes);
 #pragma unroll
-        for (int k = 0; k < kBlockK / 16; ++k) {
-          // advance 16 bf16 (32 B) along K inside the 128-byte swizzle atom
-          tc_mma_bf16(tmem_base, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), idesc,
-                      (kb > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < kBlockK / 16; ++k) {
+            // advance 16 bf16 (32 B) along K inside the 128-byte swizzle atom
+            tc_mma_bf16(d_tmem, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), idesc,
+                        (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty_bar[s]);
         }
-        tc_commit(&empty_bar[s]);
+        tc_commit(&accf_bar[acc]);
       }
-      tc_commit(accum_bar);
-      mbar_wait(accum_bar, 0, p.fault, p.limit_ns, 4);
     }
   } else {
     // ------------------------------------------------------------------ epilogue (warps 2..5)
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int m = q * 32 + lane;
-    mbar_wait(accum_bar, 0, p.fault, p.limit_ns, 5);
-    tc_fence_after();
-
-    bool valid;
-    int h = 0, w = 0, row = 0;
-    if (p.mode == 0) {
-      h = h0 + m / p.cols_t;
-      w = w0 + m % p.cols_t;
-      valid = (h < h_end) && (w < w_end);
-    } else {
-      row = m0 + m;
-      valid = row < p.M;
-    }
-    const bool vec = (p.mode == 1) ? (p.N_real % 32 == 0)
-                                   : (!p.out_ncthw && (p.C_d2s % 32 == 0));
-    const int sh = p.d2s_h, sw = p.d2s_w;
-    const bool gn = (p.gn_partials != nullptr) && p.mode == 0;
-
-    for (int j = 0; j < (p.BN + 31) / 32; ++j) {
-      uint32_t raw[32];
-      tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(j * 32), raw);
-      tmem_ld_wait();
-      const int nb = n0 + j * 32;
-      if (nb >= p.N_real) continue;
-      float v[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(raw[i]);
-
-      if (p.mode == 1) {
-        // ---- GEMM epilogue: D[bat, row, n] = alpha * acc + bias[n]
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = v[i] * p.alpha + (p.bias ? p.bias[min(nb + i, p.N_real - 1)] : 0.f);
-        if (!valid) continue;
-        const int64_t base = static_cast<int64_t>(bat) * p.stride_d + static_cast<int64_t>(row) * p.ldd;
-        if (p.residual) {
-          for (int i = 0; i < 32 && nb + i < p.N_real; ++i)
-            v[i] += p.res_f32 ? static_cast<const float*>(p.residual)[base + nb + i]
-                              : bf2f(static_cast<const __nv_bfloat16*>(p.residual)[base + nb + i]);
+    int it = 0;
+    for (int tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x, ++it) {
+      const int acc = it & 1, u = it >> 1;
+      if (!mbar_wait(&accf_bar[acc], u & 1, p.fault, p.limit_ns, 5)) break;
+      tc_fence_after();
+      const TileCoord tc = tile_coord(p, tile);
+      const int nchunks = (p.BN + 31) / 32;
+      for (int j = 0; j < nchunks; ++j) {
+        uint32_t raw[32];
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                               static_cast<uint32_t>(acc * acc_stride + j * 32),
+                           raw);
+        tmem_ld_wait();
+        if (j == nchunks - 1) {
+          // every TMEM read of this accumulator is done: hand it back to the MMA warp
+          tc_fence_before();
+          mbar_arrive(&acce_bar[acc]);
         }
-        if (vec) {
-          if (p.out_f32) {
-            float* o = static_cast<float*>(p.y) + base + nb;
+        const int nb = tc.n0 + j * 32;
+        if (nb >= p.N_real) continue;
+        float v[32];
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) store8(o + i, v + i);
-          } else {
-            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.y) + base + nb;
-#pragma unroll
-            for (int i = 0; i < 32; i += 8) store8(o + i, v + i);
-          }
-        } else {
-          for (int i = 0; i < 32 && nb + i < p.N_real; ++i) {
-            if (p.out_f32) static_cast<float*>(p.y)[base + nb + i] = v[i];
-            else static_cast<__nv_bfloat16*>(p.y)[base + nb + i] = f2bf(v[i]);
-          }
-        }
-        continue;
-      }
-
-      // ---- conv epilogue
-      if (vec) {
-        const int sub = nb / p.C_d2s;
-        const int c = nb - sub * p.C_d2s;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] += p.bias ? p.bias[(c + i) * p.S + sub] : 0.f;
-        const int dt = sub / (sh * sw);
-        const int rem = sub - dt * sh * sw;
-        const int dy = rem / sw, dx = rem - (rem / sw) * sw;
-        const int to = p.d2s_t * t + dt - p.drop;
-        if (valid && p.residual) {
-          const int64_t ridx = (((static_cast<int64_t>(b) * p.res_T_alloc + t) * p.H + h) * p.W + w) * p.N_real + nb;
-          float r8[8];
-#pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            if (p.res_f32) load8(static_cast<const float*>(p.residual) + ridx + i, r8);
-            else load8(static_cast<const __nv_bfloat16*>(p.residual) + ridx + i, r8);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) v[i + k] += r8[k];
-          }
-        }
-        const bool st_ok = valid && to >= 0;
-        if (st_ok) {
-          const int64_t oidx =
-              (((static_cast<int64_t>(b) * p.y_T_alloc + to) * p.H_out + (h * sh + dy)) * p.W_out + (w * sw + dx)) *
-                  p.C_d2s + c;
-          if (p.out_f32) {
-            float* o = static_cast<float*>(p.y) + oidx;
-#pragma unroll
-            for (int i = 0; i < 32; i += 8) store8(o + i, v + i);
-          } else {
-            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.y) + oidx;
-#pragma unroll
-            for (int i = 0; i < 32; i += 8) store8(o + i, v + i);
-            // statistics see the stored (rounded) values
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = bf2f(f2bf(v[i]));
-          }
-        }
-        if (gn) {
-          // exact per-patch group sums of the stored values; groups never straddle 8 channels here
-          // (cpg is a multiple of 8 or divides 32), the output frame is `to`.
-          const int cpg = p.gn_cpg;
-          for (int i0 = 0; i0 < 32; i0 += min(cpg, 32)) {
-            long long s1 = 0;
-            unsigned long long lo = 0, hi = 0;
-            if (st_ok) {
-              for (int i = i0; i < i0 + min(cpg, 32); ++i) {
-                const float xv = v[i];
-                if (fabsf(xv) >= 8192.f) raise_fault(p.fault, FAULT_RANGE, 20);
-                const int qv = __float2int_rn(fminf(fmaxf(xv, -8191.f), 8191.f) * 262144.f);
-                s1 += qv;
-                const unsigned long long sq = static_cast<unsigned long long>(static_cast<long long>(qv) * qv);
-                lo += sq;
-                if (lo < sq) ++hi;
-              }
-            }
-            // warp reduction (all lanes of the warp share sub, hence frame `to`, and the group)
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-              const long long o1 = __shfl_xor_sync(0xffffffffu, s1, off);
-              const unsigned long long olo = __shfl_xor_sync(0xffffffffu, lo, off);
-              const unsigned long long ohi = __shfl_xor_sync(0xffffffffu, hi, off);
-              s1 += o1;
-              const unsigned long long nlo = lo + olo;
-              hi += ohi + (nlo < lo ? 1ull : 0ull);
-              lo = nlo;
-            }
-            if (lane == 0 && to >= 0) {
-              const int g = (c + i0) / cpg;
-              GnPart* parts = static_cast<GnPart*>(p.gn_partials);
-              const int64_t slot =
-                  ((static_cast<int64_t>(patch) * p.B + b) * p.T_out + to) * p.gn_groups + g;
-              if (s1 != 0 || lo != 0 || hi != 0) gn_accumulate(parts + slot, s1, lo, hi);
-            }
-          }
-        }
-      } else {
-        // generic scalar path (NCTHW pixels, or channel counts not a multiple of 32)
-        for (int i = 0; i < 32; ++i) {
-          const int n = nb + i;
-          if (n >= p.N_real) break;
-          const int sub = n / p.C_d2s;
-          const int c = n - sub * p.C_d2s;
-          float val = v[i] + (p.bias ? p.bias[c * p.S + sub] : 0.f);
-          const int dt = sub / (sh * sw);
-          const int rem = sub - dt * sh * sw;
-          const int dy = rem / sw, dx = rem - (rem / sw) * sw;
-          const int to = p.d2s_t * t + dt - p.drop;
-          if (!valid || to < 0) continue;
-          if (p.residual) {
-            const int64_t ridx = (((static_cast<int64_t>(b) * p.res_T_alloc + t) * p.H + h) * p.W + w) * p.N_real + n;
-            val += p.res_f32 ? static_cast<const float*>(p.residual)[ridx]
-                             : bf2f(static_cast<const __nv_bfloat16*>(p.residual)[ridx]);
-          }
-          const int ho = h * sh + dy, wo = w * sw + dx;
-          int64_t oidx;
-          if (p.out_ncthw)
-            oidx = (((static_cast<int64_t>(b) * p.C_d2s + c) * p.y_T_alloc + to) * p.H_out + ho) * p.W_out + wo;
-          else
-            oidx = (((static_cast<int64_t>(b) * p.y_T_alloc + to) * p.H_out + ho) * p.W_out + wo) * p.C_d2s + c;
-          if (p.out_f32) static_cast<float*>(p.y)[oidx] = val;
-          else static_cast<__nv_bfloat16*>(p.y)[oidx] = f2bf(val);
-        }
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(raw[i]);
+        epilogue_chunk(p, tc, m, nb, v, lane);
       }
     }
   }
@@ -447,7 +491,8 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   if (p.BN % 16 != 0 || p.BN < 16) return cudaErrorInvalidValue;
   p.n_ntiles = (a.N_pad + p.BN - 1) / p.BN;
   p.tmem_cols = 32;
-  while (p.tmem_cols < p.BN) p.tmem_cols <<= 1;
+  while (p.tmem_cols < 2 * p.BN) p.tmem_cols <<= 1;  // two accumulators
+  if (p.tmem_cols > 512) return cudaErrorInvalidValue;
   const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(p.BN) * kBlockK * 2;
   p.stages = std::min(8, static_cast<int>((200u * 1024u) / stage_bytes));
   p.bias = a.bias;
@@ -530,14 +575,26 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   }
   if (n_blocks <= 0) return cudaSuccess;
   if (n_blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  const size_t smem = 1024 + static_cast<size_t>(p.stages) * stage_bytes + (2 * p.stages + 1) * 8 + 16;
+  p.n_tiles = static_cast<int>(n_blocks);
+  p.y2 = a.y2;
+  p.y2_T_alloc = a.y2_T_alloc ? a.y2_T_alloc : p.T_out;
+  if (a.y2 && (p.out_ncthw || p.C_d2s % 32 != 0)) return cudaErrorInvalidValue;
+  static int n_sm = 0;
+  if (!n_sm) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (n_sm <= 0) n_sm = 148;
+  }
+  const long long grid = std::min<long long>(n_blocks, n_sm);
+  const size_t smem = 1024 + static_cast<size_t>(p.stages) * stage_bytes + (2 * p.stages + 4) * 8 + 16;
   static int attr_set = 0;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(conv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     attr_set = 1;
   }
-  conv_tc_kernel<<<static_cast<unsigned>(n_blocks), kThreads, smem, stream>>>(tmA, tmB, p);
+  conv_tc_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmA, tmB, p);
   return cudaGetLastError();
 }
 

@@ -42,6 +42,8 @@ struct ConvTcArgs {
   int d2s_t, d2s_h, d2s_w, drop_first;
   // fused group-norm statistics of y (nullptr = none): exact per-patch sums, see norm.cu
   void* gn_partials; int gn_groups;
+  // optional second, bf16 copy of y (channels-last, y2_T_alloc frames per batch item)
+  void* y2; int y2_T_alloc;
 };
 cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t s);
 
@@ -73,9 +75,11 @@ struct GnArgs {
   const void* x; int x_f32; int x_T_alloc;  // frames per batch item in memory (0 = T)
   void* y; int y_f32; int y_T_alloc;
   const float* gamma; const float* beta;
-  void* partials;          // [nph*npw, B, T, groups] x GnPartial
+  void* partials;          // gn_workspace_bytes: [nph*npw, B, T, groups] GnPartial, then [B*T, C] float2
 };
 size_t gn_partials_bytes(int nph, int npw, int B, int T, int groups);
+// partials followed (256-aligned) by the per-(frame, channel) affine of the finalize step
+size_t gn_workspace_bytes(int nph, int npw, int B, int T, int groups, int C);
 cudaError_t launch_gn_stats(const GnArgs& a, cudaStream_t s);  // clears and fills partials
 cudaError_t launch_gn_apply(const GnArgs& a, cudaStream_t s);
 

@@ -35,6 +35,11 @@ size_t gn_partials_bytes(int nph, int npw, int B, int T, int groups) {
   return static_cast<size_t>(nph) * npw * B * T * groups * sizeof(GnPartial);
 }
 
+size_t gn_workspace_bytes(int nph, int npw, int B, int T, int groups, int C) {
+  const size_t parts = (gn_partials_bytes(nph, npw, B, T, groups) + 255) & ~size_t(255);
+  return parts + static_cast<size_t>(B) * T * C * sizeof(float2);
+}
+
 struct GnParams {
   int B, T, H, W, C, groups, cpg;
   float eps;
@@ -48,6 +53,7 @@ struct GnParams {
   const float* gamma;
   const float* beta;
   GnPartial* parts;
+  float2* affine;  // [B*T, C] per-channel (scale, shift), after the partials in the workspace
   uint32_t* fault;
   int vec_per_px;   // C / 8
   int px_per_iter;  // blockDim / vec_per_px
@@ -135,12 +141,11 @@ __global__ void __launch_bounds__(256) gn_stats_kernel(const __grid_constant__ G
   }
 }
 
-// Merge the per-patch sums (patch order) and normalise; one block per (frame, image row).
-template <typename TI, typename TO>
-__global__ void __launch_bounds__(256) gn_apply_kernel(const __grid_constant__ GnParams p) {
+// Merge the per-patch sums of one frame (patch order), then fold mean, rstd, gamma and beta into a
+// per-channel affine y = x * a[c] + s[c]; one block per (batch, frame).
+__global__ void __launch_bounds__(256) gn_finalize_kernel(const __grid_constant__ GnParams p) {
   __shared__ float sh_mean[1024], sh_rstd[1024];
-  const int row = blockIdx.x;  // frame * H + h
-  const int frame = row / p.H, h = row % p.H;
+  const int frame = blockIdx.x;
   const int b = frame / p.T, t = frame % p.T;
   const double n = static_cast<double>(p.cpg) * p.H * p.W;
   const int P = p.nph * p.npw;
@@ -152,30 +157,51 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const __grid_constant__ G
       s1 += static_cast<long long>(d.s1);
       add128(lo, hi, d.s2_lo, d.s2_hi);
     }
-    const double mq = static_cast<double>(s1) / n;                                   // mean, units 2^-18
+    const double mq = static_cast<double>(s1) / n;  // mean in units of 2^-18
     const double e2 = (static_cast<double>(hi) * 18446744073709551616.0 + static_cast<double>(lo)) / n;
-    double var = (e2 - mq * mq) * (1.0 / 68719476736.0);                             // / 2^36
+    double var = (e2 - mq * mq) * (1.0 / 68719476736.0);  // / 2^36
     if (var < 0.0) var = 0.0;
     sh_mean[g] = static_cast<float>(mq * (1.0 / 262144.0));
     sh_rstd[g] = static_cast<float>(1.0 / sqrt(var + static_cast<double>(p.eps)));
   }
   __syncthreads();
-  const TI* xr = static_cast<const TI*>(p.x) + ((static_cast<int64_t>(b) * p.x_T_alloc + t) * p.H + h) * p.W * p.C;
-  const int64_t yrow = (static_cast<int64_t>(b) * p.y_T_alloc + t) * p.H + h;
-  TO* yr = static_cast<TO*>(p.y) + yrow * p.W * p.C;
-  const int nvec = p.W * p.C / 8;
-  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-    const int c0 = (v * 8) % p.C;
-    float a[8], o[8];
-    load8(xr + static_cast<int64_t>(v) * 8, a);
+  float2* aff = p.affine + static_cast<int64_t>(frame) * p.C;
+  for (int c = threadIdx.x; c < p.C; c += blockDim.x) {
+    const int g = c / p.cpg;
+    const float a = sh_rstd[g] * p.gamma[c];
+    aff[c] = make_float2(a, p.beta[c] - sh_mean[g] * a);
+  }
+}
+
+// y = SiLU(x * a[c] + s[c]); grid (chunks of a frame, frames), 16-byte vectors.
+constexpr int kApplyVecPerThread = 8;
+template <typename TI, typename TO>
+__global__ void __launch_bounds__(256) gn_apply_kernel(const __grid_constant__ GnParams p) {
+  extern __shared__ float2 sh_aff[];
+  const int frame = blockIdx.y;
+  const int b = frame / p.T, t = frame % p.T;
+  const float2* aff = p.affine + static_cast<int64_t>(frame) * p.C;
+  for (int c = threadIdx.x; c < p.C; c += blockDim.x) sh_aff[c] = aff[c];
+  __syncthreads();
+  const int64_t fe = static_cast<int64_t>(p.H) * p.W * p.C;  // elements of one frame
+  const TI* xf = static_cast<const TI*>(p.x) + (static_cast<int64_t>(b) * p.x_T_alloc + t) * fe;
+  TO* yf = static_cast<TO*>(p.y) + (static_cast<int64_t>(b) * p.y_T_alloc + t) * fe;
+  const int64_t nvec = fe / 8;
+  const int64_t v0 = static_cast<int64_t>(blockIdx.x) * blockDim.x * kApplyVecPerThread + threadIdx.x;
+#pragma unroll
+  for (int k = 0; k < kApplyVecPerThread; ++k) {
+    const int64_t v = v0 + static_cast<int64_t>(k) * blockDim.x;
+    if (v >= nvec) break;
+    const int c0 = static_cast<int>((v * 8) % p.C);
+    float a[8];
+    load8(xf + v * 8, a);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const int c = c0 + e;
-      const int g = c / p.cpg;
-      float z = (a[e] - sh_mean[g]) * sh_rstd[g] * p.gamma[c] + p.beta[c];
-      o[e] = p.silu ? silu_f(z) : z;
+      const float2 m = sh_aff[c0 + e];
+      const float z = fmaf(a[e], m.x, m.y);
+      a[e] = p.silu ? __fdividef(z, 1.0f + __expf(-z)) : z;
     }
-    store8(yr + static_cast<int64_t>(v) * 8, o);
+    store8(yf + v * 8, a);
   }
 }
 
@@ -185,7 +211,7 @@ bool fill_gn(GnParams& p, const GnArgs& a) {
   p.B = a.B; p.T = a.T; p.H = a.H; p.W = a.W; p.C = a.C; p.groups = a.groups;
   if (a.groups <= 0 || a.groups > 1024 || a.C % a.groups) return false;
   p.cpg = a.C / a.groups;
-  if (a.C % 8 || a.C > 8192 || !(p.cpg % 8 == 0 || 8 % p.cpg == 0)) return false;
+  if (a.C % 8 || a.C > 6144 || !(p.cpg % 8 == 0 || 8 % p.cpg == 0)) return false;
   if (a.nph > kMaxP || a.npw > kMaxP) return false;
   p.eps = a.eps; p.silu = a.silu;
   p.nph = a.nph; p.npw = a.npw;
@@ -196,6 +222,8 @@ bool fill_gn(GnParams& p, const GnArgs& a) {
   p.y_T_alloc = a.y_T_alloc ? a.y_T_alloc : a.T;
   p.gamma = a.gamma; p.beta = a.beta;
   p.parts = static_cast<GnPartial*>(a.partials);
+  p.affine = reinterpret_cast<float2*>(static_cast<char*>(a.partials) +
+                                       ((gn_partials_bytes(a.nph, a.npw, a.B, a.T, a.groups) + 255) & ~size_t(255)));
   p.fault = fault_word();
   p.vec_per_px = a.C / 8;
   p.px_per_iter = std::max(1, 256 / p.vec_per_px);
@@ -230,13 +258,18 @@ cudaError_t launch_gn_stats(const GnArgs& a, cudaStream_t s) {
 cudaError_t launch_gn_apply(const GnArgs& a, cudaStream_t s) {
   static GnParams p;
   if (!fill_gn(p, a)) return cudaErrorInvalidValue;
-  const long long nb = static_cast<long long>(a.B) * a.T * a.H;
-  if (nb == 0) return cudaSuccess;
-  dim3 grid(static_cast<unsigned>(nb));
-  if (a.x_f32 && a.y_f32) gn_apply_kernel<float, float><<<grid, 256, 0, s>>>(p);
-  else if (a.x_f32) gn_apply_kernel<float, __nv_bfloat16><<<grid, 256, 0, s>>>(p);
-  else if (a.y_f32) gn_apply_kernel<__nv_bfloat16, float><<<grid, 256, 0, s>>>(p);
-  else gn_apply_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, s>>>(p);
+  const long long frames = static_cast<long long>(a.B) * a.T;
+  if (frames == 0) return cudaSuccess;
+  if (frames > 65535) return cudaErrorInvalidValue;
+  gn_finalize_kernel<<<static_cast<unsigned>(frames), 256, 0, s>>>(p);
+  const int64_t nvec = static_cast<int64_t>(a.H) * a.W * a.C / 8;
+  const int64_t per_block = 256LL * kApplyVecPerThread;
+  dim3 grid(static_cast<unsigned>((nvec + per_block - 1) / per_block), static_cast<unsigned>(frames));
+  const size_t sm = static_cast<size_t>(a.C) * sizeof(float2);
+  if (a.x_f32 && a.y_f32) gn_apply_kernel<float, float><<<grid, 256, sm, s>>>(p);
+  else if (a.x_f32) gn_apply_kernel<float, __nv_bfloat16><<<grid, 256, sm, s>>>(p);
+  else if (a.y_f32) gn_apply_kernel<__nv_bfloat16, float><<<grid, 256, sm, s>>>(p);
+  else gn_apply_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, sm, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -342,59 +375,81 @@ VAE_DEV float ramp_w(int y, int n, int lo, int hi) {
   return w;
 }
 
-// one block per output row (b, c, t, y): collect the tiles covering (t, y) in order, then gather
+// One block per output row (t, y): warp 0 lists the tiles covering (t, y) in tile order (ballot +
+// prefix count), then every (b, c) plane of the row is gathered in 8-pixel vectors.
 template <typename TT, typename TO>
 __global__ void __launch_bounds__(128) blend_kernel(const __grid_constant__ BlendParams p) {
   __shared__ int list[VAE_MAX_TILES];
   __shared__ float wty[VAE_MAX_TILES];
-  __shared__ unsigned char flag[VAE_MAX_TILES];
   __shared__ int count;
-  int64_t r = blockIdx.x;
-  const int y = static_cast<int>(r % p.H); r /= p.H;
-  const int t = static_cast<int>(r % p.T); r /= p.T;
-  const int c = static_cast<int>(r % p.C);
-  const int b = static_cast<int>(r / p.C);
-  for (int i = threadIdx.x; i < p.n; i += blockDim.x) {
-    const BlendTile& tl = p.tiles[i];
-    flag[i] = (t >= tl.t0 && t < tl.t0 + tl.nt && y >= tl.h0 && y < tl.h0 + tl.nh) ? 1 : 0;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int k = 0;
-    for (int i = 0; i < p.n; ++i)
-      if (flag[i]) {
+  const int y = blockIdx.x % p.H;
+  const int t = blockIdx.x / p.H;
+  if (threadIdx.x < 32) {
+    int base = 0;
+    for (int i0 = 0; i0 < p.n; i0 += 32) {
+      const int i = i0 + threadIdx.x;
+      bool cov = false;
+      if (i < p.n) {
+        const BlendTile& tl = p.tiles[i];
+        cov = t >= tl.t0 && t < tl.t0 + tl.nt && y >= tl.h0 && y < tl.h0 + tl.nh;
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, cov);
+      if (cov) {
+        const int k = base + __popc(m & ((1u << threadIdx.x) - 1u));
         const BlendTile& tl = p.tiles[i];
         list[k] = i;
         wty[k] = ramp_w(t - tl.t0, tl.nt, tl.ovl[0], tl.ovl[1]) * ramp_w(y - tl.h0, tl.nh, tl.ovl[2], tl.ovl[3]);
-        ++k;
       }
-    count = k;
+      base += __popc(m);
+    }
+    if (threadIdx.x == 0) count = base;
   }
   __syncthreads();
   const int nk = count;
-  TO* orow = static_cast<TO*>(p.out) + (((static_cast<int64_t>(b) * p.C + c) * p.T + t) * p.H + y) * p.W;
-  for (int x0 = threadIdx.x * 8; x0 < p.W; x0 += blockDim.x * 8) {
+  const int nv = (p.W + 7) / 8;
+  const int planes = p.B * p.C;
+  for (int job = threadIdx.x; job < planes * nv; job += blockDim.x) {
+    const int plane = job / nv;
+    const int x0 = (job - plane * nv) * 8;
     float acc[8], ws[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = ws[e] = 0.f;
     for (int k = 0; k < nk; ++k) {
       const BlendTile& tl = p.tiles[list[k]];
-      if (x0 + 8 <= tl.w0 || x0 >= tl.w0 + tl.nw) continue;
+      const int lx = x0 - tl.w0;
+      if (lx + 8 <= 0 || lx >= tl.nw) continue;
       const TT* trow = static_cast<const TT*>(tl.ptr) +
-                       (((static_cast<int64_t>(b) * p.C + c) * tl.nt + (t - tl.t0)) * tl.nh + (y - tl.h0)) * tl.nw;
+                       ((static_cast<int64_t>(plane) * tl.nt + (t - tl.t0)) * tl.nh + (y - tl.h0)) * tl.nw;
       const float wk = wty[k];
+      float v[8];
+      if (lx >= 0 && lx + 8 <= tl.nw && (lx & 7) == 0 && (tl.nw & 7) == 0) {
+        load8(trow + lx, v);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int x = x0 + e;
-        if (x < tl.w0 || x >= tl.w0 + tl.nw || x >= p.W) continue;
-        const float wx = wk * ramp_w(x - tl.w0, tl.nw, tl.ovl[4], tl.ovl[5]);
-        acc[e] += wx * to_f<TT>(trow[x - tl.w0]);
-        ws[e] += wx;
+        for (int e = 0; e < 8; ++e) {
+          const float wx = wk * ramp_w(lx + e, tl.nw, tl.ovl[4], tl.ovl[5]);
+          acc[e] = fmaf(wx, v[e], acc[e]);
+          ws[e] += wx;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int xx = lx + e;
+          if (xx < 0 || xx >= tl.nw || x0 + e >= p.W) continue;
+          const float wx = wk * ramp_w(xx, tl.nw, tl.ovl[4], tl.ovl[5]);
+          acc[e] = fmaf(wx, to_f<TT>(trow[xx]), acc[e]);
+          ws[e] += wx;
+        }
       }
     }
+    TO* orow = static_cast<TO*>(p.out) + ((static_cast<int64_t>(plane) * p.T + t) * p.H + y) * p.W;
+    float o[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-      if (x0 + e < p.W) orow[x0 + e] = from_f<TO>(ws[e] > 0.f ? acc[e] / ws[e] : 0.f);
+    for (int e = 0; e < 8; ++e) o[e] = ws[e] > 0.f ? acc[e] / ws[e] : 0.f;
+    if (x0 + 8 <= p.W && (p.W & 7) == 0) {
+      store8(orow + x0, o);
+    } else {
+      for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(o[e]);
+    }
   }
 }
 
@@ -414,7 +469,7 @@ cudaError_t launch_blend(const void* const* tiles, const vae_tile_t* meta, int n
     t.w0 = meta[i].pix[4]; t.nw = meta[i].pix[5];
     for (int k = 0; k < 6; ++k) t.ovl[k] = static_cast<unsigned short>(meta[i].ovl[k]);
   }
-  const long long nb = static_cast<long long>(d.B) * d.C * d.T * d.H;
+  const long long nb = static_cast<long long>(d.T) * d.H;
   if (nb == 0) return cudaSuccess;
   dim3 grid(static_cast<unsigned>(nb));
   if (p.tile_f32 && p.out_f32) blend_kernel<float, float><<<grid, 128, 0, s>>>(p);

@@ -46,6 +46,7 @@ struct TcParams {
   float alpha;
   int num_kb, cchunks;
   int N_real, BN, n_ntiles, tmem_cols, stages;
+  int msub;  // 128-pixel MMA sub-tiles per tile (2 when BN <= 128: both share each weight tile)
   const float* bias;
   const void* residual;
   int res_f32;
@@ -118,7 +119,7 @@ VAE_DEV TileCoord tile_coord(const TcParams& p, int tile) {
     c.patch = pi * p.npw + pj;
   } else {
     c.bat = mt / p.m_tiles_per_batch;
-    c.m0 = (mt - c.bat * p.m_tiles_per_batch) * kBlockM;
+    c.m0 = (mt - c.bat * p.m_tiles_per_batch) * kBlockM * p.msub;
   }
   return c;
 }
@@ -283,7 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t b_bytes = static_cast<uint32_t>(p.BN) * kBlockK * 2;
-  const uint32_t stage_bytes = kABytes + b_bytes;
+  const uint32_t a_bytes = kABytes * static_cast<uint32_t>(p.msub);
+  const uint32_t stage_bytes = a_bytes + b_bytes;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + p.stages * stage_bytes);
   uint64_t* empty_bar = full_bar + p.stages;
   uint64_t* accf_bar = empty_bar + p.stages;  // [2] accumulator full (MMA -> epilogue)
@@ -328,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* a_dst = smem + s * stage_bytes;
-          uint8_t* b_dst = a_dst + kABytes;
+          uint8_t* b_dst = a_dst + a_bytes;
           mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
           if (p.mode == 0) {
             const int tap = kb / p.cchunks;
@@ -366,13 +368,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + s * stage_bytes);
-          const uint64_t adesc = sdesc_kmajor_sw128(a_addr);
-          const uint64_t bdesc = sdesc_kmajor_sw128(a_addr + kABytes);
+          const uint64_t bdesc = sdesc_kmajor_sw128(a_addr + a_bytes);
+          for (int sub = 0; sub < p.msub; ++sub) {
+            const uint64_t adesc = sdesc_kmajor_sw128(a_addr + sub * kABytes);
+            const uint32_t d_sub = d_tmem + static_cast<uint32_t>(sub * p.BN);
 #pragma unroll
-          for (int k = 0; k < kBlockK / 16; ++k) {
-            // advance 16 bf16 (32 B) along K inside the 128-byte swizzle atom
-            tc_mma_bf16(d_tmem, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), idesc,
-                        (kb > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < kBlockK / 16; ++k) {
+              // advance 16 bf16 (32 B) along K inside the 128-byte swizzle atom
+              tc_mma_bf16(d_sub, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), idesc,
+                          (kb > 0 || k > 0) ? 1u : 0u);
+            }
           }
           tc_commit(&empty_bar[s]);
         }
@@ -390,23 +395,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const TileCoord tc = tile_coord(p, tile);
       const int nchunks = (p.BN + 31) / 32;
-      for (int j = 0; j < nchunks; ++j) {
-        uint32_t raw[32];
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                               static_cast<uint32_t>(acc * acc_stride + j * 32),
-                           raw);
-        tmem_ld_wait();
-        if (j == nchunks - 1) {
-          // every TMEM read of this accumulator is done: hand it back to the MMA warp
-          tc_fence_before();
-          mbar_arrive(&acce_bar[acc]);
-        }
-        const int nb = tc.n0 + j * 32;
-        if (nb >= p.N_real) continue;
-        float v[32];
+      for (int sub = 0; sub < p.msub; ++sub) {
+        for (int j = 0; j < nchunks; ++j) {
+          uint32_t raw[32];
+          tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                 static_cast<uint32_t>(acc * acc_stride + sub * p.BN + j * 32),
+                             raw);
+          tmem_ld_wait();
+          if (sub == p.msub - 1 && j == nchunks - 1) {
+            // every TMEM read of this accumulator is done: hand it back to the MMA warp
+            tc_fence_before();
+            mbar_arrive(&acce_bar[acc]);
+          }
+          const int nb = tc.n0 + j * 32;
+          if (nb >= p.N_real) continue;
+          float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(raw[i]);
-        epilogue_chunk(p, tc, m, nb, v, lane);
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(raw[i]);
+          epilogue_chunk(p, tc, sub * kBlockM + m, nb, v, lane);
+        }
       }
     }
   }
@@ -490,10 +497,11 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   }
   if (p.BN % 16 != 0 || p.BN < 16) return cudaErrorInvalidValue;
   p.n_ntiles = (a.N_pad + p.BN - 1) / p.BN;
+  p.msub = p.BN <= 128 ? 2 : 1;
   p.tmem_cols = 32;
-  while (p.tmem_cols < 2 * p.BN) p.tmem_cols <<= 1;  // two accumulators
+  while (p.tmem_cols < 2 * p.msub * p.BN) p.tmem_cols <<= 1;  // two accumulators
   if (p.tmem_cols > 512) return cudaErrorInvalidValue;
-  const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(p.BN) * kBlockK * 2;
+  const uint32_t stage_bytes = kABytes * p.msub + static_cast<uint32_t>(p.BN) * kBlockK * 2;
   p.stages = std::min(8, static_cast<int>((200u * 1024u) / stage_bytes));
   p.bias = a.bias;
   p.residual = a.residual;
@@ -514,7 +522,7 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
     for (int i = 0; i <= a.nph; ++i) p.ph_edges[i] = a.ph_edges[i];
     for (int j = 0; j <= a.npw; ++j) p.pw_edges[j] = a.pw_edges[j];
     p.cols_t = pick_cols(a.pw_edges, a.npw);
-    p.rows_t = kBlockM / p.cols_t;
+    p.rows_t = kBlockM * p.msub / p.cols_t;
     p.trow_prefix[0] = 0;
     for (int i = 0; i < a.nph; ++i)
       p.trow_prefix[i + 1] = p.trow_prefix[i] + (a.ph_edges[i + 1] - a.ph_edges[i] + p.rows_t - 1) / p.rows_t;
@@ -556,7 +564,7 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
     p.M = a.M; p.K = a.K; p.batch = a.batch; p.stride_d = a.stride_d; p.alpha = a.alpha;
     p.ldd = a.ldd ? a.ldd : a.N_real;
     if (a.K % 64 != 0) return cudaErrorInvalidValue;
-    p.m_tiles_per_batch = (a.M + kBlockM - 1) / kBlockM;
+    p.m_tiles_per_batch = (a.M + kBlockM * p.msub - 1) / (kBlockM * p.msub);
     p.num_kb = a.K / kBlockK;
     p.S = 1; p.C_d2s = a.N_real; p.d2s_t = p.d2s_h = p.d2s_w = 1;
     const int64_t sa = a.batch > 1 ? a.stride_a : static_cast<int64_t>(a.M) * a.K;
@@ -564,7 +572,7 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
     if (sa % 8 || sb % 8 || a.K % 8) return cudaErrorInvalidValue;
     uint64_t ad[3] = {(uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.batch};
     uint64_t as[2] = {(uint64_t)a.K * 2, (uint64_t)sa * 2};
-    uint32_t ab[3] = {64u, 128u, 1u};
+    uint32_t ab[3] = {64u, static_cast<uint32_t>(kBlockM * p.msub), 1u};
     if (!make_map(&tmA, a.x, 3, ad, as, ab)) return cudaErrorInvalidValue;
     // B rows beyond N_real read as zeros (never the next batch item's rows)
     uint64_t bd[3] = {(uint64_t)a.K, (uint64_t)a.N_real, (uint64_t)a.batch};

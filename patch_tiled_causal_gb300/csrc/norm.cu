@@ -173,7 +173,8 @@ __global__ void __launch_bounds__(256) gn_finalize_kernel(const __grid_constant_
   }
 }
 
-// y = SiLU(x * a[c] + s[c]); grid (chunks of a frame, frames), 16-byte vectors.
+// y = SiLU(x * a[c] + s[c]); grid (chunks of a frame, frames), 16-byte vectors.  Every thread
+// issues all its loads before any math so that enough bytes are in flight to cover HBM latency.
 constexpr int kApplyVecPerThread = 8;
 template <typename TI, typename TO>
 __global__ void __launch_bounds__(256) gn_apply_kernel(const __grid_constant__ GnParams p) {
@@ -182,26 +183,30 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const __grid_constant__ G
   const int b = frame / p.T, t = frame % p.T;
   const float2* aff = p.affine + static_cast<int64_t>(frame) * p.C;
   for (int c = threadIdx.x; c < p.C; c += blockDim.x) sh_aff[c] = aff[c];
-  __syncthreads();
   const int64_t fe = static_cast<int64_t>(p.H) * p.W * p.C;  // elements of one frame
   const TI* xf = static_cast<const TI*>(p.x) + (static_cast<int64_t>(b) * p.x_T_alloc + t) * fe;
   TO* yf = static_cast<TO*>(p.y) + (static_cast<int64_t>(b) * p.y_T_alloc + t) * fe;
   const int64_t nvec = fe / 8;
   const int64_t v0 = static_cast<int64_t>(blockIdx.x) * blockDim.x * kApplyVecPerThread + threadIdx.x;
+  float a[kApplyVecPerThread][8];
+#pragma unroll
+  for (int k = 0; k < kApplyVecPerThread; ++k) {
+    const int64_t v = v0 + static_cast<int64_t>(k) * blockDim.x;
+    if (v < nvec) load8(xf + v * 8, a[k]);
+  }
+  __syncthreads();
 #pragma unroll
   for (int k = 0; k < kApplyVecPerThread; ++k) {
     const int64_t v = v0 + static_cast<int64_t>(k) * blockDim.x;
     if (v >= nvec) break;
     const int c0 = static_cast<int>((v * 8) % p.C);
-    float a[8];
-    load8(xf + v * 8, a);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const float2 m = sh_aff[c0 + e];
-      const float z = fmaf(a[e], m.x, m.y);
-      a[e] = p.silu ? __fdividef(z, 1.0f + __expf(-z)) : z;
+      const float z = fmaf(a[k][e], m.x, m.y);
+      a[k][e] = p.silu ? __fdividef(z, 1.0f + __expf(-z)) : z;
     }
-    store8(yf + v * 8, a);
+    store8(yf + v * 8, a[k]);
   }
 }
 
@@ -368,15 +373,18 @@ struct BlendParams {
   BlendTile tiles[VAE_MAX_TILES];
 };
 
+// Ramp of a tile of n pixels at local coordinate y: (y+1)/(lo+1) over the lo-pixel overlap with the
+// previous tile, (n-y)/(hi+1) over the hi-pixel overlap with the next, 1 elsewhere.
 VAE_DEV float ramp_w(int y, int n, int lo, int hi) {
   float w = 1.f;
-  if (y < lo) w *= static_cast<float>(y + 1) / static_cast<float>(lo + 1);
-  if (y >= n - hi) w *= static_cast<float>(n - y) / static_cast<float>(hi + 1);
+  if (y < lo) w *= __fdividef(static_cast<float>(y + 1), static_cast<float>(lo + 1));
+  if (y >= n - hi) w *= __fdividef(static_cast<float>(n - y), static_cast<float>(hi + 1));
   return w;
 }
 
 // One block per output row (t, y): warp 0 lists the tiles covering (t, y) in tile order (ballot +
-// prefix count), then every (b, c) plane of the row is gathered in 8-pixel vectors.
+// prefix count); each thread then owns 8 output pixels of the row and gathers them for every (b, c)
+// plane, reusing the tile list and the per-pixel weights across planes.
 template <typename TT, typename TO>
 __global__ void __launch_bounds__(128) blend_kernel(const __grid_constant__ BlendParams p) {
   __shared__ int list[VAE_MAX_TILES];
@@ -406,49 +414,66 @@ __global__ void __launch_bounds__(128) blend_kernel(const __grid_constant__ Blen
   }
   __syncthreads();
   const int nk = count;
-  const int nv = (p.W + 7) / 8;
   const int planes = p.B * p.C;
-  for (int job = threadIdx.x; job < planes * nv; job += blockDim.x) {
-    const int plane = job / nv;
-    const int x0 = (job - plane * nv) * 8;
-    float acc[8], ws[8];
+  const int64_t plane_out = static_cast<int64_t>(p.T) * p.H * p.W;
+  for (int x0 = threadIdx.x * 8; x0 < p.W; x0 += blockDim.x * 8) {
+    // covering tiles of these 8 pixels (at most 8 kept; a pixel lies in at most 2 tiles per axis)
+    int tk[8], lxk[8];
+    float wk[8][8];
+    float wsum[8];
+    int nsel = 0;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = ws[e] = 0.f;
-    for (int k = 0; k < nk; ++k) {
+    for (int e = 0; e < 8; ++e) wsum[e] = 0.f;
+    for (int k = 0; k < nk && nsel < 8; ++k) {
       const BlendTile& tl = p.tiles[list[k]];
       const int lx = x0 - tl.w0;
       if (lx + 8 <= 0 || lx >= tl.nw) continue;
-      const TT* trow = static_cast<const TT*>(tl.ptr) +
-                       ((static_cast<int64_t>(plane) * tl.nt + (t - tl.t0)) * tl.nh + (y - tl.h0)) * tl.nw;
-      const float wk = wty[k];
-      float v[8];
-      if (lx >= 0 && lx + 8 <= tl.nw && (lx & 7) == 0 && (tl.nw & 7) == 0) {
-        load8(trow + lx, v);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float wx = wk * ramp_w(lx + e, tl.nw, tl.ovl[4], tl.ovl[5]);
-          acc[e] = fmaf(wx, v[e], acc[e]);
-          ws[e] += wx;
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int xx = lx + e;
-          if (xx < 0 || xx >= tl.nw || x0 + e >= p.W) continue;
-          const float wx = wk * ramp_w(xx, tl.nw, tl.ovl[4], tl.ovl[5]);
-          acc[e] = fmaf(wx, to_f<TT>(trow[xx]), acc[e]);
-          ws[e] += wx;
-        }
+      for (int e = 0; e < 8; ++e) {
+        const int xx = lx + e;
+        const bool in = xx >= 0 && xx < tl.nw && x0 + e < p.W;
+        const float w = in ? wty[k] * ramp_w(xx, tl.nw, tl.ovl[4], tl.ovl[5]) : 0.f;
+        wk[nsel][e] = w;
+        wsum[e] += w;
       }
+      tk[nsel] = list[k];
+      lxk[nsel] = lx;
+      ++nsel;
     }
-    TO* orow = static_cast<TO*>(p.out) + ((static_cast<int64_t>(plane) * p.T + t) * p.H + y) * p.W;
-    float o[8];
+    float rinv[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] = ws[e] > 0.f ? acc[e] / ws[e] : 0.f;
-    if (x0 + 8 <= p.W && (p.W & 7) == 0) {
-      store8(orow + x0, o);
-    } else {
-      for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(o[e]);
+    for (int e = 0; e < 8; ++e) rinv[e] = wsum[e] > 0.f ? 1.f / wsum[e] : 0.f;
+    for (int pl = 0; pl < planes; ++pl) {
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+      for (int j = 0; j < nsel; ++j) {
+        const BlendTile& tl = p.tiles[tk[j]];
+        const int lx = lxk[j];
+        const TT* trow = static_cast<const TT*>(tl.ptr) +
+                         ((static_cast<int64_t>(pl) * tl.nt + (t - tl.t0)) * tl.nh + (y - tl.h0)) * tl.nw;
+        float v[8];
+        if (lx >= 0 && lx + 8 <= tl.nw && ((lx | tl.nw) & 7) == 0) {
+          load8(trow + lx, v);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int xx = lx + e;
+            v[e] = (xx >= 0 && xx < tl.nw) ? to_f<TT>(trow[xx]) : 0.f;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(wk[j][e], v[e], acc[e]);
+      }
+      TO* orow = static_cast<TO*>(p.out) + pl * plane_out + (static_cast<int64_t>(t) * p.H + y) * p.W;
+      float o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = acc[e] * rinv[e];
+      if (x0 + 8 <= p.W && (p.W & 7) == 0) {
+        store8(orow + x0, o);
+      } else {
+        for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(o[e]);
+      }
     }
   }
 }

@@ -186,27 +186,28 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const __grid_constant__ G
   const int64_t fe = static_cast<int64_t>(p.H) * p.W * p.C;  // elements of one frame
   const TI* xf = static_cast<const TI*>(p.x) + (static_cast<int64_t>(b) * p.x_T_alloc + t) * fe;
   TO* yf = static_cast<TO*>(p.y) + (static_cast<int64_t>(b) * p.y_T_alloc + t) * fe;
-  const int64_t nvec = fe / 8;
-  const int64_t v0 = static_cast<int64_t>(blockIdx.x) * blockDim.x * kApplyVecPerThread + threadIdx.x;
+  const int nvec = static_cast<int>(fe / 8);  // < 2^31 per frame (checked on the host)
+  const int cvec = p.C / 8;
+  const int v0 = blockIdx.x * blockDim.x * kApplyVecPerThread + threadIdx.x;
   float a[kApplyVecPerThread][8];
 #pragma unroll
   for (int k = 0; k < kApplyVecPerThread; ++k) {
-    const int64_t v = v0 + static_cast<int64_t>(k) * blockDim.x;
-    if (v < nvec) load8(xf + v * 8, a[k]);
+    const int v = v0 + k * blockDim.x;
+    if (v < nvec) load8(xf + static_cast<int64_t>(v) * 8, a[k]);
   }
   __syncthreads();
 #pragma unroll
   for (int k = 0; k < kApplyVecPerThread; ++k) {
-    const int64_t v = v0 + static_cast<int64_t>(k) * blockDim.x;
+    const int v = v0 + k * blockDim.x;
     if (v >= nvec) break;
-    const int c0 = static_cast<int>((v * 8) % p.C);
+    const int c0 = ((cvec & (cvec - 1)) == 0 ? (v & (cvec - 1)) : (v % cvec)) * 8;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const float2 m = sh_aff[c0 + e];
       const float z = fmaf(a[k][e], m.x, m.y);
       a[k][e] = p.silu ? __fdividef(z, 1.0f + __expf(-z)) : z;
     }
-    store8(yf + v * 8, a[k]);
+    store8(yf + static_cast<int64_t>(v) * 8, a[k]);
   }
 }
 
@@ -265,7 +266,7 @@ cudaError_t launch_gn_apply(const GnArgs& a, cudaStream_t s) {
   if (!fill_gn(p, a)) return cudaErrorInvalidValue;
   const long long frames = static_cast<long long>(a.B) * a.T;
   if (frames == 0) return cudaSuccess;
-  if (frames > 65535) return cudaErrorInvalidValue;
+  if (frames > 65535 || static_cast<int64_t>(a.H) * a.W * a.C / 8 > 0x7fffffffLL) return cudaErrorInvalidValue;
   gn_finalize_kernel<<<static_cast<unsigned>(frames), 256, 0, s>>>(p);
   const int64_t nvec = static_cast<int64_t>(a.H) * a.W * a.C / 8;
   const int64_t per_block = 256LL * kApplyVecPerThread;
@@ -383,10 +384,11 @@ VAE_DEV float ramp_w(int y, int n, int lo, int hi) {
 }
 
 // One block per output row (t, y): warp 0 lists the tiles covering (t, y) in tile order (ballot +
-// prefix count); each thread then owns 8 output pixels of the row and gathers them for every (b, c)
-// plane, reusing the tile list and the per-pixel weights across planes.
+// prefix count); each thread then owns 8 output pixels of the row and gathers them for the (b, c)
+// planes, 8 planes at a time so one tile's weights serve several independent loads.
+constexpr int kBlendPlanes = 8;
 template <typename TT, typename TO>
-__global__ void __launch_bounds__(128) blend_kernel(const __grid_constant__ BlendParams p) {
+__global__ void __launch_bounds__(256) blend_kernel(const __grid_constant__ BlendParams p) {
   __shared__ int list[VAE_MAX_TILES];
   __shared__ float wty[VAE_MAX_TILES];
   __shared__ int count;
@@ -417,62 +419,63 @@ __global__ void __launch_bounds__(128) blend_kernel(const __grid_constant__ Blen
   const int planes = p.B * p.C;
   const int64_t plane_out = static_cast<int64_t>(p.T) * p.H * p.W;
   for (int x0 = threadIdx.x * 8; x0 < p.W; x0 += blockDim.x * 8) {
-    // covering tiles of these 8 pixels (at most 8 kept; a pixel lies in at most 2 tiles per axis)
-    int tk[8], lxk[8];
-    float wk[8][8];
-    float wsum[8];
-    int nsel = 0;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) wsum[e] = 0.f;
-    for (int k = 0; k < nk && nsel < 8; ++k) {
-      const BlendTile& tl = p.tiles[list[k]];
-      const int lx = x0 - tl.w0;
-      if (lx + 8 <= 0 || lx >= tl.nw) continue;
+    for (int pg = 0; pg < planes; pg += kBlendPlanes) {
+      const int np = min(kBlendPlanes, planes - pg);
+      float acc[kBlendPlanes][8], ws[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const int xx = lx + e;
-        const bool in = xx >= 0 && xx < tl.nw && x0 + e < p.W;
-        const float w = in ? wty[k] * ramp_w(xx, tl.nw, tl.ovl[4], tl.ovl[5]) : 0.f;
-        wk[nsel][e] = w;
-        wsum[e] += w;
+        ws[e] = 0.f;
+#pragma unroll
+        for (int j = 0; j < kBlendPlanes; ++j) acc[j][e] = 0.f;
       }
-      tk[nsel] = list[k];
-      lxk[nsel] = lx;
-      ++nsel;
-    }
-    float rinv[8];
+      for (int k = 0; k < nk; ++k) {
+        const BlendTile& tl = p.tiles[list[k]];
+        const int lx = x0 - tl.w0;
+        if (lx + 8 <= 0 || lx >= tl.nw) continue;
+        float w[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) rinv[e] = wsum[e] > 0.f ? 1.f / wsum[e] : 0.f;
-    for (int pl = 0; pl < planes; ++pl) {
-      float acc[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-      for (int j = 0; j < nsel; ++j) {
-        const BlendTile& tl = p.tiles[tk[j]];
-        const int lx = lxk[j];
-        const TT* trow = static_cast<const TT*>(tl.ptr) +
-                         ((static_cast<int64_t>(pl) * tl.nt + (t - tl.t0)) * tl.nh + (y - tl.h0)) * tl.nw;
-        float v[8];
-        if (lx >= 0 && lx + 8 <= tl.nw && ((lx | tl.nw) & 7) == 0) {
-          load8(trow + lx, v);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int xx = lx + e;
-            v[e] = (xx >= 0 && xx < tl.nw) ? to_f<TT>(trow[xx]) : 0.f;
-          }
+        for (int e = 0; e < 8; ++e) {
+          const int xx = lx + e;
+          w[e] = (xx >= 0 && xx < tl.nw) ? wty[k] * ramp_w(xx, tl.nw, tl.ovl[4], tl.ovl[5]) : 0.f;
+          ws[e] += w[e];
         }
+        const bool vec = lx >= 0 && lx + 8 <= tl.nw && ((lx | tl.nw) & 7) == 0;
+        const int64_t plane_in = static_cast<int64_t>(tl.nt) * tl.nh * tl.nw;
+        const TT* trow = static_cast<const TT*>(tl.ptr) + pg * plane_in +
+                         (static_cast<int64_t>(t - tl.t0) * tl.nh + (y - tl.h0)) * tl.nw;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = fmaf(wk[j][e], v[e], acc[e]);
+        for (int j = 0; j < kBlendPlanes; ++j) {
+          if (j >= np) break;
+          float v[8];
+          const TT* r = trow + j * plane_in;
+          if (vec) {
+            load8(r + lx, v);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int xx = lx + e;
+              v[e] = (xx >= 0 && xx < tl.nw) ? to_f<TT>(r[xx]) : 0.f;
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(w[e], v[e], acc[j][e]);
+        }
       }
-      TO* orow = static_cast<TO*>(p.out) + pl * plane_out + (static_cast<int64_t>(t) * p.H + y) * p.W;
-      float o[8];
+      float rinv[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = acc[e] * rinv[e];
-      if (x0 + 8 <= p.W && (p.W & 7) == 0) {
-        store8(orow + x0, o);
-      } else {
-        for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(o[e]);
+      for (int e = 0; e < 8; ++e) rinv[e] = ws[e] > 0.f ? 1.f / ws[e] : 0.f;
+#pragma unroll
+      for (int j = 0; j < kBlendPlanes; ++j) {
+        if (j >= np) break;
+        TO* orow = static_cast<TO*>(p.out) + (pg + j) * plane_out + (static_cast<int64_t>(t) * p.H + y) * p.W;
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = acc[j][e] * rinv[e];
+        if (x0 + 8 <= p.W && (p.W & 7) == 0) {
+          store8(orow + x0, o);
+        } else {
+          for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(o[e]);
+        }
       }
     }
   }
@@ -497,10 +500,12 @@ cudaError_t launch_blend(const void* const* tiles, const vae_tile_t* meta, int n
   const long long nb = static_cast<long long>(d.T) * d.H;
   if (nb == 0) return cudaSuccess;
   dim3 grid(static_cast<unsigned>(nb));
-  if (p.tile_f32 && p.out_f32) blend_kernel<float, float><<<grid, 128, 0, s>>>(p);
-  else if (p.tile_f32) blend_kernel<float, __nv_bfloat16><<<grid, 128, 0, s>>>(p);
-  else if (p.out_f32) blend_kernel<__nv_bfloat16, float><<<grid, 128, 0, s>>>(p);
-  else blend_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 128, 0, s>>>(p);
+  const int nv = (d.W + 7) / 8;
+  const int threads = std::min(256, std::max(32, (nv + 31) / 32 * 32));
+  if (p.tile_f32 && p.out_f32) blend_kernel<float, float><<<grid, threads, 0, s>>>(p);
+  else if (p.tile_f32) blend_kernel<float, __nv_bfloat16><<<grid, threads, 0, s>>>(p);
+  else if (p.out_f32) blend_kernel<__nv_bfloat16, float><<<grid, threads, 0, s>>>(p);
+  else blend_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, threads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

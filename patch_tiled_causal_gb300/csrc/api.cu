@@ -600,7 +600,8 @@ vae_status_t run_conv(Ctx& x, ConvL& c, const Level& L, char* in, const ConvOut&
     const int Cd = c.C_out / (c.st * c.sh * c.sw);
     const int G = d->cfg.gn_groups;
     const int cpg = Cd % G == 0 ? Cd / G : 0;
-    const bool fuse = o.stats_level && !out_ncthw && Cd % 32 == 0 && cpg > 0 &&
+    // fused sums cost one warp reduction per group per 32 columns: worth it from 16 channels per group
+    const bool fuse = o.stats_level && !out_ncthw && Cd % 32 == 0 && cpg >= 16 &&
                       (cpg < 32 ? 32 % cpg == 0 : cpg % 32 == 0);
     if (fuse) {
       CK(cudaMemsetAsync(x.b.gn, 0, gn_partials_bytes(x.p->nph, x.p->npw, B, o.stats_level->T, G), x.s));

@@ -101,16 +101,38 @@ __global__ void __launch_bounds__(256) gn_stats_kernel(const __grid_constant__ G
 #pragma unroll
   for (int k = 0; k < GPV; ++k) { s1[k] = 0; lo[k] = hi[k] = 0ull; }
   if (threadIdx.x < p.vec_per_px * p.px_per_iter) {
-    for (int w = w_beg + pxo; w < w_end; w += p.px_per_iter) {
-      float v[8];
-      load8(xr + static_cast<int64_t>(w) * p.C + c0, v);
+    // four pixels' vectors are loaded before any of them is summed (bytes in flight)
+    for (int w = w_beg + pxo; w < w_end; w += 4 * p.px_per_iter) {
+      float v[4][8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int k = (GPV == 1) ? 0 : e / (8 / GPV);
-        const int qv = quantize(v[e], p.fault);
-        s1[k] += qv;
-        const unsigned long long sq = static_cast<unsigned long long>(static_cast<long long>(qv) * qv);
-        add128(lo[k], hi[k], sq, 0ull);
+      for (int u = 0; u < 4; ++u) {
+        const int ww = w + u * p.px_per_iter;
+        if (ww < w_end) load8(xr + static_cast<int64_t>(ww) * p.C + c0, v[u]);
+        else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[u][e] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < GPV; ++k) {
+        // q^2 < 2^62: four of them fit an unsigned 64-bit sum before the 128-bit carry
+        unsigned long long sq4 = 0;
+        int n4 = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+#pragma unroll
+          for (int e = k * (8 / GPV); e < (k + 1) * (8 / GPV); ++e) {
+            const int qv = quantize(v[u][e], p.fault);
+            s1[k] += qv;
+            sq4 += static_cast<unsigned long long>(static_cast<long long>(qv) * qv);
+            if (++n4 == 4) {
+              add128(lo[k], hi[k], sq4, 0ull);
+              sq4 = 0;
+              n4 = 0;
+            }
+          }
+        }
+        if (n4) add128(lo[k], hi[k], sq4, 0ull);
       }
     }
   }
@@ -384,9 +406,7 @@ VAE_DEV float ramp_w(int y, int n, int lo, int hi) {
 }
 
 // One block per output row (t, y): warp 0 lists the tiles covering (t, y) in tile order (ballot +
-// prefix count); each thread then owns 8 output pixels of the row and gathers them for the (b, c)
-// planes, 8 planes at a time so one tile's weights serve several independent loads.
-constexpr int kBlendPlanes = 8;
+// prefix count); then each thread takes (plane, 8-pixel vector) jobs and gathers them, tile by tile.
 template <typename TT, typename TO>
 __global__ void __launch_bounds__(256) blend_kernel(const __grid_constant__ BlendParams p) {
   __shared__ int list[VAE_MAX_TILES];
@@ -416,67 +436,51 @@ __global__ void __launch_bounds__(256) blend_kernel(const __grid_constant__ Blen
   }
   __syncthreads();
   const int nk = count;
-  const int planes = p.B * p.C;
+  const int nv = (p.W + 7) / 8;
+  const int jobs = p.B * p.C * nv;
   const int64_t plane_out = static_cast<int64_t>(p.T) * p.H * p.W;
-  for (int x0 = threadIdx.x * 8; x0 < p.W; x0 += blockDim.x * 8) {
-    for (int pg = 0; pg < planes; pg += kBlendPlanes) {
-      const int np = min(kBlendPlanes, planes - pg);
-      float acc[kBlendPlanes][8], ws[8];
+  for (int job = threadIdx.x; job < jobs; job += blockDim.x) {
+    const int pl = job / nv;
+    const int x0 = (job - pl * nv) * 8;
+    float acc[8], ws[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        ws[e] = 0.f;
-#pragma unroll
-        for (int j = 0; j < kBlendPlanes; ++j) acc[j][e] = 0.f;
-      }
-      for (int k = 0; k < nk; ++k) {
-        const BlendTile& tl = p.tiles[list[k]];
-        const int lx = x0 - tl.w0;
-        if (lx + 8 <= 0 || lx >= tl.nw) continue;
-        float w[8];
+    for (int e = 0; e < 8; ++e) acc[e] = ws[e] = 0.f;
+    for (int k = 0; k < nk; ++k) {
+      const BlendTile& tl = p.tiles[list[k]];
+      const int lx = x0 - tl.w0;
+      if (lx + 8 <= 0 || lx >= tl.nw) continue;
+      const TT* r = static_cast<const TT*>(tl.ptr) +
+                    ((static_cast<int64_t>(pl) * tl.nt + (t - tl.t0)) * tl.nh + (y - tl.h0)) * tl.nw;
+      float v[8];
+      const bool full = lx >= 0 && lx + 8 <= tl.nw;
+      if (full && ((lx | tl.nw) & 7) == 0) {
+        load8(r + lx, v);
+      } else {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int xx = lx + e;
-          w[e] = (xx >= 0 && xx < tl.nw) ? wty[k] * ramp_w(xx, tl.nw, tl.ovl[4], tl.ovl[5]) : 0.f;
-          ws[e] += w[e];
-        }
-        const bool vec = lx >= 0 && lx + 8 <= tl.nw && ((lx | tl.nw) & 7) == 0;
-        const int64_t plane_in = static_cast<int64_t>(tl.nt) * tl.nh * tl.nw;
-        const TT* trow = static_cast<const TT*>(tl.ptr) + pg * plane_in +
-                         (static_cast<int64_t>(t - tl.t0) * tl.nh + (y - tl.h0)) * tl.nw;
-#pragma unroll
-        for (int j = 0; j < kBlendPlanes; ++j) {
-          if (j >= np) break;
-          float v[8];
-          const TT* r = trow + j * plane_in;
-          if (vec) {
-            load8(r + lx, v);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int xx = lx + e;
-              v[e] = (xx >= 0 && xx < tl.nw) ? to_f<TT>(r[xx]) : 0.f;
-            }
-          }
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(w[e], v[e], acc[j][e]);
+          v[e] = (xx >= 0 && xx < tl.nw) ? to_f<TT>(r[xx]) : 0.f;
         }
       }
-      float rinv[8];
+      const float wk = wty[k];
+      const int lo = tl.ovl[4], hi = tl.ovl[5];
+      const bool flat = full && lx >= lo && lx + 8 <= tl.nw - hi;  // no ramp inside these 8 pixels
 #pragma unroll
-      for (int e = 0; e < 8; ++e) rinv[e] = ws[e] > 0.f ? 1.f / ws[e] : 0.f;
-#pragma unroll
-      for (int j = 0; j < kBlendPlanes; ++j) {
-        if (j >= np) break;
-        TO* orow = static_cast<TO*>(p.out) + (pg + j) * plane_out + (static_cast<int64_t>(t) * p.H + y) * p.W;
-        float o[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = acc[j][e] * rinv[e];
-        if (x0 + 8 <= p.W && (p.W & 7) == 0) {
-          store8(orow + x0, o);
-        } else {
-          for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(o[e]);
-        }
+      for (int e = 0; e < 8; ++e) {
+        const int xx = lx + e;
+        const float w = flat ? wk : ((xx >= 0 && xx < tl.nw) ? wk * ramp_w(xx, tl.nw, lo, hi) : 0.f);
+        acc[e] = fmaf(w, v[e], acc[e]);
+        ws[e] += w;
       }
+    }
+    TO* orow = static_cast<TO*>(p.out) + pl * plane_out + (static_cast<int64_t>(t) * p.H + y) * p.W;
+    float o[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = ws[e] > 0.f ? acc[e] / ws[e] : 0.f;
+    if (x0 + 8 <= p.W && (p.W & 7) == 0) {
+      store8(orow + x0, o);
+    } else {
+      for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(o[e]);
     }
   }
 }
@@ -500,8 +504,8 @@ cudaError_t launch_blend(const void* const* tiles, const vae_tile_t* meta, int n
   const long long nb = static_cast<long long>(d.T) * d.H;
   if (nb == 0) return cudaSuccess;
   dim3 grid(static_cast<unsigned>(nb));
-  const int nv = (d.W + 7) / 8;
-  const int threads = std::min(256, std::max(32, (nv + 31) / 32 * 32));
+  const int jobs = d.B * d.C * ((d.W + 7) / 8);
+  const int threads = std::min(256, std::max(32, (jobs + 31) / 32 * 32));
   if (p.tile_f32 && p.out_f32) blend_kernel<float, float><<<grid, threads, 0, s>>>(p);
   else if (p.tile_f32) blend_kernel<float, __nv_bfloat16><<<grid, threads, 0, s>>>(p);
   else if (p.out_f32) blend_kernel<__nv_bfloat16, float><<<grid, threads, 0, s>>>(p);

@@ -268,6 +268,26 @@ size_t vae_patch_groupnorm_workspace_bytes(const vae_gn_desc_t* d);
 vae_status_t vae_patch_groupnorm_silu(const void* x, const float* gamma, const float* beta, void* y,
                                       void* workspace, const vae_gn_desc_t* d, void* stream);
 
+/* Bytes of the fixed device array that vae_patch_groupnorm_silu_noalloc uses as scratch (4 MiB). */
+#define VAE_GN_NOALLOC_SCRATCH_BYTES (4 << 20)
+
+/* PatchGroupNorm + SiLU without any allocation, for callers that cannot allocate device memory: hosts
+ * whose own pool allocator owns the whole device and that pass a plugin only its input and output
+ * buffers, or loops in which a cudaMalloc (which can synchronise the device) is not allowed.  The pages
+ * have no counterpart of this entry point; it computes exactly what vae_patch_groupnorm_silu computes
+ * (same kernels, same result), but its scratch -- the per-patch partial sums and the per-frame affine,
+ * vae_patch_groupnorm_workspace_bytes(d) bytes -- lives in a fixed device array of
+ * VAE_GN_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the library holds until
+ * the process exits.  A descriptor needing more scratch than that returns VAE_ERR_UNSUPPORTED and
+ * launches nothing.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before any stream capture.
+ * Every call shares the one array and leaves its contents behind; each call clears the partial sums it
+ * needs before using them, but calls whose GPU work overlaps (e.g. on two streams, or from two host
+ * threads) race on the array: serialise them.  No cudaMalloc, cudaFree or allocating library routine is
+ * called.  x, y, gamma, beta, d: as for vae_patch_groupnorm_silu. */
+vae_status_t vae_patch_groupnorm_silu_noalloc(const void* x, const float* gamma, const float* beta, void* y,
+                                              const vae_gn_desc_t* d, void* stream);
+
 /* Depth-to-space descriptor: x [B, T, H, W, C*s_t*s_h*s_w] channels-last. */
 typedef struct {
   int B, T, H, W, C;

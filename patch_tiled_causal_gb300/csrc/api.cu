@@ -1193,6 +1193,14 @@ vae_status_t check_gn_desc(const vae_gn_desc_t* d) {
 }
 }  // namespace
 
+namespace vae {
+vae_status_t op_error(vae_status_t code, const char* msg) { return set_err(nullptr, code, 0, 0, "%s", msg); }
+vae_status_t validate_gn_desc(const void* x, const void* y, const vae_gn_desc_t* d) {
+  if (!aligned16(x) || !aligned16(y)) return set_err(nullptr, VAE_ERR_ALIGNMENT, 0, 0, "pointers must be 16-byte aligned");
+  return check_gn_desc(d);
+}
+}  // namespace vae
+
 extern "C" vae_status_t vae_patch_groupnorm_silu(const void* x, const float* gamma, const float* beta, void* y,
                                                  void* workspace, const vae_gn_desc_t* d, void* stream) {
   if (!x || !gamma || !beta || !y || !workspace || !d) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null argument");

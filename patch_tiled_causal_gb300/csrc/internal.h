@@ -113,4 +113,9 @@ cudaError_t launch_transpose_bf16(const void* in, void* out, int batch, int rows
 
 cudaError_t launch_watchdog_test(uint64_t limit_ns, cudaStream_t s);
 
+// Op-level error reporting (records the message for vae_last_error(NULL, ...)) and the group-norm
+// descriptor checks shared by the group-norm entry points.
+vae_status_t op_error(vae_status_t code, const char* msg);
+vae_status_t validate_gn_desc(const void* x, const void* y, const vae_gn_desc_t* d);
+
 }  // namespace vae

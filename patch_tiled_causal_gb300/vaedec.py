@@ -95,6 +95,7 @@ _SIGS = {
     "vae_conv3d_causal": (C.c_int, [_P, _P, _P, _P, _P, C.POINTER(VaeConvDesc), _P]),
     "vae_patch_groupnorm_workspace_bytes": (C.c_size_t, [C.POINTER(VaeGnDesc)]),
     "vae_patch_groupnorm_silu": (C.c_int, [_P, _P, _P, _P, _P, C.POINTER(VaeGnDesc), _P]),
+    "vae_patch_groupnorm_silu_noalloc": (C.c_int, [_P, _P, _P, _P, C.POINTER(VaeGnDesc), _P]),
     "vae_upsample_d2s": (C.c_int, [_P, _P, C.POINTER(VaeD2sDesc), _P]),
     "vae_tile_blend": (C.c_int, [C.POINTER(_P), C.POINTER(VaeTile), C.c_int, _P, C.POINTER(VaeBlendDesc), _P]),
     "vae_gemm_bf16": (C.c_int, [_P, _P, _P, _P, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int64, C.c_int64,
@@ -249,6 +250,15 @@ def patch_groupnorm_silu(x, gamma, beta, y, workspace, d: VaeGnDesc, stream=None
     torch = _torch()
     _check(load().vae_patch_groupnorm_silu(_ptr(x), _ptr(gamma, torch.float32), _ptr(beta, torch.float32), _ptr(y),
                                            _ptr(workspace), C.byref(d), _stream(stream)), "vae_patch_groupnorm_silu")
+    return y
+
+
+def patch_groupnorm_silu_noalloc(x, gamma, beta, y, d: VaeGnDesc, stream=None):
+    """Same as patch_groupnorm_silu, with the scratch in the library's fixed device array."""
+    torch = _torch()
+    _check(load().vae_patch_groupnorm_silu_noalloc(_ptr(x), _ptr(gamma, torch.float32), _ptr(beta, torch.float32),
+                                                   _ptr(y), C.byref(d), _stream(stream)),
+           "vae_patch_groupnorm_silu_noalloc")
     return y
 
 

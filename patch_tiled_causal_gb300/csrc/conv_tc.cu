@@ -59,6 +59,9 @@ struct TcParams {
   void* y2;          // optional bf16 copy of y (channels-last), y2_T_alloc frames per batch item
   int y2_T_alloc;
   int n_tiles;
+  int pair;          // 1: CTAs run in clusters of 2 on adjacent M tiles of one N tile, each loading half of
+                     // the weight tile and multicasting it to both
+  int n_mtiles, seq_count;
   uint32_t* fault;
   uint64_t limit_ns;
 };
@@ -96,7 +99,22 @@ VAE_DEV void gn_accumulate(GnPart* dst, long long s1, unsigned long long lo, uns
 
 struct TileCoord {
   int b, t, h0, w0, h_end, w_end, patch, m0, bat, n0;
+  bool dummy;  // pair mode, odd M-tile count: this CTA computes a copy of the last tile and stores nothing
 };
+
+VAE_DEV TileCoord tile_coord(const TcParams& p, int tile);
+
+// Tile of work-sequence entry `seq` for this CTA.
+VAE_DEV TileCoord seq_coord(const TcParams& p, int seq, int rank) {
+  if (!p.pair) return tile_coord(p, seq);
+  const int nt = seq % p.n_ntiles;
+  int mt = 2 * (seq / p.n_ntiles) + rank;
+  const bool dummy = mt >= p.n_mtiles;
+  if (dummy) mt = p.n_mtiles - 1;
+  TileCoord c = tile_coord(p, mt * p.n_ntiles + nt);
+  c.dummy = dummy;
+  return c;
+}
 
 VAE_DEV TileCoord tile_coord(const TcParams& p, int tile) {
   TileCoord c{};
@@ -126,6 +144,7 @@ VAE_DEV TileCoord tile_coord(const TcParams& p, int tile) {
 
 // Epilogue of one 32-column chunk held by this thread (one accumulator row).
 VAE_DEV void epilogue_chunk(const TcParams& p, const TileCoord& tc, int m, int nb, float* v, int lane) {
+  if (tc.dummy) return;
   const int sh = p.d2s_h, sw = p.d2s_w;
   if (p.mode == 1) {
     // ---- GEMM epilogue: D[bat, row, n] = alpha * acc + bias[n] (+ residual)
@@ -295,11 +314,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int acc_stride = p.tmem_cols / 2;
+  const int rank = p.pair ? static_cast<int>(cluster_ctarank()) : 0;
+  const int seq0 = p.pair ? blockIdx.x >> 1 : blockIdx.x;
+  const int seq_step = p.pair ? gridDim.x >> 1 : gridDim.x;
+  const uint16_t pair_mask = 0x3;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&empty_bar[s], p.pair ? 2 : 1);  // pair: both CTAs' MMAs free a stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&accf_bar[a], 1);
@@ -314,14 +337,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (p.pair) cluster_sync();  // the peer's barriers exist before anything is multicast to them
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int kc = 0;  // k blocks issued so far (all tiles)
       bool ok = true;
-      for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x) {
-        const TileCoord tc = tile_coord(p, tile);
+      for (int seq = seq0; seq < p.seq_count && ok; seq += seq_step) {
+        const TileCoord tc = seq_coord(p, seq, rank);
         for (int kb = 0; kb < p.num_kb; ++kb, ++kc) {
           const int s = kc % p.stages;
           const int use = kc / p.stages;
@@ -338,16 +362,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kt = tap / 9, kh = (tap / 3) % 3, kw = tap % 3;
             const int ti = max(tc.t + kt - 2 + p.cache_frames, 0);
             tma_load_5d(a_dst, &tmA, &full_bar[s], cc * kBlockK, tc.w0 + kw - 1, tc.h0 + kh - 1, ti, tc.b);
-            tma_load_2d(b_dst, &tmB, &full_bar[s], tap * p.C_in_pad + cc * kBlockK, tc.n0);
+            if (p.pair)
+              tma_load_2d_mc(b_dst + rank * (b_bytes / 2), &tmB, &full_bar[s], tap * p.C_in_pad + cc * kBlockK,
+                             tc.n0 + rank * (p.BN / 2), pair_mask);
+            else
+              tma_load_2d(b_dst, &tmB, &full_bar[s], tap * p.C_in_pad + cc * kBlockK, tc.n0);
           } else {
             tma_load_3d(a_dst, &tmA, &full_bar[s], kb * kBlockK, tc.m0, tc.bat);
-            tma_load_3d(b_dst, &tmB, &full_bar[s], kb * kBlockK, tc.n0, tc.bat);
+            if (p.pair)
+              tma_load_3d_mc(b_dst + rank * (b_bytes / 2), &tmB, &full_bar[s], kb * kBlockK,
+                             tc.n0 + rank * (p.BN / 2), tc.bat, pair_mask);
+            else
+              tma_load_3d(b_dst, &tmB, &full_bar[s], kb * kBlockK, tc.n0, tc.bat);
           }
         }
       }
       // drain: every issued load has landed before the block may exit
       for (int k = max(0, kc - p.stages); k < kc; ++k)
         mbar_wait(&full_bar[k % p.stages], (k / p.stages) & 1, p.fault, p.limit_ns, 2);
+      // pair: both MMAs have released every stage, so no multicast commit is still on its way here
+      if (p.pair)
+        for (int k = max(0, kc - p.stages); k < kc; ++k)
+          mbar_wait(&empty_bar[k % p.stages], (k / p.stages) & 1, p.fault, p.limit_ns, 7);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -355,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = idesc_bf16_f32(kBlockM, static_cast<uint32_t>(p.BN));
       int kc = 0, it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++it) {
+      for (int seq = seq0; seq < p.seq_count && ok; seq += seq_step, ++it) {
         const int acc = it & 1, u = it >> 1;
         if (u > 0 && !mbar_wait(&acce_bar[acc], (u - 1) & 1, p.fault, p.limit_ns, 6)) break;
         tc_fence_after();
@@ -379,7 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                           (kb > 0 || k > 0) ? 1u : 0u);
             }
           }
-          tc_commit(&empty_bar[s]);
+          if (p.pair) tc_commit_mc(&empty_bar[s], pair_mask);
+          else tc_commit(&empty_bar[s]);
         }
         tc_commit(&accf_bar[acc]);
       }
@@ -389,11 +426,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int m = q * 32 + lane;
     int it = 0;
-    for (int tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x, ++it) {
+    for (int seq = seq0; seq < p.seq_count; seq += seq_step, ++it) {
       const int acc = it & 1, u = it >> 1;
       if (!mbar_wait(&accf_bar[acc], u & 1, p.fault, p.limit_ns, 5)) break;
       tc_fence_after();
-      const TileCoord tc = tile_coord(p, tile);
+      const TileCoord tc = seq_coord(p, seq, rank);
       const int nchunks = (p.BN + 31) / 32;
       for (int sub = 0; sub < p.msub; ++sub) {
         for (int j = 0; j < nchunks; ++j) {
@@ -424,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
   }
+  if (p.pair) cluster_sync();  // neither CTA leaves while the other may still write into it
 }
 
 // ================================================================================ host side
@@ -485,6 +523,10 @@ int pick_cols(const int* pw, int npw) {
 
 }  // namespace
 
+namespace {
+bool pair_mode_enabled() { return true; }
+}  // namespace
+
 cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   static TcParams p;  // large: built on the host then copied into the launch
   p = TcParams{};
@@ -498,6 +540,8 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   if (p.BN % 16 != 0 || p.BN < 16) return cudaErrorInvalidValue;
   p.n_ntiles = (a.N_pad + p.BN - 1) / p.BN;
   p.msub = p.BN <= 128 ? 2 : 1;
+  // clusters of 2 share each weight tile (half loaded by each CTA, multicast to both)
+  const bool want_pair = pair_mode_enabled() && p.BN % 16 == 0;
   p.tmem_cols = 32;
   while (p.tmem_cols < 2 * p.msub * p.BN) p.tmem_cols <<= 1;  // two accumulators
   if (p.tmem_cols > 512) return cudaErrorInvalidValue;
@@ -557,7 +601,7 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
     const uint64_t K = 27ull * C;
     uint64_t wd[2] = {K, (uint64_t)a.N_pad};
     uint64_t ws[1] = {K * 2};
-    uint32_t wb[2] = {64u, (uint32_t)p.BN};
+    uint32_t wb[2] = {64u, (uint32_t)(want_pair ? p.BN / 2 : p.BN)};
     if (!make_map(&tmB, a.w, 2, wd, ws, wb)) return cudaErrorInvalidValue;
     n_blocks = static_cast<long long>(a.B) * a.T * p.n_trows * p.n_tcols * p.n_ntiles;
   } else {
@@ -577,7 +621,7 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
     // B rows beyond N_real read as zeros (never the next batch item's rows)
     uint64_t bd[3] = {(uint64_t)a.K, (uint64_t)a.N_real, (uint64_t)a.batch};
     uint64_t bs[2] = {(uint64_t)a.K * 2, (uint64_t)sb * 2};
-    uint32_t bb[3] = {64u, (uint32_t)p.BN, 1u};
+    uint32_t bb[3] = {64u, (uint32_t)(want_pair ? p.BN / 2 : p.BN), 1u};
     if (!make_map(&tmB, a.w, 3, bd, bs, bb)) return cudaErrorInvalidValue;
     n_blocks = static_cast<long long>(a.batch) * p.m_tiles_per_batch * p.n_ntiles;
   }
@@ -594,15 +638,48 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
     cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
     if (n_sm <= 0) n_sm = 148;
   }
-  const long long grid = std::min<long long>(n_blocks, n_sm);
   const size_t smem = 1024 + static_cast<size_t>(p.stages) * stage_bytes + (2 * p.stages + 4) * 8 + 16;
   static int attr_set = 0;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(conv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(conv_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    (void)e;
     attr_set = 1;
   }
-  conv_tc_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmA, tmB, p);
+  p.n_mtiles = static_cast<int>(n_blocks / p.n_ntiles);
+  p.pair = want_pair ? 1 : 0;
+  if (!p.pair) {
+    p.seq_count = p.n_tiles;
+    const long long grid = std::min<long long>(n_blocks, n_sm);
+    conv_tc_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmA, tmB, p);
+    return cudaGetLastError();
+  }
+  p.seq_count = (p.n_mtiles + 1) / 2 * p.n_ntiles;
+  static int max_clusters = 0;
+  static size_t max_clusters_smem = 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_clusters <= 0 || max_clusters_smem != smem) {
+    cfg.gridDim = dim3(2 * (n_sm / 2));
+    int mc = 0;
+    if (cudaOccupancyMaxActiveClusters(&mc, conv_tc_kernel, &cfg) != cudaSuccess || mc <= 0) mc = n_sm / 2;
+    max_clusters = mc;
+    max_clusters_smem = smem;
+  }
+  const long long clusters = std::min<long long>(p.seq_count, max_clusters);
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+  cudaError_t e = cudaLaunchKernelEx(&cfg, conv_tc_kernel, tmA, tmB, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -196,10 +196,40 @@ __global__ void __launch_bounds__(256) gn_finalize_kernel(const __grid_constant_
 }
 
 // y = SiLU(x * a[c] + s[c]); grid (chunks of a frame, frames), 16-byte vectors.  Every thread
-// issues all its loads before any math so that enough bytes are in flight to cover HBM latency.
-constexpr int kApplyVecPerThread = 8;
+// issues all its loads (kept packed: 8 x 16 B of bf16 or 4 x 32 B of fp32) before any math, so that
+// enough bytes are in flight to cover HBM latency at a register count that keeps 4 blocks per SM.
+constexpr int kApplyBytesPerThread = 128;
+template <typename TI> struct ApplyVec;
+template <> struct ApplyVec<__nv_bfloat16> {
+  static constexpr int kVecs = kApplyBytesPerThread / 16;
+  uint4 raw;
+  VAE_DEV void load(const __nv_bfloat16* p) { raw = *reinterpret_cast<const uint4*>(p); }
+  VAE_DEV void get(float* v) const {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+};
+template <> struct ApplyVec<float> {
+  static constexpr int kVecs = kApplyBytesPerThread / 32;
+  float4 a, b;
+  VAE_DEV void load(const float* p) {
+    a = reinterpret_cast<const float4*>(p)[0];
+    b = reinterpret_cast<const float4*>(p)[1];
+  }
+  VAE_DEV void get(float* v) const {
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+};
+
 template <typename TI, typename TO>
-__global__ void __launch_bounds__(256) gn_apply_kernel(const __grid_constant__ GnParams p) {
+__global__ void __launch_bounds__(256, 4) gn_apply_kernel(const __grid_constant__ GnParams p) {
+  constexpr int VPT = ApplyVec<TI>::kVecs;
   extern __shared__ float2 sh_aff[];
   const int frame = blockIdx.y;
   const int b = frame / p.T, t = frame % p.T;
@@ -210,26 +240,28 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const __grid_constant__ G
   TO* yf = static_cast<TO*>(p.y) + (static_cast<int64_t>(b) * p.y_T_alloc + t) * fe;
   const int nvec = static_cast<int>(fe / 8);  // < 2^31 per frame (checked on the host)
   const int cvec = p.C / 8;
-  const int v0 = blockIdx.x * blockDim.x * kApplyVecPerThread + threadIdx.x;
-  float a[kApplyVecPerThread][8];
+  const int v0 = blockIdx.x * blockDim.x * VPT + threadIdx.x;
+  ApplyVec<TI> in[VPT];
 #pragma unroll
-  for (int k = 0; k < kApplyVecPerThread; ++k) {
+  for (int k = 0; k < VPT; ++k) {
     const int v = v0 + k * blockDim.x;
-    if (v < nvec) load8(xf + static_cast<int64_t>(v) * 8, a[k]);
+    if (v < nvec) in[k].load(xf + static_cast<int64_t>(v) * 8);
   }
   __syncthreads();
 #pragma unroll
-  for (int k = 0; k < kApplyVecPerThread; ++k) {
+  for (int k = 0; k < VPT; ++k) {
     const int v = v0 + k * blockDim.x;
     if (v >= nvec) break;
     const int c0 = ((cvec & (cvec - 1)) == 0 ? (v & (cvec - 1)) : (v % cvec)) * 8;
+    float a[8];
+    in[k].get(a);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const float2 m = sh_aff[c0 + e];
-      const float z = fmaf(a[k][e], m.x, m.y);
-      a[k][e] = p.silu ? __fdividef(z, 1.0f + __expf(-z)) : z;
+      const float z = fmaf(a[e], m.x, m.y);
+      a[e] = p.silu ? __fdividef(z, 1.0f + __expf(-z)) : z;
     }
-    store8(yf + static_cast<int64_t>(v) * 8, a[k]);
+    store8(yf + static_cast<int64_t>(v) * 8, a);
   }
 }
 
@@ -291,7 +323,7 @@ cudaError_t launch_gn_apply(const GnArgs& a, cudaStream_t s) {
   if (frames > 65535 || static_cast<int64_t>(a.H) * a.W * a.C / 8 > 0x7fffffffLL) return cudaErrorInvalidValue;
   gn_finalize_kernel<<<static_cast<unsigned>(frames), 256, 0, s>>>(p);
   const int64_t nvec = static_cast<int64_t>(a.H) * a.W * a.C / 8;
-  const int64_t per_block = 256LL * kApplyVecPerThread;
+  const int64_t per_block = 256LL * (a.x_f32 ? ApplyVec<float>::kVecs : ApplyVec<__nv_bfloat16>::kVecs);
   dim3 grid(static_cast<unsigned>((nvec + per_block - 1) / per_block), static_cast<unsigned>(frames));
   const size_t sm = static_cast<size_t>(a.C) * sizeof(float2);
   if (a.x_f32 && a.y_f32) gn_apply_kernel<float, float><<<grid, 256, sm, s>>>(p);
@@ -405,12 +437,17 @@ VAE_DEV float ramp_w(int y, int n, int lo, int hi) {
   return w;
 }
 
-// One block per output row (t, y): warp 0 lists the tiles covering (t, y) in tile order (ballot +
-// prefix count); then each thread takes (plane, 8-pixel vector) jobs and gathers them, tile by tile.
+// One block per output row (t, y).  Warp 0 lists the tiles covering (t, y) in tile order (ballot +
+// prefix count) together with everything that does not depend on x or the plane (row offset, plane
+// stride, t/y weight).  Each thread then owns 8-pixel vectors of the row: it computes the x weights
+// and their reciprocal sum once and gathers every (b, c) plane with them.
+constexpr int kBlendSel = 4;  // covering tiles of one 8-pixel vector kept in registers
 template <typename TT, typename TO>
 __global__ void __launch_bounds__(256) blend_kernel(const __grid_constant__ BlendParams p) {
   __shared__ int list[VAE_MAX_TILES];
   __shared__ float wty[VAE_MAX_TILES];
+  __shared__ long long rowoff[VAE_MAX_TILES];
+  __shared__ long long pstride[VAE_MAX_TILES];
   __shared__ int count;
   const int y = blockIdx.x % p.H;
   const int t = blockIdx.x / p.H;
@@ -429,6 +466,8 @@ __global__ void __launch_bounds__(256) blend_kernel(const __grid_constant__ Blen
         const BlendTile& tl = p.tiles[i];
         list[k] = i;
         wty[k] = ramp_w(t - tl.t0, tl.nt, tl.ovl[0], tl.ovl[1]) * ramp_w(y - tl.h0, tl.nh, tl.ovl[2], tl.ovl[3]);
+        rowoff[k] = (static_cast<long long>(t - tl.t0) * tl.nh + (y - tl.h0)) * tl.nw;
+        pstride[k] = static_cast<long long>(tl.nt) * tl.nh * tl.nw;
       }
       base += __popc(m);
     }
@@ -436,51 +475,104 @@ __global__ void __launch_bounds__(256) blend_kernel(const __grid_constant__ Blen
   }
   __syncthreads();
   const int nk = count;
-  const int nv = (p.W + 7) / 8;
-  const int jobs = p.B * p.C * nv;
+  const int planes = p.B * p.C;
   const int64_t plane_out = static_cast<int64_t>(p.T) * p.H * p.W;
-  for (int job = threadIdx.x; job < jobs; job += blockDim.x) {
-    const int pl = job / nv;
-    const int x0 = (job - pl * nv) * 8;
-    float acc[8], ws[8];
+  const int64_t row_out = (static_cast<int64_t>(t) * p.H + y) * p.W;
+  for (int x0 = threadIdx.x * 8; x0 < p.W; x0 += blockDim.x * 8) {
+    int sel[kBlendSel], lxs[kBlendSel];
+    float w[kBlendSel][8], ws[8];
+    int nsel = 0;
+    bool over = false;  // more covering tiles than registers hold: generic path below
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = ws[e] = 0.f;
+    for (int e = 0; e < 8; ++e) ws[e] = 0.f;
     for (int k = 0; k < nk; ++k) {
       const BlendTile& tl = p.tiles[list[k]];
       const int lx = x0 - tl.w0;
       if (lx + 8 <= 0 || lx >= tl.nw) continue;
-      const TT* r = static_cast<const TT*>(tl.ptr) +
-                    ((static_cast<int64_t>(pl) * tl.nt + (t - tl.t0)) * tl.nh + (y - tl.h0)) * tl.nw;
-      float v[8];
-      const bool full = lx >= 0 && lx + 8 <= tl.nw;
-      if (full && ((lx | tl.nw) & 7) == 0) {
-        load8(r + lx, v);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int xx = lx + e;
-          v[e] = (xx >= 0 && xx < tl.nw) ? to_f<TT>(r[xx]) : 0.f;
-        }
+      if (nsel == kBlendSel) {
+        over = true;
+        break;
       }
-      const float wk = wty[k];
       const int lo = tl.ovl[4], hi = tl.ovl[5];
-      const bool flat = full && lx >= lo && lx + 8 <= tl.nw - hi;  // no ramp inside these 8 pixels
+      const bool flat = lx >= lo && lx + 8 <= tl.nw - hi;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int xx = lx + e;
-        const float w = flat ? wk : ((xx >= 0 && xx < tl.nw) ? wk * ramp_w(xx, tl.nw, lo, hi) : 0.f);
-        acc[e] = fmaf(w, v[e], acc[e]);
-        ws[e] += w;
-      }
-    }
-    TO* orow = static_cast<TO*>(p.out) + pl * plane_out + (static_cast<int64_t>(t) * p.H + y) * p.W;
-    float o[8];
+        const float we = flat ? wty[k] : ((xx >= 0 && xx < tl.nw) ? wty[k] * ramp_w(xx, tl.nw, lo, hi) : 0.f);
+        ws[e] += we;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] = ws[e] > 0.f ? acc[e] / ws[e] : 0.f;
-    if (x0 + 8 <= p.W && (p.W & 7) == 0) {
-      store8(orow + x0, o);
-    } else {
-      for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(o[e]);
+        for (int j = 0; j < kBlendSel; ++j)
+          if (j == nsel) w[j][e] = we;
+      }
+#pragma unroll
+      for (int j = 0; j < kBlendSel; ++j)
+        if (j == nsel) {
+          sel[j] = k;
+          lxs[j] = lx;
+        }
+      ++nsel;
+    }
+    if (over) {
+      // rare: recompute everything per plane over all covering tiles
+      for (int pl = 0; pl < planes; ++pl) {
+        float acc[8], wsum[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = wsum[e] = 0.f;
+        for (int k = 0; k < nk; ++k) {
+          const BlendTile& tl = p.tiles[list[k]];
+          const int lx = x0 - tl.w0;
+          if (lx + 8 <= 0 || lx >= tl.nw) continue;
+          const TT* r = static_cast<const TT*>(tl.ptr) + pl * pstride[k] + rowoff[k];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int xx = lx + e;
+            if (xx < 0 || xx >= tl.nw) continue;
+            const float we = wty[k] * ramp_w(xx, tl.nw, tl.ovl[4], tl.ovl[5]);
+            acc[e] = fmaf(we, to_f<TT>(r[xx]), acc[e]);
+            wsum[e] += we;
+          }
+        }
+        TO* orow = static_cast<TO*>(p.out) + pl * plane_out + row_out;
+        for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(wsum[e] > 0.f ? acc[e] / wsum[e] : 0.f);
+      }
+      continue;
+    }
+    float rinv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) rinv[e] = ws[e] > 0.f ? __frcp_rn(ws[e]) : 0.f;
+    for (int pl = 0; pl < planes; ++pl) {
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+      for (int j = 0; j < kBlendSel; ++j) {
+        if (j >= nsel) break;
+        const int k = sel[j];
+        const BlendTile& tl = p.tiles[list[k]];
+        const int lx = lxs[j];
+        const TT* r = static_cast<const TT*>(tl.ptr) + pl * pstride[k] + rowoff[k];
+        float v[8];
+        if (lx >= 0 && lx + 8 <= tl.nw && ((lx | tl.nw) & 7) == 0) {
+          load8(r + lx, v);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int xx = lx + e;
+            v[e] = (xx >= 0 && xx < tl.nw) ? to_f<TT>(r[xx]) : 0.f;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(w[j][e], v[e], acc[e]);
+      }
+      TO* orow = static_cast<TO*>(p.out) + pl * plane_out + row_out;
+      float o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = acc[e] * rinv[e];
+      if (x0 + 8 <= p.W && (p.W & 7) == 0) {
+        store8(orow + x0, o);
+      } else {
+        for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(o[e]);
+      }
     }
   }
 }
@@ -504,8 +596,8 @@ cudaError_t launch_blend(const void* const* tiles, const vae_tile_t* meta, int n
   const long long nb = static_cast<long long>(d.T) * d.H;
   if (nb == 0) return cudaSuccess;
   dim3 grid(static_cast<unsigned>(nb));
-  const int jobs = d.B * d.C * ((d.W + 7) / 8);
-  const int threads = std::min(256, std::max(32, (jobs + 31) / 32 * 32));
+  const int nv = (d.W + 7) / 8;
+  const int threads = std::min(256, std::max(32, (nv + 31) / 32 * 32));
   if (p.tile_f32 && p.out_f32) blend_kernel<float, float><<<grid, threads, 0, s>>>(p);
   else if (p.tile_f32) blend_kernel<float, __nv_bfloat16><<<grid, threads, 0, s>>>(p);
   else if (p.out_f32) blend_kernel<__nv_bfloat16, float><<<grid, threads, 0, s>>>(p);

@@ -541,7 +541,8 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   p.n_ntiles = (a.N_pad + p.BN - 1) / p.BN;
   p.msub = p.BN <= 128 ? 2 : 1;
   // clusters of 2 share each weight tile (half loaded by each CTA, multicast to both)
-  const bool want_pair = pair_mode_enabled() && p.BN % 16 == 0;
+  // (a batched GEMM has a different B per batch item, so only unbatched GEMMs pair up)
+  const bool want_pair = pair_mode_enabled() && p.BN % 16 == 0 && (a.mode == 0 || a.batch == 1);
   p.tmem_cols = 32;
   while (p.tmem_cols < 2 * p.msub * p.BN) p.tmem_cols <<= 1;  // two accumulators
   if (p.tmem_cols > 512) return cudaErrorInvalidValue;

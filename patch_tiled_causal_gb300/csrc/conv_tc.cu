@@ -524,7 +524,9 @@ int pick_cols(const int* pw, int npw) {
 }  // namespace
 
 namespace {
-bool pair_mode_enabled() { return true; }
+// Pairing was measured to cost more than it saves here (the convs are not bound by L2-to-SMEM
+// bandwidth, and clusters of 2 leave SMs idle where a GPC has an odd count), so it is off.
+bool pair_mode_enabled() { return false; }
 }  // namespace
 
 cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {

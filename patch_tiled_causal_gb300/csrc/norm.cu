@@ -57,6 +57,7 @@ struct GnParams {
   uint32_t* fault;
   int vec_per_px;   // C / 8
   int px_per_iter;  // blockDim / vec_per_px
+  int rows_per_block, n_chunks;  // statistics: rows of one patch band per block, blocks per band
 };
 
 namespace {
@@ -78,16 +79,22 @@ VAE_DEV int quantize(float x, uint32_t* fault) {
 
 }  // namespace
 
-// One block per (frame, image row, patch column): the row segment lies in exactly one patch.
-// GPV = groups met by one 8-channel vector (1 when channels-per-group is a multiple of 8).
+// One block per (frame, patch, chunk of rows_per_block rows of the patch's band): everything a block
+// reads lies in exactly one patch.  GPV = groups met by one 8-channel vector (1 when channels-per-
+// group is a multiple of 8).
 template <int GPV, typename T>
 __global__ void __launch_bounds__(256) gn_stats_kernel(const __grid_constant__ GnParams p) {
   __shared__ unsigned long long sh_s1[1024], sh_lo[1024], sh_hi[1024];
-  const int j = blockIdx.x % p.npw;
-  const int row = blockIdx.x / p.npw;  // frame * H + h
-  const int h = row % p.H;
-  const int frame = row / p.H;
+  int rest = blockIdx.x;
+  const int chunk = rest % p.n_chunks;
+  rest /= p.n_chunks;
+  const int j = rest % p.npw;
+  rest /= p.npw;
+  const int i = rest % p.nph;
+  const int frame = rest / p.nph;
   const int fb = frame / p.T, ft = frame % p.T;
+  const int h_beg = p.ph_edges[i] + chunk * p.rows_per_block;
+  const int h_stop = min(p.ph_edges[i + 1], h_beg + p.rows_per_block);
   for (int g = threadIdx.x; g < p.groups; g += blockDim.x) sh_s1[g] = sh_lo[g] = sh_hi[g] = 0ull;
   __syncthreads();
 
@@ -95,12 +102,12 @@ __global__ void __launch_bounds__(256) gn_stats_kernel(const __grid_constant__ G
   const int pxo = threadIdx.x / p.vec_per_px;
   const int c0 = vid * 8;
   const int w_beg = p.pw_edges[j], w_end = p.pw_edges[j + 1];
-  const T* xr = static_cast<const T*>(p.x) + ((static_cast<int64_t>(fb) * p.x_T_alloc + ft) * p.H + h) * p.W * p.C;
   long long s1[GPV];
   unsigned long long lo[GPV], hi[GPV];
 #pragma unroll
   for (int k = 0; k < GPV; ++k) { s1[k] = 0; lo[k] = hi[k] = 0ull; }
-  if (threadIdx.x < p.vec_per_px * p.px_per_iter) {
+  for (int h = h_beg; h < h_stop && threadIdx.x < p.vec_per_px * p.px_per_iter; ++h) {
+    const T* xr = static_cast<const T*>(p.x) + ((static_cast<int64_t>(fb) * p.x_T_alloc + ft) * p.H + h) * p.W * p.C;
     // four pixels' vectors are loaded before any of them is summed (bytes in flight)
     for (int w = w_beg + pxo; w < w_end; w += 4 * p.px_per_iter) {
       float v[4][8];
@@ -147,11 +154,8 @@ __global__ void __launch_bounds__(256) gn_stats_kernel(const __grid_constant__ G
     }
   }
   __syncthreads();
-  // this block's segment belongs to patch (band of h, j)
-  int i = 0;
-  while (i + 1 < p.nph && p.ph_edges[i + 1] <= h) ++i;
   const int patch = i * p.npw + j;
-  const int b = frame / p.T, t = frame % p.T;
+  const int b = fb, t = ft;
   for (int g = threadIdx.x; g < p.groups; g += blockDim.x) {
     GnPartial* d = p.parts + ((static_cast<int64_t>(patch) * p.B + b) * p.T + t) * p.groups + g;
     const unsigned long long a1 = sh_s1[g], alo = sh_lo[g], ahi = sh_hi[g];
@@ -296,7 +300,12 @@ cudaError_t launch_gn_stats(const GnArgs& a, cudaStream_t s) {
   if (!fill_gn(p, a)) return cudaErrorInvalidValue;
   cudaError_t e = cudaMemsetAsync(a.partials, 0, gn_partials_bytes(a.nph, a.npw, a.B, a.T, a.groups), s);
   if (e != cudaSuccess) return e;
-  const long long nb = static_cast<long long>(a.B) * a.T * a.H * a.npw;
+  int band_max = 1, pw_max = 1;
+  for (int i = 0; i < a.nph; ++i) band_max = std::max(band_max, a.ph_edges[i + 1] - a.ph_edges[i]);
+  for (int j = 0; j < a.npw; ++j) pw_max = std::max(pw_max, a.pw_edges[j + 1] - a.pw_edges[j]);
+  p.rows_per_block = std::max(1, static_cast<int>(65536 / (static_cast<int64_t>(pw_max) * a.C)));
+  p.n_chunks = (band_max + p.rows_per_block - 1) / p.rows_per_block;
+  const long long nb = static_cast<long long>(a.B) * a.T * a.nph * a.npw * p.n_chunks;
   if (nb == 0) return cudaSuccess;
   const int threads = std::max(p.vec_per_px * p.px_per_iter, 32);
   if (threads > 1024) return cudaErrorInvalidValue;
@@ -438,16 +447,18 @@ VAE_DEV float ramp_w(int y, int n, int lo, int hi) {
 }
 
 // One block per output row (t, y).  Warp 0 lists the tiles covering (t, y) in tile order (ballot +
-// prefix count) together with everything that does not depend on x or the plane (row offset, plane
-// stride, t/y weight).  Each thread then owns 8-pixel vectors of the row: it computes the x weights
-// and their reciprocal sum once and gathers every (b, c) plane with them.
-constexpr int kBlendSel = 4;  // covering tiles of one 8-pixel vector kept in registers
+// prefix count) and stores, per listed tile, what does not depend on x or the plane (row offset,
+// plane stride, x extent and overlaps, t/y weight).  Threads then take (plane, 8-pixel vector) jobs,
+// consecutive threads on consecutive vectors of one plane, and gather from the listed tiles.
+struct RowTile {
+  const void* ptr;
+  long long rowoff, pstride;
+  int w0, nw, lo, hi;
+  float wty;
+};
 template <typename TT, typename TO>
 __global__ void __launch_bounds__(256) blend_kernel(const __grid_constant__ BlendParams p) {
-  __shared__ int list[VAE_MAX_TILES];
-  __shared__ float wty[VAE_MAX_TILES];
-  __shared__ long long rowoff[VAE_MAX_TILES];
-  __shared__ long long pstride[VAE_MAX_TILES];
+  __shared__ RowTile rt[VAE_MAX_TILES];
   __shared__ int count;
   const int y = blockIdx.x % p.H;
   const int t = blockIdx.x / p.H;
@@ -464,10 +475,16 @@ __global__ void __launch_bounds__(256) blend_kernel(const __grid_constant__ Blen
       if (cov) {
         const int k = base + __popc(m & ((1u << threadIdx.x) - 1u));
         const BlendTile& tl = p.tiles[i];
-        list[k] = i;
-        wty[k] = ramp_w(t - tl.t0, tl.nt, tl.ovl[0], tl.ovl[1]) * ramp_w(y - tl.h0, tl.nh, tl.ovl[2], tl.ovl[3]);
-        rowoff[k] = (static_cast<long long>(t - tl.t0) * tl.nh + (y - tl.h0)) * tl.nw;
-        pstride[k] = static_cast<long long>(tl.nt) * tl.nh * tl.nw;
+        RowTile r;
+        r.ptr = tl.ptr;
+        r.rowoff = (static_cast<long long>(t - tl.t0) * tl.nh + (y - tl.h0)) * tl.nw;
+        r.pstride = static_cast<long long>(tl.nt) * tl.nh * tl.nw;
+        r.w0 = tl.w0;
+        r.nw = tl.nw;
+        r.lo = tl.ovl[4];
+        r.hi = tl.ovl[5];
+        r.wty = ramp_w(t - tl.t0, tl.nt, tl.ovl[0], tl.ovl[1]) * ramp_w(y - tl.h0, tl.nh, tl.ovl[2], tl.ovl[3]);
+        rt[k] = r;
       }
       base += __popc(m);
     }
@@ -475,104 +492,56 @@ __global__ void __launch_bounds__(256) blend_kernel(const __grid_constant__ Blen
   }
   __syncthreads();
   const int nk = count;
-  const int planes = p.B * p.C;
+  const int nv = (p.W + 7) / 8;
+  const int jobs = p.B * p.C * nv;
   const int64_t plane_out = static_cast<int64_t>(p.T) * p.H * p.W;
   const int64_t row_out = (static_cast<int64_t>(t) * p.H + y) * p.W;
-  for (int x0 = threadIdx.x * 8; x0 < p.W; x0 += blockDim.x * 8) {
-    int sel[kBlendSel], lxs[kBlendSel];
-    float w[kBlendSel][8], ws[8];
-    int nsel = 0;
-    bool over = false;  // more covering tiles than registers hold: generic path below
+  for (int job = threadIdx.x; job < jobs; job += blockDim.x) {
+    const int pl = job / nv;
+    const int x0 = (job - pl * nv) * 8;
+    float acc[8], ws[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) ws[e] = 0.f;
+    for (int e = 0; e < 8; ++e) acc[e] = ws[e] = 0.f;
     for (int k = 0; k < nk; ++k) {
-      const BlendTile& tl = p.tiles[list[k]];
-      const int lx = x0 - tl.w0;
-      if (lx + 8 <= 0 || lx >= tl.nw) continue;
-      if (nsel == kBlendSel) {
-        over = true;
-        break;
-      }
-      const int lo = tl.ovl[4], hi = tl.ovl[5];
-      const bool flat = lx >= lo && lx + 8 <= tl.nw - hi;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int xx = lx + e;
-        const float we = flat ? wty[k] : ((xx >= 0 && xx < tl.nw) ? wty[k] * ramp_w(xx, tl.nw, lo, hi) : 0.f);
-        ws[e] += we;
-#pragma unroll
-        for (int j = 0; j < kBlendSel; ++j)
-          if (j == nsel) w[j][e] = we;
-      }
-#pragma unroll
-      for (int j = 0; j < kBlendSel; ++j)
-        if (j == nsel) {
-          sel[j] = k;
-          lxs[j] = lx;
-        }
-      ++nsel;
-    }
-    if (over) {
-      // rare: recompute everything per plane over all covering tiles
-      for (int pl = 0; pl < planes; ++pl) {
-        float acc[8], wsum[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = wsum[e] = 0.f;
-        for (int k = 0; k < nk; ++k) {
-          const BlendTile& tl = p.tiles[list[k]];
-          const int lx = x0 - tl.w0;
-          if (lx + 8 <= 0 || lx >= tl.nw) continue;
-          const TT* r = static_cast<const TT*>(tl.ptr) + pl * pstride[k] + rowoff[k];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int xx = lx + e;
-            if (xx < 0 || xx >= tl.nw) continue;
-            const float we = wty[k] * ramp_w(xx, tl.nw, tl.ovl[4], tl.ovl[5]);
-            acc[e] = fmaf(we, to_f<TT>(r[xx]), acc[e]);
-            wsum[e] += we;
-          }
-        }
-        TO* orow = static_cast<TO*>(p.out) + pl * plane_out + row_out;
-        for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(wsum[e] > 0.f ? acc[e] / wsum[e] : 0.f);
-      }
-      continue;
-    }
-    float rinv[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) rinv[e] = ws[e] > 0.f ? __frcp_rn(ws[e]) : 0.f;
-    for (int pl = 0; pl < planes; ++pl) {
-      float acc[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll
-      for (int j = 0; j < kBlendSel; ++j) {
-        if (j >= nsel) break;
-        const int k = sel[j];
-        const BlendTile& tl = p.tiles[list[k]];
-        const int lx = lxs[j];
-        const TT* r = static_cast<const TT*>(tl.ptr) + pl * pstride[k] + rowoff[k];
-        float v[8];
-        if (lx >= 0 && lx + 8 <= tl.nw && ((lx | tl.nw) & 7) == 0) {
-          load8(r + lx, v);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int xx = lx + e;
-            v[e] = (xx >= 0 && xx < tl.nw) ? to_f<TT>(r[xx]) : 0.f;
-          }
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = fmaf(w[j][e], v[e], acc[e]);
-      }
-      TO* orow = static_cast<TO*>(p.out) + pl * plane_out + row_out;
-      float o[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = acc[e] * rinv[e];
-      if (x0 + 8 <= p.W && (p.W & 7) == 0) {
-        store8(orow + x0, o);
+      const RowTile& r = rt[k];
+      const int lx = x0 - r.w0;
+      if (lx + 8 <= 0 || lx >= r.nw) continue;
+      const TT* src = static_cast<const TT*>(r.ptr) + pl * r.pstride + r.rowoff;
+      float v[8];
+      const bool full = lx >= 0 && lx + 8 <= r.nw;
+      if (full && ((lx | r.nw) & 7) == 0) {
+        load8(src + lx, v);
       } else {
-        for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(o[e]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int xx = lx + e;
+          v[e] = (xx >= 0 && xx < r.nw) ? to_f<TT>(src[xx]) : 0.f;
+        }
       }
+      if (full && lx >= r.lo && lx + 8 <= r.nw - r.hi) {  // no ramp across these 8 pixels
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          acc[e] = fmaf(r.wty, v[e], acc[e]);
+          ws[e] += r.wty;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int xx = lx + e;
+          const float w = (xx >= 0 && xx < r.nw) ? r.wty * ramp_w(xx, r.nw, r.lo, r.hi) : 0.f;
+          acc[e] = fmaf(w, v[e], acc[e]);
+          ws[e] += w;
+        }
+      }
+    }
+    TO* orow = static_cast<TO*>(p.out) + pl * plane_out + row_out;
+    float o[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = ws[e] > 0.f ? __fdividef(acc[e], ws[e]) : 0.f;
+    if (x0 + 8 <= p.W && (p.W & 7) == 0) {
+      store8(orow + x0, o);
+    } else {
+      for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(o[e]);
     }
   }
 }
@@ -596,8 +565,8 @@ cudaError_t launch_blend(const void* const* tiles, const vae_tile_t* meta, int n
   const long long nb = static_cast<long long>(d.T) * d.H;
   if (nb == 0) return cudaSuccess;
   dim3 grid(static_cast<unsigned>(nb));
-  const int nv = (d.W + 7) / 8;
-  const int threads = std::min(256, std::max(32, (nv + 31) / 32 * 32));
+  const int jobs = d.B * d.C * ((d.W + 7) / 8);
+  const int threads = std::min(256, std::max(32, (jobs + 31) / 32 * 32));
   if (p.tile_f32 && p.out_f32) blend_kernel<float, float><<<grid, threads, 0, s>>>(p);
   else if (p.tile_f32) blend_kernel<float, __nv_bfloat16><<<grid, threads, 0, s>>>(p);
   else if (p.out_f32) blend_kernel<__nv_bfloat16, float><<<grid, threads, 0, s>>>(p);

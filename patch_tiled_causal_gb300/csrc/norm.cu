@@ -446,8 +446,8 @@ VAE_DEV float ramp_w(int y, int n, int lo, int hi) {
   return w;
 }
 
-// One block per output row (t, y).  Warp 0 lists the tiles covering (t, y) in tile order (ballot +
-// prefix count) and stores, per listed tile, what does not depend on x or the plane (row offset,
+// One block per output row (t, y).  Thread 0 lists the tiles covering (t, y) in tile order and stores,
+// per listed tile, what does not depend on x or the plane (row offset,
 // plane stride, x extent and overlaps, t/y weight).  Threads then take (plane, 8-pixel vector) jobs,
 // consecutive threads on consecutive vectors of one plane, and gather from the listed tiles.
 struct RowTile {
@@ -462,33 +462,25 @@ __global__ void __launch_bounds__(256) blend_kernel(const __grid_constant__ Blen
   __shared__ int count;
   const int y = blockIdx.x % p.H;
   const int t = blockIdx.x / p.H;
-  if (threadIdx.x < 32) {
-    int base = 0;
-    for (int i0 = 0; i0 < p.n; i0 += 32) {
-      const int i = i0 + threadIdx.x;
-      bool cov = false;
-      if (i < p.n) {
-        const BlendTile& tl = p.tiles[i];
-        cov = t >= tl.t0 && t < tl.t0 + tl.nt && y >= tl.h0 && y < tl.h0 + tl.nh;
-      }
-      const unsigned m = __ballot_sync(0xffffffffu, cov);
-      if (cov) {
-        const int k = base + __popc(m & ((1u << threadIdx.x) - 1u));
-        const BlendTile& tl = p.tiles[i];
-        RowTile r;
-        r.ptr = tl.ptr;
-        r.rowoff = (static_cast<long long>(t - tl.t0) * tl.nh + (y - tl.h0)) * tl.nw;
-        r.pstride = static_cast<long long>(tl.nt) * tl.nh * tl.nw;
-        r.w0 = tl.w0;
-        r.nw = tl.nw;
-        r.lo = tl.ovl[4];
-        r.hi = tl.ovl[5];
-        r.wty = ramp_w(t - tl.t0, tl.nt, tl.ovl[0], tl.ovl[1]) * ramp_w(y - tl.h0, tl.nh, tl.ovl[2], tl.ovl[3]);
-        rt[k] = r;
-      }
-      base += __popc(m);
+  if (threadIdx.x == 0) {
+    // one thread walks the table so that every parameter-space read is warp-uniform (divergent
+    // reads of kernel parameters are serialised)
+    int k = 0;
+    for (int i = 0; i < p.n; ++i) {
+      const BlendTile& tl = p.tiles[i];
+      if (t < tl.t0 || t >= tl.t0 + tl.nt || y < tl.h0 || y >= tl.h0 + tl.nh) continue;
+      RowTile r;
+      r.ptr = tl.ptr;
+      r.rowoff = (static_cast<long long>(t - tl.t0) * tl.nh + (y - tl.h0)) * tl.nw;
+      r.pstride = static_cast<long long>(tl.nt) * tl.nh * tl.nw;
+      r.w0 = tl.w0;
+      r.nw = tl.nw;
+      r.lo = tl.ovl[4];
+      r.hi = tl.ovl[5];
+      r.wty = ramp_w(t - tl.t0, tl.nt, tl.ovl[0], tl.ovl[1]) * ramp_w(y - tl.h0, tl.nh, tl.ovl[2], tl.ovl[3]);
+      rt[k++] = r;
     }
-    if (threadIdx.x == 0) count = base;
+    count = k;
   }
   __syncthreads();
   const int nk = count;

@@ -456,9 +456,13 @@ struct RowTile {
   int w0, nw, lo, hi;
   float wty;
 };
+constexpr int kCovMax = 4;     // overlapping tiles remembered per 8-pixel vector
+constexpr int kMaxVecs = 1024; // vectors per row with a coverage entry (wider rows scan for the rest)
 template <typename TT, typename TO>
 __global__ void __launch_bounds__(256) blend_kernel(const __grid_constant__ BlendParams p) {
   __shared__ RowTile rt[VAE_MAX_TILES];
+  __shared__ unsigned short cov[kMaxVecs][kCovMax];
+  __shared__ unsigned char ncov[kMaxVecs];
   __shared__ int count;
   const int y = blockIdx.x % p.H;
   const int t = blockIdx.x / p.H;
@@ -485,16 +489,33 @@ __global__ void __launch_bounds__(256) blend_kernel(const __grid_constant__ Blen
   __syncthreads();
   const int nk = count;
   const int nv = (p.W + 7) / 8;
+  // per 8-pixel vector: the listed tiles it overlaps (up to kCovMax; more -> scan all of them)
+  for (int v = threadIdx.x; v < nv && v < kMaxVecs; v += blockDim.x) {
+    const int x0 = v * 8;
+    int c = 0;
+    for (int k = 0; k < nk; ++k) {
+      const int lx = x0 - rt[k].w0;
+      if (lx + 8 <= 0 || lx >= rt[k].nw) continue;
+      if (c < kCovMax) cov[v][c] = static_cast<unsigned short>(k);
+      ++c;
+    }
+    ncov[v] = static_cast<unsigned char>(c > kCovMax ? 255 : c);
+  }
+  __syncthreads();
   const int jobs = p.B * p.C * nv;
   const int64_t plane_out = static_cast<int64_t>(p.T) * p.H * p.W;
   const int64_t row_out = (static_cast<int64_t>(t) * p.H + y) * p.W;
   for (int job = threadIdx.x; job < jobs; job += blockDim.x) {
     const int pl = job / nv;
-    const int x0 = (job - pl * nv) * 8;
+    const int vi = job - pl * nv;
+    const int x0 = vi * 8;
     float acc[8], ws[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = ws[e] = 0.f;
-    for (int k = 0; k < nk; ++k) {
+    const int nc = vi < kMaxVecs ? ncov[vi] : 255;
+    const int nloop = nc == 255 ? nk : nc;
+    for (int jj = 0; jj < nloop; ++jj) {
+      const int k = nc == 255 ? jj : cov[vi][jj];
       const RowTile& r = rt[k];
       const int lx = x0 - r.w0;
       if (lx + 8 <= 0 || lx >= r.nw) continue;

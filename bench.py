@@ -171,6 +171,27 @@ def run_reference(args, cfg):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------------------------- multi-rank
+def latent_seed(rank: int) -> int:
+    """Each rank decodes its own video: the latent of rank r is drawn from seed r."""
+    return rank
+
+
+def max_over_ranks(seconds: float, dist=None, device="cpu") -> float:
+    """The timed region's length is the slowest rank's (all_reduce MAX; identity on one rank)."""
+    if dist is None:
+        return seconds
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput(frame_px_per_rank: int, steps: int, world: int, seconds: float) -> float:
+    """Whole-job Mframe-px/s: every rank decodes steps videos of frame_px_per_rank each."""
+    return frame_px_per_rank * steps * world / seconds / 1e6
+
+
 # ------------------------------------------------------------------------------------- GPU arm
 def main():
     ap = argparse.ArgumentParser()
@@ -219,7 +240,7 @@ def main():
 
     nph, npw = (int(v) for v in args.patches.lower().split("x"))
     params = synth.draw_params(cfg, 0)
-    latent_np = synth.draw_latent(cfg, seed=rank)
+    latent_np = synth.draw_latent(cfg, seed=latent_seed(rank))
     dec = vaedec.Decoder(cfg, params, vaedec.VAE_BF16)
     del params
     dec.reserve(cfg.latent_shape, nph, npw)
@@ -254,16 +275,12 @@ def main():
     prof = dec.profile_read()
     dec.profile(False)
     step_ms = [a.elapsed_time(b) for a, b in evs]
-    t_local = sum(step_ms) / 1000.0
-    t = torch.tensor([t_local], device="cuda")
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    t_max = float(t.item())
+    t_max = max_over_ranks(sum(step_ms) / 1000.0, dist, "cuda")
     code, msg = vaedec.last_error(dec.h)
     if code:
         raise RuntimeError(f"decode failed in the timed region: {msg}")
     frame_px = out.shape[0] * out.shape[2] * out.shape[3] * out.shape[4]
-    value = frame_px * args.steps * world / t_max / 1e6
+    value = throughput(frame_px, args.steps, world, t_max)
     launches = sum(v["launches"] for v in prof.values()) // args.steps
 
     # ---- end to end through the public API: pinned host latent in, pinned host pixels out
@@ -284,11 +301,8 @@ def main():
         h_out.copy_(out, non_blocking=True)
         b.record(stream)
     barrier()
-    e_local = sum(a.elapsed_time(b) for a, b in eev) / 1000.0
-    te = torch.tensor([e_local], device="cuda")
-    if dist is not None:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_value = frame_px * args.steps * world / float(te.item()) / 1e6
+    e2e_value = throughput(frame_px, args.steps, world,
+                           max_over_ranks(sum(a.elapsed_time(b) for a, b in eev) / 1000.0, dist, "cuda"))
 
     kernels = {}
     for k, v in sorted(prof.items(), key=lambda kv: -kv[1]["ms"]):

@@ -446,79 +446,87 @@ VAE_DEV float ramp_w(int y, int n, int lo, int hi) {
   return w;
 }
 
-// One block per output row (t, y).  Thread 0 lists the tiles covering (t, y) in tile order and stores,
-// per listed tile, what does not depend on x or the plane (row offset,
-// plane stride, x extent and overlaps, t/y weight).  Threads then take (plane, 8-pixel vector) jobs,
-// consecutive threads on consecutive vectors of one plane, and gather from the listed tiles.
+// One warp per output row (t, y), 8 rows per block, no block-wide synchronisation.  The warp lists
+// the tiles covering (t, y) in tile order (32 tiles per ballot round) together with everything that
+// does not depend on x or the plane (row offset, plane stride, x extent, overlaps, t/y weight); its
+// lanes then take (plane, 8-pixel vector) jobs, consecutive lanes on consecutive vectors of one
+// plane, and gather from the listed tiles.
 struct RowTile {
   const void* ptr;
   long long rowoff, pstride;
   int w0, nw, lo, hi;
   float wty;
 };
-constexpr int kCovMax = 4;     // overlapping tiles remembered per 8-pixel vector
-constexpr int kMaxVecs = 1024; // vectors per row with a coverage entry (wider rows scan for the rest)
+constexpr int kBlendRowsPerBlock = 8;
+constexpr int kRowList = 64;  // covering tiles of one row kept in shared memory
 template <typename TT, typename TO>
-__global__ void __launch_bounds__(256) blend_kernel(const __grid_constant__ BlendParams p) {
-  __shared__ RowTile rt[VAE_MAX_TILES];
-  __shared__ unsigned short cov[kMaxVecs][kCovMax];
-  __shared__ unsigned char ncov[kMaxVecs];
-  __shared__ int count;
-  const int y = blockIdx.x % p.H;
-  const int t = blockIdx.x / p.H;
-  if (threadIdx.x == 0) {
-    // one thread walks the table so that every parameter-space read is warp-uniform (divergent
-    // reads of kernel parameters are serialised)
-    int k = 0;
-    for (int i = 0; i < p.n; ++i) {
+__global__ void __launch_bounds__(32 * kBlendRowsPerBlock) blend_kernel(const __grid_constant__ BlendParams p) {
+  __shared__ RowTile rts[kBlendRowsPerBlock][kRowList];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rows_per_t = (p.H + kBlendRowsPerBlock - 1) / kBlendRowsPerBlock;
+  const int t = blockIdx.x / rows_per_t;
+  const int y = (blockIdx.x - t * rows_per_t) * kBlendRowsPerBlock + warp;
+  if (y >= p.H) return;
+  RowTile* rt = rts[warp];
+  int nk = 0;
+  for (int i0 = 0; i0 < p.n; i0 += 32) {
+    const int i = i0 + lane;
+    bool cov = false;
+    if (i < p.n) {
       const BlendTile& tl = p.tiles[i];
-      if (t < tl.t0 || t >= tl.t0 + tl.nt || y < tl.h0 || y >= tl.h0 + tl.nh) continue;
-      RowTile r;
-      r.ptr = tl.ptr;
-      r.rowoff = (static_cast<long long>(t - tl.t0) * tl.nh + (y - tl.h0)) * tl.nw;
-      r.pstride = static_cast<long long>(tl.nt) * tl.nh * tl.nw;
-      r.w0 = tl.w0;
-      r.nw = tl.nw;
-      r.lo = tl.ovl[4];
-      r.hi = tl.ovl[5];
-      r.wty = ramp_w(t - tl.t0, tl.nt, tl.ovl[0], tl.ovl[1]) * ramp_w(y - tl.h0, tl.nh, tl.ovl[2], tl.ovl[3]);
-      rt[k++] = r;
+      cov = t >= tl.t0 && t < tl.t0 + tl.nt && y >= tl.h0 && y < tl.h0 + tl.nh;
     }
-    count = k;
+    const unsigned m = __ballot_sync(0xffffffffu, cov);
+    if (cov) {
+      const int k = nk + __popc(m & ((1u << lane) - 1u));
+      if (k < kRowList) {
+        const BlendTile& tl = p.tiles[i];
+        RowTile r;
+        r.ptr = tl.ptr;
+        r.rowoff = (static_cast<long long>(t - tl.t0) * tl.nh + (y - tl.h0)) * tl.nw;
+        r.pstride = static_cast<long long>(tl.nt) * tl.nh * tl.nw;
+        r.w0 = tl.w0;
+        r.nw = tl.nw;
+        r.lo = tl.ovl[4];
+        r.hi = tl.ovl[5];
+        r.wty = ramp_w(t - tl.t0, tl.nt, tl.ovl[0], tl.ovl[1]) * ramp_w(y - tl.h0, tl.nh, tl.ovl[2], tl.ovl[3]);
+        rt[k] = r;
+      }
+    }
+    nk += __popc(m);
   }
-  __syncthreads();
-  const int nk = count;
+  __syncwarp();
+  const bool spill = nk > kRowList;  // more covering tiles than listed: read them from the table
   const int nv = (p.W + 7) / 8;
-  // per 8-pixel vector: the listed tiles it overlaps (up to kCovMax; more -> scan all of them)
-  for (int v = threadIdx.x; v < nv && v < kMaxVecs; v += blockDim.x) {
-    const int x0 = v * 8;
-    int c = 0;
-    for (int k = 0; k < nk; ++k) {
-      const int lx = x0 - rt[k].w0;
-      if (lx + 8 <= 0 || lx >= rt[k].nw) continue;
-      if (c < kCovMax) cov[v][c] = static_cast<unsigned short>(k);
-      ++c;
-    }
-    ncov[v] = static_cast<unsigned char>(c > kCovMax ? 255 : c);
-  }
-  __syncthreads();
   const int jobs = p.B * p.C * nv;
   const int64_t plane_out = static_cast<int64_t>(p.T) * p.H * p.W;
   const int64_t row_out = (static_cast<int64_t>(t) * p.H + y) * p.W;
-  for (int job = threadIdx.x; job < jobs; job += blockDim.x) {
+  for (int job = lane; job < jobs; job += 32) {
     const int pl = job / nv;
-    const int vi = job - pl * nv;
-    const int x0 = vi * 8;
+    const int x0 = (job - pl * nv) * 8;
     float acc[8], ws[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = ws[e] = 0.f;
-    const int nc = vi < kMaxVecs ? ncov[vi] : 255;
-    const int nloop = nc == 255 ? nk : nc;
-    for (int jj = 0; jj < nloop; ++jj) {
-      const int k = nc == 255 ? jj : cov[vi][jj];
-      const RowTile& r = rt[k];
+    const int nloop = spill ? p.n : nk;
+    for (int k = 0; k < nloop; ++k) {
+      RowTile r;
+      if (!spill) {
+        if (x0 + 8 <= rt[k].w0 || x0 >= rt[k].w0 + rt[k].nw) continue;  // cheap reject
+        r = rt[k];
+      } else {
+        const BlendTile& tl = p.tiles[k];
+        if (t < tl.t0 || t >= tl.t0 + tl.nt || y < tl.h0 || y >= tl.h0 + tl.nh) continue;
+        if (x0 + 8 <= tl.w0 || x0 >= tl.w0 + tl.nw) continue;
+        r.ptr = tl.ptr;
+        r.rowoff = (static_cast<long long>(t - tl.t0) * tl.nh + (y - tl.h0)) * tl.nw;
+        r.pstride = static_cast<long long>(tl.nt) * tl.nh * tl.nw;
+        r.w0 = tl.w0;
+        r.nw = tl.nw;
+        r.lo = tl.ovl[4];
+        r.hi = tl.ovl[5];
+        r.wty = ramp_w(t - tl.t0, tl.nt, tl.ovl[0], tl.ovl[1]) * ramp_w(y - tl.h0, tl.nh, tl.ovl[2], tl.ovl[3]);
+      }
       const int lx = x0 - r.w0;
-      if (lx + 8 <= 0 || lx >= r.nw) continue;
       const TT* src = static_cast<const TT*>(r.ptr) + pl * r.pstride + r.rowoff;
       float v[8];
       const bool full = lx >= 0 && lx + 8 <= r.nw;
@@ -575,11 +583,10 @@ cudaError_t launch_blend(const void* const* tiles, const vae_tile_t* meta, int n
     t.w0 = meta[i].pix[4]; t.nw = meta[i].pix[5];
     for (int k = 0; k < 6; ++k) t.ovl[k] = static_cast<unsigned short>(meta[i].ovl[k]);
   }
-  const long long nb = static_cast<long long>(d.T) * d.H;
+  const long long nb = static_cast<long long>(d.T) * ((d.H + kBlendRowsPerBlock - 1) / kBlendRowsPerBlock);
   if (nb == 0) return cudaSuccess;
   dim3 grid(static_cast<unsigned>(nb));
-  const int jobs = d.B * d.C * ((d.W + 7) / 8);
-  const int threads = std::min(256, std::max(32, (jobs + 31) / 32 * 32));
+  const int threads = 32 * kBlendRowsPerBlock;
   if (p.tile_f32 && p.out_f32) blend_kernel<float, float><<<grid, threads, 0, s>>>(p);
   else if (p.tile_f32) blend_kernel<float, __nv_bfloat16><<<grid, threads, 0, s>>>(p);
   else if (p.out_f32) blend_kernel<__nv_bfloat16, float><<<grid, threads, 0, s>>>(p);

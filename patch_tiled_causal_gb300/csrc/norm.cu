@@ -501,68 +501,115 @@ __global__ void __launch_bounds__(32 * kBlendRowsPerBlock) blend_kernel(const __
   const int jobs = p.B * p.C * nv;
   const int64_t plane_out = static_cast<int64_t>(p.T) * p.H * p.W;
   const int64_t row_out = (static_cast<int64_t>(t) * p.H + y) * p.W;
-  for (int job = lane; job < jobs; job += 32) {
-    const int pl = job / nv;
-    const int x0 = (job - pl * nv) * 8;
-    float acc[8], ws[8];
+  constexpr int kJ = 4;  // jobs per lane whose loads are all issued before any is summed
+  for (int job0 = lane; job0 < jobs; job0 += 32 * kJ) {
+    // phase 1: for each job find (at most 2) covering tiles with whole aligned vectors and load them
+    ApplyVec<TT> raw[kJ][2];
+    int sel[kJ][2];
+    int nsel[kJ];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = ws[e] = 0.f;
-    const int nloop = spill ? p.n : nk;
-    for (int k = 0; k < nloop; ++k) {
-      RowTile r;
-      if (!spill) {
-        if (x0 + 8 <= rt[k].w0 || x0 >= rt[k].w0 + rt[k].nw) continue;  // cheap reject
-        r = rt[k];
-      } else {
-        const BlendTile& tl = p.tiles[k];
-        if (t < tl.t0 || t >= tl.t0 + tl.nt || y < tl.h0 || y >= tl.h0 + tl.nh) continue;
-        if (x0 + 8 <= tl.w0 || x0 >= tl.w0 + tl.nw) continue;
-        r.ptr = tl.ptr;
-        r.rowoff = (static_cast<long long>(t - tl.t0) * tl.nh + (y - tl.h0)) * tl.nw;
-        r.pstride = static_cast<long long>(tl.nt) * tl.nh * tl.nw;
-        r.w0 = tl.w0;
-        r.nw = tl.nw;
-        r.lo = tl.ovl[4];
-        r.hi = tl.ovl[5];
-        r.wty = ramp_w(t - tl.t0, tl.nt, tl.ovl[0], tl.ovl[1]) * ramp_w(y - tl.h0, tl.nh, tl.ovl[2], tl.ovl[3]);
+    for (int u = 0; u < kJ; ++u) {
+      nsel[u] = 0;
+      const int job = job0 + 32 * u;
+      if (job >= jobs || spill) {
+        nsel[u] = job >= jobs ? 0 : -1;
+        continue;
       }
-      const int lx = x0 - r.w0;
-      const TT* src = static_cast<const TT*>(r.ptr) + pl * r.pstride + r.rowoff;
-      float v[8];
-      const bool full = lx >= 0 && lx + 8 <= r.nw;
-      if (full && ((lx | r.nw) & 7) == 0) {
-        load8(src + lx, v);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int xx = lx + e;
-          v[e] = (xx >= 0 && xx < r.nw) ? to_f<TT>(src[xx]) : 0.f;
+      const int pl = job / nv;
+      const int x0 = (job - pl * nv) * 8;
+      for (int k = 0; k < nk; ++k) {
+        const int lx = x0 - rt[k].w0;
+        if (lx + 8 <= 0 || lx >= rt[k].nw) continue;
+        const bool aligned = lx >= 0 && lx + 8 <= rt[k].nw && ((lx | rt[k].nw) & 7) == 0;
+        if (!aligned || nsel[u] == 2) {
+          nsel[u] = -1;  // generic path
+          break;
         }
-      }
-      if (full && lx >= r.lo && lx + 8 <= r.nw - r.hi) {  // no ramp across these 8 pixels
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          acc[e] = fmaf(r.wty, v[e], acc[e]);
-          ws[e] += r.wty;
+        const TT* src = static_cast<const TT*>(rt[k].ptr) + pl * rt[k].pstride + rt[k].rowoff + lx;
+        if (nsel[u] == 0) {  // constant register indices only (no local-memory arrays)
+          raw[u][0].load(src);
+          sel[u][0] = k;
+        } else {
+          raw[u][1].load(src);
+          sel[u][1] = k;
         }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int xx = lx + e;
-          const float w = (xx >= 0 && xx < r.nw) ? r.wty * ramp_w(xx, r.nw, r.lo, r.hi) : 0.f;
-          acc[e] = fmaf(w, v[e], acc[e]);
-          ws[e] += w;
-        }
+        ++nsel[u];
       }
     }
-    TO* orow = static_cast<TO*>(p.out) + pl * plane_out + row_out;
-    float o[8];
+    // phase 2: weights and sums
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] = ws[e] > 0.f ? __fdividef(acc[e], ws[e]) : 0.f;
-    if (x0 + 8 <= p.W && (p.W & 7) == 0) {
-      store8(orow + x0, o);
-    } else {
-      for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(o[e]);
+    for (int u = 0; u < kJ; ++u) {
+      const int job = job0 + 32 * u;
+      if (job >= jobs) break;
+      const int pl = job / nv;
+      const int x0 = (job - pl * nv) * 8;
+      float acc[8], ws[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = ws[e] = 0.f;
+      if (nsel[u] >= 0) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          if (j >= nsel[u]) break;
+          const RowTile& r = rt[sel[u][j]];
+          const int lx = x0 - r.w0;
+          float v[8];
+          raw[u][j].get(v);
+          if (lx >= r.lo && lx + 8 <= r.nw - r.hi) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              acc[e] = fmaf(r.wty, v[e], acc[e]);
+              ws[e] += r.wty;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float w = r.wty * ramp_w(lx + e, r.nw, r.lo, r.hi);
+              acc[e] = fmaf(w, v[e], acc[e]);
+              ws[e] += w;
+            }
+          }
+        }
+      } else {
+        // generic: every covering tile, element by element
+        const int nloop = spill ? p.n : nk;
+        for (int k = 0; k < nloop; ++k) {
+          RowTile r;
+          if (!spill) {
+            r = rt[k];
+          } else {
+            const BlendTile& tl = p.tiles[k];
+            if (t < tl.t0 || t >= tl.t0 + tl.nt || y < tl.h0 || y >= tl.h0 + tl.nh) continue;
+            r.ptr = tl.ptr;
+            r.rowoff = (static_cast<long long>(t - tl.t0) * tl.nh + (y - tl.h0)) * tl.nw;
+            r.pstride = static_cast<long long>(tl.nt) * tl.nh * tl.nw;
+            r.w0 = tl.w0;
+            r.nw = tl.nw;
+            r.lo = tl.ovl[4];
+            r.hi = tl.ovl[5];
+            r.wty = ramp_w(t - tl.t0, tl.nt, tl.ovl[0], tl.ovl[1]) * ramp_w(y - tl.h0, tl.nh, tl.ovl[2], tl.ovl[3]);
+          }
+          const int lx = x0 - r.w0;
+          if (lx + 8 <= 0 || lx >= r.nw) continue;
+          const TT* src = static_cast<const TT*>(r.ptr) + pl * r.pstride + r.rowoff;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int xx = lx + e;
+            if (xx < 0 || xx >= r.nw) continue;
+            const float w = r.wty * ramp_w(xx, r.nw, r.lo, r.hi);
+            acc[e] = fmaf(w, to_f<TT>(src[xx]), acc[e]);
+            ws[e] += w;
+          }
+        }
+      }
+      TO* orow = static_cast<TO*>(p.out) + pl * plane_out + row_out;
+      float o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = ws[e] > 0.f ? __fdividef(acc[e], ws[e]) : 0.f;
+      if (x0 + 8 <= p.W && (p.W & 7) == 0) {
+        store8(orow + x0, o);
+      } else {
+        for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(o[e]);
+      }
     }
   }
 }

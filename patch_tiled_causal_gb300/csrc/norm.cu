@@ -464,6 +464,7 @@ __global__ void __launch_bounds__(32 * kBlendRowsPerBlock) blend_kernel(const __
   __shared__ RowTile rts[kBlendRowsPerBlock][kRowList];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows_per_t = (p.H + kBlendRowsPerBlock - 1) / kBlendRowsPerBlock;
+  const int pl = blockIdx.y;  // one (b, c) plane per block: a block's reads stay in few pages
   const int t = blockIdx.x / rows_per_t;
   const int y = (blockIdx.x - t * rows_per_t) * kBlendRowsPerBlock + warp;
   if (y >= p.H) return;
@@ -498,10 +499,10 @@ __global__ void __launch_bounds__(32 * kBlendRowsPerBlock) blend_kernel(const __
   __syncwarp();
   const bool spill = nk > kRowList;  // more covering tiles than listed: read them from the table
   const int nv = (p.W + 7) / 8;
-  const int jobs = p.B * p.C * nv;
+  const int jobs = nv;
   const int64_t plane_out = static_cast<int64_t>(p.T) * p.H * p.W;
   const int64_t row_out = (static_cast<int64_t>(t) * p.H + y) * p.W;
-  constexpr int kJ = 4;  // jobs per lane whose loads are all issued before any is summed
+  constexpr int kJ = 1;  // jobs per lane whose loads are all issued before any is summed
   for (int job0 = lane; job0 < jobs; job0 += 32 * kJ) {
     // phase 1: for each job find (at most 2) covering tiles with whole aligned vectors and load them
     ApplyVec<TT> raw[kJ][2];
@@ -515,8 +516,7 @@ __global__ void __launch_bounds__(32 * kBlendRowsPerBlock) blend_kernel(const __
         nsel[u] = job >= jobs ? 0 : -1;
         continue;
       }
-      const int pl = job / nv;
-      const int x0 = (job - pl * nv) * 8;
+      const int x0 = job * 8;
       for (int k = 0; k < nk; ++k) {
         const int lx = x0 - rt[k].w0;
         if (lx + 8 <= 0 || lx >= rt[k].nw) continue;
@@ -541,8 +541,7 @@ __global__ void __launch_bounds__(32 * kBlendRowsPerBlock) blend_kernel(const __
     for (int u = 0; u < kJ; ++u) {
       const int job = job0 + 32 * u;
       if (job >= jobs) break;
-      const int pl = job / nv;
-      const int x0 = (job - pl * nv) * 8;
+      const int x0 = job * 8;
       float acc[8], ws[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = ws[e] = 0.f;
@@ -632,7 +631,8 @@ cudaError_t launch_blend(const void* const* tiles, const vae_tile_t* meta, int n
   }
   const long long nb = static_cast<long long>(d.T) * ((d.H + kBlendRowsPerBlock - 1) / kBlendRowsPerBlock);
   if (nb == 0) return cudaSuccess;
-  dim3 grid(static_cast<unsigned>(nb));
+  if (static_cast<long long>(d.B) * d.C > 65535) return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>(nb), static_cast<unsigned>(d.B * d.C));
   const int threads = 32 * kBlendRowsPerBlock;
   if (p.tile_f32 && p.out_f32) blend_kernel<float, float><<<grid, threads, 0, s>>>(p);
   else if (p.tile_f32) blend_kernel<float, __nv_bfloat16><<<grid, threads, 0, s>>>(p);

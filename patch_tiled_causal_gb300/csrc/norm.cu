@@ -613,10 +613,183 @@ __global__ void __launch_bounds__(32 * kBlendRowsPerBlock) blend_kernel(const __
   }
 }
 
+// Blend for tile sets that form a grid (the tile plan's output): tile (a, b, c) is the product of the
+// a-th temporal, b-th row and c-th column interval, and its weight the product of the three 1-D
+// ramps, so out = sum_{a,b,c} w_a w_b w_c x_abc / (sum_a w_a)(sum_b w_b)(sum_c w_c).  One warp per
+// output row of one plane: the (a, b) pairs covering (t, y) are found once per row from the interval
+// lists, the column intervals covering each 8-pixel vector once per vector.
+constexpr int kAxisMax = 64;
+struct BlendGridParams {
+  int B, C, T, H, W;
+  int n[3];                       // intervals per axis (t, h, w)
+  int s0[3][kAxisMax], len[3][kAxisMax];
+  unsigned short lo[3][kAxisMax], hi[3][kAxisMax];
+  void* out;
+  const void* ptr[VAE_MAX_TILES];  // tile (a, b, c) at ptr[(a * n[1] + b) * n[2] + c]
+};
+
+// Intervals of axis `ax` covering coordinate `x` (at most 2 when overlaps are shorter than strides;
+// a third is ignored only if the plan had one, which the host excludes) and their normalised weights.
+VAE_DEV int axis_cover(const BlendGridParams& p, int ax, int x, int* idx, float* w) {
+  int k = 0;
+  float sum = 0.f;
+  for (int i = 0; i < p.n[ax] && k < 2; ++i) {
+    const int l = x - p.s0[ax][i];
+    if (l < 0 || l >= p.len[ax][i]) continue;
+    idx[k] = i;
+    w[k] = ramp_w(l, p.len[ax][i], p.lo[ax][i], p.hi[ax][i]);
+    sum += w[k];
+    ++k;
+  }
+  for (int j = 0; j < k; ++j) w[j] = __fdividef(w[j], sum);
+  return k;
+}
+
+template <typename TT, typename TO>
+__global__ void __launch_bounds__(256) blend_grid_kernel(const __grid_constant__ BlendGridParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rows_per_t = (p.H + 7) / 8;
+  const int pl = blockIdx.y;
+  const int t = blockIdx.x / rows_per_t;
+  const int y = (blockIdx.x - t * rows_per_t) * 8 + warp;
+  if (y >= p.H) return;
+  int ia[2], ib[2];
+  float wa[2], wb[2];
+  const int na = axis_cover(p, 0, t, ia, wa);
+  const int nb = axis_cover(p, 1, y, ib, wb);
+  const int nc_axis = p.n[2];
+  TO* orow = static_cast<TO*>(p.out) + ((static_cast<int64_t>(pl) * p.T + t) * p.H + y) * p.W;
+  for (int x0 = lane * 8; x0 < p.W; x0 += 32 * 8) {
+    // column intervals overlapping [x0, x0 + 8): consecutive, at most 3
+    int cfirst = -1, ccount = 0;
+    for (int i = 0; i < nc_axis; ++i) {
+      const int l = x0 - p.s0[2][i];
+      if (l + 8 <= 0 || l >= p.len[2][i]) continue;
+      if (cfirst < 0) cfirst = i;
+      ++ccount;
+    }
+    float wc[3][8], wsum[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) wsum[e] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float w = 0.f;
+        if (j < ccount) {
+          const int i = cfirst + j;
+          const int l = x0 + e - p.s0[2][i];
+          if (l >= 0 && l < p.len[2][i]) w = ramp_w(l, p.len[2][i], p.lo[2][i], p.hi[2][i]);
+        }
+        wc[j][e] = w;
+        wsum[e] += w;
+      }
+    }
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    for (int u = 0; u < na; ++u) {
+      for (int q = 0; q < nb; ++q) {
+        const float wab = wa[u] * wb[q];
+        const int a = ia[u], b = ib[q];
+        const int ty = t - p.s0[0][a], yy = y - p.s0[1][b];
+        const int64_t plane_in = static_cast<int64_t>(p.len[0][a]) * p.len[1][b];
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+          if (j >= ccount) break;
+          const int c = cfirst + j;
+          const int nw = p.len[2][c];
+          const TT* src = static_cast<const TT*>(p.ptr[(a * p.n[1] + b) * nc_axis + c]) +
+                          ((pl * plane_in + static_cast<int64_t>(ty) * p.len[1][b]) + yy) * nw;
+          const int lx = x0 - p.s0[2][c];
+          float v[8];
+          if (lx >= 0 && lx + 8 <= nw && ((lx | nw) & 7) == 0) {
+            load8(src + lx, v);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int xx = lx + e;
+              v[e] = (xx >= 0 && xx < nw) ? to_f<TT>(src[xx]) : 0.f;
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[e] = fmaf(wab * wc[j][e], v[e], acc[e]);
+        }
+      }
+    }
+    float o[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = wsum[e] > 0.f ? __fdividef(acc[e], wsum[e]) : 0.f;
+    if (x0 + 8 <= p.W && (p.W & 7) == 0) {
+      store8(orow + x0, o);
+    } else {
+      for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(o[e]);
+    }
+  }
+}
+
+namespace {
+// Recognise a grid: tiles in raster order over per-axis interval lists with per-axis overlaps, at most
+// two intervals covering any coordinate (overlap shorter than the stride).
+bool build_grid(const void* const* tiles, const vae_tile_t* meta, int n, const vae_blend_desc_t& d,
+                BlendGridParams& g) {
+  const int extent[3] = {d.T, d.H, d.W};
+  for (int ax = 0; ax < 3; ++ax) {
+    int cnt = 0;
+    for (int i = 0; i < n; ++i) {
+      const int s0 = meta[i].pix[2 * ax], ln = meta[i].pix[2 * ax + 1];
+      bool seen = false;
+      for (int k = 0; k < cnt; ++k)
+        if (g.s0[ax][k] == s0 && g.len[ax][k] == ln) seen = true;
+      if (seen) continue;
+      if (cnt == kAxisMax) return false;
+      g.s0[ax][cnt] = s0;
+      g.len[ax][cnt] = ln;
+      g.lo[ax][cnt] = static_cast<unsigned short>(meta[i].ovl[2 * ax]);
+      g.hi[ax][cnt] = static_cast<unsigned short>(meta[i].ovl[2 * ax + 1]);
+      ++cnt;
+    }
+    g.n[ax] = cnt;
+    for (int k = 1; k < cnt; ++k)
+      if (g.s0[ax][k] <= g.s0[ax][k - 1]) return false;           // sorted starts
+    for (int k = 2; k < cnt; ++k)
+      if (g.s0[ax][k] < g.s0[ax][k - 2] + g.len[ax][k - 2]) return false;  // <= 2 cover a point
+    (void)extent;
+  }
+  if (static_cast<long long>(g.n[0]) * g.n[1] * g.n[2] != n) return false;
+  for (int i = 0; i < n; ++i) {
+    const int a = i / (g.n[1] * g.n[2]), b = (i / g.n[2]) % g.n[1], c = i % g.n[2];
+    const int idx[3] = {a, b, c};
+    for (int ax = 0; ax < 3; ++ax) {
+      const int k = idx[ax];
+      if (meta[i].pix[2 * ax] != g.s0[ax][k] || meta[i].pix[2 * ax + 1] != g.len[ax][k] ||
+          meta[i].ovl[2 * ax] != g.lo[ax][k] || meta[i].ovl[2 * ax + 1] != g.hi[ax][k])
+        return false;
+    }
+    g.ptr[i] = tiles[i];
+  }
+  return true;
+}
+}  // namespace
+
 cudaError_t launch_blend(const void* const* tiles, const vae_tile_t* meta, int n_tiles, void* out,
                          const vae_blend_desc_t& d, cudaStream_t s) {
   static BlendParams p;
+  static BlendGridParams g;
   if (n_tiles > VAE_MAX_TILES) return cudaErrorInvalidValue;
+  if (static_cast<long long>(d.B) * d.C > 65535) return cudaErrorInvalidValue;
+  if (build_grid(tiles, meta, n_tiles, d, g)) {
+    g.B = d.B; g.C = d.C; g.T = d.T; g.H = d.H; g.W = d.W; g.out = out;
+    const long long nb = static_cast<long long>(d.T) * ((d.H + 7) / 8);
+    if (nb == 0) return cudaSuccess;
+    dim3 grid(static_cast<unsigned>(nb), static_cast<unsigned>(d.B * d.C));
+    const bool tf = d.tile_dtype == VAE_FP32, of = d.out_dtype == VAE_FP32;
+    if (tf && of) blend_grid_kernel<float, float><<<grid, 256, 0, s>>>(g);
+    else if (tf) blend_grid_kernel<float, __nv_bfloat16><<<grid, 256, 0, s>>>(g);
+    else if (of) blend_grid_kernel<__nv_bfloat16, float><<<grid, 256, 0, s>>>(g);
+    else blend_grid_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, s>>>(g);
+    return cudaGetLastError();
+  }
   p.B = d.B; p.C = d.C; p.T = d.T; p.H = d.H; p.W = d.W; p.n = n_tiles;
   p.tile_f32 = d.tile_dtype == VAE_FP32;
   p.out_f32 = d.out_dtype == VAE_FP32;

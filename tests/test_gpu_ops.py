@@ -207,10 +207,13 @@ def test_d2s(vd, s, drop):
     np.testing.assert_array_equal(y.cpu().numpy(), ref)
 
 
-@pytest.mark.parametrize("dt", ["bf16", "fp32"])
-def test_tile_blend(vd, dt):
+@pytest.mark.parametrize("dt,order", [("bf16", "raster"), ("fp32", "raster"), ("fp32", "reversed")])
+def test_tile_blend(vd, dt, order):
+    # raster order is a grid (factorised kernel); any other order takes the general gather kernel
     tdt = torch.bfloat16 if dt == "bf16" else torch.float32
     plan_ = tiles.tile_plan((3, 40, 56), (2, 16, 16), (1, 4, 6), 4, 1)   # causal time, ragged last tiles
+    if order == "reversed":
+        plan_ = plan_[::-1]
     B, Cc = 2, 3
     out_shape = (B, Cc, 4 * 2 + 1, 40, 56)
     data = []

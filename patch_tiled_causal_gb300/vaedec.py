@@ -253,6 +253,21 @@ def patch_groupnorm_silu(x, gamma, beta, y, workspace, d: VaeGnDesc, stream=None
     return y
 
 
+def prepare_patch_groupnorm_silu(x, gamma, beta, y, workspace, d: VaeGnDesc, stream=None):
+    """Marshal the arguments of vae_patch_groupnorm_silu once; returns a function that only makes the
+    C call."""
+    torch = _torch()
+    args = (_ptr(x), _ptr(gamma, torch.float32), _ptr(beta, torch.float32), _ptr(y), _ptr(workspace), C.byref(d),
+            _stream(stream))
+    lib = load()
+    keep = (x, gamma, beta, y, workspace, d)
+
+    def call():
+        _check(lib.vae_patch_groupnorm_silu(*args), "vae_patch_groupnorm_silu")
+    call.keep = keep
+    return call
+
+
 def patch_groupnorm_silu_noalloc(x, gamma, beta, y, d: VaeGnDesc, stream=None):
     """Same as patch_groupnorm_silu, with the scratch in the library's fixed device array."""
     torch = _torch()
@@ -269,6 +284,27 @@ def upsample_d2s(x, y, B, T, H, W, Cc, s, drop_first, stream=None):
     d.drop_first, d.dtype = int(drop_first), _dt(x)
     _check(load().vae_upsample_d2s(_ptr(x), _ptr(y), C.byref(d), _stream(stream)), "vae_upsample_d2s")
     return y
+
+
+def prepare_tile_blend(tiles: Sequence, meta: Sequence[dict], out, stream=None):
+    """Marshal the arguments of vae_tile_blend once; returns a function that only makes the C call
+    (for loops that call the blend repeatedly on the same buffers)."""
+    n = len(tiles)
+    ptrs = (_P * n)(*[_ptr(t) for t in tiles])
+    arr = (VaeTile * n)()
+    for i, m in enumerate(meta):
+        arr[i].lat = (C.c_int * 6)(*m.get("lat", (0,) * 6))
+        arr[i].pix = (C.c_int * 6)(*m["pix"])
+        arr[i].ovl = (C.c_int * 6)(*m["ovl"])
+    d = VaeBlendDesc()
+    d.B, d.C, d.T, d.H, d.W = out.shape
+    d.tile_dtype, d.out_dtype = _dt(tiles[0]), _dt(out)
+    optr, s, lib = _ptr(out), _stream(stream), load()
+    keep = (ptrs, arr, d, tiles, out)
+
+    def call():
+        _check(lib.vae_tile_blend(keep[0], keep[1], n, optr, C.byref(keep[2]), s), "vae_tile_blend")
+    return call
 
 
 def tile_blend(tiles: Sequence, meta: Sequence[dict], out, stream=None):

@@ -645,85 +645,91 @@ VAE_DEV int axis_cover(const BlendGridParams& p, int ax, int x, int* idx, float*
   return k;
 }
 
+// Rows per block of the grid blend; each of the 8 warps handles kGridRows / 8 rows.
+constexpr int kGridRows = 32;
 template <typename TT, typename TO>
 __global__ void __launch_bounds__(256) blend_grid_kernel(const __grid_constant__ BlendGridParams p) {
+  // per output column x: first covering column interval and the normalised weights of it and of the
+  // next interval (0 when only one covers x); built once per block, used by all its rows
+  extern __shared__ unsigned char sm_raw[];
+  float* w1 = reinterpret_cast<float*>(sm_raw);
+  float* w2 = w1 + p.W;
+  short* cf = reinterpret_cast<short*>(w2 + p.W);
+  for (int x = threadIdx.x; x < p.W; x += blockDim.x) {
+    int idx[2];
+    float w[2] = {0.f, 0.f};
+    const int k = axis_cover(p, 2, x, idx, w);
+    cf[x] = static_cast<short>(k ? idx[0] : 0);
+    w1[x] = k ? w[0] : 0.f;
+    w2[x] = k > 1 ? w[1] : 0.f;
+  }
+  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rows_per_t = (p.H + 7) / 8;
+  const int blocks_per_t = (p.H + kGridRows - 1) / kGridRows;
   const int pl = blockIdx.y;
-  const int t = blockIdx.x / rows_per_t;
-  const int y = (blockIdx.x - t * rows_per_t) * 8 + warp;
-  if (y >= p.H) return;
-  int ia[2], ib[2];
-  float wa[2], wb[2];
+  const int t = blockIdx.x / blocks_per_t;
+  const int y_base = (blockIdx.x - t * blocks_per_t) * kGridRows;
+  int ia[2];
+  float wa[2];
   const int na = axis_cover(p, 0, t, ia, wa);
-  const int nb = axis_cover(p, 1, y, ib, wb);
   const int nc_axis = p.n[2];
-  TO* orow = static_cast<TO*>(p.out) + ((static_cast<int64_t>(pl) * p.T + t) * p.H + y) * p.W;
-  for (int x0 = lane * 8; x0 < p.W; x0 += 32 * 8) {
-    // column intervals overlapping [x0, x0 + 8): consecutive, at most 3
-    int cfirst = -1, ccount = 0;
-    for (int i = 0; i < nc_axis; ++i) {
-      const int l = x0 - p.s0[2][i];
-      if (l + 8 <= 0 || l >= p.len[2][i]) continue;
-      if (cfirst < 0) cfirst = i;
-      ++ccount;
-    }
-    float wc[3][8], wsum[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) wsum[e] = 0.f;
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
+  for (int r = warp; r < kGridRows; r += 8) {
+    const int y = y_base + r;
+    if (y >= p.H) break;
+    int ib[2];
+    float wb[2];
+    const int nb = axis_cover(p, 1, y, ib, wb);
+    TO* orow = static_cast<TO*>(p.out) + ((static_cast<int64_t>(pl) * p.T + t) * p.H + y) * p.W;
+    for (int x0 = lane * 8; x0 < p.W; x0 += 32 * 8) {
+      int cfe[8];
+      float a1[8], a2[8];
+      int cmin = 1 << 30, cmax = -1;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        float w = 0.f;
-        if (j < ccount) {
-          const int i = cfirst + j;
-          const int l = x0 + e - p.s0[2][i];
-          if (l >= 0 && l < p.len[2][i]) w = ramp_w(l, p.len[2][i], p.lo[2][i], p.hi[2][i]);
-        }
-        wc[j][e] = w;
-        wsum[e] += w;
+        const int x = min(x0 + e, p.W - 1);
+        cfe[e] = cf[x];
+        a1[e] = x0 + e < p.W ? w1[x] : 0.f;
+        a2[e] = x0 + e < p.W ? w2[x] : 0.f;
+        cmin = min(cmin, cfe[e]);
+        cmax = max(cmax, cfe[e] + (a2[e] > 0.f ? 1 : 0));
       }
-    }
-    float acc[8];
+      float acc[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    for (int u = 0; u < na; ++u) {
-      for (int q = 0; q < nb; ++q) {
-        const float wab = wa[u] * wb[q];
-        const int a = ia[u], b = ib[q];
-        const int ty = t - p.s0[0][a], yy = y - p.s0[1][b];
-        const int64_t plane_in = static_cast<int64_t>(p.len[0][a]) * p.len[1][b];
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+      for (int c = cmin; c <= cmax && c < nc_axis; ++c) {
+        float wc[8];
 #pragma unroll
-        for (int j = 0; j < 3; ++j) {
-          if (j >= ccount) break;
-          const int c = cfirst + j;
-          const int nw = p.len[2][c];
-          const TT* src = static_cast<const TT*>(p.ptr[(a * p.n[1] + b) * nc_axis + c]) +
-                          ((pl * plane_in + static_cast<int64_t>(ty) * p.len[1][b]) + yy) * nw;
-          const int lx = x0 - p.s0[2][c];
-          float v[8];
-          if (lx >= 0 && lx + 8 <= nw && ((lx | nw) & 7) == 0) {
-            load8(src + lx, v);
-          } else {
+        for (int e = 0; e < 8; ++e) wc[e] = c == cfe[e] ? a1[e] : (c == cfe[e] + 1 ? a2[e] : 0.f);
+        const int nw = p.len[2][c];
+        const int lx = x0 - p.s0[2][c];
+        for (int u = 0; u < na; ++u) {
+          for (int q = 0; q < nb; ++q) {
+            const int a = ia[u], b = ib[q];
+            const float wab = wa[u] * wb[q];
+            const int64_t plane_in = static_cast<int64_t>(p.len[0][a]) * p.len[1][b];
+            const TT* src = static_cast<const TT*>(p.ptr[(a * p.n[1] + b) * nc_axis + c]) +
+                            ((pl * plane_in + static_cast<int64_t>(t - p.s0[0][a]) * p.len[1][b]) + (y - p.s0[1][b])) *
+                                nw;
+            float v[8];
+            if (lx >= 0 && lx + 8 <= nw && ((lx | nw) & 7) == 0) {
+              load8(src + lx, v);
+            } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int xx = lx + e;
-              v[e] = (xx >= 0 && xx < nw) ? to_f<TT>(src[xx]) : 0.f;
+              for (int e = 0; e < 8; ++e) {
+                const int xx = lx + e;
+                v[e] = (xx >= 0 && xx < nw) ? to_f<TT>(src[xx]) : 0.f;
+              }
             }
-          }
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[e] = fmaf(wab * wc[j][e], v[e], acc[e]);
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(wab * wc[e], v[e], acc[e]);
+          }
         }
       }
-    }
-    float o[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] = wsum[e] > 0.f ? __fdividef(acc[e], wsum[e]) : 0.f;
-    if (x0 + 8 <= p.W && (p.W & 7) == 0) {
-      store8(orow + x0, o);
-    } else {
-      for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(o[e]);
+      if (x0 + 8 <= p.W && (p.W & 7) == 0) {
+        store8(orow + x0, acc);
+      } else {
+        for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(acc[e]);
+      }
     }
   }
 }
@@ -778,16 +784,17 @@ cudaError_t launch_blend(const void* const* tiles, const vae_tile_t* meta, int n
   static BlendGridParams g;
   if (n_tiles > VAE_MAX_TILES) return cudaErrorInvalidValue;
   if (static_cast<long long>(d.B) * d.C > 65535) return cudaErrorInvalidValue;
-  if (build_grid(tiles, meta, n_tiles, d, g)) {
+  if (d.W <= 4096 && build_grid(tiles, meta, n_tiles, d, g)) {  // column table fits 40 KB of shared memory
     g.B = d.B; g.C = d.C; g.T = d.T; g.H = d.H; g.W = d.W; g.out = out;
-    const long long nb = static_cast<long long>(d.T) * ((d.H + 7) / 8);
+    const long long nb = static_cast<long long>(d.T) * ((d.H + kGridRows - 1) / kGridRows);
     if (nb == 0) return cudaSuccess;
     dim3 grid(static_cast<unsigned>(nb), static_cast<unsigned>(d.B * d.C));
+    const size_t sm = static_cast<size_t>(d.W) * (2 * sizeof(float) + sizeof(short));
     const bool tf = d.tile_dtype == VAE_FP32, of = d.out_dtype == VAE_FP32;
-    if (tf && of) blend_grid_kernel<float, float><<<grid, 256, 0, s>>>(g);
-    else if (tf) blend_grid_kernel<float, __nv_bfloat16><<<grid, 256, 0, s>>>(g);
-    else if (of) blend_grid_kernel<__nv_bfloat16, float><<<grid, 256, 0, s>>>(g);
-    else blend_grid_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, s>>>(g);
+    if (tf && of) blend_grid_kernel<float, float><<<grid, 256, sm, s>>>(g);
+    else if (tf) blend_grid_kernel<float, __nv_bfloat16><<<grid, 256, sm, s>>>(g);
+    else if (of) blend_grid_kernel<__nv_bfloat16, float><<<grid, 256, sm, s>>>(g);
+    else blend_grid_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, sm, s>>>(g);
     return cudaGetLastError();
   }
   p.B = d.B; p.C = d.C; p.T = d.T; p.H = d.H; p.W = d.W; p.n = n_tiles;

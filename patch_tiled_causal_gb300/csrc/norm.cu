@@ -647,21 +647,52 @@ VAE_DEV int axis_cover(const BlendGridParams& p, int ax, int x, int* idx, float*
 
 // Rows per block of the grid blend; each of the 8 warps handles kGridRows / 8 rows.
 constexpr int kGridRows = 32;
+constexpr int kGridMaxVec = 384;  // 8-pixel vectors per row with a shared-memory entry (W <= 3072)
 template <typename TT, typename TO>
 __global__ void __launch_bounds__(256) blend_grid_kernel(const __grid_constant__ BlendGridParams p) {
-  // per output column x: first covering column interval and the normalised weights of it and of the
-  // next interval (0 when only one covers x); built once per block, used by all its rows
-  extern __shared__ unsigned char sm_raw[];
-  float* w1 = reinterpret_cast<float*>(sm_raw);
-  float* w2 = w1 + p.W;
-  short* cf = reinterpret_cast<short*>(w2 + p.W);
-  for (int x = threadIdx.x; x < p.W; x += blockDim.x) {
-    int idx[2];
-    float w[2] = {0.f, 0.f};
-    const int k = axis_cover(p, 2, x, idx, w);
-    cf[x] = static_cast<short>(k ? idx[0] : 0);
-    w1[x] = k ? w[0] : 0.f;
-    w2[x] = k > 1 ? w[1] : 0.f;
+  // Per 8-pixel vector of a row (the same for every row): first overlapping column interval c0, the
+  // number of overlapping intervals (<= 2, 3 = take the slow path) and the normalised column weight
+  // of each pixel for each of them.  Per warp and row: the source row pointer of every (t, y) pair
+  // and column interval.
+  __shared__ short vc0[kGridMaxVec];
+  __shared__ unsigned char vnc[kGridMaxVec];
+  __shared__ float4 vw[kGridMaxVec][4];                    // [j * 2 + half] -> weights of 4 pixels
+  __shared__ const TT* rowp[8][4][kAxisMax];
+  __shared__ float wpair[8][4];
+  const int nv = (p.W + 7) / 8;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    const int x0 = v * 8;
+    int c0 = -1, nc = 0;
+    for (int i = 0; i < p.n[2]; ++i) {
+      const int l = x0 - p.s0[2][i];
+      if (l + 8 <= 0 || l >= p.len[2][i]) continue;
+      if (c0 < 0) c0 = i;
+      ++nc;
+    }
+    float w[2][8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float a0 = 0.f, a1 = 0.f;
+      if (nc >= 1 && nc <= 2) {
+        const int x = x0 + e;
+        const int l0 = x - p.s0[2][c0];
+        if (x < p.W && l0 >= 0 && l0 < p.len[2][c0]) a0 = ramp_w(l0, p.len[2][c0], p.lo[2][c0], p.hi[2][c0]);
+        if (nc == 2) {
+          const int l1 = x - p.s0[2][c0 + 1];
+          if (x < p.W && l1 >= 0 && l1 < p.len[2][c0 + 1])
+            a1 = ramp_w(l1, p.len[2][c0 + 1], p.lo[2][c0 + 1], p.hi[2][c0 + 1]);
+        }
+      }
+      const float sum = a0 + a1;
+      w[0][e] = sum > 0.f ? __fdividef(a0, sum) : 0.f;
+      w[1][e] = sum > 0.f ? __fdividef(a1, sum) : 0.f;
+    }
+    vc0[v] = static_cast<short>(c0 < 0 ? 0 : c0);
+    vnc[v] = static_cast<unsigned char>(nc > 2 ? 3 : nc);
+    vw[v][0] = make_float4(w[0][0], w[0][1], w[0][2], w[0][3]);
+    vw[v][1] = make_float4(w[0][4], w[0][5], w[0][6], w[0][7]);
+    vw[v][2] = make_float4(w[1][0], w[1][1], w[1][2], w[1][3]);
+    vw[v][3] = make_float4(w[1][4], w[1][5], w[1][6], w[1][7]);
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -679,50 +710,64 @@ __global__ void __launch_bounds__(256) blend_grid_kernel(const __grid_constant__
     int ib[2];
     float wb[2];
     const int nb = axis_cover(p, 1, y, ib, wb);
+    const int npair = na * nb;
+    // row pointers of every (pair, column interval), lanes in parallel
+    for (int e = lane; e < npair * nc_axis; e += 32) {
+      const int q = e / nc_axis, c = e - (e / nc_axis) * nc_axis;
+      const int a = ia[q / nb], b = ib[q % nb];
+      const int64_t plane_in = static_cast<int64_t>(p.len[0][a]) * p.len[1][b];
+      rowp[warp][q][c] = static_cast<const TT*>(p.ptr[(a * p.n[1] + b) * nc_axis + c]) +
+                         ((pl * plane_in + static_cast<int64_t>(t - p.s0[0][a]) * p.len[1][b]) + (y - p.s0[1][b])) *
+                             p.len[2][c];
+    }
+    if (lane < npair) wpair[warp][lane] = wa[lane / nb] * wb[lane % nb];
+    __syncwarp();
     TO* orow = static_cast<TO*>(p.out) + ((static_cast<int64_t>(pl) * p.T + t) * p.H + y) * p.W;
-    for (int x0 = lane * 8; x0 < p.W; x0 += 32 * 8) {
-      int cfe[8];
-      float a1[8], a2[8];
-      int cmin = 1 << 30, cmax = -1;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int x = min(x0 + e, p.W - 1);
-        cfe[e] = cf[x];
-        a1[e] = x0 + e < p.W ? w1[x] : 0.f;
-        a2[e] = x0 + e < p.W ? w2[x] : 0.f;
-        cmin = min(cmin, cfe[e]);
-        cmax = max(cmax, cfe[e] + (a2[e] > 0.f ? 1 : 0));
-      }
+    for (int v = lane; v < nv; v += 32) {
+      const int x0 = v * 8;
+      const int c0 = vc0[v], nc = vnc[v];
       float acc[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-      for (int c = cmin; c <= cmax && c < nc_axis; ++c) {
-        float wc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) wc[e] = c == cfe[e] ? a1[e] : (c == cfe[e] + 1 ? a2[e] : 0.f);
-        const int nw = p.len[2][c];
-        const int lx = x0 - p.s0[2][c];
-        for (int u = 0; u < na; ++u) {
-          for (int q = 0; q < nb; ++q) {
-            const int a = ia[u], b = ib[q];
-            const float wab = wa[u] * wb[q];
-            const int64_t plane_in = static_cast<int64_t>(p.len[0][a]) * p.len[1][b];
-            const TT* src = static_cast<const TT*>(p.ptr[(a * p.n[1] + b) * nc_axis + c]) +
-                            ((pl * plane_in + static_cast<int64_t>(t - p.s0[0][a]) * p.len[1][b]) + (y - p.s0[1][b])) *
-                                nw;
-            float v[8];
-            if (lx >= 0 && lx + 8 <= nw && ((lx | nw) & 7) == 0) {
-              load8(src + lx, v);
+      if (nc <= 2) {
+        for (int j = 0; j < nc; ++j) {
+          const float4 wl = vw[v][2 * j], wh = vw[v][2 * j + 1];
+          const float wc[8] = {wl.x, wl.y, wl.z, wl.w, wh.x, wh.y, wh.z, wh.w};
+          const int c = c0 + j;
+          const int nw = p.len[2][c];
+          const int lx = x0 - p.s0[2][c];
+          const bool vec = lx >= 0 && lx + 8 <= nw && ((lx | nw) & 7) == 0;
+          for (int q = 0; q < npair; ++q) {
+            const TT* src = rowp[warp][q][c];
+            const float wq = wpair[warp][q];
+            float val[8];
+            if (vec) {
+              load8(src + lx, val);
             } else {
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
                 const int xx = lx + e;
-                v[e] = (xx >= 0 && xx < nw) ? to_f<TT>(src[xx]) : 0.f;
+                val[e] = (xx >= 0 && xx < nw) ? to_f<TT>(src[xx]) : 0.f;
               }
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = fmaf(wab * wc[e], v[e], acc[e]);
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(wq * wc[e], val[e], acc[e]);
           }
+        }
+      } else {
+        // a vector spanning three or more column intervals: per pixel, straight from the table
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int x = x0 + e;
+          if (x >= p.W) continue;
+          int ic[2];
+          float wc2[2];
+          const int ncx = axis_cover(p, 2, x, ic, wc2);
+          for (int j = 0; j < ncx; ++j)
+            for (int q = 0; q < npair; ++q) {
+              const TT* src = rowp[warp][q][ic[j]];
+              acc[e] = fmaf(wpair[warp][q] * wc2[j], to_f<TT>(src[x - p.s0[2][ic[j]]]), acc[e]);
+            }
         }
       }
       if (x0 + 8 <= p.W && (p.W & 7) == 0) {
@@ -731,6 +776,7 @@ __global__ void __launch_bounds__(256) blend_grid_kernel(const __grid_constant__
         for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(acc[e]);
       }
     }
+    __syncwarp();
   }
 }
 
@@ -784,12 +830,12 @@ cudaError_t launch_blend(const void* const* tiles, const vae_tile_t* meta, int n
   static BlendGridParams g;
   if (n_tiles > VAE_MAX_TILES) return cudaErrorInvalidValue;
   if (static_cast<long long>(d.B) * d.C > 65535) return cudaErrorInvalidValue;
-  if (d.W <= 4096 && build_grid(tiles, meta, n_tiles, d, g)) {  // column table fits 40 KB of shared memory
+  if (d.W <= 8 * kGridMaxVec && build_grid(tiles, meta, n_tiles, d, g)) {
     g.B = d.B; g.C = d.C; g.T = d.T; g.H = d.H; g.W = d.W; g.out = out;
     const long long nb = static_cast<long long>(d.T) * ((d.H + kGridRows - 1) / kGridRows);
     if (nb == 0) return cudaSuccess;
     dim3 grid(static_cast<unsigned>(nb), static_cast<unsigned>(d.B * d.C));
-    const size_t sm = static_cast<size_t>(d.W) * (2 * sizeof(float) + sizeof(short));
+    const size_t sm = 0;
     const bool tf = d.tile_dtype == VAE_FP32, of = d.out_dtype == VAE_FP32;
     if (tf && of) blend_grid_kernel<float, float><<<grid, 256, sm, s>>>(g);
     else if (tf) blend_grid_kernel<float, __nv_bfloat16><<<grid, 256, sm, s>>>(g);

@@ -649,7 +649,7 @@ VAE_DEV int axis_cover(const BlendGridParams& p, int ax, int x, int* idx, float*
 constexpr int kGridRows = 32;
 constexpr int kGridMaxVec = 384;  // 8-pixel vectors per row with a shared-memory entry (W <= 3072)
 template <typename TT, typename TO>
-__global__ void __launch_bounds__(256) blend_grid_kernel(const __grid_constant__ BlendGridParams p) {
+__global__ void __launch_bounds__(256, 4) blend_grid_kernel(const __grid_constant__ BlendGridParams p) {
   // Per 8-pixel vector of a row (the same for every row): first overlapping column interval c0, the
   // number of overlapping intervals (<= 2, 3 = take the slow path) and the normalised column weight
   // of each pixel for each of them.  Per warp and row: the source row pointer of every (t, y) pair

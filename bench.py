@@ -138,8 +138,8 @@ def oracle_sample(cfg, crop_thw, seed=0):
     return frame_px, dt
 
 
-REF_CROP = (5, 1, 2)   # latent frames, rows, cols of the reference arm's per-step sample
-CPU_CROP = (5, 2, 2)   # the GPU arm's cpu_baseline sample
+REF_CROP = (2, 1, 2)   # latent frames, rows, cols of the reference arm's per-step sample (~10 s)
+CPU_CROP = (3, 1, 2)   # the GPU arm's cpu_baseline sample (~20 s on the GPU machine's host cores)
 
 
 def _crop_text(cfg, crop):
@@ -317,7 +317,7 @@ def main():
         kernels[k] = e
     conv = prof.get("conv_tc", {"flops": 0.0, "ms": 1.0, "launches": 1})
     conv_tf = conv["flops"] / (conv["ms"] / 1e3) / 1e12
-    tr = _traffic("conv_tc_decode")
+    tr = _traffic(f"conv_tc_decode_{cfg.name}")
     roofline = {"bound": "tensor", "kernel": "conv_tc (tcgen05 implicit-GEMM causal conv), all launches of the decode",
                 "achieved": conv_tf, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                 "frac": conv_tf / peaks["bf16_tflops_sustained"],

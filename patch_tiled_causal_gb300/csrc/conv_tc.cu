@@ -62,6 +62,7 @@ struct TcParams {
   int pair;          // 1: CTAs run in clusters of 2 on adjacent M tiles of one N tile, each loading half of
                      // the weight tile and multicasting it to both
   int n_mtiles, seq_count;
+  int npc;           // N tiles per work chunk (divides n_ntiles)
   uint32_t* fault;
   uint64_t limit_ns;
 };
@@ -102,29 +103,34 @@ struct TileCoord {
   bool dummy;  // pair mode, odd M-tile count: this CTA computes a copy of the last tile and stores nothing
 };
 
-VAE_DEV TileCoord tile_coord(const TcParams& p, int tile);
+VAE_DEV TileCoord mn_coord(const TcParams& p, int mt, int ntile);
 
-// Tile of work-sequence entry `seq` for this CTA.
+// Work order of the persistent loop: chunks of npc N tiles (whose weights fit in L2 together)
+// outermost, then M tiles, then the N tiles of the chunk, so CTAs running at the same time share A
+// tiles and their weights stay cached.  In conv mode M tiles run spatial-major and frame-minor: CTAs
+// running together read one spatial region of consecutive frames, so the three temporal taps of a
+// frame are served from L2.  Pair mode gives CTA `rank` M tile 2i + rank of entry i.
 VAE_DEV TileCoord seq_coord(const TcParams& p, int seq, int rank) {
-  if (!p.pair) return tile_coord(p, seq);
-  const int nt = seq % p.n_ntiles;
-  int mt = 2 * (seq / p.n_ntiles) + rank;
+  const int nin = seq % p.npc;
+  const int rest = seq / p.npc;
+  const int mcount = p.pair ? (p.n_mtiles + 1) / 2 : p.n_mtiles;
+  const int mi = rest % mcount;
+  const int ntile = (rest / mcount) * p.npc + nin;
+  int mt = p.pair ? 2 * mi + rank : mi;
   const bool dummy = mt >= p.n_mtiles;
   if (dummy) mt = p.n_mtiles - 1;
-  TileCoord c = tile_coord(p, mt * p.n_ntiles + nt);
+  TileCoord c = mn_coord(p, mt, ntile);
   c.dummy = dummy;
   return c;
 }
 
-VAE_DEV TileCoord tile_coord(const TcParams& p, int tile) {
+VAE_DEV TileCoord mn_coord(const TcParams& p, int mt, int ntile) {
   TileCoord c{};
-  const int ntile = tile % p.n_ntiles;
-  const int mt = tile / p.n_ntiles;
   c.n0 = ntile * p.BN;
   if (p.mode == 0) {
-    const int per_frame = p.n_trows * p.n_tcols;
-    const int frame = mt / per_frame;
-    const int r = mt - frame * per_frame;
+    const int frames = p.B * p.T;
+    const int frame = mt % frames;
+    const int r = mt / frames;
     const int tr = r / p.n_tcols, tc = r - (r / p.n_tcols) * p.n_tcols;
     const int pi = find_band(p.trow_prefix, p.nph, tr);
     const int pj = find_band(p.tcol_prefix, p.npw, tc);
@@ -651,6 +657,17 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   }
   p.n_mtiles = static_cast<int>(n_blocks / p.n_ntiles);
   p.pair = want_pair ? 1 : 0;
+  {
+    // N tiles per chunk: as many as keep the chunk's weights within ~48 MB of L2
+    const double w_tile = static_cast<double>(p.BN) * (a.mode == 0 ? 27.0 * a.C_in_pad : static_cast<double>(a.K)) * 2.0;
+    int npc = p.n_ntiles;
+    if (a.mode == 0) {
+      npc = 1;
+      for (int d = 1; d <= p.n_ntiles; ++d)
+        if (p.n_ntiles % d == 0 && d * w_tile <= 48.0 * 1024 * 1024) npc = d;
+    }
+    p.npc = npc;
+  }
   if (!p.pair) {
     p.seq_count = p.n_tiles;
     const long long grid = std::min<long long>(n_blocks, n_sm);

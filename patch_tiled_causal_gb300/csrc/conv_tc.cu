@@ -80,20 +80,21 @@ VAE_DEV int find_band(const int* prefix, int n, int idx) {
   return i;
 }
 
-// Group-norm partial sums of one (patch, b, t, group): exact integer sums of q = round(x * 2^18)
-// and q^2 (128-bit), see norm.cu.  Layout must match GnPartial there.
+// Group-norm partial sums of one (patch, b, t, group): exact integer sums of q = round(x * 2^18) and of
+// q^2, the latter kept as two 64-bit sums (of the low 32 bits and of the rest of every contribution,
+// sum q^2 = s2a + s2b * 2^32) so that every update is a plain fire-and-forget atomic add.  Layout must
+// match GnPartial in norm.cu.
 struct GnPart {
-  unsigned long long s1;      // two's complement int64 sum of q
-  unsigned long long s2_lo;   // 128-bit sum of q^2
-  unsigned long long s2_hi;
+  unsigned long long s1;   // two's complement int64 sum of q
+  unsigned long long s2a;  // sum of (contribution mod 2^32)
+  unsigned long long s2b;  // sum of (contribution >> 32)
   unsigned long long pad;
 };
 
 VAE_DEV void gn_accumulate(GnPart* dst, long long s1, unsigned long long lo, unsigned long long hi) {
   atomicAdd(&dst->s1, static_cast<unsigned long long>(s1));
-  unsigned long long old = atomicAdd(&dst->s2_lo, lo);
-  unsigned long long carry = (old + lo < old) ? 1ull : 0ull;
-  if (hi + carry) atomicAdd(&dst->s2_hi, hi + carry);
+  atomicAdd(&dst->s2a, lo & 0xffffffffull);
+  atomicAdd(&dst->s2b, (lo >> 32) | (hi << 32));
 }
 
 }  // namespace
@@ -146,6 +147,47 @@ VAE_DEV TileCoord mn_coord(const TcParams& p, int mt, int ntile) {
     c.m0 = (mt - c.bat * p.m_tiles_per_batch) * kBlockM * p.msub;
   }
   return c;
+}
+
+// Exact group sums of one 32-column chunk (STEP channels per group inside the chunk, unrolled so the
+// values stay in registers): q = round(x * 2^18) into an int64 sum, q^2 into a 128-bit sum, warp-
+// reduced across the 32 rows of this warp, then added to the (patch, b, t, group) slot.
+template <int STEP>
+VAE_DEV void gn_chunk_sums(const TcParams& p, const TileCoord& tc, const float* v, bool st_ok, int to, int c,
+                           int lane) {
+#pragma unroll
+  for (int i0 = 0; i0 < 32; i0 += STEP) {
+    long long s1 = 0;
+    unsigned long long lo = 0, hi = 0;
+    if (st_ok) {
+#pragma unroll
+      for (int i = i0; i < i0 + STEP; ++i) {
+        const float xv = v[i];
+        if (!(fabsf(xv) < 8192.f)) raise_fault(p.fault, FAULT_RANGE, 20);
+        const int qv = __float2int_rn(fminf(fmaxf(xv, -8191.f), 8191.f) * 262144.f);
+        s1 += qv;
+        const unsigned long long sq = static_cast<unsigned long long>(static_cast<long long>(qv) * qv);
+        lo += sq;
+        if (lo < sq) ++hi;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const long long o1 = __shfl_xor_sync(0xffffffffu, s1, off);
+      const unsigned long long olo = __shfl_xor_sync(0xffffffffu, lo, off);
+      const unsigned long long ohi = __shfl_xor_sync(0xffffffffu, hi, off);
+      s1 += o1;
+      const unsigned long long nlo = lo + olo;
+      hi += ohi + (nlo < lo ? 1ull : 0ull);
+      lo = nlo;
+    }
+    if (lane == 0 && to >= 0 && (s1 != 0 || lo != 0 || hi != 0)) {
+      const int g = (c + i0) / p.gn_cpg;
+      GnPart* parts = static_cast<GnPart*>(p.gn_partials);
+      const int64_t slot = ((static_cast<int64_t>(tc.patch) * p.B + tc.b) * p.T_out + to) * p.gn_groups + g;
+      gn_accumulate(parts + slot, s1, lo, hi);
+    }
+  }
 }
 
 // Epilogue of one 32-column chunk held by this thread (one accumulator row).
@@ -236,45 +278,19 @@ VAE_DEV void epilogue_chunk(const TcParams& p, const TileCoord& tc, int m, int n
     }
     if (p.gn_partials) {
       // exact per-patch group sums of the stored values (all lanes share sub, frame `to` and the group)
-      const int cpg = p.gn_cpg;
-      const int step = min(cpg, 32);
-      for (int i0 = 0; i0 < 32; i0 += step) {
-        long long s1 = 0;
-        unsigned long long lo = 0, hi = 0;
-        if (st_ok) {
-          for (int i = i0; i < i0 + step; ++i) {
-            const float xv = v[i];
-            if (!(fabsf(xv) < 8192.f)) raise_fault(p.fault, FAULT_RANGE, 20);
-            const int qv = __float2int_rn(fminf(fmaxf(xv, -8191.f), 8191.f) * 262144.f);
-            s1 += qv;
-            const unsigned long long sq = static_cast<unsigned long long>(static_cast<long long>(qv) * qv);
-            lo += sq;
-            if (lo < sq) ++hi;
-          }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const long long o1 = __shfl_xor_sync(0xffffffffu, s1, off);
-          const unsigned long long olo = __shfl_xor_sync(0xffffffffu, lo, off);
-          const unsigned long long ohi = __shfl_xor_sync(0xffffffffu, hi, off);
-          s1 += o1;
-          const unsigned long long nlo = lo + olo;
-          hi += ohi + (nlo < lo ? 1ull : 0ull);
-          lo = nlo;
-        }
-        if (lane == 0 && to >= 0) {
-          const int g = (c + i0) / cpg;
-          GnPart* parts = static_cast<GnPart*>(p.gn_partials);
-          const int64_t slot = ((static_cast<int64_t>(tc.patch) * p.B + tc.b) * p.T_out + to) * p.gn_groups + g;
-          if (s1 != 0 || lo != 0 || hi != 0) gn_accumulate(parts + slot, s1, lo, hi);
-        }
+      switch (min(p.gn_cpg, 32)) {
+        case 4: gn_chunk_sums<4>(p, tc, v, st_ok, to, c, lane); break;
+        case 8: gn_chunk_sums<8>(p, tc, v, st_ok, to, c, lane); break;
+        case 16: gn_chunk_sums<16>(p, tc, v, st_ok, to, c, lane); break;
+        default: gn_chunk_sums<32>(p, tc, v, st_ok, to, c, lane); break;
       }
     }
   } else {
     // generic scalar path (NCTHW pixels, or channel counts not a multiple of 32)
+#pragma unroll
     for (int i = 0; i < 32; ++i) {
       const int n = nb + i;
-      if (n >= p.N_real) break;
+      if (n >= p.N_real) continue;
       const int sub = n / p.C_d2s;
       const int c = n - sub * p.C_d2s;
       float val = v[i] + (p.bias ? p.bias[c * p.S + sub] : 0.f);

@@ -24,9 +24,9 @@ namespace vae {
 
 // ============================================================================ group norm
 struct GnPartial {
-  unsigned long long s1;     // int64 sum of q (two's complement)
-  unsigned long long s2_lo;  // 128-bit sum of q^2
-  unsigned long long s2_hi;
+  unsigned long long s1;   // int64 sum of q (two's complement)
+  unsigned long long s2a;  // sum of q^2 = s2a + s2b * 2^32: s2a sums the low 32 bits of each
+  unsigned long long s2b;  // contribution and s2b the rest, so updates need no carry (plain atomics)
   unsigned long long pad;
 };
 static_assert(sizeof(GnPartial) == 32, "GnPartial layout is shared with the conv epilogue");
@@ -146,11 +146,10 @@ __global__ void __launch_bounds__(256) gn_stats_kernel(const __grid_constant__ G
 #pragma unroll
   for (int k = 0; k < GPV; ++k) {
     const int g = (GPV == 1) ? c0 / p.cpg : (c0 / p.cpg + k);
-    if (s1[k] != 0 || lo[k] != 0 || hi[k] != 0) {
+    if (s1[k] != 0 || lo[k] != 0 || hi[k] != 0) {  // plain adds: no returned values, no carries
       atomicAdd(&sh_s1[g], static_cast<unsigned long long>(s1[k]));
-      const unsigned long long old = atomicAdd(&sh_lo[g], lo[k]);
-      const unsigned long long carry = (old + lo[k] < old) ? 1ull : 0ull;
-      if (hi[k] + carry) atomicAdd(&sh_hi[g], hi[k] + carry);
+      atomicAdd(&sh_lo[g], lo[k] & 0xffffffffull);
+      atomicAdd(&sh_hi[g], (lo[k] >> 32) | (hi[k] << 32));
     }
   }
   __syncthreads();
@@ -158,12 +157,11 @@ __global__ void __launch_bounds__(256) gn_stats_kernel(const __grid_constant__ G
   const int b = fb, t = ft;
   for (int g = threadIdx.x; g < p.groups; g += blockDim.x) {
     GnPartial* d = p.parts + ((static_cast<int64_t>(patch) * p.B + b) * p.T + t) * p.groups + g;
-    const unsigned long long a1 = sh_s1[g], alo = sh_lo[g], ahi = sh_hi[g];
-    if (a1 == 0 && alo == 0 && ahi == 0) continue;
+    const unsigned long long a1 = sh_s1[g], a2 = sh_lo[g], b2 = sh_hi[g];
+    if (a1 == 0 && a2 == 0 && b2 == 0) continue;
     atomicAdd(&d->s1, a1);
-    const unsigned long long old = atomicAdd(&d->s2_lo, alo);
-    const unsigned long long carry = (old + alo < old) ? 1ull : 0ull;
-    if (ahi + carry) atomicAdd(&d->s2_hi, ahi + carry);
+    atomicAdd(&d->s2a, a2);
+    atomicAdd(&d->s2b, b2);
   }
 }
 
@@ -181,7 +179,8 @@ __global__ void __launch_bounds__(256) gn_finalize_kernel(const __grid_constant_
     for (int q = 0; q < P; ++q) {
       const GnPartial& d = p.parts[((static_cast<int64_t>(q) * p.B + b) * p.T + t) * p.groups + g];
       s1 += static_cast<long long>(d.s1);
-      add128(lo, hi, d.s2_lo, d.s2_hi);
+      add128(lo, hi, d.s2a, 0ull);
+      add128(lo, hi, d.s2b << 32, d.s2b >> 32);
     }
     const double mq = static_cast<double>(s1) / n;  // mean in units of 2^-18
     const double e2 = (static_cast<double>(hi) * 18446744073709551616.0 + static_cast<double>(lo)) / n;

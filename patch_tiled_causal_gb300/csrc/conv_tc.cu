@@ -319,12 +319,19 @@ VAE_DEV void epilogue_chunk(const TcParams& p, const TileCoord& tc, int m, int n
 // Persistent kernel: each block walks tiles blockIdx.x, blockIdx.x + gridDim.x, ...  The shared-
 // memory ring runs continuously across tiles; two TMEM accumulators let the epilogue of one tile
 // overlap the MMAs of the next.
+//
+// kPair (conv mode, clusters of 2): the two CTAs' M tiles run as ONE tcgen05 MMA of 256 x BN
+// (cta_group::2).  Each CTA loads its own 128-pixel A tiles and one half (BN/2 rows) of the weight
+// tile; the leader's full barrier counts both CTAs' bytes, the leader alone issues the MMAs, and its
+// commits free the stage and hand the accumulator to the epilogues in both CTAs.  Each SM then takes
+// in half as many weight bytes per MMA as a CTA that holds the whole weight tile.
+template <bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     conv_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t b_bytes = static_cast<uint32_t>(p.BN) * kBlockK * 2;
+  const uint32_t b_bytes = static_cast<uint32_t>(kPair ? p.BN / 2 : p.BN) * kBlockK * 2;
   const uint32_t a_bytes = kABytes * static_cast<uint32_t>(p.msub);
   const uint32_t stage_bytes = a_bytes + b_bytes;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + p.stages * stage_bytes);
@@ -344,22 +351,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], p.pair ? 2 : 1);  // pair: both CTAs' MMAs free a stage
+      // multicast-B pairs: both CTAs' MMAs free a stage; MMA pairs: the leader's commit alone
+      mbar_init(&empty_bar[s], (p.pair && !kPair) ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&accf_bar[a], 1);
-      mbar_init(&acce_bar[a], 4 * 32);
+      mbar_init(&acce_bar[a], kPair ? 2 * 4 : 4 * 32);  // MMA pairs: one arrival per epilogue warp of each CTA
     }
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, static_cast<uint32_t>(p.tmem_cols));
+  if (warp == 1) {
+    if constexpr (kPair) tmem_alloc_pair(tmem_slot, static_cast<uint32_t>(p.tmem_cols));
+    else tmem_alloc(tmem_slot, static_cast<uint32_t>(p.tmem_cols));
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  if (p.pair) cluster_sync();  // the peer's barriers exist before anything is multicast to them
+  // the peer's barriers (and, for MMA pairs, its tensor memory) exist before anything targets them
+  if (p.pair) cluster_sync();
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -377,6 +389,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* a_dst = smem + s * stage_bytes;
           uint8_t* b_dst = a_dst + a_bytes;
+          if constexpr (kPair) {
+            // both CTAs' tiles complete on the leader's barrier (the leader alone runs the MMAs)
+            const uint32_t fb = cluster_map(smem_u32(&full_bar[s]), 0);
+            if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * stage_bytes);
+            const int tap = kb / p.cchunks;
+            const int cc = kb - tap * p.cchunks;
+            const int kt = tap / 9, kh = (tap / 3) % 3, kw = tap % 3;
+            const int ti = max(tc.t + kt - 2 + p.cache_frames, 0);
+            tma_load_5d_pair(a_dst, &tmA, fb, cc * kBlockK, tc.w0 + kw - 1, tc.h0 + kh - 1, ti, tc.b);
+            tma_load_2d_pair(b_dst, &tmB, fb, tap * p.C_in_pad + cc * kBlockK, tc.n0 + rank * (p.BN / 2));
+            continue;
+          }
           mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
           if (p.mode == 0) {
             const int tap = kb / p.cchunks;
@@ -399,9 +423,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // drain: every issued load has landed before the block may exit
-      for (int k = max(0, kc - p.stages); k < kc; ++k)
-        mbar_wait(&full_bar[k % p.stages], (k / p.stages) & 1, p.fault, p.limit_ns, 2);
+      // drain: every issued load has landed before the block may exit (an MMA pair's follower sees
+      // that through the empty barriers below: the leader consumed its tiles)
+      if (!kPair || rank == 0)
+        for (int k = max(0, kc - p.stages); k < kc; ++k)
+          mbar_wait(&full_bar[k % p.stages], (k / p.stages) & 1, p.fault, p.limit_ns, 2);
       // pair: both MMAs have released every stage, so no multicast commit is still on its way here
       if (p.pair)
         for (int k = max(0, kc - p.stages); k < kc; ++k)
@@ -409,8 +435,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kBlockM, static_cast<uint32_t>(p.BN));
+    if (lane == 0 && (!kPair || rank == 0)) {
+      const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * kBlockM : kBlockM, static_cast<uint32_t>(p.BN));
       int kc = 0, it = 0;
       bool ok = true;
       for (int seq = seq0; seq < p.seq_count && ok; seq += seq_step, ++it) {
@@ -433,14 +459,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < kBlockK / 16; ++k) {
               // advance 16 bf16 (32 B) along K inside the 128-byte swizzle atom
-              tc_mma_bf16(d_sub, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), idesc,
-                          (kb > 0 || k > 0) ? 1u : 0u);
+              if constexpr (kPair)
+                tc_mma_bf16_pair(d_sub, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k),
+                                 idesc, (kb > 0 || k > 0) ? 1u : 0u);
+              else
+                tc_mma_bf16(d_sub, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k),
+                            idesc, (kb > 0 || k > 0) ? 1u : 0u);
             }
           }
-          if (p.pair) tc_commit_mc(&empty_bar[s], pair_mask);
+          if constexpr (kPair) tc_commit_pair_mc(&empty_bar[s], pair_mask);
+          else if (p.pair) tc_commit_mc(&empty_bar[s], pair_mask);
           else tc_commit(&empty_bar[s]);
         }
-        tc_commit(&accf_bar[acc]);
+        if constexpr (kPair) tc_commit_pair_mc(&accf_bar[acc], pair_mask);
+        else tc_commit(&accf_bar[acc]);
       }
     }
   } else {
@@ -464,7 +496,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (sub == p.msub - 1 && j == nchunks - 1) {
             // every TMEM read of this accumulator is done: hand it back to the MMA warp
             tc_fence_before();
-            mbar_arrive(&acce_bar[acc]);
+            if constexpr (kPair) {
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster(cluster_map(smem_u32(&acce_bar[acc]), 0));
+            } else {
+              mbar_arrive(&acce_bar[acc]);
+            }
           }
           const int nb = tc.n0 + j * 32;
           if (nb >= p.N_real) continue;
@@ -481,7 +518,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
+    if constexpr (kPair) tmem_dealloc_pair(tmem_base, static_cast<uint32_t>(p.tmem_cols));
+    else tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
   }
   if (p.pair) cluster_sync();  // neither CTA leaves while the other may still write into it
 }
@@ -548,6 +586,9 @@ int pick_cols(const int* pw, int npw) {
 namespace {
 // Pairing halves the weight-tile traffic from L2; measured A/B on one GB300: +2..6% conv throughput.
 bool pair_mode_enabled() { return true; }
+// Convs whose weight tile is 128 or 256 channels wide run each pair's two M tiles as one cta_group::2
+// MMA, each CTA holding half of the weight tile.
+bool mma_pair_enabled() { return true; }
 }  // namespace
 
 cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
@@ -566,10 +607,12 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   // clusters of 2 share each weight tile (half loaded by each CTA, multicast to both)
   // (a batched GEMM has a different B per batch item, so only unbatched GEMMs pair up)
   const bool want_pair = pair_mode_enabled() && p.BN % 16 == 0 && (a.mode == 0 || a.batch == 1);
+  const bool mma_pair = want_pair && a.mode == 0 && (p.BN == 256 || p.BN == 128) && mma_pair_enabled();
   p.tmem_cols = 32;
   while (p.tmem_cols < 2 * p.msub * p.BN) p.tmem_cols <<= 1;  // two accumulators
   if (p.tmem_cols > 512) return cudaErrorInvalidValue;
-  const uint32_t stage_bytes = kABytes * p.msub + static_cast<uint32_t>(p.BN) * kBlockK * 2;
+  const uint32_t stage_bytes =
+      kABytes * p.msub + static_cast<uint32_t>(mma_pair ? p.BN / 2 : p.BN) * kBlockK * 2;
   p.stages = std::min(8, static_cast<int>((200u * 1024u) / stage_bytes));
   p.bias = a.bias;
   p.residual = a.residual;
@@ -665,10 +708,12 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   const size_t smem = 1024 + static_cast<size_t>(p.stages) * stage_bytes + (2 * p.stages + 4) * 8 + 16;
   static int attr_set = 0;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(conv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(conv_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-    (void)e;
+    for (auto* k : {conv_tc_kernel<false>, conv_tc_kernel<true>}) {
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+      (void)e;
+    }
     attr_set = 1;
   }
   p.n_mtiles = static_cast<int>(n_blocks / p.n_ntiles);
@@ -687,12 +732,14 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   if (!p.pair) {
     p.seq_count = p.n_tiles;
     const long long grid = std::min<long long>(n_blocks, n_sm);
-    conv_tc_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmA, tmB, p);
+    conv_tc_kernel<false><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmA, tmB, p);
     return cudaGetLastError();
   }
   p.seq_count = (p.n_mtiles + 1) / 2 * p.n_ntiles;
-  static int max_clusters = 0;
-  static size_t max_clusters_smem = 0;
+  auto* kern = mma_pair ? conv_tc_kernel<true> : conv_tc_kernel<false>;
+  static int max_clusters[2] = {0, 0};
+  static size_t max_clusters_smem[2] = {0, 0};
+  const int ki = mma_pair ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -704,16 +751,16 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (max_clusters <= 0 || max_clusters_smem != smem) {
+  if (max_clusters[ki] <= 0 || max_clusters_smem[ki] != smem) {
     cfg.gridDim = dim3(2 * (n_sm / 2));
     int mc = 0;
-    if (cudaOccupancyMaxActiveClusters(&mc, conv_tc_kernel, &cfg) != cudaSuccess || mc <= 0) mc = n_sm / 2;
-    max_clusters = mc;
-    max_clusters_smem = smem;
+    if (cudaOccupancyMaxActiveClusters(&mc, kern, &cfg) != cudaSuccess || mc <= 0) mc = n_sm / 2;
+    max_clusters[ki] = mc;
+    max_clusters_smem[ki] = smem;
   }
-  const long long clusters = std::min<long long>(p.seq_count, max_clusters);
+  const long long clusters = std::min<long long>(p.seq_count, max_clusters[ki]);
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-  cudaError_t e = cudaLaunchKernelEx(&cfg, conv_tc_kernel, tmA, tmB, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -376,50 +376,63 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int kc = 0;  // k blocks issued so far (all tiles)
+      // per-k-block state advances by counters (no divisions on this thread's critical path)
+      const int stages = p.stages, num_kb = p.num_kb, cchunks = p.cchunks;
+      int kc = 0;        // k blocks issued so far (all tiles)
+      int s = 0;         // ring slot of the next k block
+      uint32_t ph = 0;   // parity of that slot's current use
       bool ok = true;
       for (int seq = seq0; seq < p.seq_count && ok; seq += seq_step) {
         const TileCoord tc = seq_coord(p, seq, rank);
-        for (int kb = 0; kb < p.num_kb; ++kb, ++kc) {
-          const int s = kc % p.stages;
-          const int use = kc / p.stages;
-          if (use > 0 && !mbar_wait(&empty_bar[s], (use - 1) & 1, p.fault, p.limit_ns, 1)) {
+        int cc = 0, kt = 0, kh = 0, kw = 0, kcol = 0;  // kcol = tap * C_in_pad + cc * 64
+        for (int kb = 0; kb < num_kb; ++kb, ++kc) {
+          if (kc >= stages && !mbar_wait(&empty_bar[s], ph ^ 1u, p.fault, p.limit_ns, 1)) {
             ok = false;
             break;
           }
           uint8_t* a_dst = smem + s * stage_bytes;
           uint8_t* b_dst = a_dst + a_bytes;
-          if constexpr (kPair) {
-            // both CTAs' tiles complete on the leader's barrier (the leader alone runs the MMAs)
-            const uint32_t fb = cluster_map(smem_u32(&full_bar[s]), 0);
-            if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * stage_bytes);
-            const int tap = kb / p.cchunks;
-            const int cc = kb - tap * p.cchunks;
-            const int kt = tap / 9, kh = (tap / 3) % 3, kw = tap % 3;
-            const int ti = max(tc.t + kt - 2 + p.cache_frames, 0);
-            tma_load_5d_pair(a_dst, &tmA, fb, cc * kBlockK, tc.w0 + kw - 1, tc.h0 + kh - 1, ti, tc.b);
-            tma_load_2d_pair(b_dst, &tmB, fb, tap * p.C_in_pad + cc * kBlockK, tc.n0 + rank * (p.BN / 2));
-            continue;
-          }
-          mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
           if (p.mode == 0) {
-            const int tap = kb / p.cchunks;
-            const int cc = kb - tap * p.cchunks;
-            const int kt = tap / 9, kh = (tap / 3) % 3, kw = tap % 3;
             const int ti = max(tc.t + kt - 2 + p.cache_frames, 0);
-            tma_load_5d(a_dst, &tmA, &full_bar[s], cc * kBlockK, tc.w0 + kw - 1, tc.h0 + kh - 1, ti, tc.b);
-            if (p.pair)
-              tma_load_2d_mc(b_dst + rank * (b_bytes / 2), &tmB, &full_bar[s], tap * p.C_in_pad + cc * kBlockK,
-                             tc.n0 + rank * (p.BN / 2), pair_mask);
-            else
-              tma_load_2d(b_dst, &tmB, &full_bar[s], tap * p.C_in_pad + cc * kBlockK, tc.n0);
+            if constexpr (kPair) {
+              // both CTAs' tiles complete on the leader's barrier (the leader alone runs the MMAs)
+              const uint32_t fb = cluster_map(smem_u32(&full_bar[s]), 0);
+              if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * stage_bytes);
+              tma_load_5d_pair(a_dst, &tmA, fb, cc * kBlockK, tc.w0 + kw - 1, tc.h0 + kh - 1, ti, tc.b);
+              tma_load_2d_pair(b_dst, &tmB, fb, kcol, tc.n0 + rank * (p.BN / 2));
+            } else {
+              mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
+              tma_load_5d(a_dst, &tmA, &full_bar[s], cc * kBlockK, tc.w0 + kw - 1, tc.h0 + kh - 1, ti, tc.b);
+              if (p.pair)
+                tma_load_2d_mc(b_dst + rank * (b_bytes / 2), &tmB, &full_bar[s], kcol, tc.n0 + rank * (p.BN / 2),
+                               pair_mask);
+              else
+                tma_load_2d(b_dst, &tmB, &full_bar[s], kcol, tc.n0);
+            }
+            // next (tap, channel chunk): channel chunks innermost, then kw, kh, kt
+            kcol += kBlockK;
+            if (++cc == cchunks) {
+              cc = 0;
+              if (++kw == 3) {
+                kw = 0;
+                if (++kh == 3) {
+                  kh = 0;
+                  ++kt;
+                }
+              }
+            }
           } else {
+            mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
             tma_load_3d(a_dst, &tmA, &full_bar[s], kb * kBlockK, tc.m0, tc.bat);
             if (p.pair)
               tma_load_3d_mc(b_dst + rank * (b_bytes / 2), &tmB, &full_bar[s], kb * kBlockK,
                              tc.n0 + rank * (p.BN / 2), tc.bat, pair_mask);
             else
               tma_load_3d(b_dst, &tmB, &full_bar[s], kb * kBlockK, tc.n0, tc.bat);
+          }
+          if (++s == stages) {
+            s = 0;
+            ph ^= 1u;
           }
         }
       }
@@ -437,25 +450,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0 && (!kPair || rank == 0)) {
       const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * kBlockM : kBlockM, static_cast<uint32_t>(p.BN));
-      int kc = 0, it = 0;
+      const int stages = p.stages, num_kb = p.num_kb, msub = p.msub;
+      const uint32_t smem_base = smem_u32(smem);
+      const uint32_t sub_cols = static_cast<uint32_t>(p.BN);
+      int s = 0, it = 0;
+      uint32_t ph = 0;
       bool ok = true;
       for (int seq = seq0; seq < p.seq_count && ok; seq += seq_step, ++it) {
         const int acc = it & 1, u = it >> 1;
         if (u > 0 && !mbar_wait(&acce_bar[acc], (u - 1) & 1, p.fault, p.limit_ns, 6)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * acc_stride);
-        for (int kb = 0; kb < p.num_kb; ++kb, ++kc) {
-          const int s = kc % p.stages;
-          if (!mbar_wait(&full_bar[s], (kc / p.stages) & 1, p.fault, p.limit_ns, 3)) {
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full_bar[s], ph, p.fault, p.limit_ns, 3)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + s * stage_bytes);
+          const uint32_t a_addr = smem_base + static_cast<uint32_t>(s) * stage_bytes;
           const uint64_t bdesc = sdesc_kmajor_sw128(a_addr + a_bytes);
-          for (int sub = 0; sub < p.msub; ++sub) {
-            const uint64_t adesc = sdesc_kmajor_sw128(a_addr + sub * kABytes);
-            const uint32_t d_sub = d_tmem + static_cast<uint32_t>(sub * p.BN);
+          for (int sub = 0; sub < msub; ++sub) {
+            const uint64_t adesc = sdesc_kmajor_sw128(a_addr + static_cast<uint32_t>(sub) * kABytes);
+            const uint32_t d_sub = d_tmem + static_cast<uint32_t>(sub) * sub_cols;
 #pragma unroll
             for (int k = 0; k < kBlockK / 16; ++k) {
               // advance 16 bf16 (32 B) along K inside the 128-byte swizzle atom
@@ -470,6 +486,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (kPair) tc_commit_pair_mc(&empty_bar[s], pair_mask);
           else if (p.pair) tc_commit_mc(&empty_bar[s], pair_mask);
           else tc_commit(&empty_bar[s]);
+          if (++s == stages) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
         if constexpr (kPair) tc_commit_pair_mc(&accf_bar[acc], pair_mask);
         else tc_commit(&accf_bar[acc]);

@@ -47,6 +47,7 @@ struct TcParams {
   int num_kb, cchunks;
   int N_real, BN, n_ntiles, tmem_cols, stages;
   int msub;  // 128-pixel MMA sub-tiles per tile (2 when BN <= 128: both share each weight tile)
+  int ks;    // k blocks (64 channels of one tap) per shared-memory stage: 1 or 2
   const float* bias;
   const void* residual;
   int res_f32;
@@ -331,9 +332,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t b_bytes = static_cast<uint32_t>(kPair ? p.BN / 2 : p.BN) * kBlockK * 2;
-  const uint32_t a_bytes = kABytes * static_cast<uint32_t>(p.msub);
-  const uint32_t stage_bytes = a_bytes + b_bytes;
+  // one stage = ks k blocks: [A of k block 0 .. ks-1][B of k block 0 .. ks-1]
+  const uint32_t b_bytes = static_cast<uint32_t>(kPair ? p.BN / 2 : p.BN) * kBlockK * 2;  // per k block
+  const uint32_t a_bytes = kABytes * static_cast<uint32_t>(p.msub);                        // per k block
+  const int ks = p.ks;
+  const uint32_t stage_bytes = static_cast<uint32_t>(ks) * (a_bytes + b_bytes);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + p.stages * stage_bytes);
   uint64_t* empty_bar = full_bar + p.stages;
   uint64_t* accf_bar = empty_bar + p.stages;  // [2] accumulator full (MMA -> epilogue)
@@ -377,51 +380,63 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       // per-k-block state advances by counters (no divisions on this thread's critical path)
-      const int stages = p.stages, num_kb = p.num_kb, cchunks = p.cchunks;
-      int kc = 0;        // k blocks issued so far (all tiles)
+      const int stages = p.stages, num_st = p.num_kb / ks, cchunks = p.cchunks;
+      int kc = 0;        // stages filled so far (all tiles)
       int s = 0;         // ring slot of the next k block
       uint32_t ph = 0;   // parity of that slot's current use
       bool ok = true;
       for (int seq = seq0; seq < p.seq_count && ok; seq += seq_step) {
         const TileCoord tc = seq_coord(p, seq, rank);
         int cc = 0, kt = 0, kh = 0, kw = 0, kcol = 0;  // kcol = tap * C_in_pad + cc * 64
-        for (int kb = 0; kb < num_kb; ++kb, ++kc) {
+        int kb = 0;                                    // k block (GEMM mode)
+        for (int st = 0; st < num_st; ++st, ++kc) {
           if (kc >= stages && !mbar_wait(&empty_bar[s], ph ^ 1u, p.fault, p.limit_ns, 1)) {
             ok = false;
             break;
           }
           uint8_t* a_dst = smem + s * stage_bytes;
-          uint8_t* b_dst = a_dst + a_bytes;
+          uint8_t* b_dst = a_dst + ks * a_bytes;
           if (p.mode == 0) {
-            const int ti = max(tc.t + kt - 2 + p.cache_frames, 0);
+            uint32_t fb = 0;
             if constexpr (kPair) {
               // both CTAs' tiles complete on the leader's barrier (the leader alone runs the MMAs)
-              const uint32_t fb = cluster_map(smem_u32(&full_bar[s]), 0);
+              fb = cluster_map(smem_u32(&full_bar[s]), 0);
               if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * stage_bytes);
-              tma_load_5d_pair(a_dst, &tmA, fb, cc * kBlockK, tc.w0 + kw - 1, tc.h0 + kh - 1, ti, tc.b);
-              tma_load_2d_pair(b_dst, &tmB, fb, kcol, tc.n0 + rank * (p.BN / 2));
             } else {
               mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
-              tma_load_5d(a_dst, &tmA, &full_bar[s], cc * kBlockK, tc.w0 + kw - 1, tc.h0 + kh - 1, ti, tc.b);
-              if (p.pair)
-                tma_load_2d_mc(b_dst + rank * (b_bytes / 2), &tmB, &full_bar[s], kcol, tc.n0 + rank * (p.BN / 2),
-                               pair_mask);
-              else
-                tma_load_2d(b_dst, &tmB, &full_bar[s], kcol, tc.n0);
             }
-            // next (tap, channel chunk): channel chunks innermost, then kw, kh, kt
-            kcol += kBlockK;
-            if (++cc == cchunks) {
-              cc = 0;
-              if (++kw == 3) {
-                kw = 0;
-                if (++kh == 3) {
-                  kh = 0;
-                  ++kt;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              if (j == ks) break;
+              const int ti = max(tc.t + kt - 2 + p.cache_frames, 0);
+              uint8_t* aj = a_dst + j * a_bytes;
+              uint8_t* bj = b_dst + j * b_bytes;
+              if constexpr (kPair) {
+                tma_load_5d_pair(aj, &tmA, fb, cc * kBlockK, tc.w0 + kw - 1, tc.h0 + kh - 1, ti, tc.b);
+                tma_load_2d_pair(bj, &tmB, fb, kcol, tc.n0 + rank * (p.BN / 2));
+              } else {
+                tma_load_5d(aj, &tmA, &full_bar[s], cc * kBlockK, tc.w0 + kw - 1, tc.h0 + kh - 1, ti, tc.b);
+                if (p.pair)
+                  tma_load_2d_mc(bj + rank * (b_bytes / 2), &tmB, &full_bar[s], kcol, tc.n0 + rank * (p.BN / 2),
+                                 pair_mask);
+                else
+                  tma_load_2d(bj, &tmB, &full_bar[s], kcol, tc.n0);
+              }
+              // next (tap, channel chunk): channel chunks innermost, then kw, kh, kt
+              kcol += kBlockK;
+              if (++cc == cchunks) {
+                cc = 0;
+                if (++kw == 3) {
+                  kw = 0;
+                  if (++kh == 3) {
+                    kh = 0;
+                    ++kt;
+                  }
                 }
               }
             }
           } else {
+            // GEMM mode: one k block per stage
             mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
             tma_load_3d(a_dst, &tmA, &full_bar[s], kb * kBlockK, tc.m0, tc.bat);
             if (p.pair)
@@ -429,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              tc.n0 + rank * (p.BN / 2), tc.bat, pair_mask);
             else
               tma_load_3d(b_dst, &tmB, &full_bar[s], kb * kBlockK, tc.n0, tc.bat);
+            ++kb;
           }
           if (++s == stages) {
             s = 0;
@@ -450,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0 && (!kPair || rank == 0)) {
       const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * kBlockM : kBlockM, static_cast<uint32_t>(p.BN));
-      const int stages = p.stages, num_kb = p.num_kb, msub = p.msub;
+      const int stages = p.stages, num_st = p.num_kb / ks, msub = p.msub;
       const uint32_t smem_base = smem_u32(smem);
       const uint32_t sub_cols = static_cast<uint32_t>(p.BN);
       int s = 0, it = 0;
@@ -461,26 +477,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u > 0 && !mbar_wait(&acce_bar[acc], (u - 1) & 1, p.fault, p.limit_ns, 6)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * acc_stride);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int st = 0; st < num_st; ++st) {
           if (!mbar_wait(&full_bar[s], ph, p.fault, p.limit_ns, 3)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a_addr = smem_base + static_cast<uint32_t>(s) * stage_bytes;
-          const uint64_t bdesc = sdesc_kmajor_sw128(a_addr + a_bytes);
-          for (int sub = 0; sub < msub; ++sub) {
-            const uint64_t adesc = sdesc_kmajor_sw128(a_addr + static_cast<uint32_t>(sub) * kABytes);
-            const uint32_t d_sub = d_tmem + static_cast<uint32_t>(sub) * sub_cols;
+          const uint32_t b_addr = a_addr + static_cast<uint32_t>(ks) * a_bytes;
 #pragma unroll
-            for (int k = 0; k < kBlockK / 16; ++k) {
-              // advance 16 bf16 (32 B) along K inside the 128-byte swizzle atom
-              if constexpr (kPair)
-                tc_mma_bf16_pair(d_sub, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k),
-                                 idesc, (kb > 0 || k > 0) ? 1u : 0u);
-              else
-                tc_mma_bf16(d_sub, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k),
-                            idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          for (int j = 0; j < 2; ++j) {
+            if (j == ks) break;
+            const uint64_t bdesc = sdesc_kmajor_sw128(b_addr + static_cast<uint32_t>(j) * b_bytes);
+#pragma unroll
+            for (int sub = 0; sub < 2; ++sub) {
+              if (sub == msub) break;
+              const uint64_t adesc =
+                  sdesc_kmajor_sw128(a_addr + static_cast<uint32_t>(j) * a_bytes + static_cast<uint32_t>(sub) * kABytes);
+              const uint32_t d_sub = d_tmem + static_cast<uint32_t>(sub) * sub_cols;
+              const uint32_t first = (st == 0 && j == 0) ? 1u : 0u;
+#pragma unroll
+              for (int k = 0; k < kBlockK / 16; ++k) {
+                // advance 16 bf16 (32 B) along K inside the 128-byte swizzle atom
+                const uint32_t accum = (first && k == 0) ? 0u : 1u;
+                if constexpr (kPair)
+                  tc_mma_bf16_pair(d_sub, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k),
+                                   idesc, accum);
+                else
+                  tc_mma_bf16(d_sub, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k),
+                              idesc, accum);
+              }
             }
           }
           if constexpr (kPair) tc_commit_pair_mc(&empty_bar[s], pair_mask);
@@ -631,8 +657,11 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   p.tmem_cols = 32;
   while (p.tmem_cols < 2 * p.msub * p.BN) p.tmem_cols <<= 1;  // two accumulators
   if (p.tmem_cols > 512) return cudaErrorInvalidValue;
-  const uint32_t stage_bytes =
-      kABytes * p.msub + static_cast<uint32_t>(mma_pair ? p.BN / 2 : p.BN) * kBlockK * 2;
+  const uint32_t kb_bytes = kABytes * p.msub + static_cast<uint32_t>(mma_pair ? p.BN / 2 : p.BN) * kBlockK * 2;
+  // MMA pairs take two k blocks per stage (half the barrier round trips per MMA) where two such stages
+  // fit; measured on one GB300: +11% on a 512->512 conv (3 stages), +12% on 128->128 (2 stages)
+  p.ks = (mma_pair && (a.C_in_pad / kBlockK) % 2 == 0 && 2u * 2u * kb_bytes <= 200u * 1024u) ? 2 : 1;
+  const uint32_t stage_bytes = static_cast<uint32_t>(p.ks) * kb_bytes;
   p.stages = std::min(8, static_cast<int>((200u * 1024u) / stage_bytes));
   p.bias = a.bias;
   p.residual = a.residual;

@@ -300,6 +300,21 @@ VAE_DEV uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
+// Same layout with 8-row groups `sbo_bytes` apart, starting at any 128-byte row of a swizzled block
+// (the block itself 1024-byte aligned): the rows of a halo tile that one tap reads.  The 128-byte
+// swizzle follows the absolute shared-memory address bits, as the TMA that wrote the block applied
+// it, so the base-offset field stays 0 (measured: setting it to the start row's phase gives wrong
+// products).
+VAE_DEV uint64_t sdesc_kmajor_sw128_rows(uint32_t saddr, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1u) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 D, M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t m, uint32_t n) {
   return (1u << 4)                 // D format: f32

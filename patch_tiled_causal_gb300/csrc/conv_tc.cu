@@ -48,6 +48,10 @@ struct TcParams {
   int N_real, BN, n_ntiles, tmem_cols, stages;
   int msub;  // 128-pixel MMA sub-tiles per tile (2 when BN <= 128: both share each weight tile)
   int ks;    // k blocks (64 channels of one tap) per shared-memory stage: 1 or 2
+  // halo mode (narrow convs): one stage = one (kt, 64-channel chunk) halo box of (rows_t + 2) x
+  // (cols_t + 2) pixels that all 9 spatial taps read in place, plus those taps' weight tiles
+  int halo;
+  uint32_t halo_a_bytes, halo_tx, halo_stage;
   const float* bias;
   const void* residual;
   int res_f32;
@@ -336,7 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_bytes = static_cast<uint32_t>(kPair ? p.BN / 2 : p.BN) * kBlockK * 2;  // per k block
   const uint32_t a_bytes = kABytes * static_cast<uint32_t>(p.msub);                        // per k block
   const int ks = p.ks;
-  const uint32_t stage_bytes = static_cast<uint32_t>(ks) * (a_bytes + b_bytes);
+  const bool halo = !kPair && p.halo;
+  const uint32_t stage_bytes = halo ? p.halo_stage : static_cast<uint32_t>(ks) * (a_bytes + b_bytes);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + p.stages * stage_bytes);
   uint64_t* empty_bar = full_bar + p.stages;
   uint64_t* accf_bar = empty_bar + p.stages;  // [2] accumulator full (MMA -> epilogue)
@@ -378,7 +383,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    if constexpr (!kPair) {
+      if (p.halo) {
+        if (lane == 0) {
+          const int stages = p.stages, cchunks = p.cchunks;
+          const uint32_t wt_bytes = static_cast<uint32_t>(p.BN) * kBlockK * 2;
+          int kc = 0, s = 0;
+          uint32_t ph = 0;
+          bool ok = true;
+          for (int seq = seq0; seq < p.seq_count && ok; seq += seq_step) {
+            const TileCoord tc = seq_coord(p, seq, rank);
+            for (int kt = 0; kt < 3 && ok; ++kt) {
+              const int ti = max(tc.t + kt - 2 + p.cache_frames, 0);
+              for (int cc = 0; cc < cchunks; ++cc, ++kc) {
+                if (kc >= stages && !mbar_wait(&empty_bar[s], ph ^ 1u, p.fault, p.limit_ns, 1)) {
+                  ok = false;
+                  break;
+                }
+                uint8_t* a_dst = smem + s * stage_bytes;
+                uint8_t* b_dst = a_dst + p.halo_a_bytes;
+                mbar_arrive_expect_tx(&full_bar[s], p.halo_tx);
+                tma_load_5d(a_dst, &tmA, &full_bar[s], cc * kBlockK, tc.w0 - 1, tc.h0 - 1, ti, tc.b);
+#pragma unroll 1
+                for (int t9 = 0; t9 < 9; ++t9)
+                  tma_load_2d(b_dst + t9 * wt_bytes, &tmB, &full_bar[s], (kt * 9 + t9) * p.C_in_pad + cc * kBlockK,
+                              tc.n0);
+                if (++s == stages) {
+                  s = 0;
+                  ph ^= 1u;
+                }
+              }
+            }
+          }
+          for (int k = max(0, kc - p.stages); k < kc; ++k)
+            mbar_wait(&full_bar[k % p.stages], (k / p.stages) & 1, p.fault, p.limit_ns, 2);
+        }
+      }
+    }
+    if (lane == 0 && !halo) {
       // per-k-block state advances by counters (no divisions on this thread's critical path)
       const int stages = p.stages, num_st = p.num_kb / ks, cchunks = p.cchunks;
       int kc = 0;        // stages filled so far (all tiles)
@@ -464,7 +506,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0 && (!kPair || rank == 0)) {
+    if constexpr (!kPair) {
+      if (p.halo) {
+        if (lane == 0) {
+          // A rows of tap (kh, kw) for sub-tile `sub`: box row (sub * rows_t / 2 + kh) * (cols_t + 2) + kw
+          // onward, one 8-pixel output row per 8-row group, groups one box row apart
+          const uint32_t idesc = idesc_bf16_f32(kBlockM, static_cast<uint32_t>(p.BN));
+          const int stages = p.stages, num_st = 3 * p.cchunks;
+          const uint32_t smem_base = smem_u32(smem);
+          const uint32_t box_w = static_cast<uint32_t>(p.cols_t + 2);
+          const uint32_t sbo = box_w * 128u;
+          const uint32_t half_rows = static_cast<uint32_t>(p.rows_t / 2);
+          const uint32_t wt_bytes = static_cast<uint32_t>(p.BN) * kBlockK * 2;
+          int s = 0, it = 0;
+          uint32_t ph = 0;
+          bool ok = true;
+          for (int seq = seq0; seq < p.seq_count && ok; seq += seq_step, ++it) {
+            const int acc = it & 1, u = it >> 1;
+            if (u > 0 && !mbar_wait(&acce_bar[acc], (u - 1) & 1, p.fault, p.limit_ns, 6)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * acc_stride);
+            for (int st = 0; st < num_st; ++st) {
+              if (!mbar_wait(&full_bar[s], ph, p.fault, p.limit_ns, 3)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t a_addr = smem_base + static_cast<uint32_t>(s) * stage_bytes;
+              const uint32_t b_addr = a_addr + p.halo_a_bytes;
+#pragma unroll 1
+              for (int t9 = 0; t9 < 9; ++t9) {
+                const uint32_t kh = static_cast<uint32_t>(t9 / 3), kw = static_cast<uint32_t>(t9 % 3);
+                const uint64_t bdesc = sdesc_kmajor_sw128(b_addr + static_cast<uint32_t>(t9) * wt_bytes);
+#pragma unroll
+                for (int sub = 0; sub < 2; ++sub) {
+                  const uint32_t row0 = (static_cast<uint32_t>(sub) * half_rows + kh) * box_w + kw;
+                  const uint64_t adesc = sdesc_kmajor_sw128_rows(a_addr + row0 * 128u, sbo);
+                  const uint32_t d_sub = d_tmem + static_cast<uint32_t>(sub * p.BN);
+#pragma unroll
+                  for (int k = 0; k < kBlockK / 16; ++k)
+                    tc_mma_bf16(d_sub, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k),
+                                idesc, (st == 0 && t9 == 0 && k == 0) ? 0u : 1u);
+                }
+              }
+              tc_commit(&empty_bar[s]);
+              if (++s == stages) {
+                s = 0;
+                ph ^= 1u;
+              }
+            }
+            tc_commit(&accf_bar[acc]);
+          }
+        }
+      }
+    }
+    if (lane == 0 && (!kPair || rank == 0) && !halo) {
       const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * kBlockM : kBlockM, static_cast<uint32_t>(p.BN));
       const int stages = p.stages, num_st = p.num_kb / ks, msub = p.msub;
       const uint32_t smem_base = smem_u32(smem);
@@ -635,6 +731,12 @@ bool pair_mode_enabled() { return true; }
 // Convs whose weight tile is 128 or 256 channels wide run each pair's two M tiles as one cta_group::2
 // MMA, each CTA holding half of the weight tile.
 bool mma_pair_enabled() { return true; }
+// Convs at most 32 channels wide (the Wan-shaped pixel head) load one halo box per (kt, channel chunk)
+// that the 9 spatial taps share, instead of 9 tap-shifted boxes (measured: 256->12 head on
+// 81x352x640 23.9 -> 16.4 ms; the 48-wide LTX head is slower that way, 3.7 -> 4.0 ms).
+bool halo_mode_enabled() { return true; }
+constexpr int kHaloCols = 8;   // tile width: one 8-row MMA core group per output row
+constexpr int kHaloRows = 32;  // tile height: two 16-row sub-tiles of 128 pixels
 }  // namespace
 
 cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
@@ -652,7 +754,8 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   p.msub = p.BN <= 128 ? 2 : 1;
   // clusters of 2 share each weight tile (half loaded by each CTA, multicast to both)
   // (a batched GEMM has a different B per batch item, so only unbatched GEMMs pair up)
-  const bool want_pair = pair_mode_enabled() && p.BN % 16 == 0 && (a.mode == 0 || a.batch == 1);
+  p.halo = (a.mode == 0 && p.BN <= 32 && halo_mode_enabled()) ? 1 : 0;
+  const bool want_pair = pair_mode_enabled() && p.BN % 16 == 0 && (a.mode == 0 || a.batch == 1) && !p.halo;
   const bool mma_pair = want_pair && a.mode == 0 && (p.BN == 256 || p.BN == 128) && mma_pair_enabled();
   p.tmem_cols = 32;
   while (p.tmem_cols < 2 * p.msub * p.BN) p.tmem_cols <<= 1;  // two accumulators
@@ -661,8 +764,18 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   // MMA pairs take two k blocks per stage (half the barrier round trips per MMA) where two such stages
   // fit; measured on one GB300: +11% on a 512->512 conv (3 stages), +12% on 128->128 (2 stages)
   p.ks = (mma_pair && (a.C_in_pad / kBlockK) % 2 == 0 && 2u * 2u * kb_bytes <= 200u * 1024u) ? 2 : 1;
-  const uint32_t stage_bytes = static_cast<uint32_t>(p.ks) * kb_bytes;
+  uint32_t stage_bytes = static_cast<uint32_t>(p.ks) * kb_bytes;
+  if (p.halo) {
+    // box of (32 + 2) x (8 + 2) pixels x 64 channels, then the 9 taps' BN x 64 weight tiles
+    const uint32_t box = static_cast<uint32_t>(kHaloRows + 2) * (kHaloCols + 2) * kBlockK * 2;
+    p.halo_a_bytes = (box + 1023u) & ~1023u;
+    p.halo_tx = box + 9u * static_cast<uint32_t>(p.BN) * kBlockK * 2;
+    p.halo_stage = p.halo_a_bytes + 9u * static_cast<uint32_t>(p.BN) * kBlockK * 2;
+    p.ks = 1;
+    stage_bytes = p.halo_stage;
+  }
   p.stages = std::min(8, static_cast<int>((200u * 1024u) / stage_bytes));
+  if (p.stages < 2) return cudaErrorInvalidValue;
   p.bias = a.bias;
   p.residual = a.residual;
   p.res_f32 = a.res_f32;
@@ -681,7 +794,7 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
     p.nph = a.nph; p.npw = a.npw;
     for (int i = 0; i <= a.nph; ++i) p.ph_edges[i] = a.ph_edges[i];
     for (int j = 0; j <= a.npw; ++j) p.pw_edges[j] = a.pw_edges[j];
-    p.cols_t = pick_cols(a.pw_edges, a.npw);
+    p.cols_t = p.halo ? kHaloCols : pick_cols(a.pw_edges, a.npw);
     p.rows_t = kBlockM * p.msub / p.cols_t;
     p.trow_prefix[0] = 0;
     for (int i = 0; i < a.nph; ++i)
@@ -713,6 +826,10 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
     uint64_t dims[5] = {C, (uint64_t)a.W, (uint64_t)a.H, (uint64_t)a.T_in, (uint64_t)a.B};
     uint64_t strides[4] = {C * 2, C * 2 * a.W, C * 2 * a.W * a.H, C * 2 * a.W * a.H * xTa};
     uint32_t box[5] = {64u, (uint32_t)p.cols_t, (uint32_t)p.rows_t, 1u, 1u};
+    if (p.halo) {
+      box[1] = static_cast<uint32_t>(p.cols_t + 2);
+      box[2] = static_cast<uint32_t>(p.rows_t + 2);
+    }
     if (!make_map(&tmA, a.x, 5, dims, strides, box)) return cudaErrorInvalidValue;
     const uint64_t K = 27ull * C;
     uint64_t wd[2] = {K, (uint64_t)a.N_pad};

@@ -100,6 +100,9 @@ CONV_CASES = [
     (1, 3, 8, 11, 64, 48, 2, 2, 0, (1, 4, 4), False, True, False),
     (1, 2, 7, 6, 64, 12, 1, 2, 0, (1, 2, 2), False, True, False),
     (1, 2, 33, 40, 64, 320, 1, 1, 0, (1, 1, 1), False, False, False),
+    # narrow convs (at most 32 channels): one shared halo box per (kt, channel chunk)
+    (1, 3, 21, 19, 128, 32, 2, 3, 2, (1, 1, 1), False, False, True),
+    (2, 2, 35, 17, 64, 16, 3, 1, 0, (1, 2, 2), False, True, False),
 ]
 
 
@@ -130,6 +133,13 @@ def test_conv_bit_identical_across_patch_counts(vd, dt):
     dtc = vd.VAE_BF16 if dt == "bf16" else vd.VAE_FP32
     outs = [_conv_case(vd, 1, 2, 24, 40, 64, 128, ph, pw, 0, (1, 1, 1), False, False, dtc, True, 40)[0]
             for ph, pw in ((1, 1), (2, 2), (2, 4), (4, 8), (3, 5))]
+    for o in outs[1:]:
+        np.testing.assert_array_equal(o, outs[0])
+
+
+def test_conv_halo_path_bit_identical_across_patch_counts(vd):
+    outs = [_conv_case(vd, 1, 2, 40, 36, 64, 16, ph, pw, 2, (1, 1, 1), False, False, vd.VAE_BF16, True, 45)[0]
+            for ph, pw in ((1, 1), (2, 2), (3, 4), (5, 2))]
     for o in outs[1:]:
         np.testing.assert_array_equal(o, outs[0])
 

@@ -68,6 +68,17 @@ VAE_DEV void add128(unsigned long long& lo, unsigned long long& hi, unsigned lon
   lo = n;
 }
 
+// max(a, |x|) that is NaN when x is NaN (so a range test on the result also catches NaN)
+VAE_DEV float max_abs_nan(float a, float x) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(fabsf(x)));
+  return r;
+}
+
+// q = round(x * 2^18) for |x| < 16 (|q| < 2^22): adding 1.5 * 2^23 rounds x * 2^18 to the nearest
+// integer (ties to even, as the float-to-int conversion below) and leaves it in the low mantissa bits.
+VAE_DEV int quantize_small(float x) { return __float_as_int(fmaf(x, 262144.f, 12582912.f)) - 0x4B400000; }
+
 VAE_DEV int quantize(float x, uint32_t* fault) {
   if (!(fabsf(x) < 8192.f)) {  // also catches NaN
     raise_fault(fault, FAULT_RANGE, 30);
@@ -119,6 +130,31 @@ __global__ void __launch_bounds__(256) gn_stats_kernel(const __grid_constant__ G
 #pragma unroll
           for (int e = 0; e < 8; ++e) v[u][e] = 0.f;
         }
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = max_abs_nan(amax, v[u][e]);
+      if (amax < 16.f) {
+        // every |q| < 2^22: 32-bit sums of q, q^2 summed in 64 bits (32 of them < 2^49)
+#pragma unroll
+        for (int k = 0; k < GPV; ++k) {
+          int s1f = 0;
+          unsigned long long sqf = 0;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+#pragma unroll
+            for (int e = k * (8 / GPV); e < (k + 1) * (8 / GPV); ++e) {
+              const int qv = quantize_small(v[u][e]);
+              s1f += qv;
+              sqf += static_cast<unsigned long long>(static_cast<long long>(qv) * qv);
+            }
+          }
+          s1[k] += s1f;
+          add128(lo[k], hi[k], sqf, 0ull);
+        }
+        continue;
       }
 #pragma unroll
       for (int k = 0; k < GPV; ++k) {

@@ -843,6 +843,221 @@ __global__ void __launch_bounds__(256, 4) blend_grid_kernel(const __grid_constan
   }
 }
 
+// axis_cover with the (at most 2) results in scalars, so they stay in registers.
+VAE_DEV int axis_cover2(const BlendGridParams& p, int ax, int x, int& i0, int& i1, float& w0, float& w1) {
+  int k = 0;
+  i0 = i1 = 0;
+  w0 = w1 = 0.f;
+  for (int i = 0; i < p.n[ax] && k < 2; ++i) {
+    const int l = x - p.s0[ax][i];
+    if (l < 0 || l >= p.len[ax][i]) continue;
+    const float w = ramp_w(l, p.len[ax][i], p.lo[ax][i], p.hi[ax][i]);
+    if (k == 0) {
+      i0 = i;
+      w0 = w;
+    } else {
+      i1 = i;
+      w1 = w;
+    }
+    ++k;
+  }
+  const float inv = __fdividef(1.f, w0 + w1);
+  w0 *= inv;
+  w1 *= inv;
+  return k;
+}
+
+// Raw 8-element loads, converted only when used (so several can be in flight per thread).
+template <typename T> struct Raw8;
+template <> struct Raw8<__nv_bfloat16> {
+  uint4 r;
+  VAE_DEV void load(const __nv_bfloat16* p) { r = *reinterpret_cast<const uint4*>(p); }
+  VAE_DEV void get(float* v) const {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+};
+template <> struct Raw8<float> {
+  float4 a, b;
+  VAE_DEV void load(const float* p) {
+    a = reinterpret_cast<const float4*>(p)[0];
+    b = reinterpret_cast<const float4*>(p)[1];
+  }
+  VAE_DEV void get(float* v) const {
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+};
+
+// Grid blend, lean form for grids with at most kG2Cols column intervals: per 8-pixel vector one
+// packed shared-memory word (first column interval, count, offsets into both intervals' rows) and
+// the first interval's normalised column weights (the second's are 1 minus them); per warp and row
+// the source row pointers of each (t, y) pair and column interval and the pair weights in
+// registers.  Each lane takes two vectors of the row at a time and issues all their source loads
+// before summing.  Rows whose (t, y) is covered by more than two pairs take the general loop.
+constexpr int kG2Cols = 16;
+template <typename TT, typename TO>
+__global__ void __launch_bounds__(256, 3) blend_grid2_kernel(const __grid_constant__ BlendGridParams p) {
+  __shared__ int4 vinfo[kGridMaxVec];
+  __shared__ float4 vw0[kGridMaxVec][2];
+  __shared__ const TT* rowp[8][4][kG2Cols];
+  const int nv = (p.W + 7) / 8;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    const int x0 = v * 8;
+    int c0 = -1, nc = 0;
+    for (int i = 0; i < p.n[2]; ++i) {
+      const int l = x0 - p.s0[2][i];
+      if (l + 8 <= 0 || l >= p.len[2][i]) continue;
+      if (c0 < 0) c0 = i;
+      ++nc;
+    }
+    if (c0 < 0) c0 = 0;
+    int lx[2] = {0, 0};
+    bool fast = nc >= 1 && nc <= 2 && x0 + 8 <= p.W;
+    float w0[8];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (j < nc && nc <= 2) {
+        lx[j] = x0 - p.s0[2][c0 + j];
+        const int nw = p.len[2][c0 + j];
+        fast = fast && lx[j] >= 0 && lx[j] + 8 <= nw && ((lx[j] | nw) & 7) == 0;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float a0 = 0.f, a1 = 0.f;
+      if (nc >= 1 && nc <= 2 && x0 + e < p.W) {
+        const int l0 = lx[0] + e, n0 = p.len[2][c0];
+        if (l0 >= 0 && l0 < n0) a0 = ramp_w(l0, n0, p.lo[2][c0], p.hi[2][c0]);
+        if (nc == 2) {
+          const int l1 = lx[1] + e, n1 = p.len[2][c0 + 1];
+          if (l1 >= 0 && l1 < n1) a1 = ramp_w(l1, n1, p.lo[2][c0 + 1], p.hi[2][c0 + 1]);
+        }
+      }
+      const float sum = a0 + a1;
+      w0[e] = sum > 0.f ? __fdividef(a0, sum) : 0.f;
+    }
+    vinfo[v] = make_int4(c0 | (nc << 8) | (fast ? 1 << 12 : 0), lx[0], lx[1], 0);
+    vw0[v][0] = make_float4(w0[0], w0[1], w0[2], w0[3]);
+    vw0[v][1] = make_float4(w0[4], w0[5], w0[6], w0[7]);
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int blocks_per_t = (p.H + kGridRows - 1) / kGridRows;
+  const int pl = blockIdx.y;
+  const int t = blockIdx.x / blocks_per_t;
+  const int y_base = (blockIdx.x - t * blocks_per_t) * kGridRows;
+  int ia0, ia1;
+  float wa0, wa1;
+  const int na = axis_cover2(p, 0, t, ia0, ia1, wa0, wa1);
+  const int n2 = p.n[2];
+  for (int r = warp; r < kGridRows; r += 8) {
+    const int y = y_base + r;
+    if (y >= p.H) break;
+    int ib0, ib1;
+    float wb0, wb1;
+    const int nb = axis_cover2(p, 1, y, ib0, ib1, wb0, wb1);
+    const int npair = na * nb;
+    for (int e = lane; e < npair * n2; e += 32) {
+      const int q = e / n2, cc = e - q * n2;
+      const int qa = nb == 2 ? q >> 1 : q, qb = nb == 2 ? q & 1 : 0;
+      const int a = qa ? ia1 : ia0, b = qb ? ib1 : ib0;
+      const int64_t plane_in = static_cast<int64_t>(p.len[0][a]) * p.len[1][b];
+      rowp[warp][q][cc] = static_cast<const TT*>(p.ptr[(a * p.n[1] + b) * n2 + cc]) +
+                          ((pl * plane_in + static_cast<int64_t>(t - p.s0[0][a]) * p.len[1][b]) + (y - p.s0[1][b])) *
+                              p.len[2][cc];
+    }
+    __syncwarp();
+    float wq[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int qa = nb == 2 ? q >> 1 : q, qb = nb == 2 ? q & 1 : 0;
+      wq[q] = q < npair ? (qa ? wa1 : wa0) * (qb ? wb1 : wb0) : 0.f;
+    }
+    TO* orow = static_cast<TO*>(p.out) + ((static_cast<int64_t>(pl) * p.T + t) * p.H + y) * p.W;
+    for (int vb = lane; vb < nv; vb += 64) {
+      int4 inf[2];
+      Raw8<TT> raw[2][2][2];  // [vector][pair][interval]
+      bool fast[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int v = vb + 32 * u;
+        fast[u] = false;
+        if (v < nv) {
+          inf[u] = vinfo[v];
+          fast[u] = ((inf[u].x >> 12) & 1) && npair <= 2;
+          if (fast[u]) {
+            const int cv = inf[u].x & 255, ncv = (inf[u].x >> 8) & 15;
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+#pragma unroll
+              for (int j = 0; j < 2; ++j)
+                if (q < npair && j < ncv) raw[u][q][j].load(rowp[warp][q][cv + j] + (j ? inf[u].z : inf[u].y));
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int v = vb + 32 * u;
+        if (v >= nv) break;
+        const int x0 = v * 8;
+        float acc[8];
+        if (fast[u]) {
+          const int ncv = (inf[u].x >> 8) & 15;
+          const float4 wl = vw0[v][0], wh = vw0[v][1];
+          const float w0[8] = {wl.x, wl.y, wl.z, wl.w, wh.x, wh.y, wh.z, wh.w};
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            float s[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s[e] = 0.f;
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+              if (q < npair && j < ncv) {
+                float val[8];
+                raw[u][q][j].get(val);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s[e] = fmaf(wq[q], val[e], s[e]);
+              }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float wc = j ? 1.f - w0[e] : w0[e];
+              acc[e] = j ? fmaf(wc, s[e], acc[e]) : wc * s[e];
+            }
+          }
+        } else {
+          // ragged or unaligned vector, or a row covered by more than two pairs: per pixel
+#pragma unroll 1
+          for (int e = 0; e < 8; ++e) {
+            acc[e] = 0.f;
+            const int x = x0 + e;
+            if (x >= p.W) continue;
+            int ic0, ic1;
+            float wc0, wc1;
+            const int ncx = axis_cover2(p, 2, x, ic0, ic1, wc0, wc1);
+            for (int q = 0; q < npair; ++q)
+              for (int j = 0; j < ncx; ++j) {
+                const int ci = j ? ic1 : ic0;
+                acc[e] = fmaf(wq[q] * (j ? wc1 : wc0), to_f<TT>(rowp[warp][q][ci][x - p.s0[2][ci]]), acc[e]);
+              }
+          }
+        }
+        if (x0 + 8 <= p.W && (p.W & 7) == 0) {
+          store8(orow + x0, acc);
+        } else {
+          for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(acc[e]);
+        }
+      }
+    }
+    __syncwarp();
+  }
+}
+
 namespace {
 // Recognise a grid: tiles in raster order over per-axis interval lists with per-axis overlaps, at most
 // two intervals covering any coordinate (overlap shorter than the stride).
@@ -898,6 +1113,11 @@ cudaError_t launch_blend(const void* const* tiles, const vae_tile_t* meta, int n
     const long long nb = static_cast<long long>(d.T) * ((d.H + kGridRows - 1) / kGridRows);
     if (nb == 0) return cudaSuccess;
     dim3 grid(static_cast<unsigned>(nb), static_cast<unsigned>(d.B * d.C));
+    if (g.n[2] <= kG2Cols && d.tile_dtype != VAE_FP32) {  // fp32 tiles would spill its loads
+      if (d.out_dtype == VAE_FP32) blend_grid2_kernel<__nv_bfloat16, float><<<grid, 256, 0, s>>>(g);
+      else blend_grid2_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, s>>>(g);
+      return cudaGetLastError();
+    }
     const size_t sm = 0;
     const bool tf = d.tile_dtype == VAE_FP32, of = d.out_dtype == VAE_FP32;
     if (tf && of) blend_grid_kernel<float, float><<<grid, 256, sm, s>>>(g);

@@ -901,8 +901,9 @@ template <> struct Raw8<float> {
 // registers.  Each lane takes two vectors of the row at a time and issues all their source loads
 // before summing.  Rows whose (t, y) is covered by more than two pairs take the general loop.
 constexpr int kG2Cols = 16;
+constexpr int kG2Vecs = 1;  // vectors per lane per step (more were slower: fewer warps fit)
 template <typename TT, typename TO>
-__global__ void __launch_bounds__(256, 3) blend_grid2_kernel(const __grid_constant__ BlendGridParams p) {
+__global__ void __launch_bounds__(256, 4) blend_grid2_kernel(const __grid_constant__ BlendGridParams p) {
   __shared__ int4 vinfo[kGridMaxVec];
   __shared__ float4 vw0[kGridMaxVec][2];
   __shared__ const TT* rowp[8][4][kG2Cols];
@@ -980,12 +981,12 @@ __global__ void __launch_bounds__(256, 3) blend_grid2_kernel(const __grid_consta
       wq[q] = q < npair ? (qa ? wa1 : wa0) * (qb ? wb1 : wb0) : 0.f;
     }
     TO* orow = static_cast<TO*>(p.out) + ((static_cast<int64_t>(pl) * p.T + t) * p.H + y) * p.W;
-    for (int vb = lane; vb < nv; vb += 64) {
-      int4 inf[2];
-      Raw8<TT> raw[2][2][2];  // [vector][pair][interval]
-      bool fast[2];
+    for (int vb = lane; vb < nv; vb += 32 * kG2Vecs) {
+      int4 inf[kG2Vecs];
+      Raw8<TT> raw[kG2Vecs][2][2];  // [vector][pair][interval]
+      bool fast[kG2Vecs];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < kG2Vecs; ++u) {
         const int v = vb + 32 * u;
         fast[u] = false;
         if (v < nv) {
@@ -1002,7 +1003,7 @@ __global__ void __launch_bounds__(256, 3) blend_grid2_kernel(const __grid_consta
         }
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < kG2Vecs; ++u) {
         const int v = vb + 32 * u;
         if (v >= nv) break;
         const int x0 = v * 8;

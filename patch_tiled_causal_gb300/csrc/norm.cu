@@ -950,16 +950,17 @@ __global__ void __launch_bounds__(256, 4) blend_grid2_kernel(const __grid_consta
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int blocks_per_t = (p.H + kGridRows - 1) / kGridRows;
-  const int pl = blockIdx.y;
+  const int n_pl = p.B * p.C;
   const int t = blockIdx.x / blocks_per_t;
   const int y_base = (blockIdx.x - t * blocks_per_t) * kGridRows;
   int ia0, ia1;
   float wa0, wa1;
   const int na = axis_cover2(p, 0, t, ia0, ia1, wa0, wa1);
   const int n2 = p.n[2];
-  for (int r = warp; r < kGridRows; r += 8) {
+  for (int task = warp; task < n_pl * kGridRows; task += 8) {
+    const int pl = task / kGridRows, r = task - (task / kGridRows) * kGridRows;
     const int y = y_base + r;
-    if (y >= p.H) break;
+    if (y >= p.H) continue;
     int ib0, ib1;
     float wb0, wb1;
     const int nb = axis_cover2(p, 1, y, ib0, ib1, wb0, wb1);
@@ -1115,8 +1116,9 @@ cudaError_t launch_blend(const void* const* tiles, const vae_tile_t* meta, int n
     if (nb == 0) return cudaSuccess;
     dim3 grid(static_cast<unsigned>(nb), static_cast<unsigned>(d.B * d.C));
     if (g.n[2] <= kG2Cols && d.tile_dtype != VAE_FP32) {  // fp32 tiles would spill its loads
-      if (d.out_dtype == VAE_FP32) blend_grid2_kernel<__nv_bfloat16, float><<<grid, 256, 0, s>>>(g);
-      else blend_grid2_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, s>>>(g);
+      const dim3 grid2(static_cast<unsigned>(nb));  // every plane of a (t, row chunk) in one block
+      if (d.out_dtype == VAE_FP32) blend_grid2_kernel<__nv_bfloat16, float><<<grid2, 256, 0, s>>>(g);
+      else blend_grid2_kernel<__nv_bfloat16, __nv_bfloat16><<<grid2, 256, 0, s>>>(g);
       return cudaGetLastError();
     }
     const size_t sm = 0;

@@ -679,8 +679,8 @@ __global__ void __launch_bounds__(32 * kBlendRowsPerBlock) blend_kernel(const __
 // Blend for tile sets that form a grid (the tile plan's output): tile (a, b, c) is the product of the
 // a-th temporal, b-th row and c-th column interval, and its weight the product of the three 1-D
 // ramps, so out = sum_{a,b,c} w_a w_b w_c x_abc / (sum_a w_a)(sum_b w_b)(sum_c w_c).  One warp per
-// output row of one plane: the (a, b) pairs covering (t, y) are found once per row from the interval
-// lists, the column intervals covering each 8-pixel vector once per vector.
+// output row of one plane at a time: the (a, b) pairs covering (t, y) are found once per row from the
+// interval lists, the column intervals covering each 8-pixel vector once per block.
 constexpr int kAxisMax = 64;
 struct BlendGridParams {
   int B, C, T, H, W;
@@ -691,157 +691,10 @@ struct BlendGridParams {
   const void* ptr[VAE_MAX_TILES];  // tile (a, b, c) at ptr[(a * n[1] + b) * n[2] + c]
 };
 
-// Intervals of axis `ax` covering coordinate `x` (at most 2 when overlaps are shorter than strides;
-// a third is ignored only if the plan had one, which the host excludes) and their normalised weights.
-VAE_DEV int axis_cover(const BlendGridParams& p, int ax, int x, int* idx, float* w) {
-  int k = 0;
-  float sum = 0.f;
-  for (int i = 0; i < p.n[ax] && k < 2; ++i) {
-    const int l = x - p.s0[ax][i];
-    if (l < 0 || l >= p.len[ax][i]) continue;
-    idx[k] = i;
-    w[k] = ramp_w(l, p.len[ax][i], p.lo[ax][i], p.hi[ax][i]);
-    sum += w[k];
-    ++k;
-  }
-  for (int j = 0; j < k; ++j) w[j] = __fdividef(w[j], sum);
-  return k;
-}
 
-// Rows per block of the grid blend; each of the 8 warps handles kGridRows / 8 rows.
+// Rows per block of the grid blend (of every plane); the 8 warps take (plane, row) tasks in turn.
 constexpr int kGridRows = 32;
 constexpr int kGridMaxVec = 384;  // 8-pixel vectors per row with a shared-memory entry (W <= 3072)
-template <typename TT, typename TO>
-__global__ void __launch_bounds__(256, 4) blend_grid_kernel(const __grid_constant__ BlendGridParams p) {
-  // Per 8-pixel vector of a row (the same for every row): first overlapping column interval c0, the
-  // number of overlapping intervals (<= 2, 3 = take the slow path) and the normalised column weight
-  // of each pixel for each of them.  Per warp and row: the source row pointer of every (t, y) pair
-  // and column interval.
-  __shared__ short vc0[kGridMaxVec];
-  __shared__ unsigned char vnc[kGridMaxVec];
-  __shared__ float4 vw[kGridMaxVec][4];                    // [j * 2 + half] -> weights of 4 pixels
-  __shared__ const TT* rowp[8][4][kAxisMax];
-  __shared__ float wpair[8][4];
-  const int nv = (p.W + 7) / 8;
-  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-    const int x0 = v * 8;
-    int c0 = -1, nc = 0;
-    for (int i = 0; i < p.n[2]; ++i) {
-      const int l = x0 - p.s0[2][i];
-      if (l + 8 <= 0 || l >= p.len[2][i]) continue;
-      if (c0 < 0) c0 = i;
-      ++nc;
-    }
-    float w[2][8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float a0 = 0.f, a1 = 0.f;
-      if (nc >= 1 && nc <= 2) {
-        const int x = x0 + e;
-        const int l0 = x - p.s0[2][c0];
-        if (x < p.W && l0 >= 0 && l0 < p.len[2][c0]) a0 = ramp_w(l0, p.len[2][c0], p.lo[2][c0], p.hi[2][c0]);
-        if (nc == 2) {
-          const int l1 = x - p.s0[2][c0 + 1];
-          if (x < p.W && l1 >= 0 && l1 < p.len[2][c0 + 1])
-            a1 = ramp_w(l1, p.len[2][c0 + 1], p.lo[2][c0 + 1], p.hi[2][c0 + 1]);
-        }
-      }
-      const float sum = a0 + a1;
-      w[0][e] = sum > 0.f ? __fdividef(a0, sum) : 0.f;
-      w[1][e] = sum > 0.f ? __fdividef(a1, sum) : 0.f;
-    }
-    vc0[v] = static_cast<short>(c0 < 0 ? 0 : c0);
-    vnc[v] = static_cast<unsigned char>(nc > 2 ? 3 : nc);
-    vw[v][0] = make_float4(w[0][0], w[0][1], w[0][2], w[0][3]);
-    vw[v][1] = make_float4(w[0][4], w[0][5], w[0][6], w[0][7]);
-    vw[v][2] = make_float4(w[1][0], w[1][1], w[1][2], w[1][3]);
-    vw[v][3] = make_float4(w[1][4], w[1][5], w[1][6], w[1][7]);
-  }
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int blocks_per_t = (p.H + kGridRows - 1) / kGridRows;
-  const int pl = blockIdx.y;
-  const int t = blockIdx.x / blocks_per_t;
-  const int y_base = (blockIdx.x - t * blocks_per_t) * kGridRows;
-  int ia[2];
-  float wa[2];
-  const int na = axis_cover(p, 0, t, ia, wa);
-  const int nc_axis = p.n[2];
-  for (int r = warp; r < kGridRows; r += 8) {
-    const int y = y_base + r;
-    if (y >= p.H) break;
-    int ib[2];
-    float wb[2];
-    const int nb = axis_cover(p, 1, y, ib, wb);
-    const int npair = na * nb;
-    // row pointers of every (pair, column interval), lanes in parallel
-    for (int e = lane; e < npair * nc_axis; e += 32) {
-      const int q = e / nc_axis, c = e - (e / nc_axis) * nc_axis;
-      const int a = ia[q / nb], b = ib[q % nb];
-      const int64_t plane_in = static_cast<int64_t>(p.len[0][a]) * p.len[1][b];
-      rowp[warp][q][c] = static_cast<const TT*>(p.ptr[(a * p.n[1] + b) * nc_axis + c]) +
-                         ((pl * plane_in + static_cast<int64_t>(t - p.s0[0][a]) * p.len[1][b]) + (y - p.s0[1][b])) *
-                             p.len[2][c];
-    }
-    if (lane < npair) wpair[warp][lane] = wa[lane / nb] * wb[lane % nb];
-    __syncwarp();
-    TO* orow = static_cast<TO*>(p.out) + ((static_cast<int64_t>(pl) * p.T + t) * p.H + y) * p.W;
-    for (int v = lane; v < nv; v += 32) {
-      const int x0 = v * 8;
-      const int c0 = vc0[v], nc = vnc[v];
-      float acc[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-      if (nc <= 2) {
-        for (int j = 0; j < nc; ++j) {
-          const float4 wl = vw[v][2 * j], wh = vw[v][2 * j + 1];
-          const float wc[8] = {wl.x, wl.y, wl.z, wl.w, wh.x, wh.y, wh.z, wh.w};
-          const int c = c0 + j;
-          const int nw = p.len[2][c];
-          const int lx = x0 - p.s0[2][c];
-          const bool vec = lx >= 0 && lx + 8 <= nw && ((lx | nw) & 7) == 0;
-          for (int q = 0; q < npair; ++q) {
-            const TT* src = rowp[warp][q][c];
-            const float wq = wpair[warp][q];
-            float val[8];
-            if (vec) {
-              load8(src + lx, val);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const int xx = lx + e;
-                val[e] = (xx >= 0 && xx < nw) ? to_f<TT>(src[xx]) : 0.f;
-              }
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = fmaf(wq * wc[e], val[e], acc[e]);
-          }
-        }
-      } else {
-        // a vector spanning three or more column intervals: per pixel, straight from the table
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int x = x0 + e;
-          if (x >= p.W) continue;
-          int ic[2];
-          float wc2[2];
-          const int ncx = axis_cover(p, 2, x, ic, wc2);
-          for (int j = 0; j < ncx; ++j)
-            for (int q = 0; q < npair; ++q) {
-              const TT* src = rowp[warp][q][ic[j]];
-              acc[e] = fmaf(wpair[warp][q] * wc2[j], to_f<TT>(src[x - p.s0[2][ic[j]]]), acc[e]);
-            }
-        }
-      }
-      if (x0 + 8 <= p.W && (p.W & 7) == 0) {
-        store8(orow + x0, acc);
-      } else {
-        for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(acc[e]);
-      }
-    }
-    __syncwarp();
-  }
-}
 
 // axis_cover with the (at most 2) results in scalars, so they stay in registers.
 VAE_DEV int axis_cover2(const BlendGridParams& p, int ax, int x, int& i0, int& i1, float& w0, float& w1) {
@@ -894,12 +747,13 @@ template <> struct Raw8<float> {
   }
 };
 
-// Grid blend, lean form for grids with at most kG2Cols column intervals: per 8-pixel vector one
-// packed shared-memory word (first column interval, count, offsets into both intervals' rows) and
-// the first interval's normalised column weights (the second's are 1 minus them); per warp and row
-// the source row pointers of each (t, y) pair and column interval and the pair weights in
-// registers.  Each lane takes two vectors of the row at a time and issues all their source loads
-// before summing.  Rows whose (t, y) is covered by more than two pairs take the general loop.
+// Grid blend for grids with at most kG2Cols column intervals (others take the general kernel).  Per
+// 8-pixel vector, built once per block: one packed shared-memory word (first column interval, count,
+// offsets into both intervals' rows) and the first interval's normalised column weights (the
+// second's are one minus them).  Per warp and (plane, row): the source row pointers of each (t, y)
+// pair and column interval, and the pair weights in registers.  A lane issues every source load of
+// its vector before summing; rows covered by more than two (t, y) pairs, and ragged or unaligned
+// vectors, take the per-pixel loop.
 constexpr int kG2Cols = 16;
 constexpr int kG2Vecs = 1;  // vectors per lane per step (more were slower: fewer warps fit)
 template <typename TT, typename TO>
@@ -1033,8 +887,9 @@ __global__ void __launch_bounds__(256, 4) blend_grid2_kernel(const __grid_consta
             }
           }
         } else {
-          // ragged or unaligned vector, or a row covered by more than two pairs: per pixel
-#pragma unroll 1
+          // ragged or unaligned vector, or a row covered by more than two pairs: per pixel (unrolled,
+          // so that acc stays in registers)
+#pragma unroll
           for (int e = 0; e < 8; ++e) {
             acc[e] = 0.f;
             const int x = x0 + e;
@@ -1042,11 +897,14 @@ __global__ void __launch_bounds__(256, 4) blend_grid2_kernel(const __grid_consta
             int ic0, ic1;
             float wc0, wc1;
             const int ncx = axis_cover2(p, 2, x, ic0, ic1, wc0, wc1);
-            for (int q = 0; q < npair; ++q)
+            for (int q = 0; q < npair; ++q) {
+              const int qa = nb == 2 ? q >> 1 : q, qb = nb == 2 ? q & 1 : 0;
+              const float wqq = (qa ? wa1 : wa0) * (qb ? wb1 : wb0);  // (no dynamically indexed array)
               for (int j = 0; j < ncx; ++j) {
                 const int ci = j ? ic1 : ic0;
-                acc[e] = fmaf(wq[q] * (j ? wc1 : wc0), to_f<TT>(rowp[warp][q][ci][x - p.s0[2][ci]]), acc[e]);
+                acc[e] = fmaf(wqq * (j ? wc1 : wc0), to_f<TT>(rowp[warp][q][ci][x - p.s0[2][ci]]), acc[e]);
               }
+            }
           }
         }
         if (x0 + 8 <= p.W && (p.W & 7) == 0) {
@@ -1110,23 +968,17 @@ cudaError_t launch_blend(const void* const* tiles, const vae_tile_t* meta, int n
   static BlendGridParams g;
   if (n_tiles > VAE_MAX_TILES) return cudaErrorInvalidValue;
   if (static_cast<long long>(d.B) * d.C > 65535) return cudaErrorInvalidValue;
-  if (d.W <= 8 * kGridMaxVec && build_grid(tiles, meta, n_tiles, d, g)) {
+  if (d.W <= 8 * kGridMaxVec && build_grid(tiles, meta, n_tiles, d, g) && g.n[2] <= kG2Cols) {
     g.B = d.B; g.C = d.C; g.T = d.T; g.H = d.H; g.W = d.W; g.out = out;
     const long long nb = static_cast<long long>(d.T) * ((d.H + kGridRows - 1) / kGridRows);
     if (nb == 0) return cudaSuccess;
-    dim3 grid(static_cast<unsigned>(nb), static_cast<unsigned>(d.B * d.C));
-    if (g.n[2] <= kG2Cols && d.tile_dtype != VAE_FP32) {  // fp32 tiles would spill its loads
-      const dim3 grid2(static_cast<unsigned>(nb));  // every plane of a (t, row chunk) in one block
-      if (d.out_dtype == VAE_FP32) blend_grid2_kernel<__nv_bfloat16, float><<<grid2, 256, 0, s>>>(g);
-      else blend_grid2_kernel<__nv_bfloat16, __nv_bfloat16><<<grid2, 256, 0, s>>>(g);
-      return cudaGetLastError();
-    }
-    const size_t sm = 0;
+    if (nb > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>(nb));  // every plane of a (t, row chunk) in one block
     const bool tf = d.tile_dtype == VAE_FP32, of = d.out_dtype == VAE_FP32;
-    if (tf && of) blend_grid_kernel<float, float><<<grid, 256, sm, s>>>(g);
-    else if (tf) blend_grid_kernel<float, __nv_bfloat16><<<grid, 256, sm, s>>>(g);
-    else if (of) blend_grid_kernel<__nv_bfloat16, float><<<grid, 256, sm, s>>>(g);
-    else blend_grid_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, sm, s>>>(g);
+    if (tf && of) blend_grid2_kernel<float, float><<<grid, 256, 0, s>>>(g);
+    else if (tf) blend_grid2_kernel<float, __nv_bfloat16><<<grid, 256, 0, s>>>(g);
+    else if (of) blend_grid2_kernel<__nv_bfloat16, float><<<grid, 256, 0, s>>>(g);
+    else blend_grid2_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, s>>>(g);
     return cudaGetLastError();
   }
   p.B = d.B; p.C = d.C; p.T = d.T; p.H = d.H; p.W = d.W; p.n = n_tiles;

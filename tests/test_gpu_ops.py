@@ -217,15 +217,17 @@ def test_d2s(vd, s, drop):
     np.testing.assert_array_equal(y.cpu().numpy(), ref)
 
 
-@pytest.mark.parametrize("dt,order", [("bf16", "raster"), ("fp32", "raster"), ("fp32", "reversed")])
-def test_tile_blend(vd, dt, order):
-    # raster order is a grid (factorised kernel); any other order takes the general gather kernel
+@pytest.mark.parametrize("dt,order,W", [("bf16", "raster", 56), ("fp32", "raster", 56), ("fp32", "reversed", 56),
+                                         ("bf16", "raster", 136)])
+def test_tile_blend(vd, dt, order, W):
+    # raster order is a grid (factorised kernel); any other order takes the general gather kernel.
+    # W = 136: 13 column intervals, so rows covered by 4 (t, y) pairs have 52 source rows per warp
     tdt = torch.bfloat16 if dt == "bf16" else torch.float32
-    plan_ = tiles.tile_plan((3, 40, 56), (2, 16, 16), (1, 4, 6), 4, 1)   # causal time, ragged last tiles
+    plan_ = tiles.tile_plan((3, 40, W), (2, 16, 16), (1, 4, 6), 4, 1)   # causal time, ragged last tiles
     if order == "reversed":
         plan_ = plan_[::-1]
     B, Cc = 2, 3
-    out_shape = (B, Cc, 4 * 2 + 1, 40, 56)
+    out_shape = (B, Cc, 4 * 2 + 1, 40, W)
     data = []
     for i, t in enumerate(plan_):
         a = synth.draw_normal((B, Cc, t.pix[1], t.pix[3], t.pix[5]), 70 + i)

@@ -720,6 +720,13 @@ VAE_DEV int axis_cover2(const BlendGridParams& p, int ax, int x, int& i0, int& i
   return k;
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), and its group fences.
+VAE_DEV void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+VAE_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N> VAE_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // Raw 8-element loads, converted only when used (so several can be in flight per thread).
 template <typename T> struct Raw8;
 template <> struct Raw8<__nv_bfloat16> {
@@ -761,6 +768,9 @@ __global__ void __launch_bounds__(256, 4) blend_grid2_kernel(const __grid_consta
   __shared__ int4 vinfo[kGridMaxVec];
   __shared__ float4 vw0[kGridMaxVec][2];
   __shared__ const TT* rowp[8][4][kG2Cols];
+  // bf16 tiles, rows covered by one (t, y) pair: each lane's source vectors (one per column
+  // interval) of its next vector are copied here asynchronously while it sums the current one
+  __shared__ uint4 stage[sizeof(TT) == 2 ? 8 : 1][2][2][32];
   const int nv = (p.W + 7) / 8;
   for (int v = threadIdx.x; v < nv; v += blockDim.x) {
     const int x0 = v * 8;
@@ -836,6 +846,77 @@ __global__ void __launch_bounds__(256, 4) blend_grid2_kernel(const __grid_consta
       wq[q] = q < npair ? (qa ? wa1 : wa0) * (qb ? wb1 : wb0) : 0.f;
     }
     TO* orow = static_cast<TO*>(p.out) + ((static_cast<int64_t>(pl) * p.T + t) * p.H + y) * p.W;
+    if constexpr (sizeof(TT) == 2) {
+      if (npair == 1) {
+        // issue the copies of vector v's sources into buffer `buf`; returns whether v is on the fast path
+        auto issue = [&](int v, int buf) -> bool {
+          if (v >= nv) return false;
+          const int4 inf = vinfo[v];
+          if (!((inf.x >> 12) & 1)) return false;
+          const int cv = inf.x & 255, ncv = (inf.x >> 8) & 15;
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            if (j < ncv) cp_async16(&stage[warp][buf][j][lane], rowp[warp][0][cv + j] + (j ? inf.z : inf.y));
+          return true;
+        };
+        bool fast_cur = issue(lane, 0);
+        cp_async_commit();
+        int buf = 0;
+        for (int v = lane; v < nv; v += 32) {
+          const bool fast_next = issue(v + 32, buf ^ 1);
+          cp_async_commit();
+          cp_async_wait<1>();  // this lane's copies for v have landed
+          const int x0 = v * 8;
+          float acc[8];
+          if (fast_cur) {
+            const int ncv = (vinfo[v].x >> 8) & 15;
+            const float4 wl = vw0[v][0], wh = vw0[v][1];
+            const float w0[8] = {wl.x, wl.y, wl.z, wl.w, wh.x, wh.y, wh.z, wh.w};
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              float val[8];
+              if (j < ncv) {
+                Raw8<TT> r;
+                r.r = stage[warp][buf][j][lane];
+                r.get(val);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) val[e] = 0.f;
+              }
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float wc = (j ? 1.f - w0[e] : w0[e]) * wq[0];
+                acc[e] = j ? fmaf(wc, val[e], acc[e]) : wc * val[e];
+              }
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              acc[e] = 0.f;
+              const int x = x0 + e;
+              if (x >= p.W) continue;
+              int ic0, ic1;
+              float wc0, wc1;
+              const int ncx = axis_cover2(p, 2, x, ic0, ic1, wc0, wc1);
+              for (int j = 0; j < ncx; ++j) {
+                const int ci = j ? ic1 : ic0;
+                acc[e] = fmaf(wq[0] * (j ? wc1 : wc0), to_f<TT>(rowp[warp][0][ci][x - p.s0[2][ci]]), acc[e]);
+              }
+            }
+          }
+          if (x0 + 8 <= p.W && (p.W & 7) == 0) {
+            store8(orow + x0, acc);
+          } else {
+            for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(acc[e]);
+          }
+          fast_cur = fast_next;
+          buf ^= 1;
+        }
+        cp_async_wait<0>();
+        __syncwarp();
+        continue;
+      }
+    }
     for (int vb = lane; vb < nv; vb += 32 * kG2Vecs) {
       int4 inf[kG2Vecs];
       Raw8<TT> raw[kG2Vecs][2][2];  // [vector][pair][interval]

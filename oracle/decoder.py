@@ -5,8 +5,8 @@ TEST INFRASTRUCTURE ONLY (see the package header).
 Structure (DistVAE PR #14 "Add tiled VAE parallelism & extended model support", Wan and LTX-2
 adapter commits; TensorRT-LLM PR #16066 "ParallelVAE_TrtllmWan for native Wan VAE"):
   conv_in -> [mid residual blocks] -> [mid attention] -> for each stage: residual blocks, then
-  (except after the last stage) the up-sampling conv + depth-to-space -> GN + SiLU -> conv_out
-  -> final depth-to-space.
+  (except after the last stage) the up-sampling conv + depth-to-space -> norm + SiLU -> conv_out
+  -> final depth-to-space.  The norms are group norms, or channel RMS norms (``cfg.norm == "rms"``).
 
 Chunked temporal decode (Wan-family decoders thread a per-convolution temporal cache through
 a chunked decode; DistVAE PR #14, Wan adapter and HunyuanVideo commits): the latent is cut into
@@ -49,19 +49,19 @@ class _ConvRunner:
 
 
 def _decode_chunk(cfg, p: dict, z: np.ndarray, conv: _ConvRunner, dtype) -> np.ndarray:
-    g, eps = cfg.gn_groups, cfg.gn_eps
+    g, eps, kind = cfg.gn_groups, cfg.gn_eps, cfg.norm
     x = conv("conv_in", z.astype(dtype))
     for r in range(cfg.mid_res):
-        x = ops.resblock(x, p, f"mid.res{r}", g, eps, conv).astype(dtype)
+        x = ops.resblock(x, p, f"mid.res{r}", g, eps, conv, kind).astype(dtype)
     if cfg.mid_attn:
-        x = ops.spatial_attention(x, p, "mid.attn", g, eps, dtype=dtype).astype(dtype)
+        x = ops.spatial_attention(x, p, "mid.attn", g, eps, dtype=dtype, kind=kind).astype(dtype)
     for i in range(cfg.n_stages):
         for r in range(cfg.n_res[i]):
-            x = ops.resblock(x, p, f"stage{i}.res{r}", g, eps, conv).astype(dtype)
+            x = ops.resblock(x, p, f"stage{i}.res{r}", g, eps, conv, kind).astype(dtype)
         if i + 1 < cfg.n_stages:
             x = conv(f"stage{i}.up", x)
             x = ops.depth_to_space(x, cfg.up[i], drop_first=conv.first)
-    x = ops.silu(ops.group_norm(x, p["head.norm.gamma"], p["head.norm.beta"], g, eps)).astype(dtype)
+    x = ops.silu(ops.norm(x, p["head.norm.gamma"], p["head.norm.beta"], g, eps, kind)).astype(dtype)
     x = conv("head.conv", x)
     return ops.depth_to_space(x, cfg.out_d2s, drop_first=conv.first)
 

@@ -139,6 +139,26 @@ def group_norm(x: np.ndarray, gamma: np.ndarray, beta: np.ndarray, groups: int,
         beta.astype(np.float64)[None, :, None, None, None]
 
 
+def channel_rms_norm(x: np.ndarray, gamma: np.ndarray, beta: np.ndarray, eps: float) -> np.ndarray:
+    """y = x / sqrt(mean_c(x^2) + eps) * gamma[c] + beta[c]: one statistic per (b, t, h, w) over
+    the channels, float64.  The channel RMS norms of the Wan / Qwen-Image, HunyuanVideo 1.5 and
+    LTX-2 decoders reduce over channels only, so a patch needs nothing from its neighbours (DistVAE
+    PR #14 "Add tiled VAE parallelism & extended model support": Qwen-Image, HunyuanVideo/1.5 and
+    LTX-2 adapter commits)."""
+    xd = x.astype(np.float64)
+    ms = (xd * xd).mean(axis=1, keepdims=True)
+    y = xd / np.sqrt(ms + eps)
+    return y * gamma.astype(np.float64)[None, :, None, None, None] + beta.astype(np.float64)[None, :, None, None, None]
+
+
+def norm(x: np.ndarray, gamma: np.ndarray, beta: np.ndarray, groups: int, eps: float,
+         kind: str = "group") -> np.ndarray:
+    """The decoder's norm: group norm (kind "group") or channel RMS norm (kind "rms")."""
+    if kind == "rms":
+        return channel_rms_norm(x, gamma, beta, eps)
+    return group_norm(x, gamma, beta, groups, eps)
+
+
 def silu(x: np.ndarray) -> np.ndarray:
     """SiLU(x) = x * sigmoid(x) = x / (1 + exp(-x))."""
     with np.errstate(over="ignore"):
@@ -174,11 +194,11 @@ def softmax(s: np.ndarray, axis: int = -1) -> np.ndarray:
 
 
 def spatial_attention(x: np.ndarray, p: dict, prefix: str, groups: int, eps: float,
-                      dtype=np.float64) -> np.ndarray:
+                      dtype=np.float64, kind: str = "group") -> np.ndarray:
     """x + o_proj(softmax(q k^T / sqrt(C)) v) over the H*W tokens of each frame, one head;
-    q, k, v are 1x1 projections of GN(x)."""
+    q, k, v are 1x1 projections of the normed x (group or channel RMS norm, no SiLU)."""
     n, c, t, h, w = x.shape
-    hn = group_norm(x, p[prefix + ".norm.gamma"], p[prefix + ".norm.beta"], groups, eps).astype(dtype)
+    hn = norm(x, p[prefix + ".norm.gamma"], p[prefix + ".norm.beta"], groups, eps, kind).astype(dtype)
     tok = hn.transpose(0, 2, 3, 4, 1).reshape(n * t, h * w, c)  # [frames, N, C]
 
     def proj(a, name):
@@ -196,11 +216,13 @@ def spatial_attention(x: np.ndarray, p: dict, prefix: str, groups: int, eps: flo
 # Residual block
 # ---------------------------------------------------------------------------------------------
 
-def resblock(x: np.ndarray, p: dict, prefix: str, groups: int, eps: float, conv) -> np.ndarray:
-    """x + conv2(SiLU(GN2(conv1(SiLU(GN1(x)))))); ``conv(name, input)`` runs a causal conv."""
+def resblock(x: np.ndarray, p: dict, prefix: str, groups: int, eps: float, conv,
+             kind: str = "group") -> np.ndarray:
+    """x + conv2(SiLU(N2(conv1(SiLU(N1(x)))))), N = group or channel RMS norm; ``conv(name, input)``
+    runs a causal conv."""
     dt = x.dtype
-    hmid = silu(group_norm(x, p[prefix + ".norm1.gamma"], p[prefix + ".norm1.beta"], groups, eps)).astype(dt)
+    hmid = silu(norm(x, p[prefix + ".norm1.gamma"], p[prefix + ".norm1.beta"], groups, eps, kind)).astype(dt)
     hmid = conv(prefix + ".conv1", hmid)
-    hmid = silu(group_norm(hmid, p[prefix + ".norm2.gamma"], p[prefix + ".norm2.beta"], groups, eps)).astype(dt)
+    hmid = silu(norm(hmid, p[prefix + ".norm2.gamma"], p[prefix + ".norm2.beta"], groups, eps, kind)).astype(dt)
     hmid = conv(prefix + ".conv2", hmid)
     return x + hmid

@@ -110,38 +110,46 @@ def _map(g: Grid, f) -> Grid:
     return [[f(p) for p in row] for row in g]
 
 
-def _resblock(g: Grid, p: dict, prefix: str, groups: int, eps: float, conv: _PatchedConv) -> Grid:
-    h = _map(_patch_group_norm(g, p[prefix + ".norm1.gamma"], p[prefix + ".norm1.beta"], groups, eps), ops.silu)
+def _patch_norm(g: Grid, gamma, beta, groups: int, eps: float, kind: str) -> Grid:
+    """Group norm merges per-patch sums; a channel RMS norm needs nothing from other patches."""
+    if kind == "rms":
+        return _map(g, lambda a: ops.channel_rms_norm(a, gamma, beta, eps))
+    return _patch_group_norm(g, gamma, beta, groups, eps)
+
+
+def _resblock(g: Grid, p: dict, prefix: str, groups: int, eps: float, conv: _PatchedConv,
+              kind: str = "group") -> Grid:
+    h = _map(_patch_norm(g, p[prefix + ".norm1.gamma"], p[prefix + ".norm1.beta"], groups, eps, kind), ops.silu)
     h = conv(prefix + ".conv1", h)
-    h = _map(_patch_group_norm(h, p[prefix + ".norm2.gamma"], p[prefix + ".norm2.beta"], groups, eps), ops.silu)
+    h = _map(_patch_norm(h, p[prefix + ".norm2.gamma"], p[prefix + ".norm2.beta"], groups, eps, kind), ops.silu)
     h = conv(prefix + ".conv2", h)
     return [[a + b for a, b in zip(ra, rb)] for ra, rb in zip(g, h)]
 
 
 def decode_patched(cfg, params: dict, latent: np.ndarray, n_patch_h: int, n_patch_w: int) -> np.ndarray:
     """Float64 patched decode; the result is merged back into one [B, out_c, T', H, W] array."""
-    gr, eps = cfg.gn_groups, cfg.gn_eps
+    gr, eps, kind = cfg.gn_groups, cfg.gn_eps, cfg.norm
     lh, lw = latent.shape[3], latent.shape[4]
     eh, ew = band_edges(lh, n_patch_h), band_edges(lw, n_patch_w)
     conv = _PatchedConv(params)
     g = split(latent.astype(np.float64), eh, ew)
     g = conv("conv_in", g)
     for r in range(cfg.mid_res):
-        g = _resblock(g, params, f"mid.res{r}", gr, eps, conv)
+        g = _resblock(g, params, f"mid.res{r}", gr, eps, conv, kind)
     if cfg.mid_attn:
         # the attention sees the whole frame: gather, attend, split on the same edges
-        whole = ops.spatial_attention(merge(g), params, "mid.attn", gr, eps)
+        whole = ops.spatial_attention(merge(g), params, "mid.attn", gr, eps, kind=kind)
         g = split(whole, eh, ew)
     sh_tot = sw_tot = 1
     for i in range(cfg.n_stages):
         for r in range(cfg.n_res[i]):
-            g = _resblock(g, params, f"stage{i}.res{r}", gr, eps, conv)
+            g = _resblock(g, params, f"stage{i}.res{r}", gr, eps, conv, kind)
         if i + 1 < cfg.n_stages:
             g = conv(f"stage{i}.up", g)
             g = _map(g, lambda a, s=cfg.up[i]: ops.depth_to_space(a, s, drop_first=True))
             sh_tot *= cfg.up[i][1]
             sw_tot *= cfg.up[i][2]
-    g = _map(_patch_group_norm(g, params["head.norm.gamma"], params["head.norm.beta"], gr, eps), ops.silu)
+    g = _map(_patch_norm(g, params["head.norm.gamma"], params["head.norm.beta"], gr, eps, kind), ops.silu)
     g = conv("head.conv", g)
     g = _map(g, lambda a: ops.depth_to_space(a, cfg.out_d2s, drop_first=True))
     return merge(g)

@@ -39,6 +39,8 @@ class DecoderConfig:
     mid_res     residual blocks at the start (after conv_in), at stage_c[0] channels.
     mid_attn    1 = single-head per-frame spatial self-attention after the mid residual blocks.
     out_c       pixel channels; out_d2s the final depth-to-space factors of conv_out.
+    norm        "group": every norm is a per-frame group norm; "rms": a channel RMS norm per pixel
+                (the Wan / Qwen-Image, HunyuanVideo 1.5 and LTX-2 decoders' norms).
     """
 
     name: str
@@ -52,6 +54,7 @@ class DecoderConfig:
     gn_eps: float = 1e-6
     out_c: int = 3
     out_d2s: Tuple[int, int, int] = (1, 1, 1)
+    norm: str = "group"  # "group" (per-frame group norm) or "rms" (channel RMS norm per pixel)
 
     @property
     def latent_c(self) -> int:
@@ -117,11 +120,16 @@ MINI_WAN = DecoderConfig(
     name="mini_wan", latent_shape=(1, 48, 3, 9, 11), stage_c=(128, 128, 64), n_res=(1, 1, 1),
     up=((2, 2, 2), (1, 2, 2)), mid_res=1, mid_attn=1, gn_groups=32, out_d2s=(1, 2, 2))
 
+# The Wan-family block structure with channel RMS norms instead of group norms (the norm the
+# Wan / Qwen-Image decoders use); same architecture otherwise.
+WAN_RMS = dataclasses.replace(WAN, name="wan_rms", norm="rms")
+MINI_WAN_RMS = dataclasses.replace(MINI_WAN, name="mini_wan_rms", norm="rms")
+
 MINI_TILED = dataclasses.replace(MINI_LTX, name="mini_tiled", latent_shape=(2, 64, 5, 7, 9))
 MINI_TILING = TilingConfig(tile=(3, 4, 4), overlap=(1, 1, 2))
 
 CONFIGS: Dict[str, DecoderConfig] = {c.name: c for c in (
-    TINY, WAN, LTX, LTX_TILED, MINI_LTX, MINI_WAN, MINI_TILED)}
+    TINY, WAN, LTX, LTX_TILED, MINI_LTX, MINI_WAN, MINI_TILED, WAN_RMS, MINI_WAN_RMS)}
 
 
 # ---------------------------------------------------------------------------------------------

@@ -153,6 +153,45 @@ def test_group_norm_per_frame():
     np.testing.assert_allclose(y2[:, :, 2], y[:, :, 2], rtol=1e-9, atol=1e-9)
 
 
+def test_channel_rms_norm_vs_torch():
+    # library routine: rms_norm over the channel axis of the channels-last view
+    x = synth.draw_normal((2, 12, 3, 5, 6), 26, offset=0.5).astype(np.float64)
+    g = synth.draw_normal((12,), 27) * 0.1 + 1.0
+    bt = synth.draw_normal((12,), 28) * 0.1
+    y = ops.channel_rms_norm(x, g, bt, 1e-6)
+    xv = torch.from_numpy(x).permute(0, 2, 3, 4, 1)
+    ref = torch.nn.functional.rms_norm(xv, (12,), torch.from_numpy(g.astype(np.float64)), eps=1e-6)
+    ref = (ref + torch.from_numpy(bt.astype(np.float64))).permute(0, 4, 1, 2, 3).numpy()
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_channel_rms_norm_brute_force_and_closed_forms():
+    x = synth.draw_normal((1, 5, 2, 2, 3), 29).astype(np.float64)
+    g = synth.draw_normal((5,), 30) * 0.1 + 1.0
+    bt = synth.draw_normal((5,), 31) * 0.1
+    y = ops.channel_rms_norm(x, g, bt, 1e-3)
+    for t in range(2):
+        for i in range(2):
+            for j in range(3):
+                v = x[0, :, t, i, j]
+                r = (sum(float(a) * float(a) for a in v) / 5 + 1e-3) ** 0.5
+                for ch in range(5):
+                    assert abs(y[0, ch, t, i, j] - (v[ch] / r * g[ch] + bt[ch])) < 1e-12
+    # a constant vector a*1 normalises to sign(a) (eps 0), whatever |a|
+    for a in (-3.0, 0.25, 1e4):
+        c = np.full((1, 4, 1, 1, 1), a)
+        np.testing.assert_allclose(ops.channel_rms_norm(c, np.ones(4), np.zeros(4), 0.0).ravel(), np.sign(a))
+    # scale invariance (eps 0) and per-pixel independence: a pixel's change leaves the others alone
+    np.testing.assert_allclose(ops.channel_rms_norm(7.5 * x, g, bt, 0.0), ops.channel_rms_norm(x, g, bt, 0.0),
+                               rtol=1e-12, atol=1e-12)
+    x2 = x.copy()
+    x2[0, :, 1, 1, 2] *= -40.0
+    y0, y2 = (ops.channel_rms_norm(a, g, bt, 1e-6) for a in (x, x2))
+    mask = np.ones(y0.shape, bool)
+    mask[0, :, 1, 1, 2] = False
+    np.testing.assert_array_equal(y2[mask], y0[mask])
+
+
 def test_silu_closed_form():
     x = np.array([-1000.0, -2.0, 0.0, 1.0, 3.0, 1000.0])
     ref = torch.nn.functional.silu(torch.from_numpy(x)).numpy()
@@ -243,7 +282,7 @@ def test_resblock_zero_conv2_is_identity():
     np.testing.assert_array_equal(ops.resblock(x, p, "stage0.res0", 8, 1e-6, run), x)
 
 
-@pytest.mark.parametrize("name", ["tiny", "mini_wan"])
+@pytest.mark.parametrize("name", ["tiny", "mini_wan", "mini_wan_rms"])
 def test_causality(name):
     cfg = synth.CONFIGS[name]
     p = synth.draw_params(cfg, 0)
@@ -259,7 +298,7 @@ def test_causality(name):
     assert np.abs(y2[:, :, keep:] - y[:, :, keep:]).max() > 1e-3
 
 
-@pytest.mark.parametrize("name", ["tiny", "mini_wan"])
+@pytest.mark.parametrize("name", ["tiny", "mini_wan", "mini_wan_rms"])
 def test_chunked_equals_whole(name):
     cfg = synth.CONFIGS[name]
     p = synth.draw_params(cfg, 0, rand_affine=True)
@@ -270,7 +309,8 @@ def test_chunked_equals_whole(name):
         np.testing.assert_allclose(yc, y, rtol=1e-12, atol=1e-12)
 
 
-@pytest.mark.parametrize("name,ph,pw", [("tiny", 2, 2), ("tiny", 1, 3), ("mini_wan", 2, 4), ("mini_ltx", 3, 2)])
+@pytest.mark.parametrize("name,ph,pw", [("tiny", 2, 2), ("tiny", 1, 3), ("mini_wan", 2, 4), ("mini_ltx", 3, 2),
+                                        ("mini_wan_rms", 2, 3)])
 def test_patched_equals_unpatched(name, ph, pw):
     cfg = synth.CONFIGS[name]
     p = synth.draw_params(cfg, 0, rand_affine=True)

@@ -9,7 +9,8 @@ One JSON line on rank 0 with the contract's keys plus:
   roofline      the dominant kernel (tcgen05 causal conv) inside the timed decodes: algorithmic
                 FLOPs / CUDA-event time over all its launches, against the measured bf16 peak
   kernels       the same per kernel class (conv, group norm stats/apply, attention GEMMs, ...)
-  ops           the op-level workloads: PatchGroupNorm+SiLU, causal conv 512->512, tile blend
+  ops           the op-level workloads: PatchGroupNorm+SiLU, channel RMS norm+SiLU, causal conv 512->512,
+                tile blend
   cpu_baseline  the CPU oracle on a bounded spatial crop of the same decode, host cores
 N > 1 (torchrun): each rank decodes its own latent (independent videos, weak scaling), no
 collective on the data path; barriers and the max over ranks bracket the timed region.
@@ -397,6 +398,13 @@ def run_ops(args, torch, vd, peaks, flush):
     res["groupnorm_silu"] = {"workload": "[1,512,21,88,160] bf16, 32 groups, 4 width patches", "ms": ms,
                              "bytes": nbytes, "gbs": nbytes / ms / 1e6, "frac_of_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"],
                              "bound": "hbm"}
+    # (a') channel RMS norm + SiLU on the same tensor (the Wan / LTX-2 norm family; no statistics pass)
+    rms = vd.prepare_channel_rmsnorm_silu(x, g, bt, y, B, T, H, W, C)
+    ms = _time(torch, rms, args.steps, flush)
+    nbytes = 2 * x.numel() * 2
+    res["channel_rmsnorm_silu"] = {"workload": "[1,512,21,88,160] bf16, per-pixel RMS over 512 channels", "ms": ms,
+                                   "bytes": nbytes, "gbs": nbytes / ms / 1e6,
+                                   "frac_of_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"], "bound": "hbm"}
     # (b) causal conv 3x3x3 512 -> 512, 4 width patches
     w = torch.from_numpy(synth.conv_weight(C, C, 101)).cuda()
     cd = vd.conv_desc(B, T, H, W, C, C, eh, ew)

@@ -53,6 +53,12 @@ typedef enum {
 
 typedef enum { VAE_BF16 = 0, VAE_FP32 = 1 } vae_dtype_t;
 
+/* The decoder's norm family.  VAE_NORM_GROUP: per-frame group norm whose statistics span patches
+ * ([DV] PatchGroupNorm commit).  VAE_NORM_CHANNEL_RMS: a channel RMS norm per pixel, the norm of the
+ * Wan / Qwen-Image, HunyuanVideo 1.5 and LTX-2 decoders, which reduces over channels only and so
+ * needs nothing from other patches ([DV] Qwen-Image, HunyuanVideo/1.5 and LTX-2 adapter commits). */
+typedef enum { VAE_NORM_GROUP = 0, VAE_NORM_CHANNEL_RMS = 1 } vae_norm_t;
+
 #define VAE_MAX_STAGES 8
 #define VAE_MAX_PATCHES 64 /* per axis */
 #define VAE_MAX_TILES 512
@@ -82,7 +88,11 @@ typedef struct {
  * population variance, eps inside the square root.  The attention is one head over each frame's
  * H*W tokens with 1x1 q/k/v/o projections, scale 1/sqrt(C), on GN(x) without SiLU, plus residual.
  * dtype: VAE_BF16 stores activations in bf16 (fp32 accumulation, statistics and blend),
- * VAE_FP32 stores everything in fp32. */
+ * VAE_FP32 stores everything in fp32.
+ * norm_type: VAE_NORM_GROUP (gn_groups, gn_eps as above), or VAE_NORM_CHANNEL_RMS: every norm above
+ * becomes x * rsqrt(mean over channels of x^2 + gn_eps) * gamma + beta per pixel (gn_groups is then
+ * ignored; stage channels must be multiples of 8 and at most 1024 with C/8 a power of two or a
+ * multiple of 32). */
 typedef struct {
   int latent_c;
   int n_stages;
@@ -96,6 +106,7 @@ typedef struct {
   int out_c;
   int out_d2s_t, out_d2s_h, out_d2s_w;
   vae_dtype_t dtype;
+  vae_norm_t norm_type;
 } vae_config_t;
 
 typedef struct vae_decoder vae_decoder_t; /* opaque */
@@ -287,6 +298,24 @@ vae_status_t vae_patch_groupnorm_silu(const void* x, const float* gamma, const f
  * called.  x, y, gamma, beta, d: as for vae_patch_groupnorm_silu. */
 vae_status_t vae_patch_groupnorm_silu_noalloc(const void* x, const float* gamma, const float* beta, void* y,
                                               const vae_gn_desc_t* d, void* stream);
+
+/* Channel RMS norm descriptor: x, y channels-last [B, T, H, W, C]. */
+typedef struct {
+  int B, T, H, W, C;
+  float eps;
+  int silu;
+  vae_dtype_t in_dtype, out_dtype;
+} vae_rms_desc_t;
+
+/* Channel RMS norm + optional SiLU ([DV] Qwen-Image, HunyuanVideo/1.5 and LTX-2 adapter commits:
+ * the norm reduces over channels, so a patch needs nothing from its neighbours).  Per pixel
+ * y = x * r * gamma + beta with r = 1 / sqrt(mean over the C channels of x^2 + eps) (fp32 sums in a
+ * fixed order per pixel, so the result does not depend on any patch grid), then SiLU when silu != 0.
+ * x, y: 16-byte aligned device pointers (y may alias x); gamma, beta: fp32 [C], 32-byte aligned.
+ * C: a multiple of 8, at most 1024, with C/8 a power of two or a multiple of 32 (else
+ * VAE_ERR_UNSUPPORTED).  Enqueued on `stream`; nothing is allocated. */
+vae_status_t vae_channel_rmsnorm_silu(const void* x, const float* gamma, const float* beta, void* y,
+                                      const vae_rms_desc_t* d, void* stream);
 
 /* Depth-to-space descriptor: x [B, T, H, W, C*s_t*s_h*s_w] channels-last. */
 typedef struct {

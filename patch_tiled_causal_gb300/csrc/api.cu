@@ -173,9 +173,9 @@ struct vae_decoder {
 namespace {
 
 enum Kind { K_CONV_TC, K_CONV_SIMT, K_GN_STATS, K_GN_APPLY, K_GEMM_TC, K_GEMM_SIMT, K_SOFTMAX, K_TRANSPOSE, K_CAST,
-            K_COPY, K_LATENT, K_BLEND, K_COUNT };
+            K_COPY, K_LATENT, K_BLEND, K_RMS, K_COUNT };
 const char* kKindNames[K_COUNT] = {"conv_tc", "conv_simt", "gn_stats", "gn_apply", "gemm_tc", "gemm_simt",
-                                   "softmax", "transpose", "cast", "copy", "latent", "blend"};
+                                   "softmax", "transpose", "cast", "copy", "latent", "blend", "rms_norm"};
 
 // Brackets one launch with events when the handle is profiling.
 struct Prof {
@@ -268,17 +268,24 @@ int count_weights(const vae_config_t& c) {
 
 vae_status_t check_config(const vae_config_t* c, vae_error_info_t* e) {
   if (!c) return set_err(e, VAE_ERR_INVALID_ARG, 0, 0, "null config");
-  if (c->n_stages < 1 || c->n_stages > VAE_MAX_STAGES || c->latent_c <= 0 || c->gn_groups <= 0 || c->out_c <= 0 ||
+  const bool rms = c->norm_type == VAE_NORM_CHANNEL_RMS;
+  if (c->norm_type != VAE_NORM_GROUP && !rms) return set_err(e, VAE_ERR_INVALID_ARG, 0, 0, "unknown norm type");
+  if (c->n_stages < 1 || c->n_stages > VAE_MAX_STAGES || c->latent_c <= 0 || (!rms && c->gn_groups <= 0) || c->out_c <= 0 ||
       c->mid_res < 0 || c->out_d2s_t < 1 || c->out_d2s_h < 1 || c->out_d2s_w < 1 ||
       (c->dtype != VAE_BF16 && c->dtype != VAE_FP32))
     return set_err(e, VAE_ERR_INVALID_ARG, 0, 0, "invalid decoder config");
   if (c->out_d2s_t != 1) return set_err(e, VAE_ERR_UNSUPPORTED, 0, 0, "temporal depth-to-space in conv_out is not supported");
   for (int i = 0; i < c->n_stages; ++i) {
     const int C = c->stage_c[i];
+    if (rms) {
+      if (C <= 0 || c->n_res[i] < 0) return set_err(e, VAE_ERR_INVALID_ARG, 0, 0, "stage %d channels", i);
+      if (!rms_supported(C)) return set_err(e, VAE_ERR_UNSUPPORTED, 0, 0, "stage %d: RMS norm over %d channels not supported", i, C);
+    } else {
     if (C <= 0 || C % c->gn_groups || c->n_res[i] < 0) return set_err(e, VAE_ERR_INVALID_ARG, 0, 0, "stage %d channels", i);
     const int cpg = C / c->gn_groups;
     if (C % 8 || C > 6144 || !(cpg % 8 == 0 || 8 % cpg == 0))
       return set_err(e, VAE_ERR_UNSUPPORTED, 0, 0, "stage %d: %d channels / %d groups not supported", i, C, c->gn_groups);
+    }
     if (i + 1 < c->n_stages && (c->up_t[i] < 1 || c->up_t[i] > 2 || c->up_h[i] < 1 || c->up_w[i] < 1 || c->up_h[i] != c->up_w[i]))
       return set_err(e, VAE_ERR_UNSUPPORTED, 0, 0, "up-sampler %d factors", i);
   }
@@ -601,7 +608,7 @@ vae_status_t run_conv(Ctx& x, ConvL& c, const Level& L, char* in, const ConvOut&
     const int G = d->cfg.gn_groups;
     const int cpg = Cd % G == 0 ? Cd / G : 0;
     // fused sums cost one warp reduction per group per 32 columns: worth it from 16 channels per group
-    const bool fuse = o.stats_level && !out_ncthw && Cd % 32 == 0 && cpg >= 16 &&
+    const bool fuse = o.stats_level && d->cfg.norm_type == VAE_NORM_GROUP && !out_ncthw && Cd % 32 == 0 && cpg >= 16 &&
                       (cpg < 32 ? 32 % cpg == 0 : cpg % 32 == 0);
     if (fuse) {
       CK(cudaMemsetAsync(x.b.gn, 0, gn_partials_bytes(x.p->nph, x.p->npw, B, o.stats_level->T, G), x.s));
@@ -657,6 +664,11 @@ vae_status_t run_gn(Ctx& x, const NormL& n, const Level& L, const void* src, int
   g.gamma = n.gamma; g.beta = n.beta;
   g.partials = x.b.gn;
   const double elems = static_cast<double>(g.B) * L.T * L.H * L.W * L.C;
+  if (d->cfg.norm_type == VAE_NORM_CHANNEL_RMS) {  // per pixel: no statistics pass
+    Prof pr(d, x.s, K_RMS, 0, elems * ((src_f32 ? 4 : 2) + act_bytes(d)));
+    CK(launch_rms(g, x.s));
+    return VAE_OK;
+  }
   if (x.stats_src != src) {  // not already summed by the producing conv's epilogue
     Prof pr(d, x.s, K_GN_STATS, 0, elems * (src_f32 ? 4 : 2));
     CK(launch_gn_stats(g, x.s));
@@ -704,13 +716,18 @@ vae_status_t run_attention(Ctx& x, const Level& L) {
     g.gamma = d->attn.n.gamma; g.beta = d->attn.n.beta;
     g.partials = x.b.gn;
     const double elems = static_cast<double>(g.B) * L.T * L.H * L.W * C;
-    {
-      Prof pr(d, x.s, K_GN_STATS, 0, elems * (rf ? 4 : 2));
-      CK(launch_gn_stats(g, x.s));
-    }
-    {
-      Prof pr(d, x.s, K_GN_APPLY, 0, elems * ((rf ? 4 : 2) + act_bytes(d)));
-      CK(launch_gn_apply(g, x.s));
+    if (d->cfg.norm_type == VAE_NORM_CHANNEL_RMS) {
+      Prof pr(d, x.s, K_RMS, 0, elems * ((rf ? 4 : 2) + act_bytes(d)));
+      CK(launch_rms(g, x.s));
+    } else {
+      {
+        Prof pr(d, x.s, K_GN_STATS, 0, elems * (rf ? 4 : 2));
+        CK(launch_gn_stats(g, x.s));
+      }
+      {
+        Prof pr(d, x.s, K_GN_APPLY, 0, elems * ((rf ? 4 : 2) + act_bytes(d)));
+        CK(launch_gn_apply(g, x.s));
+      }
     }
   }
   const float scale = 1.0f / std::sqrt(static_cast<float>(C));
@@ -847,6 +864,7 @@ vae_status_t check_shape(vae_decoder* d, const int64_t* shp, int nph, int npw) {
 
 vae_status_t check_gn_range(vae_decoder* d, const Plan& p) {
   // exact integer group sums need fewer than 2^23 elements per (frame, group)
+  if (d->cfg.norm_type != VAE_NORM_GROUP) return VAE_OK;
   for (int i = 0; i < d->cfg.n_stages; ++i) {
     const Level& L = p.lv[i];
     const double n = static_cast<double>(L.C / d->cfg.gn_groups) * L.H * L.W;
@@ -1216,6 +1234,25 @@ extern "C" vae_status_t vae_patch_groupnorm_silu(const void* x, const float* gam
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CK(launch_gn_stats(g, s));
   CK(launch_gn_apply(g, s));
+  return VAE_OK;
+}
+
+extern "C" vae_status_t vae_channel_rmsnorm_silu(const void* x, const float* gamma, const float* beta, void* y,
+                                                 const vae_rms_desc_t* d, void* stream) {
+  if (!x || !gamma || !beta || !y || !d) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null argument");
+  if (!aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(gamma) & 31) ||
+      (reinterpret_cast<uintptr_t>(beta) & 31))
+    return set_err(nullptr, VAE_ERR_ALIGNMENT, 0, 0, "x, y must be 16-byte and gamma, beta 32-byte aligned");
+  if (d->B <= 0 || d->T <= 0 || d->H <= 0 || d->W <= 0 || d->C <= 0 || !(d->eps >= 0.f))
+    return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "bad RMS-norm descriptor");
+  if ((d->in_dtype != VAE_BF16 && d->in_dtype != VAE_FP32) || (d->out_dtype != VAE_BF16 && d->out_dtype != VAE_FP32))
+    return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "bad dtype");
+  if (!rms_supported(d->C)) return set_err(nullptr, VAE_ERR_UNSUPPORTED, 0, 0, "RMS norm over %d channels not supported", d->C);
+  GnArgs g{};
+  g.B = d->B; g.T = d->T; g.H = d->H; g.W = d->W; g.C = d->C; g.eps = d->eps; g.silu = d->silu;
+  g.x = x; g.x_f32 = d->in_dtype == VAE_FP32; g.y = y; g.y_f32 = d->out_dtype == VAE_FP32;
+  g.gamma = gamma; g.beta = beta;
+  CK(launch_rms(g, static_cast<cudaStream_t>(stream)));
   return VAE_OK;
 }
 

@@ -82,6 +82,9 @@ size_t gn_partials_bytes(int nph, int npw, int B, int T, int groups);
 size_t gn_workspace_bytes(int nph, int npw, int B, int T, int groups, int C);
 cudaError_t launch_gn_stats(const GnArgs& a, cudaStream_t s);  // clears and fills partials
 cudaError_t launch_gn_apply(const GnArgs& a, cudaStream_t s);
+// Channel RMS norm (+ SiLU when a.silu) per pixel; uses B..C, eps, silu, x*, y*, gamma, beta of a.
+bool rms_supported(int C);
+cudaError_t launch_rms(const GnArgs& a, cudaStream_t s);
 
 // Layout helpers.
 // Latent box [B, C, t0:t0+nt, h0:h0+nh, w0:w0+nw] of an NCTHW fp32 tensor [B, C, T, H, W] ->

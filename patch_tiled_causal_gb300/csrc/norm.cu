@@ -405,6 +405,108 @@ cudaError_t launch_gn_apply(const GnArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// ============================================================================ channel RMS norm
+// Per pixel r = 1 / sqrt(mean_c x^2 + eps), y = x * r * gamma[c] + beta[c] (then SiLU): the norm of
+// the Wan / Qwen-Image, HunyuanVideo 1.5 and LTX-2 decoders, which reduces over channels only and so
+// needs nothing from other patches.  A team of L = min(32, C/8) lanes (a power of two) owns a pixel:
+// lane j of the team takes the 8-channel vectors j, j + L, ..., sums their squares in that order and
+// the team adds its lanes by xor shuffles, so a pixel's result never depends on the patch grid or on
+// which block runs it.  All lanes of a warp run every loop step (pixels past the end are masked), so
+// the shuffles always see the full warp.
+struct RmsParams {
+  int B, T, H, W, C;
+  float eps;
+  int silu;
+  const void* x;
+  int x_T_alloc;
+  void* y;
+  int y_T_alloc;
+  const float* gamma;
+  const float* beta;
+  int team, vpl;  // lanes per pixel, 8-channel vectors per lane
+};
+constexpr int kRmsMaxVpl = 4;
+
+template <typename TI, typename TO>
+__global__ void __launch_bounds__(256) rms_apply_kernel(const __grid_constant__ RmsParams p) {
+  const int lane = threadIdx.x & 31;
+  const int L = p.team;
+  const int sub = lane & (L - 1);
+  const int per_warp = 32 / L;
+  const int64_t hw = static_cast<int64_t>(p.H) * p.W;
+  const int64_t npx = static_cast<int64_t>(p.B) * p.T * hw;
+  const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const float inv_c = 1.0f / static_cast<float>(p.C);
+  for (int64_t base = warp_id * per_warp; base < npx; base += n_warps * per_warp) {
+    const int64_t px = base + (lane / L);
+    const bool valid = px < npx;
+    const int64_t f = valid ? px / hw : 0;
+    const int64_t r = valid ? px - f * hw : 0;
+    const int b = static_cast<int>(f / p.T), t = static_cast<int>(f - (f / p.T) * p.T);
+    const TI* xp = static_cast<const TI*>(p.x) + ((static_cast<int64_t>(b) * p.x_T_alloc + t) * hw + r) * p.C;
+    TO* yp = static_cast<TO*>(p.y) + ((static_cast<int64_t>(b) * p.y_T_alloc + t) * hw + r) * p.C;
+    float v[kRmsMaxVpl][8];
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < kRmsMaxVpl; ++k) {
+      if (k < p.vpl && valid) {
+        load8(xp + (k * L + sub) * 8, v[k]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(v[k][e], v[k][e], ss);
+      }
+    }
+    for (int off = L >> 1; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float rr = 1.0f / sqrtf(ss * inv_c + p.eps);
+#pragma unroll
+    for (int k = 0; k < kRmsMaxVpl; ++k) {
+      if (k < p.vpl && valid) {
+        const int c0 = (k * L + sub) * 8;
+        const float4* g4 = reinterpret_cast<const float4*>(p.gamma + c0);
+        const float4* b4 = reinterpret_cast<const float4*>(p.beta + c0);
+        const float4 g0 = __ldg(g4), g1 = __ldg(g4 + 1), b0 = __ldg(b4), b1 = __ldg(b4 + 1);
+        const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float z = fmaf(v[k][e] * rr, gg[e], bb[e]);
+          o[e] = p.silu ? __fdividef(z, 1.0f + __expf(-z)) : z;
+        }
+        store8(yp + c0, o);
+      }
+    }
+  }
+}
+
+bool rms_supported(int C) {
+  if (C <= 0 || C % 8) return false;
+  const int nv = C / 8;
+  const int L = nv >= 32 ? 32 : nv;
+  return (L & (L - 1)) == 0 && nv % L == 0 && nv / L <= kRmsMaxVpl;
+}
+
+cudaError_t launch_rms(const GnArgs& a, cudaStream_t s) {
+  if (!rms_supported(a.C)) return cudaErrorInvalidValue;
+  RmsParams p{};
+  p.B = a.B; p.T = a.T; p.H = a.H; p.W = a.W; p.C = a.C; p.eps = a.eps; p.silu = a.silu;
+  p.x = a.x; p.x_T_alloc = a.x_T_alloc ? a.x_T_alloc : a.T;
+  p.y = a.y; p.y_T_alloc = a.y_T_alloc ? a.y_T_alloc : a.T;
+  p.gamma = a.gamma; p.beta = a.beta;
+  const int nv = a.C / 8;
+  p.team = nv >= 32 ? 32 : nv;
+  p.vpl = nv / p.team;
+  const int64_t npx = static_cast<int64_t>(a.B) * a.T * a.H * a.W;
+  if (npx == 0) return cudaSuccess;
+  const int64_t warps = (npx + (32 / p.team) - 1) / (32 / p.team);
+  const int blocks = static_cast<int>(std::min<int64_t>((warps + 7) / 8, 152LL * 8));
+  if (a.x_f32 && a.y_f32) rms_apply_kernel<float, float><<<blocks, 256, 0, s>>>(p);
+  else if (a.x_f32) rms_apply_kernel<float, __nv_bfloat16><<<blocks, 256, 0, s>>>(p);
+  else if (a.y_f32) rms_apply_kernel<__nv_bfloat16, float><<<blocks, 256, 0, s>>>(p);
+  else rms_apply_kernel<__nv_bfloat16, __nv_bfloat16><<<blocks, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
 // ============================================================================ layouts
 template <typename TO>
 __global__ void latent_to_cl_kernel(const float* z, int B, int C, int T, int H, int W, int t0, int nt, int h0, int nh,

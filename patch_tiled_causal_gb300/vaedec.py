@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libvaedec.so")
 VAE_OK, VAE_ERR_INVALID_ARG, VAE_ERR_UNSUPPORTED, VAE_ERR_PATCH_TOO_NARROW = 0, 1, 2, 3
 VAE_ERR_ALIGNMENT, VAE_ERR_OOM, VAE_ERR_CUDA, VAE_ERR_TIMEOUT, VAE_ERR_RANGE = 4, 5, 6, 7, 8
 VAE_BF16, VAE_FP32 = 0, 1
+VAE_NORM_GROUP, VAE_NORM_CHANNEL_RMS = 0, 1
 MAX_STAGES, MAX_PATCHES, MAX_TILES = 8, 64, 512
 
 STATUS_NAMES = {0: "VAE_OK", 1: "VAE_ERR_INVALID_ARG", 2: "VAE_ERR_UNSUPPORTED", 3: "VAE_ERR_PATCH_TOO_NARROW",
@@ -31,7 +32,7 @@ class VaeConfig(C.Structure):
                 ("n_res", C.c_int * MAX_STAGES), ("up_t", C.c_int * MAX_STAGES), ("up_h", C.c_int * MAX_STAGES),
                 ("up_w", C.c_int * MAX_STAGES), ("mid_res", C.c_int), ("mid_attn", C.c_int),
                 ("gn_groups", C.c_int), ("gn_eps", C.c_float), ("out_c", C.c_int), ("out_d2s_t", C.c_int),
-                ("out_d2s_h", C.c_int), ("out_d2s_w", C.c_int), ("dtype", C.c_int)]
+                ("out_d2s_h", C.c_int), ("out_d2s_w", C.c_int), ("dtype", C.c_int), ("norm_type", C.c_int)]
 
 
 class VaeErrorInfo(C.Structure):
@@ -58,6 +59,11 @@ class VaeGnDesc(C.Structure):
                 ("groups", C.c_int), ("eps", C.c_float), ("silu", C.c_int), ("n_patch_h", C.c_int),
                 ("n_patch_w", C.c_int), ("patch_h_edges", _EDGES), ("patch_w_edges", _EDGES),
                 ("in_dtype", C.c_int), ("out_dtype", C.c_int)]
+
+
+class VaeRmsDesc(C.Structure):
+    _fields_ = [("B", C.c_int), ("T", C.c_int), ("H", C.c_int), ("W", C.c_int), ("C", C.c_int),
+                ("eps", C.c_float), ("silu", C.c_int), ("in_dtype", C.c_int), ("out_dtype", C.c_int)]
 
 
 class VaeD2sDesc(C.Structure):
@@ -96,6 +102,7 @@ _SIGS = {
     "vae_patch_groupnorm_workspace_bytes": (C.c_size_t, [C.POINTER(VaeGnDesc)]),
     "vae_patch_groupnorm_silu": (C.c_int, [_P, _P, _P, _P, _P, C.POINTER(VaeGnDesc), _P]),
     "vae_patch_groupnorm_silu_noalloc": (C.c_int, [_P, _P, _P, _P, C.POINTER(VaeGnDesc), _P]),
+    "vae_channel_rmsnorm_silu": (C.c_int, [_P, _P, _P, _P, C.POINTER(VaeRmsDesc), _P]),
     "vae_upsample_d2s": (C.c_int, [_P, _P, C.POINTER(VaeD2sDesc), _P]),
     "vae_tile_blend": (C.c_int, [C.POINTER(_P), C.POINTER(VaeTile), C.c_int, _P, C.POINTER(VaeBlendDesc), _P]),
     "vae_gemm_bf16": (C.c_int, [_P, _P, _P, _P, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int64, C.c_int64,
@@ -277,6 +284,34 @@ def patch_groupnorm_silu_noalloc(x, gamma, beta, y, d: VaeGnDesc, stream=None):
     return y
 
 
+def channel_rmsnorm_silu(x, gamma, beta, y, B, T, H, W, Cc, eps=1e-6, silu=True, stream=None):
+    """Channel RMS norm (+ SiLU) of channels-last x [B, T, H, W, C] into y (vae_channel_rmsnorm_silu)."""
+    torch = _torch()
+    d = VaeRmsDesc()
+    d.B, d.T, d.H, d.W, d.C = B, T, H, W, Cc
+    d.eps, d.silu = eps, int(silu)
+    d.in_dtype, d.out_dtype = _dt(x), _dt(y)
+    _check(load().vae_channel_rmsnorm_silu(_ptr(x), _ptr(gamma, torch.float32), _ptr(beta, torch.float32), _ptr(y),
+                                           C.byref(d), _stream(stream)), "vae_channel_rmsnorm_silu")
+    return y
+
+
+def prepare_channel_rmsnorm_silu(x, gamma, beta, y, B, T, H, W, Cc, eps=1e-6, silu=True, stream=None):
+    """Marshal the arguments of vae_channel_rmsnorm_silu once; returns a function that only makes the call."""
+    torch = _torch()
+    d = VaeRmsDesc()
+    d.B, d.T, d.H, d.W, d.C = B, T, H, W, Cc
+    d.eps, d.silu = eps, int(silu)
+    d.in_dtype, d.out_dtype = _dt(x), _dt(y)
+    lib = load()
+    args = (_ptr(x), _ptr(gamma, torch.float32), _ptr(beta, torch.float32), _ptr(y), C.byref(d), _stream(stream))
+
+    def call():
+        _check(lib.vae_channel_rmsnorm_silu(*args), "vae_channel_rmsnorm_silu")
+    call.keep = (d, x, gamma, beta, y)
+    return call
+
+
 def upsample_d2s(x, y, B, T, H, W, Cc, s, drop_first, stream=None):
     d = VaeD2sDesc()
     d.B, d.T, d.H, d.W, d.C = B, T, H, W, Cc
@@ -355,6 +390,7 @@ def make_config(cfg, dtype: int = VAE_BF16) -> VaeConfig:
     c.out_c = cfg.out_c
     c.out_d2s_t, c.out_d2s_h, c.out_d2s_w = cfg.out_d2s
     c.dtype = dtype
+    c.norm_type = VAE_NORM_CHANNEL_RMS if getattr(cfg, "norm", "group") == "rms" else VAE_NORM_GROUP
     return c
 
 

@@ -49,7 +49,7 @@ def gpu_decode(vd, cfg, dtype, nph=1, npw=1, rand_affine=True):
     return y.float().cpu().numpy()
 
 
-@pytest.mark.parametrize("name", ["tiny", "mini_ltx", "mini_wan"])
+@pytest.mark.parametrize("name", ["tiny", "mini_ltx", "mini_wan", "mini_wan_rms"])
 def test_fp32_mode_matches_oracle(vd, name):
     cfg = synth.CONFIGS[name]
     g = gpu_decode(vd, cfg, vd.VAE_FP32, 2, 2)
@@ -58,7 +58,7 @@ def test_fp32_mode_matches_oracle(vd, name):
     assert metrics.max_rel(g, r) <= 1e-4
 
 
-@pytest.mark.parametrize("name", ["tiny", "mini_ltx", "mini_wan"])
+@pytest.mark.parametrize("name", ["tiny", "mini_ltx", "mini_wan", "mini_wan_rms"])
 def test_bf16_mode_matches_oracle(vd, name):
     cfg = synth.CONFIGS[name]
     g = gpu_decode(vd, cfg, vd.VAE_BF16, 2, 3)
@@ -69,6 +69,7 @@ def test_bf16_mode_matches_oracle(vd, name):
 
 @pytest.mark.parametrize("name,grids", [("mini_ltx", [(1, 1), (2, 2), (2, 4), (3, 5), (10, 13)]),
                                         ("mini_wan", [(1, 1), (1, 4), (3, 2), (9, 11)]),
+                                        ("mini_wan_rms", [(1, 1), (2, 3), (9, 11)]),
                                         ("tiny", [(1, 1), (2, 2), (4, 4), (16, 16)])])
 @pytest.mark.parametrize("dt", ["bf16", "fp32"])
 def test_bit_identical_across_patch_counts(vd, name, grids, dt):
@@ -81,8 +82,9 @@ def test_bit_identical_across_patch_counts(vd, name, grids, dt):
 
 @pytest.mark.parametrize("dt", ["bf16", "fp32"])
 @pytest.mark.parametrize("per", [1, 2])
-def test_chunked_equals_whole(vd, dt, per):
-    cfg = dataclasses.replace(synth.MINI_WAN, latent_shape=(1, 48, 4, 9, 11))
+@pytest.mark.parametrize("base", ["mini_wan", "mini_wan_rms"])
+def test_chunked_equals_whole(vd, dt, per, base):
+    cfg = dataclasses.replace(synth.CONFIGS[base], latent_shape=(1, 48, 4, 9, 11))
     dtc = vd.VAE_BF16 if dt == "bf16" else vd.VAE_FP32
     p = synth.draw_params(cfg, 0, rand_affine=True)
     z = torch.from_numpy(synth.draw_latent(cfg, 0)).cuda()

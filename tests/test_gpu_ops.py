@@ -144,6 +144,42 @@ def test_conv_halo_path_bit_identical_across_patch_counts(vd):
         np.testing.assert_array_equal(o, outs[0])
 
 
+# ----------------------------------------------------------------------------- channel RMS norm
+
+@pytest.mark.parametrize("Cc,din,dout,silu", [(64, "fp32", "fp32", True), (256, "bf16", "bf16", True),
+                                             (1024, "fp32", "bf16", True), (128, "bf16", "fp32", False),
+                                             (512, "fp32", "fp32", False), (8, "fp32", "fp32", True)])
+def test_channel_rmsnorm(vd, Cc, din, dout, silu):
+    shape = (2, 3, 7, 13, Cc)  # ragged pixel count: the last warp's teams run partly masked
+    x = synth.draw_normal(shape, 80, offset=0.3)
+    g = synth.draw_normal((Cc,), 81) * 0.1 + 1.0
+    b = synth.draw_normal((Cc,), 82) * 0.1
+    tin = torch.bfloat16 if din == "bf16" else torch.float32
+    tout = torch.bfloat16 if dout == "bf16" else torch.float32
+    if din == "bf16":
+        x = bf16_round(x)
+    y = torch.full(shape, float("nan"), dtype=tout, device="cuda")
+    vd.channel_rmsnorm_silu(to_dev(x, tin), to_dev(g, torch.float32), to_dev(b, torch.float32), y, *shape, eps=1e-6,
+                            silu=silu)
+    torch.cuda.synchronize()
+    ref = ops.channel_rms_norm(x.transpose(0, 4, 1, 2, 3).astype(np.float64), g, b, 1e-6)
+    if silu:
+        ref = ops.silu(ref)
+    ref = ref.transpose(0, 2, 3, 4, 1)
+    out = y.float().cpu().numpy()
+    assert np.isfinite(out).all()
+    assert rel_err(out, ref) < (BF16_TOL if dout == "bf16" else F32_TOL)
+
+
+def test_channel_rmsnorm_refuses_unsupported_channels(vd):
+    x = torch.zeros(16, dtype=torch.float32, device="cuda")  # never read: refused on the host
+    one = torch.ones(2048, device="cuda")
+    for Cc in (2048, 1032, 12):
+        with pytest.raises(vd.VaeError) as e:
+            vd.channel_rmsnorm_silu(x, one, one, x, 1, 1, 1, 1, Cc)
+        assert e.value.code in (vd.VAE_ERR_UNSUPPORTED,)
+
+
 # ----------------------------------------------------------------------------- PatchGroupNorm
 
 def _gn_case(vd, shape, groups, ph, pw, dt_in, dt_out, offset=0.0, silu=True, seed=50):

@@ -426,54 +426,105 @@ struct RmsParams {
   int team, vpl;  // lanes per pixel, 8-channel vectors per lane
 };
 constexpr int kRmsMaxVpl = 4;
+constexpr int kRmsVecs = 4;  // 8-channel vectors a lane holds per step: kRmsVecs / VPL pixels per team
 
-template <typename TI, typename TO>
+// Raw 8-element loads, converted only when used.
+template <typename T> struct RmsRaw;
+template <> struct RmsRaw<__nv_bfloat16> {
+  uint4 r;
+  VAE_DEV void load(const __nv_bfloat16* p) { r = *reinterpret_cast<const uint4*>(p); }
+  VAE_DEV void get(float* v) const {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+};
+template <> struct RmsRaw<float> {
+  float4 a, b;
+  VAE_DEV void load(const float* p) {
+    a = reinterpret_cast<const float4*>(p)[0];
+    b = reinterpret_cast<const float4*>(p)[1];
+  }
+  VAE_DEV void get(float* v) const {
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+};
+
+// VPL vectors per lane per pixel; each team takes NP = kRmsVecs / VPL consecutive pixels per step and
+// issues all their loads before any sum, then reduces the NP sums side by side.
+template <typename TI, typename TO, int VPL>
 __global__ void __launch_bounds__(256) rms_apply_kernel(const __grid_constant__ RmsParams p) {
+  constexpr int NP = kRmsVecs / VPL;
   const int lane = threadIdx.x & 31;
   const int L = p.team;
   const int sub = lane & (L - 1);
-  const int per_warp = 32 / L;
+  const int teams_per_warp = 32 / L;
   const int64_t hw = static_cast<int64_t>(p.H) * p.W;
   const int64_t npx = static_cast<int64_t>(p.B) * p.T * hw;
   const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const float inv_c = 1.0f / static_cast<float>(p.C);
-  for (int64_t base = warp_id * per_warp; base < npx; base += n_warps * per_warp) {
-    const int64_t px = base + (lane / L);
-    const bool valid = px < npx;
-    const int64_t f = valid ? px / hw : 0;
-    const int64_t r = valid ? px - f * hw : 0;
-    const int b = static_cast<int>(f / p.T), t = static_cast<int>(f - (f / p.T) * p.T);
-    const TI* xp = static_cast<const TI*>(p.x) + ((static_cast<int64_t>(b) * p.x_T_alloc + t) * hw + r) * p.C;
-    TO* yp = static_cast<TO*>(p.y) + ((static_cast<int64_t>(b) * p.y_T_alloc + t) * hw + r) * p.C;
-    float v[kRmsMaxVpl][8];
-    float ss = 0.f;
+  const int64_t per_step = static_cast<int64_t>(teams_per_warp) * NP;  // pixels per warp step
+  for (int64_t base = warp_id * per_step; base < npx; base += n_warps * per_step) {
+    const int64_t px0 = base + static_cast<int64_t>(lane / L) * NP;
+    RmsRaw<TI> raw[NP][VPL];
+    const TI* xp[NP];
+    TO* yp[NP];
+    bool valid[NP];
 #pragma unroll
-    for (int k = 0; k < kRmsMaxVpl; ++k) {
-      if (k < p.vpl && valid) {
-        load8(xp + (k * L + sub) * 8, v[k]);
+    for (int k = 0; k < NP; ++k) {
+      const int64_t px = px0 + k;
+      valid[k] = px < npx;
+      const int64_t f = valid[k] ? px / hw : 0;
+      const int64_t r = valid[k] ? px - f * hw : 0;
+      const int b = static_cast<int>(f / p.T), t = static_cast<int>(f - (f / p.T) * p.T);
+      xp[k] = static_cast<const TI*>(p.x) + ((static_cast<int64_t>(b) * p.x_T_alloc + t) * hw + r) * p.C;
+      yp[k] = static_cast<TO*>(p.y) + ((static_cast<int64_t>(b) * p.y_T_alloc + t) * hw + r) * p.C;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(v[k][e], v[k][e], ss);
-      }
+      for (int j = 0; j < VPL; ++j)
+        if (valid[k]) raw[k][j].load(xp[k] + (j * L + sub) * 8);
     }
-    for (int off = L >> 1; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    const float rr = 1.0f / sqrtf(ss * inv_c + p.eps);
+    float ss[NP];
 #pragma unroll
-    for (int k = 0; k < kRmsMaxVpl; ++k) {
-      if (k < p.vpl && valid) {
-        const int c0 = (k * L + sub) * 8;
-        const float4* g4 = reinterpret_cast<const float4*>(p.gamma + c0);
-        const float4* b4 = reinterpret_cast<const float4*>(p.beta + c0);
-        const float4 g0 = __ldg(g4), g1 = __ldg(g4 + 1), b0 = __ldg(b4), b1 = __ldg(b4 + 1);
-        const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-        const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-        float o[8];
+    for (int k = 0; k < NP; ++k) {
+      ss[k] = 0.f;
+#pragma unroll
+      for (int j = 0; j < VPL; ++j)
+        if (valid[k]) {
+          float v[8];
+          raw[k][j].get(v);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ss[k] = fmaf(v[e], v[e], ss[k]);
+        }
+    }
+    for (int off = L >> 1; off > 0; off >>= 1)
+#pragma unroll
+      for (int k = 0; k < NP; ++k) ss[k] += __shfl_xor_sync(0xffffffffu, ss[k], off);
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int c0 = (j * L + sub) * 8;
+      const float4* g4 = reinterpret_cast<const float4*>(p.gamma + c0);
+      const float4* b4 = reinterpret_cast<const float4*>(p.beta + c0);
+      const float4 g0 = __ldg(g4), g1 = __ldg(g4 + 1), b0 = __ldg(b4), b1 = __ldg(b4 + 1);
+      const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int k = 0; k < NP; ++k) {
+        if (!valid[k]) continue;
+        const float rr = 1.0f / sqrtf(ss[k] * inv_c + p.eps);
+        float v[8], o[8];
+        raw[k][j].get(v);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float z = fmaf(v[k][e] * rr, gg[e], bb[e]);
+          const float z = fmaf(v[e] * rr, gg[e], bb[e]);
           o[e] = p.silu ? __fdividef(z, 1.0f + __expf(-z)) : z;
         }
-        store8(yp + c0, o);
+        store8(yp[k] + c0, o);
       }
     }
   }
@@ -498,12 +549,20 @@ cudaError_t launch_rms(const GnArgs& a, cudaStream_t s) {
   p.vpl = nv / p.team;
   const int64_t npx = static_cast<int64_t>(a.B) * a.T * a.H * a.W;
   if (npx == 0) return cudaSuccess;
-  const int64_t warps = (npx + (32 / p.team) - 1) / (32 / p.team);
+  const int64_t per_warp = static_cast<int64_t>(32 / p.team) * (kRmsVecs / p.vpl);
+  const int64_t warps = (npx + per_warp - 1) / per_warp;
   const int blocks = static_cast<int>(std::min<int64_t>((warps + 7) / 8, 152LL * 8));
-  if (a.x_f32 && a.y_f32) rms_apply_kernel<float, float><<<blocks, 256, 0, s>>>(p);
-  else if (a.x_f32) rms_apply_kernel<float, __nv_bfloat16><<<blocks, 256, 0, s>>>(p);
-  else if (a.y_f32) rms_apply_kernel<__nv_bfloat16, float><<<blocks, 256, 0, s>>>(p);
-  else rms_apply_kernel<__nv_bfloat16, __nv_bfloat16><<<blocks, 256, 0, s>>>(p);
+#define VAE_RMS(VPL)                                                                                     \
+  if (a.x_f32 && a.y_f32) rms_apply_kernel<float, float, VPL><<<blocks, 256, 0, s>>>(p);                 \
+  else if (a.x_f32) rms_apply_kernel<float, __nv_bfloat16, VPL><<<blocks, 256, 0, s>>>(p);               \
+  else if (a.y_f32) rms_apply_kernel<__nv_bfloat16, float, VPL><<<blocks, 256, 0, s>>>(p);               \
+  else rms_apply_kernel<__nv_bfloat16, __nv_bfloat16, VPL><<<blocks, 256, 0, s>>>(p);
+  switch (p.vpl) {
+    case 1: VAE_RMS(1) break;
+    case 2: VAE_RMS(2) break;
+    default: VAE_RMS(4) break;
+  }
+#undef VAE_RMS
   return cudaGetLastError();
 }
 

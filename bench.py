@@ -200,7 +200,8 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="wan", choices=["wan", "ltx"])
+    ap.add_argument("--workload", default="wan", choices=["wan", "ltx", "wan_rms"],
+                    help="wan_rms: the Wan-shaped decoder with channel RMS norms instead of group norms")
     ap.add_argument("--patches", default="1x4", help="patch grid h x w of the timed decode")
     ap.add_argument("--no-ops", action="store_true", help="skip the op-level workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
@@ -208,7 +209,7 @@ def main():
                     help="run only the decode or only the op workloads (profiling runs)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    cfg = synth.WAN if args.workload == "wan" else synth.LTX
+    cfg = {"wan": synth.WAN, "ltx": synth.LTX, "wan_rms": synth.WAN_RMS}[args.workload]
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -7,7 +7,7 @@
 // padding at image edges, halo rows from the neighbour patch at interior edges; the temporal pad is
 // one-sided, frames repeated).
 //
-// GEMM view: M = output pixels of one frame tile (128 = rows_t x cols_t pixels of one patch),
+// GEMM view: M = output pixels of one frame tile (128 or 256 = rows_t x cols_t pixels of one patch),
 // N = output channels (tile BN <= 256), K = 27 taps x C_in, walked tap-major in 64-channel blocks.
 // Per K block one TMA box load brings the tap-shifted 128 x 64 input tile (5-D tensor map over the
 // channels-last activation; out-of-image rows and columns arrive as zeros, the causal time index is
@@ -21,6 +21,14 @@
 // owns the tensor memory and issues tcgen05.mma (128 x BN x 16, bf16 -> fp32 accumulators in TMEM),
 // warps 2-5 drain TMEM with tcgen05.ld and run the epilogue (bias, residual, depth-to-space scatter,
 // bf16/fp32 store, optional fused group-norm partial sums).  Every mbarrier wait is bounded.
+//
+// Launch forms: CTAs run in clusters of 2.  For weight tiles 128 or 256 wide the pair's two M tiles
+// run as one cta_group::2 MMA (each CTA holds half of the weight tile; two 64-channel k blocks per
+// stage where they fit); narrower weight tiles are shared by multicasting each half to both CTAs.
+// Convs at most 32 channels wide (a pixel head) use halo mode: one (rows_t + 2) x (cols_t + 2) box
+// per (kt, channel chunk) feeds all 9 spatial taps through row-offset operand descriptors.  The
+// producer and the MMA issuer advance ring slot, phase and tap with counters (no divisions on
+// their single-thread critical paths).
 #include <cuda.h>
 
 #include <algorithm>

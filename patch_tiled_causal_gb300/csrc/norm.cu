@@ -428,9 +428,9 @@ struct RmsParams {
 constexpr int kRmsMaxVpl = 4;
 constexpr int kRmsVecs = 4;  // 8-channel vectors a lane holds per step: kRmsVecs / VPL pixels per team
 
-// Raw 8-element loads, converted only when used.
-template <typename T> struct RmsRaw;
-template <> struct RmsRaw<__nv_bfloat16> {
+// Raw 8-element loads, converted only when used (so several can be in flight per thread).
+template <typename T> struct Raw8;
+template <> struct Raw8<__nv_bfloat16> {
   uint4 r;
   VAE_DEV void load(const __nv_bfloat16* p) { r = *reinterpret_cast<const uint4*>(p); }
   VAE_DEV void get(float* v) const {
@@ -443,7 +443,7 @@ template <> struct RmsRaw<__nv_bfloat16> {
     }
   }
 };
-template <> struct RmsRaw<float> {
+template <> struct Raw8<float> {
   float4 a, b;
   VAE_DEV void load(const float* p) {
     a = reinterpret_cast<const float4*>(p)[0];
@@ -472,7 +472,7 @@ __global__ void __launch_bounds__(256) rms_apply_kernel(const __grid_constant__ 
   const int64_t per_step = static_cast<int64_t>(teams_per_warp) * NP;  // pixels per warp step
   for (int64_t base = warp_id * per_step; base < npx; base += n_warps * per_step) {
     const int64_t px0 = base + static_cast<int64_t>(lane / L) * NP;
-    RmsRaw<TI> raw[NP][VPL];
+    Raw8<TI> raw[NP][VPL];
     const TI* xp[NP];
     TO* yp[NP];
     bool valid[NP];
@@ -887,33 +887,6 @@ VAE_DEV void cp_async16(void* smem_dst, const void* gsrc) {
 }
 VAE_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N> VAE_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// Raw 8-element loads, converted only when used (so several can be in flight per thread).
-template <typename T> struct Raw8;
-template <> struct Raw8<__nv_bfloat16> {
-  uint4 r;
-  VAE_DEV void load(const __nv_bfloat16* p) { r = *reinterpret_cast<const uint4*>(p); }
-  VAE_DEV void get(float* v) const {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = __bfloat1622float2(h[i]);
-      v[2 * i] = f.x;
-      v[2 * i + 1] = f.y;
-    }
-  }
-};
-template <> struct Raw8<float> {
-  float4 a, b;
-  VAE_DEV void load(const float* p) {
-    a = reinterpret_cast<const float4*>(p)[0];
-    b = reinterpret_cast<const float4*>(p)[1];
-  }
-  VAE_DEV void get(float* v) const {
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-  }
-};
 
 // Grid blend for grids with at most kG2Cols column intervals (others take the general kernel).  Per
 // 8-pixel vector, built once per block: one packed shared-memory word (first column interval, count,

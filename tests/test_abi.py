@@ -68,3 +68,63 @@ def test_invalid_arguments_are_refused(lib):
     import ctypes as C
     n = C.c_int(0)
     assert lib.vae_decoder_n_weights(None, C.byref(n)) == vaedec.VAE_ERR_INVALID_ARG
+
+
+# ctypes mirrors of the header's structs, checked field by field against the C compiler's layout
+STRUCTS = [("VaeConfig", "vae_config_t"), ("VaeErrorInfo", "vae_error_info_t"), ("VaeTile", "vae_tile_t"),
+           ("VaeConvDesc", "vae_conv_desc_t"), ("VaeGnDesc", "vae_gn_desc_t"), ("VaeRmsDesc", "vae_rms_desc_t"),
+           ("VaeD2sDesc", "vae_d2s_desc_t"), ("VaeBlendDesc", "vae_blend_desc_t"), ("VaeProf", "vae_prof_t")]
+
+
+def test_binding_structs_match_header_layout(tmp_path):
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no host C compiler")
+    lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "vaedec.h"', "int main(void) {"]
+    for py, c in STRUCTS:
+        cls = getattr(vaedec, py)
+        lines.append(f'  printf("{py} size %zu\\n", sizeof({c}));')
+        for name, _ in cls._fields_:
+            lines.append(f'  printf("{py} {name} %zu\\n", offsetof({c}, {name}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = {}
+    for line in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines():
+        py, key, val = line.split()
+        got[(py, key)] = int(val)
+    import ctypes as C
+    for py, _ in STRUCTS:
+        cls = getattr(vaedec, py)
+        assert got[(py, "size")] == C.sizeof(cls), py
+        for name, _ in cls._fields_:
+            assert got[(py, name)] == getattr(cls, name).offset, (py, name)
+
+
+def test_config_checks_for_both_norm_families(lib):
+    # host-only validation (no GPU): vae_decoder_n_weights checks the config first
+    import ctypes as C
+    from patch_tiled_causal_gb300 import synth
+    n = C.c_int(0)
+    for name in ("mini_wan", "mini_wan_rms", "wan_rms"):
+        cfg = vaedec.make_config(synth.CONFIGS[name])
+        assert lib.vae_decoder_n_weights(C.byref(cfg), C.byref(n)) == vaedec.VAE_OK, name
+        assert n.value == len(vaedec.param_order(synth.CONFIGS[name]))
+    rms = vaedec.make_config(synth.MINI_WAN_RMS)
+    assert rms.norm_type == vaedec.VAE_NORM_CHANNEL_RMS
+    rms.gn_groups = 0  # ignored by RMS norms
+    assert lib.vae_decoder_n_weights(C.byref(rms), C.byref(n)) == vaedec.VAE_OK
+    for bad_c in (1032, 2048, 12):  # not a power-of-two / multiple-of-32 vector count, too wide, not / 8
+        c = vaedec.make_config(synth.MINI_WAN_RMS)
+        c.stage_c[1] = bad_c
+        assert lib.vae_decoder_n_weights(C.byref(c), C.byref(n)) == vaedec.VAE_ERR_UNSUPPORTED, bad_c
+    c = vaedec.make_config(synth.MINI_WAN)
+    c.norm_type = 7
+    assert lib.vae_decoder_n_weights(C.byref(c), C.byref(n)) == vaedec.VAE_ERR_INVALID_ARG
+    c = vaedec.make_config(synth.MINI_WAN)
+    c.gn_groups = 0  # group norms need groups
+    assert lib.vae_decoder_n_weights(C.byref(c), C.byref(n)) == vaedec.VAE_ERR_INVALID_ARG

@@ -451,7 +451,8 @@ vae_status_t make_plan(vae_decoder* d, int B, int Tlat, int h, int w, int nph, i
     p.x_bytes = std::max(p.x_bytes, px * L.T * L.C * rb);
     p.hin_bytes = std::max(p.hin_bytes, px * (L.T + 2) * L.C * ab);
     p.c1_bytes = std::max(p.c1_bytes, px * std::max<size_t>(static_cast<size_t>(L.T) * cb, (L.T + 2ull) * ab) * L.C);
-    p.gn_bytes = std::max(p.gn_bytes, gn_workspace_bytes(nph, npw, B, L.T, c.gn_groups, L.C));
+    const int groups = c.norm_type == VAE_NORM_GROUP ? c.gn_groups : 0;  // RMS norms keep no partial sums
+    p.gn_bytes = std::max(p.gn_bytes, gn_workspace_bytes(nph, npw, B, L.T, groups, L.C));
   }
   const int Clat = d->conv_in.C_in_pad;
   p.lat_bytes = static_cast<size_t>(B) * (Tlat + 2) * h * w * Clat * ab;
@@ -605,8 +606,8 @@ vae_status_t run_conv(Ctx& x, ConvL& c, const Level& L, char* in, const ConvOut&
     a.y = y; a.out_f32 = y_f32; a.out_ncthw = out_ncthw; a.y_T_alloc = y_T_alloc;
     a.d2s_t = c.st; a.d2s_h = c.sh; a.d2s_w = c.sw; a.drop_first = drop_first;
     const int Cd = c.C_out / (c.st * c.sh * c.sw);
-    const int G = d->cfg.gn_groups;
-    const int cpg = Cd % G == 0 ? Cd / G : 0;
+    const int G = d->cfg.gn_groups;  // (ignored, possibly 0, by channel-RMS decoders)
+    const int cpg = (G > 0 && Cd % G == 0) ? Cd / G : 0;
     // fused sums cost one warp reduction per group per 32 columns: worth it from 16 channels per group
     const bool fuse = o.stats_level && d->cfg.norm_type == VAE_NORM_GROUP && !out_ncthw && Cd % 32 == 0 && cpg >= 16 &&
                       (cpg < 32 ? 32 % cpg == 0 : cpg % 32 == 0);

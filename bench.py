@@ -14,7 +14,8 @@ One JSON line on rank 0 with the contract's keys plus:
   cpu_baseline  the CPU oracle on a bounded spatial crop of the same decode, host cores
 N > 1 (torchrun): each rank decodes its own latent (independent videos, weak scaling), no
 collective on the data path; barriers and the max over ranks bracket the timed region.
---impl reference times the CPU oracle (the reference arm of this build) on rank 0.
+--impl reference times the CPU oracle (the reference arm) on rank 0.
+--workload ltx / wan_rms: the LTX-shaped decoder, or the Wan-shaped one with channel RMS norms.
 """
 from __future__ import annotations
 
@@ -140,7 +141,7 @@ def oracle_sample(cfg, crop_thw, seed=0):
 
 
 REF_CROP = (2, 1, 2)   # latent frames, rows, cols of the reference arm's per-step sample (~10 s)
-CPU_CROP = (3, 1, 2)   # the GPU arm's cpu_baseline sample (~20 s on the GPU machine's host cores)
+CPU_CROP = (3, 1, 2)   # the GPU arm's cpu_baseline sample (~20 s on a GB300 host's 16 Arm cores)
 
 
 def _crop_text(cfg, crop):

@@ -27,7 +27,7 @@ decode, constant tiles blend to the constant, the 576 px LTX-2.5 grid, brute-for
 from __future__ import annotations
 
 import dataclasses
-from typing import List, Sequence, Tuple
+from typing import List, Optional, Sequence, Tuple
 
 import numpy as np
 
@@ -94,15 +94,24 @@ def tile_weight(t: Tile) -> np.ndarray:
     return np.einsum("t,h,w->thw", ramp(nt, a, b), ramp(nh, c, d), ramp(nw, e, f))
 
 
-def blend(tiles: Sequence[Tile], data: Sequence[np.ndarray], out_shape: Sequence[int]) -> np.ndarray:
-    """sum_i w_i x_i / sum_i w_i in float64, raster order.  data[i] is [B, C, nt, nh, nw]."""
-    acc = np.zeros(tuple(out_shape), dtype=np.float64)
-    wsum = np.zeros(tuple(out_shape[2:]), dtype=np.float64)
+def blend(tiles: Sequence[Tile], data: Sequence[np.ndarray], out_shape: Sequence[int],
+          frames: Optional[Tuple[int, int]] = None) -> np.ndarray:
+    """sum_i w_i x_i / sum_i w_i in float64, raster order.  data[i] is [B, C, nt, nh, nw].
+
+    frames = (f0, f1): form only output frames f0 .. f1-1 (every tile keeps its whole weight; a
+    tile not covering those frames contributes nothing and its data may be None)."""
+    f0, f1 = frames if frames is not None else (0, out_shape[2])
+    shape = (out_shape[0], out_shape[1], f1 - f0) + tuple(out_shape[3:])
+    acc = np.zeros(shape, dtype=np.float64)
+    wsum = np.zeros(shape[2:], dtype=np.float64)
     for t, x in zip(tiles, data):
         t0, nt, h0, nh, w0, nw = t.pix
-        wt = tile_weight(t)
-        acc[:, :, t0:t0 + nt, h0:h0 + nh, w0:w0 + nw] += wt * x.astype(np.float64)
-        wsum[t0:t0 + nt, h0:h0 + nh, w0:w0 + nw] += wt
+        a, b = max(t0, f0), min(t0 + nt, f1)
+        if a >= b:
+            continue
+        wt = tile_weight(t)[a - t0:b - t0]
+        acc[:, :, a - f0:b - f0, h0:h0 + nh, w0:w0 + nw] += wt * x[:, :, a - t0:b - t0].astype(np.float64)
+        wsum[a - f0:b - f0, h0:h0 + nh, w0:w0 + nw] += wt
     return acc / wsum
 
 

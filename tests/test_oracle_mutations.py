@@ -8,7 +8,7 @@ test_oracle_pins.py and are imported, not restated.
 import numpy as np
 import pytest
 
-from oracle import ops, tiles
+from oracle import decoder, ops, tiles
 from tests import test_oracle_pins as pins
 
 
@@ -27,6 +27,8 @@ def test_pins_pass_unmutated():
     pins.test_channel_rms_norm_vs_torch()
     pins.test_ramps_sum_to_one_in_overlaps()
     pins.test_silu_closed_form()
+    pins.test_resblock_vs_library("group")
+    pins.test_decoder_vs_library("mini_wan")
 
 
 def test_flipped_kernel_is_caught(monkeypatch):
@@ -108,3 +110,70 @@ def test_sign_error_in_silu_is_caught(monkeypatch):
             return x / (1.0 + np.exp(x))
     monkeypatch.setattr(ops, "silu", wrong_sign)
     _fails(pins.test_silu_closed_form)
+
+
+def test_swapped_norm_parameters_in_resblock_are_caught(monkeypatch):
+    # norm2's scale and shift used for the first norm and norm1's for the second
+    orig = ops.resblock
+
+    def swapped(x, p, prefix, groups, eps, conv, kind="group"):
+        q = dict(p)
+        for k in ("gamma", "beta"):
+            q[f"{prefix}.norm1.{k}"], q[f"{prefix}.norm2.{k}"] = p[f"{prefix}.norm2.{k}"], p[f"{prefix}.norm1.{k}"]
+        return orig(x, q, prefix, groups, eps, conv, kind)
+    monkeypatch.setattr(ops, "resblock", swapped)
+    _fails(pins.test_resblock_vs_library, "group")
+    _fails(pins.test_decoder_vs_library, "mini_wan")
+
+
+def test_dropped_silu_before_conv2_is_caught(monkeypatch):
+    def no_second_silu(x, p, prefix, groups, eps, conv, kind="group"):
+        dt = x.dtype
+        h = ops.silu(ops.norm(x, p[prefix + ".norm1.gamma"], p[prefix + ".norm1.beta"], groups, eps, kind)).astype(dt)
+        h = conv(prefix + ".conv1", h)
+        h = ops.norm(h, p[prefix + ".norm2.gamma"], p[prefix + ".norm2.beta"], groups, eps, kind).astype(dt)
+        return x + conv(prefix + ".conv2", h)
+    monkeypatch.setattr(ops, "resblock", no_second_silu)
+    _fails(pins.test_resblock_vs_library, "group")
+    _fails(pins.test_decoder_vs_library, "mini_wan")
+
+
+def _mutated_chunk(skip=None, up_first=False):
+    """The decoder's layer sequence with one residual block skipped, or with a stage's up-sampling
+    conv run before that stage's residual blocks (where the channel counts allow it)."""
+    def run(cfg, p, z, conv, dtype):
+        g, eps, kind = cfg.gn_groups, cfg.gn_eps, cfg.norm
+        x = conv("conv_in", z.astype(dtype))
+        for r in range(cfg.mid_res):
+            x = ops.resblock(x, p, f"mid.res{r}", g, eps, conv, kind).astype(dtype)
+        if cfg.mid_attn:
+            x = ops.spatial_attention(x, p, "mid.attn", g, eps, dtype=dtype, kind=kind).astype(dtype)
+        for i in range(cfg.n_stages):
+            early = up_first and i + 1 < cfg.n_stages and cfg.stage_c[i] == cfg.stage_c[i + 1]
+            if early:
+                x = ops.depth_to_space(conv(f"stage{i}.up", x), cfg.up[i], drop_first=conv.first)
+            for r in range(cfg.n_res[i]):
+                if (i, r) != skip:
+                    x = ops.resblock(x, p, f"stage{i}.res{r}", g, eps, conv, kind).astype(dtype)
+            if i + 1 < cfg.n_stages and not early:
+                x = ops.depth_to_space(conv(f"stage{i}.up", x), cfg.up[i], drop_first=conv.first)
+        x = ops.silu(ops.norm(x, p["head.norm.gamma"], p["head.norm.beta"], g, eps, kind)).astype(dtype)
+        return ops.depth_to_space(conv("head.conv", x), cfg.out_d2s, drop_first=conv.first)
+    return run
+
+
+def test_skipped_resblock_is_caught(monkeypatch):
+    monkeypatch.setattr(decoder, "_decode_chunk", _mutated_chunk(skip=(1, 0)))
+    _fails(pins.test_decoder_vs_library, "mini_wan")
+
+
+def test_up_conv_before_the_stage_resblocks_is_caught(monkeypatch):
+    # mini_wan's first two stages have the same width, so the reordered decoder still runs
+    monkeypatch.setattr(decoder, "_decode_chunk", _mutated_chunk(up_first=True))
+    _fails(pins.test_decoder_vs_library, "mini_wan")
+
+
+def test_unmutated_copy_of_the_layer_sequence_passes(monkeypatch):
+    # the copy above, with no mutation switched on, is the oracle's sequence: the pin passes on it
+    monkeypatch.setattr(decoder, "_decode_chunk", _mutated_chunk())
+    pins.test_decoder_vs_library("mini_wan")

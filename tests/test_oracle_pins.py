@@ -282,6 +282,120 @@ def test_resblock_zero_conv2_is_identity():
     np.testing.assert_array_equal(ops.resblock(x, p, "stage0.res0", 8, 1e-6, run), x)
 
 
+# A second formulation of the residual block and of the whole decoder, written from the stated
+# architecture with library routines only (torch.nn.functional conv3d, group_norm, rms_norm, silu,
+# linear, scaled_dot_product_attention; depth-to-space as strided assignments).  It shares no code
+# with the oracle, so a wiring mistake in the oracle (parameters of one norm used for the other, a
+# missing activation, a skipped block, a stage's layers in the wrong order) shows up as a mismatch.
+
+def _lt(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64))
+
+
+def _lib_conv(x, p, name):
+    """Causal 3x3x3 conv: frame 0 twice in front, one zero pixel on each spatial side."""
+    w = _lt(p[name + ".weight"])
+    front = x[:, :, :1].expand(-1, -1, w.shape[2] - 1, -1, -1)
+    return torch.nn.functional.conv3d(torch.cat([front, x], dim=2), w, _lt(p[name + ".bias"]), padding=(0, 1, 1))
+
+
+def _lib_norm(x, p, name, groups, eps, kind):
+    """Group norm of each frame ([B*T, C, H, W] view), or RMS norm over the channels of each pixel."""
+    b, c, t, h, w = x.shape
+    g, bt = _lt(p[name + ".gamma"]), _lt(p[name + ".beta"])
+    if kind == "rms":
+        y = torch.nn.functional.rms_norm(x.permute(0, 2, 3, 4, 1), (c,), eps=eps) * g + bt
+        return y.permute(0, 4, 1, 2, 3)
+    v = x.permute(0, 2, 1, 3, 4).reshape(b * t, c, h, w)
+    y = torch.nn.functional.group_norm(v, groups, g, bt, eps)
+    return y.reshape(b, t, c, h, w).permute(0, 2, 1, 3, 4)
+
+
+def _lib_d2s(x, s, drop_first):
+    """Channel c*S + dt*sh*sw + dy*sw + dx -> (c, st*t + dt, sh*y + dy, sw*x + dx), by strided writes."""
+    st, sh, sw = s
+    S = st * sh * sw
+    b, cs, t, h, w = x.shape
+    y = torch.empty((b, cs // S, st * t, sh * h, sw * w), dtype=x.dtype)
+    for dt in range(st):
+        for dy in range(sh):
+            for dx in range(sw):
+                y[:, :, dt::st, dy::sh, dx::sw] = x[:, dt * sh * sw + dy * sw + dx::S]
+    return y[:, :, st - 1:] if drop_first and st > 1 else y
+
+
+def _lib_resblock(x, p, prefix, groups, eps, kind):
+    silu = torch.nn.functional.silu
+    hmid = _lib_conv(silu(_lib_norm(x, p, prefix + ".norm1", groups, eps, kind)), p, prefix + ".conv1")
+    hmid = _lib_conv(silu(_lib_norm(hmid, p, prefix + ".norm2", groups, eps, kind)), p, prefix + ".conv2")
+    return x + hmid
+
+
+def _lib_attention(x, p, prefix, groups, eps, kind):
+    b, c, t, h, w = x.shape
+    tok = _lib_norm(x, p, prefix + ".norm", groups, eps, kind).permute(0, 2, 3, 4, 1).reshape(b * t, 1, h * w, c)
+    lin = lambda a, n: torch.nn.functional.linear(a, _lt(p[f"{prefix}.{n}.weight"]), _lt(p[f"{prefix}.{n}.bias"]))
+    o = torch.nn.functional.scaled_dot_product_attention(lin(tok, "q"), lin(tok, "k"), lin(tok, "v"))
+    return x + lin(o, "o").reshape(b, t, h, w, c).permute(0, 4, 1, 2, 3)
+
+
+def _lib_decode(cfg, p, z):
+    g, eps, kind = cfg.gn_groups, cfg.gn_eps, cfg.norm
+    x = _lib_conv(_lt(z), p, "conv_in")
+    for r in range(cfg.mid_res):
+        x = _lib_resblock(x, p, f"mid.res{r}", g, eps, kind)
+    if cfg.mid_attn:
+        x = _lib_attention(x, p, "mid.attn", g, eps, kind)
+    for i in range(cfg.n_stages):
+        for r in range(cfg.n_res[i]):
+            x = _lib_resblock(x, p, f"stage{i}.res{r}", g, eps, kind)
+        if i + 1 < cfg.n_stages:
+            x = _lib_d2s(_lib_conv(x, p, f"stage{i}.up"), cfg.up[i], True)
+    x = torch.nn.functional.silu(_lib_norm(x, p, "head.norm", g, eps, kind))
+    return _lib_d2s(_lib_conv(x, p, "head.conv"), cfg.out_d2s, True).numpy()
+
+
+@pytest.mark.parametrize("kind", ["group", "rms"])
+def test_resblock_vs_library(kind):
+    # random norm affines and conv biases, so that norm1 / norm2 and conv1 / conv2 are told apart
+    cfg = synth.TINY
+    p = synth.draw_params(cfg, 0, rand_affine=True)
+    x = synth.draw_normal((1, 32, 3, 5, 6), 26).astype(np.float64)
+    y = ops.resblock(x, p, "stage0.res1", 8, 1e-6, decoder._ConvRunner(p, "A"), kind)
+    ref = _lib_resblock(_lt(x), p, "stage0.res1", 8, 1e-6, kind).numpy()
+    np.testing.assert_allclose(y, ref, rtol=1e-10, atol=1e-10)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mini_wan", "mini_ltx", "mini_wan_rms"])
+def test_decoder_vs_library(name):
+    cfg = synth.CONFIGS[name]
+    p = synth.draw_params(cfg, 0, rand_affine=True)
+    z = synth.draw_latent(cfg, 0)
+    y = decoder.decode(cfg, p, z)
+    ref = _lib_decode(cfg, p, z)
+    assert y.shape == ref.shape
+    assert metrics.max_rel(y, ref) < 1e-10
+
+
+@pytest.mark.parametrize("name", ["tiny", "mini_wan"])
+def test_every_parameter_reaches_the_output(name):
+    # a skipped layer, norm or projection would leave its parameters without effect on the pixels.
+    # The one exception is exact: a key bias adds q.b_k to every score of a query, and the softmax
+    # over keys ignores a per-query constant, so that bias must have no effect.
+    cfg = synth.CONFIGS[name]
+    p = synth.draw_params(cfg, 0, rand_affine=True)
+    z = synth.draw_latent(cfg, 0)
+    y = decoder.decode(cfg, p, z, tier="B")
+    for k in p:
+        q = dict(p)
+        q[k] = p[k] + synth.draw_normal(p[k].shape, 27, std=0.5)
+        change = np.abs(decoder.decode(cfg, q, z, tier="B") - y).max() / np.abs(y).max()
+        if k.endswith("attn.k.bias"):
+            assert change < 1e-5, k
+        else:
+            assert change > 1e-4, k
+
+
 @pytest.mark.parametrize("name", ["tiny", "mini_wan", "mini_wan_rms"])
 def test_causality(name):
     cfg = synth.CONFIGS[name]
@@ -298,7 +412,7 @@ def test_causality(name):
     assert np.abs(y2[:, :, keep:] - y[:, :, keep:]).max() > 1e-3
 
 
-@pytest.mark.parametrize("name", ["tiny", "mini_wan", "mini_wan_rms"])
+@pytest.mark.parametrize("name", ["tiny", "mini_wan", "mini_wan_rms", "mini_ltx"])
 def test_chunked_equals_whole(name):
     cfg = synth.CONFIGS[name]
     p = synth.draw_params(cfg, 0, rand_affine=True)
@@ -409,6 +523,17 @@ def test_blend_brute_force_and_constant():
             np.testing.assert_allclose(out[0, :, 0, y, x], num / den, rtol=1e-13)
     const = tiles.blend(t, [np.full_like(d, 3.25) for d in data], shape)
     np.testing.assert_allclose(const, 3.25, rtol=1e-15)
+
+
+def test_blend_frame_window_equals_full_blend():
+    # forming only a window of output frames gives exactly those frames of the full blend
+    t = tiles.tile_plan((4, 10, 9), (2, 6, 5), (1, 2, 2), 4, 1)  # causal time: 13 frames, 1-frame overlaps
+    shape = (1, 2, 13, 10, 9)
+    data = [synth.draw_normal((1, 2) + (tl.pix[1], tl.pix[3], tl.pix[5]), 40 + i).astype(np.float64)
+            for i, tl in enumerate(t)]
+    full = tiles.blend(t, data, shape)
+    for f0, f1 in [(0, 13), (3, 6), (4, 5), (12, 13)]:
+        np.testing.assert_array_equal(tiles.blend(t, data, shape, frames=(f0, f1)), full[:, :, f0:f1])
 
 
 def test_single_tile_equals_untiled_decode():

@@ -11,7 +11,10 @@ One JSON line on rank 0 with the contract's keys plus:
   kernels       the same per kernel class (conv, group norm stats/apply, attention GEMMs, ...)
   ops           the op-level workloads: PatchGroupNorm+SiLU, channel RMS norm+SiLU, causal conv 512->512,
                 tile blend
-  cpu_baseline  the CPU oracle on a bounded spatial crop of the same decode, host cores
+  extra         the LTX-shaped 720p x 81f decode (1x4 and 2x4 patches) and the batch-2 overlap-tiled LTX
+                decode (45 tiles -> [2,3,129,1088,1920]): Mframe-px/s, conv fraction, per-kernel table
+  cpu_baseline  the CPU oracle on a bounded sample of the same decode (first 2 latent frames of one
+                full-width latent row), host cores
 N > 1 (torchrun): each rank decodes its own latent (independent videos, weak scaling), no
 collective on the data path; barriers and the max over ranks bracket the timed region.
 --impl reference times the CPU oracle (the reference arm) on rank 0.
@@ -124,14 +127,20 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------- CPU oracle
+_PARAMS = {}
+
+
 def oracle_sample(cfg, crop_thw, seed=0):
-    """Time the CPU oracle (Tier B, float32) decoding a crop (first frames, top-left latent pixels)
-    of the workload's latent; returns (decoded frame-px, seconds)."""
+    """Time the CPU oracle (Tier B, float32) decoding a crop (first frames, top latent rows, left
+    latent columns) of the workload's latent; returns (decoded frame-px, seconds).  The parameters
+    are drawn once per workload, outside the timing."""
     from oracle import decoder as odec
     b, c, t, h, w = cfg.latent_shape
     ct, ch, cw = crop_thw
     sub = dataclasses.replace(cfg, latent_shape=(b, c, ct, ch, cw))
-    p = synth.draw_params(sub, seed)
+    if cfg.name not in _PARAMS:
+        _PARAMS[cfg.name] = synth.draw_params(cfg, seed)
+    p = _PARAMS[cfg.name]
     z = synth.draw_latent(cfg, seed)[:, :, :ct, :ch, :cw].copy()
     t0 = time.perf_counter()
     y = odec.decode(sub, p, z, tier="B")
@@ -140,17 +149,26 @@ def oracle_sample(cfg, crop_thw, seed=0):
     return frame_px, dt
 
 
-REF_CROP = (2, 1, 2)   # latent frames, rows, cols of the reference arm's per-step sample (~10 s)
-CPU_CROP = (3, 1, 2)   # the GPU arm's cpu_baseline sample (~20 s on a GB300 host's 16 Arm cores)
+# The oracle's bounded sample: the first 2 latent frames (-> 5 output frames) of one full-width row of
+# latent pixels, so every layer runs its real channel counts over a full image row (realistic BLAS
+# shapes); ~15 s per sample on 16 host cores.  The reference arm times one such sample per step.
+SAMPLE_ROWS = 1
+SAMPLE_FRAMES = 2
+METRIC = "decoded Mframe-px/s at 720p x 81f bf16"
+
+
+def sample_crop(cfg):
+    return (SAMPLE_FRAMES, SAMPLE_ROWS, cfg.latent_shape[4])
 
 
 def _crop_text(cfg, crop):
-    return (f"{cfg.name} decode of the first {crop[0]} latent frames x a {crop[1]}x{crop[2]} latent crop "
-            f"(of {cfg.latent_shape[2]} x {cfg.latent_shape[3]}x{cfg.latent_shape[4]}), Tier B float32 (numpy BLAS)")
+    return (f"{cfg.name} decode of the first {crop[0]} latent frames x {crop[1]} full-width row(s) of {crop[2]} latent "
+            f"pixels (of {cfg.latent_shape[2]} x {cfg.latent_shape[3]}x{cfg.latent_shape[4]}), Tier B float32 "
+            f"(numpy BLAS)")
 
 
 def run_reference(args, cfg):
-    crop = REF_CROP
+    crop = sample_crop(cfg)
     for _ in range(args.warmup):
         oracle_sample(cfg, crop)
     times, fpx = [], 0
@@ -160,7 +178,7 @@ def run_reference(args, cfg):
     total = sum(times)
     v = fpx * args.steps / total / 1e6
     cores = os.cpu_count()
-    line = {"impl": "reference", "metric": "decoded Mframe-px/s at 720p x 81f (bf16 target; oracle fp32)",
+    line = {"impl": "reference", "metric": METRIC,
             "value": v, "unit": "Mframe-px/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000 * total / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -206,6 +224,7 @@ def main():
     ap.add_argument("--patches", default="1x4", help="patch grid h x w of the timed decode")
     ap.add_argument("--no-ops", action="store_true", help="skip the op-level workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-extra", action="store_true", help="skip the LTX-shaped and tiled decode sub-lines")
     ap.add_argument("--only", default="all", choices=["all", "decode", "ops"],
                     help="run only the decode or only the op workloads (profiling runs)")
     args = ap.parse_args()
@@ -239,7 +258,7 @@ def main():
         print(json.dumps({"ops": run_ops(args, torch, vaedec, peaks, flush), "peaks": peaks}), flush=True)
         return
     if args.only == "decode":
-        args.no_ops = args.no_cpu = True
+        args.no_ops = args.no_cpu = args.no_extra = True
 
     nph, npw = (int(v) for v in args.patches.lower().split("x"))
     params = synth.draw_params(cfg, 0)
@@ -307,18 +326,8 @@ def main():
     e2e_value = throughput(frame_px, args.steps, world,
                            max_over_ranks(sum(a.elapsed_time(b) for a, b in eev) / 1000.0, dist, "cuda"))
 
-    kernels = {}
-    for k, v in sorted(prof.items(), key=lambda kv: -kv[1]["ms"]):
-        e = {"launches_per_step": v["launches"] // args.steps, "ms_per_step": v["ms"] / args.steps,
-             "share": v["ms"] / max(sum(x["ms"] for x in prof.values()), 1e-9)}
-        if v["flops"]:
-            e["tflops"] = v["flops"] / (v["ms"] / 1e3) / 1e12
-            e["frac_of_bf16_sustained"] = e["tflops"] / peaks["bf16_tflops_sustained"]
-        if v["bytes"]:
-            e["gbs"] = v["bytes"] / (v["ms"] / 1e3) / 1e9
-            e["frac_of_hbm"] = e["gbs"] / peaks["hbm_gbs"]
-        kernels[k] = e
-    conv = prof.get("conv_tc", {"flops": 0.0, "ms": 1.0, "launches": 1})
+    kernels = kernel_table(prof, args.steps, peaks)
+    conv = conv_totals(prof)
     conv_tf = conv["flops"] / (conv["ms"] / 1e3) / 1e12
     tr = _traffic(f"conv_tc_decode_{cfg.name}")
     roofline = {"bound": "tensor", "kernel": "conv_tc (tcgen05 implicit-GEMM causal conv), all launches of the decode",
@@ -334,16 +343,22 @@ def main():
     ops = None
     if not args.no_ops and rank == 0:
         ops = run_ops(args, torch, vaedec, peaks, flush)
+    extra = None
+    if not args.no_extra and rank == 0 and args.workload == "wan":
+        dec.close()  # frees the Wan decoder's workspace before the LTX decoders are built
+        torch.cuda.empty_cache()
+        extra = run_ltx(args, torch, vaedec, peaks, flush, stream)
 
     cpu = None
     if not args.no_cpu and rank == 0 and world == 1:
-        fpx, dt = oracle_sample(cfg, CPU_CROP)
+        crop = sample_crop(cfg)
+        fpx, dt = oracle_sample(cfg, crop)
         cpu = {"value": fpx / dt / 1e6, "unit": "Mframe-px/s", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": _crop_text(cfg, CPU_CROP) + f", {fpx} frame-px in {dt:.1f} s"}
+               "sample": _crop_text(cfg, crop) + f", {fpx} frame-px in {dt:.1f} s"}
 
     if rank == 0:
         line = {
-            "metric": "decoded Mframe-px/s at 720p x 81f bf16", "value": value, "unit": "Mframe-px/s",
+            "metric": METRIC, "value": value, "unit": "Mframe-px/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * t_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) latent, N(0,1/fan_in) random-init weights)",
@@ -360,12 +375,91 @@ def main():
             "clocks": clocks,
             "cpu_baseline": cpu,
             "ops": ops,
+            "extra": extra,
             "peaks": peaks,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def kernel_table(prof, steps, peaks):
+    """Per kernel class: launches and device time per step, share, and the fraction of its roofline."""
+    kernels = {}
+    total = max(sum(x["ms"] for x in prof.values()), 1e-9)
+    for k, v in sorted(prof.items(), key=lambda kv: -kv[1]["ms"]):
+        e = {"launches_per_step": v["launches"] // steps, "ms_per_step": v["ms"] / steps, "share": v["ms"] / total}
+        if v["flops"]:
+            e["tflops"] = v["flops"] / (v["ms"] / 1e3) / 1e12
+            e["frac_of_bf16_sustained"] = e["tflops"] / peaks["bf16_tflops_sustained"]
+        if v["bytes"]:
+            e["gbs"] = v["bytes"] / (v["ms"] / 1e3) / 1e9
+            e["frac_of_hbm"] = e["gbs"] / peaks["hbm_gbs"]
+        kernels[k] = e
+    return kernels
+
+
+def conv_totals(prof):
+    """The tcgen05 conv kernel over all its launches: the body convs plus the pixel head (conv_head)."""
+    conv = {k: sum(prof.get(c, {}).get(k, 0) for c in ("conv_tc", "conv_head")) for k in ("flops", "ms", "launches")}
+    return conv if conv["launches"] else {"flops": 0.0, "ms": 1.0, "launches": 1}
+
+
+def timed_decodes(torch, dec, fn, steps, warmup, flush, stream):
+    """Run fn (one decode) warmup times, then steps timed times with L2 flushed before each; returns
+    (ms per decode from CUDA events on the launching stream, per-kernel profile of the timed decodes)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    dec.profile(True)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    prof = dec.profile_read()
+    dec.profile(False)
+    return sum(a.elapsed_time(b) for a, b in evs) / steps, prof
+
+
+def run_ltx(args, torch, vd, peaks, flush, stream):
+    """The LTX-shaped 720p x 81f decode at 1x4 and 2x4 patches, and the batch-2 overlap-tiled LTX decode
+    (latent [2,128,17,34,60] -> [2,3,129,1088,1920], 45 tiles of 8x16x16 latents, 1x4x4 overlap)."""
+    res = {}
+    for cfg, tiled in ((synth.LTX, False), (synth.LTX_TILED, True)):
+        params = synth.draw_params(cfg, 0)
+        dec = vd.Decoder(cfg, params, vd.VAE_BF16)
+        del params
+        z = torch.from_numpy(synth.draw_latent(cfg, 0)).cuda()
+        out = torch.empty(dec.output_shape(z.shape), dtype=torch.bfloat16, device="cuda")
+        runs = [("tiled", None)] if tiled else [("1x4", (1, 4)), ("2x4", (2, 4))]
+        for tag, grid in runs:
+            if tiled:
+                tl = synth.LTX_TILING
+                fn = lambda: dec.decode_tiled(z, tl.tile, tl.overlap, out)
+            else:
+                fn = lambda g=grid: dec.decode(z, out, g[0], g[1])
+            ms, prof = timed_decodes(torch, dec, fn, args.steps, args.warmup, flush, stream)
+            code, msg = vd.last_error(dec.h)
+            if code:
+                raise RuntimeError(f"{cfg.name} decode failed: {msg}")
+            fpx = out.shape[0] * out.shape[2] * out.shape[3] * out.shape[4]
+            conv = conv_totals(prof)
+            tf = conv["flops"] / (conv["ms"] / 1e3) / 1e12
+            res[f"{cfg.name}_{tag}"] = {
+                "workload": f"{cfg.name}-shaped decoder, latent {list(cfg.latent_shape)} -> pixels {list(out.shape)}, "
+                            + ("45 overlap tiles of 8x16x16 latents (1x4x4 overlap), blended" if tiled
+                               else f"{grid[0]}x{grid[1]} spatial patches"),
+                "value": fpx / ms / 1e3, "unit": "Mframe-px/s", "ms_per_step": ms,
+                "conv_tflops": tf, "conv_frac_of_bf16_sustained": tf / peaks["bf16_tflops_sustained"],
+                "kernels": kernel_table(prof, args.steps, peaks)}
+        dec.close()
+        del z, out
+        torch.cuda.empty_cache()
+    return res
 
 
 def _time(torch, fn, steps, flush):

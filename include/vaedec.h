@@ -48,10 +48,22 @@ typedef enum {
   VAE_ERR_OOM = 5,              /* a library-owned allocation failed */
   VAE_ERR_CUDA = 6,             /* a CUDA runtime call failed */
   VAE_ERR_TIMEOUT = 7,          /* a bounded wait inside a kernel ran out (device watchdog) */
-  VAE_ERR_RANGE = 8             /* a group-norm input with |x| >= 8192 (outside the exact-sum range) */
+  VAE_ERR_RANGE = 8             /* a group-norm input with |x| >= 8192 (outside the exact-sum range), or an
+                                   e4m3 conv operand with |x| > 448 (stored saturated) */
 } vae_status_t;
 
-typedef enum { VAE_BF16 = 0, VAE_FP32 = 1 } vae_dtype_t;
+/* Storage / arithmetic types.  VAE_FP8 is e4m3 (1 sign, 4 exponent, 3 mantissa bits; largest finite
+ * value 448) for convolution operands, multiplied on the tcgen05 tensor cores (kind::f8f6f4, fp32
+ * accumulation); the low-precision conv of [WAN]'s reviewer comment (FP4 conv quantisation with the
+ * RMSNorm/SiLU -> quantisation fusion), here at 8 bits.  Weights are e4m3 with one fp32 scale per
+ * output channel (max |w| / 448) applied in the conv epilogue; activations are stored unscaled
+ * (round to nearest even; a value beyond +-448 is saturated and flags VAE_ERR_RANGE).  As a decoder
+ * dtype: the residual blocks' and up-samplers' convs whose input channels are a multiple of 128 take
+ * e4m3 operands written by the norm (norm + SiLU -> quantisation in one pass) or by the last residual
+ * block's conv epilogue; conv_in, conv_out, attention, the residual stream and conv1's output stay as in
+ * bf16 mode; pixels are bf16.  Accuracy bar against the fp32 oracle: relative L2 <= 0.1 and PSNR >= 35 dB
+ * (each e4m3 rounding has unit roundoff 2^-4). */
+typedef enum { VAE_BF16 = 0, VAE_FP32 = 1, VAE_FP8 = 2 } vae_dtype_t;
 
 /* The decoder's norm family.  VAE_NORM_GROUP: per-frame group norm whose statistics span patches
  * ([DV] PatchGroupNorm commit).  VAE_NORM_CHANNEL_RMS: a channel RMS norm per pixel, the norm of the
@@ -167,8 +179,9 @@ vae_status_t vae_decode_tiled(vae_decoder_t* dec, const void* latent, const int6
  * reads and writes the operation needs).  Enabling creates events per launch: do not enable it
  * inside a CUDA-graph capture. */
 typedef struct {
-  char name[32];   /* kernel class: conv_tc, conv_simt, gn_stats, gn_apply, gemm_tc, gemm_simt, softmax,
-                      transpose, cast, copy, latent, blend */
+  char name[32];   /* kernel class: conv_tc (tensor-core convs but the pixel head), conv_head (the
+                      tensor-core conv_out), conv_simt, gn_stats, gn_apply, gemm_tc, gemm_simt, softmax,
+                      transpose, cast, copy, latent, blend, rms_norm */
   int launches;    /* launches since the last read */
   double ms;       /* summed device time of those launches */
   double flops;    /* summed algorithmic FLOPs */
@@ -236,7 +249,9 @@ size_t vae_conv3d_packed_bytes(const vae_conv_desc_t* d);
 /* Repack an fp32 PyTorch-layout weight [C_out, C_in, 3, 3, 3] (device) into the library layout
  * (device, vae_conv3d_packed_bytes(d) bytes, caller-owned): for bf16 a K-major [N_pad, 27*C_in_pad]
  * matrix whose rows are ordered (depth-to-space sub-position, channel) so that the fused
- * depth-to-space stores contiguous channels; for fp32 [27, C_in, C_out]. */
+ * depth-to-space stores contiguous channels; for fp8 the same matrix in e4m3 bytes, each row divided
+ * by its scale max|row| / 448, followed (at the next 256-byte boundary) by the fp32 scales [N_pad];
+ * for fp32 [27, C_in, C_out]. */
 vae_status_t vae_conv3d_pack_weights(const float* w, const vae_conv_desc_t* d, void* w_packed, void* stream);
 
 /* Causal Conv3d ([DV] PatchConv3d padding commit, HunyuanVideo/LTX-2 commits): for every output
@@ -247,8 +262,10 @@ vae_status_t vae_conv3d_pack_weights(const float* w, const vae_conv_desc_t* d, v
  * or NULL (only without depth-to-space); y: [B, T', H*d2s_h, W*d2s_w, C_out/(d2s)] channels-last or
  * NCTHW, T' = d2s_t*T - (drop_first ? d2s_t-1 : 0).  Each patch's outputs are computed by blocks
  * that own that patch; their halo taps read the neighbour patch's rows in place.  bf16 inputs with
- * C_in % 64 == 0 run on the tcgen05 tensor-core kernel, the rest on a CUDA-core kernel.  y must
- * not alias x or residual. */
+ * C_in % 64 == 0 run on the tcgen05 tensor-core kernel, the rest on a CUDA-core kernel; e4m3 inputs
+ * (in_dtype VAE_FP8, C_in % 128 == 0, weights packed for VAE_FP8) run on the tensor cores with e4m3
+ * products (kind::f8f6f4), each output channel's sum multiplied by its weight scale before the bias.
+ * y must not alias x or residual. */
 vae_status_t vae_conv3d_causal(const void* x, const void* w_packed, const float* bias, const void* residual,
                                void* y, const vae_conv_desc_t* d, void* stream);
 
@@ -263,6 +280,8 @@ typedef struct {
   int patch_w_edges[VAE_MAX_PATCHES + 1];
   vae_dtype_t in_dtype, out_dtype;
 } vae_gn_desc_t;
+
+/* out_dtype VAE_FP8: y is written as e4m3 operands of a following fp8 conv (in_dtype bf16 or fp32). */
 
 /* Bytes of scratch `vae_patch_groupnorm_silu` needs for `d`. */
 size_t vae_patch_groupnorm_workspace_bytes(const vae_gn_desc_t* d);
@@ -299,7 +318,7 @@ vae_status_t vae_patch_groupnorm_silu(const void* x, const float* gamma, const f
 vae_status_t vae_patch_groupnorm_silu_noalloc(const void* x, const float* gamma, const float* beta, void* y,
                                               const vae_gn_desc_t* d, void* stream);
 
-/* Channel RMS norm descriptor: x, y channels-last [B, T, H, W, C]. */
+/* Channel RMS norm descriptor: x, y channels-last [B, T, H, W, C] (out_dtype VAE_FP8: e4m3 y). */
 typedef struct {
   int B, T, H, W, C;
   float eps;

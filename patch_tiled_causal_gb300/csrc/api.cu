@@ -109,6 +109,8 @@ constexpr bool kC1F32 = true;
 struct ConvL {
   int C_in = 0, C_out = 0, C_in_pad = 0, N_pad = 0, st = 1, sh = 1, sw = 1;
   bool tc = false;
+  bool fp8 = false;        // e4m3 operands and weights (fp8 decoders)
+  float* wscale = nullptr; // fp8: per-output-channel weight scales (inside the packed weight buffer)
   void* w = nullptr;       // packed weights
   float* bias = nullptr;   // fp32 [C_out]
   void* cache = nullptr;   // [B, 2, H, W, C_in_pad] (chunked decode)
@@ -139,6 +141,7 @@ struct Level {  // one spatial/temporal scale of the decode
 struct vae_decoder {
   vae_config_t cfg{};
   bool f32 = false;  // fp32 storage mode
+  bool f8 = false;   // e4m3 operands for the residual blocks' and up-samplers' convs
   ConvL conv_in;
   std::vector<ResL> mid;
   bool has_attn = false;
@@ -172,10 +175,12 @@ struct vae_decoder {
 
 namespace {
 
+// conv_head: the tensor-core conv_out (pixel head), timed apart from the other convs
 enum Kind { K_CONV_TC, K_CONV_SIMT, K_GN_STATS, K_GN_APPLY, K_GEMM_TC, K_GEMM_SIMT, K_SOFTMAX, K_TRANSPOSE, K_CAST,
-            K_COPY, K_LATENT, K_BLEND, K_RMS, K_COUNT };
+            K_COPY, K_LATENT, K_BLEND, K_RMS, K_CONV_HEAD, K_COUNT };
 const char* kKindNames[K_COUNT] = {"conv_tc", "conv_simt", "gn_stats", "gn_apply", "gemm_tc", "gemm_simt",
-                                   "softmax", "transpose", "cast", "copy", "latent", "blend", "rms_norm"};
+                                   "softmax", "transpose", "cast", "copy", "latent", "blend", "rms_norm",
+                                   "conv_head"};
 
 // Brackets one launch with events when the handle is profiling.
 struct Prof {
@@ -212,11 +217,13 @@ vae_status_t dalloc(vae_decoder* d, T** p, size_t bytes) {
 }
 
 int act_bytes(const vae_decoder* d) { return d->f32 ? 4 : 2; }
+// bytes of one element of conv c's operand (e4m3 convs of an fp8 decoder take 1)
+int op_bytes(const vae_decoder* d, const ConvL& c) { return c.fp8 ? 1 : act_bytes(d); }
 int res_bytes(const vae_decoder* d) { return (d->f32 || kResidF32) ? 4 : 2; }
 int c1_bytes(const vae_decoder* d) { return (d->f32 || kC1F32) ? 4 : 2; }
 
 vae_status_t make_conv(vae_decoder* d, ConvL& c, const float* w, const float* b, int C_in, int C_out, int st, int sh,
-                       int sw, bool pad_input = false) {
+                       int sw, bool pad_input = false, bool allow_fp8 = false) {
   c.C_in = C_in;
   c.C_out = C_out;
   c.st = st; c.sh = sh; c.sw = sw;
@@ -225,7 +232,15 @@ vae_status_t make_conv(vae_decoder* d, ConvL& c, const float* w, const float* b,
   // tensor cores take 64-channel K blocks; the latent is zero-padded up to them when it is converted
   c.tc = !d->f32 && (C_in % 64 == 0 || pad_input);
   c.C_in_pad = c.tc ? round_up(C_in, 64) : C_in;
-  if (c.tc) {
+  c.fp8 = d->f8 && allow_fp8 && c.tc && C_in % 128 == 0;
+  if (c.fp8) {
+    c.N_pad = round_up(C_out, 16);
+    const size_t off = fp8_scale_offset(c.N_pad, c.C_in_pad);
+    vae_status_t s = dalloc(d, &c.w, off + static_cast<size_t>(c.N_pad) * 4);
+    if (s) return s;
+    c.wscale = reinterpret_cast<float*>(static_cast<char*>(c.w) + off);
+    CK(launch_pack_weights_fp8(w, C_out, C_in, c.C_in_pad, c.N_pad, S, c.w, nullptr));
+  } else if (c.tc) {
     c.N_pad = C_out <= 256 ? round_up(C_out, 16) : round_up(C_out, 16);
     const size_t bytes = static_cast<size_t>(c.N_pad) * 27 * c.C_in_pad * 2;
     vae_status_t s = dalloc(d, &c.w, bytes);
@@ -272,7 +287,7 @@ vae_status_t check_config(const vae_config_t* c, vae_error_info_t* e) {
   if (c->norm_type != VAE_NORM_GROUP && !rms) return set_err(e, VAE_ERR_INVALID_ARG, 0, 0, "unknown norm type");
   if (c->n_stages < 1 || c->n_stages > VAE_MAX_STAGES || c->latent_c <= 0 || (!rms && c->gn_groups <= 0) || c->out_c <= 0 ||
       c->mid_res < 0 || c->out_d2s_t < 1 || c->out_d2s_h < 1 || c->out_d2s_w < 1 ||
-      (c->dtype != VAE_BF16 && c->dtype != VAE_FP32))
+      (c->dtype != VAE_BF16 && c->dtype != VAE_FP32 && c->dtype != VAE_FP8))
     return set_err(e, VAE_ERR_INVALID_ARG, 0, 0, "invalid decoder config");
   if (c->out_d2s_t != 1) return set_err(e, VAE_ERR_UNSUPPORTED, 0, 0, "temporal depth-to-space in conv_out is not supported");
   for (int i = 0; i < c->n_stages; ++i) {
@@ -328,14 +343,15 @@ extern "C" vae_status_t vae_decoder_create(const vae_config_t* cfg, const void* 
   vae_decoder* d = new vae_decoder();
   d->cfg = *cfg;
   d->f32 = cfg->dtype == VAE_FP32;
+  d->f8 = cfg->dtype == VAE_FP8;
   int k = 0;
   auto W = [&](void) { return static_cast<const float*>(weights[k++]); };
   auto res_block = [&](ResL& r, int C) -> vae_status_t {
     const float *g1 = W(), *b1 = W(), *w1 = W(), *bb1 = W(), *g2 = W(), *b2 = W(), *w2 = W(), *bb2 = W();
     vae_status_t st = make_norm(d, r.n1, g1, b1, C);
-    if (!st) st = make_conv(d, r.c1, w1, bb1, C, C, 1, 1, 1);
+    if (!st) st = make_conv(d, r.c1, w1, bb1, C, C, 1, 1, 1, false, true);
     if (!st) st = make_norm(d, r.n2, g2, b2, C);
-    if (!st) st = make_conv(d, r.c2, w2, bb2, C, C, 1, 1, 1);
+    if (!st) st = make_conv(d, r.c2, w2, bb2, C, C, 1, 1, 1, false, true);
     return st;
   };
   const int C0 = cfg->stage_c[0];
@@ -374,7 +390,8 @@ extern "C" vae_status_t vae_decoder_create(const vae_config_t* cfg, const void* 
       const float* w = W();
       const float* b = W();
       const int S = cfg->up_t[i] * cfg->up_h[i] * cfg->up_w[i];
-      s = make_conv(d, d->ups[i], w, b, cfg->stage_c[i], S * cfg->stage_c[i + 1], cfg->up_t[i], cfg->up_h[i], cfg->up_w[i]);
+      s = make_conv(d, d->ups[i], w, b, cfg->stage_c[i], S * cfg->stage_c[i + 1], cfg->up_t[i], cfg->up_h[i], cfg->up_w[i],
+                    false, true);
     }
   }
   if (!s) {
@@ -532,7 +549,7 @@ vae_status_t ensure_caches(vae_decoder* d, const Plan& p) {
   vae_status_t st = VAE_OK;
   for_each_conv(d, [&](ConvL& c, int lvl) {
     const Level& L = p.lv[lvl];
-    const size_t need = static_cast<size_t>(p.B) * 2 * L.H * L.W * c.C_in_pad * act_bytes(d);
+    const size_t need = static_cast<size_t>(p.B) * 2 * L.H * L.W * c.C_in_pad * op_bytes(d, c);
     if (c.cache_bytes < need) ok = false;
   });
   if (ok) return VAE_OK;
@@ -540,7 +557,7 @@ vae_status_t ensure_caches(vae_decoder* d, const Plan& p) {
   for_each_conv(d, [&](ConvL& c, int lvl) {
     if (st) return;
     const Level& L = p.lv[lvl];
-    const size_t need = static_cast<size_t>(p.B) * 2 * L.H * L.W * c.C_in_pad * act_bytes(d);
+    const size_t need = static_cast<size_t>(p.B) * 2 * L.H * L.W * c.C_in_pad * op_bytes(d, c);
     if (c.cache_bytes >= need) return;
     void* q = nullptr;
     if (cudaMalloc(&q, need) != cudaSuccess) {
@@ -573,7 +590,8 @@ struct ConvOut {
   int res_f32 = 0;
   int drop_first = 0;
   const Level* stats_level = nullptr;  // fuse group-norm partial sums of y at this level (nullptr = no)
-  void* y2 = nullptr;                  // bf16 copy of y behind 2 cache frames (next conv's operand)
+  void* y2 = nullptr;                  // copy of y behind 2 cache frames (next conv's operand) ...
+  int y2_fp8 = 0;                      // ... in e4m3 (else bf16)
 };
 
 // Run conv `c` at level L.  `in` is its input buffer (conv operand dtype, B x (2+T) frames, frames 0..1
@@ -581,7 +599,7 @@ struct ConvOut {
 vae_status_t run_conv(Ctx& x, ConvL& c, const Level& L, char* in, const ConvOut& o) {
   vae_decoder* d = x.d;
   const int B = x.p->B, T = L.T, Ta = T + 2;
-  const int64_t frame_bytes = static_cast<int64_t>(L.H) * L.W * c.C_in_pad * act_bytes(d);
+  const int64_t frame_bytes = static_cast<int64_t>(L.H) * L.W * c.C_in_pad * op_bytes(d, c);
   const bool use_cache = x.chunked && !x.p->first;
   x.stats_src = nullptr;
   void* y = o.y;
@@ -605,6 +623,7 @@ vae_status_t run_conv(Ctx& x, ConvL& c, const Level& L, char* in, const ConvOut&
     a.residual = residual; a.res_f32 = res_f32; a.res_T_alloc = T;
     a.y = y; a.out_f32 = y_f32; a.out_ncthw = out_ncthw; a.y_T_alloc = y_T_alloc;
     a.d2s_t = c.st; a.d2s_h = c.sh; a.d2s_w = c.sw; a.drop_first = drop_first;
+    a.fp8 = c.fp8; a.wscale = c.wscale;
     const int Cd = c.C_out / (c.st * c.sh * c.sw);
     const int G = d->cfg.gn_groups;  // (ignored, possibly 0, by channel-RMS decoders)
     const int cpg = (G > 0 && Cd % G == 0) ? Cd / G : 0;
@@ -617,12 +636,13 @@ vae_status_t run_conv(Ctx& x, ConvL& c, const Level& L, char* in, const ConvOut&
       a.gn_groups = G;
     }
     if (o.y2) {
-      const int64_t f2 = static_cast<int64_t>(L.H) * c.sh * L.W * c.sw * Cd * 2;
+      const int64_t f2 = static_cast<int64_t>(L.H) * c.sh * L.W * c.sw * Cd * (o.y2_fp8 ? 1 : 2);
       a.y2 = static_cast<char*>(o.y2) + 2 * f2;
       a.y2_T_alloc = (o.stats_level ? o.stats_level->T : T) + 2;
+      a.y2_fp8 = o.y2_fp8;
     }
     {
-      Prof pr(d, x.s, K_CONV_TC, conv_flops, 0);
+      Prof pr(d, x.s, &c == &d->head ? K_CONV_HEAD : K_CONV_TC, conv_flops, 0);
       CK(launch_conv_tc(a, x.s));
     }
     if (fuse) x.stats_src = y;
@@ -652,21 +672,23 @@ vae_status_t run_conv(Ctx& x, ConvL& c, const Level& L, char* in, const ConvOut&
   return VAE_OK;
 }
 
-// GN (+SiLU) of src (B x T frames, dtype src_f32) into hin frames [2, 2+T)
-vae_status_t run_gn(Ctx& x, const NormL& n, const Level& L, const void* src, int src_f32, int silu) {
+// GN (+SiLU) of src (B x T frames, dtype src_f32) into hin frames [2, 2+T), in the operand type of the
+// conv that reads them (out_fp8: e4m3)
+vae_status_t run_gn(Ctx& x, const NormL& n, const Level& L, const void* src, int src_f32, int silu, bool out_fp8) {
   vae_decoder* d = x.d;
   GnArgs g{};
   g.B = x.p->B; g.T = L.T; g.H = L.H; g.W = L.W; g.C = L.C; g.groups = d->cfg.gn_groups;
   g.eps = d->cfg.gn_eps; g.silu = silu;
   g.nph = x.p->nph; g.npw = x.p->npw; g.ph_edges = L.ph; g.pw_edges = L.pw;
   g.x = src; g.x_f32 = src_f32; g.x_T_alloc = L.T;
-  const int64_t frame_bytes = static_cast<int64_t>(L.H) * L.W * L.C * act_bytes(d);
-  g.y = x.b.hin + 2 * frame_bytes; g.y_f32 = d->f32; g.y_T_alloc = L.T + 2;
+  const int ob = out_fp8 ? 1 : act_bytes(d);
+  const int64_t frame_bytes = static_cast<int64_t>(L.H) * L.W * L.C * ob;
+  g.y = x.b.hin + 2 * frame_bytes; g.y_f32 = d->f32; g.y_T_alloc = L.T + 2; g.y_fp8 = out_fp8;
   g.gamma = n.gamma; g.beta = n.beta;
   g.partials = x.b.gn;
   const double elems = static_cast<double>(g.B) * L.T * L.H * L.W * L.C;
   if (d->cfg.norm_type == VAE_NORM_CHANNEL_RMS) {  // per pixel: no statistics pass
-    Prof pr(d, x.s, K_RMS, 0, elems * ((src_f32 ? 4 : 2) + act_bytes(d)));
+    Prof pr(d, x.s, K_RMS, 0, elems * ((src_f32 ? 4 : 2) + ob));
     CK(launch_rms(g, x.s));
     return VAE_OK;
   }
@@ -675,26 +697,31 @@ vae_status_t run_gn(Ctx& x, const NormL& n, const Level& L, const void* src, int
     CK(launch_gn_stats(g, x.s));
   }
   {
-    Prof pr(d, x.s, K_GN_APPLY, 0, elems * ((src_f32 ? 4 : 2) + act_bytes(d)));
+    Prof pr(d, x.s, K_GN_APPLY, 0, elems * ((src_f32 ? 4 : 2) + ob));
     CK(launch_gn_apply(g, x.s));
   }
   return VAE_OK;
 }
 
-// One residual block.  With up_copy, conv2 also stores a bf16 copy of the new residual stream into
-// the conv1 buffer (behind 2 cache frames) for the up-sampling conv that follows; *copied says so.
-vae_status_t run_resblock(Ctx& x, ResL& r, const Level& L, bool up_copy = false, bool* copied = nullptr) {
+// One residual block.  With up_copy, conv2 also stores a copy of the new residual stream into the
+// conv1 buffer (behind 2 cache frames) for the up-sampling conv that follows, in that conv's operand
+// type (e4m3 when up_fp8, else bf16); *copied says so.
+vae_status_t run_resblock(Ctx& x, ResL& r, const Level& L, bool up_copy = false, bool* copied = nullptr,
+                          bool up_fp8 = false) {
   vae_decoder* d = x.d;
   const int rf = res_bytes(d) == 4, cf = c1_bytes(d) == 4;
-  vae_status_t s = run_gn(x, r.n1, L, x.b.x, rf, 1);
+  vae_status_t s = run_gn(x, r.n1, L, x.b.x, rf, 1, r.c1.fp8);
   ConvOut o1;
   o1.y = x.b.c1; o1.y_f32 = cf; o1.y_T_alloc = L.T; o1.stats_level = &L;
   if (!s) s = run_conv(x, r.c1, L, x.b.hin, o1);
-  if (!s) s = run_gn(x, r.n2, L, x.b.c1, cf, 1);
+  if (!s) s = run_gn(x, r.n2, L, x.b.c1, cf, 1, r.c2.fp8);
   ConvOut o2;  // in-place residual add
   o2.y = x.b.x; o2.y_f32 = rf; o2.y_T_alloc = L.T; o2.residual = x.b.x; o2.res_f32 = rf; o2.stats_level = &L;
   const bool cp = up_copy && r.c2.tc && !d->f32 && L.C % 32 == 0;
-  if (cp) o2.y2 = x.b.c1;
+  if (cp) {
+    o2.y2 = x.b.c1;
+    o2.y2_fp8 = up_fp8;
+  }
   if (!s) s = run_conv(x, r.c2, L, x.b.hin, o2);
   if (copied) *copied = cp && !s;
   return s;
@@ -824,7 +851,7 @@ vae_status_t run_decode(vae_decoder* d, const Plan& p, const float* latent, cons
     bool copied = false;
     for (size_t r = 0; r < d->stages[i].size(); ++r) {
       const bool last = r + 1 == d->stages[i].size() && i + 1 < c.n_stages;
-      st = run_resblock(x, d->stages[i][r], L, last, &copied);
+      st = run_resblock(x, d->stages[i][r], L, last, &copied, last && d->ups[i].fp8);
       if (st) return st;
     }
     if (i + 1 < c.n_stages) {
@@ -834,8 +861,10 @@ vae_status_t run_decode(vae_decoder* d, const Plan& p, const float* latent, cons
       char* in = x.b.c1;
       if (!copied) {
         in = x.b.hin;
-        Prof pr(d, s, K_CAST, 0, static_cast<double>(p.B) * L.T * fe * (res_bytes(d) + act_bytes(d)));
-        CK(launch_cast_frames(x.b.x, rf, L.T, x.b.hin + 2 * fe * act_bytes(d), d->f32, L.T + 2, p.B, L.T, fe, s));
+        const int ob = op_bytes(d, d->ups[i]);
+        Prof pr(d, s, K_CAST, 0, static_cast<double>(p.B) * L.T * fe * (res_bytes(d) + ob));
+        CK(launch_cast_frames(x.b.x, rf, L.T, x.b.hin + 2 * fe * ob, d->ups[i].fp8 ? 2 : (d->f32 ? 1 : 0), L.T + 2, p.B,
+                              L.T, fe, s));
       }
       ConvOut o;
       o.y = x.b.x; o.y_f32 = rf; o.y_T_alloc = p.lv[i + 1].T; o.drop_first = p.first ? 1 : 0;
@@ -845,7 +874,7 @@ vae_status_t run_decode(vae_decoder* d, const Plan& p, const float* latent, cons
     }
   }
   const Level& LL = p.lv[c.n_stages - 1];
-  st = run_gn(x, d->head_norm, LL, x.b.x, rf, 1);
+  st = run_gn(x, d->head_norm, LL, x.b.x, rf, 1, d->head.fp8);
   if (st) return st;
   ConvOut o;
   o.y = out; o.y_f32 = d->f32; o.y_T_alloc = out_T_alloc; o.out_ncthw = 1; o.drop_first = p.first ? 1 : 0;
@@ -1131,11 +1160,13 @@ vae_status_t check_edges(int n, const int* e, int extent, const char* what) {
   return VAE_OK;
 }
 bool conv_tc_ok(const vae_conv_desc_t* d) { return d->in_dtype == VAE_BF16 && d->C_in % 64 == 0; }
+bool conv_fp8(const vae_conv_desc_t* d) { return d->in_dtype == VAE_FP8; }
 int conv_npad(const vae_conv_desc_t* d) { return (d->C_out + 15) / 16 * 16; }
 }  // namespace
 
 extern "C" size_t vae_conv3d_packed_bytes(const vae_conv_desc_t* d) {
   if (!d || d->C_in <= 0 || d->C_out <= 0) return 0;
+  if (conv_fp8(d)) return fp8_scale_offset(conv_npad(d), d->C_in) + static_cast<size_t>(conv_npad(d)) * 4;
   if (conv_tc_ok(d)) return static_cast<size_t>(conv_npad(d)) * 27 * d->C_in * 2;
   return 27ull * d->C_in * d->C_out * 4;
 }
@@ -1145,7 +1176,10 @@ extern "C" vae_status_t vae_conv3d_pack_weights(const float* w, const vae_conv_d
   const int S = d->d2s_t * d->d2s_h * d->d2s_w;
   if (S < 1 || d->C_out % S) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "C_out %% depth-to-space");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (conv_tc_ok(d)) CK(launch_pack_weights_bf16(w, d->C_out, d->C_in, d->C_in, conv_npad(d), S, w_packed, s));
+  if (conv_fp8(d) && d->C_in % 128)
+    return set_err(nullptr, VAE_ERR_UNSUPPORTED, 0, 0, "fp8 convs need C_in %% 128 == 0 (got %d)", d->C_in);
+  if (conv_fp8(d)) CK(launch_pack_weights_fp8(w, d->C_out, d->C_in, d->C_in, conv_npad(d), S, w_packed, s));
+  else if (conv_tc_ok(d)) CK(launch_pack_weights_bf16(w, d->C_out, d->C_in, d->C_in, conv_npad(d), S, w_packed, s));
   else CK(launch_pack_weights_f32(w, d->C_out, d->C_in, w_packed, s));
   return VAE_OK;
 }
@@ -1161,14 +1195,23 @@ extern "C" vae_status_t vae_conv3d_causal(const void* x, const void* w_packed, c
   const int S = d->d2s_t * d->d2s_h * d->d2s_w;
   if (d->C_out % S) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "C_out not divisible by the depth-to-space factor");
   if (residual && S != 1) return set_err(nullptr, VAE_ERR_UNSUPPORTED, 0, 0, "residual with depth-to-space");
-  if (d->in_dtype == VAE_FP32 && d->out_dtype == VAE_BF16 && false) return VAE_ERR_UNSUPPORTED;
+  if (d->in_dtype != VAE_BF16 && d->in_dtype != VAE_FP32 && d->in_dtype != VAE_FP8)
+    return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "bad input dtype");
+  if (d->out_dtype == VAE_FP8 || d->res_dtype == VAE_FP8)
+    return set_err(nullptr, VAE_ERR_UNSUPPORTED, 0, 0, "conv outputs and residuals are bf16 or fp32");
+  if (conv_fp8(d) && d->C_in % 128)
+    return set_err(nullptr, VAE_ERR_UNSUPPORTED, 0, 0, "fp8 convs need C_in %% 128 == 0 (got %d)", d->C_in);
   vae_status_t st = check_edges(d->n_patch_h, d->patch_h_edges, d->H, "height");
   if (!st) st = check_edges(d->n_patch_w, d->patch_w_edges, d->W, "width");
   if (st) return st;
   if ((x == y) || (residual && residual == y && S != 1)) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "y aliases x");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (conv_tc_ok(d)) {
+  if (conv_tc_ok(d) || conv_fp8(d)) {
     ConvTcArgs a{};
+    if (conv_fp8(d)) {
+      a.fp8 = 1;
+      a.wscale = reinterpret_cast<const float*>(static_cast<const char*>(w_packed) + fp8_scale_offset(conv_npad(d), d->C_in));
+    }
     a.mode = 0;
     a.B = d->B; a.T = d->T; a.H = d->H; a.W = d->W; a.C_in_pad = d->C_in;
     a.T_in = d->T + d->cache_frames; a.x_T_alloc = a.T_in; a.cache_frames = d->cache_frames;
@@ -1201,6 +1244,9 @@ namespace {
 vae_status_t check_gn_desc(const vae_gn_desc_t* d) {
   if (d->B <= 0 || d->T <= 0 || d->H <= 0 || d->W <= 0 || d->C <= 0 || d->groups <= 0 || d->C % d->groups)
     return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "bad group-norm descriptor");
+  if ((d->in_dtype != VAE_BF16 && d->in_dtype != VAE_FP32) ||
+      (d->out_dtype != VAE_BF16 && d->out_dtype != VAE_FP32 && d->out_dtype != VAE_FP8))
+    return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "bad group-norm dtypes");
   const int cpg = d->C / d->groups;
   if (d->C % 8 || d->C > 6144 || d->groups > 1024 || !(cpg % 8 == 0 || 8 % cpg == 0))
     return set_err(nullptr, VAE_ERR_UNSUPPORTED, 0, 0, "%d channels in %d groups not supported", d->C, d->groups);
@@ -1231,6 +1277,7 @@ extern "C" vae_status_t vae_patch_groupnorm_silu(const void* x, const float* gam
   g.B = d->B; g.T = d->T; g.H = d->H; g.W = d->W; g.C = d->C; g.groups = d->groups; g.eps = d->eps; g.silu = d->silu;
   g.nph = d->n_patch_h; g.npw = d->n_patch_w; g.ph_edges = d->patch_h_edges; g.pw_edges = d->patch_w_edges;
   g.x = x; g.x_f32 = d->in_dtype == VAE_FP32; g.y = y; g.y_f32 = d->out_dtype == VAE_FP32;
+  g.y_fp8 = d->out_dtype == VAE_FP8;
   g.gamma = gamma; g.beta = beta; g.partials = workspace;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CK(launch_gn_stats(g, s));
@@ -1246,12 +1293,14 @@ extern "C" vae_status_t vae_channel_rmsnorm_silu(const void* x, const float* gam
     return set_err(nullptr, VAE_ERR_ALIGNMENT, 0, 0, "x, y must be 16-byte and gamma, beta 32-byte aligned");
   if (d->B <= 0 || d->T <= 0 || d->H <= 0 || d->W <= 0 || d->C <= 0 || !(d->eps >= 0.f))
     return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "bad RMS-norm descriptor");
-  if ((d->in_dtype != VAE_BF16 && d->in_dtype != VAE_FP32) || (d->out_dtype != VAE_BF16 && d->out_dtype != VAE_FP32))
+  if ((d->in_dtype != VAE_BF16 && d->in_dtype != VAE_FP32) ||
+      (d->out_dtype != VAE_BF16 && d->out_dtype != VAE_FP32 && d->out_dtype != VAE_FP8))
     return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "bad dtype");
   if (!rms_supported(d->C)) return set_err(nullptr, VAE_ERR_UNSUPPORTED, 0, 0, "RMS norm over %d channels not supported", d->C);
   GnArgs g{};
   g.B = d->B; g.T = d->T; g.H = d->H; g.W = d->W; g.C = d->C; g.eps = d->eps; g.silu = d->silu;
   g.x = x; g.x_f32 = d->in_dtype == VAE_FP32; g.y = y; g.y_f32 = d->out_dtype == VAE_FP32;
+  g.y_fp8 = d->out_dtype == VAE_FP8;
   g.gamma = gamma; g.beta = beta;
   CK(launch_rms(g, static_cast<cudaStream_t>(stream)));
   return VAE_OK;

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -65,6 +66,36 @@ VAE_DEV void store8(__nv_bfloat16* p, const float* v) {
 VAE_DEV void store8(float* p, const float* v) {
   reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
   reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// 8 consecutive e4m3 bytes (FP8 conv operands: 1 sign, 4 exponent, 3 mantissa bits, largest finite 448).
+// Round to nearest even with saturation to +-448; returns false if any |v| exceeded 448 (or was NaN),
+// so the caller can flag a range fault instead of passing on a clipped operand.
+VAE_DEV bool store8_e4m3(__nv_fp8_e4m3* p, const float* v) {
+  uint2 u;
+  unsigned short* h = reinterpret_cast<unsigned short*>(&u);
+  bool ok = true;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    ok = ok && fabsf(v[2 * i]) <= 448.f && fabsf(v[2 * i + 1]) <= 448.f;
+    h[i] = __nv_cvt_float2_to_fp8x2(make_float2(v[2 * i], v[2 * i + 1]), __NV_SATFINITE, __NV_E4M3);
+  }
+  *reinterpret_cast<uint2*>(p) = u;
+  return ok;
+}
+VAE_DEV float e4m3_to_f(__nv_fp8_e4m3 v) { return static_cast<float>(v); }
+template <> VAE_DEV float to_f<__nv_fp8_e4m3>(__nv_fp8_e4m3 v) { return static_cast<float>(v); }
+template <> VAE_DEV __nv_fp8_e4m3 from_f<__nv_fp8_e4m3>(float v) {
+  __nv_fp8_e4m3 r;
+  r.__x = __nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+  return r;
+}
+
+// Store 8 values in the operand type; an e4m3 store that had to saturate records a range fault.
+VAE_DEV void vstore8(__nv_bfloat16* p, const float* v, uint32_t*) { store8(p, v); }
+VAE_DEV void vstore8(float* p, const float* v, uint32_t*) { store8(p, v); }
+VAE_DEV void vstore8(__nv_fp8_e4m3* p, const float* v, uint32_t* fault) {
+  if (!store8_e4m3(p, v)) raise_fault(fault, FAULT_RANGE, 22);
 }
 
 VAE_DEV float silu_f(float x) { return x / (1.0f + __expf(-x)); }
@@ -144,25 +175,6 @@ VAE_DEV void tma_load_5d(void* smem_dst, const void* tmap, uint64_t* bar, int c0
       : "memory");
 }
 
-// TMA loads multicast to every CTA of the cluster in cta_mask: the box lands at the same shared-memory
-// offset in each of them and completes bytes on the mbarrier at the same offset in each.
-VAE_DEV void tma_load_2d_mc(void* smem_dst, const void* tmap, uint64_t* bar, int c0, int c1, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(cta_mask)
-      : "memory");
-}
-
-VAE_DEV void tma_load_3d_mc(void* smem_dst, const void* tmap, uint64_t* bar, int c0, int c1, int c2,
-                            uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "h"(cta_mask)
-      : "memory");
-}
-
 // ---- CTA pairs (a cluster of 2 whose tensor cores run one MMA together, tcgen05 cta_group::2)
 // Address of the same shared-memory variable in CTA `rank` of this cluster (shared::cluster window).
 VAE_DEV uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
@@ -181,6 +193,13 @@ VAE_DEV void tma_load_2d_pair(void* smem_dst, const void* tmap, uint32_t bar_clu
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar_cluster)
+      : "memory");
+}
+VAE_DEV void tma_load_3d_pair(void* smem_dst, const void* tmap, uint32_t bar_cluster, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster)
       : "memory");
 }
 VAE_DEV void tma_load_5d_pair(void* smem_dst, const void* tmap, uint32_t bar_cluster, int c0, int c1, int c2,
@@ -227,20 +246,21 @@ VAE_DEV void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint
       : "memory");
 }
 
+// Same with e4m3 A and B (kind::f8f6f4: 32 K elements = 32 bytes per instruction, fp32 accumulation).
+VAE_DEV void tc_mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on an mbarrier once all previously issued tcgen05 ops of this thread have completed.
 VAE_DEV void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
-}
-
-// Same, arriving on the mbarrier at this offset in every CTA of the cluster in cta_mask.
-VAE_DEV void tc_commit_mc(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
 }
 
 // Pair forms (cta_group::2): one warp of EACH CTA of the pair runs the alloc / dealloc together; the
@@ -264,7 +284,19 @@ VAE_DEV void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-VAE_DEV void tc_commit_pair_mc(uint64_t* bar, uint16_t cta_mask) {
+// Completion signal of the pair's MMAs: one arrival on the mbarrier at this offset in each CTA named
+// by cta_mask (the pair's two CTAs).  It moves no data: every operand load in this library is a
+// plain TMA load into the issuing CTA's own shared memory.
+VAE_DEV void tc_mma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+VAE_DEV void tc_commit_pair_arrive_both(uint64_t* bar, uint16_t cta_mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
           smem_u32(bar)),
@@ -313,6 +345,13 @@ VAE_DEV uint64_t sdesc_kmajor_sw128_rows(uint32_t saddr, uint32_t sbo_bytes) {
   d |= static_cast<uint64_t>(1u) << 46;
   d |= static_cast<uint64_t>(2u) << 61;
   return d;
+}
+
+// Instruction descriptor, kind::f8f6f4: e4m3 A and B (format code 0, K-major), fp32 D, M x N.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t m, uint32_t n) {
+  return (1u << 4)                 // D format: f32
+         | ((n >> 3) << 17)        // N / 8
+         | ((m >> 4) << 24);       // M / 16
 }
 
 // Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 D, M x N.

@@ -104,8 +104,7 @@ __global__ void __launch_bounds__(128) conv_simt_kernel(const __grid_constant__ 
 }
 
 cudaError_t launch_conv_simt(const ConvSimtArgs& a, cudaStream_t s) {
-  static SimtParams p;
-  p = SimtParams{};
+  SimtParams p{};  // per call (launches from several host threads never share it)
   p.B = a.B; p.T = a.T; p.H = a.H; p.W = a.W; p.C_in = a.C_in; p.C_out = a.C_out;
   p.T_in = a.T_in; p.cache_frames = a.cache_frames;
   p.x_T_alloc = a.x_T_alloc ? a.x_T_alloc : a.T_in;

@@ -22,9 +22,11 @@
 // warps 2-5 drain TMEM with tcgen05.ld and run the epilogue (bias, residual, depth-to-space scatter,
 // bf16/fp32 store, optional fused group-norm partial sums).  Every mbarrier wait is bounded.
 //
-// Launch forms: CTAs run in clusters of 2.  For weight tiles 128 or 256 wide the pair's two M tiles
-// run as one cta_group::2 MMA (each CTA holds half of the weight tile; two 64-channel k blocks per
-// stage where they fit); narrower weight tiles are shared by multicasting each half to both CTAs.
+// Launch forms: for weight tiles 128 or 256 wide (convs and unbatched GEMMs) CTAs run in clusters
+// of 2 and the pair's two M tiles run as one cta_group::2 MMA (each CTA loads its own A tiles and
+// half of the weight tile into its own shared memory; two 64-channel k blocks per stage where they
+// fit).  Other weight widths and batched GEMMs run one CTA per tile, each loading its whole weight
+// tile.  Every operand load is a plain TMA load into the issuing CTA's shared memory.
 // Convs at most 32 channels wide (a pixel head) use halo mode: one (rows_t + 2) x (cols_t + 2) box
 // per (kt, channel chunk) feeds all 9 spatial taps through row-offset operand descriptors.  The
 // producer and the MMA issuer advance ring slot, phase and tap with counters (no divisions on
@@ -69,11 +71,14 @@ struct TcParams {
   int T_out, H_out, W_out;
   void* gn_partials;
   int gn_groups, gn_cpg;
-  void* y2;          // optional bf16 copy of y (channels-last), y2_T_alloc frames per batch item
-  int y2_T_alloc;
+  void* y2;          // optional copy of y (channels-last), y2_T_alloc frames per batch item: bf16, or e4m3
+  int y2_T_alloc, y2_fp8;
+  int fp8;           // e4m3 operands (kind::f8f6f4); kc = channels per 128-byte k block (64 bf16, 128 e4m3)
+  int kc;
+  const float* wscale;  // fp8: per-output-channel weight scale (packed row order)
   int n_tiles;
-  int pair;          // 1: CTAs run in clusters of 2 on adjacent M tiles of one N tile, each loading half of
-                     // the weight tile and multicasting it to both
+  int pair;          // 1: CTAs run in clusters of 2 on adjacent M tiles of one N tile as one cta_group::2
+                     // MMA, each loading half of the weight tile into its own shared memory
   int n_mtiles, seq_count;
   int npc;           // N tiles per work chunk (divides n_ntiles)
   uint32_t* fault;
@@ -246,6 +251,10 @@ VAE_DEV void epilogue_chunk(const TcParams& p, const TileCoord& tc, int m, int n
   if (vec) {
     const int sub = nb / p.C_d2s;
     const int c = nb - sub * p.C_d2s;
+    if (p.wscale) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] *= p.wscale[nb + i];
+    }
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] += p.bias ? p.bias[(c + i) * p.S + sub] : 0.f;
     const int dt = sub / (sh * sw);
@@ -280,13 +289,21 @@ VAE_DEV void epilogue_chunk(const TcParams& p, const TileCoord& tc, int m, int n
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = bf2f(f2bf(v[i]));  // statistics see the stored values
       }
-      if (p.y2) {  // bf16 copy for the next conv's operand
+      if (p.y2) {  // copy in the next conv's operand type (bf16 or e4m3)
         const int64_t o2 =
             (((static_cast<int64_t>(tc.b) * p.y2_T_alloc + to) * p.H_out + (h * sh + dy)) * p.W_out + (w * sw + dx)) *
                 p.C_d2s + c;
-        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.y2) + o2;
+        if (p.y2_fp8) {
+          __nv_fp8_e4m3* o = static_cast<__nv_fp8_e4m3*>(p.y2) + o2;
+          bool ok = true;
 #pragma unroll
-        for (int i = 0; i < 32; i += 8) store8(o + i, v + i);
+          for (int i = 0; i < 32; i += 8) ok = store8_e4m3(o + i, v + i) && ok;
+          if (!ok) raise_fault(p.fault, FAULT_RANGE, 21);
+        } else {
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.y2) + o2;
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) store8(o + i, v + i);
+        }
       }
     }
     if (p.gn_partials) {
@@ -306,7 +323,7 @@ VAE_DEV void epilogue_chunk(const TcParams& p, const TileCoord& tc, int m, int n
       if (n >= p.N_real) continue;
       const int sub = n / p.C_d2s;
       const int c = n - sub * p.C_d2s;
-      float val = v[i] + (p.bias ? p.bias[c * p.S + sub] : 0.f);
+      float val = v[i] * (p.wscale ? p.wscale[n] : 1.f) + (p.bias ? p.bias[c * p.S + sub] : 0.f);
       const int dt = sub / (sh * sw);
       const int rem = sub - dt * sh * sw;
       const int dy = rem / sw, dx = rem - (rem / sw) * sw;
@@ -367,8 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full_bar[s], 1);
-      // multicast-B pairs: both CTAs' MMAs free a stage; MMA pairs: the leader's commit alone
-      mbar_init(&empty_bar[s], (p.pair && !kPair) ? 2 : 1);
+      mbar_init(&empty_bar[s], 1);  // MMA pairs: the leader's commit frees the stage in both CTAs
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&accf_bar[a], 1);
@@ -437,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int seq = seq0; seq < p.seq_count && ok; seq += seq_step) {
         const TileCoord tc = seq_coord(p, seq, rank);
-        int cc = 0, kt = 0, kh = 0, kw = 0, kcol = 0;  // kcol = tap * C_in_pad + cc * 64
+        int cc = 0, kt = 0, kh = 0, kw = 0, kcol = 0;  // kcol = tap * C_in_pad + cc * kc
         int kb = 0;                                    // k block (GEMM mode)
         for (int st = 0; st < num_st; ++st, ++kc) {
           if (kc >= stages && !mbar_wait(&empty_bar[s], ph ^ 1u, p.fault, p.limit_ns, 1)) {
@@ -462,18 +478,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint8_t* aj = a_dst + j * a_bytes;
               uint8_t* bj = b_dst + j * b_bytes;
               if constexpr (kPair) {
-                tma_load_5d_pair(aj, &tmA, fb, cc * kBlockK, tc.w0 + kw - 1, tc.h0 + kh - 1, ti, tc.b);
+                tma_load_5d_pair(aj, &tmA, fb, cc * p.kc, tc.w0 + kw - 1, tc.h0 + kh - 1, ti, tc.b);
                 tma_load_2d_pair(bj, &tmB, fb, kcol, tc.n0 + rank * (p.BN / 2));
               } else {
-                tma_load_5d(aj, &tmA, &full_bar[s], cc * kBlockK, tc.w0 + kw - 1, tc.h0 + kh - 1, ti, tc.b);
-                if (p.pair)
-                  tma_load_2d_mc(bj + rank * (b_bytes / 2), &tmB, &full_bar[s], kcol, tc.n0 + rank * (p.BN / 2),
-                                 pair_mask);
-                else
-                  tma_load_2d(bj, &tmB, &full_bar[s], kcol, tc.n0);
+                tma_load_5d(aj, &tmA, &full_bar[s], cc * p.kc, tc.w0 + kw - 1, tc.h0 + kh - 1, ti, tc.b);
+                tma_load_2d(bj, &tmB, &full_bar[s], kcol, tc.n0);
               }
               // next (tap, channel chunk): channel chunks innermost, then kw, kh, kt
-              kcol += kBlockK;
+              kcol += p.kc;
               if (++cc == cchunks) {
                 cc = 0;
                 if (++kw == 3) {
@@ -486,15 +498,28 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           } else {
-            // GEMM mode: one k block per stage
-            mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
-            tma_load_3d(a_dst, &tmA, &full_bar[s], kb * kBlockK, tc.m0, tc.bat);
-            if (p.pair)
-              tma_load_3d_mc(b_dst + rank * (b_bytes / 2), &tmB, &full_bar[s], kb * kBlockK,
-                             tc.n0 + rank * (p.BN / 2), tc.bat, pair_mask);
-            else
-              tma_load_3d(b_dst, &tmB, &full_bar[s], kb * kBlockK, tc.n0, tc.bat);
-            ++kb;
+            // GEMM mode: ks consecutive k blocks per stage
+            uint32_t fb = 0;
+            if constexpr (kPair) {
+              fb = cluster_map(smem_u32(&full_bar[s]), 0);
+              if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * stage_bytes);
+            } else {
+              mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              if (j == ks) break;
+              uint8_t* aj = a_dst + j * a_bytes;
+              uint8_t* bj = b_dst + j * b_bytes;
+              if constexpr (kPair) {
+                tma_load_3d_pair(aj, &tmA, fb, kb * kBlockK, tc.m0, tc.bat);
+                tma_load_3d_pair(bj, &tmB, fb, kb * kBlockK, tc.n0 + rank * (p.BN / 2), tc.bat);
+              } else {
+                tma_load_3d(aj, &tmA, &full_bar[s], kb * kBlockK, tc.m0, tc.bat);
+                tma_load_3d(bj, &tmB, &full_bar[s], kb * kBlockK, tc.n0, tc.bat);
+              }
+              ++kb;
+            }
           }
           if (++s == stages) {
             s = 0;
@@ -507,8 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!kPair || rank == 0)
         for (int k = max(0, kc - p.stages); k < kc; ++k)
           mbar_wait(&full_bar[k % p.stages], (k / p.stages) & 1, p.fault, p.limit_ns, 2);
-      // pair: both MMAs have released every stage, so no multicast commit is still on its way here
-      if (p.pair)
+      // MMA pair: the leader's MMAs have released every stage, so no commit arrival is still on its way
+      if (kPair)
         for (int k = max(0, kc - p.stages); k < kc; ++k)
           mbar_wait(&empty_bar[k % p.stages], (k / p.stages) & 1, p.fault, p.limit_ns, 7);
     }
@@ -569,7 +594,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (lane == 0 && (!kPair || rank == 0) && !halo) {
-      const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * kBlockM : kBlockM, static_cast<uint32_t>(p.BN));
+      const uint32_t mm = kPair ? 2 * kBlockM : kBlockM;
+      const bool fp8 = p.fp8 != 0;
+      const uint32_t idesc = fp8 ? idesc_e4m3_f32(mm, static_cast<uint32_t>(p.BN)) : idesc_bf16_f32(mm, static_cast<uint32_t>(p.BN));
       const int stages = p.stages, num_st = p.num_kb / ks, msub = p.msub;
       const uint32_t smem_base = smem_u32(smem);
       const uint32_t sub_cols = static_cast<uint32_t>(p.BN);
@@ -601,27 +628,28 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t d_sub = d_tmem + static_cast<uint32_t>(sub) * sub_cols;
               const uint32_t first = (st == 0 && j == 0) ? 1u : 0u;
 #pragma unroll
-              for (int k = 0; k < kBlockK / 16; ++k) {
-                // advance 16 bf16 (32 B) along K inside the 128-byte swizzle atom
+              for (int k = 0; k < 4; ++k) {
+                // advance 32 B along K inside the 128-byte swizzle atom: 16 bf16 or 32 e4m3 per MMA
                 const uint32_t accum = (first && k == 0) ? 0u : 1u;
-                if constexpr (kPair)
-                  tc_mma_bf16_pair(d_sub, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k),
-                                   idesc, accum);
-                else
-                  tc_mma_bf16(d_sub, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k),
-                              idesc, accum);
+                const uint64_t ak = adesc + static_cast<uint64_t>(2 * k), bk = bdesc + static_cast<uint64_t>(2 * k);
+                if constexpr (kPair) {
+                  if (fp8) tc_mma_e4m3_pair(d_sub, ak, bk, idesc, accum);
+                  else tc_mma_bf16_pair(d_sub, ak, bk, idesc, accum);
+                } else {
+                  if (fp8) tc_mma_e4m3(d_sub, ak, bk, idesc, accum);
+                  else tc_mma_bf16(d_sub, ak, bk, idesc, accum);
+                }
               }
             }
           }
-          if constexpr (kPair) tc_commit_pair_mc(&empty_bar[s], pair_mask);
-          else if (p.pair) tc_commit_mc(&empty_bar[s], pair_mask);
+          if constexpr (kPair) tc_commit_pair_arrive_both(&empty_bar[s], pair_mask);
           else tc_commit(&empty_bar[s]);
           if (++s == stages) {
             s = 0;
             ph ^= 1u;
           }
         }
-        if constexpr (kPair) tc_commit_pair_mc(&accf_bar[acc], pair_mask);
+        if constexpr (kPair) tc_commit_pair_arrive_both(&accf_bar[acc], pair_mask);
         else tc_commit(&accf_bar[acc]);
       }
     }
@@ -696,7 +724,7 @@ EncodeTiledFn encode_fn() {
 }
 
 bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-              const uint32_t* box) {
+              const uint32_t* box, bool bytes = false) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t d[5], s[4];
@@ -707,7 +735,8 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, 
     es[i] = 1;
     if (i + 1 < rank) s[i] = strides_bytes[i];
   }
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, s, bx, es,
+  CUresult r = fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+                  const_cast<void*>(base), d, s, bx, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -734,10 +763,9 @@ int pick_cols(const int* pw, int npw) {
 }  // namespace
 
 namespace {
-// Pairing halves the weight-tile traffic from L2; measured A/B on one GB300: +2..6% conv throughput.
-bool pair_mode_enabled() { return true; }
-// Convs whose weight tile is 128 or 256 channels wide run each pair's two M tiles as one cta_group::2
-// MMA, each CTA holding half of the weight tile.
+// Convs and unbatched GEMMs whose weight tile is 128 or 256 channels wide run each pair's two M tiles
+// as one cta_group::2 MMA, each CTA holding half of the weight tile (measured on one GB300: op conv
+// 512->512 1311 -> 1386 TFLOP/s).
 bool mma_pair_enabled() { return true; }
 // Convs at most 32 channels wide (the Wan-shaped pixel head) load one halo box per (kt, channel chunk)
 // that the 9 spatial taps share, instead of 9 tap-shifted boxes (measured: 256->12 head on
@@ -747,9 +775,20 @@ constexpr int kHaloCols = 8;   // tile width: one 8-row MMA core group per outpu
 constexpr int kHaloRows = 32;  // tile height: two 16-row sub-tiles of 128 pixels
 }  // namespace
 
+namespace {
+// Per-device launch facts, filled once per device under a lock (several host threads may launch).
+struct DevLaunch {
+  bool ready = false;
+  int n_sm = 0;
+  int max_clusters = 0;          // clusters of 2 resident at once for the pair kernel ...
+  size_t max_clusters_smem = 0;  // ... at this dynamic shared-memory size
+};
+std::mutex g_dev_mu;
+DevLaunch g_dev[64];
+}  // namespace
+
 cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
-  static TcParams p;  // large: built on the host then copied into the launch
-  p = TcParams{};
+  TcParams p{};  // per call: concurrent launches from several host threads never share it
   p.mode = a.mode;
   p.N_real = a.N_real;
   if (a.N_pad <= 256) {
@@ -760,18 +799,25 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   if (p.BN % 16 != 0 || p.BN < 16) return cudaErrorInvalidValue;
   p.n_ntiles = (a.N_pad + p.BN - 1) / p.BN;
   p.msub = p.BN <= 128 ? 2 : 1;
-  // clusters of 2 share each weight tile (half loaded by each CTA, multicast to both)
-  // (a batched GEMM has a different B per batch item, so only unbatched GEMMs pair up)
-  p.halo = (a.mode == 0 && p.BN <= 32 && halo_mode_enabled()) ? 1 : 0;
-  const bool want_pair = pair_mode_enabled() && p.BN % 16 == 0 && (a.mode == 0 || a.batch == 1) && !p.halo;
-  const bool mma_pair = want_pair && a.mode == 0 && (p.BN == 256 || p.BN == 128) && mma_pair_enabled();
+  // clusters of 2 run one cta_group::2 MMA over two adjacent M tiles of one weight tile (a batched GEMM
+  // has a different B per batch item, so only unbatched GEMMs pair up)
+  p.fp8 = a.fp8 ? 1 : 0;
+  p.kc = p.fp8 ? 128 : 64;
+  if (p.fp8 && (a.mode != 0 || !a.wscale || a.C_in_pad % 128 != 0)) return cudaErrorInvalidValue;
+  p.wscale = p.fp8 ? a.wscale : nullptr;
+  p.halo = (a.mode == 0 && p.BN <= 32 && !p.fp8 && halo_mode_enabled()) ? 1 : 0;
+  const bool mma_pair =
+      mma_pair_enabled() && (p.BN == 256 || p.BN == 128) && (a.mode == 0 || a.batch == 1) && !p.halo;
+  const bool want_pair = mma_pair;
   p.tmem_cols = 32;
   while (p.tmem_cols < 2 * p.msub * p.BN) p.tmem_cols <<= 1;  // two accumulators
   if (p.tmem_cols > 512) return cudaErrorInvalidValue;
   const uint32_t kb_bytes = kABytes * p.msub + static_cast<uint32_t>(mma_pair ? p.BN / 2 : p.BN) * kBlockK * 2;
   // MMA pairs take two k blocks per stage (half the barrier round trips per MMA) where two such stages
   // fit; measured on one GB300: +11% on a 512->512 conv (3 stages), +12% on 128->128 (2 stages)
-  p.ks = (mma_pair && (a.C_in_pad / kBlockK) % 2 == 0 && 2u * 2u * kb_bytes <= 200u * 1024u) ? 2 : 1;
+  // (a conv's 27 taps x cchunks k blocks split evenly into pairs when cchunks is even)
+  const int kb_even = a.mode == 0 ? (a.C_in_pad / p.kc) % 2 == 0 : (a.K / kBlockK) % 2 == 0;
+  p.ks = (mma_pair && kb_even && 2u * 2u * kb_bytes <= 200u * 1024u) ? 2 : 1;
   uint32_t stage_bytes = static_cast<uint32_t>(p.ks) * kb_bytes;
   if (p.halo) {
     // box of (32 + 2) x (8 + 2) pixels x 64 channels, then the 9 taps' BN x 64 weight tiles
@@ -798,7 +844,7 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   if (a.mode == 0) {
     p.B = a.B; p.T = a.T; p.H = a.H; p.W = a.W; p.T_in = a.T_in; p.cache_frames = a.cache_frames;
     p.C_in_pad = a.C_in_pad;
-    if (a.C_in_pad % 64 != 0 || a.nph > kMaxP || a.npw > kMaxP) return cudaErrorInvalidValue;
+    if (a.C_in_pad % p.kc != 0 || a.nph > kMaxP || a.npw > kMaxP) return cudaErrorInvalidValue;
     p.nph = a.nph; p.npw = a.npw;
     for (int i = 0; i <= a.nph; ++i) p.ph_edges[i] = a.ph_edges[i];
     for (int j = 0; j <= a.npw; ++j) p.pw_edges[j] = a.pw_edges[j];
@@ -812,7 +858,7 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
       p.tcol_prefix[j + 1] = p.tcol_prefix[j] + (a.pw_edges[j + 1] - a.pw_edges[j] + p.cols_t - 1) / p.cols_t;
     p.n_trows = p.trow_prefix[a.nph];
     p.n_tcols = p.tcol_prefix[a.npw];
-    p.cchunks = a.C_in_pad / kBlockK;
+    p.cchunks = a.C_in_pad / p.kc;
     p.num_kb = 27 * p.cchunks;
     p.d2s_t = a.d2s_t; p.d2s_h = a.d2s_h; p.d2s_w = a.d2s_w;
     p.S = a.d2s_t * a.d2s_h * a.d2s_w;
@@ -830,20 +876,21 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
     if (a.gn_partials && (p.C_d2s % 32 != 0 || a.out_ncthw || (p.gn_cpg < 32 ? 32 % p.gn_cpg : p.gn_cpg % 32) != 0))
       return cudaErrorInvalidValue;
     const uint64_t C = a.C_in_pad;
+    const uint64_t eb = p.fp8 ? 1 : 2;  // bytes per operand element
     const uint64_t xTa = a.x_T_alloc ? a.x_T_alloc : a.T_in;
     uint64_t dims[5] = {C, (uint64_t)a.W, (uint64_t)a.H, (uint64_t)a.T_in, (uint64_t)a.B};
-    uint64_t strides[4] = {C * 2, C * 2 * a.W, C * 2 * a.W * a.H, C * 2 * a.W * a.H * xTa};
-    uint32_t box[5] = {64u, (uint32_t)p.cols_t, (uint32_t)p.rows_t, 1u, 1u};
+    uint64_t strides[4] = {C * eb, C * eb * a.W, C * eb * a.W * a.H, C * eb * a.W * a.H * xTa};
+    uint32_t box[5] = {(uint32_t)p.kc, (uint32_t)p.cols_t, (uint32_t)p.rows_t, 1u, 1u};
     if (p.halo) {
       box[1] = static_cast<uint32_t>(p.cols_t + 2);
       box[2] = static_cast<uint32_t>(p.rows_t + 2);
     }
-    if (!make_map(&tmA, a.x, 5, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_map(&tmA, a.x, 5, dims, strides, box, p.fp8)) return cudaErrorInvalidValue;
     const uint64_t K = 27ull * C;
     uint64_t wd[2] = {K, (uint64_t)a.N_pad};
-    uint64_t ws[1] = {K * 2};
-    uint32_t wb[2] = {64u, (uint32_t)(want_pair ? p.BN / 2 : p.BN)};
-    if (!make_map(&tmB, a.w, 2, wd, ws, wb)) return cudaErrorInvalidValue;
+    uint64_t ws[1] = {K * eb};
+    uint32_t wb[2] = {(uint32_t)p.kc, (uint32_t)(want_pair ? p.BN / 2 : p.BN)};
+    if (!make_map(&tmB, a.w, 2, wd, ws, wb, p.fp8)) return cudaErrorInvalidValue;
     n_blocks = static_cast<long long>(a.B) * a.T * p.n_trows * p.n_tcols * p.n_ntiles;
   } else {
     p.M = a.M; p.K = a.K; p.batch = a.batch; p.stride_d = a.stride_d; p.alpha = a.alpha;
@@ -871,30 +918,36 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   p.n_tiles = static_cast<int>(n_blocks);
   p.y2 = a.y2;
   p.y2_T_alloc = a.y2_T_alloc ? a.y2_T_alloc : p.T_out;
+  p.y2_fp8 = a.y2_fp8;
   if (a.y2 && (p.out_ncthw || p.C_d2s % 32 != 0)) return cudaErrorInvalidValue;
-  static int n_sm = 0;
-  if (!n_sm) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-    if (n_sm <= 0) n_sm = 148;
+  int dev = 0;
+  {
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   }
   const size_t smem = 1024 + static_cast<size_t>(p.stages) * stage_bytes + (2 * p.stages + 4) * 8 + 16;
-  static int attr_set = 0;
-  if (!attr_set) {
-    for (auto* k : {conv_tc_kernel<false>, conv_tc_kernel<true>}) {
-      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-      if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-      (void)e;
+  int n_sm = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DevLaunch& dl = g_dev[dev];
+    if (!dl.ready) {
+      if (cudaDeviceGetAttribute(&dl.n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || dl.n_sm <= 0)
+        dl.n_sm = 148;
+      for (auto* k : {conv_tc_kernel<false>, conv_tc_kernel<true>}) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess) return e;
+      }
+      dl.ready = true;
     }
-    attr_set = 1;
+    n_sm = dl.n_sm;
   }
   p.n_mtiles = static_cast<int>(n_blocks / p.n_ntiles);
   p.pair = want_pair ? 1 : 0;
   {
     // N tiles per chunk: as many as keep the chunk's weights within ~48 MB of L2
-    const double w_tile = static_cast<double>(p.BN) * (a.mode == 0 ? 27.0 * a.C_in_pad : static_cast<double>(a.K)) * 2.0;
+    const double w_tile =
+        static_cast<double>(p.BN) * (a.mode == 0 ? 27.0 * a.C_in_pad : static_cast<double>(a.K)) * (p.fp8 ? 1.0 : 2.0);
     int npc = p.n_ntiles;
     if (a.mode == 0) {
       npc = 1;
@@ -910,10 +963,7 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
     return cudaGetLastError();
   }
   p.seq_count = (p.n_mtiles + 1) / 2 * p.n_ntiles;
-  auto* kern = mma_pair ? conv_tc_kernel<true> : conv_tc_kernel<false>;
-  static int max_clusters[2] = {0, 0};
-  static size_t max_clusters_smem[2] = {0, 0};
-  const int ki = mma_pair ? 1 : 0;
+  auto* kern = conv_tc_kernel<true>;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -925,14 +975,20 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (max_clusters[ki] <= 0 || max_clusters_smem[ki] != smem) {
-    cfg.gridDim = dim3(2 * (n_sm / 2));
-    int mc = 0;
-    if (cudaOccupancyMaxActiveClusters(&mc, kern, &cfg) != cudaSuccess || mc <= 0) mc = n_sm / 2;
-    max_clusters[ki] = mc;
-    max_clusters_smem[ki] = smem;
+  int max_clusters = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DevLaunch& dl = g_dev[dev];
+    if (dl.max_clusters <= 0 || dl.max_clusters_smem != smem) {
+      cfg.gridDim = dim3(2 * (n_sm / 2));
+      int mc = 0;
+      if (cudaOccupancyMaxActiveClusters(&mc, kern, &cfg) != cudaSuccess || mc <= 0) mc = n_sm / 2;
+      dl.max_clusters = mc;
+      dl.max_clusters_smem = smem;
+    }
+    max_clusters = dl.max_clusters;
   }
-  const long long clusters = std::min<long long>(p.seq_count, max_clusters[ki]);
+  const long long clusters = std::min<long long>(p.seq_count, max_clusters);
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
   if (e != cudaSuccess) return e;

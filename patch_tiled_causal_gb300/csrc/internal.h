@@ -42,8 +42,11 @@ struct ConvTcArgs {
   int d2s_t, d2s_h, d2s_w, drop_first;
   // fused group-norm statistics of y (nullptr = none): exact per-patch sums, see norm.cu
   void* gn_partials; int gn_groups;
-  // optional second, bf16 copy of y (channels-last, y2_T_alloc frames per batch item)
-  void* y2; int y2_T_alloc;
+  // optional second copy of y (channels-last, y2_T_alloc frames per batch item): bf16, or e4m3 with y2_fp8
+  void* y2; int y2_T_alloc; int y2_fp8;
+  // conv mode, e4m3 operands: x and w hold e4m3 bytes (C_in_pad a multiple of 128) and the product of
+  // output channel n (packed row order) is multiplied by wscale[n] (its weights' scale)
+  int fp8; const float* wscale;
 };
 cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t s);
 
@@ -65,6 +68,11 @@ cudaError_t launch_pack_weights_bf16(const float* w, int C_out, int C_in, int C_
                                      void* out, cudaStream_t s);
 cudaError_t launch_pack_weights_f32(const float* w, int C_out, int C_in, void* out, cudaStream_t s);
 cudaError_t launch_pack_matrix_bf16(const float* w, int rows, int cols, void* out, cudaStream_t s);
+// e4m3 K-major [N_pad, 27 * C_in_pad] (rows as the bf16 packing), each row scaled by its own
+// scale = max|w| / 448, followed at fp8_scale_offset() bytes by the float scales [N_pad].
+size_t fp8_scale_offset(int N_pad, int C_in_pad);
+cudaError_t launch_pack_weights_fp8(const float* w, int C_out, int C_in, int C_in_pad, int N_pad, int S, void* out,
+                                    cudaStream_t s);
 
 // Group norm.
 struct GnArgs {
@@ -74,6 +82,7 @@ struct GnArgs {
   int nph, npw; const int* ph_edges; const int* pw_edges;
   const void* x; int x_f32; int x_T_alloc;  // frames per batch item in memory (0 = T)
   void* y; int y_f32; int y_T_alloc;
+  int y_fp8;               // y holds e4m3 conv operands (round to nearest, |y| > 448 flags VAE_ERR_RANGE)
   const float* gamma; const float* beta;
   void* partials;          // gn_workspace_bytes: [nph*npw, B, T, groups] GnPartial, then [B*T, C] float2
 };
@@ -105,8 +114,8 @@ cudaError_t launch_blend(const void* const* tiles, const vae_tile_t* meta, int n
 cudaError_t launch_gemm_simt(const float* A, const float* Bm, float* D, const float* bias, const float* residual,
                              int M, int N, int K, int batch, int64_t sa, int64_t sb, int64_t sd, int64_t ldb_n,
                              int64_t ldb_k, float alpha, cudaStream_t s);
-// Cast / copy a channels-last tensor between frame layouts and dtypes.
-cudaError_t launch_cast_frames(const void* x, int x_f32, int x_T_alloc, void* y, int y_f32, int y_T_alloc, int B, int T,
+// Cast / copy a channels-last tensor between frame layouts and dtypes (y_kind: 0 bf16, 1 fp32, 2 e4m3).
+cudaError_t launch_cast_frames(const void* x, int x_f32, int x_T_alloc, void* y, int y_kind, int y_T_alloc, int B, int T,
                                int64_t frame_elems, cudaStream_t s);
 
 // Softmax over rows of an fp32 matrix, written as bf16 (attention probabilities).

@@ -64,6 +64,7 @@ extern "C" vae_status_t vae_patch_groupnorm_silu_noalloc(const void* x, const fl
   g.B = d->B; g.T = d->T; g.H = d->H; g.W = d->W; g.C = d->C; g.groups = d->groups; g.eps = d->eps; g.silu = d->silu;
   g.nph = d->n_patch_h; g.npw = d->n_patch_w; g.ph_edges = d->patch_h_edges; g.pw_edges = d->patch_w_edges;
   g.x = x; g.x_f32 = d->in_dtype == VAE_FP32; g.y = y; g.y_f32 = d->out_dtype == VAE_FP32;
+  g.y_fp8 = d->out_dtype == VAE_FP8;
   g.gamma = gamma; g.beta = beta; g.partials = scratch;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // launch_gn_stats clears the partial sums (they must start at zero) before it adds into them; the

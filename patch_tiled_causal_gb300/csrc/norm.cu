@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(256, sizeof(TI) == 2 ? 3 : 4) gn_apply_kernel(
         const float z = fmaf(a[e], m[e].x, m[e].y);
         a[e] = p.silu ? __fdividef(z, 1.0f + __expf(-z)) : z;
       }
-      store8(yf + static_cast<int64_t>(v) * 8, a);
+      vstore8(yf + static_cast<int64_t>(v) * 8, a, p.fault);
     }
     return;
   }
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(256, sizeof(TI) == 2 ? 3 : 4) gn_apply_kernel(
       const float z = fmaf(a[e], m.x, m.y);
       a[e] = p.silu ? __fdividef(z, 1.0f + __expf(-z)) : z;
     }
-    store8(yf + static_cast<int64_t>(v) * 8, a);
+    vstore8(yf + static_cast<int64_t>(v) * 8, a, p.fault);
   }
 }
 
@@ -359,7 +359,7 @@ bool fill_gn(GnParams& p, const GnArgs& a) {
 }  // namespace
 
 cudaError_t launch_gn_stats(const GnArgs& a, cudaStream_t s) {
-  static GnParams p;
+  GnParams p;  // per call (several host threads may launch)
   if (!fill_gn(p, a)) return cudaErrorInvalidValue;
   cudaError_t e = cudaMemsetAsync(a.partials, 0, gn_partials_bytes(a.nph, a.npw, a.B, a.T, a.groups), s);
   if (e != cudaSuccess) return e;
@@ -388,7 +388,7 @@ cudaError_t launch_gn_stats(const GnArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_gn_apply(const GnArgs& a, cudaStream_t s) {
-  static GnParams p;
+  GnParams p;  // per call (several host threads may launch)
   if (!fill_gn(p, a)) return cudaErrorInvalidValue;
   const long long frames = static_cast<long long>(a.B) * a.T;
   if (frames == 0) return cudaSuccess;
@@ -398,7 +398,9 @@ cudaError_t launch_gn_apply(const GnArgs& a, cudaStream_t s) {
   const int64_t per_block = 256LL * (a.x_f32 ? ApplyVec<float>::kVecs : ApplyVec<__nv_bfloat16>::kVecs);
   dim3 grid(static_cast<unsigned>((nvec + per_block - 1) / per_block), static_cast<unsigned>(frames));
   const size_t sm = static_cast<size_t>(a.C) * sizeof(float2);
-  if (a.x_f32 && a.y_f32) gn_apply_kernel<float, float><<<grid, 256, sm, s>>>(p);
+  if (a.y_fp8 && a.x_f32) gn_apply_kernel<float, __nv_fp8_e4m3><<<grid, 256, sm, s>>>(p);
+  else if (a.y_fp8) gn_apply_kernel<__nv_bfloat16, __nv_fp8_e4m3><<<grid, 256, sm, s>>>(p);
+  else if (a.x_f32 && a.y_f32) gn_apply_kernel<float, float><<<grid, 256, sm, s>>>(p);
   else if (a.x_f32) gn_apply_kernel<float, __nv_bfloat16><<<grid, 256, sm, s>>>(p);
   else if (a.y_f32) gn_apply_kernel<__nv_bfloat16, float><<<grid, 256, sm, s>>>(p);
   else gn_apply_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, sm, s>>>(p);
@@ -424,6 +426,7 @@ struct RmsParams {
   const float* gamma;
   const float* beta;
   int team, vpl;  // lanes per pixel, 8-channel vectors per lane
+  uint32_t* fault;
 };
 constexpr int kRmsMaxVpl = 4;
 constexpr int kRmsVecs = 4;  // 8-channel vectors a lane holds per step: kRmsVecs / VPL pixels per team
@@ -524,7 +527,7 @@ __global__ void __launch_bounds__(256) rms_apply_kernel(const __grid_constant__ 
           const float z = fmaf(v[e] * rr, gg[e], bb[e]);
           o[e] = p.silu ? __fdividef(z, 1.0f + __expf(-z)) : z;
         }
-        store8(yp[k] + c0, o);
+        vstore8(yp[k] + c0, o, p.fault);
       }
     }
   }
@@ -544,6 +547,7 @@ cudaError_t launch_rms(const GnArgs& a, cudaStream_t s) {
   p.x = a.x; p.x_T_alloc = a.x_T_alloc ? a.x_T_alloc : a.T;
   p.y = a.y; p.y_T_alloc = a.y_T_alloc ? a.y_T_alloc : a.T;
   p.gamma = a.gamma; p.beta = a.beta;
+  p.fault = fault_word();
   const int nv = a.C / 8;
   p.team = nv >= 32 ? 32 : nv;
   p.vpl = nv / p.team;
@@ -553,7 +557,9 @@ cudaError_t launch_rms(const GnArgs& a, cudaStream_t s) {
   const int64_t warps = (npx + per_warp - 1) / per_warp;
   const int blocks = static_cast<int>(std::min<int64_t>((warps + 7) / 8, 152LL * 8));
 #define VAE_RMS(VPL)                                                                                     \
-  if (a.x_f32 && a.y_f32) rms_apply_kernel<float, float, VPL><<<blocks, 256, 0, s>>>(p);                 \
+  if (a.y_fp8 && a.x_f32) rms_apply_kernel<float, __nv_fp8_e4m3, VPL><<<blocks, 256, 0, s>>>(p);         \
+  else if (a.y_fp8) rms_apply_kernel<__nv_bfloat16, __nv_fp8_e4m3, VPL><<<blocks, 256, 0, s>>>(p);      \
+  else if (a.x_f32 && a.y_f32) rms_apply_kernel<float, float, VPL><<<blocks, 256, 0, s>>>(p);            \
   else if (a.x_f32) rms_apply_kernel<float, __nv_bfloat16, VPL><<<blocks, 256, 0, s>>>(p);               \
   else if (a.y_f32) rms_apply_kernel<__nv_bfloat16, float, VPL><<<blocks, 256, 0, s>>>(p);               \
   else rms_apply_kernel<__nv_bfloat16, __nv_bfloat16, VPL><<<blocks, 256, 0, s>>>(p);
@@ -1179,8 +1185,12 @@ bool build_grid(const void* const* tiles, const vae_tile_t* meta, int n, const v
 
 cudaError_t launch_blend(const void* const* tiles, const vae_tile_t* meta, int n_tiles, void* out,
                          const vae_blend_desc_t& d, cudaStream_t s) {
-  static BlendParams p;
-  static BlendGridParams g;
+  // per call and per host thread (about 20 KB each, kept off the stack): concurrent launches never
+  // share them, and a launch copies its parameters before returning
+  thread_local BlendParams p;
+  thread_local BlendGridParams g;
+  p = BlendParams{};
+  g = BlendGridParams{};
   if (n_tiles > VAE_MAX_TILES) return cudaErrorInvalidValue;
   if (static_cast<long long>(d.B) * d.C > 65535) return cudaErrorInvalidValue;
   if (d.W <= 8 * kGridMaxVec && build_grid(tiles, meta, n_tiles, d, g) && g.n[2] <= kG2Cols) {
@@ -1311,27 +1321,37 @@ cudaError_t launch_gemm_simt(const float* A, const float* Bm, float* D, const fl
 }
 
 template <typename TI, typename TO>
-__global__ void cast_frames_kernel(const TI* x, int xTa, TO* y, int yTa, int T, int64_t fe, int64_t n) {
+__global__ void cast_frames_kernel(const TI* x, int xTa, TO* y, int yTa, int T, int64_t fe, int64_t n, uint32_t* fault) {
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t e = i % fe;
     const int64_t f = i / fe;
     const int64_t t = f % T, b = f / T;
-    y[(b * yTa + t) * fe + e] = from_f<TO>(to_f<TI>(x[(b * xTa + t) * fe + e]));
+    const float v = to_f<TI>(x[(b * xTa + t) * fe + e]);
+    if (sizeof(TO) == 1 && !(fabsf(v) <= 448.f)) raise_fault(fault, FAULT_RANGE, 23);
+    y[(b * yTa + t) * fe + e] = from_f<TO>(v);
   }
 }
 
-cudaError_t launch_cast_frames(const void* x, int x_f32, int x_T_alloc, void* y, int y_f32, int y_T_alloc, int B, int T,
+cudaError_t launch_cast_frames(const void* x, int x_f32, int x_T_alloc, void* y, int y_kind, int y_T_alloc, int B, int T,
                                int64_t frame_elems, cudaStream_t s) {
   const int64_t n = static_cast<int64_t>(B) * T * frame_elems;
   if (n <= 0) return cudaSuccess;
   const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 152 * 64));
   const float* xf = static_cast<const float*>(x);
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-  if (x_f32 && y_f32) cast_frames_kernel<<<blocks, 256, 0, s>>>(xf, x_T_alloc, static_cast<float*>(y), y_T_alloc, T, frame_elems, n);
-  else if (x_f32) cast_frames_kernel<<<blocks, 256, 0, s>>>(xf, x_T_alloc, static_cast<__nv_bfloat16*>(y), y_T_alloc, T, frame_elems, n);
-  else if (y_f32) cast_frames_kernel<<<blocks, 256, 0, s>>>(xb, x_T_alloc, static_cast<float*>(y), y_T_alloc, T, frame_elems, n);
-  else cast_frames_kernel<<<blocks, 256, 0, s>>>(xb, x_T_alloc, static_cast<__nv_bfloat16*>(y), y_T_alloc, T, frame_elems, n);
+  uint32_t* fault = fault_word();
+  const int y_f32 = y_kind == 1;
+  if (y_kind == 2) {
+    __nv_fp8_e4m3* y8 = static_cast<__nv_fp8_e4m3*>(y);
+    if (x_f32) cast_frames_kernel<<<blocks, 256, 0, s>>>(xf, x_T_alloc, y8, y_T_alloc, T, frame_elems, n, fault);
+    else cast_frames_kernel<<<blocks, 256, 0, s>>>(xb, x_T_alloc, y8, y_T_alloc, T, frame_elems, n, fault);
+    return cudaGetLastError();
+  }
+  if (x_f32 && y_f32) cast_frames_kernel<<<blocks, 256, 0, s>>>(xf, x_T_alloc, static_cast<float*>(y), y_T_alloc, T, frame_elems, n, fault);
+  else if (x_f32) cast_frames_kernel<<<blocks, 256, 0, s>>>(xf, x_T_alloc, static_cast<__nv_bfloat16*>(y), y_T_alloc, T, frame_elems, n, fault);
+  else if (y_f32) cast_frames_kernel<<<blocks, 256, 0, s>>>(xb, x_T_alloc, static_cast<float*>(y), y_T_alloc, T, frame_elems, n, fault);
+  else cast_frames_kernel<<<blocks, 256, 0, s>>>(xb, x_T_alloc, static_cast<__nv_bfloat16*>(y), y_T_alloc, T, frame_elems, n, fault);
   return cudaGetLastError();
 }
 
@@ -1387,6 +1407,48 @@ cudaError_t launch_pack_weights_bf16(const float* w, int C_out, int C_in, int C_
   const int64_t n = static_cast<int64_t>(N_pad) * 27 * C_in_pad;
   const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 152 * 64));
   pack_bf16_kernel<<<blocks, 256, 0, s>>>(w, C_out, C_in, C_in_pad, N_pad, S, static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+// e4m3 K-major [N_pad, 27 * C_in_pad] with the bf16 packing's row order; one block per packed row: the
+// row's scale is max|w| / 448 (1 for an all-zero or padding row), its bytes round w / scale to nearest
+// even.  The scales follow the bytes at fp8_scale_offset().
+size_t fp8_scale_offset(int N_pad, int C_in_pad) {
+  return (static_cast<size_t>(N_pad) * 27 * C_in_pad + 255) & ~size_t(255);
+}
+
+__global__ void __launch_bounds__(256) pack_fp8_kernel(const float* w, int C_out, int C_in, int C_in_pad, int S,
+                                                        __nv_fp8_e4m3* out, float* scales) {
+  __shared__ float red[8];
+  const int np = blockIdx.x;
+  const int Cd = C_out / S;
+  const int64_t K = 27LL * C_in_pad;
+  const bool real = np < C_out;
+  const int co = real ? (np % Cd) * S + np / Cd : 0;
+  const float* wr = w + static_cast<int64_t>(co) * C_in * 27;  // [C_in, 27] of output channel co
+  float m = 0.f;
+  if (real)
+    for (int64_t i = threadIdx.x; i < 27LL * C_in; i += blockDim.x) m = fmaxf(m, fabsf(wr[i]));
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = 0.f;
+  for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
+  const float scale = m > 0.f ? m / 448.f : 1.f;
+  if (threadIdx.x == 0) scales[np] = scale;
+  for (int64_t i = threadIdx.x; i < K; i += blockDim.x) {
+    const int ci = static_cast<int>(i % C_in_pad);
+    const int tap = static_cast<int>(i / C_in_pad);
+    const float v = (real && ci < C_in) ? wr[static_cast<int64_t>(ci) * 27 + tap] / scale : 0.f;
+    out[static_cast<int64_t>(np) * K + i] = from_f<__nv_fp8_e4m3>(fminf(fmaxf(v, -448.f), 448.f));
+  }
+}
+
+cudaError_t launch_pack_weights_fp8(const float* w, int C_out, int C_in, int C_in_pad, int N_pad, int S, void* out,
+                                    cudaStream_t s) {
+  if (N_pad <= 0) return cudaSuccess;
+  pack_fp8_kernel<<<N_pad, 256, 0, s>>>(w, C_out, C_in, C_in_pad, S, static_cast<__nv_fp8_e4m3*>(out),
+                                        reinterpret_cast<float*>(static_cast<char*>(out) + fp8_scale_offset(N_pad, C_in_pad)));
   return cudaGetLastError();
 }
 

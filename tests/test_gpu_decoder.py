@@ -58,10 +58,12 @@ def test_fp32_mode_matches_oracle(vd, name):
     assert metrics.max_rel(g, r) <= 1e-4
 
 
-@pytest.mark.parametrize("name", ["tiny", "mini_ltx", "mini_wan", "mini_wan_rms"])
+@pytest.mark.parametrize("name", ["tiny", "mini_ltx", "mini_wan", "mini_wan_rms", "mini_wan_rms_g0"])
 def test_bf16_mode_matches_oracle(vd, name):
-    cfg = synth.CONFIGS[name]
-    g = gpu_decode(vd, cfg, vd.VAE_BF16, 2, 3)
+    # mini_wan_rms_g0: the channel-RMS decoder handed gn_groups = 0 (it keeps no group statistics)
+    cfg = synth.CONFIGS[name.replace("_g0", "")]
+    gcfg = dataclasses.replace(cfg, gn_groups=0) if name.endswith("_g0") else cfg
+    g = gpu_decode(vd, gcfg, vd.VAE_BF16, 2, 3)
     r = oracle_out(cfg, True)
     assert metrics.rel_l2(g, r) <= 1e-2
     assert metrics.psnr(g, r) >= 50.0
@@ -82,9 +84,10 @@ def test_bit_identical_across_patch_counts(vd, name, grids, dt):
 
 @pytest.mark.parametrize("dt", ["bf16", "fp32"])
 @pytest.mark.parametrize("per", [1, 2])
-@pytest.mark.parametrize("base", ["mini_wan", "mini_wan_rms"])
+@pytest.mark.parametrize("base", ["mini_wan", "mini_wan_rms", "mini_ltx"])
 def test_chunked_equals_whole(vd, dt, per, base):
-    cfg = dataclasses.replace(synth.CONFIGS[base], latent_shape=(1, 48, 4, 9, 11))
+    c0 = synth.CONFIGS[base]
+    cfg = dataclasses.replace(c0, latent_shape=(1, c0.latent_c, 4, 9, 11))
     dtc = vd.VAE_BF16 if dt == "bf16" else vd.VAE_FP32
     p = synth.draw_params(cfg, 0, rand_affine=True)
     z = torch.from_numpy(synth.draw_latent(cfg, 0)).cuda()

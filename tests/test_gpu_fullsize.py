@@ -2,7 +2,8 @@
 
 The CPU oracle cannot decode a whole 720p x 81f video in test time, so full-size checks use
 properties that hold at any size plus a prefix the oracle can afford:
-  * bit-identical output across patch grids (1x1, 2x2, 2x4 / 1x4), and chunked == whole;
+  * bit-identical output across patch grids (1x1, 2x2, 2x4 / 1x4), and chunked == whole (chunks of
+    1, 4 and 21 latent frames for the Wan-shaped decoder, 1 and 4 for the LTX-shaped one);
   * causality: output frames 0 .. s_t*(k-1) depend only on latent frames 0 .. k-1, so the first
     frames of the full decode must match the oracle's decode of the first latent frame(s) at full
     spatial size (bf16 bar: relative L2 <= 1e-2, PSNR >= 50 dB against the fp32 oracle).
@@ -48,17 +49,22 @@ def test_full_size_bit_identical_across_patch_grids(vd, name, grids):
     dec.close()
 
 
-def test_full_size_wan_chunked_equals_whole(vd):
-    cfg = synth.WAN
+@pytest.mark.parametrize("name,pers", [("wan", (1, 4, 21)), ("ltx", (1, 4))])
+def test_full_size_chunked_equals_whole(vd, name, pers):
+    # chunk 0 = latent frame 0, then chunks of `per` latent frames (per = 21: the rest in one piece)
+    cfg = synth.CONFIGS[name]
+    st = cfg.scale()[0]
     dec, _ = _decoder(vd, cfg)
     z = torch.from_numpy(synth.draw_latent(cfg, 0)).cuda()
     whole = dec.decode(z, n_patch_h=1, n_patch_w=4)
-    t0 = 0
-    for i, s in enumerate(odec.chunk_sizes(z.shape[2], 1)):
-        part = dec.decode_chunk(z[:, :, t0:t0 + s].contiguous(), i == 0, n_patch_h=1, n_patch_w=4)
-        f0 = 0 if i == 0 else 1 + 4 * (t0 - 1)
-        assert torch.equal(part, whole[:, :, f0:f0 + part.shape[2]]), i
-        t0 += s
+    for per in pers:
+        t0 = 0
+        for i, s in enumerate(odec.chunk_sizes(z.shape[2], per)):
+            part = dec.decode_chunk(z[:, :, t0:t0 + s].contiguous(), i == 0, n_patch_h=1, n_patch_w=4)
+            f0 = 0 if i == 0 else 1 + st * (t0 - 1)
+            assert torch.equal(part, whole[:, :, f0:f0 + part.shape[2]]), (per, i)
+            t0 += s
+    assert vd.last_error(dec.h)[0] == vd.VAE_OK
     dec.close()
 
 

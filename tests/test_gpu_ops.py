@@ -41,7 +41,10 @@ def rel_err(g, r):
 
 # ----------------------------------------------------------------------------- GEMM core
 
-@pytest.mark.parametrize("M,N,K,batch", [(200, 96, 128, 2), (128, 256, 64, 1), (77, 48, 192, 3), (300, 512, 256, 1)])
+# unbatched GEMMs with 128- or 256-wide weight tiles run as cta_group::2 pairs (odd M-tile counts leave
+# the last pair's second CTA with no tile of its own; an odd k-block count takes one k block per stage)
+@pytest.mark.parametrize("M,N,K,batch", [(200, 96, 128, 2), (128, 256, 64, 1), (77, 48, 192, 3), (300, 512, 256, 1),
+                                         (700, 128, 256, 1), (520, 128, 192, 1), (260, 384, 128, 1), (90, 256, 320, 1)])
 def test_gemm_bf16(vd, M, N, K, batch):
     A = bf16_round(synth.draw_normal((batch, M, K), 1))
     B = bf16_round(synth.draw_normal((batch, N, K), 2))

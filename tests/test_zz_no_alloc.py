@@ -1,22 +1,19 @@
 """The allocation-free group-norm entry point, for callers that cannot allocate device memory.
 
 vae_patch_groupnorm_silu_noalloc keeps its scratch in a fixed device array inside the library instead
-of taking a workspace.  Through the C ABI, two calls in a row (different shapes, patch grids and
-data, so the second call must clear what the first left in the shared array) must give what the
-workspace-taking vae_patch_groupnorm_silu gives, within the bf16 tolerance the op tests use; a
-descriptor needing more scratch than the array holds is refused.  This file is collected last and
-must also pass on its own in a fresh process.
+of taking a workspace.  Both entry points run the same kernels on the same exact integer sums, so
+through the C ABI two calls in a row must give, bit for bit, what the workspace-taking
+vae_patch_groupnorm_silu gives.  The first call is the larger one (more patches, frames and
+groups), so that the second, smaller call would read nonzero leftovers in the shared array if it
+did not clear what it needs.  A descriptor needing more scratch than the array holds is refused.
+This file is collected last and must also pass on its own in a fresh process.
 """
-import numpy as np
 import pytest
 import torch
 
 from patch_tiled_causal_gb300 import synth
 
 pytestmark = pytest.mark.gpu
-
-BF16_TOL = 2.0 ** -8
-
 
 @pytest.fixture(scope="module")
 def vd():
@@ -35,8 +32,8 @@ def _edges(n, parts):
 
 
 def test_noalloc_matches_workspace_entry_point_twice(vd):
-    cases = [((1, 3, 20, 36, 256), 32, (2, 3), vd.VAE_BF16, 0.0, 11),
-             ((2, 2, 9, 24, 128), 32, (1, 4), vd.VAE_FP32, 3.0, 12)]
+    cases = [((2, 4, 20, 36, 256), 32, (4, 6), vd.VAE_BF16, 0.0, 11),   # 24 patches x 8 frames x 32 groups
+             ((1, 2, 9, 24, 128), 16, (1, 4), vd.VAE_FP32, 3.0, 12)]
     for shape, groups, (ph, pw), dt, offset, seed in cases:
         B, T, H, W, Cc = shape
         tdt = torch.bfloat16 if dt == vd.VAE_BF16 else torch.float32
@@ -51,10 +48,8 @@ def test_noalloc_matches_workspace_entry_point_twice(vd):
         vd.patch_groupnorm_silu_noalloc(x, g, b, y_na, d)
         torch.cuda.synchronize()
         assert vd.last_error()[0] == vd.VAE_OK
-        r = y_ref.float().cpu().numpy()
-        a = y_na.float().cpu().numpy()
-        assert np.isfinite(a).all()
-        assert np.abs(a - r).max() <= BF16_TOL * np.abs(r).max()
+        assert torch.isfinite(y_na.float()).all()
+        assert torch.equal(y_na, y_ref)
 
 
 def test_noalloc_refuses_oversized_scratch(vd):

@@ -183,6 +183,36 @@ def depth_to_space(x: np.ndarray, s: Sequence[int], drop_first: bool) -> np.ndar
     return np.ascontiguousarray(y)
 
 
+def space_to_depth(x: np.ndarray, s: Sequence[int], pad_first: bool) -> np.ndarray:
+    """[B, C, T, H, W] -> [B, C*st*sh*sw, T/st, H/sh, W/sw]: position (c, st*t+dt, sh*y+dy, sw*x+dx)
+    goes to channel c*(st sh sw) + dt*sh*sw + dy*sw + dx (PixelUnshuffle order in 3-D, the inverse of
+    depth_to_space).  With pad_first and st > 1, st-1 copies of frame 0 are put in front first (a
+    causal sequence of T frames folds into (T + st - 1) / st, its first frame into one)."""
+    st, sh, sw = s
+    if pad_first and st > 1:
+        x = np.concatenate([np.repeat(x[:, :, :1], st - 1, axis=2), x], axis=2)
+    n, c, t, h, w = x.shape
+    assert t % st == 0 and h % sh == 0 and w % sw == 0, (x.shape, s)
+    y = x.reshape(n, c, t // st, st, h // sh, sh, w // sw, sw).transpose(0, 1, 3, 5, 7, 2, 4, 6)
+    return np.ascontiguousarray(y.reshape(n, c * st * sh * sw, t // st, h // sh, w // sw))
+
+
+def conv2d_stride2_pad_end(x: np.ndarray, w: np.ndarray, b: np.ndarray, tier: str = "A") -> np.ndarray:
+    """The stride-2 down-sampler of each frame: one zero row below and one zero column to the right,
+    then y[n,o,t,i,j] = b[o] + sum_{kh,kw,c} w[o,c,kh,kw] * xp[n,c,t,2i+kh,2j+kw] (H, W even)."""
+    dt = np.float64 if tier == "A" else np.float32
+    n, c, t, h, wd = x.shape
+    assert h % 2 == 0 and wd % 2 == 0, x.shape
+    xp = np.pad(x.astype(dt), ((0, 0), (0, 0), (0, 0), (0, 1), (0, 1)))
+    wt = w.astype(dt)
+    y = np.zeros((n, w.shape[0], t, h // 2, wd // 2), dtype=dt)
+    for kh in range(3):
+        for kw in range(3):
+            sl = xp[:, :, :, kh:kh + h:2, kw:kw + wd:2]
+            y += np.tensordot(wt[:, :, kh, kw], sl, axes=([1], [1])).transpose(1, 0, 2, 3, 4)
+    return y + b.astype(dt)[None, :, None, None, None]
+
+
 # ---------------------------------------------------------------------------------------------
 # Mid-block spatial attention
 # ---------------------------------------------------------------------------------------------

@@ -81,6 +81,59 @@ class DecoderConfig:
 
 
 @dataclasses.dataclass(frozen=True)
+class EncoderConfig:
+    """Architecture hyper-parameters of a causal video-VAE encoder (a decoder read backwards).
+
+    video_shape  [B, C_pix, T, H, W] pixels.
+    patchify     (s_h, s_w): space-to-depth of the pixels before conv_in ((1, 1) = none).
+    stage_c[i]   channels of stage i; n_res[i] residual blocks in stage i.
+    down[i]      (kind, (s_t, s_h, s_w)) of the down-sampler after stage i (i < n_stages - 1):
+                 "fold"   a stride-1 causal conv to stage_c[i+1] / (s_t*s_h*s_w) channels, then
+                          space-to-depth by (s_t, s_h, s_w);
+                 "stride" zero padding of one row below and one column right, then a 3x3 stride-2
+                          conv of each frame to stage_c[i+1] channels ((s_t, s_h, s_w) = (1, 2, 2)).
+    mid_res      residual blocks after the last stage.
+    latent_c     latent channels; conv_out writes 2 * latent_c (the moments: mean, log-variance).
+    norm         "group" (per-frame group norm) or "rms" (channel RMS norm per pixel).
+    """
+
+    name: str
+    video_shape: Tuple[int, int, int, int, int]
+    stage_c: Tuple[int, ...]
+    n_res: Tuple[int, ...]
+    down: Tuple[Tuple[str, Tuple[int, int, int]], ...]
+    patchify: Tuple[int, int] = (1, 1)
+    mid_res: int = 0
+    gn_groups: int = 32
+    gn_eps: float = 1e-6
+    latent_c: int = 16
+    norm: str = "group"
+
+    @property
+    def pix_c(self) -> int:
+        return self.video_shape[1]
+
+    @property
+    def n_stages(self) -> int:
+        return len(self.stage_c)
+
+    def scale(self) -> Tuple[int, int, int]:
+        """Total (t, h, w) down-sampling factor from pixels to latent."""
+        st, sh, sw = 1, self.patchify[0], self.patchify[1]
+        for _, f in self.down:
+            st *= f[0]
+            sh *= f[1]
+            sw *= f[2]
+        return st, sh, sw
+
+    def latent_shape(self, video_shape: Optional[Sequence[int]] = None) -> Tuple[int, ...]:
+        """[B, 2*latent_c, T', h, w]: causal time, the first pixel frame -> one latent frame."""
+        b, _, t, h, w = video_shape if video_shape is not None else self.video_shape
+        st, sh, sw = self.scale()
+        return (b, 2 * self.latent_c, (t - 1) // st + 1, h // sh, w // sw)
+
+
+@dataclasses.dataclass(frozen=True)
 class TilingConfig:
     """Overlap-tiled decode: tile length and overlap per axis, in latent units (t, h, w)."""
 
@@ -131,6 +184,29 @@ MINI_TILING = TilingConfig(tile=(3, 4, 4), overlap=(1, 1, 2))
 CONFIGS: Dict[str, DecoderConfig] = {c.name: c for c in (
     TINY, WAN, LTX, LTX_TILED, MINI_LTX, MINI_WAN, MINI_TILED, WAN_RMS, MINI_WAN_RMS)}
 
+# Encoders: the LTX-shaped decoder read backwards (720p x 81f pixels -> latent [1, 256, 11, 22, 40]
+# moments: patchify 4 x 4, three space-to-depth down-samplers (2, 2, 2)), and small ones that the
+# oracle runs in seconds, one per down-sampler kind.
+LTX_ENC = EncoderConfig(
+    name="ltx_enc", video_shape=(1, 3, 81, 704, 1280), stage_c=(128, 256, 512, 1024), n_res=(3, 3, 3, 3),
+    down=(("fold", (2, 2, 2)),) * 3, patchify=(4, 4), gn_groups=32, latent_c=128)
+TINY_ENC = EncoderConfig(
+    name="tiny_enc", video_shape=(1, 3, 5, 16, 16), stage_c=(32, 32), n_res=(1, 1),
+    down=(("fold", (2, 2, 2)),), gn_groups=8, latent_c=4)
+TINY_ENC_STRIDE = EncoderConfig(
+    name="tiny_enc_stride", video_shape=(1, 3, 3, 16, 16), stage_c=(32, 32), n_res=(1, 1),
+    down=(("stride", (1, 2, 2)),), gn_groups=8, latent_c=4)
+MINI_ENC = EncoderConfig(
+    name="mini_enc", video_shape=(1, 3, 9, 40, 56), stage_c=(128, 128), n_res=(1, 1),
+    down=(("fold", (2, 2, 2)),), patchify=(4, 4), mid_res=1, gn_groups=32, latent_c=16)
+MINI_ENC_STRIDE = EncoderConfig(
+    name="mini_enc_stride", video_shape=(1, 3, 5, 24, 40), stage_c=(64, 128), n_res=(1, 1),
+    down=(("stride", (1, 2, 2)),), patchify=(2, 2), gn_groups=32, latent_c=16)
+MINI_ENC_RMS = dataclasses.replace(MINI_ENC, name="mini_enc_rms", norm="rms")
+
+ENCODERS: Dict[str, EncoderConfig] = {c.name: c for c in (
+    LTX_ENC, TINY_ENC, TINY_ENC_STRIDE, MINI_ENC, MINI_ENC_STRIDE, MINI_ENC_RMS)}
+
 
 # ---------------------------------------------------------------------------------------------
 # Parameter list (declaration order) and draws.
@@ -145,11 +221,41 @@ def _resblock_params(prefix: str, c: int) -> List[Tuple[str, Tuple[int, ...]]]:
     ]
 
 
-def param_specs(cfg: DecoderConfig) -> "OrderedDict[str, Tuple[int, ...]]":
-    """Every parameter of the decoder, in declaration order, with its shape.
+def encoder_param_specs(cfg: EncoderConfig) -> "OrderedDict[str, Tuple[int, ...]]":
+    """Every parameter of the encoder, in declaration order, with its shape.
+
+    Causal conv weights are [C_out, C_in, 3, 3, 3]; the stride-2 down-sampler's [C_out, C_in, 3, 3].
+    """
+    specs: List[Tuple[str, Tuple[int, ...]]] = []
+    c0 = cfg.stage_c[0]
+    cin = cfg.pix_c * cfg.patchify[0] * cfg.patchify[1]
+    specs += [("conv_in.weight", (c0, cin, 3, 3, 3)), ("conv_in.bias", (c0,))]
+    for i, c in enumerate(cfg.stage_c):
+        for r in range(cfg.n_res[i]):
+            specs += _resblock_params(f"stage{i}.res{r}", c)
+        if i + 1 < cfg.n_stages:
+            kind, (st, sh, sw) = cfg.down[i]
+            if kind == "fold":
+                co = cfg.stage_c[i + 1] // (st * sh * sw)
+                specs += [(f"stage{i}.down.weight", (co, c, 3, 3, 3)), (f"stage{i}.down.bias", (co,))]
+            else:
+                co = cfg.stage_c[i + 1]
+                specs += [(f"stage{i}.down.weight", (co, c, 3, 3)), (f"stage{i}.down.bias", (co,))]
+    cl = cfg.stage_c[-1]
+    for r in range(cfg.mid_res):
+        specs += _resblock_params(f"mid.res{r}", cl)
+    specs += [("head.norm.gamma", (cl,)), ("head.norm.beta", (cl,)),
+              ("head.conv.weight", (2 * cfg.latent_c, cl, 3, 3, 3)), ("head.conv.bias", (2 * cfg.latent_c,))]
+    return OrderedDict(specs)
+
+
+def param_specs(cfg) -> "OrderedDict[str, Tuple[int, ...]]":
+    """Every parameter of the decoder (or encoder), in declaration order, with its shape.
 
     Convolution weights are [C_out, C_in, k_t, k_h, k_w]; attention projections [C_out, C_in].
     """
+    if isinstance(cfg, EncoderConfig):
+        return encoder_param_specs(cfg)
     specs: List[Tuple[str, Tuple[int, ...]]] = []
     c0 = cfg.stage_c[0]
     specs += [("conv_in.weight", (c0, cfg.latent_c, 3, 3, 3)), ("conv_in.bias", (c0,))]
@@ -172,6 +278,12 @@ def param_specs(cfg: DecoderConfig) -> "OrderedDict[str, Tuple[int, ...]]":
               ("head.conv.weight", (cfg.out_c * st * sh * sw, cl, 3, 3, 3)),
               ("head.conv.bias", (cfg.out_c * st * sh * sw,))]
     return OrderedDict(specs)
+
+
+def draw_video(cfg: EncoderConfig, seed: int = 0, shape: Optional[Sequence[int]] = None) -> np.ndarray:
+    """Pixels [B, C_pix, T, H, W] ~ N(0, 1), float32, from PCG64(seed)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return rng.standard_normal(tuple(shape or cfg.video_shape), dtype=np.float32)
 
 
 def draw_latent(cfg: DecoderConfig, seed: int = 0,

@@ -11,8 +11,9 @@ One JSON line on rank 0 with the contract's keys plus:
   kernels       the same per kernel class (conv, group norm stats/apply, attention GEMMs, ...)
   ops           the op-level workloads: PatchGroupNorm+SiLU, channel RMS norm+SiLU, causal conv 512->512,
                 tile blend
-  extra         the LTX-shaped 720p x 81f decode (1x4 and 2x4 patches) and the batch-2 overlap-tiled LTX
-                decode (45 tiles -> [2,3,129,1088,1920]): Mframe-px/s, conv fraction, per-kernel table
+  extra         the LTX-shaped 720p x 81f decode (1x4 and 2x4 patches), the batch-2 overlap-tiled LTX
+                decode (45 tiles -> [2,3,129,1088,1920]), the Wan-shaped decode with e4m3 conv operands and
+                the LTX-shaped encode of 720p x 81f: Mframe-px/s, conv fraction, per-kernel table
   cpu_baseline  the CPU oracle on a bounded sample of the same decode (first 2 latent frames of one
                 full-width latent row), host cores
 N > 1 (torchrun): each rank decodes its own latent (independent videos, weak scaling), no
@@ -227,6 +228,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the LTX-shaped and tiled decode sub-lines")
     ap.add_argument("--only", default="all", choices=["all", "decode", "ops"],
                     help="run only the decode or only the op workloads (profiling runs)")
+    ap.add_argument("--ops-frames", type=int, default=0,
+                    help="frames of the op workloads (0: the full sizes; small values for profiler captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     cfg = {"wan": synth.WAN, "ltx": synth.LTX, "wan_rms": synth.WAN_RMS}[args.workload]
@@ -348,6 +351,8 @@ def main():
         dec.close()  # frees the Wan decoder's workspace before the LTX decoders are built
         torch.cuda.empty_cache()
         extra = run_ltx(args, torch, vaedec, peaks, flush, stream)
+        extra["wan_fp8_1x4"] = run_wan_fp8(args, torch, vaedec, peaks, flush, stream)
+        extra["ltx_encode_1x4"] = run_ltx_encode(args, torch, vaedec, peaks, flush, stream)
 
     cpu = None
     if not args.no_cpu and rank == 0 and world == 1:
@@ -425,6 +430,53 @@ def timed_decodes(torch, dec, fn, steps, warmup, flush, stream):
     return sum(a.elapsed_time(b) for a, b in evs) / steps, prof
 
 
+def run_wan_fp8(args, torch, vd, peaks, flush, stream):
+    """The Wan-shaped 720p x 81f decode (1x4 patches) with e4m3 conv operands (VAE_FP8)."""
+    cfg = synth.WAN
+    params = synth.draw_params(cfg, 0)
+    dec = vd.Decoder(cfg, params, vd.VAE_FP8)
+    del params
+    z = torch.from_numpy(synth.draw_latent(cfg, 0)).cuda()
+    out = torch.empty(dec.output_shape(z.shape), dtype=torch.bfloat16, device="cuda")
+    ms, prof = timed_decodes(torch, dec, lambda: dec.decode(z, out, 1, 4), args.steps, args.warmup, flush, stream)
+    code, msg = vd.last_error(dec.h)
+    if code:
+        raise RuntimeError(f"fp8 decode failed: {msg}")
+    dec.close()
+    fpx = out.shape[0] * out.shape[2] * out.shape[3] * out.shape[4]
+    del z, out
+    torch.cuda.empty_cache()
+    return {"workload": f"wan-shaped decoder, latent {list(cfg.latent_shape)}, 1x4 patches, e4m3 operands for the "
+                        "residual-block and up-sampler convs (conv_in, conv_out, attention bf16), pixels bf16",
+            "value": fpx / ms / 1e3, "unit": "Mframe-px/s", "ms_per_step": ms, "dtype": "fp8 (e4m3) conv operands",
+            "kernels": kernel_table(prof, args.steps, peaks)}
+
+
+def run_ltx_encode(args, torch, vd, peaks, flush, stream):
+    """The LTX-shaped encoder (the decoder read backwards): pixels [1,3,81,704,1280] -> moments
+    [1,256,11,22,40], 1x4 patches; throughput in encoded Mframe-px/s of the input video."""
+    cfg = synth.LTX_ENC
+    params = synth.draw_params(cfg, 0)
+    enc = vd.Encoder(cfg, params, vd.VAE_BF16)
+    del params
+    v = torch.from_numpy(synth.draw_video(cfg, 0)).cuda()
+    out = torch.empty(enc.output_shape(v.shape), dtype=torch.float32, device="cuda")
+    ms, prof = timed_decodes(torch, enc, lambda: enc.encode(v, out, 1, 4), args.steps, args.warmup, flush, stream)
+    code, msg = enc.last_error()
+    if code:
+        raise RuntimeError(f"encode failed: {msg}")
+    enc.close()
+    fpx = v.shape[0] * v.shape[2] * v.shape[3] * v.shape[4]
+    conv = conv_totals(prof)
+    tf = conv["flops"] / (conv["ms"] / 1e3) / 1e12
+    del v, out
+    torch.cuda.empty_cache()
+    return {"workload": f"ltx-shaped encoder, pixels {list(cfg.video_shape)} -> moments {list(cfg.latent_shape())}, "
+                        "1x4 patches", "value": fpx / ms / 1e3, "unit": "encoded Mframe-px/s", "ms_per_step": ms,
+            "conv_tflops": tf, "conv_frac_of_bf16_sustained": tf / peaks["bf16_tflops_sustained"],
+            "kernels": kernel_table(prof, args.steps, peaks)}
+
+
 def run_ltx(args, torch, vd, peaks, flush, stream):
     """The LTX-shaped 720p x 81f decode at 1x4 and 2x4 patches, and the batch-2 overlap-tiled LTX decode
     (latent [2,128,17,34,60] -> [2,3,129,1088,1920], 45 tiles of 8x16x16 latents, 1x4x4 overlap)."""
@@ -479,7 +531,7 @@ def _time(torch, fn, steps, flush):
 
 def run_ops(args, torch, vd, peaks, flush):
     res = {}
-    B, C, T, H, W = 1, 512, 21, 88, 160
+    B, C, T, H, W = 1, 512, args.ops_frames or 21, 88, 160
     eh, ew = vd.patch_edges(H, 1), vd.patch_edges(W, 4)
     # (a) PatchGroupNorm + SiLU, 4 width patches
     x = torch.from_numpy(synth.draw_normal((B, T, H, W, C), 100)).to("cuda", torch.bfloat16)
@@ -512,7 +564,36 @@ def run_ops(args, torch, vd, peaks, flush):
     res["conv3d_causal"] = {"workload": "3x3x3 512->512 on [1,512,21,88,160] bf16, 4 width patches", "ms": ms,
                             "tflops": fl / ms / 1e9, "frac_of_bf16": fl / ms / 1e9 / peaks["bf16_tflops"],
                             "bound": "tensor", "traffic": tr["bytes_per_launch"] if tr else None}
-    del x, y, yc, wp
+    # (b') the same conv with e4m3 operands and per-channel-scaled e4m3 weights (kind::f8f6f4); the peak is
+    # the measured bf16 peak x 2, the nominal dense fp8 : bf16 ratio (4.5 : 2.25 PFLOP/s)
+    cd8 = vd.conv_desc(B, T, H, W, C, C, eh, ew, in_dtype=vd.VAE_FP8)
+    wp8 = vd.conv3d_pack_weights(w, cd8)
+    x8 = x.float().clamp(-448, 448).to(torch.float8_e4m3fn)  # input preparation, not timed
+    ms = _time(torch, lambda: vd.conv3d_causal(x8, wp8, None, None, yc, cd8), args.steps, flush)
+    res["conv3d_causal_fp8"] = {"workload": "3x3x3 512->512 on [1,512,21,88,160], e4m3 operands, bf16 out, 4 width patches",
+                                "ms": ms, "tflops": fl / ms / 1e9, "frac_of_fp8": fl / ms / 1e9 / (2 * peaks["bf16_tflops"]),
+                                "peak_kind": "fp8 dense = 2 x measured bf16 burst (nominal ratio)", "bound": "tensor",
+                                "speedup_vs_bf16": res["conv3d_causal"]["ms"] / ms}
+    del x, y, yc, wp, x8, wp8
+    # (d) the pixel heads (conv_out + final depth-to-space, NCTHW pixels): Wan 256 -> 12, d2s (1,2,2) on
+    # [1,256,81,352,640]; LTX 128 -> 48, d2s (1,4,4) on [1,128,81,176,320]; 4 width patches
+    for name, Ci, Co, Hh, Wh, d2 in (("conv_head_wan", 256, 12, 352, 640, (1, 2, 2)),
+                                     ("conv_head_ltx", 128, 48, 176, 320, (1, 4, 4))):
+        Th = args.ops_frames or 81
+        xh = torch.from_numpy(synth.draw_normal((1, Th, Hh, Wh, Ci), 102)).to("cuda", torch.bfloat16)
+        wh = torch.from_numpy(synth.conv_weight(Co, Ci, 103)).cuda()
+        hd = vd.conv_desc(1, Th, Hh, Wh, Ci, Co, vd.patch_edges(Hh, 1), vd.patch_edges(Wh, 4), d2s=d2, out_ncthw=True)
+        whp = vd.conv3d_pack_weights(wh, hd)
+        yh = torch.empty((1, Co // (d2[1] * d2[2]), Th, Hh * d2[1], Wh * d2[2]), dtype=torch.bfloat16, device="cuda")
+        ms = _time(torch, lambda: vd.conv3d_causal(xh, whp, None, None, yh, hd), args.steps, flush)
+        flh = 2.0 * 27 * Ci * Co * Th * Hh * Wh
+        byh = xh.numel() * 2 + yh.numel() * 2
+        t_floor = max(flh / (peaks["bf16_tflops"] * 1e12), byh / (peaks["hbm_gbs"] * 1e9)) * 1e3
+        res[name] = {"workload": f"3x3x3 {Ci}->{Co}, d2s {d2}, on [1,{Ci},{Th},{Hh},{Wh}] bf16 -> NCTHW pixels, "
+                                 "4 width patches", "ms": ms, "tflops": flh / ms / 1e9, "gbs": byh / ms / 1e6,
+                     "roofline_ms": t_floor, "frac_of_roofline": t_floor / ms,
+                     "bound": "max(FLOP / bf16 peak, bytes / HBM)"}
+        del xh, yh, whp
     # (c) tile blend: 28 tiles of 256^2 with 64 px overlap -> [1, 3, 81, 704, 1280]
     meta = vd.tile_plan((81, 704, 1280), (81, 256, 256), (0, 64, 64), 1, 1, causal_t=False)
     tiles = [torch.from_numpy(synth.draw_normal((1, 3, m["pix"][1], m["pix"][3], m["pix"][5]), 200 + i)).to(

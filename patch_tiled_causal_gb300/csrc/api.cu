@@ -320,12 +320,22 @@ extern "C" vae_status_t vae_decoder_n_weights(const vae_config_t* cfg, int* n_we
   return VAE_OK;
 }
 
-extern "C" void vae_decoder_destroy(vae_decoder_t* d) {
-  if (!d) return;
+namespace {
+// Every device allocation of a handle (weights, workspace, caches, tile storage).
+void release_memory(vae_decoder* d) {
   cudaDeviceSynchronize();
   for (void* p : d->owned) cudaFree(p);
+  d->owned.clear();
   if (d->ws) cudaFree(d->ws);
   if (d->tiles) cudaFree(d->tiles);
+  d->ws = d->tiles = nullptr;
+  d->ws_bytes = d->tiles_bytes = 0;
+}
+}  // namespace
+
+extern "C" void vae_decoder_destroy(vae_decoder_t* d) {
+  if (!d) return;
+  release_memory(d);
   delete d;
 }
 
@@ -1147,6 +1157,421 @@ extern "C" vae_status_t vae_decoder_profile_read(vae_decoder_t* d, vae_prof_t* o
   return VAE_OK;
 }
 #undef ERRP
+
+// ================================================================================ encoder
+// The encoder runs the decoder's layers read backwards ([DV] encoder commits): the same convs, norms and
+// residual blocks (through an embedded decoder core that holds the norm configuration, dtype, error
+// record, profiling and allocations), with down-samplers in place of up-samplers.
+struct vae_encoder {
+  vae_decoder core;
+  vae_encoder_config_t ecfg{};
+  ConvL conv_in;
+  std::vector<std::vector<ResL>> stages;
+  std::vector<ConvL> downs;
+  std::vector<ResL> mid;
+  NormL head_norm;
+  ConvL head;
+};
+
+namespace {
+
+int count_enc_weights(const vae_encoder_config_t& c) {
+  int n = 2;
+  for (int i = 0; i < c.n_stages; ++i) {
+    n += 8 * c.n_res[i];
+    if (i + 1 < c.n_stages) n += 2;
+  }
+  return n + 8 * c.mid_res + 4;
+}
+
+vae_status_t check_enc_config(const vae_encoder_config_t* c) {
+  if (!c) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null encoder config");
+  const bool rms = c->norm_type == VAE_NORM_CHANNEL_RMS;
+  if ((c->norm_type != VAE_NORM_GROUP && !rms) || c->n_stages < 1 || c->n_stages > VAE_MAX_STAGES || c->pix_c <= 0 ||
+      c->patch_h < 1 || c->patch_w < 1 || c->latent_c <= 0 || c->mid_res < 0 || (!rms && c->gn_groups <= 0) ||
+      (c->dtype != VAE_BF16 && c->dtype != VAE_FP32 && c->dtype != VAE_FP8))
+    return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "invalid encoder config");
+  for (int i = 0; i < c->n_stages; ++i) {
+    const int C = c->stage_c[i];
+    if (C <= 0 || c->n_res[i] < 0) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "stage %d channels", i);
+    if (rms ? !rms_supported(C)
+            : (C % c->gn_groups || C % 8 || C > 6144 || !((C / c->gn_groups) % 8 == 0 || 8 % (C / c->gn_groups) == 0)))
+      return set_err(nullptr, VAE_ERR_UNSUPPORTED, 0, 0, "stage %d: %d channels not supported by its norm", i, C);
+    if (i + 1 < c->n_stages) {
+      const int st = c->down_t[i], sh = c->down_h[i], sw = c->down_w[i];
+      if (c->down_kind[i] == VAE_DOWN_FOLD) {
+        if (st < 1 || st > 2 || sh < 1 || sw < 1 || c->stage_c[i + 1] % (st * sh * sw))
+          return set_err(nullptr, VAE_ERR_UNSUPPORTED, 0, 0, "fold down-sampler %d factors", i);
+      } else if (c->down_kind[i] == VAE_DOWN_STRIDE) {
+        if (st != 1 || sh != 2 || sw != 2)
+          return set_err(nullptr, VAE_ERR_UNSUPPORTED, 0, 0, "the strided down-sampler %d takes factors (1, 2, 2)", i);
+      } else {
+        return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "down-sampler %d kind", i);
+      }
+    }
+  }
+  return VAE_OK;
+}
+
+struct EncPlan {
+  Plan p;                 // B, patch grid, buffer sizes (no attention); p.lv = one level per stage
+  int T0, H0, W0, Cin;    // the patchified pixels (conv_in's input)
+};
+
+// Levels: stage i at T_i x H_i x W_i; bands cut on the latent grid, scaled by what stage i still narrows.
+vae_status_t make_enc_plan(vae_encoder* e, int B, int T, int H, int W, int nph, int npw, EncPlan& ep) {
+  const vae_encoder_config_t& c = e->ecfg;
+  vae_decoder* d = &e->core;
+  int st_tot = 1, sh_tot = c.patch_h, sw_tot = c.patch_w;
+  for (int i = 0; i + 1 < c.n_stages; ++i) {
+    st_tot *= c.down_t[i];
+    sh_tot *= c.down_h[i];
+    sw_tot *= c.down_w[i];
+  }
+  if (H % sh_tot || W % sw_tot || (T - 1) % st_tot)
+    return set_err(&d->err, VAE_ERR_INVALID_ARG, 0, 0,
+                   "video %dx%dx%d: frames - 1 must divide by %d and rows / cols by %d / %d", T, H, W, st_tot, sh_tot,
+                   sw_tot);
+  const int h_lat = H / sh_tot, w_lat = W / sw_tot;
+  Plan& p = ep.p;
+  p.B = B; p.nph = nph; p.npw = npw; p.first = true;
+  p.Tlat = (T - 1) / st_tot + 1; p.h = h_lat; p.w = w_lat;
+  p.lv.clear();
+  ep.T0 = T; ep.H0 = H / c.patch_h; ep.W0 = W / c.patch_w;
+  ep.Cin = c.pix_c * c.patch_h * c.patch_w;
+  int Ti = T, sh = sh_tot / c.patch_h, sw = sw_tot / c.patch_w;
+  for (int i = 0; i < c.n_stages; ++i) {
+    Level L{};
+    L.T = Ti; L.H = h_lat * sh; L.W = w_lat * sw; L.C = c.stage_c[i];
+    vae_status_t s = band_edges(h_lat, nph, sh, 1, L.ph, &d->err);
+    if (!s) s = band_edges(w_lat, npw, sw, 1, L.pw, &d->err);
+    if (s) return s;
+    p.lv.push_back(L);
+    if (i + 1 < c.n_stages) {
+      Ti = (Ti + c.down_t[i] - 1) / c.down_t[i];
+      sh /= c.down_h[i];
+      sw /= c.down_w[i];
+    }
+  }
+  const int ab = act_bytes(d), rb = res_bytes(d), cb = c1_bytes(d);
+  p.x_bytes = p.hin_bytes = p.c1_bytes = p.gn_bytes = 0;
+  p.hin_bytes = static_cast<size_t>(B) * (T + 2) * ep.H0 * ep.W0 * e->conv_in.C_in_pad * ab;
+  for (int i = 0; i < c.n_stages; ++i) {
+    const Level& L = p.lv[i];
+    const size_t px = static_cast<size_t>(B) * L.H * L.W;
+    p.x_bytes = std::max(p.x_bytes, px * L.T * L.C * rb);
+    p.hin_bytes = std::max(p.hin_bytes, px * (L.T + 2) * L.C * ab);
+    p.c1_bytes = std::max(p.c1_bytes, px * L.T * L.C * cb);
+    const int groups = c.norm_type == VAE_NORM_GROUP ? c.gn_groups : 0;
+    p.gn_bytes = std::max(p.gn_bytes, gn_workspace_bytes(nph, npw, B, L.T, groups, L.C));
+    if (i + 1 < c.n_stages) {
+      const Level& N = p.lv[i + 1];
+      if (c.down_kind[i] == VAE_DOWN_FOLD)  // the down conv's unfolded output
+        p.c1_bytes = std::max(p.c1_bytes, px * L.T * e->downs[i].C_out * rb);
+      else                                  // the (1,2,2)-folded input of the strided conv
+        p.hin_bytes = std::max(p.hin_bytes, static_cast<size_t>(B) * (N.T + 2) * N.H * N.W * 4 * L.C * ab);
+    }
+    if (c.norm_type == VAE_NORM_GROUP &&
+        static_cast<double>(L.C / c.gn_groups) * L.H * L.W >= 8388608.0)
+      return set_err(&d->err, VAE_ERR_UNSUPPORTED, 0, 0, "stage %d: group exceeds the exact-sum range", i);
+  }
+  p.lat_bytes = 0;
+  p.attn_tok = p.attn_tokp = 0;
+  p.q_bytes = p.vt_bytes = p.s_bytes = p.p_bytes = 0;
+  return VAE_OK;
+}
+
+#define ERRP (&d->err)
+// Encode the pixel box rows [h0, h0 + H), cols [w0, w0 + W) (pixel units) of video [B, pix_c, T, Hf, Wf]
+// into moments NCTHW fp32 [B, 2*latent_c, T', h, w].
+vae_status_t run_encode(vae_encoder* e, const EncPlan& ep, const float* video, int Hf, int Wf, int h0, int w0,
+                        float* out, cudaStream_t s) {
+  vae_decoder* d = &e->core;
+  const vae_encoder_config_t& c = e->ecfg;
+  const Plan& p = ep.p;
+  Ctx x{d, &p, carve(d->ws, p), s, false};
+  const int rf = res_bytes(d) == 4;
+  auto kind_of = [&](const ConvL& cv) { return cv.fp8 ? 2 : (d->f32 ? 1 : 0); };
+  {
+    const Level& L0 = p.lv[0];
+    const int ob = op_bytes(d, e->conv_in);
+    const int64_t fb = static_cast<int64_t>(ep.H0) * ep.W0 * e->conv_in.C_in_pad * ob;
+    {
+      Prof pr(d, s, K_LATENT, 0, static_cast<double>(p.B) * ep.T0 * ep.H0 * ep.W0 * (ep.Cin * 4.0 + e->conv_in.C_in_pad * ob));
+      CK(launch_pixels_to_cl(video, p.B, c.pix_c, ep.T0, Hf, Wf, c.patch_h, c.patch_w, h0 / c.patch_h, ep.H0,
+                             w0 / c.patch_w, ep.W0, e->conv_in.C_in_pad, x.b.hin + 2 * fb, kind_of(e->conv_in), ep.T0 + 2,
+                             s));
+    }
+    ConvOut o;
+    o.y = x.b.x; o.y_f32 = rf; o.y_T_alloc = L0.T; o.stats_level = &L0;
+    vae_status_t st = run_conv(x, e->conv_in, L0, x.b.hin, o);
+    if (st) return st;
+  }
+  for (int i = 0; i < c.n_stages; ++i) {
+    const Level& L = p.lv[i];
+    for (auto& r : e->stages[i]) {
+      vae_status_t st = run_resblock(x, r, L);
+      if (st) return st;
+    }
+    if (i + 1 == c.n_stages) break;
+    const Level& N = p.lv[i + 1];
+    ConvL& dc = e->downs[i];
+    const int ob = op_bytes(d, dc);
+    if (c.down_kind[i] == VAE_DOWN_FOLD) {
+      // stride-1 conv of the residual stream (cast to the conv's operand type), then the fold
+      const int64_t fe = static_cast<int64_t>(L.H) * L.W * L.C;
+      {
+        Prof pr(d, s, K_CAST, 0, static_cast<double>(p.B) * L.T * fe * (res_bytes(d) + ob));
+        CK(launch_cast_frames(x.b.x, rf, L.T, x.b.hin + 2 * fe * ob, kind_of(dc), L.T + 2, p.B, L.T, fe, s));
+      }
+      ConvOut od;
+      od.y = x.b.c1; od.y_f32 = rf; od.y_T_alloc = L.T;
+      vae_status_t st = run_conv(x, dc, L, x.b.hin, od);
+      if (st) return st;
+      Prof pr(d, s, K_COPY, 0, 2.0 * p.B * L.T * L.H * L.W * dc.C_out * res_bytes(d));
+      CK(launch_fold_frames(x.b.c1, rf, L.T, p.B, L.T, L.H, L.W, dc.C_out, c.down_t[i], c.down_h[i], c.down_w[i], x.b.x,
+                            rf ? 1 : 0, N.T, s));
+      x.stats_src = nullptr;
+    } else {
+      // fold (1, 2, 2) into the conv's operand type, then the stride-1 conv with rearranged weights
+      const int64_t fe2 = static_cast<int64_t>(N.H) * N.W * 4 * L.C;
+      {
+        Prof pr(d, s, K_COPY, 0, static_cast<double>(p.B) * N.T * fe2 * (res_bytes(d) + ob));
+        CK(launch_fold_frames(x.b.x, rf, L.T, p.B, L.T, L.H, L.W, L.C, 1, 2, 2, x.b.hin + 2 * fe2 * ob, kind_of(dc),
+                              N.T + 2, s));
+      }
+      ConvOut od;
+      od.y = x.b.x; od.y_f32 = rf; od.y_T_alloc = N.T; od.stats_level = &N;
+      vae_status_t st = run_conv(x, dc, N, x.b.hin, od);
+      if (st) return st;
+    }
+  }
+  const Level& LL = p.lv[c.n_stages - 1];
+  for (auto& r : e->mid) {
+    vae_status_t st = run_resblock(x, r, LL);
+    if (st) return st;
+  }
+  vae_status_t st = run_gn(x, e->head_norm, LL, x.b.x, rf, 1, e->head.fp8);
+  if (st) return st;
+  ConvOut o;
+  o.y = out; o.y_f32 = 1; o.y_T_alloc = LL.T; o.out_ncthw = 1;
+  return run_conv(x, e->head, LL, x.b.hin, o);
+}
+#undef ERRP
+
+vae_status_t check_video(vae_encoder* e, const int64_t* shp, int nph, int npw) {
+  vae_decoder* d = &e->core;
+  if (!shp) return set_err(&d->err, VAE_ERR_INVALID_ARG, 0, 0, "null shape");
+  if (shp[0] <= 0 || shp[1] != e->ecfg.pix_c || shp[2] <= 0 || shp[3] <= 0 || shp[4] <= 0)
+    return set_err(&d->err, VAE_ERR_INVALID_ARG, 0, 0, "video shape mismatch");
+  if (shp[0] > 64 || shp[2] > 4096 || shp[3] > 16384 || shp[4] > 16384)
+    return set_err(&d->err, VAE_ERR_UNSUPPORTED, 0, 0, "video too large");
+  if (nph < 1 || npw < 1 || nph > VAE_MAX_PATCHES || npw > VAE_MAX_PATCHES)
+    return set_err(&d->err, VAE_ERR_INVALID_ARG, 0, 0, "patch counts %d x %d", nph, npw);
+  return VAE_OK;
+}
+
+}  // namespace
+
+extern "C" vae_status_t vae_encoder_n_weights(const vae_encoder_config_t* cfg, int* n_weights) {
+  vae_status_t s = check_enc_config(cfg);
+  if (s) return s;
+  if (!n_weights) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null n_weights");
+  *n_weights = count_enc_weights(*cfg);
+  return VAE_OK;
+}
+
+extern "C" void vae_encoder_destroy(vae_encoder_t* e) {
+  if (!e) return;
+  release_memory(&e->core);
+  delete e;
+}
+
+extern "C" vae_status_t vae_encoder_create(const vae_encoder_config_t* cfg, const void* const* weights, int n_weights,
+                                           vae_encoder_t** out) {
+  if (!out) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null out");
+  *out = nullptr;
+  vae_status_t s = check_enc_config(cfg);
+  if (s) return s;
+  if (!weights || n_weights != count_enc_weights(*cfg))
+    return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "expected %d weight tensors, got %d", count_enc_weights(*cfg),
+                   n_weights);
+  for (int i = 0; i < n_weights; ++i)
+    if (!weights[i] || !aligned16(weights[i]))
+      return set_err(nullptr, weights[i] ? VAE_ERR_ALIGNMENT : VAE_ERR_INVALID_ARG, 0, 0, "weight %d pointer", i);
+  vae_encoder* e = new vae_encoder();
+  e->ecfg = *cfg;
+  vae_decoder* d = &e->core;
+  d->cfg.gn_groups = cfg->gn_groups;
+  d->cfg.gn_eps = cfg->gn_eps;
+  d->cfg.norm_type = cfg->norm_type;
+  d->cfg.dtype = cfg->dtype;
+  d->f32 = cfg->dtype == VAE_FP32;
+  d->f8 = cfg->dtype == VAE_FP8;
+  int k = 0;
+  auto W = [&](void) { return static_cast<const float*>(weights[k++]); };
+  auto res_block = [&](ResL& r, int C) -> vae_status_t {
+    const float *g1 = W(), *b1 = W(), *w1 = W(), *bb1 = W(), *g2 = W(), *b2 = W(), *w2 = W(), *bb2 = W();
+    vae_status_t st = make_norm(d, r.n1, g1, b1, C);
+    if (!st) st = make_conv(d, r.c1, w1, bb1, C, C, 1, 1, 1, false, true);
+    if (!st) st = make_norm(d, r.n2, g2, b2, C);
+    if (!st) st = make_conv(d, r.c2, w2, bb2, C, C, 1, 1, 1, false, true);
+    return st;
+  };
+  {
+    const float* w = W();
+    const float* b = W();
+    s = make_conv(d, e->conv_in, w, b, cfg->pix_c * cfg->patch_h * cfg->patch_w, cfg->stage_c[0], 1, 1, 1, true);
+  }
+  e->stages.resize(cfg->n_stages);
+  e->downs.resize(std::max(0, cfg->n_stages - 1));
+  float* tmp = nullptr;  // rearranged stride-2 weights
+  for (int i = 0; i < cfg->n_stages && !s; ++i) {
+    const int C = cfg->stage_c[i];
+    e->stages[i].resize(cfg->n_res[i]);
+    for (int r = 0; r < cfg->n_res[i] && !s; ++r) s = res_block(e->stages[i][r], C);
+    if (i + 1 < cfg->n_stages && !s) {
+      const float* w = W();
+      const float* b = W();
+      const int Cn = cfg->stage_c[i + 1];
+      if (cfg->down_kind[i] == VAE_DOWN_FOLD) {
+        const int S = cfg->down_t[i] * cfg->down_h[i] * cfg->down_w[i];
+        s = make_conv(d, e->downs[i], w, b, C, Cn / S, 1, 1, 1, false, true);
+      } else {
+        if (!tmp) s = dalloc(d, &tmp, static_cast<size_t>(Cn) * 4 * C * 27 * 4);  // freed with the handle
+        cudaError_t ce = s ? cudaSuccess : launch_stride2_weights(w, Cn, C, tmp, nullptr);
+        if (ce != cudaSuccess) s = set_err(&d->err, VAE_ERR_CUDA, 0, 0, "stride-2 weights: %s", cudaGetErrorString(ce));
+        if (!s) s = make_conv(d, e->downs[i], tmp, b, 4 * C, Cn, 1, 1, 1, false, true);
+        if (!s && cudaDeviceSynchronize() != cudaSuccess) s = set_err(&d->err, VAE_ERR_CUDA, 0, 0, "weight packing");
+        tmp = nullptr;  // the next strided down-sampler (if any) gets its own scratch
+      }
+    }
+  }
+  const int CL = cfg->stage_c[cfg->n_stages - 1];
+  e->mid.resize(cfg->mid_res);
+  for (int r = 0; r < cfg->mid_res && !s; ++r) s = res_block(e->mid[r], CL);
+  if (!s) {
+    const float* g = W();
+    const float* b = W();
+    s = make_norm(d, e->head_norm, g, b, CL);
+    const float* w = W();
+    const float* bb = W();
+    if (!s) s = make_conv(d, e->head, w, bb, CL, 2 * cfg->latent_c, 1, 1, 1);
+  }
+  if (!s) {
+    cudaError_t ce = cudaDeviceSynchronize();
+    if (ce != cudaSuccess) s = set_err(&d->err, VAE_ERR_CUDA, 0, 0, "weight packing: %s", cudaGetErrorString(ce));
+  }
+  if (s) {
+    {
+      std::lock_guard<std::mutex> lk(g_last_mu);
+      g_last = d->err;
+    }
+    vae_encoder_destroy(e);
+    return s;
+  }
+  *out = e;
+  return VAE_OK;
+}
+
+#define ERRP (&e->core.err)
+extern "C" vae_status_t vae_encode(vae_encoder_t* e, const void* video, const int64_t shp[5], void* moments, int nph,
+                                   int npw, void* stream) {
+  if (!e) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null encoder");
+  if (!video || !moments) return set_err(&e->core.err, VAE_ERR_INVALID_ARG, 0, 0, "null video or moments");
+  if (!aligned16(video) || !aligned16(moments))
+    return set_err(&e->core.err, VAE_ERR_ALIGNMENT, 0, 0, "video/moments not 16-byte aligned");
+  vae_status_t s = check_video(e, shp, nph, npw);
+  if (s) return s;
+  EncPlan ep;
+  s = make_enc_plan(e, static_cast<int>(shp[0]), static_cast<int>(shp[2]), static_cast<int>(shp[3]),
+                    static_cast<int>(shp[4]), nph, npw, ep);
+  if (s) return s;
+  s = ensure_ws(&e->core, ep.p);
+  if (s) return s;
+  return run_encode(e, ep, static_cast<const float*>(video), static_cast<int>(shp[3]), static_cast<int>(shp[4]), 0, 0,
+                    static_cast<float*>(moments), static_cast<cudaStream_t>(stream));
+}
+
+extern "C" vae_status_t vae_encode_tiled(vae_encoder_t* e, const void* video, const int64_t shp[5], void* moments,
+                                         const int tile_hw[2], const int ovl_hw[2], void* stream) {
+  if (!e) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null encoder");
+  vae_decoder* d = &e->core;
+  if (!video || !moments || !tile_hw || !ovl_hw) return set_err(&d->err, VAE_ERR_INVALID_ARG, 0, 0, "null argument");
+  if (!aligned16(video) || !aligned16(moments))
+    return set_err(&d->err, VAE_ERR_ALIGNMENT, 0, 0, "video/moments not 16-byte aligned");
+  vae_status_t s = check_video(e, shp, 1, 1);
+  if (s) return s;
+  EncPlan whole;
+  s = make_enc_plan(e, static_cast<int>(shp[0]), static_cast<int>(shp[2]), static_cast<int>(shp[3]),
+                    static_cast<int>(shp[4]), 1, 1, whole);
+  if (s) return s;
+  const int B = static_cast<int>(shp[0]);
+  const int sh_tot = static_cast<int>(shp[3]) / whole.p.h, sw_tot = static_cast<int>(shp[4]) / whole.p.w;
+  const int lat[3] = {whole.p.Tlat, whole.p.h, whole.p.w};
+  const int tile[3] = {whole.p.Tlat, tile_hw[0], tile_hw[1]};
+  const int ovl[3] = {0, ovl_hw[0], ovl_hw[1]};
+  std::vector<vae_tile_t> tl(VAE_MAX_TILES);
+  int n = VAE_MAX_TILES;
+  s = vae_tile_plan(lat, tile, ovl, 1, 1, 0, tl.data(), &n);
+  if (s) return set_err(&d->err, s, 0, 0, "tile plan failed (%d tiles max)", VAE_MAX_TILES);
+  const int M = 2 * e->ecfg.latent_c;
+  size_t total = 0;
+  std::vector<size_t> off(n);
+  for (int i = 0; i < n; ++i) {
+    off[i] = total;
+    total += align_up(static_cast<size_t>(B) * M * tl[i].pix[1] * tl[i].pix[3] * tl[i].pix[5] * 4);
+  }
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  {
+    EncPlan pm;  // the first tile is the largest: size the workspace before anything is enqueued
+    s = make_enc_plan(e, B, static_cast<int>(shp[2]), tl[0].lat[3] * sh_tot, tl[0].lat[5] * sw_tot, 1, 1, pm);
+    if (!s) s = ensure_ws(d, pm.p);
+    if (s) return s;
+  }
+  if (d->tiles_bytes < total) {
+    CK(cudaDeviceSynchronize());
+    if (d->tiles) cudaFree(d->tiles);
+    d->tiles = nullptr;
+    d->tiles_bytes = 0;
+    CK(cudaMalloc(&d->tiles, total));
+    d->tiles_bytes = total;
+  }
+  char* base = static_cast<char*>(d->tiles);
+  std::vector<const void*> ptrs(n);
+  for (int i = 0; i < n; ++i) {
+    EncPlan ep;
+    s = make_enc_plan(e, B, static_cast<int>(shp[2]), tl[i].lat[3] * sh_tot, tl[i].lat[5] * sw_tot, 1, 1, ep);
+    if (!s) s = ensure_ws(d, ep.p);
+    if (!s)
+      s = run_encode(e, ep, static_cast<const float*>(video), static_cast<int>(shp[3]), static_cast<int>(shp[4]),
+                     tl[i].lat[2] * sh_tot, tl[i].lat[4] * sw_tot, reinterpret_cast<float*>(base + off[i]), strm);
+    if (s) return s;
+    ptrs[i] = base + off[i];
+  }
+  vae_blend_desc_t bd{};
+  bd.B = B; bd.C = M; bd.T = lat[0]; bd.H = lat[1]; bd.W = lat[2];
+  bd.tile_dtype = bd.out_dtype = VAE_FP32;
+  Prof pr(d, strm, K_BLEND, 0, 8.0 * B * M * lat[0] * lat[1] * lat[2]);
+  CK(launch_blend(ptrs.data(), tl.data(), n, moments, bd, strm));
+  return VAE_OK;
+}
+#undef ERRP
+
+extern "C" vae_status_t vae_encoder_profile(vae_encoder_t* e, int enable) {
+  if (!e) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null encoder");
+  return vae_decoder_profile(&e->core, enable);
+}
+
+extern "C" vae_status_t vae_encoder_profile_read(vae_encoder_t* e, vae_prof_t* out, int* n) {
+  if (!e) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null encoder");
+  return vae_decoder_profile_read(&e->core, out, n);
+}
+
+extern "C" vae_status_t vae_encoder_last_error(vae_encoder_t* e, vae_error_info_t* info) {
+  if (!e) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null encoder");
+  return vae_last_error(&e->core, info);
+}
 
 // ================================================================================ op level
 #define ERRP nullptr

@@ -318,6 +318,16 @@ VAE_DEV void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t* r) {
       : "r"(taddr)
       : "memory");
 }
+// 32 lanes x 16 consecutive 32-bit columns.
+VAE_DEV void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
 VAE_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 B, 8-row
@@ -329,21 +339,6 @@ VAE_DEV uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   d |= static_cast<uint64_t>(1024u >> 4) << 32;          // stride byte offset: 8 rows x 128 B
   d |= static_cast<uint64_t>(1u) << 46;                  // descriptor version
   d |= static_cast<uint64_t>(2u) << 61;                  // swizzle mode: 128 B
-  return d;
-}
-
-// Same layout with 8-row groups `sbo_bytes` apart, starting at any 128-byte row of a swizzled block
-// (the block itself 1024-byte aligned): the rows of a halo tile that one tap reads.  The 128-byte
-// swizzle follows the absolute shared-memory address bits, as the TMA that wrote the block applied
-// it, so the base-offset field stays 0 (measured: setting it to the start row's phase gives wrong
-// products).
-VAE_DEV uint64_t sdesc_kmajor_sw128_rows(uint32_t saddr, uint32_t sbo_bytes) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(1u) << 16;
-  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1u) << 46;
-  d |= static_cast<uint64_t>(2u) << 61;
   return d;
 }
 

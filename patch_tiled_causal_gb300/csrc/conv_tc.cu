@@ -27,10 +27,13 @@
 // half of the weight tile into its own shared memory; two 64-channel k blocks per stage where they
 // fit).  Other weight widths and batched GEMMs run one CTA per tile, each loading its whole weight
 // tile.  Every operand load is a plain TMA load into the issuing CTA's shared memory.
-// Convs at most 32 channels wide (a pixel head) use halo mode: one (rows_t + 2) x (cols_t + 2) box
-// per (kt, channel chunk) feeds all 9 spatial taps through row-offset operand descriptors.  The
-// producer and the MMA issuer advance ring slot, phase and tap with counters (no divisions on
-// their single-thread critical paths).
+// Convs at most 64 channels wide (the Wan pixel head, 64-channel stages) use halo mode: one box of (rows_t + 2) rows of 16
+// pixels per (kt, channel chunk) feeds all 9 spatial taps.  The three horizontal taps are stacked
+// along N (one MMA of N = 3 x BN per tap row kh, its A rows starting kh box rows down), so each A row
+// read from shared memory serves three taps; accumulator row m then holds, for box pixel m, its
+// contribution to the outputs one and two columns to its left, and the epilogue adds rows m, m + 1
+// and m + 2 (same 16-lane half-warp) with warp shuffles.  The producer and the MMA issuer advance
+// ring slot, phase and tap with counters (no divisions on their single-thread critical paths).
 #include <cuda.h>
 
 #include <algorithm>
@@ -58,8 +61,9 @@ struct TcParams {
   int N_real, BN, n_ntiles, tmem_cols, stages;
   int msub;  // 128-pixel MMA sub-tiles per tile (2 when BN <= 128: both share each weight tile)
   int ks;    // k blocks (64 channels of one tap) per shared-memory stage: 1 or 2
-  // halo mode (narrow convs): one stage = one (kt, 64-channel chunk) halo box of (rows_t + 2) x
-  // (cols_t + 2) pixels that all 9 spatial taps read in place, plus those taps' weight tiles
+  // halo mode (narrow convs): one stage = one (kt, 64-channel chunk) halo box of (rows_t + 2) x 16
+  // pixels (rows_t = 8 x msub output rows of cols_t = 14 pixels) that all 9 spatial taps read in place,
+  // plus those taps' weight tiles ([kh][kw][BN rows]: the 3 kw tiles of one kh form one N = 3 BN operand)
   int halo;
   uint32_t halo_a_bytes, halo_tx, halo_stage;
   const float* bias;
@@ -243,10 +247,13 @@ VAE_DEV void epilogue_chunk(const TcParams& p, const TileCoord& tc, int m, int n
     }
     return;
   }
-  // ---- conv epilogue
-  const int h = tc.h0 + m / p.cols_t;
-  const int w = tc.w0 + m % p.cols_t;
-  const bool valid = (h < tc.h_end) && (w < tc.w_end);
+  // ---- conv epilogue (halo mode: row m = box pixel (m / 16, m % 16) of the sub-tiles; columns 14, 15
+  // of each box row are halo and store nothing)
+  const int hm = p.halo ? (m >> 4) : m / p.cols_t;
+  const int wm = p.halo ? (m & 15) : m % p.cols_t;
+  const int h = tc.h0 + hm;
+  const int w = tc.w0 + wm;
+  const bool valid = (h < tc.h_end) && (w < tc.w_end) && wm < p.cols_t;
   const bool vec = !p.out_ncthw && (p.C_d2s % 32 == 0);
   if (vec) {
     const int sub = nb / p.C_d2s;
@@ -355,7 +362,9 @@ VAE_DEV void epilogue_chunk(const TcParams& p, const TileCoord& tc, int m, int n
 // tile; the leader's full barrier counts both CTAs' bytes, the leader alone issues the MMAs, and its
 // commits free the stage and hand the accumulator to the epilogues in both CTAs.  Each SM then takes
 // in half as many weight bytes per MMA as a CTA that holds the whole weight tile.
-template <bool kPair>
+// kF8: e4m3 operands (kind::f8f6f4); a template parameter so the bf16 kernel's single-thread MMA issue
+// loop carries no test of it.
+template <bool kPair, bool kF8>
 __global__ void __launch_bounds__(kThreads, 1)
     conv_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ TcParams p) {
@@ -542,14 +551,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (!kPair) {
       if (p.halo) {
         if (lane == 0) {
-          // A rows of tap (kh, kw) for sub-tile `sub`: box row (sub * rows_t / 2 + kh) * (cols_t + 2) + kw
-          // onward, one 8-pixel output row per 8-row group, groups one box row apart
-          const uint32_t idesc = idesc_bf16_f32(kBlockM, static_cast<uint32_t>(p.BN));
-          const int stages = p.stages, num_st = 3 * p.cchunks;
+          // tap row kh, sub-tile sub: A = the 128 box pixels from box row sub * 8 + kh on (8 box rows of
+          // 16 pixels, 2048 B each, so every start is 1024-byte aligned), B = the kw = 0, 1, 2 weight tiles of
+          // kh (3 BN rows), D = 3 BN columns of the sub-tile's accumulator
+          const uint32_t n3 = 3u * static_cast<uint32_t>(p.BN);
+          const uint32_t idesc = idesc_bf16_f32(kBlockM, n3);
+          const int stages = p.stages, num_st = 3 * p.cchunks, msub = p.msub;
           const uint32_t smem_base = smem_u32(smem);
-          const uint32_t box_w = static_cast<uint32_t>(p.cols_t + 2);
-          const uint32_t sbo = box_w * 128u;
-          const uint32_t half_rows = static_cast<uint32_t>(p.rows_t / 2);
           const uint32_t wt_bytes = static_cast<uint32_t>(p.BN) * kBlockK * 2;
           int s = 0, it = 0;
           uint32_t ph = 0;
@@ -568,18 +576,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t a_addr = smem_base + static_cast<uint32_t>(s) * stage_bytes;
               const uint32_t b_addr = a_addr + p.halo_a_bytes;
 #pragma unroll 1
-              for (int t9 = 0; t9 < 9; ++t9) {
-                const uint32_t kh = static_cast<uint32_t>(t9 / 3), kw = static_cast<uint32_t>(t9 % 3);
-                const uint64_t bdesc = sdesc_kmajor_sw128(b_addr + static_cast<uint32_t>(t9) * wt_bytes);
-#pragma unroll
-                for (int sub = 0; sub < 2; ++sub) {
-                  const uint32_t row0 = (static_cast<uint32_t>(sub) * half_rows + kh) * box_w + kw;
-                  const uint64_t adesc = sdesc_kmajor_sw128_rows(a_addr + row0 * 128u, sbo);
-                  const uint32_t d_sub = d_tmem + static_cast<uint32_t>(sub * p.BN);
+              for (uint32_t kh = 0; kh < 3; ++kh) {
+                const uint64_t bdesc = sdesc_kmajor_sw128(b_addr + kh * 3u * wt_bytes);
+                for (int sub = 0; sub < msub; ++sub) {
+                  const uint32_t row0 = (static_cast<uint32_t>(sub) * 8u + kh) * 16u;
+                  const uint64_t adesc = sdesc_kmajor_sw128(a_addr + row0 * 128u);
+                  const uint32_t d_sub = d_tmem + static_cast<uint32_t>(sub) * n3;
 #pragma unroll
                   for (int k = 0; k < kBlockK / 16; ++k)
                     tc_mma_bf16(d_sub, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k),
-                                idesc, (st == 0 && t9 == 0 && k == 0) ? 0u : 1u);
+                                idesc, (st == 0 && kh == 0 && k == 0) ? 0u : 1u);
                 }
               }
               tc_commit(&empty_bar[s]);
@@ -595,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0 && (!kPair || rank == 0) && !halo) {
       const uint32_t mm = kPair ? 2 * kBlockM : kBlockM;
-      const bool fp8 = p.fp8 != 0;
+      constexpr bool fp8 = kF8;
       const uint32_t idesc = fp8 ? idesc_e4m3_f32(mm, static_cast<uint32_t>(p.BN)) : idesc_bf16_f32(mm, static_cast<uint32_t>(p.BN));
       const int stages = p.stages, num_st = p.num_kb / ks, msub = p.msub;
       const uint32_t smem_base = smem_u32(smem);
@@ -632,13 +638,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // advance 32 B along K inside the 128-byte swizzle atom: 16 bf16 or 32 e4m3 per MMA
                 const uint32_t accum = (first && k == 0) ? 0u : 1u;
                 const uint64_t ak = adesc + static_cast<uint64_t>(2 * k), bk = bdesc + static_cast<uint64_t>(2 * k);
-                if constexpr (kPair) {
-                  if (fp8) tc_mma_e4m3_pair(d_sub, ak, bk, idesc, accum);
-                  else tc_mma_bf16_pair(d_sub, ak, bk, idesc, accum);
-                } else {
-                  if (fp8) tc_mma_e4m3(d_sub, ak, bk, idesc, accum);
-                  else tc_mma_bf16(d_sub, ak, bk, idesc, accum);
-                }
+                if constexpr (kPair && fp8) tc_mma_e4m3_pair(d_sub, ak, bk, idesc, accum);
+                else if constexpr (kPair) tc_mma_bf16_pair(d_sub, ak, bk, idesc, accum);
+                else if constexpr (fp8) tc_mma_e4m3(d_sub, ak, bk, idesc, accum);
+                else tc_mma_bf16(d_sub, ak, bk, idesc, accum);
               }
             }
           }
@@ -664,6 +667,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const TileCoord tc = seq_coord(p, seq, rank);
       const int nchunks = (p.BN + 31) / 32;
+      if (!kPair && p.halo) {
+        // output (r, c) of the sub-tile = sum over kw of accumulator row (r, c + kw), columns kw * BN + n
+        const int n3 = 3 * p.BN;
+        for (int sub = 0; sub < p.msub; ++sub) {
+          for (int j = 0; j < nchunks; ++j) {
+            float v[32];
+#pragma unroll
+            for (int kw = 0; kw < 3; ++kw) {
+              uint32_t raw[32];
+              const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                     static_cast<uint32_t>(acc * acc_stride + sub * n3 + kw * p.BN + j * 32);
+              if (p.BN - j * 32 >= 32) {
+                tmem_ld_32x32b_x32(taddr, raw);
+              } else {
+                tmem_ld_32x32b_x16(taddr, raw);
+#pragma unroll
+                for (int i = 16; i < 32; ++i) raw[i] = 0u;
+              }
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                float f = __uint_as_float(raw[i]);
+                if (kw) f = __shfl_down_sync(0xffffffffu, f, kw);
+                v[i] = kw ? v[i] + f : f;
+              }
+            }
+            if (sub == p.msub - 1 && j == nchunks - 1) {
+              tc_fence_before();
+              mbar_arrive(&acce_bar[acc]);
+            }
+            const int nb = tc.n0 + j * 32;
+            if (nb < p.N_real) epilogue_chunk(p, tc, sub * kBlockM + m, nb, v, lane);
+          }
+        }
+        continue;
+      }
       for (int sub = 0; sub < p.msub; ++sub) {
         for (int j = 0; j < nchunks; ++j) {
           uint32_t raw[32];
@@ -767,12 +806,11 @@ namespace {
 // as one cta_group::2 MMA, each CTA holding half of the weight tile (measured on one GB300: op conv
 // 512->512 1311 -> 1386 TFLOP/s).
 bool mma_pair_enabled() { return true; }
-// Convs at most 32 channels wide (the Wan-shaped pixel head) load one halo box per (kt, channel chunk)
-// that the 9 spatial taps share, instead of 9 tap-shifted boxes (measured: 256->12 head on
-// 81x352x640 23.9 -> 16.4 ms; the 48-wide LTX head is slower that way, 3.7 -> 4.0 ms).
+// Convs at most 64 channels wide load one halo box per (kt, channel chunk) that the 9 spatial taps share,
+// and stack the 3 horizontal taps along N (measured on one GB300: Wan 256->12 head on 81x352x640
+// 16.35 -> 8.19 ms, 64->64 conv on 41x176x320 0.84 -> 0.51 ms).
 bool halo_mode_enabled() { return true; }
-constexpr int kHaloCols = 8;   // tile width: one 8-row MMA core group per output row
-constexpr int kHaloRows = 32;  // tile height: two 16-row sub-tiles of 128 pixels
+constexpr int kHaloCols = 14;  // output columns of a tile: box rows of 16 pixels (14 + 2 halo)
 }  // namespace
 
 namespace {
@@ -781,7 +819,8 @@ struct DevLaunch {
   bool ready = false;
   int n_sm = 0;
   int max_clusters = 0;          // clusters of 2 resident at once for the pair kernel ...
-  size_t max_clusters_smem = 0;  // ... at this dynamic shared-memory size
+  size_t max_clusters_smem = 0;  // ... at this dynamic shared-memory size ...
+  const void* max_clusters_kern = nullptr;  // ... for this kernel
 };
 std::mutex g_dev_mu;
 DevLaunch g_dev[64];
@@ -805,12 +844,16 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   p.kc = p.fp8 ? 128 : 64;
   if (p.fp8 && (a.mode != 0 || !a.wscale || a.C_in_pad % 128 != 0)) return cudaErrorInvalidValue;
   p.wscale = p.fp8 ? a.wscale : nullptr;
-  p.halo = (a.mode == 0 && p.BN <= 32 && !p.fp8 && halo_mode_enabled()) ? 1 : 0;
+  // (not for NCTHW pixel outputs of more than 16 channels: their scalar store epilogue then outlasts the
+  // shorter MMA phase; measured on one GB300: LTX 128->48 head 3.66 ms per tap, 5.73 ms in halo mode)
+  p.halo = (a.mode == 0 && p.BN <= 64 && !p.fp8 && (!a.out_ncthw || a.N_real <= 16) && halo_mode_enabled()) ? 1 : 0;
+  // halo mode: sub-tiles of 8 x 16 box pixels; two accumulators of msub x 3 BN columns must fit TMEM
+  if (p.halo) p.msub = 2 * 2 * 3 * p.BN <= 512 ? 2 : 1;
   const bool mma_pair =
       mma_pair_enabled() && (p.BN == 256 || p.BN == 128) && (a.mode == 0 || a.batch == 1) && !p.halo;
   const bool want_pair = mma_pair;
   p.tmem_cols = 32;
-  while (p.tmem_cols < 2 * p.msub * p.BN) p.tmem_cols <<= 1;  // two accumulators
+  while (p.tmem_cols < 2 * p.msub * (p.halo ? 3 * p.BN : p.BN)) p.tmem_cols <<= 1;  // two accumulators
   if (p.tmem_cols > 512) return cudaErrorInvalidValue;
   const uint32_t kb_bytes = kABytes * p.msub + static_cast<uint32_t>(mma_pair ? p.BN / 2 : p.BN) * kBlockK * 2;
   // MMA pairs take two k blocks per stage (half the barrier round trips per MMA) where two such stages
@@ -820,8 +863,8 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   p.ks = (mma_pair && kb_even && 2u * 2u * kb_bytes <= 200u * 1024u) ? 2 : 1;
   uint32_t stage_bytes = static_cast<uint32_t>(p.ks) * kb_bytes;
   if (p.halo) {
-    // box of (32 + 2) x (8 + 2) pixels x 64 channels, then the 9 taps' BN x 64 weight tiles
-    const uint32_t box = static_cast<uint32_t>(kHaloRows + 2) * (kHaloCols + 2) * kBlockK * 2;
+    // box of (8 msub + 2) x 16 pixels x 64 channels, then the 9 taps' BN x 64 weight tiles
+    const uint32_t box = static_cast<uint32_t>(8 * p.msub + 2) * (kHaloCols + 2) * kBlockK * 2;
     p.halo_a_bytes = (box + 1023u) & ~1023u;
     p.halo_tx = box + 9u * static_cast<uint32_t>(p.BN) * kBlockK * 2;
     p.halo_stage = p.halo_a_bytes + 9u * static_cast<uint32_t>(p.BN) * kBlockK * 2;
@@ -849,7 +892,7 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
     for (int i = 0; i <= a.nph; ++i) p.ph_edges[i] = a.ph_edges[i];
     for (int j = 0; j <= a.npw; ++j) p.pw_edges[j] = a.pw_edges[j];
     p.cols_t = p.halo ? kHaloCols : pick_cols(a.pw_edges, a.npw);
-    p.rows_t = kBlockM * p.msub / p.cols_t;
+    p.rows_t = p.halo ? 8 * p.msub : kBlockM * p.msub / p.cols_t;
     p.trow_prefix[0] = 0;
     for (int i = 0; i < a.nph; ++i)
       p.trow_prefix[i + 1] = p.trow_prefix[i] + (a.ph_edges[i + 1] - a.ph_edges[i] + p.rows_t - 1) / p.rows_t;
@@ -934,7 +977,8 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
     if (!dl.ready) {
       if (cudaDeviceGetAttribute(&dl.n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || dl.n_sm <= 0)
         dl.n_sm = 148;
-      for (auto* k : {conv_tc_kernel<false>, conv_tc_kernel<true>}) {
+      for (auto* k : {conv_tc_kernel<false, false>, conv_tc_kernel<true, false>, conv_tc_kernel<false, true>,
+                      conv_tc_kernel<true, true>}) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
       }
@@ -959,11 +1003,12 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   if (!p.pair) {
     p.seq_count = p.n_tiles;
     const long long grid = std::min<long long>(n_blocks, n_sm);
-    conv_tc_kernel<false><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmA, tmB, p);
+    if (p.fp8) conv_tc_kernel<false, true><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmA, tmB, p);
+    else conv_tc_kernel<false, false><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmA, tmB, p);
     return cudaGetLastError();
   }
   p.seq_count = (p.n_mtiles + 1) / 2 * p.n_ntiles;
-  auto* kern = conv_tc_kernel<true>;
+  auto* kern = p.fp8 ? conv_tc_kernel<true, true> : conv_tc_kernel<true, false>;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -979,12 +1024,14 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
     DevLaunch& dl = g_dev[dev];
-    if (dl.max_clusters <= 0 || dl.max_clusters_smem != smem) {
+    if (dl.max_clusters <= 0 || dl.max_clusters_smem != smem ||
+        dl.max_clusters_kern != reinterpret_cast<const void*>(kern)) {
       cfg.gridDim = dim3(2 * (n_sm / 2));
       int mc = 0;
       if (cudaOccupancyMaxActiveClusters(&mc, kern, &cfg) != cudaSuccess || mc <= 0) mc = n_sm / 2;
       dl.max_clusters = mc;
       dl.max_clusters_smem = smem;
+      dl.max_clusters_kern = reinterpret_cast<const void*>(kern);
     }
     max_clusters = dl.max_clusters;
   }

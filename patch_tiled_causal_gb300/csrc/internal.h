@@ -102,6 +102,21 @@ cudaError_t launch_latent_to_cl(const float* z, int B, int C, int T, int H, int 
                                 int nw, int C_pad, void* y, int y_f32, int y_T_alloc, cudaStream_t s);
 cudaError_t launch_d2s(const void* x, void* y, int B, int T, int H, int W, int C, int st, int sh, int sw,
                        int drop_first, int f32, cudaStream_t s);
+// Pixels NCTHW fp32 [B, C, T, H, W] -> channels-last [B, y_T_alloc, nh, nw, C_pad] (frames 0..T-1) of
+// the space-to-depth box (h0, nh, w0, nw in folded units) with fold (1, ph, pw): channel
+// c*ph*pw + dy*pw + dx <- pixel (c, t, ph*(h0+y)+dy, pw*(w0+x)+dx); channels >= C*ph*pw are 0.
+// y_kind: 0 bf16, 1 fp32, 2 e4m3.
+cudaError_t launch_pixels_to_cl(const float* v, int B, int C, int T, int H, int W, int ph, int pw, int h0, int nh,
+                                int w0, int nw, int C_pad, void* y, int y_kind, int y_T_alloc, cudaStream_t s);
+// Causal space-to-depth of a channels-last tensor [B, x_T_alloc, H, W, C] (frames 0..T-1) into
+// [B, y_T_alloc, H/sh, W/sw, C*st*sh*sw]: channel c*S + dt*sh*sw + dy*sw + dx of output frame t' <- input
+// (max(st*t' + dt - (st-1), 0), sh*y+dy, sw*x+dx, c); (T + st - 1) / st output frames.
+cudaError_t launch_fold_frames(const void* x, int x_f32, int x_T_alloc, int B, int T, int H, int W, int C, int st,
+                               int sh, int sw, void* y, int y_kind, int y_T_alloc, cudaStream_t s);
+// The stride-2 down-sampler's weights w [C_out, C_in, 3, 3] as a stride-1 3x3x3 causal conv over the
+// (1,2,2)-folded input: out [C_out, 4*C_in, 3, 3, 3] with out[o, c*4 + dy*2 + dx, 2, kh, kw] =
+// w[o, c, 2(kh-1)+dy, 2(kw-1)+dx] for kh, kw >= 1 where that index is <= 2, and 0 elsewhere.
+cudaError_t launch_stride2_weights(const float* w, int C_out, int C_in, float* out, cudaStream_t s);
 cudaError_t launch_copy_frames(const void* src, int src_T, int src_t0, void* dst, int dst_T, int dst_t0, int n_frames,
                                int B, int64_t frame_bytes, cudaStream_t s);
 

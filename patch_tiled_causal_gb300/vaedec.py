@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libvaedec.so")
 
 VAE_OK, VAE_ERR_INVALID_ARG, VAE_ERR_UNSUPPORTED, VAE_ERR_PATCH_TOO_NARROW = 0, 1, 2, 3
 VAE_ERR_ALIGNMENT, VAE_ERR_OOM, VAE_ERR_CUDA, VAE_ERR_TIMEOUT, VAE_ERR_RANGE = 4, 5, 6, 7, 8
-VAE_BF16, VAE_FP32 = 0, 1
+VAE_BF16, VAE_FP32, VAE_FP8 = 0, 1, 2
 VAE_NORM_GROUP, VAE_NORM_CHANNEL_RMS = 0, 1
 MAX_STAGES, MAX_PATCHES, MAX_TILES = 8, 64, 512
 
@@ -33,6 +33,18 @@ class VaeConfig(C.Structure):
                 ("up_w", C.c_int * MAX_STAGES), ("mid_res", C.c_int), ("mid_attn", C.c_int),
                 ("gn_groups", C.c_int), ("gn_eps", C.c_float), ("out_c", C.c_int), ("out_d2s_t", C.c_int),
                 ("out_d2s_h", C.c_int), ("out_d2s_w", C.c_int), ("dtype", C.c_int), ("norm_type", C.c_int)]
+
+
+VAE_DOWN_FOLD, VAE_DOWN_STRIDE = 0, 1
+
+
+class VaeEncoderConfig(C.Structure):
+    _fields_ = [("pix_c", C.c_int), ("patch_h", C.c_int), ("patch_w", C.c_int), ("n_stages", C.c_int),
+                ("stage_c", C.c_int * MAX_STAGES), ("n_res", C.c_int * MAX_STAGES),
+                ("down_kind", C.c_int * MAX_STAGES), ("down_t", C.c_int * MAX_STAGES),
+                ("down_h", C.c_int * MAX_STAGES), ("down_w", C.c_int * MAX_STAGES), ("mid_res", C.c_int),
+                ("gn_groups", C.c_int), ("gn_eps", C.c_float), ("latent_c", C.c_int), ("dtype", C.c_int),
+                ("norm_type", C.c_int)]
 
 
 class VaeErrorInfo(C.Structure):
@@ -108,6 +120,14 @@ _SIGS = {
     "vae_gemm_bf16": (C.c_int, [_P, _P, _P, _P, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int64, C.c_int64,
                                 C.c_int64, C.c_float, C.c_int, _P]),
     "vae_watchdog_selftest": (C.c_int, [C.c_int, _P]),
+    "vae_encoder_n_weights": (C.c_int, [C.POINTER(VaeEncoderConfig), C.POINTER(C.c_int)]),
+    "vae_encoder_create": (C.c_int, [C.POINTER(VaeEncoderConfig), C.POINTER(_P), C.c_int, C.POINTER(_P)]),
+    "vae_encoder_destroy": (None, [_P]),
+    "vae_encode": (C.c_int, [_P, _P, C.POINTER(C.c_int64), _P, C.c_int, C.c_int, _P]),
+    "vae_encode_tiled": (C.c_int, [_P, _P, C.POINTER(C.c_int64), _P, C.POINTER(C.c_int), C.POINTER(C.c_int), _P]),
+    "vae_encoder_profile": (C.c_int, [_P, C.c_int]),
+    "vae_encoder_profile_read": (C.c_int, [_P, C.POINTER(VaeProf), C.POINTER(C.c_int)]),
+    "vae_encoder_last_error": (C.c_int, [_P, C.POINTER(VaeErrorInfo)]),
 }
 
 _lib: Optional[C.CDLL] = None
@@ -141,10 +161,13 @@ class VaeError(RuntimeError):
         super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} {msg}".strip())
 
 
-def _check(code: int, where: str, dec=None):
+def _check(code: int, where: str, dec=None, enc=None):
     if code != VAE_OK:
         info = VaeErrorInfo()
-        load().vae_last_error(dec, C.byref(info))
+        if enc is not None:
+            load().vae_encoder_last_error(enc, C.byref(info))
+        else:
+            load().vae_last_error(dec, C.byref(info))
         raise VaeError(code, info, where)
 
 
@@ -181,7 +204,9 @@ def _ptr(t, dtype=None) -> Optional[int]:
 
 def _dt(t) -> int:
     torch = _torch()
-    return VAE_FP32 if t.dtype == torch.float32 else VAE_BF16
+    if t.dtype == torch.float32:
+        return VAE_FP32
+    return VAE_FP8 if t.dtype == torch.float8_e4m3fn else VAE_BF16
 
 
 def _edges_array(edges: Sequence[int]):
@@ -486,4 +511,98 @@ class Decoder:
         _check(load().vae_decode_tiled(self.h, _ptr(latent, torch.float32), shp, _ptr(out, self.out_dtype()),
                                        (C.c_int * 3)(*tile_thw), (C.c_int * 3)(*ovl_thw), _stream(stream)),
                "vae_decode_tiled", self.h)
+        return out
+
+
+# --------------------------------------------------------------------------- encoder
+def make_encoder_config(cfg, dtype: int = VAE_BF16) -> VaeEncoderConfig:
+    """VaeEncoderConfig from a ``synth.EncoderConfig``."""
+    c = VaeEncoderConfig()
+    c.pix_c = cfg.pix_c
+    c.patch_h, c.patch_w = cfg.patchify
+    c.n_stages = cfg.n_stages
+    for i, ch in enumerate(cfg.stage_c):
+        c.stage_c[i] = ch
+        c.n_res[i] = cfg.n_res[i]
+    for i, (kind, f) in enumerate(cfg.down):
+        c.down_kind[i] = VAE_DOWN_FOLD if kind == "fold" else VAE_DOWN_STRIDE
+        c.down_t[i], c.down_h[i], c.down_w[i] = f
+    c.mid_res = cfg.mid_res
+    c.gn_groups, c.gn_eps = cfg.gn_groups, cfg.gn_eps
+    c.latent_c = cfg.latent_c
+    c.dtype = dtype
+    c.norm_type = VAE_NORM_CHANNEL_RMS if cfg.norm == "rms" else VAE_NORM_GROUP
+    return c
+
+
+class Encoder:
+    """A libvaedec encoder handle built from a config and fp32 parameter tensors (by name)."""
+
+    def __init__(self, cfg, params: Dict[str, "object"], dtype: int = VAE_BF16, device="cuda"):
+        torch = _torch()
+        lib = load()
+        self.cfg = cfg
+        self.dtype = dtype
+        self.c = make_encoder_config(cfg, dtype)
+        names = param_order(cfg)
+        dev = [params[n] if isinstance(params[n], torch.Tensor) else torch.from_numpy(np.ascontiguousarray(params[n]))
+               for n in names]
+        dev = [t.to(device=device, dtype=torch.float32).contiguous() for t in dev]
+        n = C.c_int(0)
+        _check(lib.vae_encoder_n_weights(C.byref(self.c), C.byref(n)), "vae_encoder_n_weights")
+        if n.value != len(dev):
+            raise ValueError(f"library expects {n.value} parameters, config lists {len(dev)}")
+        arr = (_P * len(dev))(*[t.data_ptr() for t in dev])
+        h = _P()
+        _check(lib.vae_encoder_create(C.byref(self.c), arr, len(dev), C.byref(h)), "vae_encoder_create")
+        self.h = h
+        del dev
+
+    def close(self):
+        if getattr(self, "h", None):
+            load().vae_encoder_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def output_shape(self, video_shape):
+        return self.cfg.latent_shape(video_shape)
+
+    def last_error(self) -> Tuple[int, str]:
+        info = VaeErrorInfo()
+        code = load().vae_encoder_last_error(self.h, C.byref(info))
+        return code, info.message.decode(errors="replace")
+
+    def profile(self, enable: bool):
+        _check(load().vae_encoder_profile(self.h, int(enable)), "vae_encoder_profile", enc=self.h)
+
+    def profile_read(self) -> Dict[str, dict]:
+        arr = (VaeProf * 32)()
+        n = C.c_int(32)
+        _check(load().vae_encoder_profile_read(self.h, arr, C.byref(n)), "vae_encoder_profile_read", enc=self.h)
+        return {arr[i].name.decode(): {"launches": arr[i].launches, "ms": arr[i].ms, "flops": arr[i].flops,
+                                        "bytes": arr[i].bytes} for i in range(n.value)}
+
+    def encode(self, video, out=None, n_patch_h=1, n_patch_w=1, stream=None):
+        """Pixels [B, C, T, H, W] fp32 -> moments [B, 2*latent_c, T', h, w] fp32 (vae_encode)."""
+        torch = _torch()
+        if out is None:
+            out = torch.empty(self.output_shape(video.shape), dtype=torch.float32, device=video.device)
+        shp = (C.c_int64 * 5)(*video.shape)
+        _check(load().vae_encode(self.h, _ptr(video, torch.float32), shp, _ptr(out, torch.float32), n_patch_h,
+                                 n_patch_w, _stream(stream)), "vae_encode", enc=self.h)
+        return out
+
+    def encode_tiled(self, video, tile_hw, ovl_hw, out=None, stream=None):
+        torch = _torch()
+        if out is None:
+            out = torch.empty(self.output_shape(video.shape), dtype=torch.float32, device=video.device)
+        shp = (C.c_int64 * 5)(*video.shape)
+        _check(load().vae_encode_tiled(self.h, _ptr(video, torch.float32), shp, _ptr(out, torch.float32),
+                                       (C.c_int * 2)(*tile_hw), (C.c_int * 2)(*ovl_hw), _stream(stream)),
+               "vae_encode_tiled", enc=self.h)
         return out

@@ -73,7 +73,8 @@ def test_invalid_arguments_are_refused(lib):
 # ctypes mirrors of the header's structs, checked field by field against the C compiler's layout
 STRUCTS = [("VaeConfig", "vae_config_t"), ("VaeErrorInfo", "vae_error_info_t"), ("VaeTile", "vae_tile_t"),
            ("VaeConvDesc", "vae_conv_desc_t"), ("VaeGnDesc", "vae_gn_desc_t"), ("VaeRmsDesc", "vae_rms_desc_t"),
-           ("VaeD2sDesc", "vae_d2s_desc_t"), ("VaeBlendDesc", "vae_blend_desc_t"), ("VaeProf", "vae_prof_t")]
+           ("VaeD2sDesc", "vae_d2s_desc_t"), ("VaeBlendDesc", "vae_blend_desc_t"), ("VaeProf", "vae_prof_t"),
+           ("VaeEncoderConfig", "vae_encoder_config_t")]
 
 
 def test_binding_structs_match_header_layout(tmp_path):
@@ -128,3 +129,20 @@ def test_config_checks_for_both_norm_families(lib):
     c = vaedec.make_config(synth.MINI_WAN)
     c.gn_groups = 0  # group norms need groups
     assert lib.vae_decoder_n_weights(C.byref(c), C.byref(n)) == vaedec.VAE_ERR_INVALID_ARG
+
+
+def test_encoder_config_checks(lib):
+    # host-only validation (no GPU): vae_encoder_n_weights checks the config first
+    import ctypes as C
+    from patch_tiled_causal_gb300 import synth
+    n = C.c_int(0)
+    for name, cfg in synth.ENCODERS.items():
+        c = vaedec.make_encoder_config(cfg)
+        assert lib.vae_encoder_n_weights(C.byref(c), C.byref(n)) == vaedec.VAE_OK, name
+        assert n.value == len(vaedec.param_order(cfg)), name
+    bad = vaedec.make_encoder_config(synth.MINI_ENC_STRIDE)
+    bad.down_h[0] = 3  # the strided down-sampler halves rows and columns only
+    assert lib.vae_encoder_n_weights(C.byref(bad), C.byref(n)) == vaedec.VAE_ERR_UNSUPPORTED
+    bad = vaedec.make_encoder_config(synth.MINI_ENC)
+    bad.down_kind[0] = 7
+    assert lib.vae_encoder_n_weights(C.byref(bad), C.byref(n)) == vaedec.VAE_ERR_INVALID_ARG

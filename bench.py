@@ -228,11 +228,16 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the LTX-shaped and tiled decode sub-lines")
     ap.add_argument("--only", default="all", choices=["all", "decode", "ops"],
                     help="run only the decode or only the op workloads (profiling runs)")
+    ap.add_argument("--latent-frames", type=int, default=0,
+                    help="decode only the first N latent frames (0: all; small values for profiler captures)")
     ap.add_argument("--ops-frames", type=int, default=0,
                     help="frames of the op workloads (0: the full sizes; small values for profiler captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     cfg = {"wan": synth.WAN, "ltx": synth.LTX, "wan_rms": synth.WAN_RMS}[args.workload]
+    if args.latent_frames:
+        shp = cfg.latent_shape
+        cfg = dataclasses.replace(cfg, latent_shape=(shp[0], shp[1], args.latent_frames, shp[3], shp[4]))
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -110,6 +110,7 @@ struct ConvL {
   int C_in = 0, C_out = 0, C_in_pad = 0, N_pad = 0, st = 1, sh = 1, sw = 1;
   bool tc = false;
   bool fp8 = false;        // e4m3 operands and weights (fp8 decoders)
+  bool natural = false;    // weight rows in PyTorch channel order (convs that store NCTHW pixels)
   float* wscale = nullptr; // fp8: per-output-channel weight scales (inside the packed weight buffer)
   void* w = nullptr;       // packed weights
   float* bias = nullptr;   // fp32 [C_out]
@@ -223,7 +224,7 @@ int res_bytes(const vae_decoder* d) { return (d->f32 || kResidF32) ? 4 : 2; }
 int c1_bytes(const vae_decoder* d) { return (d->f32 || kC1F32) ? 4 : 2; }
 
 vae_status_t make_conv(vae_decoder* d, ConvL& c, const float* w, const float* b, int C_in, int C_out, int st, int sh,
-                       int sw, bool pad_input = false, bool allow_fp8 = false) {
+                       int sw, bool pad_input = false, bool allow_fp8 = false, bool natural = false) {
   c.C_in = C_in;
   c.C_out = C_out;
   c.st = st; c.sh = sh; c.sw = sw;
@@ -233,19 +234,20 @@ vae_status_t make_conv(vae_decoder* d, ConvL& c, const float* w, const float* b,
   c.tc = !d->f32 && (C_in % 64 == 0 || pad_input);
   c.C_in_pad = c.tc ? round_up(C_in, 64) : C_in;
   c.fp8 = d->f8 && allow_fp8 && c.tc && C_in % 128 == 0;
+  c.natural = natural;
   if (c.fp8) {
     c.N_pad = round_up(C_out, 16);
     const size_t off = fp8_scale_offset(c.N_pad, c.C_in_pad);
     vae_status_t s = dalloc(d, &c.w, off + static_cast<size_t>(c.N_pad) * 4);
     if (s) return s;
     c.wscale = reinterpret_cast<float*>(static_cast<char*>(c.w) + off);
-    CK(launch_pack_weights_fp8(w, C_out, C_in, c.C_in_pad, c.N_pad, S, c.w, nullptr));
+    CK(launch_pack_weights_fp8(w, C_out, C_in, c.C_in_pad, c.N_pad, S, c.w, nullptr, natural));
   } else if (c.tc) {
     c.N_pad = C_out <= 256 ? round_up(C_out, 16) : round_up(C_out, 16);
     const size_t bytes = static_cast<size_t>(c.N_pad) * 27 * c.C_in_pad * 2;
     vae_status_t s = dalloc(d, &c.w, bytes);
     if (s) return s;
-    CK(launch_pack_weights_bf16(w, C_out, C_in, c.C_in_pad, c.N_pad, S, c.w, nullptr));
+    CK(launch_pack_weights_bf16(w, C_out, C_in, c.C_in_pad, c.N_pad, S, c.w, nullptr, natural));
   } else {
     const size_t bytes = 27ull * C_in * C_out * 4;
     vae_status_t s = dalloc(d, &c.w, bytes);
@@ -412,7 +414,9 @@ extern "C" vae_status_t vae_decoder_create(const vae_config_t* cfg, const void* 
     const float* w = W();
     const float* bb = W();
     const int S = cfg->out_d2s_t * cfg->out_d2s_h * cfg->out_d2s_w;
-    if (!s) s = make_conv(d, d->head, w, bb, CL, cfg->out_c * S, cfg->out_d2s_t, cfg->out_d2s_h, cfg->out_d2s_w);
+    if (!s)
+      s = make_conv(d, d->head, w, bb, CL, cfg->out_c * S, cfg->out_d2s_t, cfg->out_d2s_h, cfg->out_d2s_w, false, false,
+                    true);
   }
   if (!s) {
     cudaError_t e = cudaDeviceSynchronize();
@@ -633,7 +637,7 @@ vae_status_t run_conv(Ctx& x, ConvL& c, const Level& L, char* in, const ConvOut&
     a.residual = residual; a.res_f32 = res_f32; a.res_T_alloc = T;
     a.y = y; a.out_f32 = y_f32; a.out_ncthw = out_ncthw; a.y_T_alloc = y_T_alloc;
     a.d2s_t = c.st; a.d2s_h = c.sh; a.d2s_w = c.sw; a.drop_first = drop_first;
-    a.fp8 = c.fp8; a.wscale = c.wscale;
+    a.fp8 = c.fp8; a.wscale = c.wscale; a.natural = c.natural;
     const int Cd = c.C_out / (c.st * c.sh * c.sw);
     const int G = d->cfg.gn_groups;  // (ignored, possibly 0, by channel-RMS decoders)
     const int cpg = (G > 0 && Cd % G == 0) ? Cd / G : 0;
@@ -1456,7 +1460,7 @@ extern "C" vae_status_t vae_encoder_create(const vae_encoder_config_t* cfg, cons
     s = make_norm(d, e->head_norm, g, b, CL);
     const float* w = W();
     const float* bb = W();
-    if (!s) s = make_conv(d, e->head, w, bb, CL, 2 * cfg->latent_c, 1, 1, 1);
+    if (!s) s = make_conv(d, e->head, w, bb, CL, 2 * cfg->latent_c, 1, 1, 1, false, false, true);
   }
   if (!s) {
     cudaError_t ce = cudaDeviceSynchronize();
@@ -1603,8 +1607,10 @@ extern "C" vae_status_t vae_conv3d_pack_weights(const float* w, const vae_conv_d
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (conv_fp8(d) && d->C_in % 128)
     return set_err(nullptr, VAE_ERR_UNSUPPORTED, 0, 0, "fp8 convs need C_in %% 128 == 0 (got %d)", d->C_in);
-  if (conv_fp8(d)) CK(launch_pack_weights_fp8(w, d->C_out, d->C_in, d->C_in, conv_npad(d), S, w_packed, s));
-  else if (conv_tc_ok(d)) CK(launch_pack_weights_bf16(w, d->C_out, d->C_in, d->C_in, conv_npad(d), S, w_packed, s));
+  if (conv_fp8(d))
+    CK(launch_pack_weights_fp8(w, d->C_out, d->C_in, d->C_in, conv_npad(d), S, w_packed, s, d->out_ncthw));
+  else if (conv_tc_ok(d))
+    CK(launch_pack_weights_bf16(w, d->C_out, d->C_in, d->C_in, conv_npad(d), S, w_packed, s, d->out_ncthw));
   else CK(launch_pack_weights_f32(w, d->C_out, d->C_in, w_packed, s));
   return VAE_OK;
 }
@@ -1645,6 +1651,7 @@ extern "C" vae_status_t vae_conv3d_causal(const void* x, const void* w_packed, c
     a.residual = residual; a.res_f32 = d->res_dtype == VAE_FP32;
     a.y = y; a.out_f32 = d->out_dtype == VAE_FP32; a.out_ncthw = d->out_ncthw;
     a.d2s_t = d->d2s_t; a.d2s_h = d->d2s_h; a.d2s_w = d->d2s_w; a.drop_first = d->drop_first;
+    a.natural = d->out_ncthw;
     CK(launch_conv_tc(a, s));
   } else {
     ConvSimtArgs a{};

@@ -80,6 +80,7 @@ struct TcParams {
   int fp8;           // e4m3 operands (kind::f8f6f4); kc = channels per 128-byte k block (64 bf16, 128 e4m3)
   int kc;
   const float* wscale;  // fp8: per-output-channel weight scale (packed row order)
+  int natural;       // weight rows (and so accumulator columns) in PyTorch channel order c * S + sub
   int n_tiles;
   int pair;          // 1: CTAs run in clusters of 2 on adjacent M tiles of one N tile as one cta_group::2
                      // MMA, each loading half of the weight tile into its own shared memory
@@ -212,6 +213,54 @@ VAE_DEV void gn_chunk_sums(const TcParams& p, const TileCoord& tc, const float* 
   }
 }
 
+// NCTHW pixels with the natural channel order n = c*S + dt*sh*sw + dy*sw + dx: each run of SW columns is a
+// segment of SW horizontally adjacent output pixels of one (c, frame, row), stored as one vector (coalesced
+// across the warp, whose lanes hold adjacent input columns).
+template <int SW>
+VAE_DEV void ncthw_store_runs(const TcParams& p, const TileCoord& tc, int h, int w, int nb, const float* v) {
+  const int sh = p.d2s_h;
+#pragma unroll
+  for (int i = 0; i < 32; i += SW) {
+    const int n = nb + i;
+    if (n >= p.N_real) break;
+    const int c = n / p.S, sub = n - c * p.S;
+    const int dt = sub / (sh * SW), dy = (sub - dt * sh * SW) / SW;
+    const int to = p.d2s_t * tc.t + dt - p.drop;
+    if (to < 0) continue;
+    float o[SW];
+#pragma unroll
+    for (int dx = 0; dx < SW; ++dx)
+      o[dx] = v[i + dx] * (p.wscale ? p.wscale[n + dx] : 1.f) + (p.bias ? p.bias[n + dx] : 0.f);
+    if (p.residual) {  // (depth-to-space factor 1 only)
+      const int64_t ridx = (((static_cast<int64_t>(tc.b) * p.res_T_alloc + tc.t) * p.H + h) * p.W + w) * p.N_real + n;
+#pragma unroll
+      for (int dx = 0; dx < SW; ++dx)
+        o[dx] += p.res_f32 ? static_cast<const float*>(p.residual)[ridx + dx]
+                           : bf2f(static_cast<const __nv_bfloat16*>(p.residual)[ridx + dx]);
+    }
+    const int64_t oidx =
+        (((static_cast<int64_t>(tc.b) * p.C_d2s + c) * p.y_T_alloc + to) * p.H_out + (h * sh + dy)) * p.W_out + w * SW;
+    if (p.out_f32) {
+      float* y = static_cast<float*>(p.y) + oidx;
+      if constexpr (SW == 4) *reinterpret_cast<float4*>(y) = make_float4(o[0], o[1], o[2], o[3]);
+      else if constexpr (SW == 2) *reinterpret_cast<float2*>(y) = make_float2(o[0], o[1]);
+      else y[0] = o[0];
+    } else {
+      __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y) + oidx;
+      if constexpr (SW == 4) {
+        uint2 u;
+        reinterpret_cast<__nv_bfloat162*>(&u)[0] = __floats2bfloat162_rn(o[0], o[1]);
+        reinterpret_cast<__nv_bfloat162*>(&u)[1] = __floats2bfloat162_rn(o[2], o[3]);
+        *reinterpret_cast<uint2*>(y) = u;
+      } else if constexpr (SW == 2) {
+        *reinterpret_cast<__nv_bfloat162*>(y) = __floats2bfloat162_rn(o[0], o[1]);
+      } else {
+        y[0] = f2bf(o[0]);
+      }
+    }
+  }
+}
+
 // Epilogue of one 32-column chunk held by this thread (one accumulator row).
 VAE_DEV void epilogue_chunk(const TcParams& p, const TileCoord& tc, int m, int nb, float* v, int lane) {
   if (tc.dummy) return;
@@ -322,14 +371,19 @@ VAE_DEV void epilogue_chunk(const TcParams& p, const TileCoord& tc, int m, int n
         default: gn_chunk_sums<32>(p, tc, v, st_ok, to, c, lane); break;
       }
     }
+  } else if (p.out_ncthw && p.natural && (sw == 1 || sw == 2 || sw == 4)) {
+    if (!valid) return;
+    if (sw == 4) ncthw_store_runs<4>(p, tc, h, w, nb, v);
+    else if (sw == 2) ncthw_store_runs<2>(p, tc, h, w, nb, v);
+    else ncthw_store_runs<1>(p, tc, h, w, nb, v);
   } else {
     // generic scalar path (NCTHW pixels, or channel counts not a multiple of 32)
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const int n = nb + i;
       if (n >= p.N_real) continue;
-      const int sub = n / p.C_d2s;
-      const int c = n - sub * p.C_d2s;
+      const int sub = p.natural ? n % p.S : n / p.C_d2s;
+      const int c = p.natural ? n / p.S : n - sub * p.C_d2s;
       float val = v[i] * (p.wscale ? p.wscale[n] : 1.f) + (p.bias ? p.bias[c * p.S + sub] : 0.f);
       const int dt = sub / (sh * sw);
       const int rem = sub - dt * sh * sw;
@@ -844,9 +898,12 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   p.kc = p.fp8 ? 128 : 64;
   if (p.fp8 && (a.mode != 0 || !a.wscale || a.C_in_pad % 128 != 0)) return cudaErrorInvalidValue;
   p.wscale = p.fp8 ? a.wscale : nullptr;
-  // (not for NCTHW pixel outputs of more than 16 channels: their scalar store epilogue then outlasts the
-  // shorter MMA phase; measured on one GB300: LTX 128->48 head 3.66 ms per tap, 5.73 ms in halo mode)
-  p.halo = (a.mode == 0 && p.BN <= 64 && !p.fp8 && (!a.out_ncthw || a.N_real <= 16) && halo_mode_enabled()) ? 1 : 0;
+  // (NCTHW pixel outputs wider than 16 channels only with vector stores (natural channel order): with
+  // scalar stores the epilogue outlasts the shorter MMA phase; measured on one GB300: LTX 128->48 head
+  // 3.66 ms per tap, 5.73 ms in halo mode with scalar stores)
+  p.halo = (a.mode == 0 && p.BN <= 64 && !p.fp8 && (!a.out_ncthw || a.natural || a.N_real <= 16) && halo_mode_enabled())
+               ? 1
+               : 0;
   // halo mode: sub-tiles of 8 x 16 box pixels; two accumulators of msub x 3 BN columns must fit TMEM
   if (p.halo) p.msub = 2 * 2 * 3 * p.BN <= 512 ? 2 : 1;
   const bool mma_pair =
@@ -879,6 +936,7 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   p.y = a.y;
   p.out_f32 = a.out_f32;
   p.out_ncthw = a.out_ncthw;
+  p.natural = a.natural;
   p.fault = fault_word();
   p.limit_ns = wait_limit_ns();
 

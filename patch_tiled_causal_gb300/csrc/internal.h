@@ -47,6 +47,8 @@ struct ConvTcArgs {
   // conv mode, e4m3 operands: x and w hold e4m3 bytes (C_in_pad a multiple of 128) and the product of
   // output channel n (packed row order) is multiplied by wscale[n] (its weights' scale)
   int fp8; const float* wscale;
+  // weight rows in PyTorch channel order (packed with natural != 0); required for NCTHW outputs
+  int natural;
 };
 cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t s);
 
@@ -63,16 +65,18 @@ struct ConvSimtArgs {
 };
 cudaError_t launch_conv_simt(const ConvSimtArgs& a, cudaStream_t s);
 
-// Weight packing.
+// Weight packing.  Rows are ordered (depth-to-space sub-position, channel) so that a 32-column epilogue
+// chunk is 32 channels of one sub-position; natural != 0 keeps PyTorch's channel order (c*S + sub),
+// which convs storing NCTHW pixels use (a chunk then holds whole runs of horizontally adjacent pixels).
 cudaError_t launch_pack_weights_bf16(const float* w, int C_out, int C_in, int C_in_pad, int N_pad, int S,
-                                     void* out, cudaStream_t s);
+                                     void* out, cudaStream_t s, int natural = 0);
 cudaError_t launch_pack_weights_f32(const float* w, int C_out, int C_in, void* out, cudaStream_t s);
 cudaError_t launch_pack_matrix_bf16(const float* w, int rows, int cols, void* out, cudaStream_t s);
 // e4m3 K-major [N_pad, 27 * C_in_pad] (rows as the bf16 packing), each row scaled by its own
 // scale = max|w| / 448, followed at fp8_scale_offset() bytes by the float scales [N_pad].
 size_t fp8_scale_offset(int N_pad, int C_in_pad);
 cudaError_t launch_pack_weights_fp8(const float* w, int C_out, int C_in, int C_in_pad, int N_pad, int S, void* out,
-                                    cudaStream_t s);
+                                    cudaStream_t s, int natural = 0);
 
 // Group norm.
 struct GnArgs {

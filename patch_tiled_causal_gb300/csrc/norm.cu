@@ -16,7 +16,6 @@
 // per-tile mask built on the device from 1-D parts, weighted sum over the weight sum); here each
 // output pixel gathers the tiles that cover it, in tile order, so the result is written once.
 #include <algorithm>
-#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -856,8 +855,6 @@ struct BlendGridParams {
   int s0[3][kAxisMax], len[3][kAxisMax];
   unsigned short lo[3][kAxisMax], hi[3][kAxisMax];
   void* out;
-  uint32_t* fault;
-  uint64_t limit_ns;
   const void* ptr[VAE_MAX_TILES];  // tile (a, b, c) at ptr[(a * n[1] + b) * n[2] + c]
 };
 
@@ -1151,209 +1148,7 @@ __global__ void __launch_bounds__(256, 4) blend_grid2_kernel(const __grid_consta
 }
 
 
-// Staged grid blend.  A warp blends one output row (one plane) at a time; one lane first copies every
-// source row segment that row needs (each covering tile row of each column interval: contiguous,
-// 16-byte aligned) into the warp's shared-memory buffer with 1-D bulk async copies that complete on an
-// mbarrier, kBsDepth rows ahead of the row being blended, so each warp keeps whole rows of loads in
-// flight instead of one vector per lane.  Rows whose segments are unaligned or do not fit a buffer are
-// read from global memory directly (the same arithmetic).  Same sums, same order, same results as
-// blend_grid2_kernel.
-constexpr int kBsWarps = 8;
-constexpr int kBsDepth = 3;              // rows per warp in flight (buffers per warp)
-constexpr int kBsBufBytes = 8192;        // bytes per buffer
-constexpr size_t kBsSmem = static_cast<size_t>(kBsWarps) * kBsDepth * kBsBufBytes;
-
-VAE_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  uint64_t g;
-  asm volatile("cvta.to.global.u64 %0, %1;" : "=l"(g) : "l"(reinterpret_cast<uint64_t>(src)));
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_u32(dst)),
-               "l"(g), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
-}
-
-template <typename TT, typename TO>
-__global__ void __launch_bounds__(32 * kBsWarps, 1) blend_stage_kernel(const __grid_constant__ BlendGridParams p) {
-  extern __shared__ __align__(128) uint8_t bs_buf[];  // [kBsWarps][kBsDepth][kBsBufBytes]
-  __shared__ int4 vinfo[kGridMaxVec];
-  __shared__ float4 vw0[kGridMaxVec][2];
-  __shared__ const TT* rowp[kBsWarps][kBsDepth][4][kG2Cols];
-  __shared__ int staged[kBsWarps][kBsDepth];
-  __shared__ __align__(8) uint64_t bar[kBsWarps][kBsDepth];
-  const int nv = (p.W + 7) / 8;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) {
-    for (int b = 0; b < kBsDepth; ++b) mbar_init(&bar[warp][b], 1);
-    fence_barrier_init();
-  }
-  build_vec_table(p, vinfo, vw0);
-  __syncthreads();
-  // persistent: this block takes units (frame, 32-row chunk) blockIdx.x, + gridDim.x, ...; a unit is
-  // n_pl * kGridRows (plane, row) tasks; warp w takes the block's tasks w, w + kBsWarps, ... in order
-  const int blocks_per_t = (p.H + kGridRows - 1) / kGridRows;
-  const int n_units = p.T * blocks_per_t;
-  const int n_pl = p.B * p.C;
-  const int n2 = p.n[2];
-  const int per_unit = n_pl * kGridRows;
-  const int my_units = blockIdx.x < n_units ? (n_units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  const long long n_block_tasks = static_cast<long long>(my_units) * per_unit;
-  const int my_tasks = static_cast<int>(n_block_tasks > warp ? (n_block_tasks - warp + kBsWarps - 1) / kBsWarps : 0);
-  struct Task {
-    int pl, t, y;
-  };
-  auto task_of = [&](int k) {
-    const long long g = warp + static_cast<long long>(k) * kBsWarps;
-    const int j = static_cast<int>(g / per_unit), r = static_cast<int>(g - static_cast<long long>(j) * per_unit);
-    const int u = blockIdx.x + j * gridDim.x;
-    const int t = u / blocks_per_t;
-    Task tk;
-    tk.pl = r / kGridRows;
-    tk.t = t;
-    tk.y = (u - t * blocks_per_t) * kGridRows + (r - (r / kGridRows) * kGridRows);
-    return tk;
-  };
-  // lane 0: the source row pointers of task k into buffer b, staged in shared memory where possible
-  auto prepare = [&](int k, int b) {
-    const Task tk = task_of(k);
-    int st = 0;
-    if (tk.y < p.H) {
-      int ia0, ia1, ib0, ib1;
-      float wa0, wa1, wb0, wb1;
-      const int na = axis_cover2(p, 0, tk.t, ia0, ia1, wa0, wa1);
-      const int nb = axis_cover2(p, 1, tk.y, ib0, ib1, wb0, wb1);
-      const int npair = na * nb;
-      uint32_t total = 0;
-      bool ok = true;
-      for (int q = 0; q < npair; ++q)
-        for (int cc = 0; cc < n2; ++cc) {
-          const int qa = nb == 2 ? q >> 1 : q, qb = nb == 2 ? q & 1 : 0;
-          const int a = qa ? ia1 : ia0, bb = qb ? ib1 : ib0;
-          const int64_t plane_in = static_cast<int64_t>(p.len[0][a]) * p.len[1][bb];
-          const TT* src = static_cast<const TT*>(p.ptr[(a * p.n[1] + bb) * n2 + cc]) +
-                          ((tk.pl * plane_in + static_cast<int64_t>(tk.t - p.s0[0][a]) * p.len[1][bb]) +
-                           (tk.y - p.s0[1][bb])) * p.len[2][cc];
-          rowp[warp][b][q][cc] = src;
-          const uint32_t bytes = static_cast<uint32_t>(p.len[2][cc]) * sizeof(TT);
-          ok = ok && (reinterpret_cast<uintptr_t>(src) & 15u) == 0 && (bytes & 15u) == 0;
-          total += bytes;
-        }
-      if (ok && total <= static_cast<uint32_t>(kBsBufBytes)) {
-        uint8_t* dst = bs_buf + (static_cast<size_t>(warp) * kBsDepth + b) * kBsBufBytes;
-        fence_proxy_async();  // earlier generic reads of this buffer come before the copies overwrite it
-        mbar_arrive_expect_tx(&bar[warp][b], total);
-        for (int q = 0; q < npair; ++q)
-          for (int cc = 0; cc < n2; ++cc) {
-            const uint32_t bytes = static_cast<uint32_t>(p.len[2][cc]) * sizeof(TT);
-            bulk_g2s(dst, rowp[warp][b][q][cc], bytes, &bar[warp][b]);
-            rowp[warp][b][q][cc] = reinterpret_cast<const TT*>(dst);
-            dst += bytes;
-          }
-        st = 1;
-      }
-    }
-    staged[warp][b] = st;
-  };
-  uint32_t phase = 0;  // bit b: parity of buffer b's next completion
-  if (lane == 0)
-    for (int k = 0; k < kBsDepth - 1 && k < my_tasks; ++k) prepare(k, k);
-  for (int k = 0; k < my_tasks; ++k) {
-    const int b = k % kBsDepth;
-    // refill the buffer that the previous task used (its reads ended at the last __syncwarp)
-    if (lane == 0 && k + kBsDepth - 1 < my_tasks) prepare(k + kBsDepth - 1, (k + kBsDepth - 1) % kBsDepth);
-    __syncwarp();
-    const Task tk = task_of(k);
-    if (tk.y >= p.H) continue;
-    if (staged[warp][b]) {
-      if (!mbar_wait(&bar[warp][b], (phase >> b) & 1u, p.fault, p.limit_ns, 40)) {
-        // give up: wait (bounded) for this warp's other copies in flight, then leave
-        for (int j = 1; j < kBsDepth && k + j < my_tasks; ++j) {
-          const int bj = (k + j) % kBsDepth;
-          if (staged[warp][bj]) mbar_wait(&bar[warp][bj], (phase >> bj) & 1u, p.fault, p.limit_ns, 41);
-        }
-        return;
-      }
-      phase ^= 1u << b;
-    }
-    int ia0, ia1, ib0, ib1;
-    float wa0, wa1, wb0, wb1;
-    const int na = axis_cover2(p, 0, tk.t, ia0, ia1, wa0, wa1);
-    const int nb = axis_cover2(p, 1, tk.y, ib0, ib1, wb0, wb1);
-    const int npair = na * nb;
-    float wq[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int qa = nb == 2 ? q >> 1 : q, qb = nb == 2 ? q & 1 : 0;
-      wq[q] = q < npair ? (qa ? wa1 : wa0) * (qb ? wb1 : wb0) : 0.f;
-    }
-    TO* orow = static_cast<TO*>(p.out) + ((static_cast<int64_t>(tk.pl) * p.T + tk.t) * p.H + tk.y) * p.W;
-    for (int v = lane; v < nv; v += 32) {
-      const int4 inf = vinfo[v];
-      const int x0 = v * 8;
-      float acc[8];
-      if (((inf.x >> 12) & 1) && npair <= 2) {
-        const int cv = inf.x & 255, ncv = (inf.x >> 8) & 15;
-        Raw8<TT> raw[2][2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
-            if (q < npair && j < ncv) raw[q][j].load(rowp[warp][b][q][cv + j] + (j ? inf.z : inf.y));
-        const float4 wl = vw0[v][0], wh = vw0[v][1];
-        const float w0[8] = {wl.x, wl.y, wl.z, wl.w, wh.x, wh.y, wh.z, wh.w};
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          float sm[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) sm[e] = 0.f;
-#pragma unroll
-          for (int q = 0; q < 2; ++q)
-            if (q < npair && j < ncv) {
-              float val[8];
-              raw[q][j].get(val);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) sm[e] = fmaf(wq[q], val[e], sm[e]);
-            }
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float wc = j ? 1.f - w0[e] : w0[e];
-            acc[e] = j ? fmaf(wc, sm[e], acc[e]) : wc * sm[e];
-          }
-        }
-      } else {
-        // ragged or unaligned vector, or a row covered by more than two pairs: per pixel
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          acc[e] = 0.f;
-          const int x = x0 + e;
-          if (x >= p.W) continue;
-          int ic0, ic1;
-          float wc0, wc1;
-          const int ncx = axis_cover2(p, 2, x, ic0, ic1, wc0, wc1);
-          for (int q = 0; q < npair; ++q) {
-            const int qa = nb == 2 ? q >> 1 : q, qb = nb == 2 ? q & 1 : 0;
-            const float wqq = (qa ? wa1 : wa0) * (qb ? wb1 : wb0);
-            for (int j = 0; j < ncx; ++j) {
-              const int ci = j ? ic1 : ic0;
-              acc[e] = fmaf(wqq * (j ? wc1 : wc0), to_f<TT>(rowp[warp][b][q][ci][x - p.s0[2][ci]]), acc[e]);
-            }
-          }
-        }
-      }
-      if (x0 + 8 <= p.W && (p.W & 7) == 0) {
-        store8(orow + x0, acc);
-      } else {
-        for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(acc[e]);
-      }
-    }
-    __syncwarp();
-  }
-}
-
 namespace {
-// Staged grid blend (bulk copies into shared memory, persistent); the unstaged grid kernel stays for
-// comparison.
-bool staged_blend_enabled() { return true; }
-
 // Recognise a grid: tiles in raster order over per-axis interval lists with per-axis overlaps, at most
 // two intervals covering any coordinate (overlap shorter than the stride).
 bool build_grid(const void* const* tiles, const vae_tile_t* meta, int n, const vae_blend_desc_t& d,
@@ -1413,33 +1208,6 @@ cudaError_t launch_blend(const void* const* tiles, const vae_tile_t* meta, int n
     if (nb == 0) return cudaSuccess;
     if (nb > 0x7fffffffLL) return cudaErrorInvalidValue;
     const bool tf = d.tile_dtype == VAE_FP32, of = d.out_dtype == VAE_FP32;
-    g.fault = fault_word();
-    g.limit_ns = wait_limit_ns();
-    if (staged_blend_enabled()) {
-      // persistent, one block per SM (the staging buffers take most of its shared memory)
-      int dev = 0, n_sm = 0;
-      if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) !=
-                                                     cudaSuccess || n_sm <= 0)
-        n_sm = 148;
-      static std::once_flag attr_once;
-      static cudaError_t attr_err = cudaSuccess;
-      std::call_once(attr_once, [] {
-        for (auto* k : {blend_stage_kernel<float, float>, blend_stage_kernel<float, __nv_bfloat16>,
-                        blend_stage_kernel<__nv_bfloat16, float>, blend_stage_kernel<__nv_bfloat16, __nv_bfloat16>}) {
-          const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     static_cast<int>(kBsSmem));
-          if (e != cudaSuccess) attr_err = e;
-        }
-      });
-      if (attr_err != cudaSuccess) return attr_err;
-      const dim3 grid(static_cast<unsigned>(std::min<long long>(nb, n_sm)));
-      const dim3 blk(32 * kBsWarps);
-      if (tf && of) blend_stage_kernel<float, float><<<grid, blk, kBsSmem, s>>>(g);
-      else if (tf) blend_stage_kernel<float, __nv_bfloat16><<<grid, blk, kBsSmem, s>>>(g);
-      else if (of) blend_stage_kernel<__nv_bfloat16, float><<<grid, blk, kBsSmem, s>>>(g);
-      else blend_stage_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, blk, kBsSmem, s>>>(g);
-      return cudaGetLastError();
-    }
     const dim3 grid(static_cast<unsigned>(nb));  // every plane of a (t, row chunk) in one block
     if (tf && of) blend_grid2_kernel<float, float><<<grid, 256, 0, s>>>(g);
     else if (tf) blend_grid2_kernel<float, __nv_bfloat16><<<grid, 256, 0, s>>>(g);
@@ -1743,7 +1511,8 @@ cudaError_t launch_stride2_weights(const float* w, int C_out, int C_in, float* o
 
 // ============================================================================ weight packing
 // bf16 K-major [N_pad, 27 * C_in_pad]; row n' = sub * (C_out/S) + c holds PyTorch channel c * S + sub
-__global__ void pack_bf16_kernel(const float* w, int C_out, int C_in, int C_in_pad, int N_pad, int S,
+// (natural: row n' holds channel n', for convs that store NCTHW pixels)
+__global__ void pack_bf16_kernel(const float* w, int C_out, int C_in, int C_in_pad, int N_pad, int S, int natural,
                                  __nv_bfloat16* out) {
   const int64_t n = static_cast<int64_t>(N_pad) * 27 * C_in_pad;
   const int Cd = C_out / S;
@@ -1755,7 +1524,7 @@ __global__ void pack_bf16_kernel(const float* w, int C_out, int C_in, int C_in_p
     float v = 0.f;
     if (np < C_out && ci < C_in) {
       const int sub = np / Cd, c = np % Cd;
-      const int co = c * S + sub;
+      const int co = natural ? np : c * S + sub;
       v = w[(static_cast<int64_t>(co) * C_in + ci) * 27 + tap];
     }
     out[i] = f2bf(v);
@@ -1763,10 +1532,11 @@ __global__ void pack_bf16_kernel(const float* w, int C_out, int C_in, int C_in_p
 }
 
 cudaError_t launch_pack_weights_bf16(const float* w, int C_out, int C_in, int C_in_pad, int N_pad, int S, void* out,
-                                     cudaStream_t s) {
+                                     cudaStream_t s, int natural) {
   const int64_t n = static_cast<int64_t>(N_pad) * 27 * C_in_pad;
   const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 152 * 64));
-  pack_bf16_kernel<<<blocks, 256, 0, s>>>(w, C_out, C_in, C_in_pad, N_pad, S, static_cast<__nv_bfloat16*>(out));
+  pack_bf16_kernel<<<blocks, 256, 0, s>>>(w, C_out, C_in, C_in_pad, N_pad, S, natural,
+                                          static_cast<__nv_bfloat16*>(out));
   return cudaGetLastError();
 }
 
@@ -1778,13 +1548,13 @@ size_t fp8_scale_offset(int N_pad, int C_in_pad) {
 }
 
 __global__ void __launch_bounds__(256) pack_fp8_kernel(const float* w, int C_out, int C_in, int C_in_pad, int S,
-                                                        __nv_fp8_e4m3* out, float* scales) {
+                                                        int natural, __nv_fp8_e4m3* out, float* scales) {
   __shared__ float red[8];
   const int np = blockIdx.x;
   const int Cd = C_out / S;
   const int64_t K = 27LL * C_in_pad;
   const bool real = np < C_out;
-  const int co = real ? (np % Cd) * S + np / Cd : 0;
+  const int co = real ? (natural ? np : (np % Cd) * S + np / Cd) : 0;
   const float* wr = w + static_cast<int64_t>(co) * C_in * 27;  // [C_in, 27] of output channel co
   float m = 0.f;
   if (real)
@@ -1805,9 +1575,9 @@ __global__ void __launch_bounds__(256) pack_fp8_kernel(const float* w, int C_out
 }
 
 cudaError_t launch_pack_weights_fp8(const float* w, int C_out, int C_in, int C_in_pad, int N_pad, int S, void* out,
-                                    cudaStream_t s) {
+                                    cudaStream_t s, int natural) {
   if (N_pad <= 0) return cudaSuccess;
-  pack_fp8_kernel<<<N_pad, 256, 0, s>>>(w, C_out, C_in, C_in_pad, S, static_cast<__nv_fp8_e4m3*>(out),
+  pack_fp8_kernel<<<N_pad, 256, 0, s>>>(w, C_out, C_in, C_in_pad, S, natural, static_cast<__nv_fp8_e4m3*>(out),
                                         reinterpret_cast<float*>(static_cast<char*>(out) + fp8_scale_offset(N_pad, C_in_pad)));
   return cudaGetLastError();
 }

@@ -231,7 +231,7 @@ def main():
     ap.add_argument("--latent-frames", type=int, default=0,
                     help="decode only the first N latent frames (0: all; small values for profiler captures)")
     ap.add_argument("--ops-frames", type=int, default=0,
-                    help="frames of the op workloads (0: the full sizes; small values for profiler captures)")
+                    help="frames of the pixel-head op workloads (0: 81; smaller values for profiler captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     cfg = {"wan": synth.WAN, "ltx": synth.LTX, "wan_rms": synth.WAN_RMS}[args.workload]
@@ -536,7 +536,7 @@ def _time(torch, fn, steps, flush):
 
 def run_ops(args, torch, vd, peaks, flush):
     res = {}
-    B, C, T, H, W = 1, 512, args.ops_frames or 21, 88, 160
+    B, C, T, H, W = 1, 512, 21, 88, 160
     eh, ew = vd.patch_edges(H, 1), vd.patch_edges(W, 4)
     # (a) PatchGroupNorm + SiLU, 4 width patches
     x = torch.from_numpy(synth.draw_normal((B, T, H, W, C), 100)).to("cuda", torch.bfloat16)

@@ -1342,10 +1342,44 @@ __global__ void cast_frames_kernel(const TI* x, int xTa, TO* y, int yTa, int T, 
   }
 }
 
+// 8 consecutive elements per thread (frame_elems a multiple of 8): one 16- or 32-byte load, one store
+template <typename TI, typename TO>
+__global__ void cast_frames8_kernel(const TI* x, int xTa, TO* y, int yTa, int T, int64_t fv, int64_t nv, uint32_t* fault) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nv;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = i % fv;
+    const int64_t f = i / fv;
+    const int64_t t = f % T, b = f / T;
+    float v[8];
+    load8(x + ((b * xTa + t) * fv + e) * 8, v);
+    vstore8(y + ((b * yTa + t) * fv + e) * 8, v, fault);
+  }
+}
+
 cudaError_t launch_cast_frames(const void* x, int x_f32, int x_T_alloc, void* y, int y_kind, int y_T_alloc, int B, int T,
                                int64_t frame_elems, cudaStream_t s) {
   const int64_t n = static_cast<int64_t>(B) * T * frame_elems;
   if (n <= 0) return cudaSuccess;
+  if (frame_elems % 8 == 0) {
+    const int64_t fv = frame_elems / 8, nv = n / 8;
+    const int blocks8 = static_cast<int>(std::min<int64_t>((nv + 255) / 256, 152 * 16));
+    uint32_t* f8 = fault_word();
+    const float* xf = static_cast<const float*>(x);
+    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+#define VAE_CAST8(XP, TO) \
+  cast_frames8_kernel<<<blocks8, 256, 0, s>>>(XP, x_T_alloc, static_cast<TO*>(y), y_T_alloc, T, fv, nv, f8)
+    if (x_f32) {
+      if (y_kind == 1) VAE_CAST8(xf, float);
+      else if (y_kind == 2) VAE_CAST8(xf, __nv_fp8_e4m3);
+      else VAE_CAST8(xf, __nv_bfloat16);
+    } else {
+      if (y_kind == 1) VAE_CAST8(xb, float);
+      else if (y_kind == 2) VAE_CAST8(xb, __nv_fp8_e4m3);
+      else VAE_CAST8(xb, __nv_bfloat16);
+    }
+#undef VAE_CAST8
+    return cudaGetLastError();
+  }
   const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 152 * 64));
   const float* xf = static_cast<const float*>(x);
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
@@ -1417,10 +1451,59 @@ __global__ void pixels_to_cl_kernel(const float* v, int B, int C, int T, int H, 
   }
 }
 
+// pw == 4, C_pad == 64: one thread per output pixel: C*ph float4 reads (the 4 adjacent pixels of one
+// (c, dy); consecutive threads take consecutive output columns, so every read is coalesced) and the
+// whole 64-channel pixel written as 16-byte vectors (consecutive threads, consecutive pixels)
+template <typename TO>
+__global__ void pixels_to_cl64_kernel(const float* v, int B, int C, int T, int H, int W, int ph, int h0, int nh, int w0,
+                                      int nw, TO* y, int yTa, uint32_t* fault) {
+  const int runs = C * ph;  // (c, dy) pairs, <= 16
+  const int64_t n = static_cast<int64_t>(B) * T * nh * nw;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int xx = static_cast<int>(i % nw);
+    int64_t r = i / nw;
+    const int yy = static_cast<int>(r % nh);
+    r /= nh;
+    const int t = static_cast<int>(r % T);
+    const int b = static_cast<int>(r / T);
+    float o[64];
+#pragma unroll
+    for (int g = 0; g < 16; ++g) {
+      float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (g < runs) {
+        const int c = g / ph, dy = g - (g / ph) * ph;
+        q = *reinterpret_cast<const float4*>(v + ((static_cast<int64_t>(b) * C + c) * T + t) * H * static_cast<int64_t>(W) +
+                                             static_cast<int64_t>((h0 + yy) * ph + dy) * W +
+                                             static_cast<int64_t>(w0 + xx) * 4);
+      }
+      o[4 * g] = q.x; o[4 * g + 1] = q.y; o[4 * g + 2] = q.z; o[4 * g + 3] = q.w;
+    }
+    TO* dst = y + (((static_cast<int64_t>(b) * yTa + t) * nh + yy) * nw + xx) * 64;
+#pragma unroll
+    for (int k = 0; k < 64; k += 8) vstore8(dst + k, o + k, fault);
+  }
+}
+
 cudaError_t launch_pixels_to_cl(const float* v, int B, int C, int T, int H, int W, int ph, int pw, int h0, int nh,
                                 int w0, int nw, int C_pad, void* y, int y_kind, int y_T_alloc, cudaStream_t s) {
   const int64_t n = static_cast<int64_t>(B) * T * nh * nw * C_pad;
   if (n <= 0) return cudaSuccess;
+  if (pw == 4 && C_pad == 64 && C * ph <= 16 && W % 4 == 0 && (reinterpret_cast<uintptr_t>(v) & 15u) == 0) {
+    const int64_t np = static_cast<int64_t>(B) * T * nh * nw;
+    const int blocks4 = static_cast<int>(std::min<int64_t>((np + 255) / 256, 152 * 16));
+    uint32_t* f4 = fault_word();
+    if (y_kind == 1)
+      pixels_to_cl64_kernel<<<blocks4, 256, 0, s>>>(v, B, C, T, H, W, ph, h0, nh, w0, nw, static_cast<float*>(y),
+                                                    y_T_alloc, f4);
+    else if (y_kind == 2)
+      pixels_to_cl64_kernel<<<blocks4, 256, 0, s>>>(v, B, C, T, H, W, ph, h0, nh, w0, nw,
+                                                    static_cast<__nv_fp8_e4m3*>(y), y_T_alloc, f4);
+    else
+      pixels_to_cl64_kernel<<<blocks4, 256, 0, s>>>(v, B, C, T, H, W, ph, h0, nh, w0, nw,
+                                                    static_cast<__nv_bfloat16*>(y), y_T_alloc, f4);
+    return cudaGetLastError();
+  }
   const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 152 * 64));
   uint32_t* f = fault_word();
   if (y_kind == 1)
@@ -1462,9 +1545,62 @@ __global__ void fold_frames_kernel(const TI* x, int xTa, int B, int T, int H, in
   }
 }
 
+// one thread per (output pixel, input channel c): for each of the S sub-positions one read of channel c of
+// an input pixel (consecutive threads: consecutive c, coalesced) and one write of output channel
+// c*S + sub (the S writes of a thread are contiguous)
+template <typename TI, typename TO, int S>
+__global__ void fold_frames_s_kernel(const TI* x, int xTa, int B, int T, int H, int W, int C, int st, int sh, int sw,
+                                     TO* y, int yTa, uint32_t* fault) {
+  const int To = (T + st - 1) / st, Ho = H / sh, Wo = W / sw;
+  const int64_t n = static_cast<int64_t>(B) * To * Ho * Wo * C;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(i % C);
+    int64_t r = i / C;
+    const int xo = static_cast<int>(r % Wo);
+    r /= Wo;
+    const int yo = static_cast<int>(r % Ho);
+    r /= Ho;
+    const int to = static_cast<int>(r % To);
+    const int b = static_cast<int>(r / To);
+    TO* dst = y + ((((static_cast<int64_t>(b) * yTa + to) * Ho + yo) * Wo + xo) * C + c) * S;
+#pragma unroll
+    for (int sub = 0; sub < S; ++sub) {
+      const int dt = sub / (sh * sw), dy = (sub / sw) % sh, dx = sub % sw;
+      const int ti = max(st * to + dt - (st - 1), 0);
+      const float val =
+          to_f<TI>(x[(((static_cast<int64_t>(b) * xTa + ti) * H + (sh * yo + dy)) * W + (sw * xo + dx)) * C + c]);
+      if (sizeof(TO) == 1 && !(fabsf(val) <= 448.f)) raise_fault(fault, FAULT_RANGE, 25);
+      dst[sub] = from_f<TO>(val);
+    }
+  }
+}
+
 cudaError_t launch_fold_frames(const void* x, int x_f32, int x_T_alloc, int B, int T, int H, int W, int C, int st,
                                int sh, int sw, void* y, int y_kind, int y_T_alloc, cudaStream_t s) {
   if (st < 1 || sh < 1 || sw < 1 || H % sh || W % sw) return cudaErrorInvalidValue;
+  const int S = st * sh * sw;
+  if (S == 4 || S == 8) {
+    const int64_t nt = static_cast<int64_t>(B) * ((T + st - 1) / st) * (H / sh) * (W / sw) * C;
+    if (nt <= 0) return cudaSuccess;
+    const int bl = static_cast<int>(std::min<int64_t>((nt + 255) / 256, 152 * 16));
+    uint32_t* fs = fault_word();
+#define VAE_FOLDS(TI, TO, SS)                                                                                       \
+  fold_frames_s_kernel<TI, TO, SS><<<bl, 256, 0, s>>>(static_cast<const TI*>(x), x_T_alloc, B, T, H, W, C, st, sh, sw, \
+                                                      static_cast<TO*>(y), y_T_alloc, fs)
+#define VAE_FOLDS_T(TI, SS)                                   \
+  if (y_kind == 1) VAE_FOLDS(TI, float, SS);                  \
+  else if (y_kind == 2) VAE_FOLDS(TI, __nv_fp8_e4m3, SS);     \
+  else VAE_FOLDS(TI, __nv_bfloat16, SS);
+    if (x_f32) {
+      if (S == 4) { VAE_FOLDS_T(float, 4) } else { VAE_FOLDS_T(float, 8) }
+    } else {
+      if (S == 4) { VAE_FOLDS_T(__nv_bfloat16, 4) } else { VAE_FOLDS_T(__nv_bfloat16, 8) }
+    }
+#undef VAE_FOLDS_T
+#undef VAE_FOLDS
+    return cudaGetLastError();
+  }
   const int64_t n = static_cast<int64_t>(B) * ((T + st - 1) / st) * (H / sh) * (W / sw) * C * st * sh * sw;
   if (n <= 0) return cudaSuccess;
   const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 152 * 64));

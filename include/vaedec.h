@@ -330,7 +330,10 @@ size_t vae_conv3d_packed_bytes(const vae_conv_desc_t* d);
  * depth-to-space stores contiguous channels; for fp8 the same matrix in e4m3 bytes, each row divided
  * by its scale max|row| / 448, followed (at the next 256-byte boundary) by the fp32 scales [N_pad];
  * for fp32 [27, C_in, C_out].  With out_ncthw the bf16 / fp8 rows keep PyTorch's channel order (so the
- * conv's store writes runs of horizontally adjacent pixels); pack and conv must use the same out_ncthw. */
+ * conv's store writes runs of horizontally adjacent pixels); pack and conv must use the same out_ncthw.
+ * bf16 convs with C_out <= 12 pack tap-stacked instead: [3 (k_t)][112][C_in], row (k_h*3 + k_w)*12 + n
+ * holding packed column n (same order as above) of that spatial tap, zero rows elsewhere, so that one
+ * tensor-core instruction covers all 9 spatial taps of a narrow conv. */
 vae_status_t vae_conv3d_pack_weights(const float* w, const vae_conv_desc_t* d, void* w_packed, void* stream);
 
 /* Causal Conv3d ([DV] PatchConv3d padding commit, HunyuanVideo/LTX-2 commits): for every output

@@ -111,6 +111,7 @@ struct ConvL {
   bool tc = false;
   bool fp8 = false;        // e4m3 operands and weights (fp8 decoders)
   bool natural = false;    // weight rows in PyTorch channel order (convs that store NCTHW pixels)
+  bool tap = false;        // narrow bf16 conv: weights packed tap-stacked (all 9 spatial taps in one MMA)
   float* wscale = nullptr; // fp8: per-output-channel weight scales (inside the packed weight buffer)
   void* w = nullptr;       // packed weights
   float* bias = nullptr;   // fp32 [C_out]
@@ -243,11 +244,12 @@ vae_status_t make_conv(vae_decoder* d, ConvL& c, const float* w, const float* b,
     c.wscale = reinterpret_cast<float*>(static_cast<char*>(c.w) + off);
     CK(launch_pack_weights_fp8(w, C_out, C_in, c.C_in_pad, c.N_pad, S, c.w, nullptr, natural));
   } else if (c.tc) {
-    c.N_pad = C_out <= 256 ? round_up(C_out, 16) : round_up(C_out, 16);
-    const size_t bytes = static_cast<size_t>(c.N_pad) * 27 * c.C_in_pad * 2;
+    c.N_pad = round_up(C_out, 16);
+    c.tap = conv_tap_stacked(C_out, 0);
+    const size_t bytes = c.tap ? 3ull * kTapRows * c.C_in_pad * 2 : static_cast<size_t>(c.N_pad) * 27 * c.C_in_pad * 2;
     vae_status_t s = dalloc(d, &c.w, bytes);
     if (s) return s;
-    CK(launch_pack_weights_bf16(w, C_out, C_in, c.C_in_pad, c.N_pad, S, c.w, nullptr, natural));
+    CK(launch_pack_weights_bf16(w, C_out, C_in, c.C_in_pad, c.N_pad, S, c.w, nullptr, natural, c.tap));
   } else {
     const size_t bytes = 27ull * C_in * C_out * 4;
     vae_status_t s = dalloc(d, &c.w, bytes);
@@ -637,7 +639,7 @@ vae_status_t run_conv(Ctx& x, ConvL& c, const Level& L, char* in, const ConvOut&
     a.residual = residual; a.res_f32 = res_f32; a.res_T_alloc = T;
     a.y = y; a.out_f32 = y_f32; a.out_ncthw = out_ncthw; a.y_T_alloc = y_T_alloc;
     a.d2s_t = c.st; a.d2s_h = c.sh; a.d2s_w = c.sw; a.drop_first = drop_first;
-    a.fp8 = c.fp8; a.wscale = c.wscale; a.natural = c.natural;
+    a.fp8 = c.fp8; a.wscale = c.wscale; a.natural = c.natural; a.tap_stacked = c.tap;
     const int Cd = c.C_out / (c.st * c.sh * c.sw);
     const int G = d->cfg.gn_groups;  // (ignored, possibly 0, by channel-RMS decoders)
     const int cpg = (G > 0 && Cd % G == 0) ? Cd / G : 0;
@@ -1596,6 +1598,7 @@ int conv_npad(const vae_conv_desc_t* d) { return (d->C_out + 15) / 16 * 16; }
 extern "C" size_t vae_conv3d_packed_bytes(const vae_conv_desc_t* d) {
   if (!d || d->C_in <= 0 || d->C_out <= 0) return 0;
   if (conv_fp8(d)) return fp8_scale_offset(conv_npad(d), d->C_in) + static_cast<size_t>(conv_npad(d)) * 4;
+  if (conv_tc_ok(d) && conv_tap_stacked(d->C_out, 0)) return 3ull * kTapRows * d->C_in * 2;
   if (conv_tc_ok(d)) return static_cast<size_t>(conv_npad(d)) * 27 * d->C_in * 2;
   return 27ull * d->C_in * d->C_out * 4;
 }
@@ -1610,7 +1613,8 @@ extern "C" vae_status_t vae_conv3d_pack_weights(const float* w, const vae_conv_d
   if (conv_fp8(d))
     CK(launch_pack_weights_fp8(w, d->C_out, d->C_in, d->C_in, conv_npad(d), S, w_packed, s, d->out_ncthw));
   else if (conv_tc_ok(d))
-    CK(launch_pack_weights_bf16(w, d->C_out, d->C_in, d->C_in, conv_npad(d), S, w_packed, s, d->out_ncthw));
+    CK(launch_pack_weights_bf16(w, d->C_out, d->C_in, d->C_in, conv_npad(d), S, w_packed, s, d->out_ncthw,
+                                conv_tap_stacked(d->C_out, 0)));
   else CK(launch_pack_weights_f32(w, d->C_out, d->C_in, w_packed, s));
   return VAE_OK;
 }
@@ -1652,6 +1656,7 @@ extern "C" vae_status_t vae_conv3d_causal(const void* x, const void* w_packed, c
     a.y = y; a.out_f32 = d->out_dtype == VAE_FP32; a.out_ncthw = d->out_ncthw;
     a.d2s_t = d->d2s_t; a.d2s_h = d->d2s_h; a.d2s_w = d->d2s_w; a.drop_first = d->drop_first;
     a.natural = d->out_ncthw;
+    a.tap_stacked = !a.fp8 && conv_tap_stacked(d->C_out, 0);
     CK(launch_conv_tc(a, s));
   } else {
     ConvSimtArgs a{};

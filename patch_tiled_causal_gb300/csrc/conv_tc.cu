@@ -64,8 +64,12 @@ struct TcParams {
   // halo mode (narrow convs): one stage = one (kt, 64-channel chunk) halo box of (rows_t + 2) x 16
   // pixels (rows_t = 8 x msub output rows of cols_t = 14 pixels) that all 9 spatial taps read in place,
   // plus those taps' weight tiles ([kh][kw][BN rows]: the 3 kw tiles of one kh form one N = 3 BN operand)
+  // halo = 2, tap-stacked (at most kTapMaxN output channels): a box of 16 x 16 pixels (14 x 14 outputs)
+  // and one tile of kTapRows weight rows holding all 9 spatial taps, so each MMA is N = kTapRows wide;
+  // the epilogue adds the taps' partial sums of neighbouring pixels (kw: warp shuffles within a box
+  // row; kh: through scratch shared memory at scratch_off, 2 x kTapMaxN floats per box pixel)
   int halo;
-  uint32_t halo_a_bytes, halo_tx, halo_stage;
+  uint32_t halo_a_bytes, halo_tx, halo_stage, scratch_off;
   const float* bias;
   const void* residual;
   int res_f32;
@@ -96,6 +100,23 @@ constexpr int kThreads = 192;
 constexpr int kBlockM = 128;
 constexpr int kBlockK = 64;
 constexpr uint32_t kABytes = kBlockM * kBlockK * 2;  // 16 KB
+constexpr int kTapBoxPx = 256;                      // tap-stacked box: 16 rows x 16 pixels
+
+// named barrier 1 over the 4 epilogue warps (barrier 0 is __syncthreads)
+VAE_DEV void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// the same barrier, returning whether pred held in every one of the 128 threads
+VAE_DEV bool epi_bar_and(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred))
+      : "memory");
+  return r != 0;
+}
 
 VAE_DEV int find_band(const int* prefix, int n, int idx) {
   int i = 0;
@@ -302,7 +323,7 @@ VAE_DEV void epilogue_chunk(const TcParams& p, const TileCoord& tc, int m, int n
   const int wm = p.halo ? (m & 15) : m % p.cols_t;
   const int h = tc.h0 + hm;
   const int w = tc.w0 + wm;
-  const bool valid = (h < tc.h_end) && (w < tc.w_end) && wm < p.cols_t;
+  const bool valid = (h < tc.h_end) && (w < tc.w_end) && wm < p.cols_t && (!p.halo || hm < p.rows_t);
   const bool vec = !p.out_ncthw && (p.C_d2s % 32 == 0);
   if (vec) {
     const int sub = nb / p.C_d2s;
@@ -491,10 +512,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t* b_dst = a_dst + p.halo_a_bytes;
                 mbar_arrive_expect_tx(&full_bar[s], p.halo_tx);
                 tma_load_5d(a_dst, &tmA, &full_bar[s], cc * kBlockK, tc.w0 - 1, tc.h0 - 1, ti, tc.b);
+                if (p.halo == 2) {
+                  tma_load_2d(b_dst, &tmB, &full_bar[s], cc * kBlockK, kt * kTapRows);
+                } else {
 #pragma unroll 1
-                for (int t9 = 0; t9 < 9; ++t9)
-                  tma_load_2d(b_dst + t9 * wt_bytes, &tmB, &full_bar[s], (kt * 9 + t9) * p.C_in_pad + cc * kBlockK,
-                              tc.n0);
+                  for (int t9 = 0; t9 < 9; ++t9)
+                    tma_load_2d(b_dst + t9 * wt_bytes, &tmB, &full_bar[s], (kt * 9 + t9) * p.C_in_pad + cc * kBlockK,
+                                tc.n0);
+                }
                 if (++s == stages) {
                   s = 0;
                   ph ^= 1u;
@@ -608,8 +633,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // tap row kh, sub-tile sub: A = the 128 box pixels from box row sub * 8 + kh on (8 box rows of
           // 16 pixels, 2048 B each, so every start is 1024-byte aligned), B = the kw = 0, 1, 2 weight tiles of
           // kh (3 BN rows), D = 3 BN columns of the sub-tile's accumulator
+          // (tap-stacked: A = the 128 box pixels from box row sub * 8, B = all 9 taps' kTapRows rows)
+          const bool tap = p.halo == 2;
           const uint32_t n3 = 3u * static_cast<uint32_t>(p.BN);
-          const uint32_t idesc = idesc_bf16_f32(kBlockM, n3);
+          const uint32_t idesc = idesc_bf16_f32(kBlockM, tap ? static_cast<uint32_t>(kTapRows) : n3);
           const int stages = p.stages, num_st = 3 * p.cchunks, msub = p.msub;
           const uint32_t smem_base = smem_u32(smem);
           const uint32_t wt_bytes = static_cast<uint32_t>(p.BN) * kBlockK * 2;
@@ -629,8 +656,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
               const uint32_t a_addr = smem_base + static_cast<uint32_t>(s) * stage_bytes;
               const uint32_t b_addr = a_addr + p.halo_a_bytes;
+              if (tap) {
+                const uint64_t bdesc = sdesc_kmajor_sw128(b_addr);
+                for (int sub = 0; sub < msub; ++sub) {
+                  const uint64_t adesc = sdesc_kmajor_sw128(a_addr + static_cast<uint32_t>(sub) * kBlockM * 128u);
+                  const uint32_t d_sub = d_tmem + static_cast<uint32_t>(sub * kTapRows);
+#pragma unroll
+                  for (int k = 0; k < kBlockK / 16; ++k)
+                    tc_mma_bf16(d_sub, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k),
+                                idesc, (st == 0 && k == 0) ? 0u : 1u);
+                }
+              }
 #pragma unroll 1
-              for (uint32_t kh = 0; kh < 3; ++kh) {
+              for (uint32_t kh = 0; kh < (tap ? 0u : 3u); ++kh) {
                 const uint64_t bdesc = sdesc_kmajor_sw128(b_addr + kh * 3u * wt_bytes);
                 for (int sub = 0; sub < msub; ++sub) {
                   const uint32_t row0 = (static_cast<uint32_t>(sub) * 8u + kh) * 16u;
@@ -715,7 +753,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int m = q * 32 + lane;
     int it = 0;
-    for (int seq = seq0; seq < p.seq_count; seq += seq_step, ++it) {
+    if (!kPair && p.halo == 2) {
+      // tap-stacked: accumulator row p = box pixel (p / 16, p % 16), column (kh * 3 + kw) * kTapMaxN + n.
+      // R_kh(p) = sum over kw of row p + kw, column tap(kh, kw) (shuffles within the 16-lane box row);
+      // output (r, c) = R_0(p) + R_1(p + 16) + R_2(p + 32), the last two through scratch[kh - 1][n][p].
+      float* scr = reinterpret_cast<float*>(smem + p.scratch_off);
+      for (int seq = seq0; seq < p.seq_count; seq += seq_step, ++it) {
+        const int acc = it & 1, u = it >> 1;
+        const bool got = mbar_wait(&accf_bar[acc], u & 1, p.fault, p.limit_ns, 5);
+        if (!epi_bar_and(got)) break;  // the four warps leave together, so no later barrier waits alone
+        tc_fence_after();
+        const TileCoord tc = seq_coord(p, seq, rank);
+        float r0[2][kTapMaxN];
+#pragma unroll
+        for (int sub = 0; sub < 2; ++sub) {
+#pragma unroll
+          for (int kh = 0; kh < 3; ++kh) {
+            const int c0 = kh * 3 * kTapMaxN, lo = c0 / 16 * 16;
+            uint32_t raw[48];
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(acc * acc_stride + sub * kTapRows + lo);
+            tmem_ld_32x32b_x16(taddr, raw);
+            tmem_ld_32x32b_x16(taddr + 16u, raw + 16);
+            tmem_ld_32x32b_x16(taddr + 32u, raw + 32);
+            tmem_ld_wait();
+#pragma unroll
+            for (int n = 0; n < kTapMaxN; ++n) {
+              const int o = c0 - lo + n;
+              float v = __uint_as_float(raw[o]);
+              v += __shfl_down_sync(0xffffffffu, __uint_as_float(raw[o + kTapMaxN]), 1);
+              v += __shfl_down_sync(0xffffffffu, __uint_as_float(raw[o + 2 * kTapMaxN]), 2);
+              if (kh == 0) r0[sub][n] = v;
+              else scr[((kh - 1) * kTapMaxN + n) * kTapBoxPx + sub * kBlockM + m] = v;
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&acce_bar[acc]);  // every TMEM read of this accumulator is done
+        epi_bar_sync();
+#pragma unroll
+        for (int sub = 0; sub < 2; ++sub) {
+          const int px = sub * kBlockM + m;
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          if ((px >> 4) < 14 && (px & 15) < 14) {  // an output pixel: px + 32 stays inside the box
+#pragma unroll
+            for (int n = 0; n < kTapMaxN; ++n)
+              v[n] = r0[sub][n] + scr[n * kTapBoxPx + px + 16] + scr[(kTapMaxN + n) * kTapBoxPx + px + 32];
+          }
+          epilogue_chunk(p, tc, px, tc.n0, v, lane);  // (n0 = 0: one weight tile)
+        }
+        epi_bar_sync();  // scratch is read before the next tile writes it
+      }
+    }
+    for (int seq = seq0; seq < p.seq_count && !(!kPair && p.halo == 2); seq += seq_step, ++it) {
       const int acc = it & 1, u = it >> 1;
       if (!mbar_wait(&accf_bar[acc], u & 1, p.fault, p.limit_ns, 5)) break;
       tc_fence_after();
@@ -904,13 +996,18 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   p.halo = (a.mode == 0 && p.BN <= 64 && !p.fp8 && (!a.out_ncthw || a.natural || a.N_real <= 16) && halo_mode_enabled())
                ? 1
                : 0;
+  if (a.tap_stacked) {  // weights packed tap-stacked (the caller decides, as it packs them)
+    if (a.mode != 0 || p.fp8 || a.N_real > kTapMaxN || p.BN != 16 || !halo_mode_enabled()) return cudaErrorInvalidValue;
+    p.halo = 2;
+  }
   // halo mode: sub-tiles of 8 x 16 box pixels; two accumulators of msub x 3 BN columns must fit TMEM
-  if (p.halo) p.msub = 2 * 2 * 3 * p.BN <= 512 ? 2 : 1;
+  if (p.halo == 1) p.msub = 2 * 2 * 3 * p.BN <= 512 ? 2 : 1;
+  if (p.halo == 2) p.msub = 2;
   const bool mma_pair =
       mma_pair_enabled() && (p.BN == 256 || p.BN == 128) && (a.mode == 0 || a.batch == 1) && !p.halo;
   const bool want_pair = mma_pair;
   p.tmem_cols = 32;
-  while (p.tmem_cols < 2 * p.msub * (p.halo ? 3 * p.BN : p.BN)) p.tmem_cols <<= 1;  // two accumulators
+  while (p.tmem_cols < 2 * p.msub * (p.halo == 2 ? kTapRows : p.halo ? 3 * p.BN : p.BN)) p.tmem_cols <<= 1;
   if (p.tmem_cols > 512) return cudaErrorInvalidValue;
   const uint32_t kb_bytes = kABytes * p.msub + static_cast<uint32_t>(mma_pair ? p.BN / 2 : p.BN) * kBlockK * 2;
   // MMA pairs take two k blocks per stage (half the barrier round trips per MMA) where two such stages
@@ -919,17 +1016,28 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   const int kb_even = a.mode == 0 ? (a.C_in_pad / p.kc) % 2 == 0 : (a.K / kBlockK) % 2 == 0;
   p.ks = (mma_pair && kb_even && 2u * 2u * kb_bytes <= 200u * 1024u) ? 2 : 1;
   uint32_t stage_bytes = static_cast<uint32_t>(p.ks) * kb_bytes;
-  if (p.halo) {
+  if (p.halo == 1) {
     // box of (8 msub + 2) x 16 pixels x 64 channels, then the 9 taps' BN x 64 weight tiles
     const uint32_t box = static_cast<uint32_t>(8 * p.msub + 2) * (kHaloCols + 2) * kBlockK * 2;
     p.halo_a_bytes = (box + 1023u) & ~1023u;
     p.halo_tx = box + 9u * static_cast<uint32_t>(p.BN) * kBlockK * 2;
     p.halo_stage = p.halo_a_bytes + 9u * static_cast<uint32_t>(p.BN) * kBlockK * 2;
+  } else if (p.halo == 2) {
+    // box of 16 x 16 pixels x 64 channels, then one kTapRows x 64 tap-stacked weight tile
+    const uint32_t box = static_cast<uint32_t>(kTapBoxPx) * kBlockK * 2;
+    p.halo_a_bytes = box;
+    p.halo_tx = box + static_cast<uint32_t>(kTapRows) * kBlockK * 2;
+    p.halo_stage = p.halo_tx;
+  }
+  if (p.halo) {
     p.ks = 1;
     stage_bytes = p.halo_stage;
   }
   p.stages = std::min(8, static_cast<int>((200u * 1024u) / stage_bytes));
   if (p.stages < 2) return cudaErrorInvalidValue;
+  // barriers after the stages, then (tap-stacked) the epilogue's exchange of the kh = 1, 2 partial sums
+  p.scratch_off = static_cast<uint32_t>(p.stages) * stage_bytes + (2u * p.stages + 4u) * 8u + 16u;
+  const uint32_t scratch_bytes = p.halo == 2 ? 2u * kTapMaxN * kTapBoxPx * 4u : 0u;
   p.bias = a.bias;
   p.residual = a.residual;
   p.res_f32 = a.res_f32;
@@ -950,7 +1058,7 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
     for (int i = 0; i <= a.nph; ++i) p.ph_edges[i] = a.ph_edges[i];
     for (int j = 0; j <= a.npw; ++j) p.pw_edges[j] = a.pw_edges[j];
     p.cols_t = p.halo ? kHaloCols : pick_cols(a.pw_edges, a.npw);
-    p.rows_t = p.halo ? 8 * p.msub : kBlockM * p.msub / p.cols_t;
+    p.rows_t = p.halo == 2 ? 14 : p.halo ? 8 * p.msub : kBlockM * p.msub / p.cols_t;
     p.trow_prefix[0] = 0;
     for (int i = 0; i < a.nph; ++i)
       p.trow_prefix[i + 1] = p.trow_prefix[i] + (a.ph_edges[i + 1] - a.ph_edges[i] + p.rows_t - 1) / p.rows_t;
@@ -991,6 +1099,12 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
     uint64_t wd[2] = {K, (uint64_t)a.N_pad};
     uint64_t ws[1] = {K * eb};
     uint32_t wb[2] = {(uint32_t)p.kc, (uint32_t)(want_pair ? p.BN / 2 : p.BN)};
+    if (p.halo == 2) {  // [3 kt][kTapRows][C]: one kTapRows-row tile per (kt, channel chunk)
+      wd[0] = C;
+      wd[1] = 3ull * kTapRows;
+      ws[0] = C * eb;
+      wb[1] = static_cast<uint32_t>(kTapRows);
+    }
     if (!make_map(&tmB, a.w, 2, wd, ws, wb, p.fp8)) return cudaErrorInvalidValue;
     n_blocks = static_cast<long long>(a.B) * a.T * p.n_trows * p.n_tcols * p.n_ntiles;
   } else {
@@ -1027,7 +1141,8 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   }
-  const size_t smem = 1024 + static_cast<size_t>(p.stages) * stage_bytes + (2 * p.stages + 4) * 8 + 16;
+  const size_t smem = 1024 + static_cast<size_t>(p.scratch_off) + scratch_bytes;
+  if (smem > 227u * 1024u) return cudaErrorInvalidValue;
   int n_sm = 0;
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);

@@ -49,7 +49,16 @@ struct ConvTcArgs {
   int fp8; const float* wscale;
   // weight rows in PyTorch channel order (packed with natural != 0); required for NCTHW outputs
   int natural;
+  // conv mode, weights packed tap-stacked (see kTapRows): all 9 spatial taps in one MMA
+  int tap_stacked;
 };
+
+// Narrow bf16 convs (at most kTapMaxN output channels) pack their weights tap-stacked: for each temporal
+// tap kt one K-major tile of kTapRows rows, row (kh*3 + kw) * kTapMaxN + n holding output column n of
+// spatial tap (kh, kw) (zero rows beyond 9 * kTapMaxN and beyond the real columns): [3][kTapRows][C_in_pad].
+constexpr int kTapMaxN = 12;
+constexpr int kTapRows = 112;  // 9 * 12 = 108 rounded up to a multiple of 16
+inline bool conv_tap_stacked(int N_real, int fp8) { return !fp8 && N_real <= kTapMaxN; }
 cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t s);
 
 // CUDA-core convolution (any channel count, fp32 or bf16 storage, fp32 accumulation).
@@ -69,7 +78,7 @@ cudaError_t launch_conv_simt(const ConvSimtArgs& a, cudaStream_t s);
 // chunk is 32 channels of one sub-position; natural != 0 keeps PyTorch's channel order (c*S + sub),
 // which convs storing NCTHW pixels use (a chunk then holds whole runs of horizontally adjacent pixels).
 cudaError_t launch_pack_weights_bf16(const float* w, int C_out, int C_in, int C_in_pad, int N_pad, int S,
-                                     void* out, cudaStream_t s, int natural = 0);
+                                     void* out, cudaStream_t s, int natural = 0, int tap_stacked = 0);
 cudaError_t launch_pack_weights_f32(const float* w, int C_out, int C_in, void* out, cudaStream_t s);
 cudaError_t launch_pack_matrix_bf16(const float* w, int rows, int cols, void* out, cudaStream_t s);
 // e4m3 K-major [N_pad, 27 * C_in_pad] (rows as the bf16 packing), each row scaled by its own

@@ -459,51 +459,48 @@ template <> struct Raw8<float> {
 };
 
 // VPL vectors per lane per pixel; each team takes NP = kRmsVecs / VPL consecutive pixels per step and
-// issues all their loads before any sum, then reduces the NP sums side by side.
+// issues all their loads before any sum, then reduces the NP sums side by side.  A warp step covers
+// one chunk of 32 / team * NP pixels of one frame, so a step costs one 32-bit division for its frame
+// and chunk and none per pixel.
 template <typename TI, typename TO, int VPL>
 __global__ void __launch_bounds__(256) rms_apply_kernel(const __grid_constant__ RmsParams p) {
   constexpr int NP = kRmsVecs / VPL;
   const int lane = threadIdx.x & 31;
   const int L = p.team;
   const int sub = lane & (L - 1);
-  const int teams_per_warp = 32 / L;
-  const int64_t hw = static_cast<int64_t>(p.H) * p.W;
-  const int64_t npx = static_cast<int64_t>(p.B) * p.T * hw;
-  const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int per_step = (32 / L) * NP;  // pixels per warp step, all in one frame
+  const int hw = p.H * p.W;
+  const int n_chunks = (hw + per_step - 1) / per_step;
+  const int items = p.B * p.T * n_chunks;
+  const int warp_id = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int n_warps = static_cast<int>((gridDim.x * blockDim.x) >> 5);
   const float inv_c = 1.0f / static_cast<float>(p.C);
-  const int64_t per_step = static_cast<int64_t>(teams_per_warp) * NP;  // pixels per warp step
-  for (int64_t base = warp_id * per_step; base < npx; base += n_warps * per_step) {
-    const int64_t px0 = base + static_cast<int64_t>(lane / L) * NP;
+  for (int item = warp_id; item < items; item += n_warps) {
+    const int f = item / n_chunks;
+    const int r0 = (item - f * n_chunks) * per_step + (lane / L) * NP;
+    const int b = f / p.T, t = f - b * p.T;
+    const TI* xf = static_cast<const TI*>(p.x) + (static_cast<int64_t>(b) * p.x_T_alloc + t) * hw * p.C;
+    TO* yf = static_cast<TO*>(p.y) + (static_cast<int64_t>(b) * p.y_T_alloc + t) * hw * p.C;
     Raw8<TI> raw[NP][VPL];
-    const TI* xp[NP];
-    TO* yp[NP];
-    bool valid[NP];
 #pragma unroll
-    for (int k = 0; k < NP; ++k) {
-      const int64_t px = px0 + k;
-      valid[k] = px < npx;
-      const int64_t f = valid[k] ? px / hw : 0;
-      const int64_t r = valid[k] ? px - f * hw : 0;
-      const int b = static_cast<int>(f / p.T), t = static_cast<int>(f - (f / p.T) * p.T);
-      xp[k] = static_cast<const TI*>(p.x) + ((static_cast<int64_t>(b) * p.x_T_alloc + t) * hw + r) * p.C;
-      yp[k] = static_cast<TO*>(p.y) + ((static_cast<int64_t>(b) * p.y_T_alloc + t) * hw + r) * p.C;
+    for (int k = 0; k < NP; ++k)
+      if (r0 + k < hw) {
 #pragma unroll
-      for (int j = 0; j < VPL; ++j)
-        if (valid[k]) raw[k][j].load(xp[k] + (j * L + sub) * 8);
-    }
+        for (int j = 0; j < VPL; ++j) raw[k][j].load(xf + static_cast<int64_t>(r0 + k) * p.C + (j * L + sub) * 8);
+      }
     float ss[NP];
 #pragma unroll
     for (int k = 0; k < NP; ++k) {
       ss[k] = 0.f;
+      if (r0 + k < hw) {
 #pragma unroll
-      for (int j = 0; j < VPL; ++j)
-        if (valid[k]) {
+        for (int j = 0; j < VPL; ++j) {
           float v[8];
           raw[k][j].get(v);
 #pragma unroll
           for (int e = 0; e < 8; ++e) ss[k] = fmaf(v[e], v[e], ss[k]);
         }
+      }
     }
     for (int off = L >> 1; off > 0; off >>= 1)
 #pragma unroll
@@ -518,7 +515,7 @@ __global__ void __launch_bounds__(256) rms_apply_kernel(const __grid_constant__ 
       const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
       for (int k = 0; k < NP; ++k) {
-        if (!valid[k]) continue;
+        if (r0 + k >= hw) continue;
         const float rr = 1.0f / sqrtf(ss[k] * inv_c + p.eps);
         float v[8], o[8];
         raw[k][j].get(v);
@@ -527,7 +524,7 @@ __global__ void __launch_bounds__(256) rms_apply_kernel(const __grid_constant__ 
           const float z = fmaf(v[e] * rr, gg[e], bb[e]);
           o[e] = p.silu ? __fdividef(z, 1.0f + __expf(-z)) : z;
         }
-        vstore8(yp[k] + c0, o, p.fault);
+        vstore8(yf + static_cast<int64_t>(r0 + k) * p.C + c0, o, p.fault);
       }
     }
   }
@@ -554,7 +551,8 @@ cudaError_t launch_rms(const GnArgs& a, cudaStream_t s) {
   const int64_t npx = static_cast<int64_t>(a.B) * a.T * a.H * a.W;
   if (npx == 0) return cudaSuccess;
   const int64_t per_warp = static_cast<int64_t>(32 / p.team) * (kRmsVecs / p.vpl);
-  const int64_t warps = (npx + per_warp - 1) / per_warp;
+  const int64_t warps = static_cast<int64_t>(a.B) * a.T * ((static_cast<int64_t>(a.H) * a.W + per_warp - 1) / per_warp);
+  if (warps >= (1LL << 30) || static_cast<int64_t>(a.H) * a.W >= (1LL << 30)) return cudaErrorInvalidValue;  // 32-bit indexing
   const int blocks = static_cast<int>(std::min<int64_t>((warps + 7) / 8, 152LL * 8));
 #define VAE_RMS(VPL)                                                                                     \
   if (a.y_fp8 && a.x_f32) rms_apply_kernel<float, __nv_fp8_e4m3, VPL><<<blocks, 256, 0, s>>>(p);         \
@@ -1545,34 +1543,56 @@ __global__ void fold_frames_kernel(const TI* x, int xTa, int B, int T, int H, in
   }
 }
 
-// one thread per (output pixel, input channel c): for each of the S sub-positions one read of channel c of
-// an input pixel (consecutive threads: consecutive c, coalesced) and one write of output channel
-// c*S + sub (the S writes of a thread are contiguous)
+// 4 consecutive input channels as floats (one 16- or 8-byte load)
+VAE_DEV void load4f(const float* p, float* v) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+}
+VAE_DEV void load4f(const __nv_bfloat16* p, float* v) {
+  const uint2 a = *reinterpret_cast<const uint2*>(p);
+  const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.x));
+  const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.y));
+  v[0] = lo.x; v[1] = lo.y; v[2] = hi.x; v[3] = hi.y;
+}
+
+// one thread per (output pixel, run of 4 input channels c0..c0+3): S vector reads (one per sub-position,
+// consecutive threads reading consecutive channels of the same input pixel) and one contiguous run of
+// 4*S output channels c*S + sub written as 16-byte vectors; 32-bit index arithmetic once per thread
 template <typename TI, typename TO, int S>
-__global__ void fold_frames_s_kernel(const TI* x, int xTa, int B, int T, int H, int W, int C, int st, int sh, int sw,
+__global__ void fold_frames_v_kernel(const TI* x, int xTa, int B, int T, int H, int W, int C, int st, int sh, int sw,
                                      TO* y, int yTa, uint32_t* fault) {
+  constexpr int CPT = 4;
   const int To = (T + st - 1) / st, Ho = H / sh, Wo = W / sw;
-  const int64_t n = static_cast<int64_t>(B) * To * Ho * Wo * C;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int c = static_cast<int>(i % C);
-    int64_t r = i / C;
-    const int xo = static_cast<int>(r % Wo);
+  const int team = C / CPT;
+  const int n = B * To * Ho * Wo * team;  // < 2^30 (the launcher checks)
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const int j = i % team;
+    int r = i / team;
+    const int xo = r % Wo;
     r /= Wo;
-    const int yo = static_cast<int>(r % Ho);
+    const int yo = r % Ho;
     r /= Ho;
-    const int to = static_cast<int>(r % To);
-    const int b = static_cast<int>(r / To);
-    TO* dst = y + ((((static_cast<int64_t>(b) * yTa + to) * Ho + yo) * Wo + xo) * C + c) * S;
+    const int to = r % To;
+    const int b = r / To;
+    const int c0 = j * CPT;
+    float v[S][CPT];
 #pragma unroll
     for (int sub = 0; sub < S; ++sub) {
       const int dt = sub / (sh * sw), dy = (sub / sw) % sh, dx = sub % sw;
       const int ti = max(st * to + dt - (st - 1), 0);
-      const float val =
-          to_f<TI>(x[(((static_cast<int64_t>(b) * xTa + ti) * H + (sh * yo + dy)) * W + (sw * xo + dx)) * C + c]);
-      if (sizeof(TO) == 1 && !(fabsf(val) <= 448.f)) raise_fault(fault, FAULT_RANGE, 25);
-      dst[sub] = from_f<TO>(val);
+      load4f(x + ((static_cast<int64_t>(b) * xTa + ti) * H + (sh * yo + dy)) * static_cast<int64_t>(W) * C +
+                 static_cast<int64_t>(sw * xo + dx) * C + c0,
+             v[sub]);
     }
+    float o[CPT * S];
+#pragma unroll
+    for (int cc = 0; cc < CPT; ++cc)
+#pragma unroll
+      for (int sub = 0; sub < S; ++sub) o[cc * S + sub] = v[sub][cc];
+    TO* dst = y + (((static_cast<int64_t>(b) * yTa + to) * Ho + yo) * Wo + xo) * static_cast<int64_t>(C) * S +
+              static_cast<int64_t>(c0) * S;
+#pragma unroll
+    for (int q = 0; q < CPT * S; q += 8) vstore8(dst + q, o + q, fault);
   }
 }
 
@@ -1580,25 +1600,25 @@ cudaError_t launch_fold_frames(const void* x, int x_f32, int x_T_alloc, int B, i
                                int sh, int sw, void* y, int y_kind, int y_T_alloc, cudaStream_t s) {
   if (st < 1 || sh < 1 || sw < 1 || H % sh || W % sw) return cudaErrorInvalidValue;
   const int S = st * sh * sw;
-  if (S == 4 || S == 8) {
-    const int64_t nt = static_cast<int64_t>(B) * ((T + st - 1) / st) * (H / sh) * (W / sw) * C;
-    if (nt <= 0) return cudaSuccess;
-    const int bl = static_cast<int>(std::min<int64_t>((nt + 255) / 256, 152 * 16));
+  const int64_t nv = static_cast<int64_t>(B) * ((T + st - 1) / st) * (H / sh) * (W / sw) * (C / 4);
+  if ((S == 4 || S == 8) && C % 4 == 0 && nv < (1LL << 30)) {
+    if (nv <= 0) return cudaSuccess;
+    const int bl = static_cast<int>(std::min<int64_t>((nv + 255) / 256, 152 * 16));
     uint32_t* fs = fault_word();
-#define VAE_FOLDS(TI, TO, SS)                                                                                       \
-  fold_frames_s_kernel<TI, TO, SS><<<bl, 256, 0, s>>>(static_cast<const TI*>(x), x_T_alloc, B, T, H, W, C, st, sh, sw, \
+#define VAE_FOLDV(TI, TO, SS)                                                                                       \
+  fold_frames_v_kernel<TI, TO, SS><<<bl, 256, 0, s>>>(static_cast<const TI*>(x), x_T_alloc, B, T, H, W, C, st, sh, sw, \
                                                       static_cast<TO*>(y), y_T_alloc, fs)
-#define VAE_FOLDS_T(TI, SS)                                   \
-  if (y_kind == 1) VAE_FOLDS(TI, float, SS);                  \
-  else if (y_kind == 2) VAE_FOLDS(TI, __nv_fp8_e4m3, SS);     \
-  else VAE_FOLDS(TI, __nv_bfloat16, SS);
+#define VAE_FOLDV_T(TI, SS)                                   \
+  if (y_kind == 1) VAE_FOLDV(TI, float, SS);                  \
+  else if (y_kind == 2) VAE_FOLDV(TI, __nv_fp8_e4m3, SS);     \
+  else VAE_FOLDV(TI, __nv_bfloat16, SS);
     if (x_f32) {
-      if (S == 4) { VAE_FOLDS_T(float, 4) } else { VAE_FOLDS_T(float, 8) }
+      if (S == 4) { VAE_FOLDV_T(float, 4) } else { VAE_FOLDV_T(float, 8) }
     } else {
-      if (S == 4) { VAE_FOLDS_T(__nv_bfloat16, 4) } else { VAE_FOLDS_T(__nv_bfloat16, 8) }
+      if (S == 4) { VAE_FOLDV_T(__nv_bfloat16, 4) } else { VAE_FOLDV_T(__nv_bfloat16, 8) }
     }
-#undef VAE_FOLDS_T
-#undef VAE_FOLDS
+#undef VAE_FOLDV_T
+#undef VAE_FOLDV
     return cudaGetLastError();
   }
   const int64_t n = static_cast<int64_t>(B) * ((T + st - 1) / st) * (H / sh) * (W / sw) * C * st * sh * sw;
@@ -1667,8 +1687,36 @@ __global__ void pack_bf16_kernel(const float* w, int C_out, int C_in, int C_in_p
   }
 }
 
+// tap-stacked packing of a narrow conv: [3 kt][kTapRows][C_in_pad], row (kh*3 + kw) * kTapMaxN + np
+__global__ void pack_tap_bf16_kernel(const float* w, int C_out, int C_in, int C_in_pad, int S, int natural,
+                                     __nv_bfloat16* out) {
+  const int64_t n = 3LL * kTapRows * C_in_pad;
+  const int Cd = C_out / S;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int ci = static_cast<int>(i % C_in_pad);
+    const int row = static_cast<int>((i / C_in_pad) % kTapRows);
+    const int kt = static_cast<int>(i / (static_cast<int64_t>(kTapRows) * C_in_pad));
+    const int t9 = row / kTapMaxN, np = row % kTapMaxN;
+    float v = 0.f;
+    if (t9 < 9 && np < C_out && ci < C_in) {
+      const int sub = np / Cd, c = np % Cd;
+      const int co = natural ? np : c * S + sub;
+      v = w[(static_cast<int64_t>(co) * C_in + ci) * 27 + kt * 9 + t9];
+    }
+    out[i] = f2bf(v);
+  }
+}
+
 cudaError_t launch_pack_weights_bf16(const float* w, int C_out, int C_in, int C_in_pad, int N_pad, int S, void* out,
-                                     cudaStream_t s, int natural) {
+                                     cudaStream_t s, int natural, int tap_stacked) {
+  if (tap_stacked) {
+    if (C_out > kTapMaxN) return cudaErrorInvalidValue;
+    const int64_t n = 3LL * kTapRows * C_in_pad;
+    const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 152 * 64));
+    pack_tap_bf16_kernel<<<blocks, 256, 0, s>>>(w, C_out, C_in, C_in_pad, S, natural, static_cast<__nv_bfloat16*>(out));
+    return cudaGetLastError();
+  }
   const int64_t n = static_cast<int64_t>(N_pad) * 27 * C_in_pad;
   const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 152 * 64));
   pack_bf16_kernel<<<blocks, 256, 0, s>>>(w, C_out, C_in, C_in_pad, N_pad, S, natural,

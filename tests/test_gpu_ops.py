@@ -106,6 +106,11 @@ CONV_CASES = [
     # narrow convs (at most 32 channels): one shared halo box per (kt, channel chunk)
     (1, 3, 21, 19, 128, 32, 2, 3, 2, (1, 1, 1), False, False, True),
     (2, 2, 35, 17, 64, 16, 3, 1, 0, (1, 2, 2), False, True, False),
+    # at most 12 channels: tap-stacked weights (all 9 spatial taps in one MMA of N = 112)
+    (2, 3, 30, 33, 128, 12, 3, 2, 2, (1, 2, 2), False, True, False),
+    (1, 3, 29, 31, 64, 8, 2, 3, 0, (1, 1, 1), False, False, True),
+    (1, 2, 17, 45, 192, 3, 1, 4, 2, (1, 1, 1), False, True, False),
+    (1, 4, 15, 14, 64, 12, 1, 1, 0, (2, 1, 2), True, False, False),
 ]
 
 
@@ -140,11 +145,32 @@ def test_conv_bit_identical_across_patch_counts(vd, dt):
         np.testing.assert_array_equal(o, outs[0])
 
 
-def test_conv_halo_path_bit_identical_across_patch_counts(vd):
-    outs = [_conv_case(vd, 1, 2, 40, 36, 64, 16, ph, pw, 2, (1, 1, 1), False, False, vd.VAE_BF16, True, 45)[0]
+@pytest.mark.parametrize("Co,d2s,ncthw", [(16, (1, 1, 1), False), (12, (1, 2, 2), True), (8, (1, 1, 1), False)])
+def test_conv_halo_path_bit_identical_across_patch_counts(vd, Co, d2s, ncthw):
+    outs = [_conv_case(vd, 1, 2, 40, 36, 64, Co, ph, pw, 2, d2s, False, ncthw, vd.VAE_BF16, d2s == (1, 1, 1), 45)[0]
             for ph, pw in ((1, 1), (2, 2), (3, 4), (5, 2))]
     for o in outs[1:]:
         np.testing.assert_array_equal(o, outs[0])
+
+
+@pytest.mark.parametrize("Co,Ci,d2s,ncthw", [(12, 64, (1, 2, 2), True), (8, 128, (1, 1, 1), False),
+                                             (12, 64, (1, 2, 2), False)])
+def test_tap_stacked_weight_packing(vd, Co, Ci, d2s, ncthw):
+    # [3 kt][112 rows][Ci]: row (kh*3 + kw)*12 + n holds packed column n of tap (kh, kw), the columns in
+    # PyTorch order for NCTHW outputs, else (depth-to-space sub-position, channel); zeros elsewhere
+    w = synth.conv_weight(Co, Ci, 6)
+    d = vd.conv_desc(1, 1, 4, 4, Ci, Co, [0, 4], [0, 4], d2s=d2s, out_ncthw=ncthw)
+    wp = vd.conv3d_pack_weights(torch.from_numpy(w).cuda(), d).cpu()
+    assert wp.numel() * wp.element_size() == 3 * 112 * Ci * 2
+    got = wp.view(torch.bfloat16).float().numpy().reshape(3, 112, Ci)
+    S = d2s[0] * d2s[1] * d2s[2]
+    Cd = Co // S
+    co = np.arange(Co) if ncthw else np.array([(n % Cd) * S + n // Cd for n in range(Co)])
+    wr = torch.from_numpy(w).to(torch.bfloat16).float().numpy().reshape(Co, Ci, 3, 9)
+    want = np.zeros((3, 112, Ci), np.float32)
+    for t9 in range(9):
+        want[:, t9 * 12:t9 * 12 + Co] = wr[co][:, :, :, t9].transpose(2, 0, 1)
+    np.testing.assert_array_equal(got, want)
 
 
 # ----------------------------------------------------------------------------- channel RMS norm

@@ -610,6 +610,24 @@ def run_ops(args, torch, vd, peaks, flush):
     res["tile_blend"] = {"workload": f"{len(meta)} tiles of up to [1,3,81,256,256] bf16, 64 px overlap -> "
                                      "[1,3,81,704,1280]", "ms": ms, "bytes": nbytes, "gbs": nbytes / ms / 1e6,
                          "frac_of_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"], "bound": "hbm"}
+    del tiles, outb, blend
+    # (d) the blend of the batch-2 overlap-tiled LTX decode: 45 tiles overlapping in time and space
+    cfg, tl = synth.LTX_TILED, synth.LTX_TILING
+    st, ss, _ = cfg.scale()
+    meta = vd.tile_plan(cfg.latent_shape[2:], tl.tile, tl.overlap, st, ss)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(201)
+    tiles = [torch.randn((2, 3, m["pix"][1], m["pix"][3], m["pix"][5]), generator=gen, device="cuda").to(torch.bfloat16)
+             for m in meta]
+    outb = torch.empty(cfg.output_shape(), dtype=torch.bfloat16, device="cuda")
+    blend = vd.prepare_tile_blend(tiles, meta, outb)
+    ms = _time(torch, blend, args.steps, flush)
+    nbytes = sum(t.numel() for t in tiles) * 2 + outb.numel() * 2
+    res["tile_blend_ltx_tiled"] = {"workload": f"{len(meta)} tiles of up to [2,3,57,512,512] bf16 (overlap 8 frames, "
+                                               f"128 px) -> {list(cfg.output_shape())}", "ms": ms, "bytes": nbytes,
+                                   "gbs": nbytes / ms / 1e6, "frac_of_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"],
+                                   "bound": "hbm"}
+    del tiles, outb, blend
     return res
 
 

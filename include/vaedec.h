@@ -170,7 +170,9 @@ vae_status_t vae_decode_chunk(vae_decoder_t* dec, const void* latent_chunk, cons
 
 /* Overlap-tiled decode ([TP] Approach): tiles of tile_thw latent frames/rows/cols overlapping by
  * ovl_thw (host arrays) are planned with `vae_tile_plan`, each decoded causally on its own, and
- * blended with `vae_tile_blend`.  The result differs from `vae_decode` inside overlaps by design. */
+ * blended with `vae_tile_blend`.  The result differs from `vae_decode` inside overlaps by design.
+ * Tiles of one latent shape are decoded together as one batch (up to 16 GiB of workspace per batch);
+ * each tile's pixels are bit-identical to `vae_decode` of that tile's latent box on its own. */
 vae_status_t vae_decode_tiled(vae_decoder_t* dec, const void* latent, const int64_t latent_shape[5],
                               void* out, const int tile_thw[3], const int ovl_thw[3], void* stream);
 
@@ -263,7 +265,8 @@ vae_status_t vae_encode(vae_encoder_t* enc, const void* video, const int64_t vid
 /* Overlap-tiled encode ([ENC] encode_tile_split / exec / merge): spatial tiles planned on the latent grid
  * by the tile plan's rule (tile_hw latent rows/cols, overlap ovl_hw), each tile's pixels encoded on
  * their own, the latent tiles blended with the decode's ramps and normalised weighted sum (in latent
- * units, the whole clip in time).  Same shapes as vae_encode. */
+ * units, the whole clip in time).  Same shapes as vae_encode.  Tiles of one shape are encoded together
+ * as one batch (up to 16 GiB of workspace per batch), each bit-identical to encoding it on its own. */
 vae_status_t vae_encode_tiled(vae_encoder_t* enc, const void* video, const int64_t video_shape[5], void* moments,
                               const int tile_hw[2], const int ovl_hw[2], void* stream);
 

@@ -833,8 +833,10 @@ vae_status_t run_attention(Ctx& x, const Level& L) {
 
 // Decode one chunk (or the whole latent) into out (NCTHW, out_T_alloc frames per (b, c)).
 // lat_full = (T, H, W) of the latent tensor, lat_box = (t0, h0, w0) of the decoded box.
-vae_status_t run_decode(vae_decoder* d, const Plan& p, const float* latent, const int lat_full[3], const int lat_box[3],
-                        void* out, int out_T_alloc, bool chunked, cudaStream_t s) {
+// Decode p.B = n_boxes x B_lat items: the latent boxes lat_boxes[3 i .. 3 i + 2] (t0, h0, w0) of the B_lat items
+// of `latent` (full extent lat_full), box after box along the batch (tiles of one shape decode together).
+vae_status_t run_decode(vae_decoder* d, const Plan& p, const float* latent, const int lat_full[3], const int* lat_boxes,
+                        int n_boxes, void* out, int out_T_alloc, bool chunked, cudaStream_t s) {
   Ctx x{d, &p, carve(d->ws, p), s, chunked};
   const vae_config_t& c = d->cfg;
   const int rf = res_bytes(d) == 4;
@@ -844,10 +846,14 @@ vae_status_t run_decode(vae_decoder* d, const Plan& p, const float* latent, cons
     const Level& L0 = p.lv[0];
     const int Cp = d->conv_in.C_in_pad;
     const int64_t fb = static_cast<int64_t>(p.h) * p.w * Cp * act_bytes(d);
-    {
-      Prof pr(d, s, K_LATENT, 0, static_cast<double>(p.B) * p.Tlat * p.h * p.w * (c.latent_c * 4.0 + Cp * act_bytes(d)));
-      CK(launch_latent_to_cl(latent, p.B, c.latent_c, lat_full[0], lat_full[1], lat_full[2], lat_box[0], p.Tlat,
-                             lat_box[1], p.h, lat_box[2], p.w, Cp, x.b.hin + 2 * fb, d->f32, p.Tlat + 2, s));
+    if (n_boxes < 1 || p.B % n_boxes) return set_err(&d->err, VAE_ERR_INVALID_ARG, 0, 0, "bad latent box batch");
+    const int Bl = p.B / n_boxes;
+    for (int i = 0; i < n_boxes; ++i) {
+      const int* bx = lat_boxes + 3 * i;
+      Prof pr(d, s, K_LATENT, 0, static_cast<double>(Bl) * p.Tlat * p.h * p.w * (c.latent_c * 4.0 + Cp * act_bytes(d)));
+      CK(launch_latent_to_cl(latent, Bl, c.latent_c, lat_full[0], lat_full[1], lat_full[2], bx[0], p.Tlat, bx[1], p.h,
+                             bx[2], p.w, Cp, x.b.hin + 2 * fb + static_cast<int64_t>(i) * Bl * (p.Tlat + 2) * fb, d->f32,
+                             p.Tlat + 2, s));
     }
     ConvOut o;
     o.y = x.b.x; o.y_f32 = rf; o.y_T_alloc = L0.T; o.stats_level = &L0;
@@ -950,7 +956,7 @@ extern "C" vae_status_t vae_decode(vae_decoder_t* d, const void* latent, const i
   if (s) return s;
   const int full[3] = {static_cast<int>(shp[2]), static_cast<int>(shp[3]), static_cast<int>(shp[4])};
   const int box[3] = {0, 0, 0};
-  return run_decode(d, p, static_cast<const float*>(latent), full, box, out, p.lv.back().T, false,
+  return run_decode(d, p, static_cast<const float*>(latent), full, box, 1, out, p.lv.back().T, false,
                     static_cast<cudaStream_t>(stream));
 }
 
@@ -986,7 +992,7 @@ extern "C" vae_status_t vae_decode_chunk(vae_decoder_t* d, const void* latent, c
   d->cache_npw = npw;
   const int full[3] = {static_cast<int>(shp[2]), static_cast<int>(shp[3]), static_cast<int>(shp[4])};
   const int box[3] = {0, 0, 0};
-  return run_decode(d, p, static_cast<const float*>(latent), full, box, out, p.lv.back().T, true,
+  return run_decode(d, p, static_cast<const float*>(latent), full, box, 1, out, p.lv.back().T, true,
                     static_cast<cudaStream_t>(stream));
 }
 
@@ -1070,27 +1076,55 @@ extern "C" vae_status_t vae_decode_tiled(vae_decoder_t* d, const void* latent, c
   const int lat[3] = {static_cast<int>(shp[2]), static_cast<int>(shp[3]), static_cast<int>(shp[4])};
   std::vector<vae_tile_t> tl(VAE_MAX_TILES);
   int n = VAE_MAX_TILES;
+  constexpr size_t kTileBatchWorkspace = 16ull << 30;  // workspace budget of one batch of equal-shape tiles
   s = vae_tile_plan(lat, tile_thw, ovl_thw, st, ss, 1, tl.data(), &n);
   if (s) return set_err(&d->err, s, 0, 0, "tile plan failed (%d tiles max)", VAE_MAX_TILES);
-  const int B = static_cast<int>(shp[0]), Cl = c.latent_c;
+  const int B = static_cast<int>(shp[0]);
   const int ob = d->f32 ? 4 : 2;
-  // storage for every decoded tile (the blend gathers them)
-  size_t total = 0;
-  std::vector<size_t> off(n);
-  for (int i = 0; i < n; ++i) {
-    off[i] = total;
-    total += align_up(static_cast<size_t>(B) * c.out_c * tl[i].pix[1] * tl[i].pix[3] * tl[i].pix[5] * ob);
-  }
-  (void)Cl;
-  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  auto tile_bytes = [&](int i) {
+    return static_cast<size_t>(B) * c.out_c * tl[i].pix[1] * tl[i].pix[3] * tl[i].pix[5] * ob;
+  };
+  // Tiles of one latent shape decode together as one batch of K x B items (each item's arithmetic is
+  // the same whatever else is in the batch), K bounded by the workspace budget; a batch's tile outputs
+  // are contiguous, in the batch's tile order.
+  std::vector<std::vector<int>> batches;
   {
-    // workspace for the largest tile first, so the loop below allocates nothing
-    Plan pm;
-    s = make_plan(d, B, tl[0].lat[1], tl[0].lat[3], tl[0].lat[5], 1, 1, true, pm);
+    std::vector<char> taken(n, 0);
+    for (int i = 0; i < n; ++i) {
+      if (taken[i]) continue;
+      std::vector<int> grp;
+      for (int j = i; j < n; ++j)
+        if (!taken[j] && tl[j].lat[1] == tl[i].lat[1] && tl[j].lat[3] == tl[i].lat[3] && tl[j].lat[5] == tl[i].lat[5]) {
+          grp.push_back(j);
+          taken[j] = 1;
+        }
+      int K = tile_bytes(i) % 256 == 0 ? static_cast<int>(grp.size()) : 1;
+      while (K > 1) {
+        Plan pk;
+        s = make_plan(d, K * B, tl[i].lat[1], tl[i].lat[3], tl[i].lat[5], 1, 1, true, pk);
+        if (s) return s;
+        if (ws_total(pk) <= kTileBatchWorkspace) break;
+        --K;
+      }
+      for (size_t a = 0; a < grp.size(); a += K)
+        batches.emplace_back(grp.begin() + a, grp.begin() + std::min(grp.size(), a + K));
+    }
+  }
+  // storage for every decoded tile (the blend gathers them); workspace for the largest batch first, so
+  // the loop below allocates nothing
+  size_t total = 0;
+  std::vector<size_t> boff(batches.size());
+  for (size_t b = 0; b < batches.size(); ++b) {
+    boff[b] = total;
+    total += align_up(batches[b].size() * tile_bytes(batches[b][0]));
+    Plan pb;
+    const vae_tile_t& t = tl[batches[b][0]];
+    s = make_plan(d, static_cast<int>(batches[b].size()) * B, t.lat[1], t.lat[3], t.lat[5], 1, 1, true, pb);
     if (s) return s;
-    s = ensure_ws(d, pm);
+    s = ensure_ws(d, pb);
     if (s) return s;
   }
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
   if (d->tiles_bytes < total) {
     CK(cudaDeviceSynchronize());
     if (d->tiles) cudaFree(d->tiles);
@@ -1102,19 +1136,27 @@ extern "C" vae_status_t vae_decode_tiled(vae_decoder_t* d, const void* latent, c
   char* base = static_cast<char*>(d->tiles);
   std::vector<const void*> ptrs(n);
   const int full[3] = {lat[0], lat[1], lat[2]};
-  for (int i = 0; i < n; ++i) {
-    const vae_tile_t& t = tl[i];
+  for (size_t b = 0; b < batches.size(); ++b) {
+    const std::vector<int>& bt = batches[b];
+    const int K = static_cast<int>(bt.size());
+    const vae_tile_t& t = tl[bt[0]];
     Plan p;
-    s = make_plan(d, B, t.lat[1], t.lat[3], t.lat[5], 1, 1, true, p);
+    s = make_plan(d, K * B, t.lat[1], t.lat[3], t.lat[5], 1, 1, true, p);
     if (s) return s;
     s = check_gn_range(d, p);
     if (s) return s;
     s = ensure_ws(d, p);
     if (s) return s;
-    const int box[3] = {t.lat[0], t.lat[2], t.lat[4]};
-    s = run_decode(d, p, static_cast<const float*>(latent), full, box, base + off[i], p.lv.back().T, false, strm);
+    std::vector<int> boxes(3 * K);
+    for (int k = 0; k < K; ++k) {
+      boxes[3 * k] = tl[bt[k]].lat[0];
+      boxes[3 * k + 1] = tl[bt[k]].lat[2];
+      boxes[3 * k + 2] = tl[bt[k]].lat[4];
+      ptrs[bt[k]] = base + boff[b] + k * tile_bytes(bt[k]);
+    }
+    s = run_decode(d, p, static_cast<const float*>(latent), full, boxes.data(), K, base + boff[b], p.lv.back().T, false,
+                   strm);
     if (s) return s;
-    ptrs[i] = base + off[i];
   }
   vae_blend_desc_t bd{};
   bd.B = B; bd.C = c.out_c;
@@ -1290,8 +1332,10 @@ vae_status_t make_enc_plan(vae_encoder* e, int B, int T, int H, int W, int nph, 
 #define ERRP (&d->err)
 // Encode the pixel box rows [h0, h0 + H), cols [w0, w0 + W) (pixel units) of video [B, pix_c, T, Hf, Wf]
 // into moments NCTHW fp32 [B, 2*latent_c, T', h, w].
-vae_status_t run_encode(vae_encoder* e, const EncPlan& ep, const float* video, int Hf, int Wf, int h0, int w0,
-                        float* out, cudaStream_t s) {
+// Encode ep.p.B = n_boxes x B_v items: the pixel boxes (h0, w0) = boxes[2 i], boxes[2 i + 1] of the B_v videos
+// (full frames Hf x Wf), box after box along the batch.
+vae_status_t run_encode(vae_encoder* e, const EncPlan& ep, const float* video, int Hf, int Wf, const int* boxes,
+                        int n_boxes, float* out, cudaStream_t s) {
   vae_decoder* d = &e->core;
   const vae_encoder_config_t& c = e->ecfg;
   const Plan& p = ep.p;
@@ -1302,11 +1346,15 @@ vae_status_t run_encode(vae_encoder* e, const EncPlan& ep, const float* video, i
     const Level& L0 = p.lv[0];
     const int ob = op_bytes(d, e->conv_in);
     const int64_t fb = static_cast<int64_t>(ep.H0) * ep.W0 * e->conv_in.C_in_pad * ob;
-    {
-      Prof pr(d, s, K_LATENT, 0, static_cast<double>(p.B) * ep.T0 * ep.H0 * ep.W0 * (ep.Cin * 4.0 + e->conv_in.C_in_pad * ob));
-      CK(launch_pixels_to_cl(video, p.B, c.pix_c, ep.T0, Hf, Wf, c.patch_h, c.patch_w, h0 / c.patch_h, ep.H0,
-                             w0 / c.patch_w, ep.W0, e->conv_in.C_in_pad, x.b.hin + 2 * fb, kind_of(e->conv_in), ep.T0 + 2,
-                             s));
+    if (n_boxes < 1 || p.B % n_boxes) return set_err(&d->err, VAE_ERR_INVALID_ARG, 0, 0, "bad pixel box batch");
+    const int Bv = p.B / n_boxes;
+    for (int i = 0; i < n_boxes; ++i) {
+      const int h0 = boxes[2 * i], w0 = boxes[2 * i + 1];
+      Prof pr(d, s, K_LATENT, 0, static_cast<double>(Bv) * ep.T0 * ep.H0 * ep.W0 * (ep.Cin * 4.0 + e->conv_in.C_in_pad * ob));
+      CK(launch_pixels_to_cl(video, Bv, c.pix_c, ep.T0, Hf, Wf, c.patch_h, c.patch_w, h0 / c.patch_h, ep.H0,
+                             w0 / c.patch_w, ep.W0, e->conv_in.C_in_pad,
+                             x.b.hin + 2 * fb + static_cast<int64_t>(i) * Bv * (ep.T0 + 2) * fb, kind_of(e->conv_in),
+                             ep.T0 + 2, s));
     }
     ConvOut o;
     o.y = x.b.x; o.y_f32 = rf; o.y_T_alloc = L0.T; o.stats_level = &L0;
@@ -1495,7 +1543,8 @@ extern "C" vae_status_t vae_encode(vae_encoder_t* e, const void* video, const in
   if (s) return s;
   s = ensure_ws(&e->core, ep.p);
   if (s) return s;
-  return run_encode(e, ep, static_cast<const float*>(video), static_cast<int>(shp[3]), static_cast<int>(shp[4]), 0, 0,
+  const int box0[2] = {0, 0};
+  return run_encode(e, ep, static_cast<const float*>(video), static_cast<int>(shp[3]), static_cast<int>(shp[4]), box0, 1,
                     static_cast<float*>(moments), static_cast<cudaStream_t>(stream));
 }
 
@@ -1519,22 +1568,48 @@ extern "C" vae_status_t vae_encode_tiled(vae_encoder_t* e, const void* video, co
   const int ovl[3] = {0, ovl_hw[0], ovl_hw[1]};
   std::vector<vae_tile_t> tl(VAE_MAX_TILES);
   int n = VAE_MAX_TILES;
+  constexpr size_t kTileBatchWorkspace = 16ull << 30;  // workspace budget of one batch of equal-shape tiles
   s = vae_tile_plan(lat, tile, ovl, 1, 1, 0, tl.data(), &n);
   if (s) return set_err(&d->err, s, 0, 0, "tile plan failed (%d tiles max)", VAE_MAX_TILES);
   const int M = 2 * e->ecfg.latent_c;
-  size_t total = 0;
-  std::vector<size_t> off(n);
-  for (int i = 0; i < n; ++i) {
-    off[i] = total;
-    total += align_up(static_cast<size_t>(B) * M * tl[i].pix[1] * tl[i].pix[3] * tl[i].pix[5] * 4);
-  }
-  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  auto tile_bytes = [&](int i) { return static_cast<size_t>(B) * M * tl[i].pix[1] * tl[i].pix[3] * tl[i].pix[5] * 4; };
+  // tiles of one shape encode together as one batch (within the workspace budget), outputs contiguous
+  std::vector<std::vector<int>> batches;
   {
-    EncPlan pm;  // the first tile is the largest: size the workspace before anything is enqueued
-    s = make_enc_plan(e, B, static_cast<int>(shp[2]), tl[0].lat[3] * sh_tot, tl[0].lat[5] * sw_tot, 1, 1, pm);
-    if (!s) s = ensure_ws(d, pm.p);
+    std::vector<char> taken(n, 0);
+    for (int i = 0; i < n; ++i) {
+      if (taken[i]) continue;
+      std::vector<int> grp;
+      for (int j = i; j < n; ++j)
+        if (!taken[j] && tl[j].lat[3] == tl[i].lat[3] && tl[j].lat[5] == tl[i].lat[5]) {
+          grp.push_back(j);
+          taken[j] = 1;
+        }
+      int K = tile_bytes(i) % 256 == 0 ? static_cast<int>(grp.size()) : 1;
+      while (K > 1) {
+        EncPlan pk;
+        s = make_enc_plan(e, K * B, static_cast<int>(shp[2]), tl[i].lat[3] * sh_tot, tl[i].lat[5] * sw_tot, 1, 1, pk);
+        if (s) return s;
+        if (ws_total(pk.p) <= kTileBatchWorkspace) break;
+        --K;
+      }
+      for (size_t a = 0; a < grp.size(); a += K)
+        batches.emplace_back(grp.begin() + a, grp.begin() + std::min(grp.size(), a + K));
+    }
+  }
+  size_t total = 0;
+  std::vector<size_t> boff(batches.size());
+  for (size_t b = 0; b < batches.size(); ++b) {  // workspace before anything is enqueued
+    boff[b] = total;
+    total += align_up(batches[b].size() * tile_bytes(batches[b][0]));
+    const vae_tile_t& t = tl[batches[b][0]];
+    EncPlan pb;
+    s = make_enc_plan(e, static_cast<int>(batches[b].size()) * B, static_cast<int>(shp[2]), t.lat[3] * sh_tot,
+                      t.lat[5] * sw_tot, 1, 1, pb);
+    if (!s) s = ensure_ws(d, pb.p);
     if (s) return s;
   }
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
   if (d->tiles_bytes < total) {
     CK(cudaDeviceSynchronize());
     if (d->tiles) cudaFree(d->tiles);
@@ -1545,15 +1620,23 @@ extern "C" vae_status_t vae_encode_tiled(vae_encoder_t* e, const void* video, co
   }
   char* base = static_cast<char*>(d->tiles);
   std::vector<const void*> ptrs(n);
-  for (int i = 0; i < n; ++i) {
+  for (size_t b = 0; b < batches.size(); ++b) {
+    const std::vector<int>& bt = batches[b];
+    const int K = static_cast<int>(bt.size());
+    const vae_tile_t& t = tl[bt[0]];
     EncPlan ep;
-    s = make_enc_plan(e, B, static_cast<int>(shp[2]), tl[i].lat[3] * sh_tot, tl[i].lat[5] * sw_tot, 1, 1, ep);
+    s = make_enc_plan(e, K * B, static_cast<int>(shp[2]), t.lat[3] * sh_tot, t.lat[5] * sw_tot, 1, 1, ep);
     if (!s) s = ensure_ws(d, ep.p);
-    if (!s)
-      s = run_encode(e, ep, static_cast<const float*>(video), static_cast<int>(shp[3]), static_cast<int>(shp[4]),
-                     tl[i].lat[2] * sh_tot, tl[i].lat[4] * sw_tot, reinterpret_cast<float*>(base + off[i]), strm);
     if (s) return s;
-    ptrs[i] = base + off[i];
+    std::vector<int> boxes(2 * K);
+    for (int k = 0; k < K; ++k) {
+      boxes[2 * k] = tl[bt[k]].lat[2] * sh_tot;
+      boxes[2 * k + 1] = tl[bt[k]].lat[4] * sw_tot;
+      ptrs[bt[k]] = base + boff[b] + k * tile_bytes(bt[k]);
+    }
+    s = run_encode(e, ep, static_cast<const float*>(video), static_cast<int>(shp[3]), static_cast<int>(shp[4]),
+                   boxes.data(), K, reinterpret_cast<float*>(base + boff[b]), strm);
+    if (s) return s;
   }
   vae_blend_desc_t bd{};
   bd.B = B; bd.C = M; bd.T = lat[0]; bd.H = lat[1]; bd.W = lat[2];

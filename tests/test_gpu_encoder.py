@@ -114,6 +114,32 @@ def test_tiled_encode_matches_oracle(vd, dt):
         assert metrics.rel_l2(g, ref) <= 1e-2 and metrics.psnr(g, ref) >= 50.0
 
 
+@pytest.mark.parametrize("dt", ["bf16", "fp32"])
+def test_tiled_encode_equals_blend_of_separate_tile_encodes(vd, dt):
+    # the tiled driver batches the 9 equal-shape tiles into one encode of 18 items; each tile's moments
+    # must be those of encoding its pixels on their own, and the blend the library blend of those
+    cfg = dataclasses.replace(synth.MINI_ENC_STRIDE, video_shape=(2, 3, 5, 40, 56))   # latent 10 x 14
+    tile, ovl = (4, 6), (1, 2)
+    p = synth.draw_params(cfg, 0, rand_affine=True)
+    dtc = vd.VAE_BF16 if dt == "bf16" else vd.VAE_FP32
+    enc = vd.Encoder(cfg, p, dtc)
+    vt = torch.from_numpy(synth.draw_video(cfg, 0)).cuda()
+    out = enc.encode_tiled(vt, tile, ovl)
+    lat = cfg.latent_shape()
+    s = cfg.video_shape[3] // lat[3]
+    meta = vd.tile_plan(lat[2:], (lat[2],) + tile, (0,) + ovl, 1, 1, False)
+    assert len(meta) == 9
+    parts = []
+    for m in meta:
+        _, _, h0, nh, w0, nw = m["lat"]
+        parts.append(enc.encode(vt[:, :, :, h0 * s:(h0 + nh) * s, w0 * s:(w0 + nw) * s].contiguous()))
+    out2 = vd.tile_blend(parts, meta, torch.full_like(out, float("nan")))
+    torch.cuda.synchronize()
+    assert enc.last_error()[0] == vd.VAE_OK
+    enc.close()
+    assert torch.equal(out2, out)
+
+
 def test_encoder_refusals(vd):
     cfg = synth.MINI_ENC
     enc = vd.Encoder(cfg, synth.draw_params(cfg, 0), vd.VAE_BF16)

@@ -230,6 +230,8 @@ def main():
                     help="run only the decode or only the op workloads (profiling runs)")
     ap.add_argument("--latent-frames", type=int, default=0,
                     help="decode only the first N latent frames (0: all; small values for profiler captures)")
+    ap.add_argument("--blend-small", action="store_true",
+                    help="op-level blend of the tiled LTX plan on batch 1 and 9 latent frames (profiler captures)")
     ap.add_argument("--ops-frames", type=int, default=0,
                     help="frames of the pixel-head op workloads (0: 81; smaller values for profiler captures)")
     args = ap.parse_args()
@@ -613,17 +615,20 @@ def run_ops(args, torch, vd, peaks, flush):
     del tiles, outb, blend
     # (d) the blend of the batch-2 overlap-tiled LTX decode: 45 tiles overlapping in time and space
     cfg, tl = synth.LTX_TILED, synth.LTX_TILING
+    if args.blend_small:  # a smaller case of the same plan for profiler captures: batch 1, 9 latent frames
+        cfg = dataclasses.replace(cfg, latent_shape=(1, cfg.latent_shape[1], 9) + tuple(cfg.latent_shape[3:]))
     st, ss, _ = cfg.scale()
     meta = vd.tile_plan(cfg.latent_shape[2:], tl.tile, tl.overlap, st, ss)
     gen = torch.Generator(device="cuda")
     gen.manual_seed(201)
-    tiles = [torch.randn((2, 3, m["pix"][1], m["pix"][3], m["pix"][5]), generator=gen, device="cuda").to(torch.bfloat16)
-             for m in meta]
+    nbat = cfg.latent_shape[0]
+    tiles = [torch.randn((nbat, 3, m["pix"][1], m["pix"][3], m["pix"][5]), generator=gen, device="cuda").to(
+        torch.bfloat16) for m in meta]
     outb = torch.empty(cfg.output_shape(), dtype=torch.bfloat16, device="cuda")
     blend = vd.prepare_tile_blend(tiles, meta, outb)
     ms = _time(torch, blend, args.steps, flush)
     nbytes = sum(t.numel() for t in tiles) * 2 + outb.numel() * 2
-    res["tile_blend_ltx_tiled"] = {"workload": f"{len(meta)} tiles of up to [2,3,57,512,512] bf16 (overlap 8 frames, "
+    res["tile_blend_ltx_tiled"] = {"workload": f"{len(meta)} tiles of up to [{nbat},3,57,512,512] bf16 (overlap 8 frames, "
                                                f"128 px) -> {list(cfg.output_shape())}", "ms": ms, "bytes": nbytes,
                                    "gbs": nbytes / ms / 1e6, "frac_of_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"],
                                    "bound": "hbm"}

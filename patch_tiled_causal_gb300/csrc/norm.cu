@@ -900,6 +900,7 @@ template <int N> VAE_DEV void cp_async_wait() { asm volatile("cp.async.wait_grou
 // its vector before summing; rows covered by more than two (t, y) pairs, and ragged or unaligned
 // vectors, take the per-pixel loop.
 constexpr int kG2Cols = 16;
+constexpr int kBlendRing = 3;  // staged source vectors per lane: 2 in flight while one is summed (static smem <= 48 KB)
 // Per 8-pixel vector of an output row, built once per block: one packed word (first column interval,
 // count, fast-path flag, offsets into both intervals' rows) and the first interval's normalised column
 // weights (the second's are one minus them).
@@ -946,15 +947,15 @@ VAE_DEV void build_vec_table(const BlendGridParams& p, int4* vinfo, float4 (*vw0
   }
 }
 
-constexpr int kG2Vecs = 1;  // vectors per lane per step (more were slower: fewer warps fit)
 template <typename TT, typename TO>
 __global__ void __launch_bounds__(256, 4) blend_grid2_kernel(const __grid_constant__ BlendGridParams p) {
   __shared__ int4 vinfo[kGridMaxVec];
   __shared__ float4 vw0[kGridMaxVec][2];
   __shared__ const TT* rowp[8][4][kG2Cols];
   // bf16 tiles, rows covered by one (t, y) pair: each lane's source vectors (one per column
-  // interval) of its next vector are copied here asynchronously while it sums the current one
-  __shared__ uint4 stage[sizeof(TT) == 2 ? 8 : 1][2][2][32];
+  // interval) of its next kBlendRing - 1 vectors are copied here asynchronously while it sums the
+  // current one
+  __shared__ uint4 stage[sizeof(TT) == 2 ? 8 : 1][kBlendRing][2][32];
   const int nv = (p.W + 7) / 8;
   build_vec_table(p, vinfo, vw0);
   __syncthreads();
@@ -1005,13 +1006,20 @@ __global__ void __launch_bounds__(256, 4) blend_grid2_kernel(const __grid_consta
             if (j < ncv) cp_async16(&stage[warp][buf][j][lane], rowp[warp][0][cv + j] + (j ? inf.z : inf.y));
           return true;
         };
-        bool fast_cur = issue(lane, 0);
-        cp_async_commit();
+        uint32_t fm = 0;  // bit k: ring slot k holds a fast-path vector
+#pragma unroll
+        for (int k = 0; k < kBlendRing - 1; ++k) {
+          if (issue(lane + 32 * k, k)) fm |= 1u << k;
+          cp_async_commit();
+        }
         int buf = 0;
         for (int v = lane; v < nv; v += 32) {
-          const bool fast_next = issue(v + 32, buf ^ 1);
+          const int refill = buf == 0 ? kBlendRing - 1 : buf - 1;  // the slot consumed last step
+          fm &= ~(1u << refill);
+          if (issue(v + 32 * (kBlendRing - 1), refill)) fm |= 1u << refill;
           cp_async_commit();
-          cp_async_wait<1>();  // this lane's copies for v have landed
+          cp_async_wait<kBlendRing - 1>();  // this lane's copies for v have landed
+          const bool fast_cur = (fm >> buf) & 1u;
           const int x0 = v * 8;
           float acc[8];
           if (fast_cur) {
@@ -1055,90 +1063,75 @@ __global__ void __launch_bounds__(256, 4) blend_grid2_kernel(const __grid_consta
           } else {
             for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(acc[e]);
           }
-          fast_cur = fast_next;
-          buf ^= 1;
+          buf = buf + 1 == kBlendRing ? 0 : buf + 1;
         }
         cp_async_wait<0>();
         __syncwarp();
         continue;
       }
     }
-    for (int vb = lane; vb < nv; vb += 32 * kG2Vecs) {
-      int4 inf[kG2Vecs];
-      Raw8<TT> raw[kG2Vecs][2][2];  // [vector][pair][interval]
-      bool fast[kG2Vecs];
+    for (int v = lane; v < nv; v += 32) {
+      const int4 inf = vinfo[v];
+      const bool fast = (inf.x >> 12) & 1;
+      const int x0 = v * 8;
+      float acc[8];
+      if (fast) {
+        // up to 4 (t, y) pairs (frames and rows both in overlaps), taken two at a time: the loads of
+        // two pairs are in flight together, the pair-weighted sums s[j] kept per column interval j
+        const int cv = inf.x & 255, ncv = (inf.x >> 8) & 15;
+        float s2[2][8];
 #pragma unroll
-      for (int u = 0; u < kG2Vecs; ++u) {
-        const int v = vb + 32 * u;
-        fast[u] = false;
-        if (v < nv) {
-          inf[u] = vinfo[v];
-          fast[u] = ((inf[u].x >> 12) & 1) && npair <= 2;
-          if (fast[u]) {
-            const int cv = inf[u].x & 255, ncv = (inf[u].x >> 8) & 15;
+        for (int j = 0; j < 2; ++j)
 #pragma unroll
-            for (int q = 0; q < 2; ++q)
+          for (int e = 0; e < 8; ++e) s2[j][e] = 0.f;
 #pragma unroll
-              for (int j = 0; j < 2; ++j)
-                if (q < npair && j < ncv) raw[u][q][j].load(rowp[warp][q][cv + j] + (j ? inf[u].z : inf[u].y));
+        for (int h = 0; h < 2; ++h) {
+          if (2 * h >= npair) break;
+          Raw8<TT> raw[2][2];  // [pair][interval]
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              if (2 * h + q < npair && j < ncv) raw[q][j].load(rowp[warp][2 * h + q][cv + j] + (j ? inf.z : inf.y));
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              if (2 * h + q < npair && j < ncv) {
+                float val[8];
+                raw[q][j].get(val);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s2[j][e] = fmaf(wq[2 * h + q], val[e], s2[j][e]);
+              }
+        }
+        const float4 wl = vw0[v][0], wh = vw0[v][1];
+        const float w0[8] = {wl.x, wl.y, wl.z, wl.w, wh.x, wh.y, wh.z, wh.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(1.f - w0[e], s2[1][e], w0[e] * s2[0][e]);
+      } else {
+        // ragged or unaligned vector: per pixel (unrolled, so that acc stays in registers)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          acc[e] = 0.f;
+          const int x = x0 + e;
+          if (x >= p.W) continue;
+          int ic0, ic1;
+          float wc0, wc1;
+          const int ncx = axis_cover2(p, 2, x, ic0, ic1, wc0, wc1);
+          for (int q = 0; q < npair; ++q) {
+            const int qa = nb == 2 ? q >> 1 : q, qb = nb == 2 ? q & 1 : 0;
+            const float wqq = (qa ? wa1 : wa0) * (qb ? wb1 : wb0);  // (no dynamically indexed array)
+            for (int j = 0; j < ncx; ++j) {
+              const int ci = j ? ic1 : ic0;
+              acc[e] = fmaf(wqq * (j ? wc1 : wc0), to_f<TT>(rowp[warp][q][ci][x - p.s0[2][ci]]), acc[e]);
+            }
           }
         }
       }
-#pragma unroll
-      for (int u = 0; u < kG2Vecs; ++u) {
-        const int v = vb + 32 * u;
-        if (v >= nv) break;
-        const int x0 = v * 8;
-        float acc[8];
-        if (fast[u]) {
-          const int ncv = (inf[u].x >> 8) & 15;
-          const float4 wl = vw0[v][0], wh = vw0[v][1];
-          const float w0[8] = {wl.x, wl.y, wl.z, wl.w, wh.x, wh.y, wh.z, wh.w};
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            float s[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) s[e] = 0.f;
-#pragma unroll
-            for (int q = 0; q < 2; ++q)
-              if (q < npair && j < ncv) {
-                float val[8];
-                raw[u][q][j].get(val);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) s[e] = fmaf(wq[q], val[e], s[e]);
-              }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float wc = j ? 1.f - w0[e] : w0[e];
-              acc[e] = j ? fmaf(wc, s[e], acc[e]) : wc * s[e];
-            }
-          }
-        } else {
-          // ragged or unaligned vector, or a row covered by more than two pairs: per pixel (unrolled,
-          // so that acc stays in registers)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            acc[e] = 0.f;
-            const int x = x0 + e;
-            if (x >= p.W) continue;
-            int ic0, ic1;
-            float wc0, wc1;
-            const int ncx = axis_cover2(p, 2, x, ic0, ic1, wc0, wc1);
-            for (int q = 0; q < npair; ++q) {
-              const int qa = nb == 2 ? q >> 1 : q, qb = nb == 2 ? q & 1 : 0;
-              const float wqq = (qa ? wa1 : wa0) * (qb ? wb1 : wb0);  // (no dynamically indexed array)
-              for (int j = 0; j < ncx; ++j) {
-                const int ci = j ? ic1 : ic0;
-                acc[e] = fmaf(wqq * (j ? wc1 : wc0), to_f<TT>(rowp[warp][q][ci][x - p.s0[2][ci]]), acc[e]);
-              }
-            }
-          }
-        }
-        if (x0 + 8 <= p.W && (p.W & 7) == 0) {
-          store8(orow + x0, acc);
-        } else {
-          for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(acc[e]);
-        }
+      if (x0 + 8 <= p.W && (p.W & 7) == 0) {
+        store8(orow + x0, acc);
+      } else {
+        for (int e = 0; e < 8 && x0 + e < p.W; ++e) orow[x0 + e] = from_f<TO>(acc[e]);
       }
     }
     __syncwarp();

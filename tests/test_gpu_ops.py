@@ -306,6 +306,28 @@ def test_tile_blend(vd, dt, order, W):
     assert rel_err(out.float().cpu().numpy(), ref) < (BF16_TOL if dt == "bf16" else F32_TOL)
 
 
+@pytest.mark.parametrize("dt", ["bf16", "fp32"])
+def test_tile_blend_aligned_grid(vd, dt):
+    # tile edges on 8-pixel boundaries: every vector takes the vector path, including rows whose frames
+    # and rows both lie in overlaps (4 (t, y) pairs, 2 column intervals: 8 source vectors)
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    plan_ = tiles.tile_plan((3, 56, 112), (2, 32, 32), (1, 8, 8), 4, 1)
+    B, Cc = 2, 3
+    out_shape = (B, Cc, 4 * 2 + 1, 56, 112)
+    data = []
+    for i, t in enumerate(plan_):
+        a = synth.draw_normal((B, Cc, t.pix[1], t.pix[3], t.pix[5]), 90 + i)
+        data.append(bf16_round(a) if dt == "bf16" else a)
+    ref = tiles.blend(plan_, data, out_shape)
+    out = torch.full(out_shape, float("nan"), dtype=tdt, device="cuda")
+    meta = [{"lat": t.lat, "pix": t.pix, "ovl": t.ovl} for t in plan_]
+    vd.tile_blend([to_dev(a, tdt) for a in data], meta, out)
+    torch.cuda.synchronize()
+    g = out.float().cpu().numpy()
+    assert not np.isnan(g).any()
+    assert rel_err(g, ref) < (BF16_TOL if dt == "bf16" else F32_TOL)
+
+
 # ----------------------------------------------------------------------------- watchdog
 
 def test_watchdog_times_out_and_context_survives(vd):

@@ -13,7 +13,8 @@ One JSON line on rank 0 with the contract's keys plus:
                 tile blend
   extra         the LTX-shaped 720p x 81f decode (1x4 and 2x4 patches), the batch-2 overlap-tiled LTX
                 decode (45 tiles -> [2,3,129,1088,1920]), the Wan-shaped decode with e4m3 conv operands and
-                the LTX-shaped encode of 720p x 81f: Mframe-px/s, conv fraction, per-kernel table
+                the LTX-shaped encode of 720p x 81f, the LTX-shaped decode in fp32 (3 x TF32 convs):
+                Mframe-px/s, conv fraction, per-kernel table
   cpu_baseline  the CPU oracle on a bounded sample of the same decode (first 2 latent frames of one
                 full-width latent row), host cores
 N > 1 (torchrun): each rank decodes its own latent (independent videos, weak scaling), no
@@ -360,6 +361,7 @@ def main():
         extra = run_ltx(args, torch, vaedec, peaks, flush, stream)
         extra["wan_fp8_1x4"] = run_wan_fp8(args, torch, vaedec, peaks, flush, stream)
         extra["ltx_encode_1x4"] = run_ltx_encode(args, torch, vaedec, peaks, flush, stream)
+        extra["ltx_fp32_1x4"] = run_ltx_fp32(args, torch, vaedec, peaks, flush, stream)
 
     cpu = None
     if not args.no_cpu and rank == 0 and world == 1:
@@ -456,6 +458,35 @@ def run_wan_fp8(args, torch, vd, peaks, flush, stream):
     return {"workload": f"wan-shaped decoder, latent {list(cfg.latent_shape)}, 1x4 patches, e4m3 operands for the "
                         "residual-block and up-sampler convs (conv_in, conv_out, attention bf16), pixels bf16",
             "value": fpx / ms / 1e3, "unit": "Mframe-px/s", "ms_per_step": ms, "dtype": "fp8 (e4m3) conv operands",
+            "kernels": kernel_table(prof, args.steps, peaks)}
+
+
+def run_ltx_fp32(args, torch, vd, peaks, flush, stream):
+    """The LTX-shaped 720p x 81f decode (1x4 patches) in fp32 storage (VAE_FP32): convs as three TF32
+    products per fp32 product on the tensor cores."""
+    cfg = synth.LTX
+    params = synth.draw_params(cfg, 0)
+    dec = vd.Decoder(cfg, params, vd.VAE_FP32)
+    del params
+    z = torch.from_numpy(synth.draw_latent(cfg, 0)).cuda()
+    out = torch.empty(dec.output_shape(z.shape), dtype=torch.float32, device="cuda")
+    ms, prof = timed_decodes(torch, dec, lambda: dec.decode(z, out, 1, 4), args.steps, args.warmup, flush, stream)
+    code, msg = vd.last_error(dec.h)
+    if code:
+        raise RuntimeError(f"fp32 decode failed: {msg}")
+    dec.close()
+    fpx = out.shape[0] * out.shape[2] * out.shape[3] * out.shape[4]
+    conv = conv_totals(prof)
+    tf = conv["flops"] / (conv["ms"] / 1e3) / 1e12
+    # three TF32 products per fp32 product: the effective peak is a third of the tf32 dense peak, taken as
+    # the measured sustained bf16 figure x the nominal tf32 / bf16 ratio (1.1 / 2.25)
+    eff_peak = peaks["bf16_tflops_sustained"] * (1.1 / 2.25) / 3.0
+    del z, out
+    torch.cuda.empty_cache()
+    return {"workload": f"ltx-shaped decoder, latent {list(cfg.latent_shape)}, 1x4 patches, fp32 storage, convs as "
+                        "3 x TF32 products on the tensor cores, pixels fp32",
+            "value": fpx / ms / 1e3, "unit": "Mframe-px/s", "ms_per_step": ms, "dtype": "fp32 (3 x tf32 convs)",
+            "conv_tflops": tf, "conv_frac_of_3xtf32_peak": tf / eff_peak,
             "kernels": kernel_table(prof, args.steps, peaks)}
 
 

@@ -60,8 +60,8 @@ typedef enum {
  * (round to nearest even; a value beyond +-448 is saturated and flags VAE_ERR_RANGE).  As a decoder
  * dtype: the residual blocks' and up-samplers' convs whose input channels are a multiple of 128 take
  * e4m3 operands written by the norm (norm + SiLU -> quantisation in one pass) or by the last residual
- * block's conv epilogue; conv_in, conv_out, attention, the residual stream and conv1's output stay as in
- * bf16 mode; pixels are bf16.  Accuracy bar against the fp32 oracle: relative L2 <= 0.15 and PSNR >= 35 dB
+ * block's conv epilogue; conv_in, conv_out and attention stay as in bf16 mode, the residual stream and
+ * conv1's output are stored in bf16; pixels are bf16.  Accuracy bar against the fp32 oracle: relative L2 <= 0.15 and PSNR >= 35 dB
  * (each e4m3 rounding has unit roundoff 2^-4; the same rounding points emulated in the oracle give
  * relative L2 0.05-0.07 on small decoders and 0.094 on the first frame of the Wan-shaped decode). */
 typedef enum { VAE_BF16 = 0, VAE_FP32 = 1, VAE_FP8 = 2 } vae_dtype_t;
@@ -101,7 +101,11 @@ typedef struct {
  * population variance, eps inside the square root.  The attention is one head over each frame's
  * H*W tokens with 1x1 q/k/v/o projections, scale 1/sqrt(C), on GN(x) without SiLU, plus residual.
  * dtype: VAE_BF16 stores activations in bf16 (fp32 accumulation, statistics and blend),
- * VAE_FP32 stores everything in fp32.
+ * VAE_FP32 stores everything in fp32; its convs with input channels a multiple of 32 run on the
+ * tcgen05 tensor cores as three TF32 products per fp32 product (kind::tf32: the high part of each
+ * operand is the value with its 13 low mantissa bits cleared, the remainder is exact in fp32, and
+ * a_hi b_hi + a_hi b_lo + a_lo b_hi is summed in fp32), the others and the attention GEMMs on the CUDA
+ * cores.
  * norm_type: VAE_NORM_GROUP (gn_groups, gn_eps as above), or VAE_NORM_CHANNEL_RMS: every norm above
  * becomes x * rsqrt(mean over channels of x^2 + gn_eps) * gamma + beta per pixel (gn_groups is then
  * ignored; stage channels must be multiples of 8 and at most 1024 with C/8 a power of two or a

@@ -114,6 +114,7 @@ struct ConvL {
   bool fp8 = false;        // e4m3 operands and weights (fp8 decoders)
   bool natural = false;    // weight rows in PyTorch channel order (convs that store NCTHW pixels)
   bool tap = false;        // narrow bf16 conv: weights packed tap-stacked (all 9 spatial taps in one MMA)
+  bool tf32 = false;       // fp32 decoder on the tensor cores: 3 TF32 products per fp32 product
   float* wscale = nullptr; // fp8: per-output-channel weight scales (inside the packed weight buffer)
   void* w = nullptr;       // packed weights
   float* bias = nullptr;   // fp32 [C_out]
@@ -233,9 +234,12 @@ vae_status_t make_conv(vae_decoder* d, ConvL& c, const float* w, const float* b,
   c.st = st; c.sh = sh; c.sw = sw;
   const int S = st * sh * sw;
   if (C_out % S) return set_err(&d->err, VAE_ERR_INVALID_ARG, 0, 0, "conv out channels %d not divisible by %d", C_out, S);
-  // tensor cores take 64-channel K blocks; the latent is zero-padded up to them when it is converted
-  c.tc = !d->f32 && (C_in % 64 == 0 || pad_input);
-  c.C_in_pad = c.tc ? round_up(C_in, 64) : C_in;
+  // tensor cores take 64-channel K blocks (32 fp32 channels for the 3 x TF32 products of fp32
+  // decoders); the latent is zero-padded up to them when it is converted
+  const int kb = d->f32 ? 32 : 64;
+  c.tc = C_in % kb == 0 || pad_input;
+  c.tf32 = d->f32 && c.tc;
+  c.C_in_pad = c.tc ? round_up(C_in, kb) : C_in;
   c.fp8 = d->f8 && allow_fp8 && c.tc && C_in % 128 == 0;
   c.natural = natural;
   if (c.fp8) {
@@ -245,6 +249,11 @@ vae_status_t make_conv(vae_decoder* d, ConvL& c, const float* w, const float* b,
     if (s) return s;
     c.wscale = reinterpret_cast<float*>(static_cast<char*>(c.w) + off);
     CK(launch_pack_weights_fp8(w, C_out, C_in, c.C_in_pad, c.N_pad, S, c.w, nullptr, natural));
+  } else if (c.tf32) {
+    c.N_pad = round_up(C_out, 16);
+    vae_status_t s = dalloc(d, &c.w, 2ull * c.N_pad * 27 * c.C_in_pad * 4);
+    if (s) return s;
+    CK(launch_pack_weights_tf32(w, C_out, C_in, c.C_in_pad, c.N_pad, S, c.w, nullptr, natural));
   } else if (c.tc) {
     c.N_pad = round_up(C_out, 16);
     c.tap = conv_tap_stacked(C_out, 0);
@@ -447,6 +456,7 @@ struct Plan {
   bool first;
   // buffer sizes in bytes
   size_t x_bytes, hin_bytes, c1_bytes, gn_bytes, lat_bytes;
+  size_t split_bytes = 0;  // fp32 decoders: each of the high-part and remainder copies of a conv input
   size_t attn_tok, attn_tokp;  // tokens per frame and padded
   size_t q_bytes, s_bytes, p_bytes, vt_bytes;
 };
@@ -492,6 +502,7 @@ vae_status_t make_plan(vae_decoder* d, int B, int Tlat, int h, int w, int nph, i
   const int Clat = d->conv_in.C_in_pad;
   p.lat_bytes = static_cast<size_t>(B) * (Tlat + 2) * h * w * Clat * ab;
   p.hin_bytes = std::max(p.hin_bytes, p.lat_bytes);
+  p.split_bytes = d->f32 ? p.hin_bytes : 0;  // every conv input lives in hin
   p.attn_tok = static_cast<size_t>(h) * w;
   p.attn_tokp = round_up(static_cast<int>(p.attn_tok), 64);
   if (d->has_attn) {
@@ -509,12 +520,13 @@ vae_status_t make_plan(vae_decoder* d, int B, int Tlat, int h, int w, int nph, i
 size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Bufs {
-  char *x, *hin, *c1, *gn, *q, *k, *v, *vt, *s, *p, *o;
+  char *x, *hin, *c1, *gn, *q, *k, *v, *vt, *s, *p, *o, *hi, *lo;
 };
 
 size_t ws_total(const Plan& p) {
   return align_up(p.x_bytes) + align_up(p.hin_bytes) + align_up(p.c1_bytes) + align_up(p.gn_bytes) +
-         4 * align_up(p.q_bytes) + align_up(p.vt_bytes) + align_up(p.s_bytes) + align_up(p.p_bytes) + 256;
+         4 * align_up(p.q_bytes) + align_up(p.vt_bytes) + align_up(p.s_bytes) + align_up(p.p_bytes) +
+         2 * align_up(p.split_bytes) + 256;
 }
 
 Bufs carve(void* base, const Plan& p) {
@@ -530,7 +542,9 @@ Bufs carve(void* base, const Plan& p) {
   b.o = c; c += align_up(p.q_bytes);
   b.vt = c; c += align_up(p.vt_bytes);
   b.s = c; c += align_up(p.s_bytes);
-  b.p = c;
+  b.p = c; c += align_up(p.p_bytes);
+  b.hi = c; c += align_up(p.split_bytes);
+  b.lo = c;
   return b;
 }
 
@@ -642,6 +656,20 @@ vae_status_t run_conv(Ctx& x, ConvL& c, const Level& L, char* in, const ConvOut&
     a.y = y; a.out_f32 = y_f32; a.out_ncthw = out_ncthw; a.y_T_alloc = y_T_alloc;
     a.d2s_t = c.st; a.d2s_h = c.sh; a.d2s_w = c.sw; a.drop_first = drop_first;
     a.fp8 = c.fp8; a.wscale = c.wscale; a.natural = c.natural; a.tap_stacked = c.tap;
+    if (c.tf32) {
+      // 3 x TF32: split the whole input (cache frames included) into high parts and remainders
+      const int64_t n = static_cast<int64_t>(B) * Ta * (frame_bytes / 4);
+      if (static_cast<size_t>(n) * 4 > x.p->split_bytes)
+        return set_err(&d->err, VAE_ERR_UNSUPPORTED, 0, 0, "conv input larger than the split buffers");
+      {
+        Prof pr(d, x.s, K_CAST, 0, 12.0 * n);
+        CK(launch_split_tf32(reinterpret_cast<const float*>(in), reinterpret_cast<float*>(x.b.hi),
+                             reinterpret_cast<float*>(x.b.lo), n, x.s));
+      }
+      a.tf32 = 1;
+      a.x = x.b.hi + (xin - in);
+      a.x_lo = x.b.lo + (xin - in);
+    }
     const int Cd = c.C_out / (c.st * c.sh * c.sw);
     const int G = d->cfg.gn_groups;  // (ignored, possibly 0, by channel-RMS decoders)
     const int cpg = (G > 0 && Cd % G == 0) ? Cd / G : 0;
@@ -1326,6 +1354,7 @@ vae_status_t make_enc_plan(vae_encoder* e, int B, int T, int H, int W, int nph, 
       return set_err(&d->err, VAE_ERR_UNSUPPORTED, 0, 0, "stage %d: group exceeds the exact-sum range", i);
   }
   p.lat_bytes = 0;
+  p.split_bytes = d->f32 ? p.hin_bytes : 0;  // every conv input lives in hin
   p.attn_tok = p.attn_tokp = 0;
   p.q_bytes = p.vt_bytes = p.s_bytes = p.p_bytes = 0;
   return VAE_OK;

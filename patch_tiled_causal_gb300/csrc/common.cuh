@@ -247,6 +247,15 @@ VAE_DEV void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint
 }
 
 // Same with e4m3 A and B (kind::f8f6f4: 32 K elements = 32 bytes per instruction, fp32 accumulation).
+VAE_DEV void tc_mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 VAE_DEV void tc_mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -287,6 +296,16 @@ VAE_DEV void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
 // Completion signal of the pair's MMAs: one arrival on the mbarrier at this offset in each CTA named
 // by cta_mask (the pair's two CTAs).  It moves no data: every operand load in this library is a
 // plain TMA load into the issuing CTA's own shared memory.
+VAE_DEV void tc_mma_tf32_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 VAE_DEV void tc_mma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                               uint32_t accumulate) {
   asm volatile(
@@ -345,6 +364,15 @@ VAE_DEV uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
 // Instruction descriptor, kind::f8f6f4: e4m3 A and B (format code 0, K-major), fp32 D, M x N.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t m, uint32_t n) {
   return (1u << 4)                 // D format: f32
+         | ((n >> 3) << 17)        // N / 8
+         | ((m >> 4) << 24);       // M / 16
+}
+
+// Instruction descriptor, kind::tf32: tf32 A and B (format code 2, K-major), fp32 D, M x N.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(uint32_t m, uint32_t n) {
+  return (1u << 4)                 // D format: f32
+         | (2u << 7)               // A format: tf32
+         | (2u << 10)              // B format: tf32
          | ((n >> 3) << 17)        // N / 8
          | ((m >> 4) << 24);       // M / 16
 }

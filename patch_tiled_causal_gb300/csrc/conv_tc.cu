@@ -39,6 +39,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <mutex>
+#include <cstring>
 
 #include "common.cuh"
 #include "internal.h"
@@ -83,6 +84,8 @@ struct TcParams {
   int y2_T_alloc, y2_fp8;
   int fp8;           // e4m3 operands (kind::f8f6f4); kc = channels per 128-byte k block (64 bf16, 128 e4m3)
   int kc;
+  int tf32;          // fp32 operands as 3 TF32 products (kc = 32); the weights' remainder rows start at w_lo_row
+  int w_lo_row;
   const float* wscale;  // fp8: per-output-channel weight scale (packed row order)
   int natural;       // weight rows (and so accumulator columns) in PyTorch channel order c * S + sub
   int n_tiles;
@@ -437,17 +440,25 @@ VAE_DEV void epilogue_chunk(const TcParams& p, const TileCoord& tc, int m, int n
 // tile; the leader's full barrier counts both CTAs' bytes, the leader alone issues the MMAs, and its
 // commits free the stage and hand the accumulator to the epilogues in both CTAs.  Each SM then takes
 // in half as many weight bytes per MMA as a CTA that holds the whole weight tile.
-// kF8: e4m3 operands (kind::f8f6f4); a template parameter so the bf16 kernel's single-thread MMA issue
-// loop carries no test of it.
-template <bool kPair, bool kF8>
+// kOp, the operand kind (a template parameter so that each kernel's single-thread MMA issue loop carries
+// no test of it): 0 bf16 (kind::f16), 1 e4m3 (kind::f8f6f4), 2 fp32 as three TF32 products
+// (kind::tf32: a_hi b_hi + a_hi b_lo + a_lo b_hi, the high parts and remainders loaded as separate
+// tiles, tmA2 the remainders of x; 32 fp32 channels per 128-byte k block).
+template <bool kPair, int kOp>
 __global__ void __launch_bounds__(kThreads, 1)
     conv_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ TcParams p) {
+                   const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ TcParams p) {
+  constexpr bool kF8 = kOp == 1;
+  constexpr bool kT32 = kOp == 2;
+  constexpr uint32_t kParts = kT32 ? 2u : 1u;  // high parts and remainders
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // one stage = ks k blocks: [A of k block 0 .. ks-1][B of k block 0 .. ks-1]
-  const uint32_t b_bytes = static_cast<uint32_t>(kPair ? p.BN / 2 : p.BN) * kBlockK * 2;  // per k block
-  const uint32_t a_bytes = kABytes * static_cast<uint32_t>(p.msub);                        // per k block
+  // one stage = ks k blocks: [A of k block 0 .. ks-1][B of k block 0 .. ks-1]; with kT32 each A and B
+  // block holds the high-part tile, then the remainder tile
+  const uint32_t b_half = static_cast<uint32_t>(kPair ? p.BN / 2 : p.BN) * kBlockK * 2;
+  const uint32_t a_half = kABytes * static_cast<uint32_t>(p.msub);
+  const uint32_t b_bytes = b_half * kParts;  // per k block
+  const uint32_t a_bytes = a_half * kParts;  // per k block
   const int ks = p.ks;
   const bool halo = !kPair && p.halo;
   const uint32_t stage_bytes = halo ? p.halo_stage : static_cast<uint32_t>(ks) * (a_bytes + b_bytes);
@@ -477,6 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if constexpr (kT32) tma_prefetch_desc(&tmA2);
   }
   if (warp == 1) {
     if constexpr (kPair) tmem_alloc_pair(tmem_slot, static_cast<uint32_t>(p.tmem_cols));
@@ -568,9 +580,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               if constexpr (kPair) {
                 tma_load_5d_pair(aj, &tmA, fb, cc * p.kc, tc.w0 + kw - 1, tc.h0 + kh - 1, ti, tc.b);
                 tma_load_2d_pair(bj, &tmB, fb, kcol, tc.n0 + rank * (p.BN / 2));
+                if constexpr (kT32) {
+                  tma_load_5d_pair(aj + a_half, &tmA2, fb, cc * p.kc, tc.w0 + kw - 1, tc.h0 + kh - 1, ti, tc.b);
+                  tma_load_2d_pair(bj + b_half, &tmB, fb, kcol, p.w_lo_row + tc.n0 + rank * (p.BN / 2));
+                }
               } else {
                 tma_load_5d(aj, &tmA, &full_bar[s], cc * p.kc, tc.w0 + kw - 1, tc.h0 + kh - 1, ti, tc.b);
                 tma_load_2d(bj, &tmB, &full_bar[s], kcol, tc.n0);
+                if constexpr (kT32) {
+                  tma_load_5d(aj + a_half, &tmA2, &full_bar[s], cc * p.kc, tc.w0 + kw - 1, tc.h0 + kh - 1, ti, tc.b);
+                  tma_load_2d(bj + b_half, &tmB, &full_bar[s], kcol, p.w_lo_row + tc.n0);
+                }
               }
               // next (tap, channel chunk): channel chunks innermost, then kw, kh, kt
               kcol += p.kc;
@@ -694,7 +714,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && (!kPair || rank == 0) && !halo) {
       const uint32_t mm = kPair ? 2 * kBlockM : kBlockM;
       constexpr bool fp8 = kF8;
-      const uint32_t idesc = fp8 ? idesc_e4m3_f32(mm, static_cast<uint32_t>(p.BN)) : idesc_bf16_f32(mm, static_cast<uint32_t>(p.BN));
+      const uint32_t idesc = fp8    ? idesc_e4m3_f32(mm, static_cast<uint32_t>(p.BN))
+                             : kT32 ? idesc_tf32_f32(mm, static_cast<uint32_t>(p.BN))
+                                    : idesc_bf16_f32(mm, static_cast<uint32_t>(p.BN));
       const int stages = p.stages, num_st = p.num_kb / ks, msub = p.msub;
       const uint32_t smem_base = smem_u32(smem);
       const uint32_t sub_cols = static_cast<uint32_t>(p.BN);
@@ -727,10 +749,23 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t first = (st == 0 && j == 0) ? 1u : 0u;
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                // advance 32 B along K inside the 128-byte swizzle atom: 16 bf16 or 32 e4m3 per MMA
+                // advance 32 B along K inside the 128-byte swizzle atom: 16 bf16, 32 e4m3 or 8 tf32 per MMA
                 const uint32_t accum = (first && k == 0) ? 0u : 1u;
                 const uint64_t ak = adesc + static_cast<uint64_t>(2 * k), bk = bdesc + static_cast<uint64_t>(2 * k);
-                if constexpr (kPair && fp8) tc_mma_e4m3_pair(d_sub, ak, bk, idesc, accum);
+                if constexpr (kT32) {
+                  // the remainder tiles sit a_half / b_half bytes after the high parts (16-byte units)
+                  const uint64_t akl = ak + static_cast<uint64_t>(a_half >> 4);
+                  const uint64_t bkl = bk + static_cast<uint64_t>(b_half >> 4);
+                  if constexpr (kPair) {
+                    tc_mma_tf32_pair(d_sub, ak, bk, idesc, accum);
+                    tc_mma_tf32_pair(d_sub, ak, bkl, idesc, 1u);
+                    tc_mma_tf32_pair(d_sub, akl, bk, idesc, 1u);
+                  } else {
+                    tc_mma_tf32(d_sub, ak, bk, idesc, accum);
+                    tc_mma_tf32(d_sub, ak, bkl, idesc, 1u);
+                    tc_mma_tf32(d_sub, akl, bk, idesc, 1u);
+                  }
+                } else if constexpr (kPair && fp8) tc_mma_e4m3_pair(d_sub, ak, bk, idesc, accum);
                 else if constexpr (kPair) tc_mma_bf16_pair(d_sub, ak, bk, idesc, accum);
                 else if constexpr (fp8) tc_mma_e4m3(d_sub, ak, bk, idesc, accum);
                 else tc_mma_bf16(d_sub, ak, bk, idesc, accum);
@@ -908,8 +943,9 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// esz: element bytes (1 = e4m3 bytes, 2 = bf16, 4 = fp32)
 bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-              const uint32_t* box, bool bytes = false) {
+              const uint32_t* box, int esz = 2) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t d[5], s[4];
@@ -920,7 +956,10 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, 
     es[i] = 1;
     if (i + 1 < rank) s[i] = strides_bytes[i];
   }
-  CUresult r = fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+  const CUtensorMapDataType dt = esz == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : esz == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = fn(m, dt, rank,
                   const_cast<void*>(base), d, s, bx, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -987,13 +1026,17 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   // clusters of 2 run one cta_group::2 MMA over two adjacent M tiles of one weight tile (a batched GEMM
   // has a different B per batch item, so only unbatched GEMMs pair up)
   p.fp8 = a.fp8 ? 1 : 0;
-  p.kc = p.fp8 ? 128 : 64;
+  p.tf32 = a.tf32 ? 1 : 0;
+  p.kc = p.fp8 ? 128 : p.tf32 ? 32 : 64;
   if (p.fp8 && (a.mode != 0 || !a.wscale || a.C_in_pad % 128 != 0)) return cudaErrorInvalidValue;
+  if (p.tf32 && (a.mode != 0 || p.fp8 || !a.x_lo || a.tap_stacked || a.C_in_pad % 32 != 0)) return cudaErrorInvalidValue;
+  p.w_lo_row = a.N_pad;
   p.wscale = p.fp8 ? a.wscale : nullptr;
   // (NCTHW pixel outputs wider than 16 channels only with vector stores (natural channel order): with
   // scalar stores the epilogue outlasts the shorter MMA phase; measured on one GB300: LTX 128->48 head
   // 3.66 ms per tap, 5.73 ms in halo mode with scalar stores)
-  p.halo = (a.mode == 0 && p.BN <= 64 && !p.fp8 && (!a.out_ncthw || a.natural || a.N_real <= 16) && halo_mode_enabled())
+  p.halo = (a.mode == 0 && p.BN <= 64 && !p.fp8 && !p.tf32 && (!a.out_ncthw || a.natural || a.N_real <= 16) &&
+            halo_mode_enabled())
                ? 1
                : 0;
   if (a.tap_stacked) {  // weights packed tap-stacked (the caller decides, as it packs them)
@@ -1009,7 +1052,8 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   p.tmem_cols = 32;
   while (p.tmem_cols < 2 * p.msub * (p.halo == 2 ? kTapRows : p.halo ? 3 * p.BN : p.BN)) p.tmem_cols <<= 1;
   if (p.tmem_cols > 512) return cudaErrorInvalidValue;
-  const uint32_t kb_bytes = kABytes * p.msub + static_cast<uint32_t>(mma_pair ? p.BN / 2 : p.BN) * kBlockK * 2;
+  const uint32_t kb_bytes = (kABytes * p.msub + static_cast<uint32_t>(mma_pair ? p.BN / 2 : p.BN) * kBlockK * 2) *
+                            (p.tf32 ? 2u : 1u);  // (3 x TF32: high parts and remainders)
   // MMA pairs take two k blocks per stage (half the barrier round trips per MMA) where two such stages
   // fit; measured on one GB300: +11% on a 512->512 conv (3 stages), +12% on 128->128 (2 stages)
   // (a conv's 27 taps x cchunks k blocks split evenly into pairs when cchunks is even)
@@ -1048,7 +1092,8 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   p.fault = fault_word();
   p.limit_ns = wait_limit_ns();
 
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmA2;
+  memset(&tmA2, 0, sizeof(tmA2));
   long long n_blocks;
   if (a.mode == 0) {
     p.B = a.B; p.T = a.T; p.H = a.H; p.W = a.W; p.T_in = a.T_in; p.cache_frames = a.cache_frames;
@@ -1085,7 +1130,7 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
     if (a.gn_partials && (p.C_d2s % 32 != 0 || a.out_ncthw || (p.gn_cpg < 32 ? 32 % p.gn_cpg : p.gn_cpg % 32) != 0))
       return cudaErrorInvalidValue;
     const uint64_t C = a.C_in_pad;
-    const uint64_t eb = p.fp8 ? 1 : 2;  // bytes per operand element
+    const uint64_t eb = p.fp8 ? 1 : p.tf32 ? 4 : 2;  // bytes per operand element
     const uint64_t xTa = a.x_T_alloc ? a.x_T_alloc : a.T_in;
     uint64_t dims[5] = {C, (uint64_t)a.W, (uint64_t)a.H, (uint64_t)a.T_in, (uint64_t)a.B};
     uint64_t strides[4] = {C * eb, C * eb * a.W, C * eb * a.W * a.H, C * eb * a.W * a.H * xTa};
@@ -1094,7 +1139,8 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
       box[1] = static_cast<uint32_t>(p.cols_t + 2);
       box[2] = static_cast<uint32_t>(p.rows_t + 2);
     }
-    if (!make_map(&tmA, a.x, 5, dims, strides, box, p.fp8)) return cudaErrorInvalidValue;
+    if (!make_map(&tmA, a.x, 5, dims, strides, box, static_cast<int>(eb))) return cudaErrorInvalidValue;
+    if (p.tf32 && !make_map(&tmA2, a.x_lo, 5, dims, strides, box, 4)) return cudaErrorInvalidValue;
     const uint64_t K = 27ull * C;
     uint64_t wd[2] = {K, (uint64_t)a.N_pad};
     uint64_t ws[1] = {K * eb};
@@ -1105,7 +1151,8 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
       ws[0] = C * eb;
       wb[1] = static_cast<uint32_t>(kTapRows);
     }
-    if (!make_map(&tmB, a.w, 2, wd, ws, wb, p.fp8)) return cudaErrorInvalidValue;
+    if (p.tf32) wd[1] = 2ull * a.N_pad;  // high parts, then remainders
+    if (!make_map(&tmB, a.w, 2, wd, ws, wb, static_cast<int>(eb))) return cudaErrorInvalidValue;
     n_blocks = static_cast<long long>(a.B) * a.T * p.n_trows * p.n_tcols * p.n_ntiles;
   } else {
     p.M = a.M; p.K = a.K; p.batch = a.batch; p.stride_d = a.stride_d; p.alpha = a.alpha;
@@ -1150,8 +1197,8 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
     if (!dl.ready) {
       if (cudaDeviceGetAttribute(&dl.n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || dl.n_sm <= 0)
         dl.n_sm = 148;
-      for (auto* k : {conv_tc_kernel<false, false>, conv_tc_kernel<true, false>, conv_tc_kernel<false, true>,
-                      conv_tc_kernel<true, true>}) {
+      for (auto* k : {conv_tc_kernel<false, 0>, conv_tc_kernel<true, 0>, conv_tc_kernel<false, 1>,
+                      conv_tc_kernel<true, 1>, conv_tc_kernel<false, 2>, conv_tc_kernel<true, 2>}) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
       }
@@ -1164,7 +1211,8 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   {
     // N tiles per chunk: as many as keep the chunk's weights within ~48 MB of L2
     const double w_tile =
-        static_cast<double>(p.BN) * (a.mode == 0 ? 27.0 * a.C_in_pad : static_cast<double>(a.K)) * (p.fp8 ? 1.0 : 2.0);
+        static_cast<double>(p.BN) * (a.mode == 0 ? 27.0 * a.C_in_pad : static_cast<double>(a.K)) *
+        (p.fp8 ? 1.0 : p.tf32 ? 8.0 : 2.0);
     int npc = p.n_ntiles;
     if (a.mode == 0) {
       npc = 1;
@@ -1176,12 +1224,14 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   if (!p.pair) {
     p.seq_count = p.n_tiles;
     const long long grid = std::min<long long>(n_blocks, n_sm);
-    if (p.fp8) conv_tc_kernel<false, true><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmA, tmB, p);
-    else conv_tc_kernel<false, false><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmA, tmB, p);
+    const unsigned g = static_cast<unsigned>(grid);
+    if (p.fp8) conv_tc_kernel<false, 1><<<g, kThreads, smem, stream>>>(tmA, tmB, tmA2, p);
+    else if (p.tf32) conv_tc_kernel<false, 2><<<g, kThreads, smem, stream>>>(tmA, tmB, tmA2, p);
+    else conv_tc_kernel<false, 0><<<g, kThreads, smem, stream>>>(tmA, tmB, tmA2, p);
     return cudaGetLastError();
   }
   p.seq_count = (p.n_mtiles + 1) / 2 * p.n_ntiles;
-  auto* kern = p.fp8 ? conv_tc_kernel<true, true> : conv_tc_kernel<true, false>;
+  auto* kern = p.fp8 ? conv_tc_kernel<true, 1> : p.tf32 ? conv_tc_kernel<true, 2> : conv_tc_kernel<true, 0>;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1210,7 +1260,7 @@ cudaError_t launch_conv_tc(const ConvTcArgs& a, cudaStream_t stream) {
   }
   const long long clusters = std::min<long long>(p.seq_count, max_clusters);
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmA2, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

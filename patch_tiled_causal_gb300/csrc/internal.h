@@ -51,6 +51,11 @@ struct ConvTcArgs {
   int natural;
   // conv mode, weights packed tap-stacked (see kTapRows): all 9 spatial taps in one MMA
   int tap_stacked;
+  // conv mode, fp32 operands as 3 x TF32 products (kind::tf32): x holds the tf32 high parts of the
+  // fp32 input and x_lo the remainders (same layout); w holds [2][N_pad][27 * C_in_pad] fp32 (high
+  // parts, then remainders); each product is a_hi b_hi + a_hi b_lo + a_lo b_hi; C_in_pad % 32 == 0
+  int tf32;
+  const void* x_lo;
 };
 
 // Narrow bf16 convs (at most kTapMaxN output channels) pack their weights tap-stacked: for each temporal
@@ -80,6 +85,12 @@ cudaError_t launch_conv_simt(const ConvSimtArgs& a, cudaStream_t s);
 cudaError_t launch_pack_weights_bf16(const float* w, int C_out, int C_in, int C_in_pad, int N_pad, int S,
                                      void* out, cudaStream_t s, int natural = 0, int tap_stacked = 0);
 cudaError_t launch_pack_weights_f32(const float* w, int C_out, int C_in, void* out, cudaStream_t s);
+// fp32 weights for the 3 x TF32 conv: the bf16 packing's rows, K-major fp32 [2][N_pad][27 * C_in_pad]:
+// high parts (the fp32 value with its 13 low mantissa bits cleared), then the exact remainders.
+cudaError_t launch_pack_weights_tf32(const float* w, int C_out, int C_in, int C_in_pad, int N_pad, int S, void* out,
+                                     cudaStream_t s, int natural = 0);
+// x = hi + lo exactly, hi = x with its 13 low mantissa bits cleared (a tf32 value), n elements.
+cudaError_t launch_split_tf32(const float* x, float* hi, float* lo, int64_t n, cudaStream_t s);
 cudaError_t launch_pack_matrix_bf16(const float* w, int rows, int cols, void* out, cudaStream_t s);
 // e4m3 K-major [N_pad, 27 * C_in_pad] (rows as the bf16 packing), each row scaled by its own
 // scale = max|w| / 448, followed at fp8_scale_offset() bytes by the float scales [N_pad].

@@ -1661,6 +1661,69 @@ cudaError_t launch_stride2_weights(const float* w, int C_out, int C_in, float* o
 // ============================================================================ weight packing
 // bf16 K-major [N_pad, 27 * C_in_pad]; row n' = sub * (C_out/S) + c holds PyTorch channel c * S + sub
 // (natural: row n' holds channel n', for convs that store NCTHW pixels)
+// The tf32 high part of an fp32 value: its 13 low mantissa bits cleared (so whatever a tf32 consumer does
+// with those bits, it sees exactly this value); the remainder x - hi is exact in fp32.
+VAE_DEV float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xffffe000u); }
+
+__global__ void pack_tf32_kernel(const float* w, int C_out, int C_in, int C_in_pad, int N_pad, int S, int natural,
+                                 float* out) {
+  const int64_t n = static_cast<int64_t>(N_pad) * 27 * C_in_pad;
+  const int Cd = C_out / S;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int ci = static_cast<int>(i % C_in_pad);
+    const int tap = static_cast<int>((i / C_in_pad) % 27);
+    const int np = static_cast<int>(i / (27LL * C_in_pad));
+    float v = 0.f;
+    if (np < C_out && ci < C_in) {
+      const int sub = np / Cd, c = np % Cd;
+      const int co = natural ? np : c * S + sub;
+      v = w[(static_cast<int64_t>(co) * C_in + ci) * 27 + tap];
+    }
+    const float hi = tf32_hi(v);
+    out[i] = hi;
+    out[n + i] = v - hi;
+  }
+}
+
+cudaError_t launch_pack_weights_tf32(const float* w, int C_out, int C_in, int C_in_pad, int N_pad, int S, void* out,
+                                     cudaStream_t s, int natural) {
+  const int64_t n = static_cast<int64_t>(N_pad) * 27 * C_in_pad;
+  const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 152 * 64));
+  pack_tf32_kernel<<<blocks, 256, 0, s>>>(w, C_out, C_in, C_in_pad, N_pad, S, natural, static_cast<float*>(out));
+  return cudaGetLastError();
+}
+
+// 4 elements per thread (n % 4 == 0, 16-byte aligned arrays) or one
+__global__ void split_tf32_kernel(const float* x, float* hi, float* lo, int64_t n) {
+  const int64_t n4 = (n % 4 == 0) ? n / 4 : 0;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 v = reinterpret_cast<const float4*>(x)[i];
+    const float4 h = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
+    reinterpret_cast<float4*>(hi)[i] = h;
+    reinterpret_cast<float4*>(lo)[i] = make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
+  }
+  if (n4 == 0)
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      const float h = tf32_hi(x[i]);
+      hi[i] = h;
+      lo[i] = x[i] - h;
+    }
+}
+
+cudaError_t launch_split_tf32(const float* x, float* hi, float* lo, int64_t n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const bool vec = n % 4 == 0 && (reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(hi) |
+                                  reinterpret_cast<uintptr_t>(lo)) % 16 == 0;
+  if (!vec && n % 4 == 0) return cudaErrorMisalignedAddress;
+  const int64_t work = n % 4 == 0 ? n / 4 : n;
+  const int blocks = static_cast<int>(std::min<int64_t>((work + 255) / 256, 152 * 16));
+  split_tf32_kernel<<<blocks, 256, 0, s>>>(x, hi, lo, n);
+  return cudaGetLastError();
+}
+
 __global__ void pack_bf16_kernel(const float* w, int C_out, int C_in, int C_in_pad, int N_pad, int S, int natural,
                                  __nv_bfloat16* out) {
   const int64_t n = static_cast<int64_t>(N_pad) * 27 * C_in_pad;

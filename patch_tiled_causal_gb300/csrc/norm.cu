@@ -268,6 +268,21 @@ template <> struct ApplyVec<float> {
 
 // bf16 input keeps twice the vectors in flight per thread: 3 blocks per SM leave it room (measured:
 // 0.201 -> 0.186 ms on [1,512,21,88,160]); fp32 input runs best at 4 (the decoders' case).
+// SiLU z * sigmoid(z) in the output type's precision.  For e4m3 outputs (unit roundoff 2^-4) the sigmoid
+// comes from one tanh.approx, sigmoid(z) = (1 + tanh(z / 2)) / 2 (relative error near 2^-11): one MUFU
+// operation per element instead of two (exp and reciprocal), which a 3-byte-per-element e4m3 pass
+// would otherwise saturate; every other output type keeps z / (1 + exp(-z)).
+template <typename TO>
+VAE_DEV float silu_to(float z) {
+  if constexpr (sizeof(TO) == 1) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * z));
+    return z * fmaf(0.5f, t, 0.5f);
+  } else {
+    return __fdividef(z, 1.0f + __expf(-z));
+  }
+}
+
 template <typename TI, typename TO>
 __global__ void __launch_bounds__(256, sizeof(TI) == 2 ? 3 : 4) gn_apply_kernel(const __grid_constant__ GnParams p) {
   constexpr int VPT = ApplyVec<TI>::kVecs;
@@ -307,7 +322,7 @@ __global__ void __launch_bounds__(256, sizeof(TI) == 2 ? 3 : 4) gn_apply_kernel(
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float z = fmaf(a[e], m[e].x, m[e].y);
-        a[e] = p.silu ? __fdividef(z, 1.0f + __expf(-z)) : z;
+        a[e] = p.silu ? silu_to<TO>(z) : z;
       }
       vstore8(yf + static_cast<int64_t>(v) * 8, a, p.fault);
     }
@@ -326,7 +341,7 @@ __global__ void __launch_bounds__(256, sizeof(TI) == 2 ? 3 : 4) gn_apply_kernel(
     for (int e = 0; e < 8; ++e) {
       const float2 m = sh_aff[c0 + e];
       const float z = fmaf(a[e], m.x, m.y);
-      a[e] = p.silu ? __fdividef(z, 1.0f + __expf(-z)) : z;
+      a[e] = p.silu ? silu_to<TO>(z) : z;
     }
     vstore8(yf + static_cast<int64_t>(v) * 8, a, p.fault);
   }
@@ -522,7 +537,7 @@ __global__ void __launch_bounds__(256) rms_apply_kernel(const __grid_constant__ 
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float z = fmaf(v[e] * rr, gg[e], bb[e]);
-          o[e] = p.silu ? __fdividef(z, 1.0f + __expf(-z)) : z;
+          o[e] = p.silu ? silu_to<TO>(z) : z;
         }
         vstore8(yf + static_cast<int64_t>(r0 + k) * p.C + c0, o, p.fault);
       }

@@ -266,8 +266,6 @@ template <> struct ApplyVec<float> {
   }
 };
 
-// bf16 input keeps twice the vectors in flight per thread: 3 blocks per SM leave it room (measured:
-// 0.201 -> 0.186 ms on [1,512,21,88,160]); fp32 input runs best at 4 (the decoders' case).
 // SiLU z * sigmoid(z) in the output type's precision.  For e4m3 outputs (unit roundoff 2^-4) the sigmoid
 // comes from one tanh.approx, sigmoid(z) = (1 + tanh(z / 2)) / 2 (relative error near 2^-11): one MUFU
 // operation per element instead of two (exp and reciprocal), which a 3-byte-per-element e4m3 pass
@@ -283,6 +281,8 @@ VAE_DEV float silu_to(float z) {
   }
 }
 
+// bf16 input keeps twice the vectors in flight per thread: 3 blocks per SM leave it room (measured:
+// 0.201 -> 0.186 ms on [1,512,21,88,160]); fp32 input runs best at 4 (the decoders' case).
 template <typename TI, typename TO>
 __global__ void __launch_bounds__(256, sizeof(TI) == 2 ? 3 : 4) gn_apply_kernel(const __grid_constant__ GnParams p) {
   constexpr int VPT = ApplyVec<TI>::kVecs;

@@ -15,9 +15,13 @@ front of the next chunk instead of the copies of frame 0; the temporal depth-to-
 first frame only in the first chunk.  With per-frame group statistics the chunked decode equals
 the whole decode.
 
-Parity: pinned by the CPU tests through its parts (ops), the causality invariant, chunked ==
-whole, zero-conv2 residual identity and Tier A / Tier B agreement.  Whole-decoder output values
-are otherwise "parity unpinned": the pages print no output value for any input.
+Parity: the pages print no output value for any input, so the whole decoder is pinned against a
+second formulation of the same architecture written only with library routines (torch conv3d,
+group_norm / rms_norm, silu, pixel-shuffle-style reshapes, softmax attention; tests/test_oracle_pins.py,
+1e-10), on small configs of every family, together with: every parameter reaching the output, the
+causality invariant, chunked == whole, patched == unpatched, Tier A / Tier B agreement, and planted
+mistakes in the layer order and the residual block that those pins must catch
+(tests/test_oracle_mutations.py).
 """
 from __future__ import annotations
 

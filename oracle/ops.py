@@ -28,8 +28,9 @@ Readings where the pages are silent (each is listed in the design notes):
   * attention: one head over the H*W tokens of each frame, 1x1 q/k/v/o projections with bias,
     scale 1/sqrt(C), softmax over keys, residual add; its input is group-normed (no SiLU).
 
-Parity: conv, group norm, SiLU, depth-to-space and attention are pinned by the CPU tests
-(brute force, library routines, closed forms, invariants).
+Parity: conv, group norm, channel RMS norm, SiLU, depth-to-space and attention are pinned by the
+CPU tests (brute force, library routines, closed forms, invariants); the residual block against a
+library-routine formulation, with planted mistakes (swapped norms, a dropped SiLU) that must fail.
 """
 from __future__ import annotations
 

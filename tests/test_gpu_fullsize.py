@@ -6,7 +6,8 @@ properties that hold at any size plus a prefix the oracle can afford:
     1, 4 and 21 latent frames for the Wan-shaped decoder, 1 and 4 for the LTX-shaped one);
   * causality: output frames 0 .. s_t*(k-1) depend only on latent frames 0 .. k-1, so the first
     frames of the full decode must match the oracle's decode of the first latent frame(s) at full
-    spatial size (bf16 bar: relative L2 <= 1e-2, PSNR >= 50 dB against the fp32 oracle).
+    spatial size (bf16 bar: relative L2 <= 1e-2, PSNR >= 50 dB against the fp32 oracle; the fp32
+    decode, whose convs run as three TF32 products: relative L2 <= 1e-4).
 """
 import dataclasses
 
@@ -68,19 +69,36 @@ def test_full_size_chunked_equals_whole(vd, name, pers):
     dec.close()
 
 
-@pytest.mark.parametrize("name,k", [("ltx", 2), ("wan", 1)])
-def test_full_size_prefix_matches_oracle(vd, name, k):
+_prefix_refs = {}
+
+
+def _prefix_ref(cfg, p, zn, k):
+    # the oracle's decode of the first k latent frames at full spatial size (shared by the dtype cases)
+    if (cfg.name, k) not in _prefix_refs:
+        sub = dataclasses.replace(cfg, latent_shape=(1, cfg.latent_c, k) + cfg.latent_shape[3:])
+        _prefix_refs[(cfg.name, k)] = odec.decode(sub, p, zn[:, :, :k].copy(), tier="B")
+    return _prefix_refs[(cfg.name, k)]
+
+
+@pytest.mark.parametrize("name,k,dt", [("ltx", 2, "bf16"), ("ltx", 2, "fp32"), ("wan", 1, "bf16")])
+def test_full_size_prefix_matches_oracle(vd, name, k, dt):
+    # bf16 bar: relative L2 <= 1e-2 and PSNR >= 50 dB; fp32 (convs as three TF32 products on the tensor
+    # cores, at the full channel counts): relative L2 <= 1e-4 against the oracle's float32 tier
     cfg = synth.CONFIGS[name]
-    dec, p = _decoder(vd, cfg)
+    p = synth.draw_params(cfg, 0)
+    dec = vd.Decoder(cfg, p, vd.VAE_BF16 if dt == "bf16" else vd.VAE_FP32)
     zn = synth.draw_latent(cfg, 0)
     y = dec.decode(torch.from_numpy(zn).cuda(), n_patch_h=1, n_patch_w=4)
     st = cfg.scale()[0]
     nf = st * (k - 1) + 1
     got = y[:, :, :nf].float().cpu().numpy()
+    assert vd.last_error(dec.h)[0] == vd.VAE_OK
     dec.close()
-    sub = dataclasses.replace(cfg, latent_shape=(1, cfg.latent_c, k) + cfg.latent_shape[3:])
-    ref = odec.decode(sub, p, zn[:, :, :k].copy(), tier="B")
+    ref = _prefix_ref(cfg, p, zn, k)
     assert ref.shape == got.shape
     rl2, ps = metrics.rel_l2(got, ref), metrics.psnr(got, ref)
-    print(f"{name}: first {nf} frames, rel L2 {rl2:.3e}, PSNR {ps:.1f} dB")
-    assert rl2 <= 1e-2 and ps >= 50.0
+    print(f"{name} {dt}: first {nf} frames, rel L2 {rl2:.3e}, PSNR {ps:.1f} dB")
+    if dt == "bf16":
+        assert rl2 <= 1e-2 and ps >= 50.0
+    else:
+        assert rl2 <= 1e-4

@@ -105,7 +105,7 @@ typedef struct {
  * tcgen05 tensor cores as three TF32 products per fp32 product (kind::tf32: the high part of each
  * operand is the value with its 13 low mantissa bits cleared, the remainder is exact in fp32, and
  * a_hi b_hi + a_hi b_lo + a_lo b_hi is summed in fp32), the others and the attention GEMMs on the CUDA
- * cores.
+ * cores; its workspace holds two more copies (high parts, remainders) of the largest conv input.
  * norm_type: VAE_NORM_GROUP (gn_groups, gn_eps as above), or VAE_NORM_CHANNEL_RMS: every norm above
  * becomes x * rsqrt(mean over channels of x^2 + gn_eps) * gamma + beta per pixel (gn_groups is then
  * ignored; stage channels must be multiples of 8 and at most 1024 with C/8 a power of two or a

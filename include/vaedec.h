@@ -64,7 +64,7 @@ typedef enum {
  * conv1's output are stored in bf16; pixels are bf16.  Accuracy bar against the fp32 oracle: relative L2 <= 0.15 and PSNR >= 35 dB
  * (each e4m3 rounding has unit roundoff 2^-4; the same rounding points emulated in the oracle give
  * relative L2 0.05-0.07 on small decoders and 0.094 on the first frame of the Wan-shaped decode). */
-typedef enum { VAE_BF16 = 0, VAE_FP32 = 1, VAE_FP8 = 2 } vae_dtype_t;
+typedef enum { VAE_BF16 = 0, VAE_FP32 = 1, VAE_FP8 = 2, VAE_FP32_TC = 3 } vae_dtype_t;
 
 /* The decoder's norm family.  VAE_NORM_GROUP: per-frame group norm whose statistics span patches
  * ([DV] PatchGroupNorm commit).  VAE_NORM_CHANNEL_RMS: a channel RMS norm per pixel, the norm of the
@@ -101,11 +101,15 @@ typedef struct {
  * population variance, eps inside the square root.  The attention is one head over each frame's
  * H*W tokens with 1x1 q/k/v/o projections, scale 1/sqrt(C), on GN(x) without SiLU, plus residual.
  * dtype: VAE_BF16 stores activations in bf16 (fp32 accumulation, statistics and blend),
- * VAE_FP32 stores everything in fp32; its convs with input channels a multiple of 32 run on the
- * tcgen05 tensor cores as three TF32 products per fp32 product (kind::tf32: the high part of each
- * operand is the value with its 13 low mantissa bits cleared, the remainder is exact in fp32, and
- * a_hi b_hi + a_hi b_lo + a_lo b_hi is summed in fp32), the others and the attention GEMMs on the CUDA
- * cores; its workspace holds two more copies (high parts, remainders) of the largest conv input.
+ * VAE_FP32 stores everything in fp32 and runs on the CUDA cores (fp32 FMAs in a fixed order): the
+ * parity mode, max relative error <= 1e-4 against the fp64 oracle.
+ * VAE_FP32_TC (decoder / encoder dtype only) is VAE_FP32 with the convs whose input channels are a
+ * multiple of 32 on the tcgen05 tensor cores as three TF32 products per fp32 product (kind::tf32: the
+ * high part of each operand is the value with its 13 low mantissa bits cleared, the remainder is exact
+ * in fp32, and a_hi b_hi + a_hi b_lo + a_lo b_hi goes into the fp32 accumulator), about 70x faster;
+ * the tensor cores' accumulation over 27 * C_in terms leaves relative errors near 3e-4 at 1024
+ * channels (measured on the LTX-shaped 720p decode), so it is a fast fp32 reference, not the parity
+ * mode.  Its workspace holds two more copies (high parts, remainders) of the largest conv input.
  * norm_type: VAE_NORM_GROUP (gn_groups, gn_eps as above), or VAE_NORM_CHANNEL_RMS: every norm above
  * becomes x * rsqrt(mean over channels of x^2 + gn_eps) * gamma + beta per pixel (gn_groups is then
  * ignored; stage channels must be multiples of 8 and at most 1024 with C/8 a power of two or a

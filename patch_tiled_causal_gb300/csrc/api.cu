@@ -147,6 +147,7 @@ struct vae_decoder {
   vae_config_t cfg{};
   bool f32 = false;  // fp32 storage mode
   bool f8 = false;   // e4m3 operands for the residual blocks' and up-samplers' convs
+  bool f32tc = false;  // fp32 storage with the convs as three TF32 products on the tensor cores
   ConvL conv_in;
   std::vector<ResL> mid;
   bool has_attn = false;
@@ -237,7 +238,7 @@ vae_status_t make_conv(vae_decoder* d, ConvL& c, const float* w, const float* b,
   // tensor cores take 64-channel K blocks (32 fp32 channels for the 3 x TF32 products of fp32
   // decoders); the latent is zero-padded up to them when it is converted
   const int kb = d->f32 ? 32 : 64;
-  c.tc = C_in % kb == 0 || pad_input;
+  c.tc = (!d->f32 || d->f32tc) && (C_in % kb == 0 || pad_input);
   c.tf32 = d->f32 && c.tc;
   c.C_in_pad = c.tc ? round_up(C_in, kb) : C_in;
   c.fp8 = d->f8 && allow_fp8 && c.tc && C_in % 128 == 0;
@@ -302,7 +303,7 @@ vae_status_t check_config(const vae_config_t* c, vae_error_info_t* e) {
   if (c->norm_type != VAE_NORM_GROUP && !rms) return set_err(e, VAE_ERR_INVALID_ARG, 0, 0, "unknown norm type");
   if (c->n_stages < 1 || c->n_stages > VAE_MAX_STAGES || c->latent_c <= 0 || (!rms && c->gn_groups <= 0) || c->out_c <= 0 ||
       c->mid_res < 0 || c->out_d2s_t < 1 || c->out_d2s_h < 1 || c->out_d2s_w < 1 ||
-      (c->dtype != VAE_BF16 && c->dtype != VAE_FP32 && c->dtype != VAE_FP8))
+      (c->dtype != VAE_BF16 && c->dtype != VAE_FP32 && c->dtype != VAE_FP8 && c->dtype != VAE_FP32_TC))
     return set_err(e, VAE_ERR_INVALID_ARG, 0, 0, "invalid decoder config");
   if (c->out_d2s_t != 1) return set_err(e, VAE_ERR_UNSUPPORTED, 0, 0, "temporal depth-to-space in conv_out is not supported");
   for (int i = 0; i < c->n_stages; ++i) {
@@ -367,7 +368,8 @@ extern "C" vae_status_t vae_decoder_create(const vae_config_t* cfg, const void* 
       return set_err(nullptr, weights[i] ? VAE_ERR_ALIGNMENT : VAE_ERR_INVALID_ARG, 0, 0, "weight %d pointer", i);
   vae_decoder* d = new vae_decoder();
   d->cfg = *cfg;
-  d->f32 = cfg->dtype == VAE_FP32;
+  d->f32 = cfg->dtype == VAE_FP32 || cfg->dtype == VAE_FP32_TC;
+  d->f32tc = cfg->dtype == VAE_FP32_TC;
   d->f8 = cfg->dtype == VAE_FP8;
   int k = 0;
   auto W = [&](void) { return static_cast<const float*>(weights[k++]); };
@@ -1267,7 +1269,7 @@ vae_status_t check_enc_config(const vae_encoder_config_t* c) {
   const bool rms = c->norm_type == VAE_NORM_CHANNEL_RMS;
   if ((c->norm_type != VAE_NORM_GROUP && !rms) || c->n_stages < 1 || c->n_stages > VAE_MAX_STAGES || c->pix_c <= 0 ||
       c->patch_h < 1 || c->patch_w < 1 || c->latent_c <= 0 || c->mid_res < 0 || (!rms && c->gn_groups <= 0) ||
-      (c->dtype != VAE_BF16 && c->dtype != VAE_FP32 && c->dtype != VAE_FP8))
+      (c->dtype != VAE_BF16 && c->dtype != VAE_FP32 && c->dtype != VAE_FP8 && c->dtype != VAE_FP32_TC))
     return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "invalid encoder config");
   for (int i = 0; i < c->n_stages; ++i) {
     const int C = c->stage_c[i];
@@ -1491,7 +1493,8 @@ extern "C" vae_status_t vae_encoder_create(const vae_encoder_config_t* cfg, cons
   d->cfg.gn_eps = cfg->gn_eps;
   d->cfg.norm_type = cfg->norm_type;
   d->cfg.dtype = cfg->dtype;
-  d->f32 = cfg->dtype == VAE_FP32;
+  d->f32 = cfg->dtype == VAE_FP32 || cfg->dtype == VAE_FP32_TC;
+  d->f32tc = cfg->dtype == VAE_FP32_TC;
   d->f8 = cfg->dtype == VAE_FP8;
   int k = 0;
   auto W = [&](void) { return static_cast<const float*>(weights[k++]); };

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libvaedec.so")
 
 VAE_OK, VAE_ERR_INVALID_ARG, VAE_ERR_UNSUPPORTED, VAE_ERR_PATCH_TOO_NARROW = 0, 1, 2, 3
 VAE_ERR_ALIGNMENT, VAE_ERR_OOM, VAE_ERR_CUDA, VAE_ERR_TIMEOUT, VAE_ERR_RANGE = 4, 5, 6, 7, 8
-VAE_BF16, VAE_FP32, VAE_FP8 = 0, 1, 2
+VAE_BF16, VAE_FP32, VAE_FP8, VAE_FP32_TC = 0, 1, 2, 3
 VAE_NORM_GROUP, VAE_NORM_CHANNEL_RMS = 0, 1
 MAX_STAGES, MAX_PATCHES, MAX_TILES = 8, 64, 512
 
@@ -461,7 +461,7 @@ class Decoder:
 
     def out_dtype(self):
         torch = _torch()
-        return torch.float32 if self.dtype == VAE_FP32 else torch.bfloat16
+        return torch.float32 if self.dtype in (VAE_FP32, VAE_FP32_TC) else torch.bfloat16
 
     def output_shape(self, latent_shape, first_chunk=True):
         b, _, t, h, w = latent_shape

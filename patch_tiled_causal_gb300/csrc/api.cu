@@ -168,6 +168,13 @@ struct vae_decoder {
   // tiled decode tile storage
   void* tiles = nullptr;
   size_t tiles_bytes = 0;
+  // host-buffer decode: the copy stream, double-buffered latent / pixel chunks, and its events
+  cudaStream_t copy_stream = nullptr;
+  void* hb_lat[2] = {nullptr, nullptr};
+  void* hb_out[2] = {nullptr, nullptr};
+  size_t hb_lat_bytes = 0, hb_out_bytes = 0;
+  cudaEvent_t hb_ev[8] = {};  // [0,1] latent in, [2,3] chunk decoded, [4,5] pixels out, [6] start, [7] end
+  bool hb_ready = false;
   vae_error_info_t err{};
   // profiling: events around every launch while enabled
   bool prof = false;
@@ -346,6 +353,18 @@ void release_memory(vae_decoder* d) {
   if (d->tiles) cudaFree(d->tiles);
   d->ws = d->tiles = nullptr;
   d->ws_bytes = d->tiles_bytes = 0;
+  for (int i = 0; i < 2; ++i) {
+    if (d->hb_lat[i]) cudaFree(d->hb_lat[i]);
+    if (d->hb_out[i]) cudaFree(d->hb_out[i]);
+    d->hb_lat[i] = d->hb_out[i] = nullptr;
+  }
+  d->hb_lat_bytes = d->hb_out_bytes = 0;
+  if (d->hb_ready) {
+    for (cudaEvent_t& e : d->hb_ev) cudaEventDestroy(e);
+    cudaStreamDestroy(d->copy_stream);
+    d->copy_stream = nullptr;
+    d->hb_ready = false;
+  }
 }
 }  // namespace
 
@@ -1026,6 +1045,93 @@ extern "C" vae_status_t vae_decode_chunk(vae_decoder_t* d, const void* latent, c
   const int box[3] = {0, 0, 0};
   return run_decode(d, p, static_cast<const float*>(latent), full, box, 1, out, p.lv.back().T, true,
                     static_cast<cudaStream_t>(stream));
+}
+
+// Decode from and to host memory: temporal chunks (chunk 0 = latent frame 0, then frames_per_chunk frames)
+// go through vae_decode_chunk on `stream`, while a second stream copies the next latent chunk in and the
+// previous chunk's pixels out (double-buffered device chunks), so the copies overlap the decode.
+extern "C" vae_status_t vae_decode_host(vae_decoder_t* d, const void* latent_host, const int64_t shp[5],
+                                        void* out_host, int nph, int npw, int frames_per_chunk, void* stream) {
+  if (!d) return set_err(nullptr, VAE_ERR_INVALID_ARG, 0, 0, "null decoder");
+  if (!latent_host || !out_host || !shp) return set_err(&d->err, VAE_ERR_INVALID_ARG, 0, 0, "null argument");
+  vae_status_t s = check_shape(d, shp, nph, npw);
+  if (s) return s;
+  const vae_config_t& c = d->cfg;
+  int st = c.out_d2s_t, ss = c.out_d2s_h;
+  for (int i = 0; i + 1 < c.n_stages; ++i) {
+    st *= c.up_t[i];
+    ss *= c.up_h[i];
+  }
+  const int B = static_cast<int>(shp[0]), Cl = static_cast<int>(shp[1]), T = static_cast<int>(shp[2]);
+  const int h = static_cast<int>(shp[3]), w = static_cast<int>(shp[4]);
+  const int per = frames_per_chunk > 0 ? frames_per_chunk : std::max(1, (T - 1 + 4) / 5);
+  const int To = st * (T - 1) + 1, Ho = ss * h, Wo = ss * w, Co = c.out_c;
+  const size_t ob = d->f32 ? 4 : 2;
+  const size_t lat_frame = static_cast<size_t>(h) * w * 4, out_frame = static_cast<size_t>(Ho) * Wo * ob;
+  const int max_lat = std::min(per, std::max(T - 1, 1)), max_out = std::max(1, st * max_lat);
+  const size_t lat_bytes = static_cast<size_t>(B) * Cl * max_lat * lat_frame;
+  const size_t out_bytes = static_cast<size_t>(B) * Co * max_out * out_frame;
+  // everything allocated before anything is enqueued: the chunk buffers, and the workspace of the
+  // largest chunk (so no chunk call has to grow it in the middle of the stream)
+  if (!d->hb_ready) {
+    CK(cudaStreamCreateWithFlags(&d->copy_stream, cudaStreamNonBlocking));
+    for (cudaEvent_t& e : d->hb_ev) CK(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    d->hb_ready = true;
+  }
+  if (d->hb_lat_bytes < lat_bytes || d->hb_out_bytes < out_bytes) {
+    CK(cudaDeviceSynchronize());
+    for (int i = 0; i < 2; ++i) {
+      if (d->hb_lat[i]) cudaFree(d->hb_lat[i]);
+      if (d->hb_out[i]) cudaFree(d->hb_out[i]);
+      d->hb_lat[i] = d->hb_out[i] = nullptr;
+    }
+    d->hb_lat_bytes = d->hb_out_bytes = 0;
+    for (int i = 0; i < 2; ++i) {
+      CK(cudaMalloc(&d->hb_lat[i], lat_bytes));
+      CK(cudaMalloc(&d->hb_out[i], out_bytes));
+    }
+    d->hb_lat_bytes = lat_bytes;
+    d->hb_out_bytes = out_bytes;
+  }
+  {
+    Plan pmax;
+    s = make_plan(d, B, max_lat, h, w, nph, npw, false, pmax);
+    if (!s) s = ensure_ws(d, pmax);
+    if (s) return s;
+  }
+  cudaStream_t cs = static_cast<cudaStream_t>(stream), cp = d->copy_stream;
+  cudaEvent_t* ev = d->hb_ev;
+  CK(cudaEventRecord(ev[6], cs));  // the copies start after what `stream` already holds
+  CK(cudaStreamWaitEvent(cp, ev[6], 0));
+  const char* lat = static_cast<const char*>(latent_host);
+  char* out = static_cast<char*>(out_host);
+  int t0 = 0;
+  for (int i = 0; t0 < T; ++i) {
+    const int n = i == 0 ? 1 : std::min(per, T - t0);
+    const int buf = i & 1;
+    // latent frames [t0, t0 + n) of every (b, c) plane -> hb_lat[buf] (free once chunk i - 2 decoded)
+    if (i >= 2) CK(cudaStreamWaitEvent(cp, ev[2 + buf], 0));
+    CK(cudaMemcpy2DAsync(d->hb_lat[buf], n * lat_frame, lat + t0 * lat_frame, T * lat_frame, n * lat_frame,
+                         static_cast<size_t>(B) * Cl, cudaMemcpyHostToDevice, cp));
+    CK(cudaEventRecord(ev[buf], cp));
+    // decode the chunk into hb_out[buf] (free once chunk i - 2's pixels are out)
+    CK(cudaStreamWaitEvent(cs, ev[buf], 0));
+    if (i >= 2) CK(cudaStreamWaitEvent(cs, ev[4 + buf], 0));
+    const int64_t cshp[5] = {B, Cl, n, h, w};
+    s = vae_decode_chunk(d, d->hb_lat[buf], cshp, i == 0, d->hb_out[buf], nph, npw, stream);
+    if (s) return s;
+    CK(cudaEventRecord(ev[2 + buf], cs));
+    // its pixel frames [f0, f0 + nf) of every (b, c) plane -> out_host
+    const int f0 = i == 0 ? 0 : 1 + st * (t0 - 1), nf = i == 0 ? 1 : st * n;
+    CK(cudaStreamWaitEvent(cp, ev[2 + buf], 0));
+    CK(cudaMemcpy2DAsync(out + f0 * out_frame, To * out_frame, d->hb_out[buf], nf * out_frame, nf * out_frame,
+                         static_cast<size_t>(B) * Co, cudaMemcpyDeviceToHost, cp));
+    CK(cudaEventRecord(ev[4 + buf], cp));
+    t0 += n;
+  }
+  CK(cudaEventRecord(ev[7], cp));  // `stream` ends with the last copy
+  CK(cudaStreamWaitEvent(cs, ev[7], 0));
+  return VAE_OK;
 }
 
 #undef ERRP

@@ -103,6 +103,7 @@ _SIGS = {
     "vae_decoder_reserve": (C.c_int, [_P, C.POINTER(C.c_int64), C.c_int, C.c_int]),
     "vae_decode": (C.c_int, [_P, _P, C.POINTER(C.c_int64), _P, C.c_int, C.c_int, _P]),
     "vae_decode_chunk": (C.c_int, [_P, _P, C.POINTER(C.c_int64), C.c_int, _P, C.c_int, C.c_int, _P]),
+    "vae_decode_host": (C.c_int, [_P, _P, C.POINTER(C.c_int64), _P, C.c_int, C.c_int, C.c_int, _P]),
     "vae_decode_tiled": (C.c_int, [_P, _P, C.POINTER(C.c_int64), _P, C.POINTER(C.c_int), C.POINTER(C.c_int), _P]),
     "vae_last_error": (C.c_int, [_P, C.POINTER(VaeErrorInfo)]),
     "vae_patch_edges": (C.c_int, [C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(C.c_int)]),
@@ -187,6 +188,17 @@ def _stream(stream=None) -> int:
     torch = _torch()
     s = stream if stream is not None else torch.cuda.current_stream()
     return s.cuda_stream
+
+
+def _hptr(t, dtype) -> int:
+    """Pointer to a contiguous host (CPU) tensor of the given dtype."""
+    if t.is_cuda:
+        raise ValueError("expected a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"expected {dtype}, got {t.dtype}")
+    return t.data_ptr()
 
 
 def _ptr(t, dtype=None) -> Optional[int]:
@@ -491,6 +503,17 @@ class Decoder:
         _check(load().vae_decode(self.h, _ptr(latent, torch.float32), shp, _ptr(out, self.out_dtype()), n_patch_h,
                                  n_patch_w, _stream(stream)), "vae_decode", self.h)
         return out
+
+    def decode_host(self, latent_cpu, out_cpu=None, n_patch_h=1, n_patch_w=1, frames_per_chunk=0, stream=None):
+        """Host latent (CPU fp32, page-locked for overlap) -> host pixels (vae_decode_host)."""
+        torch = _torch()
+        if out_cpu is None:
+            out_cpu = torch.empty(self.output_shape(latent_cpu.shape), dtype=self.out_dtype(), pin_memory=True)
+        shp = (C.c_int64 * 5)(*latent_cpu.shape)
+        _check(load().vae_decode_host(self.h, _hptr(latent_cpu, torch.float32), shp, _hptr(out_cpu, self.out_dtype()),
+                                      n_patch_h, n_patch_w, frames_per_chunk, _stream(stream)), "vae_decode_host",
+               self.h)
+        return out_cpu
 
     def decode_chunk(self, latent_chunk, first_chunk, out=None, n_patch_h=1, n_patch_w=1, stream=None):
         torch = _torch()

@@ -107,6 +107,25 @@ def test_chunked_equals_whole(vd, dt, per, base):
 
 
 @pytest.mark.parametrize("dt", ["bf16", "fp32"])
+@pytest.mark.parametrize("per", [0, 1, 3])
+@pytest.mark.parametrize("base", ["mini_wan", "mini_ltx"])
+def test_host_decode_equals_device_decode(vd, dt, per, base):
+    # host latent in, host pixels out, copies overlapped with the chunked decode: the same bits as decode()
+    c0 = synth.CONFIGS[base]
+    cfg = dataclasses.replace(c0, latent_shape=(2, c0.latent_c, 6, 9, 11))
+    dtc = vd.VAE_BF16 if dt == "bf16" else vd.VAE_FP32
+    p = synth.draw_params(cfg, 0, rand_affine=True)
+    zn = synth.draw_latent(cfg, 0)
+    dec = vd.Decoder(cfg, p, dtc)
+    ref = dec.decode(torch.from_numpy(zn).cuda(), n_patch_h=2, n_patch_w=1).cpu()
+    got = dec.decode_host(torch.from_numpy(zn).pin_memory(), n_patch_h=2, n_patch_w=1, frames_per_chunk=per)
+    torch.cuda.synchronize()
+    assert vd.last_error(dec.h)[0] == vd.VAE_OK
+    dec.close()
+    assert torch.equal(got, ref)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp32"])
 def test_tiled_decode_matches_oracle(vd, dt):
     cfg = synth.MINI_TILED
     dtc = vd.VAE_BF16 if dt == "bf16" else vd.VAE_FP32

@@ -232,7 +232,7 @@ def main():
     ap.add_argument("--no-ops", action="store_true", help="skip the op-level workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-extra", action="store_true", help="skip the LTX-shaped and tiled decode sub-lines")
-    ap.add_argument("--only", default="all", choices=["all", "decode", "ops"],
+    ap.add_argument("--only", default="all", choices=["all", "decode", "ops", "encode"],
                     help="run only the decode or only the op workloads (profiling runs)")
     ap.add_argument("--latent-frames", type=int, default=0,
                     help="decode only the first N latent frames (0: all; small values for profiler captures)")
@@ -272,6 +272,10 @@ def main():
     if args.only == "ops":
         flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
         print(json.dumps({"ops": run_ops(args, torch, vaedec, peaks, flush), "peaks": peaks}), flush=True)
+        return
+    if args.only == "encode":  # the LTX-shaped encode alone (profiling runs)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        print(json.dumps({"ltx_encode_1x4": run_ltx_encode(args, torch, vaedec, peaks, flush, stream)}), flush=True)
         return
     if args.only == "decode":
         args.no_ops = args.no_cpu = args.no_extra = True

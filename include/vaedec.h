@@ -176,7 +176,8 @@ vae_status_t vae_decode(vae_decoder_t* dec, const void* latent, const int64_t la
 vae_status_t vae_decode_chunk(vae_decoder_t* dec, const void* latent_chunk, const int64_t chunk_shape[5],
                               int first_chunk, void* out_chunk, int n_patch_h, int n_patch_w, void* stream);
 
-/* Decode from host memory to host memory: latent_host is the NCTHW fp32 latent [B, C, T, h, w] and
+/* Decode from host memory to host memory, through the chunked temporal decode above ([DV] Wan adapter
+ * commit): latent_host is the NCTHW fp32 latent [B, C, T, h, w] and
  * out_host the NCTHW pixels (bf16, or fp32 for the fp32 dtypes) [B, out_c, T', H, W], both in host
  * memory (page-locked for the copies to overlap; pageable memory works, serialised).  The latent goes
  * in and the pixels come out in the temporal chunks of vae_decode_chunk (chunk 0 = latent frame 0, then
